@@ -1,0 +1,187 @@
+"""Gated DeltaNet-2 token-mixer core for GB300 (sm_103a): thin Python binding of libgdn2.so.
+
+Every step of the computation runs in the library's CUDA kernels; this module only marshals
+arguments (device pointers, sizes, the current CUDA stream) from torch tensors to the C ABI declared
+in include/gdn2.h, and raises on a non-zero status. torch provides device memory and streams only.
+
+The binding fails loudly: importing it raises if libgdn2.so has not been built.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libgdn2.so")
+
+GDN2_OK, GDN2_ERR_INVALID_ARG, GDN2_ERR_UNSUPPORTED = 0, -1, -2
+GDN2_ERR_MISALIGNED, GDN2_ERR_WORKSPACE, GDN2_ERR_CUDA, GDN2_ERR_TIMEOUT = -3, -4, -5, -6
+GDN2_F32, GDN2_BF16 = 0, 1
+PATHS = {"auto": 0, "simt": 1, "tcgen05": 2}
+
+#: names of the extern "C" functions exported by libgdn2.so (all declared in include/gdn2.h)
+EXPORTS = (
+    "gdn2_status_string", "gdn2_version", "gdn2_chunk_fwd_workspace_size",
+    "gdn2_chunk_fwd_workspace_size_path", "gdn2_chunk_fwd", "gdn2_chunk_fwd_path",
+    "gdn2_recurrent_step", "gdn2_last_device_status", "gdn2_set_wait_limit", "gdn2_selftest_umma",
+)
+
+
+class Gdn2Error(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} ({status})")
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"{LIB_PATH} is missing: build it first (python -c 'import __graft_entry__ as g; g.build()' "
+            "or python gated_deltanet_mixer_gdn2_gb300/_build.py)")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, I, F, Z, L = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t, ctypes.c_longlong
+    sig = {
+        "gdn2_status_string": (ctypes.c_char_p, [I]),
+        "gdn2_version": (I, []),
+        "gdn2_chunk_fwd_workspace_size": (Z, [I] * 7 + [I]),
+        "gdn2_chunk_fwd_workspace_size_path": (Z, [I] + [I] * 7 + [I]),
+        "gdn2_chunk_fwd": (I, [P] * 9 + [I] * 7 + [F, I, P, Z, P]),
+        "gdn2_chunk_fwd_path": (I, [I] + [P] * 9 + [I] * 7 + [F, I, P, Z, P]),
+        "gdn2_recurrent_step": (I, [P] * 8 + [I] * 5 + [F, I, P]),
+        "gdn2_last_device_status": (I, [P]),
+        "gdn2_set_wait_limit": (None, [L]),
+        "gdn2_selftest_umma": (I, [I, I, P, P, P, P]),
+    }
+    for name, (res, args) in sig.items():
+        f = getattr(lib, name)
+        f.restype = res
+        f.argtypes = args
+    return lib
+
+
+lib = _load()
+
+
+def status_string(status: int) -> str:
+    return lib.gdn2_status_string(int(status)).decode()
+
+
+def _check(status: int, what: str):
+    if status != GDN2_OK:
+        raise Gdn2Error(status, what)
+
+
+def _dtype_code(t) -> int:
+    import torch
+
+    if t.dtype == torch.bfloat16:
+        return GDN2_BF16
+    if t.dtype == torch.float32:
+        return GDN2_F32
+    raise TypeError(f"unsupported token dtype {t.dtype} (float32 or bfloat16)")
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("tensors must live on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError("tensors must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    import torch
+
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def gdn2_version() -> int:
+    return lib.gdn2_version()
+
+
+def gdn2_chunk_fwd_workspace_size(B, T, Hk, Hv, dk, dv, C=64, dtype=GDN2_BF16, path="auto") -> int:
+    return lib.gdn2_chunk_fwd_workspace_size_path(PATHS[path], B, T, Hk, Hv, dk, dv, C, dtype)
+
+
+def gdn2_chunk_fwd(q, k, v, g, b, w, o, initial_state=None, final_state=None, *, C=64, scale=1.0,
+                   workspace=None, path="auto", stream=None):
+    """Chunked forward (C ABI gdn2_chunk_fwd_path). Writes `o` and, if given, `final_state`.
+
+    q, k: [B, T, H_k, d_k]; v, w: [B, T, H_v, d_v]; g, b: [B, T, H_v, d_k]; o: like v;
+    states: [B, H_v, d_k, d_v] float32. `workspace`: a uint8 CUDA tensor of at least
+    gdn2_chunk_fwd_workspace_size(...) bytes (allocated here when None).
+    """
+    import torch
+
+    B, T, Hk, dk = q.shape
+    Hv, dv = v.shape[2], v.shape[3]
+    dt = _dtype_code(q)
+    for t in (k, v, g, b, w, o):
+        if t.dtype != q.dtype:
+            raise TypeError("all token tensors and o must share one dtype")
+    for t in (initial_state, final_state):
+        if t is not None and t.dtype != torch.float32:
+            raise TypeError("states are float32")
+    need = gdn2_chunk_fwd_workspace_size(B, T, Hk, Hv, dk, dv, C, dt, path)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    st = lib.gdn2_chunk_fwd_path(PATHS[path], _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(b), _ptr(w),
+                                 _ptr(initial_state), _ptr(final_state), _ptr(o), B, T, Hk, Hv, dk, dv,
+                                 C, float(scale), dt, _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(st, "gdn2_chunk_fwd")
+    return o, final_state
+
+
+def gdn2_recurrent_step(q, k, v, g, b, w, state, o, *, scale=1.0, stream=None):
+    """One decode token (C ABI gdn2_recurrent_step); updates `state` in place and writes `o`.
+
+    q, k: [B, H_k, d_k]; v, w: [B, H_v, d_v]; g, b: [B, H_v, d_k]; state: [B, H_v, d_k, d_v] fp32.
+    """
+    B, Hk, dk = q.shape
+    Hv, dv = v.shape[1], v.shape[2]
+    dt = _dtype_code(q)
+    st = lib.gdn2_recurrent_step(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(b), _ptr(w), _ptr(state),
+                                 _ptr(o), B, Hk, Hv, dk, dv, float(scale), dt, _stream(stream))
+    _check(st, "gdn2_recurrent_step")
+    return o
+
+
+def gdn2_last_device_status(stream=None) -> int:
+    return lib.gdn2_last_device_status(_stream(stream))
+
+
+def gdn2_set_wait_limit(ns: int) -> None:
+    lib.gdn2_set_wait_limit(int(ns))
+
+
+def gdn2_selftest_umma(case_id: int, soft: int, a, b, d, stream=None):
+    _check(lib.gdn2_selftest_umma(case_id, soft, _ptr(a), _ptr(b), _ptr(d), _stream(stream)),
+           "gdn2_selftest_umma")
+    return d
+
+
+# ---- convenience wrappers that allocate outputs (torch is used for memory only) -------------------
+
+def chunk_fwd(q, k, v, g, b, w, initial_state=None, *, output_final_state=True, C=64, scale=1.0,
+              path="auto", workspace=None, stream=None):
+    """Returns (o, final_state or None)."""
+    import torch
+
+    B, T, Hk, dk = q.shape
+    Hv, dv = v.shape[2], v.shape[3]
+    o = torch.empty((B, T, Hv, dv), dtype=q.dtype, device=q.device)
+    fs = torch.empty((B, Hv, dk, dv), dtype=torch.float32, device=q.device) if output_final_state else None
+    return gdn2_chunk_fwd(q, k, v, g, b, w, o, initial_state, fs, C=C, scale=scale, workspace=workspace,
+                          path=path, stream=stream)
+
+
+def recurrent_step(q, k, v, g, b, w, state, *, scale=1.0, stream=None):
+    """Returns o; `state` is updated in place."""
+    import torch
+
+    o = torch.empty(v.shape, dtype=q.dtype, device=q.device)
+    return gdn2_recurrent_step(q, k, v, g, b, w, state, o, scale=scale, stream=stream)

@@ -1,0 +1,286 @@
+// chunk_simt.cu -- chunked forward on CUDA cores (fp32 arithmetic), for fp32 inputs and for any
+// supported shape that the tensor-core path does not cover.
+//
+// Chunked WY / UT form of the recurrence (burn-gdn2 0.1.5 docs: "chunked WY decomposition
+// (training)"). For a chunk of C tokens entering with state S_n, with G_i the inclusive
+// cumulative log-decay of the chunk (per key channel):
+//     A_ij = sum_c b_i k_i k_j e^{G_i - G_j}   (j < i)        M_ij = sum_c q_i k_j e^{G_i - G_j}  (j <= i)
+//     T    = (I + A)^{-1}   (unit lower triangular, forward substitution)
+//     W    = T (b . k . e^{G}),   U~ = T (w . v)
+//     U    = U~ - W S_n
+//     O    = (q . e^{G}) S_n + M U
+//     S_{n+1} = diag(e^{G_last}) S_n + (k . e^{G_last - G})^T U
+//
+// Two kernels:
+//   factors (grid: chunks x heads, fully parallel) computes everything that does not depend on the
+//           state and stores it in the workspace: W^T, (q . e^{G})^T, (k . e^{G_last - G})^T [d_k x C],
+//           M [C x C], U~^T [d_v x C], e^{G_last} [d_k];
+//   state   (grid: heads x 16-column slices of d_v, sequential over chunks) carries S_n and writes o.
+// Padding: tokens past T read as zeros (k = q = b = v = w = 0, g = 0), which leaves S unchanged.
+#include "common.cuh"
+
+namespace gdn2 {
+
+namespace {
+
+__device__ int g_status_simt;
+
+struct SimtWs {
+    int dk, dv, C;
+    __host__ __device__ size_t unit_floats() const {
+        size_t n = 3 * (size_t)dk * C + (size_t)C * C + (size_t)dv * C + dk;
+        return (n + 3) & ~size_t(3);
+    }
+    __host__ __device__ size_t off_wt() const { return 0; }
+    __host__ __device__ size_t off_qbt() const { return (size_t)dk * C; }
+    __host__ __device__ size_t off_kht() const { return 2 * (size_t)dk * C; }
+    __host__ __device__ size_t off_m() const { return 3 * (size_t)dk * C; }
+    __host__ __device__ size_t off_utt() const { return 3 * (size_t)dk * C + (size_t)C * C; }
+    __host__ __device__ size_t off_gam() const { return 3 * (size_t)dk * C + (size_t)C * C + (size_t)dv * C; }
+};
+
+template <typename Tin>
+__global__ void __launch_bounds__(256) factors_simt_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k,
+                                                           const Tin* __restrict__ v, const Tin* __restrict__ g,
+                                                           const Tin* __restrict__ b, const Tin* __restrict__ w,
+                                                           float* __restrict__ ws, int T, int Hk, int Hv, int dk,
+                                                           int dv, int C) {
+    extern __shared__ float smem[];
+    const int n = blockIdx.x;                // chunk
+    const int bh = blockIdx.y;               // bi * Hv + hv
+    const int NC = gridDim.x;
+    const int bi = bh / Hv, hv = bh - bi * Hv, hk = hv / (Hv / Hk);
+    const int t0 = n * C;
+    const int tid = threadIdx.x, nt = blockDim.x;
+    const int LD = dk + 1;
+    const int LDQ = (dk > dv ? dk : dv) + 1;
+    float* sG = smem;                        // [C][LD]   cumulative log-decay
+    float* sK = sG + C * LD;                 // [C][LD]   k
+    float* sBK = sK + C * LD;                // [C][LD]   b . k, later b . k . e^{G}
+    float* sQ = sBK + C * LD;                // [C][LDQ]  q, later w . v
+    float* sA = sQ + C * LDQ;                // [C][C+1]
+    float* sT = sA + C * (C + 1);            // [C][C+1]
+
+    const SimtWs L{dk, dv, C};
+    float* u = ws + ((size_t)bh * NC + n) * L.unit_floats();
+
+    for (int idx = tid; idx < C * dk; idx += nt) {
+        const int t = idx / dk, c = idx - t * dk;
+        const int tok = t0 + t;
+        float gg = 0.f, kk = 0.f, bb = 0.f, qq = 0.f;
+        if (tok < T) {
+            const size_t kq_i = (((size_t)bi * T + tok) * Hk + hk) * dk + c;
+            const size_t gb_i = (((size_t)bi * T + tok) * Hv + hv) * dk + c;
+            gg = to_f32(g[gb_i]);
+            bb = to_f32(b[gb_i]);
+            kk = to_f32(k[kq_i]);
+            qq = to_f32(q[kq_i]);
+        }
+        sG[t * LD + c] = gg;
+        sK[t * LD + c] = kk;
+        sBK[t * LD + c] = bb * kk;
+        sQ[t * LDQ + c] = qq;
+    }
+    __syncthreads();
+    // inclusive cumulative log-decay per key channel, and the chunk decay e^{G_last}
+    for (int c = tid; c < dk; c += nt) {
+        float acc = 0.f;
+        for (int t = 0; t < C; ++t) {
+            acc += sG[t * LD + c];
+            sG[t * LD + c] = acc;
+        }
+        u[L.off_gam() + c] = expf(acc);
+    }
+    __syncthreads();
+    // erase interaction A (strictly lower) and causal q-k M (lower incl. diagonal)
+    float* Mws = u + L.off_m();
+    for (int p = tid; p < C * C; p += nt) {
+        const int i = p / C, j = p - i * C;
+        float a = 0.f, m = 0.f;
+        if (j <= i) {
+            for (int c = 0; c < dk; ++c) {
+                const float e = expf(sG[i * LD + c] - sG[j * LD + c]);
+                const float kj = sK[j * LD + c] * e;
+                a = fmaf(sBK[i * LD + c], kj, a);
+                m = fmaf(sQ[i * LDQ + c], kj, m);
+            }
+        }
+        sA[i * (C + 1) + j] = (j < i) ? a : 0.f;
+        Mws[p] = (j <= i) ? m : 0.f;
+    }
+    __syncthreads();
+    // T = (I + A)^{-1}: thread j solves column j by forward substitution
+    for (int j = tid; j < C; j += nt) {
+        for (int i = 0; i < j; ++i) sT[i * (C + 1) + j] = 0.f;
+        sT[j * (C + 1) + j] = 1.f;
+        for (int i = j + 1; i < C; ++i) {
+            float acc = 0.f;
+            for (int l = j; l < i; ++l) acc = fmaf(sA[i * (C + 1) + l], sT[l * (C + 1) + j], acc);
+            sT[i * (C + 1) + j] = -acc;
+        }
+    }
+    // decayed q and k (transposed, [d_k][C]) for the state kernel; b . k . e^{G} in place
+    for (int p = tid; p < dk * C; p += nt) {
+        const int c = p / C, i = p - c * C;
+        const float Gi = sG[i * LD + c];
+        u[L.off_qbt() + p] = sQ[i * LDQ + c] * expf(Gi);
+        u[L.off_kht() + p] = sK[i * LD + c] * expf(sG[(C - 1) * LD + c] - Gi);
+    }
+    __syncthreads();
+    for (int idx = tid; idx < C * dk; idx += nt) {
+        const int t = idx / dk, c = idx - t * dk;
+        sBK[t * LD + c] *= expf(sG[t * LD + c]);
+    }
+    for (int idx = tid; idx < C * dv; idx += nt) {
+        const int t = idx / dv, c = idx - t * dv;
+        const int tok = t0 + t;
+        float x = 0.f;
+        if (tok < T) {
+            const size_t vw_i = (((size_t)bi * T + tok) * Hv + hv) * dv + c;
+            x = to_f32(w[vw_i]) * to_f32(v[vw_i]);
+        }
+        sQ[t * LDQ + c] = x;
+    }
+    __syncthreads();
+    // W^T [d_k][C] = (T X)^T with X = b . k . e^{G};  U~^T [d_v][C] = (T (w . v))^T
+    for (int p = tid; p < dk * C; p += nt) {
+        const int c = p / C, i = p - c * C;
+        float acc = 0.f;
+        for (int j = 0; j <= i; ++j) acc = fmaf(sT[i * (C + 1) + j], sBK[j * LD + c], acc);
+        u[L.off_wt() + p] = acc;
+    }
+    for (int p = tid; p < dv * C; p += nt) {
+        const int c = p / C, i = p - c * C;
+        float acc = 0.f;
+        for (int j = 0; j <= i; ++j) acc = fmaf(sT[i * (C + 1) + j], sQ[j * LDQ + c], acc);
+        u[L.off_utt() + p] = acc;
+    }
+}
+
+constexpr int kSlice = 16;
+
+template <typename Tin>
+__global__ void __launch_bounds__(256) state_simt_kernel(const float* __restrict__ ws, const float* __restrict__ s0,
+                                                         float* __restrict__ sT_out, Tin* __restrict__ o, int T,
+                                                         int Hv, int dk, int dv, int C, int NC, float scale) {
+    extern __shared__ float smem[];
+    const int bh = blockIdx.x;
+    const int bi = bh / Hv, hv = bh - bi * Hv;
+    const int col0 = blockIdx.y * kSlice;
+    const int tid = threadIdx.x, nt = blockDim.x;
+    float* sS = smem;                        // [dk][kSlice]
+    float* sWT = sS + dk * kSlice;           // [dk][C]
+    float* sQb = sWT + dk * C;               // [dk][C]
+    float* sKh = sQb + dk * C;               // [dk][C]
+    float* sM = sKh + dk * C;                // [C][C]
+    float* sUt = sM + C * C;                 // [kSlice][C]
+    float* sGam = sUt + kSlice * C;          // [dk]
+    float* sU = sGam + dk;                   // [C][kSlice]
+    float* sP = sU + C * kSlice;             // [C][kSlice]
+    const SimtWs L{dk, dv, C};
+
+    for (int p = tid; p < dk * kSlice; p += nt) {
+        const int c = p / kSlice, j = p - c * kSlice;
+        sS[p] = s0 ? s0[((size_t)bh * dk + c) * dv + col0 + j] : 0.f;
+    }
+    for (int n = 0; n < NC; ++n) {
+        const float* u = ws + ((size_t)bh * NC + n) * L.unit_floats();
+        __syncthreads();
+        for (int p = tid; p < dk * C; p += nt) {
+            sWT[p] = u[L.off_wt() + p];
+            sQb[p] = u[L.off_qbt() + p];
+            sKh[p] = u[L.off_kht() + p];
+        }
+        for (int p = tid; p < C * C; p += nt) sM[p] = u[L.off_m() + p];
+        for (int p = tid; p < kSlice * C; p += nt) sUt[p] = u[L.off_utt() + (size_t)col0 * C + p];
+        for (int p = tid; p < dk; p += nt) sGam[p] = u[L.off_gam() + p];
+        __syncthreads();
+        // U = U~ - W S_n ;  P = (q . e^{G}) S_n
+        for (int p = tid; p < C * kSlice; p += nt) {
+            const int i = p / kSlice, j = p - i * kSlice;
+            float ws_ = 0.f, qs = 0.f;
+            for (int c = 0; c < dk; ++c) {
+                const float s = sS[c * kSlice + j];
+                ws_ = fmaf(sWT[c * C + i], s, ws_);
+                qs = fmaf(sQb[c * C + i], s, qs);
+            }
+            sU[p] = sUt[j * C + i] - ws_;
+            sP[p] = qs;
+        }
+        __syncthreads();
+        // O = P + M U ;  S_{n+1} = diag(e^{G_last}) S_n + K^^T U
+        for (int p = tid; p < C * kSlice; p += nt) {
+            const int i = p / kSlice, j = p - i * kSlice;
+            const int tok = n * C + i;
+            if (tok < T) {
+                float acc = sP[p];
+                for (int l = 0; l <= i; ++l) acc = fmaf(sM[i * C + l], sU[l * kSlice + j], acc);
+                o[(((size_t)bi * T + tok) * Hv + hv) * dv + col0 + j] = from_f32<Tin>(scale * acc);
+            }
+        }
+        for (int p = tid; p < dk * kSlice; p += nt) {
+            const int c = p / kSlice, j = p - c * kSlice;
+            float acc = sGam[c] * sS[p];
+            for (int i = 0; i < C; ++i) acc = fmaf(sKh[c * C + i], sU[i * kSlice + j], acc);
+            sS[p] = acc;
+        }
+    }
+    __syncthreads();
+    if (sT_out)
+        for (int p = tid; p < dk * kSlice; p += nt) {
+            const int c = p / kSlice, j = p - c * kSlice;
+            sT_out[((size_t)bh * dk + c) * dv + col0 + j] = sS[p];
+        }
+}
+
+size_t factors_smem(int dk, int dv, int C) {
+    const int LD = dk + 1, LDQ = (dk > dv ? dk : dv) + 1;
+    return sizeof(float) * ((size_t)3 * C * LD + (size_t)C * LDQ + 2 * (size_t)C * (C + 1));
+}
+size_t state_smem(int dk, int C) {
+    return sizeof(float) * ((size_t)dk * kSlice + 3 * (size_t)dk * C + (size_t)C * C + (size_t)kSlice * C + dk +
+                            2 * (size_t)C * kSlice);
+}
+
+template <typename Tin>
+cudaError_t launch_t(const void* q, const void* k, const void* v, const void* g, const void* b, const void* w,
+                     const float* s0, float* sT, void* o, const ChunkShape& sh, float scale, void* ws, cudaStream_t s) {
+    const int NC = sh.nchunks();
+    const size_t f_smem = factors_smem(sh.dk, sh.dv, sh.C);
+    const size_t s_smem = state_smem(sh.dk, sh.C);
+    cudaError_t e = cudaFuncSetAttribute(factors_simt_kernel<Tin>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)f_smem);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(state_simt_kernel<Tin>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s_smem);
+    if (e != cudaSuccess) return e;
+    factors_simt_kernel<Tin><<<dim3(NC, sh.B * sh.Hv), 256, f_smem, s>>>(
+        static_cast<const Tin*>(q), static_cast<const Tin*>(k), static_cast<const Tin*>(v),
+        static_cast<const Tin*>(g), static_cast<const Tin*>(b), static_cast<const Tin*>(w), static_cast<float*>(ws),
+        sh.T, sh.Hk, sh.Hv, sh.dk, sh.dv, sh.C);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    state_simt_kernel<Tin><<<dim3(sh.B * sh.Hv, sh.dv / kSlice), 256, s_smem, s>>>(
+        static_cast<const float*>(ws), s0, sT, static_cast<Tin*>(o), sh.T, sh.Hv, sh.dk, sh.dv, sh.C, NC, scale);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t chunk_simt_workspace_bytes(const ChunkShape& sh) {
+    const SimtWs L{sh.dk, sh.dv, sh.C};
+    return sizeof(float) * L.unit_floats() * (size_t)sh.nchunks() * sh.B * sh.Hv;
+}
+
+cudaError_t launch_chunk_simt(const void* q, const void* k, const void* v, const void* g, const void* b,
+                              const void* w, const float* s0, float* sT, void* o, const ChunkShape& sh, float scale,
+                              gdn2_dtype dt, void* ws, cudaStream_t s) {
+    if (dt == GDN2_BF16) return launch_t<__nv_bfloat16>(q, k, v, g, b, w, s0, sT, o, sh, scale, ws, s);
+    return launch_t<float>(q, k, v, g, b, w, s0, sT, o, sh, scale, ws, s);
+}
+
+int chunk_simt_read_clear_status(cudaStream_t) {
+    (void)g_status_simt;
+    return 0;  // no bounded waits in the SIMT kernels
+}
+
+}  // namespace gdn2

@@ -1,0 +1,65 @@
+// common.cuh -- internal definitions shared by the translation units of libgdn2.so.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+#include "../../include/gdn2.h"
+
+namespace gdn2 {
+
+// Default budget of a bounded wait, in nanoseconds of polling.
+constexpr long long kDefaultWaitNs = 2000000000LL;
+
+// Device status bits (one word per translation unit, read and cleared by the host).
+constexpr int kStatusTimeout = 1;
+
+template <typename T>
+__device__ __forceinline__ float to_f32(T x);
+template <>
+__device__ __forceinline__ float to_f32<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <typename T>
+__device__ __forceinline__ T from_f32(float x);
+template <>
+__device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Shapes of one chunked-forward call.
+struct ChunkShape {
+    int B, T, Hk, Hv, dk, dv, C;
+    int nchunks() const { return (T + C - 1) / C; }
+};
+
+// Per-translation-unit status readers (defined next to the kernels).
+int decode_read_clear_status(cudaStream_t s);
+int chunk_simt_read_clear_status(cudaStream_t s);
+int chunk_tc_read_clear_status(cudaStream_t s);
+
+long long wait_limit_ns();
+
+// Launchers (host side). Return cudaSuccess or the launch error.
+cudaError_t launch_recurrent_step(const void* q, const void* k, const void* v, const void* g, const void* b,
+                                  const void* w, float* state, void* o, int B, int Hk, int Hv, int dk, int dv,
+                                  float scale, gdn2_dtype dt, cudaStream_t s);
+
+size_t chunk_simt_workspace_bytes(const ChunkShape& sh);
+cudaError_t launch_chunk_simt(const void* q, const void* k, const void* v, const void* g, const void* b,
+                              const void* w, const float* s0, float* sT, void* o, const ChunkShape& sh, float scale,
+                              gdn2_dtype dt, void* ws, cudaStream_t s);
+
+size_t chunk_tc_workspace_bytes(const ChunkShape& sh);
+cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const void* g, const void* b,
+                            const void* w, const float* s0, float* sT, void* o, const ChunkShape& sh, float scale,
+                            void* ws, cudaStream_t s, long long wait_ns);
+
+}  // namespace gdn2

@@ -1,0 +1,157 @@
+/*
+ * gdn2.h -- C ABI of libgdn2.so, the GB300 (sm_103a) Gated DeltaNet-2 token-mixer core.
+ *
+ * The operation (burn-gdn2 0.1.5 docs, "Architecture"): per batch element and value head, on a
+ * matrix state S in R^{d_k x d_v},
+ *
+ *     S_t = (I - k_t (b_t . k_t)^T) diag(alpha_t) S_{t-1} + k_t (w_t . v_t)^T,    o_t = scale * S_t^T q_t
+ *
+ * where alpha_t = exp(g_t) is a per-key-channel decay, b_t the key-axis erase gate and w_t the
+ * value-axis write gate ("." is the element-wise product; o_t reads the post-update state). The
+ * same page names the two modes exported here: a chunked WY decomposition over a whole sequence
+ * (training / prefill) and a token-by-token recurrent step on a persistent state (inference).
+ *
+ * Conventions shared by every entry point
+ *   - Pointers: every tensor pointer is a DEVICE pointer to a caller-owned, contiguous, row-major
+ *     buffer aligned to 16 bytes. The library never allocates, frees or keeps device memory.
+ *   - Grouped heads: q and k belong to H_k key heads; g, b, v, w, o and the state to H_v value
+ *     heads; H_v must be a multiple of H_k and value head h reads key head h / (H_v / H_k).
+ *   - Token dtype: GDN2_F32 (float) or GDN2_BF16 (bfloat16) for q, k, v, g, b, w and o. States
+ *     are always fp32. Arithmetic is fp32 (the bf16 chunked path feeds bf16 operands to the
+ *     tensor cores with fp32 accumulation).
+ *   - g is log(alpha) (expected <= 0, not checked); b is the erase gate after its activation, with
+ *     values in (0, 2) when negative eigenvalues are allowed (the caller doubles it); w is the write
+ *     gate after its activation.
+ *   - Streams: `stream` is a cudaStream_t passed as void* (NULL = legacy default stream). Every
+ *     entry point only enqueues work: it returns without synchronising the host.
+ *   - Errors: entry points never abort, trap or print. Argument errors are detected on the host
+ *     before any work is enqueued and return a negative gdn2_status. A kernel that exceeds its
+ *     bounded wait records GDN2_ERR_TIMEOUT in a device status word read by
+ *     gdn2_last_device_status().
+ */
+#ifndef GDN2_H
+#define GDN2_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum gdn2_status {
+    GDN2_OK = 0,
+    GDN2_ERR_INVALID_ARG = -1, /* null required pointer, non-positive size, H_v % H_k != 0     */
+    GDN2_ERR_UNSUPPORTED = -2, /* shape / chunk size / dtype / path combination not built       */
+    GDN2_ERR_MISALIGNED = -3,  /* a pointer is not 16-byte aligned                               */
+    GDN2_ERR_WORKSPACE = -4,   /* workspace pointer null or smaller than required                */
+    GDN2_ERR_CUDA = -5,        /* a CUDA runtime/driver call failed (launch, attribute, symbol)  */
+    GDN2_ERR_TIMEOUT = -6      /* a kernel gave up a bounded wait (device status word)           */
+} gdn2_status;
+
+typedef enum gdn2_dtype { GDN2_F32 = 0, GDN2_BF16 = 1 } gdn2_dtype;
+
+/* Kernel family used by the chunked forward. AUTO picks TCGEN05 for bf16 with d_k = d_v = 128 and
+ * C = 64, and SIMT otherwise. */
+typedef enum gdn2_path { GDN2_PATH_AUTO = 0, GDN2_PATH_SIMT = 1, GDN2_PATH_TCGEN05 = 2 } gdn2_path;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* gdn2_status_string(gdn2_status s);
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+int gdn2_version(void);
+
+/*
+ * gdn2_chunk_fwd_workspace_size -- bytes of device workspace gdn2_chunk_fwd needs (AUTO path).
+ * The chunked forward stores per-chunk factors (W, U~, decayed q and k, the causal q-k matrix, the
+ * chunk decay) between its two kernels. Returns 0 for shapes the path does not support (and for
+ * empty problems). Pure host function.
+ */
+size_t gdn2_chunk_fwd_workspace_size(int B, int T, int Hk, int Hv, int dk, int dv, int C,
+                                     gdn2_dtype dt);
+size_t gdn2_chunk_fwd_workspace_size_path(gdn2_path path, int B, int T, int Hk, int Hv, int dk,
+                                          int dv, int C, gdn2_dtype dt);
+
+/*
+ * gdn2_chunk_fwd -- chunked forward over whole sequences (burn-gdn2 docs: "chunked WY
+ * decomposition (training)"; chunk_size 64 by default in its configuration table).
+ *
+ *   q, k           [B, T, H_k, d_k]  dt
+ *   v, w           [B, T, H_v, d_v]  dt
+ *   g, b           [B, T, H_v, d_k]  dt
+ *   initial_state  [B, H_v, d_k, d_v] fp32, may be NULL (zeros)
+ *   final_state    [B, H_v, d_k, d_v] fp32, may be NULL (not written); may alias initial_state
+ *   o              [B, T, H_v, d_v]  dt (output)
+ *   C              chunk length: 64 on the tensor-core path; 16, 32 or 64 on the SIMT path
+ *   workspace      device buffer of at least gdn2_chunk_fwd_workspace_size(...) bytes, 256-byte
+ *                  aligned; its contents on entry are ignored and on return are unspecified
+ *
+ * T need not be a multiple of C (the last chunk is padded with tokens that leave the state
+ * unchanged). T == 0 or B == 0 is valid: o is untouched and final_state receives initial_state (or
+ * zeros). Supported: d_k, d_v multiples of 16 in [16, 128] (SIMT, fp32 or bf16); bf16 with
+ * d_k = d_v = 128 and C = 64 (TCGEN05). Within one chunk the per-channel cumulative log-decay must
+ * span less than about 160 (alpha above about exp(-2.5) per token on average) on the TCGEN05 path;
+ * beyond that its decay factors leave the fp32 exponent range.
+ */
+gdn2_status gdn2_chunk_fwd(const void* q, const void* k, const void* v, const void* g,
+                           const void* b, const void* w, const float* initial_state,
+                           float* final_state, void* o, int B, int T, int Hk, int Hv, int dk,
+                           int dv, int C, float scale, gdn2_dtype dt, void* workspace,
+                           size_t ws_bytes, void* stream);
+gdn2_status gdn2_chunk_fwd_path(gdn2_path path, const void* q, const void* k, const void* v,
+                                const void* g, const void* b, const void* w,
+                                const float* initial_state, float* final_state, void* o, int B,
+                                int T, int Hk, int Hv, int dk, int dv, int C, float scale,
+                                gdn2_dtype dt, void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * gdn2_recurrent_step -- one decode token against a persistent fp32 state, updated in place
+ * (burn-gdn2 docs: token-by-token recurrent mode with persistent state; the same single fused
+ * update that the llama.cpp GDN decode study describes for the scalar-beta rule).
+ *
+ *   q, k   [B, H_k, d_k] dt;   v, w [B, H_v, d_v] dt;   g, b [B, H_v, d_k] dt
+ *   state  [B, H_v, d_k, d_v] fp32, read and written in place (read once, written once)
+ *   o      [B, H_v, d_v] dt (output)
+ *
+ * Supported: d_k in {16, 32, 64, 128}; d_v a multiple of 16 up to 512. B == 0 is a no-op.
+ */
+gdn2_status gdn2_recurrent_step(const void* q, const void* k, const void* v, const void* g,
+                                const void* b, const void* w, float* state, void* o, int B,
+                                int Hk, int Hv, int dk, int dv, float scale, gdn2_dtype dt,
+                                void* stream);
+
+/*
+ * gdn2_last_device_status -- synchronises `stream`, then reads and clears the device status word
+ * of the current device. Returns GDN2_OK, GDN2_ERR_TIMEOUT (a kernel gave up a bounded wait since
+ * the last call) or GDN2_ERR_CUDA (the synchronisation itself failed).
+ */
+gdn2_status gdn2_last_device_status(void* stream);
+
+/*
+ * gdn2_set_wait_limit -- nanoseconds a kernel polls one barrier before it gives up and records
+ * GDN2_ERR_TIMEOUT. Negative restores the default (two seconds). Applies to
+ * launches enqueued after the call, process-wide. Zero makes every guarded wait give up at once;
+ * the kernel then still drains its own copies and tensor-core work (with the default limit)
+ * before it returns, so the device stays usable. Intended for tests of the error path.
+ */
+void gdn2_set_wait_limit(long long ns);
+
+/*
+ * gdn2_selftest_umma -- diagnostics: one tcgen05 product D[128][64] = A * B (bf16 in, fp32 out)
+ * with the shared-memory operand layouts the tensor-core chunked kernels use, so that a test can
+ * check them against a host matrix product. The operands are row-major bf16 device arrays:
+ *   case 0: A [128 (M)][128 (K)],  B [64 (N)][128 (K)]   (both K-major)
+ *   case 1: A [64 (K)][128 (M)],   B [64 (N)][64 (K)]    (A MN-major, B K-major)
+ *   case 2: A [128 (K)][128 (M)],  B [128 (K)][64 (N)]   (both MN-major)
+ *   case 3: A [128 (M)][64 (K)],   B [64 (K)][64 (N)]    (A K-major, B MN-major)
+ * soft = 0 stages them with TMA (128-byte swizzle), soft = 1 with ordinary stores using the same
+ * swizzle. d_out: [128][64] fp32 device array. Asynchronous on `stream`.
+ */
+gdn2_status gdn2_selftest_umma(int case_id, int soft, const void* a_storage, const void* b_storage,
+                               float* d_out, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN2_H */

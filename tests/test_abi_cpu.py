@@ -1,0 +1,119 @@
+"""The C ABI without a GPU: the library loads, exports every function include/gdn2.h declares, and
+rejects bad arguments on the host before touching the device (CPU only)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_functions():
+    src = open(os.path.join(ROOT, "include", "gdn2.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(gdn2_[a-z0-9_]+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def g():
+    from gated_deltanet_mixer_gdn2_gb300 import _build
+
+    _build.build()
+    import gated_deltanet_mixer_gdn2_gb300 as mod
+
+    return mod
+
+
+def test_header_declares_the_two_entry_points():
+    names = _declared_functions()
+    for fn in ("gdn2_chunk_fwd", "gdn2_recurrent_step", "gdn2_chunk_fwd_workspace_size",
+               "gdn2_status_string", "gdn2_last_device_status"):
+        assert fn in names
+
+
+def test_every_declared_symbol_is_exported(g):
+    lib = ctypes.CDLL(g.LIB_PATH)
+    for fn in _declared_functions():
+        assert hasattr(lib, fn), f"{fn} declared in include/gdn2.h but not exported"
+    assert set(g.EXPORTS) == set(_declared_functions())
+
+
+def test_status_strings(g):
+    for s in range(0, -7, -1):
+        assert g.status_string(s) and g.status_string(s) != "unknown status"
+    assert g.status_string(42) == "unknown status"
+
+
+def test_workspace_sizes(g):
+    # tensor-core path: one 91136-byte unit per (chunk, batch, value head)
+    assert g.gdn2_chunk_fwd_workspace_size(2, 32768, 16, 32, 128, 128, 64, g.GDN2_BF16) == 91136 * 512 * 64
+    # ragged tail rounds the chunk count up
+    assert g.gdn2_chunk_fwd_workspace_size(1, 65, 1, 1, 128, 128, 64, g.GDN2_BF16) == 91136 * 2
+    # fp32 goes to the SIMT path: (3 dk C + C^2 + dv C + dk) floats, rounded to 4
+    n = 3 * 64 * 64 + 64 * 64 + 64 * 64 + 64
+    assert g.gdn2_chunk_fwd_workspace_size(1, 256, 4, 4, 64, 64, 64, g.GDN2_F32) == 4 * n * 4 * 4
+    assert g.gdn2_chunk_fwd_workspace_size(1, 0, 4, 4, 64, 64, 64, g.GDN2_F32) == 0
+    assert g.gdn2_chunk_fwd_workspace_size(1, 10, 3, 4, 64, 64, 64, g.GDN2_F32) == 0        # Hv % Hk
+    assert g.gdn2_chunk_fwd_workspace_size(1, 10, 4, 4, 72, 64, 64, g.GDN2_F32) == 0        # dk % 16
+    assert g.gdn2_chunk_fwd_workspace_size(1, 10, 4, 4, 64, 64, 64, g.GDN2_BF16, "tcgen05") == 0
+
+
+def _chunk(g, path=0, B=1, T=8, Hk=1, Hv=1, dk=128, dv=128, C=64, dt=1, ptr=0x10000, ws=None, wsb=1 << 30,
+           s0=None, sT=None):
+    p = ctypes.c_void_p(ptr) if ptr else None
+    return g.lib.gdn2_chunk_fwd_path(path, p, p, p, p, p, p, s0, sT, p, B, T, Hk, Hv, dk, dv, C, 1.0, dt,
+                                     ctypes.c_void_p(ws if ws is not None else ptr), wsb, None)
+
+
+def test_chunk_argument_errors(g):
+    assert _chunk(g, ptr=0) == g.GDN2_ERR_INVALID_ARG                 # null tensors
+    assert _chunk(g, Hk=3, Hv=4) == g.GDN2_ERR_INVALID_ARG            # H_v % H_k
+    assert _chunk(g, T=-1) == g.GDN2_ERR_INVALID_ARG
+    assert _chunk(g, dt=7) == g.GDN2_ERR_INVALID_ARG
+    assert _chunk(g, path=9) == g.GDN2_ERR_INVALID_ARG
+    assert _chunk(g, dk=72) == g.GDN2_ERR_UNSUPPORTED
+    assert _chunk(g, C=48) == g.GDN2_ERR_UNSUPPORTED
+    assert _chunk(g, path=2, dt=0) == g.GDN2_ERR_UNSUPPORTED           # tensor cores need bf16
+    assert _chunk(g, path=2, dk=64, dv=64) == g.GDN2_ERR_UNSUPPORTED
+    assert _chunk(g, ptr=0x10008) == g.GDN2_ERR_MISALIGNED
+    assert _chunk(g, ws=0) == g.GDN2_ERR_WORKSPACE
+    assert _chunk(g, wsb=100) == g.GDN2_ERR_WORKSPACE
+    assert _chunk(g, ws=0x10004) == g.GDN2_ERR_MISALIGNED
+    assert _chunk(g, s0=ctypes.c_void_p(0x10004)) == g.GDN2_ERR_MISALIGNED
+    # empty problems need no tensors at all (nothing to copy without a final state)
+    assert _chunk(g, ptr=0, T=0) == g.GDN2_OK
+    assert _chunk(g, ptr=0, B=0) == g.GDN2_OK
+
+
+def test_decode_argument_errors(g):
+    P = ctypes.c_void_p(0x10000)
+    f = lambda B=1, Hk=1, Hv=1, dk=128, dv=128, dt=1, p=P: g.lib.gdn2_recurrent_step(
+        p, p, p, p, p, p, p, p, B, Hk, Hv, dk, dv, 1.0, dt, None)
+    assert f(p=None) == g.GDN2_ERR_INVALID_ARG
+    assert f(Hk=2, Hv=3) == g.GDN2_ERR_INVALID_ARG
+    assert f(dk=96) == g.GDN2_ERR_UNSUPPORTED
+    assert f(dv=100) == g.GDN2_ERR_UNSUPPORTED
+    assert f(dv=1024) == g.GDN2_ERR_UNSUPPORTED
+    assert f(p=ctypes.c_void_p(0x10002)) == g.GDN2_ERR_MISALIGNED
+    assert f(B=0, p=None) == g.GDN2_OK
+    assert f(dt=3) == g.GDN2_ERR_INVALID_ARG
+
+
+def test_binding_refuses_cpu_tensors(g):
+    import torch
+
+    x = torch.zeros(1, 4, 1, 128, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        g.chunk_fwd(x, x, x, x, x, x)
+
+
+def test_product_path_does_not_touch_the_oracle():
+    """The package and its sources never import or name the oracle / test infrastructure."""
+    pkg = os.path.join(ROOT, "gated_deltanet_mixer_gdn2_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                src = open(os.path.join(dirpath, f)).read()
+                assert "oracle" not in src.lower(), f"{f} mentions the oracle"
+                assert "import synth" not in src and "from synth" not in src

@@ -1,0 +1,221 @@
+"""GPU parity: the CUDA path (through the C ABI binding) against the fp64 oracle on the same seeded
+inputs. Tolerances (max normwise relative error, max|x - ref| / max|ref|, for o and for the final
+state separately): 1e-4 for fp32 token inputs, 2e-2 for bf16 token inputs."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from tests import gpu_helpers as H
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def g():
+    import gated_deltanet_mixer_gdn2_gb300 as mod
+
+    mod.gdn2_set_wait_limit(-1)
+    return mod
+
+
+def _check(name, got, ref, tol):
+    err = oracle.max_rel_err(got, ref)
+    assert np.isfinite(got).all(), f"{name}: non-finite values"
+    assert err <= tol, f"{name}: max rel err {err:.3e} > {tol:.1e}"
+    return err
+
+
+# ---------------------------------------------------------------------------------------------
+# decode step
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("dk,dv,Hk,Hv", [(128, 128, 2, 4), (64, 64, 1, 3), (32, 48, 2, 2), (16, 256, 1, 2),
+                                         (128, 16, 1, 1)])
+def test_decode_small(g, dtype, dk, dv, Hk, Hv):
+    wl = synth.Workload("t", B=3, T=0, Hk=Hk, Hv=Hv, dk=dk, dv=dv, dtype=dtype, seed=7, s0_std=0.02,
+                        decode_steps=9)
+    inp = synth.make_inputs(wl)
+    st = H.state_to_device(inp.s0)
+    o = H.run_decode(g, inp, st, 0, 9, scale=0.5)
+    o_ref, s_ref = oracle.run_inputs(inp, scale=0.5)
+    tol = H.tol_for(dtype)
+    _check("o", o, o_ref, tol)
+    _check("state", st.cpu().numpy(), s_ref, tol)
+
+
+def test_decode_b64_256_steps(g):
+    """The 64-sequence, 48-value-head decode workload, all 256 steps; oracle on sampled heads."""
+    wl = synth.WORKLOADS["decode_b64"]
+    inp = synth.make_inputs(wl)
+    st = H.state_to_device(inp.s0)
+    o = H.run_decode(g, inp, st, 0, wl.decode_steps)
+    units = synth.sample_heads(wl, 8)
+    for bi, hv in units:
+        sub = inp.heads(bi, hv, wl.Hk, wl.Hv)
+        o_ref, s_ref = oracle.run_inputs(sub)
+        _check(f"o[{bi},{hv}]", o[bi:bi + 1, :, hv:hv + 1], o_ref, H.BF16_TOL)
+        _check(f"S[{bi},{hv}]", st[bi, hv].cpu().numpy(), s_ref[0, 0], H.BF16_TOL)
+
+
+def test_decode_batch_zero_is_noop(g):
+    import torch
+
+    e = torch.empty((0, 1, 128), dtype=torch.bfloat16, device="cuda")
+    s = torch.empty((0, 1, 128, 128), dtype=torch.float32, device="cuda")
+    g.gdn2_recurrent_step(e, e, e, e, e, e, s, e)
+
+
+# ---------------------------------------------------------------------------------------------
+# chunked forward, SIMT path (fp32 inputs, and any shape)
+
+def test_chunk_tiny_f32(g):
+    wl = synth.WORKLOADS["tiny_f32"]
+    inp = synth.make_inputs(wl)
+    o, st = H.run_chunk(g, inp, C=wl.C)
+    o_ref, s_ref = oracle.run_inputs(inp)
+    _check("o", o, o_ref, H.F32_TOL)
+    _check("state", st.cpu().numpy(), s_ref, H.F32_TOL)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("T,C,dk,dv,Hk,Hv", [(1, 64, 64, 64, 1, 1), (37, 16, 32, 48, 1, 2), (100, 32, 128, 128, 2, 4),
+                                             (130, 64, 128, 64, 1, 3), (64, 64, 16, 16, 2, 2)])
+def test_chunk_simt_shapes(g, dtype, T, C, dk, dv, Hk, Hv):
+    wl = synth.Workload("t", B=2, T=T, Hk=Hk, Hv=Hv, dk=dk, dv=dv, C=C, dtype=dtype, seed=T + dk, s0_std=0.02,
+                        neg_eigval=(T % 2 == 1))
+    inp = synth.make_inputs(wl)
+    o, st = H.run_chunk(g, inp, C=C, path="simt")
+    o_ref, s_ref = oracle.run_inputs(inp)
+    tol = H.tol_for(dtype)
+    _check("o", o, o_ref, tol)
+    _check("state", st.cpu().numpy(), s_ref, tol)
+
+
+# ---------------------------------------------------------------------------------------------
+# chunked forward, tensor-core path
+
+@pytest.mark.parametrize("T,Hk,Hv,s0", [(64, 1, 1, False), (1, 1, 1, True), (100, 1, 2, True), (200, 2, 2, False),
+                                        (191, 1, 3, True)])
+def test_chunk_tc_small(g, T, Hk, Hv, s0):
+    wl = synth.Workload("t", B=2, T=T, Hk=Hk, Hv=Hv, dk=128, dv=128, dtype="bf16", seed=11 + T,
+                        s0_std=0.02 if s0 else 0.0)
+    inp = synth.make_inputs(wl)
+    o, st = H.run_chunk(g, inp, path="tcgen05")
+    o_ref, s_ref = oracle.run_inputs(inp)
+    _check("o", o, o_ref, H.BF16_TOL)
+    _check("state", st.cpu().numpy(), s_ref, H.BF16_TOL)
+
+
+def test_chunk_tc_train_bf16(g):
+    """4 x 2048 tokens, 8 heads, S0 ~ N(0, 0.02^2): every head checked."""
+    wl = synth.WORKLOADS["train_bf16"]
+    inp = synth.make_inputs(wl)
+    o, st = H.run_chunk(g, inp)
+    o_ref, s_ref = oracle.run_inputs(inp)
+    _check("o", o, o_ref, H.BF16_TOL)
+    _check("state", st.cpu().numpy(), s_ref, H.BF16_TOL)
+
+
+def test_chunk_tc_long_negeig(g):
+    """1 x 8192 tokens, 16 heads, b in (0, 2): every head checked."""
+    wl = synth.WORKLOADS["long_negeig_bf16"]
+    inp = synth.make_inputs(wl)
+    o, st = H.run_chunk(g, inp)
+    o_ref, s_ref = oracle.run_inputs(inp)
+    _check("o", o, o_ref, H.BF16_TOL)
+    _check("state", st.cpu().numpy(), s_ref, H.BF16_TOL)
+
+
+def test_prefill32k_then_decode(g):
+    """2 x 32768-token prefill (16 key / 32 value heads), then 64 decode steps from its final state;
+    the oracle runs the same 32832 tokens straight through on sampled heads."""
+    wl = synth.WORKLOADS["prefill32k_decode"]
+    inp = synth.make_inputs(wl)
+    o, st = H.run_chunk(g, inp, t0=0, t1=wl.T)
+    od = H.run_decode(g, inp, st, wl.T, wl.T + wl.decode_steps)
+    for bi, hv in synth.sample_heads(wl, 4):
+        sub = inp.heads(bi, hv, wl.Hk, wl.Hv)
+        o_ref, s_ref = oracle.run_inputs(sub)
+        _check(f"prefill o[{bi},{hv}]", o[bi:bi + 1, :, hv:hv + 1], o_ref[:, :wl.T], H.BF16_TOL)
+        _check(f"decode o[{bi},{hv}]", od[bi:bi + 1, :, hv:hv + 1], o_ref[:, wl.T:], H.BF16_TOL)
+        _check(f"S[{bi},{hv}]", st[bi, hv].cpu().numpy(), s_ref[0, 0], H.BF16_TOL)
+
+
+def test_chunk_paths_agree(g):
+    wl = synth.Workload("t", B=1, T=300, Hk=2, Hv=4, dk=128, dv=128, dtype="bf16", seed=5, s0_std=0.02)
+    inp = synth.make_inputs(wl)
+    o1, s1 = H.run_chunk(g, inp, path="simt")
+    o2, s2 = H.run_chunk(g, inp, path="tcgen05")
+    assert oracle.max_rel_err(o2, o1) < H.BF16_TOL
+    assert oracle.max_rel_err(s2.cpu().numpy(), s1.cpu().numpy()) < H.BF16_TOL
+
+
+@pytest.mark.parametrize("path", ["tcgen05", "simt"])
+def test_chunk_state_chaining(g, path):
+    """chunk(T) equals chunk(T1) -> final state -> chunk(T - T1)."""
+    wl = synth.Workload("t", B=1, T=320, Hk=1, Hv=2, dk=128, dv=128, dtype="bf16", seed=9, s0_std=0.02)
+    inp = synth.make_inputs(wl)
+    o, st = H.run_chunk(g, inp, path=path)
+    o1, s1 = H.run_chunk(g, inp, path=path, t0=0, t1=128)
+    o2, s2 = H.run_chunk(g, inp, path=path, t0=128, t1=320, s0=s1.cpu().numpy())
+    assert oracle.max_rel_err(np.concatenate([o1, o2], axis=1), o) < 1e-2
+    assert oracle.max_rel_err(s2.cpu().numpy(), st.cpu().numpy()) < 1e-2
+
+
+def test_chunk_then_step_matches_longer_chunk(g):
+    wl = synth.Workload("t", B=2, T=129, Hk=1, Hv=2, dk=128, dv=128, dtype="bf16", seed=3)
+    inp = synth.make_inputs(wl)
+    o_full, s_full = H.run_chunk(g, inp)
+    o_pre, s = H.run_chunk(g, inp, t0=0, t1=128)
+    od = H.run_decode(g, inp, s, 128, 129)
+    assert oracle.max_rel_err(od, o_full[:, 128:]) < H.BF16_TOL
+    assert oracle.max_rel_err(s.cpu().numpy(), s_full.cpu().numpy()) < H.BF16_TOL
+
+
+def test_chunk_state_aliasing(g):
+    """initial_state and final_state may be the same buffer."""
+    import torch
+
+    wl = synth.Workload("t", B=1, T=96, Hk=1, Hv=2, dk=128, dv=128, dtype="bf16", seed=4, s0_std=0.02)
+    inp = synth.make_inputs(wl)
+    o_ref, s_ref = oracle.run_inputs(inp)
+    q, k, v, gg, b, w = H.upload(inp, 0, wl.T)
+    st = H.state_to_device(inp.s0)
+    o = torch.empty_like(v)
+    g.gdn2_chunk_fwd(q, k, v, gg, b, w, o, st, st)
+    torch.cuda.synchronize()
+    _check("o", H.to_np(o), o_ref, H.BF16_TOL)
+    _check("state", st.cpu().numpy(), s_ref, H.BF16_TOL)
+
+
+def test_chunk_empty_sequence(g):
+    import torch
+
+    s0 = torch.randn(1, 2, 128, 128, device="cuda")
+    fs = torch.full_like(s0, float("nan"))
+    e = torch.empty((1, 0, 2, 128), dtype=torch.bfloat16, device="cuda")
+    g.gdn2_chunk_fwd(e, e, e, e, e, e, e, s0, fs)
+    torch.cuda.synchronize()
+    assert torch.equal(fs, s0)
+    g.gdn2_chunk_fwd(e, e, e, e, e, e, e, None, fs)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(fs).item() == 0
+
+
+def test_wait_timeout_is_reported_and_recoverable(g):
+    """A zero wait budget makes every guarded wait give up at once: the call reports a timeout
+    through the device status word, the device stays usable, and the next call is correct."""
+    wl = synth.Workload("t", B=1, T=130, Hk=1, Hv=1, dk=128, dv=128, dtype="bf16", seed=2)
+    inp = synth.make_inputs(wl)
+    q, k, v, gg, b, w = H.upload(inp, 0, wl.T)
+    g.gdn2_set_wait_limit(0)
+    try:
+        g.chunk_fwd(q, k, v, gg, b, w, None, path="tcgen05")
+        assert g.gdn2_last_device_status() == g.GDN2_ERR_TIMEOUT
+    finally:
+        g.gdn2_set_wait_limit(-1)
+    assert g.gdn2_last_device_status() == g.GDN2_OK
+    o, st = H.run_chunk(g, inp, path="tcgen05")
+    o_ref, s_ref = oracle.run_inputs(inp)
+    _check("o", o, o_ref, H.BF16_TOL)
