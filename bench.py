@@ -1,0 +1,464 @@
+"""Benchmark of the Gated DeltaNet-2 core on GB300.
+
+One step = the whole hot path once: the chunked forward (gdn2_chunk_fwd) over a 2 x 32768-token
+prefill with 16 key / 32 value heads, d_k = d_v = 128, C = 64, from a zero state, then 64
+single-token decode steps (gdn2_recurrent_step) from its final state. Prints ONE JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+N > 1 runs under torchrun (one process per GPU); every rank runs its own copy of the workload
+(independent sequences: weak scaling, no data-path collective); rank 0 prints. `--impl reference`
+times the fp64 CPU oracle on a bounded sample of the same workload (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "chunk-fwd tokens/s & % bf16 TC peak; decode step GB/s vs HBM peak (1×GB300)"
+WORKLOAD = "prefill32k_decode"
+DECODE_WORKLOAD = "decode_b64"
+FLUSH_BYTES = 256 << 20  # > 129 MB L2
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(p.get("bf16_tflops_sustained", p["bf16_tflops"])), "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+# ---- algorithmic work --------------------------------------------------------------------------
+
+def chunk_bytes(wl) -> int:
+    """Bytes the chunked forward must move: every token input once, o once, the final state once."""
+    tok = wl.B * wl.T
+    per_tok = 2 * wl.Hk * wl.dk * 2 + wl.Hv * (2 * wl.dk + 2 * wl.dv) * 2 + wl.Hv * wl.dv * 2
+    return tok * per_tok + wl.B * wl.Hv * wl.dk * wl.dv * 4 * (2 if wl.s0_std > 0 else 1)
+
+
+def chunk_flops(wl) -> int:
+    """Triangle-aware flops of the chunked form per (head, token): C(3 d_k + 2 d_v) + 6 d_k d_v."""
+    return wl.B * wl.T * wl.Hv * (wl.C * (3 * wl.dk + 2 * wl.dv) + 6 * wl.dk * wl.dv)
+
+
+def decode_step_bytes(B, Hk, Hv, dk, dv) -> int:
+    """State read + write, token inputs, output; bf16 tokens, fp32 state."""
+    return 2 * B * Hv * dk * dv * 4 + B * (2 * Hk * dk + Hv * (2 * dk + 2 * dv)) * 2 + B * Hv * dv * 2
+
+
+# ---- clocks ------------------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("timestamp,uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid: str | None):
+        self.uuid = uuid
+        self.proc = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def mark(self, which):
+        setattr(self, which, time.time())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        rows = []
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            if self.uuid and parts[1] != self.uuid:
+                continue
+            try:
+                ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                rows.append((ts, float(parts[2]), float(parts[3]), parts[5:]))
+            except Exception:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        inside = [r for r in rows if self.t0 is not None and self.t0 - 1 <= r[0] <= self.t1 + 1] or rows
+        names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in inside:
+            for name, val in zip(names[1:], r[3][1:]):
+                if val.lower() in ("active", "1", "yes"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r[1] for r in inside), "sm_max_mhz": max(r[2] for r in inside),
+                "reasons": sorted(reasons), "samples": len(inside)}
+
+
+# ---- our implementation -------------------------------------------------------------------------
+
+def run_ours(args, rank, world, device):
+    import torch
+
+    import gated_deltanet_mixer_gdn2_gb300 as g
+
+    hbm, tc_burst, tc_sust, peak_kind = peaks()
+    wl = synth.WORKLOADS[WORKLOAD]
+    inp = synth.make_inputs(wl)               # host float32 values of bf16 numbers, T + decode tokens
+    T, D = wl.T, wl.decode_steps
+    host = {n: synth.to_torch(np.ascontiguousarray(getattr(inp, n)), "bf16").pin_memory()
+            for n in ("q", "k", "v", "g", "b", "w")}
+    dev = {n: t.to(device) for n, t in host.items()}
+    pre = {n: dev[n][:, :T].contiguous() for n in dev}
+    dec = [{n: dev[n][:, t].contiguous() for n in dev} for t in range(T, T + D)]
+    del dev
+    B, Hk, Hv, dk, dv = wl.B, wl.Hk, wl.Hv, wl.dk, wl.dv
+    o = torch.empty((B, T, Hv, dv), dtype=torch.bfloat16, device=device)
+    od = torch.empty((D, B, Hv, dv), dtype=torch.bfloat16, device=device)
+    state = torch.empty((B, Hv, dk, dv), dtype=torch.float32, device=device)
+    ws_bytes = g.gdn2_chunk_fwd_workspace_size(B, T, Hk, Hv, dk, dv, wl.C, g.GDN2_BF16)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=device)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def step(ev=None):
+        if ev:
+            ev[0].record(stream)
+        g.gdn2_chunk_fwd(pre["q"], pre["k"], pre["v"], pre["g"], pre["b"], pre["w"], o, None, state, C=wl.C,
+                         workspace=ws)
+        if ev:
+            ev[1].record(stream)
+        for i in range(D):
+            d = dec[i]
+            g.gdn2_recurrent_step(d["q"], d["k"], d["v"], d["g"], d["b"], d["w"], state, od[i])
+        if ev:
+            ev[2].record(stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(device)
+    assert g.gdn2_last_device_status() == g.GDN2_OK
+
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(device).uuid)
+        uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+    except Exception:
+        pass
+    clk = ClockSampler(uuid)
+    clk.start()
+    time.sleep(0.3)
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize(device)
+    clk.mark("t0")
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()                          # L2 flush between steps, outside the events
+        step(events[i])
+    torch.cuda.synchronize(device)
+    wall1 = time.perf_counter()
+    clk.mark("t1")
+    if world > 1:
+        dist.barrier()
+    clocks = clk.stop()
+    status = g.gdn2_last_device_status()
+    chunk_ms = [e[0].elapsed_time(e[1]) for e in events]
+    dec_ms = [e[1].elapsed_time(e[2]) for e in events]
+    step_ms = [a + b for a, b in zip(chunk_ms, dec_ms)]
+    ms_per_step = sum(step_ms) / len(step_ms)
+    if world > 1:
+        t = torch.tensor([ms_per_step], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_per_step = float(t.item())
+    tokens = B * T + B * D
+    value = world * tokens / (ms_per_step * 1e-3)
+
+    # roofline of the dominant operation: the chunked forward (factors + state kernels)
+    ch_ms = statistics.mean(chunk_ms)
+    cb = chunk_bytes(wl)
+    ach_gbs = cb / (ch_ms * 1e-3) / 1e9
+    flops = chunk_flops(wl)
+    ach_tf = flops / (ch_ms * 1e-3) / 1e12
+    dstep_b = decode_step_bytes(B, Hk, Hv, dk, dv)
+    d_ms = statistics.mean(dec_ms) / D
+
+    decode_line = decode_roofline(g, device, hbm) if rank == 0 and not args.no_decode_workload else None
+
+    # end to end through the public API with host buffers (inputs H2D, results D2H every step)
+    e2e = None
+    if not args.no_e2e:
+        e2e = end_to_end(g, wl, host, device, args, tokens)
+
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{WORKLOAD}: {wl.description}", "B": B, "T": T, "H_k": Hk, "H_v": Hv,
+                   "d_k": dk, "d_v": dv, "chunk": wl.C, "decode_steps": D, "tokens_per_step": tokens,
+                   "l2": "flushed between steps (256 MB write); prefill inputs 2.7 GB > L2",
+                   "parallelism": f"replicas{world}" if world > 1 else "single GPU"},
+        "roofline": {"kernel": "gdn2_chunk_fwd (factors_tc + state_tc)", "bound": "hbm",
+                     "achieved": round(ach_gbs, 1), "peak": hbm, "unit": "GB/s",
+                     "frac": round(ach_gbs / hbm, 4), "traffic": None,
+                     "algorithmic_bytes": cb, "ms": round(ch_ms, 4), "peak_kind": f"{peak_kind} hbm_gbs",
+                     "tflops": round(ach_tf, 1), "tc_frac": round(ach_tf / tc_burst, 4),
+                     "tc_peak": tc_burst, "flops": flops},
+        "decode_in_step": {"us_per_step": round(d_ms * 1e3, 2), "bytes_per_step": dstep_b,
+                           "GB/s": round(dstep_b / (d_ms * 1e-3) / 1e9, 1),
+                           "note": "4.2 MB state, L2-resident across steps"},
+        "gpu_launches": args.steps * (2 + D),
+        "clocks": clocks,
+        "status": g.status_string(status),
+        "wall_s_timed": round(wall1 - wall0, 3),
+    }
+    if decode_line:
+        line["decode"] = decode_line
+    if e2e:
+        line["e2e"] = e2e
+    return line
+
+
+def decode_roofline(g, device, hbm):
+    """The decode kernel alone on the 64-sequence / 48-value-head workload (201 MB state)."""
+    import torch
+
+    wl = synth.WORKLOADS[DECODE_WORKLOAD]
+    B, Hk, Hv, dk, dv = wl.B, wl.Hk, wl.Hv, wl.dk, wl.dv
+    gen = torch.Generator(device=device)
+    gen.manual_seed(wl.seed)
+    steps = wl.decode_steps
+    st = torch.randn((B, Hv, dk, dv), generator=gen, device=device) * wl.s0_std
+    toks = []
+    for name, H, d in (("q", Hk, dk), ("k", Hk, dk), ("v", Hv, dv), ("g", Hv, dk), ("b", Hv, dk), ("w", Hv, dv)):
+        x = torch.randn((steps, B, H, d), generator=gen, device=device, dtype=torch.float32)
+        if name in ("q", "k"):
+            x = x / x.norm(dim=-1, keepdim=True)
+        elif name == "g":
+            x = -torch.nn.functional.softplus(x)
+        elif name in ("b", "w"):
+            x = torch.sigmoid(x)
+        toks.append(x.to(torch.bfloat16))
+    o = torch.empty((steps, B, Hv, dv), dtype=torch.bfloat16, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def run_all():
+        for t in range(steps):
+            g.gdn2_recurrent_step(toks[0][t], toks[1][t], toks[2][t], toks[3][t], toks[4][t], toks[5][t], st, o[t])
+
+    for _ in range(3):
+        run_all()
+    torch.cuda.synchronize(device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = 3
+    e0.record(stream)
+    for _ in range(reps):
+        run_all()
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    us = e0.elapsed_time(e1) * 1e3 / (reps * steps)
+    b = decode_step_bytes(B, Hk, Hv, dk, dv)
+    gbs = b / (us * 1e-6) / 1e9
+    return {"workload": f"{DECODE_WORKLOAD}: {wl.description}", "kernel": "recurrent_step_kernel",
+            "us_per_step": round(us, 2), "bytes_per_step": b, "achieved": round(gbs, 1), "peak": hbm,
+            "unit": "GB/s", "frac": round(gbs / hbm, 4), "bound": "hbm",
+            "l2": "state 201 MB > L2; 256 back-to-back steps"}
+
+
+def end_to_end(g, wl, host, device, args, tokens):
+    """Same step through the public API with host (pinned) buffers: inputs copied in, o copied out."""
+    import torch
+
+    T, D = wl.T, wl.decode_steps
+    B, Hv, dv = wl.B, wl.Hv, wl.dv
+    hpre = {n: host[n][:, :T].contiguous().pin_memory() for n in host}
+    hdec = {n: host[n][:, T:T + D].transpose(0, 1).contiguous().pin_memory() for n in host}  # [D, B, H, d]
+    o_h = torch.empty((B, T, Hv, dv), dtype=torch.bfloat16).pin_memory()
+    od_h = torch.empty((B, D, Hv, dv), dtype=torch.bfloat16).pin_memory()
+    stream = torch.cuda.current_stream(device)
+    h2d = sum(t.numel() * t.element_size() for t in hpre.values()) + sum(
+        t.numel() * t.element_size() for t in hdec.values())
+    d2h = o_h.numel() * 2 + od_h.numel() * 2
+
+    def step():
+        d = {n: t.to(device, non_blocking=True) for n, t in hpre.items()}
+        dd = {n: t.to(device, non_blocking=True) for n, t in hdec.items()}
+        o, st = g.chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["b"], d["w"], None)
+        outs = []
+        for i in range(D):
+            outs.append(g.recurrent_step(*(dd[n][i] for n in ("q", "k", "v", "g", "b", "w")), st))
+        o_h.copy_(o, non_blocking=True)
+        od_h.copy_(torch.stack(outs, dim=1), non_blocking=True)
+
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize(device)
+    n = max(2, min(args.steps, 5))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    ms = e0.elapsed_time(e1) / n
+    return {"value": round(tokens / (ms * 1e-3), 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 3), "steps": n}
+
+
+# ---- CPU baseline (the fp64 oracle) --------------------------------------------------------------
+
+def cpu_sample(target_s: float = 12.0, max_tokens: int = 4096):
+    """Time the oracle on one sequence of the workload (all 32 value heads) for a bounded number of
+    tokens, sized to about `target_s` seconds of CPU time. Returns (tokens/s, sample description, threads)."""
+    import oracle
+
+    wl = synth.WORKLOADS[WORKLOAD]
+    nth = min(oracle.default_threads(), wl.Hv)
+
+    def timed(Ts):
+        inp = synth.make_inputs(wl.with_(B=1), T=Ts)
+        t0 = time.perf_counter()
+        oracle.run_inputs(inp, nthreads=nth)
+        return time.perf_counter() - t0
+
+    t_cal = timed(64)
+    Ts = int(min(max_tokens, max(64, 64 * target_s / max(t_cal, 1e-3))))
+    dt = timed(Ts)
+    return Ts / dt, f"1 sequence x {wl.Hv} value heads x {Ts} tokens of {WORKLOAD} (fp64 recurrent form)", nth, dt
+
+
+def run_reference(args):
+    import oracle  # noqa: F401
+
+    wl = synth.WORKLOADS[WORKLOAD]
+    nth = min(os.cpu_count() or 1, wl.Hv)
+    Ts = 256
+    inp = synth.make_inputs(wl.with_(B=1), T=Ts)
+    import oracle as orc
+    for _ in range(args.warmup):
+        orc.run_inputs(inp, nthreads=nth)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        orc.run_inputs(inp, nthreads=nth)
+        times.append(time.perf_counter() - t0)
+    ms = 1e3 * sum(times) / len(times)
+    value = Ts / (ms * 1e-3)
+    sample = f"each step: 1 sequence x {wl.Hv} value heads x {Ts} tokens of {WORKLOAD} (fp64 recurrent form)"
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{WORKLOAD}: {wl.description}"},
+        "cpu_baseline": {"value": round(value, 1), "unit": "tokens/s", "cores": nth, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 1), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def run_profile(spec: str):
+    """One operation of one workload, twice (the second call is the one to capture with ncu -s 1).
+    spec: 'chunk:<workload>' or 'decode:<workload>'."""
+    import torch
+
+    import gated_deltanet_mixer_gdn2_gb300 as g
+
+    op, name = spec.split(":")
+    wl = synth.WORKLOADS[name]
+    device = torch.device("cuda", 0)
+    if op == "chunk":
+        inp = synth.make_inputs(wl, T=wl.T)
+        q, k, v, gg, b, w = (synth.to_torch(np.ascontiguousarray(getattr(inp, n)), wl.dtype, device)
+                             for n in ("q", "k", "v", "g", "b", "w"))
+        s0 = None if inp.s0 is None else torch.from_numpy(inp.s0).to(device)
+        for _ in range(2):
+            g.chunk_fwd(q, k, v, gg, b, w, s0, C=wl.C)
+    elif op == "decode":
+        inp = synth.make_inputs(wl, T=2)
+        st = torch.from_numpy(inp.s0).to(device)
+        for t in range(2):
+            tok = [synth.to_torch(np.ascontiguousarray(getattr(inp, n)[:, t]), wl.dtype, device)
+                   for n in ("q", "k", "v", "g", "b", "w")]
+            g.recurrent_step(*tok, st)
+    else:
+        raise SystemExit(f"unknown op {op}")
+    torch.cuda.synchronize()
+    status = g.gdn2_last_device_status()
+    print(json.dumps({"profile": spec, "status": g.status_string(status)}))
+    if status != g.GDN2_OK:
+        raise SystemExit(1)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--profile", default=None, help="op:workload, e.g. chunk:long_negeig_bf16 (for ncu)")
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-decode-workload", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.profile:
+        run_profile(args.profile)
+        return
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+
+    import torch
+
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+    # the oracle's CPU baseline runs before any GPU work of this process touches a thread pool
+    cpu = None
+    if rank == 0 and not args.no_cpu:
+        tps, sample, cores, secs = cpu_sample()
+        cpu = {"value": round(tps, 1), "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample,
+               "seconds": round(secs, 2)}
+    line = run_ours(args, rank, world, device)
+    if cpu:
+        line["cpu_baseline"] = cpu
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -17,9 +17,9 @@ def _declared_functions():
 
 @pytest.fixture(scope="module")
 def g():
-    from gated_deltanet_mixer_gdn2_gb300 import _build
+    import __graft_entry__
 
-    _build.build()
+    __graft_entry__._build_module().build()
     import gated_deltanet_mixer_gdn2_gb300 as mod
 
     return mod
