@@ -24,6 +24,7 @@ EXPORTS = (
     "gdn2_status_string", "gdn2_version", "gdn2_chunk_fwd_workspace_size",
     "gdn2_chunk_fwd_workspace_size_path", "gdn2_chunk_fwd", "gdn2_chunk_fwd_path",
     "gdn2_recurrent_step", "gdn2_last_device_status", "gdn2_set_wait_limit", "gdn2_selftest_umma",
+    "gdn2_chunk_fwd_noalloc",
 )
 
 
@@ -51,6 +52,7 @@ def _load() -> ctypes.CDLL:
         "gdn2_last_device_status": (I, [P]),
         "gdn2_set_wait_limit": (None, [L]),
         "gdn2_selftest_umma": (I, [I, I, P, P, P, P]),
+        "gdn2_chunk_fwd_noalloc": (I, [P] * 9 + [I] * 7 + [F, I, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -133,6 +135,19 @@ def gdn2_chunk_fwd(q, k, v, g, b, w, o, initial_state=None, final_state=None, *,
                                  _ptr(initial_state), _ptr(final_state), _ptr(o), B, T, Hk, Hv, dk, dv,
                                  C, float(scale), dt, _ptr(workspace), workspace.numel(), _stream(stream))
     _check(st, "gdn2_chunk_fwd")
+    return o, final_state
+
+
+def gdn2_chunk_fwd_noalloc(q, k, v, g, b, w, o, initial_state=None, final_state=None, *, C=64, scale=1.0,
+                           stream=None):
+    """Chunked forward without a caller workspace (C ABI gdn2_chunk_fwd_noalloc): for callers that
+    cannot allocate device memory; the library's fixed 32 MiB device array serves as workspace."""
+    B, T, Hk, dk = q.shape
+    Hv, dv = v.shape[2], v.shape[3]
+    st = lib.gdn2_chunk_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(b), _ptr(w), _ptr(initial_state),
+                                    _ptr(final_state), _ptr(o), B, T, Hk, Hv, dk, dv, C, float(scale),
+                                    _dtype_code(q), _stream(stream))
+    _check(st, "gdn2_chunk_fwd_noalloc")
     return o, final_state
 
 

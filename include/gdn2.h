@@ -105,6 +105,29 @@ gdn2_status gdn2_chunk_fwd_path(gdn2_path path, const void* q, const void* k, co
                                 gdn2_dtype dt, void* workspace, size_t ws_bytes, void* stream);
 
 /*
+ * gdn2_chunk_fwd_noalloc -- gdn2_chunk_fwd for callers that cannot allocate device memory. The
+ * pages have no counterpart: this is a convenience of this library. Some callers cannot call
+ * cudaMalloc -- a plugin whose host framework has reserved the device memory and owns the
+ * allocator, or a serving loop that must not call cudaMalloc / cudaFree (cudaFree synchronises the
+ * device; cudaMalloc can block or fail once memory is reserved) -- so they cannot provide the
+ * workspace gdn2_chunk_fwd needs. This entry point takes the same arguments minus the workspace
+ * and uses a fixed 32 MiB array in device memory that every GPU loading the library keeps until
+ * the process exits. It allocates nothing.
+ *   - Limit: problems whose workspace (gdn2_chunk_fwd_workspace_size) exceeds 33 554 432 bytes
+ *     are rejected with GDN2_ERR_WORKSPACE before any work is enqueued (on the tensor-core path,
+ *     one 91 136-byte unit per chunk and value head: at most 368 of them).
+ *   - Set-up: the first call on a device looks up the array's device address (with that device
+ *     current) and caches it; make that first call before any stream capture.
+ *   - Sharing: all calls share the array and it keeps the last call's contents (nothing in it needs
+ *     to start at zero); calls whose kernels overlap on the GPU race on it.
+ * Other arguments, errors and results: as gdn2_chunk_fwd (AUTO path).
+ */
+gdn2_status gdn2_chunk_fwd_noalloc(const void* q, const void* k, const void* v, const void* g,
+                                   const void* b, const void* w, const float* initial_state,
+                                   float* final_state, void* o, int B, int T, int Hk, int Hv,
+                                   int dk, int dv, int C, float scale, gdn2_dtype dt, void* stream);
+
+/*
  * gdn2_recurrent_step -- one decode token against a persistent fp32 state, updated in place
  * (burn-gdn2 docs: token-by-token recurrent mode with persistent state; the same single fused
  * update that the llama.cpp GDN decode study describes for the scalar-beta rule).
