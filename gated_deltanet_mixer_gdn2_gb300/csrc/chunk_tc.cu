@@ -37,9 +37,9 @@ constexpr int kD = 128;
 constexpr int kSlice = 64;
 
 // workspace unit (one chunk of one value head), bytes
-constexpr uint32_t kWsWT = 0;        // W^T      [128][64] bf16
-constexpr uint32_t kWsQbT = 16384;   // (q.e^G)^T [128][64] bf16
-constexpr uint32_t kWsKhT = 32768;   // (k.e^{G_last-G})^T [128][64] bf16
+constexpr uint32_t kWsW = 0;         // W = T (b.k.e^G)      token-major [64][128] bf16
+constexpr uint32_t kWsQb = 16384;    // q.e^G                token-major [64][128] bf16
+constexpr uint32_t kWsKh = 32768;    // k.e^{G_last - G}     token-major [64][128] bf16
 constexpr uint32_t kWsM = 49152;     // M        [64][64]  bf16
 constexpr uint32_t kWsUtT = 57344;   // U~^T     [128][64] fp32
 constexpr uint32_t kWsGam = 90112;   // e^{G_last} [128] fp32
@@ -73,12 +73,6 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<const uint32_t*>(&v);
 }
 
-__device__ __forceinline__ float bf16_at(const uint8_t* base, uint32_t off) {
-    return __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(base + off));
-}
-__device__ __forceinline__ void store_bf16(uint8_t* base, uint32_t off, float x) {
-    *reinterpret_cast<__nv_bfloat16*>(base + off) = __float2bfloat16_rn(x);
-}
 
 // 64 fp32 columns of this warp's TMEM lanes starting at column `col`.
 __device__ __forceinline__ void tmem_ld64(uint32_t tmem_base, int warp, int col, float (&x)[64]) {
@@ -92,55 +86,95 @@ __device__ __forceinline__ void tmem_ld64(uint32_t tmem_base, int warp, int col,
     }
 }
 
-// Write 64 values as one 128-byte bf16 row `row` of a 128B-swizzled tile at `tile`.
-__device__ __forceinline__ void store_row_sw128(uint8_t* tile, int row, const float (&x)[64]) {
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-        uint4 u;
-        u.x = pack_bf16x2(x[8 * c + 0], x[8 * c + 1]);
-        u.y = pack_bf16x2(x[8 * c + 2], x[8 * c + 3]);
-        u.z = pack_bf16x2(x[8 * c + 4], x[8 * c + 5]);
-        u.w = pack_bf16x2(x[8 * c + 6], x[8 * c + 7]);
-        *reinterpret_cast<uint4*>(tile + row * 128 + ((c ^ (row & 7)) << 4)) = u;
-    }
-}
-
-__device__ __forceinline__ void store_row_bf16_global(void* dst, const float (&x)[64], float scale) {
-    uint4* p = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-        uint4 u;
-        u.x = pack_bf16x2(scale * x[8 * c + 0], scale * x[8 * c + 1]);
-        u.y = pack_bf16x2(scale * x[8 * c + 2], scale * x[8 * c + 3]);
-        u.z = pack_bf16x2(scale * x[8 * c + 4], scale * x[8 * c + 5]);
-        u.w = pack_bf16x2(scale * x[8 * c + 6], scale * x[8 * c + 7]);
-        p[c] = u;
-    }
-}
 
 // ---------------------------------------------------------------------------------------------
 // kernel 1: per-chunk factors
 
 struct FactorMaps {
-    CUtensorMap q, k, g, b, v, w;
+    CUtensorMap q, k, g, b, v, w;  // token tiles (loads)
+    CUtensorMap m_st, utt_st;      // workspace sections written with TMA stores
 };
 
 namespace fs {  // shared-memory layout of the factor kernel (offsets from a 1024-aligned base)
 constexpr uint32_t A1 = 0;        // [b.k.e^{G-a} ; q.e^{G-a}] 128 x 128, K-major, two 64-wide K blocks
 constexpr uint32_t K = 32768;     // k -> k.e^{a-G} (64 x 128, K-major, two K blocks)
-constexpr uint32_t G = 49152;     // g -> b.k.e^{G} (64 tokens x 128, MN-major for M = d_k)
-constexpr uint32_t V = 65536;     // v -> w.v       (MN-major for M = d_v)
-constexpr uint32_t W = 81920;     // w (then fp32 scratch for the blocked solve)
-constexpr uint32_t T = 98304;     // T = (I + A)^{-1} bf16, 64 x 64, K-major (rows i, columns j)
+constexpr uint32_t G = 49152;     // g (prefix pass only), then M staging [64][64] bf16
+constexpr uint32_t V = 65536;     // v -> w.v        (64 tokens x 128, MN-major A operand for M = d_v)
+constexpr uint32_t W = 81920;     // w -> b.k.e^{G}  (64 tokens x 128, MN-major A operand for M = d_k)
+constexpr uint32_t T = 98304;     // token-group sums (fp32 [16][128]), then T = (I + A)^{-1} bf16 64 x 64
 constexpr uint32_t BAR = 106496;  // 2 mbarriers, TMEM base, flag
-constexpr uint32_t TOTAL = BAR + 64;
-constexpr uint32_t AF = 0;        // fp32 A [64][65] (aliases A1/K once A|M has been read)
-constexpr uint32_t TF = 16640;    // fp32 T [64][65]
-constexpr uint32_t PF = W;        // fp32 [3][16][16] partial products
-constexpr int LDF = 65;
+constexpr uint32_t CST = BAR + 64;  // per-channel anchor a, e^{a}, e^{G_last - a} (fp32 [3][128])
+constexpr uint32_t TOTAL = CST + 3 * 512;
+// solve scratch (A1/K are dead once A|M has been read): fp32, 16-byte aligned rows of 68
+constexpr int LDF = 68;
+constexpr uint32_t AF = 0;                       // A [64][68]
+constexpr uint32_t TF = 64 * LDF * 4;            // T [64][68]
+constexpr uint32_t PF = 2 * 64 * LDF * 4;        // products [32][36]
+constexpr int LDP = 36;
+// output staging after the last MMA: W token-major [64][128] bf16 and U~^T [128][64] fp32
+constexpr uint32_t WSTG = 0;
+constexpr uint32_t USTG = 16384;
+constexpr int kThreads = 256;
 }  // namespace fs
 
-__global__ void __launch_bounds__(128, 2)
+__device__ __forceinline__ void unpack8(const uint4& u, float (&x)[8]) {
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 f = __bfloat1622float2(h[i]);
+        x[2 * i] = f.x;
+        x[2 * i + 1] = f.y;
+    }
+}
+__device__ __forceinline__ uint4 pack8(const float (&x)[8]) {
+    return make_uint4(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]), pack_bf16x2(x[4], x[5]),
+                      pack_bf16x2(x[6], x[7]));
+}
+
+// Issue n16 x 16-column TMEM loads of this warp's lanes, then one wait.
+template <int N16>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float (&x)[16 * N16]) {
+    uint32_t r[N16][16];
+#pragma unroll
+    for (int q = 0; q < N16; ++q) tmem_ld16(taddr + 16 * q, r[q]);
+    tmem_ld_wait();
+#pragma unroll
+    for (int q = 0; q < N16; ++q)
+#pragma unroll
+        for (int i = 0; i < 16; ++i) x[16 * q + i] = __uint_as_float(r[q][i]);
+}
+
+__device__ __forceinline__ void bulk_store(void* gdst, const void* ssrc, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(reinterpret_cast<uint64_t>(gdst)),
+                 "r"(smem_u32(ssrc)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void tma_store_3d(const void* map, const void* src, int c0, int c1, int c2) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// out[r][c4..c4+3] = sum_k L[r][k] R[k][c4..c4+3] over k in [k0, k1) (fp32 smem, 16-byte rows)
+template <int KN>
+__device__ __forceinline__ float4 row_times(const float* Lrow, const float* R, int ldr, int c4) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int k = 0; k < KN; ++k) {
+        const float a = Lrow[k];
+        const float4 b = *reinterpret_cast<const float4*>(R + k * ldr + c4);
+        acc.x = fmaf(a, b.x, acc.x);
+        acc.y = fmaf(a, b.y, acc.y);
+        acc.z = fmaf(a, b.z, acc.z);
+        acc.w = fmaf(a, b.w, acc.w);
+    }
+    return acc;
+}
+
+__global__ void __launch_bounds__(fs::kThreads, 2)
     factors_tc_kernel(const __grid_constant__ FactorMaps maps, uint8_t* __restrict__ ws, int Hk, int Hv, int NC,
                       long long wait_ns) {
     extern __shared__ uint8_t smem_raw[];
@@ -150,11 +184,16 @@ __global__ void __launch_bounds__(128, 2)
     uint64_t* bar_mma = bar_tma + 1;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + fs::BAR + 16);
     int* flag = reinterpret_cast<int*>(sm + fs::BAR + 20);
+    float* s_anc = reinterpret_cast<float*>(sm + fs::CST);
+    float* s_ea = s_anc + 128;
+    float* s_ela = s_anc + 256;
+    float* s_gs = reinterpret_cast<float*>(sm + fs::T);  // [16 token groups][128 channels]
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int n = blockIdx.x, bh = blockIdx.y;
     const int bi = bh / Hv, hv = bh - bi * Hv, hk = hv / (Hv / Hk);
-    uint8_t* unit = ws + (static_cast<size_t>(bh) * NC + n) * kWsUnit;
+    const int unit_idx = bh * NC + n;
+    uint8_t* unit = ws + static_cast<size_t>(unit_idx) * kWsUnit;
 
     if (tid == 0) {
         mbar_init(bar_tma, 1);
@@ -185,57 +224,100 @@ __global__ void __launch_bounds__(128, 2)
     }
     bool ok = cta_wait(bar_tma, 0, wait_ns, flag);
     if (ok) {
-        // ---- one pass over the chunk per channel c (thread c): decayed operands, outputs
-        const int c = tid;
-        const int kb = c >> 6, cc = c & 63;
-        uint8_t* pA1b = sm + fs::A1 + kb * 16384;
-        uint8_t* pA1q = pA1b + 8192;
+        // ---- elementwise pass. Thread = (channel chunk j: 8 channels, token group tg: 4 tokens);
+        //      every shared-memory access is one 16-byte chunk of a 128-byte swizzled row.
+        const int j = tid & 15, tg = tid >> 4;
+        const int kb = j >> 3, cj = j & 7;
+        uint8_t* pB = sm + fs::A1 + kb * 16384;
+        uint8_t* pQ = pB + 8192;
         uint8_t* pK = sm + fs::K + kb * 8192;
         uint8_t* pG = sm + fs::G + kb * 8192;
         uint8_t* pV = sm + fs::V + kb * 8192;
         uint8_t* pW = sm + fs::W + kb * 8192;
-        float gmin = 0.f, gmax = 0.f, acc = 0.f;
-        for (int t = 0; t < kC; ++t) {
-            acc += bf16_at(pG, sw128_off(t, cc));
-            gmin = (t == 0) ? acc : fminf(gmin, acc);
-            gmax = (t == 0) ? acc : fmaxf(gmax, acc);
-        }
-        const float glast = acc;
-        const float anc = 0.5f * (gmin + gmax);
-        uint32_t qb_pack[4], kh_pack[4];
-        float G = 0.f;
-        for (int t = 0; t < kC; ++t) {
-            const uint32_t off = sw128_off(t, cc);
-            G += bf16_at(pG, off);
-            const float e1 = __expf(G - anc);
-            const float e2 = __expf(anc - G);
-            const float eg = __expf(G);
-            const float er = __expf(glast - G);
-            const float kk = bf16_at(pK, off), qq = bf16_at(pA1q, off), bb = bf16_at(pA1b, off);
-            const float vv = bf16_at(pV, off), ww = bf16_at(pW, off);
-            store_bf16(pA1b, off, bb * kk * e1);
-            store_bf16(pA1q, off, qq * e1);
-            store_bf16(pK, off, kk * e2);
-            store_bf16(pG, off, bb * kk * eg);
-            store_bf16(pV, off, ww * vv);
-            const float qb = qq * eg, kh = kk * er;
-            const int slot = (t & 7) >> 1;
-            if (t & 1) {
-                qb_pack[slot] |= static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(qb))) << 16;
-                kh_pack[slot] |= static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(kh))) << 16;
-            } else {
-                qb_pack[slot] = __bfloat16_as_ushort(__float2bfloat16_rn(qb));
-                kh_pack[slot] = __bfloat16_as_ushort(__float2bfloat16_rn(kh));
+        auto off = [&](int t) { return t * 128 + ((cj ^ (t & 7)) << 4); };
+        float L[4][8];  // inclusive prefix of g within the token group
+        {
+            float x[8];
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                unpack8(*reinterpret_cast<const uint4*>(pG + off(4 * tg + r)), x);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) L[r][i] = (r ? L[r - 1][i] : 0.f) + x[i];
             }
-            if ((t & 7) == 7) {
-                const int chunk = t >> 3;
-                *reinterpret_cast<uint4*>(unit + kWsQbT + c * 128 + chunk * 16) =
-                    make_uint4(qb_pack[0], qb_pack[1], qb_pack[2], qb_pack[3]);
-                *reinterpret_cast<uint4*>(unit + kWsKhT + c * 128 + chunk * 16) =
-                    make_uint4(kh_pack[0], kh_pack[1], kh_pack[2], kh_pack[3]);
+            float4* dst = reinterpret_cast<float4*>(s_gs + tg * 128 + 8 * j);
+            dst[0] = make_float4(L[3][0], L[3][1], L[3][2], L[3][3]);
+            dst[1] = make_float4(L[3][4], L[3][5], L[3][6], L[3][7]);
+        }
+        __syncthreads();
+        if (tid < 128) {  // exclusive prefix over the 16 token groups, per channel
+            const int c = tid;
+            float run = 0.f;
+#pragma unroll
+            for (int q = 0; q < 16; ++q) {
+                const float x = s_gs[q * 128 + c];
+                s_gs[q * 128 + c] = run;
+                run += x;
+            }
+            const float g0 = __bfloat162float(
+                *reinterpret_cast<const __nv_bfloat16*>(sm + fs::G + (c >> 6) * 8192 + sw128_off(0, c & 63)));
+            const float a = 0.5f * (g0 + run);  // G_0 and G_last bracket G when log-decays are <= 0
+            s_anc[c] = a;
+            s_ea[c] = __expf(a);
+            s_ela[c] = __expf(run - a);
+            reinterpret_cast<float*>(unit + kWsGam)[c] = __expf(run);
+        }
+        __syncthreads();
+        {
+            float pre[8], anc[8], ea[8], ela[8];
+            {
+                const float4* p4 = reinterpret_cast<const float4*>(s_gs + tg * 128 + 8 * j);
+                const float4* a4 = reinterpret_cast<const float4*>(s_anc + 8 * j);
+                const float4* e4 = reinterpret_cast<const float4*>(s_ea + 8 * j);
+                const float4* l4 = reinterpret_cast<const float4*>(s_ela + 8 * j);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const float4 pp = p4[h], aa = a4[h], ee = e4[h], ll = l4[h];
+                    pre[4 * h] = pp.x; pre[4 * h + 1] = pp.y; pre[4 * h + 2] = pp.z; pre[4 * h + 3] = pp.w;
+                    anc[4 * h] = aa.x; anc[4 * h + 1] = aa.y; anc[4 * h + 2] = aa.z; anc[4 * h + 3] = aa.w;
+                    ea[4 * h] = ee.x; ea[4 * h + 1] = ee.y; ea[4 * h + 2] = ee.z; ea[4 * h + 3] = ee.w;
+                    ela[4 * h] = ll.x; ela[4 * h + 1] = ll.y; ela[4 * h + 2] = ll.z; ela[4 * h + 3] = ll.w;
+                }
+            }
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const int t = 4 * tg + r;
+                const int o = off(t);
+                float kk[8], qq[8], bb[8], vv[8], wv[8];
+                unpack8(*reinterpret_cast<const uint4*>(pK + o), kk);
+                unpack8(*reinterpret_cast<const uint4*>(pQ + o), qq);
+                unpack8(*reinterpret_cast<const uint4*>(pB + o), bb);
+                unpack8(*reinterpret_cast<const uint4*>(pV + o), vv);
+                unpack8(*reinterpret_cast<const uint4*>(pW + o), wv);
+                float o_kb[8], o_qa[8], o_kt[8], o_kg[8], qb[8], kh[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float Gi = pre[i] + L[r][i];
+                    const float e1 = __expf(Gi - anc[i]);   // e^{G - a}
+                    const float e2 = __expf(anc[i] - Gi);   // e^{a - G}
+                    const float bk = bb[i] * kk[i];
+                    o_kb[i] = bk * e1;
+                    o_qa[i] = qq[i] * e1;
+                    o_kt[i] = kk[i] * e2;
+                    o_kg[i] = bk * (e1 * ea[i]);            // b.k.e^{G}
+                    qb[i] = qq[i] * (e1 * ea[i]);            // q.e^{G}
+                    kh[i] = kk[i] * (e2 * ela[i]);           // k.e^{G_last - G}
+                    wv[i] *= vv[i];
+                }
+                *reinterpret_cast<uint4*>(pB + o) = pack8(o_kb);
+                *reinterpret_cast<uint4*>(pQ + o) = pack8(o_qa);
+                *reinterpret_cast<uint4*>(pK + o) = pack8(o_kt);
+                *reinterpret_cast<uint4*>(pW + o) = pack8(o_kg);   // in place of w (same thread, same chunk)
+                *reinterpret_cast<uint4*>(pV + o) = pack8(wv);
+                // decayed q and k, token-major rows of 256 bytes: one 16-byte chunk per thread
+                *reinterpret_cast<uint4*>(unit + kWsQb + t * 256 + j * 16) = pack8(qb);
+                *reinterpret_cast<uint4*>(unit + kWsKh + t * 256 + j * 16) = pack8(kh);
             }
         }
-        reinterpret_cast<float*>(unit + kWsGam)[c] = __expf(glast);
         fence_proxy_async_smem();
         __syncthreads();
 
@@ -258,23 +340,46 @@ __global__ void __launch_bounds__(128, 2)
         float* AF = reinterpret_cast<float*>(sm + fs::AF);
         float* TF = reinterpret_cast<float*>(sm + fs::TF);
         float* PF = reinterpret_cast<float*>(sm + fs::PF);
+        // T scratch starts at zero: the blocked solve below relies on its strictly upper blocks being 0
+        for (int p = tid; p < 64 * fs::LDF / 4; p += fs::kThreads)
+            reinterpret_cast<float4*>(TF)[p] = make_float4(0.f, 0.f, 0.f, 0.f);
         {
-            float x[64];
-            tmem_ld64(tmem, warp, 0, x);
-            if (warp < 2) {
-                const int i = 32 * warp + lane;
+            // warp w reads lanes 32(w%4).. and columns 32(w/4)..+31
+            const int q4 = warp & 3, half = warp >> 2;
+            float x[32];
+            tmem_ld_cols<2>(tmem + (static_cast<uint32_t>(32 * q4) << 16) + 32 * half, x);
+            if (q4 < 2) {  // A rows, strictly lower
+                const int i = 32 * q4 + lane;
+                float4* dst = reinterpret_cast<float4*>(AF + i * fs::LDF + 32 * half);
 #pragma unroll
-                for (int j = 0; j < 64; ++j) AF[i * fs::LDF + j] = (j < i) ? x[j] : 0.f;
-            } else {
-                const int i = 32 * (warp - 2) + lane;
+                for (int c4 = 0; c4 < 8; ++c4) {
+                    float y[4];
 #pragma unroll
-                for (int j = 0; j < 64; ++j) x[j] = (j <= i) ? x[j] : 0.f;
-                store_row_bf16_global(unit + kWsM + i * 128, x, 1.f);
+                    for (int e = 0; e < 4; ++e) y[e] = (32 * half + 4 * c4 + e < i) ? x[4 * c4 + e] : 0.f;
+                    dst[c4] = make_float4(y[0], y[1], y[2], y[3]);
+                }
+            } else {       // M rows, lower incl. diagonal, staged (128-byte swizzle) for a TMA store
+                const int i = 32 * (q4 - 2) + lane;
+#pragma unroll
+                for (int c8 = 0; c8 < 4; ++c8) {
+                    float y[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) y[e] = (32 * half + 8 * c8 + e <= i) ? x[8 * c8 + e] : 0.f;
+                    *reinterpret_cast<uint4*>(sm + fs::G + i * 128 + (((4 * half + c8) ^ (i & 7)) << 4)) = pack8(y);
+                }
             }
         }
+        fence_proxy_async_smem();
         __syncthreads();
-        // ---- T = (I + A)^{-1}: diagonal 16x16 blocks (one warp each), then block rows
-        if (lane < 16) {
+        if (tid == 0) {
+            tma_store_3d(&maps.m_st, sm + fs::G, 0, 0, unit_idx);
+            bulk_commit();
+        }
+        // ---- T = (I + A)^{-1}, blocked: (1) the four 16x16 diagonal blocks by forward substitution
+        //      (warps 0-3, one column per lane); (2) the two 16x16 blocks below them inside each
+        //      32x32 diagonal block, T_{i+1,i} = -D_{i+1} A_{i+1,i} D_i; (3) the 32x32 block below
+        //      the diagonal, T_10 = -T_11 A_10 T_00.
+        if (warp < 4 && lane < 16) {
             const int base = 16 * warp, jj = lane;
             float x[16];
 #pragma unroll
@@ -288,26 +393,41 @@ __global__ void __launch_bounds__(128, 2)
             for (int i = 0; i < 16; ++i) TF[(base + i) * fs::LDF + base + jj] = x[i];
         }
         __syncthreads();
-        for (int I = 1; I < 4; ++I) {
-            for (int e = tid; e < I * 256; e += 128) {
-                const int J = e >> 8, r = (e >> 4) & 15, cq = e & 15;
-                float s = 0.f;
-                for (int m = 16 * J; m < 16 * I; ++m) s = fmaf(AF[(16 * I + r) * fs::LDF + m], TF[m * fs::LDF + 16 * J + cq], s);
-                PF[e] = s;
-            }
-            __syncthreads();
-            for (int e = tid; e < I * 256; e += 128) {
-                const int J = e >> 8, r = (e >> 4) & 15, cq = e & 15;
-                float s = 0.f;
-#pragma unroll
-                for (int m = 0; m < 16; ++m) s = fmaf(TF[(16 * I + r) * fs::LDF + 16 * I + m], PF[(J << 8) + (m << 4) + cq], s);
-                TF[(16 * I + r) * fs::LDF + 16 * J + cq] = -s;
-            }
-            __syncthreads();
+        if (tid < 128) {  // Y_i = A_{i+1,i} D_i for diagonal blocks i = 0, 2 (16 x 16 each, 4 columns per thread)
+            const int blk = tid >> 6, r = (tid >> 2) & 15, c4 = (tid & 3) * 4;
+            const int i0 = 32 * blk;  // D_i at rows/cols i0..i0+15; A_{i+1,i} at rows i0+16.., cols i0..
+            const float4 y = row_times<16>(AF + (i0 + 16 + r) * fs::LDF + i0, TF + i0 * fs::LDF + i0, fs::LDF, c4);
+            *reinterpret_cast<float4*>(PF + (blk * 16 + r) * fs::LDP + c4) = y;
         }
-        for (int p = tid; p < 64 * 64; p += 128) {
-            const int i = p >> 6, j = p & 63;
-            store_bf16(sm + fs::T, sw128_off(i, j), (j <= i) ? TF[i * fs::LDF + j] : 0.f);
+        __syncthreads();
+        if (tid < 128) {  // T_{i+1,i} = -D_{i+1} Y_i
+            const int blk = tid >> 6, r = (tid >> 2) & 15, c4 = (tid & 3) * 4;
+            const int i1 = 32 * blk + 16;
+            const float4 y = row_times<16>(TF + (i1 + r) * fs::LDF + i1, PF + (blk * 16) * fs::LDP, fs::LDP, c4);
+            *reinterpret_cast<float4*>(TF + (i1 + r) * fs::LDF + i1 - 16 + c4) = make_float4(-y.x, -y.y, -y.z, -y.w);
+        }
+        __syncthreads();
+        {  // X = A_10 T_00 (32 x 32; rows 32.., cols 0..31), one float4 per thread
+            const int r = tid >> 3, c4 = (tid & 7) * 4;
+            const float4 y = row_times<32>(AF + (32 + r) * fs::LDF, TF, fs::LDF, c4);
+            *reinterpret_cast<float4*>(PF + r * fs::LDP + c4) = y;
+        }
+        __syncthreads();
+        {  // T_10 = -T_11 X
+            const int r = tid >> 3, c4 = (tid & 7) * 4;
+            const float4 y = row_times<32>(TF + (32 + r) * fs::LDF + 32, PF, fs::LDP, c4);
+            *reinterpret_cast<float4*>(TF + (32 + r) * fs::LDF + c4) = make_float4(-y.x, -y.y, -y.z, -y.w);
+        }
+        __syncthreads();
+        for (int p = tid; p < 64 * 8; p += fs::kThreads) {  // bf16 T, K-major rows (one 16-byte chunk per item)
+            const int i = p >> 3, c8 = p & 7;
+            float y[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const int jc = 8 * c8 + e;
+                y[e] = (jc <= i) ? TF[i * fs::LDF + jc] : 0.f;
+            }
+            *reinterpret_cast<uint4*>(sm + fs::T + i * 128 + ((c8 ^ (i & 7)) << 4)) = pack8(y);
         }
         fence_proxy_async_smem();
         tc_fence_before();
@@ -319,7 +439,7 @@ __global__ void __launch_bounds__(128, 2)
 #pragma unroll
             for (int s = 0; s < 4; ++s) {
                 const uint64_t bd = smem_desc(sbase + fs::T + s * 32, 16, 1024, kSwizzle128B);
-                const uint64_t a1 = smem_desc(sbase + fs::G + s * 2048, 8192, 1024, kSwizzle128B);
+                const uint64_t a1 = smem_desc(sbase + fs::W + s * 2048, 8192, 1024, kSwizzle128B);
                 const uint64_t a2 = smem_desc(sbase + fs::V + s * 2048, 8192, 1024, kSwizzle128B);
                 mma_bf16(tmem + 64, a1, bd, id, s > 0);
                 mma_bf16(tmem + 128, a2, bd, id, s > 0);
@@ -329,16 +449,32 @@ __global__ void __launch_bounds__(128, 2)
         ok = cta_wait(bar_mma, 1, wait_ns, flag);
         if (ok) {
             tc_fence_after();
-            const int c = tid;
+            const int q4 = warp & 3;
+            const int c = 32 * q4 + lane;
             float x[64];
-            tmem_ld64(tmem, warp, 64, x);
-            store_row_bf16_global(unit + kWsWT + c * 128, x, 1.f);
-            tmem_ld64(tmem, warp, 128, x);
-            float4* dst = reinterpret_cast<float4*>(unit + kWsUtT + c * 256);
+            if (warp < 4) {  // W token-major: column c of [64 tokens][128 channels] bf16
+                tmem_ld_cols<4>(tmem + (static_cast<uint32_t>(32 * q4) << 16) + 64, x);
+                __nv_bfloat16* wst = reinterpret_cast<__nv_bfloat16*>(sm + fs::WSTG);
 #pragma unroll
-            for (int q4 = 0; q4 < 16; ++q4) dst[q4] = make_float4(x[4 * q4], x[4 * q4 + 1], x[4 * q4 + 2], x[4 * q4 + 3]);
+                for (int t = 0; t < 64; ++t) wst[t * 128 + c] = __float2bfloat16_rn(x[t]);
+            } else {         // U~^T row c, fp32, as two 128-byte-swizzled [128][32] tiles for TMA stores
+                tmem_ld_cols<4>(tmem + (static_cast<uint32_t>(32 * q4) << 16) + 128, x);
+#pragma unroll
+                for (int q = 0; q < 16; ++q)
+                    *reinterpret_cast<float4*>(sm + fs::USTG + (q >> 3) * 16384 + c * 128 + (((q & 7) ^ (c & 7)) << 4)) =
+                        make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
+            }
+            fence_proxy_async_smem();
+            __syncthreads();
+            if (tid == 0) {
+                bulk_store(unit + kWsW, sm + fs::WSTG, 16384);
+                tma_store_3d(&maps.utt_st, sm + fs::USTG, 0, 0, unit_idx);
+                tma_store_3d(&maps.utt_st, sm + fs::USTG + 16384, 32, 0, unit_idx);
+                bulk_commit();
+            }
         }
     }
+    if (tid == 0) bulk_wait_all();
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, 256);
@@ -348,12 +484,12 @@ __global__ void __launch_bounds__(128, 2)
 // kernel 2: state chain + output
 
 struct StateMaps {
-    CUtensorMap wt, qbt, kht, m, utt;
+    CUtensorMap w, qb, kh, m, utt;
 };
 
 namespace ss {
-constexpr uint32_t A1 = 0;          // [W ; Q] MN-major: W^T tile, then (q.e^G)^T tile (16 KB each)
-constexpr uint32_t A3 = 32768;      // (k.e^{G_last-G})^T, K-major (rows d_k, K = tokens)
+constexpr uint32_t A1 = 0;          // [W ; Q] K-major, two 64-wide K blocks of [128 rows][128 B]
+constexpr uint32_t A3 = 32768;      // k.e^{G_last-G} token-major = MN-major A for K^^T (two 64-channel blocks)
 constexpr uint32_t A2 = 49152;      // [0 ; M], K-major (rows 0..63 zero)
 constexpr uint32_t UT = 65536;      // U~^T slice, fp32 [64 columns][64 tokens]
 constexpr uint32_t GAM = 81920;     // e^{G_last} fp32 [128]
@@ -363,9 +499,25 @@ constexpr uint32_t UBF = SBF + 16384;       // U bf16 [64 tokens][64], MN-major 
 constexpr uint32_t BAR = UBF + 8192;        // full[2], mma, TMEM base, 3 flags
 constexpr uint32_t TOTAL = BAR + 64;
 constexpr uint32_t TX = 16384 * 3 + 8192 + 16384 + 512;
+constexpr int kThreads = 256;
+// TMEM columns: D1 (rows 0-63: W S_n; rows 64-127: Q S_n + M U) double-buffered at 0 and 128,
+// D2 = K^^T U at 64.
+__host__ __device__ constexpr uint32_t d1_col(int n) { return (n & 1) ? 128u : 0u; }
+constexpr uint32_t kD2 = 64;
 }  // namespace ss
 
-__global__ void __launch_bounds__(128, 1)
+// Write 32 values as half `half` (16-byte chunks 4*half .. 4*half+3) of 128-byte swizzled row `row`.
+__device__ __forceinline__ void store_halfrow_sw128(uint8_t* tile, int row, int half, const float (&x)[32]) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        float y[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) y[e] = x[8 * c + e];
+        *reinterpret_cast<uint4*>(tile + row * 128 + (((4 * half + c) ^ (row & 7)) << 4)) = pack8(y);
+    }
+}
+
+__global__ void __launch_bounds__(ss::kThreads, 1)
     state_tc_kernel(const __grid_constant__ StateMaps maps, const uint8_t* __restrict__ ws,
                     const float* __restrict__ s0, float* __restrict__ sT_out, __nv_bfloat16* __restrict__ o, int T,
                     int Hv, int NC, float scale, long long wait_ns) {
@@ -378,10 +530,12 @@ __global__ void __launch_bounds__(128, 1)
     int* flag = reinterpret_cast<int*>(sm + ss::BAR + 28);  // 3 slots: one per wait site, so that a
                                                             // slot is never rewritten before all read it
 
-    const int tid = threadIdx.x, warp = tid >> 5;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int q4 = warp & 3, half = warp >> 2;  // TMEM lane quarter, column half
     const int bh = blockIdx.x, z = blockIdx.y;
     const int bi = bh / Hv, hv = bh - bi * Hv;
-    const int r = tid;  // d_k row owned by this thread (= TMEM lane)
+    const int r = 32 * q4 + lane;  // d_k row of the state (= TMEM lane) owned by this thread
+    const uint32_t lane_base = static_cast<uint32_t>(32 * q4) << 16;
 
     if (tid == 0) {
         mbar_init(full, 1);
@@ -390,26 +544,25 @@ __global__ void __launch_bounds__(128, 1)
         fence_mbar_init();
     }
     if (warp == 0) {
-        tmem_alloc(tmem_slot, 128);
+        tmem_alloc(tmem_slot, 256);
         tmem_relinquish();
     }
-    // zero rows 0..63 of the [0 ; M] operand in both stages
-    for (int p = tid; p < 2 * 512; p += 128) {
+    for (int p = tid; p < 2 * 512; p += ss::kThreads) {  // rows 0..63 of [0 ; M], both stages
         const int st = p >> 9, q16 = p & 511;
         reinterpret_cast<uint4*>(sm + st * ss::STAGE + ss::A2)[q16] = make_uint4(0, 0, 0, 0);
     }
-    float S[64];
+    float S[32];  // S_n[r][32*half + j], fp32
     {
-        const float* src = s0 ? s0 + (static_cast<size_t>(bh) * kD + r) * kD + z * kSlice : nullptr;
+        const float* src = s0 ? s0 + (static_cast<size_t>(bh) * kD + r) * kD + z * kSlice + 32 * half : nullptr;
 #pragma unroll
-        for (int j = 0; j < 64; j += 4) {
-            float4 t4 = src ? *reinterpret_cast<const float4*>(src + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int j = 0; j < 32; j += 4) {
+            const float4 t4 = src ? *reinterpret_cast<const float4*>(src + j) : make_float4(0.f, 0.f, 0.f, 0.f);
             S[j] = t4.x;
             S[j + 1] = t4.y;
             S[j + 2] = t4.z;
             S[j + 3] = t4.w;
         }
-        store_row_sw128(sm + ss::SBF, r, S);
+        store_halfrow_sw128(sm + ss::SBF, r, half, S);
     }
     fence_proxy_async_smem();
     tc_fence_before();
@@ -422,12 +575,34 @@ __global__ void __launch_bounds__(128, 1)
         uint8_t* sb = sm + st * ss::STAGE;
         const int u = bh * NC + n;
         mbar_arrive_expect_tx(full + st, ss::TX);
-        tma_load_3d(sb + ss::A1, &maps.wt, 0, 0, u, full + st);
-        tma_load_3d(sb + ss::A1 + 16384, &maps.qbt, 0, 0, u, full + st);
-        tma_load_3d(sb + ss::A3, &maps.kht, 0, 0, u, full + st);
+#pragma unroll
+        for (int kb = 0; kb < 2; ++kb) {
+            tma_load_3d(sb + ss::A1 + kb * 16384, &maps.w, 64 * kb, 0, u, full + st);
+            tma_load_3d(sb + ss::A1 + kb * 16384 + 8192, &maps.qb, 64 * kb, 0, u, full + st);
+            tma_load_3d(sb + ss::A3 + kb * 8192, &maps.kh, 64 * kb, 0, u, full + st);
+        }
         tma_load_3d(sb + ss::A2 + 8192, &maps.m, 0, 0, u, full + st);
         tma_load_3d(sb + ss::UT, &maps.utt, 0, z * kSlice, u, full + st);
         bulk_load(sb + ss::GAM, ws + static_cast<size_t>(u) * kWsUnit + kWsGam, 512, full + st);
+    };
+    // O rows of chunk m (tokens 64m..64m+63) from the D1 buffer it was accumulated in
+    auto emit_o = [&](int m) {
+        if (q4 < 2) return;
+        const int i = 32 * (q4 - 2) + lane;
+        const int tok = m * kC + i;
+        float x[32];
+        tmem_ld_cols<2>(tmem + lane_base + ss::d1_col(m) + 32 * half, x);
+        if (tok < T) {
+            uint4* dst = reinterpret_cast<uint4*>(o + ((static_cast<size_t>(bi) * T + tok) * Hv + hv) * kD +
+                                                  z * kSlice + 32 * half);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                float y[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) y[e] = scale * x[8 * c + e];
+                dst[c] = pack8(y);
+            }
+        }
     };
     if (tid == 0 && NC > 0) issue(0);
 
@@ -437,48 +612,51 @@ __global__ void __launch_bounds__(128, 1)
     for (; n < NC && ok; ++n) {
         const int st = n & 1;
         const uint32_t sb = sbase + st * ss::STAGE;
+        const uint32_t d1 = tmem + ss::d1_col(n);
         if (tid == 0 && n + 1 < NC) issue(n + 1);
         ok = cta_wait(full + st, (n >> 1) & 1, wait_ns, flag + 0);
         if (!ok) break;
-        // ---- D1 = [W ; Q] S_n   (M = 128, N = 64, K = 128; A and B MN-major)
-        if (tid == 0) {
-            tc_fence_after();
-            constexpr uint32_t id = idesc_bf16(128, 64, true, true);
-#pragma unroll
-            for (int s = 0; s < 8; ++s) {
-                const uint64_t ad = smem_desc(sb + ss::A1 + s * 2048, 16384, 1024, kSwizzle128B);
-                const uint64_t bd = smem_desc(sbase + ss::SBF + s * 2048, 16384, 1024, kSwizzle128B);
-                mma_bf16(tmem, ad, bd, id, s > 0);
-            }
-            mma_commit(bar_mma);
-        }
-        ok = cta_wait(bar_mma, mma_phase, wait_ns, flag + 1);
-        mma_phase ^= 1;
-        if (!ok) break;
-        tc_fence_after();
-        if (warp < 2) {  // U = U~ - W S_n for tokens i = 0..63
-            const int i = tid;
-            float x[64];
-            tmem_ld64(tmem, warp, 0, x);
-            const float* ut = reinterpret_cast<const float*>(sm + st * ss::STAGE + ss::UT);
-#pragma unroll
-            for (int j = 0; j < 64; ++j) x[j] = ut[j * 64 + i] - x[j];
-            store_row_sw128(sm + ss::UBF, i, x);
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        // ---- D1 += [0 ; M] U  and  D2 = K^^T U   (M = 128, N = 64, K = 64; A K-major, B MN-major)
+        // ---- D1 = [W ; Q] S_n   (M = 128, N = 64, K = 128; A K-major, B MN-major)
         if (tid == 0) {
             tc_fence_after();
             constexpr uint32_t id = idesc_bf16(128, 64, false, true);
 #pragma unroll
+            for (int s = 0; s < 8; ++s) {
+                const uint64_t ad = smem_desc(sb + ss::A1 + (s >> 2) * 16384 + (s & 3) * 32, 16, 1024, kSwizzle128B);
+                const uint64_t bd = smem_desc(sbase + ss::SBF + s * 2048, 16384, 1024, kSwizzle128B);
+                mma_bf16(d1, ad, bd, id, s > 0);
+            }
+            mma_commit(bar_mma);
+        }
+        if (n > 0) emit_o(n - 1);  // previous chunk's output, overlapping this MMA
+        ok = cta_wait(bar_mma, mma_phase, wait_ns, flag + 1);
+        mma_phase ^= 1;
+        if (!ok) break;
+        tc_fence_after();
+        if (q4 < 2) {  // U = U~ - W S_n for tokens i = 0..63, this thread's 32 columns
+            const int i = r;
+            float x[32];
+            tmem_ld_cols<2>(d1 + lane_base + 32 * half, x);
+            const float* ut = reinterpret_cast<const float*>(sm + st * ss::STAGE + ss::UT);
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj) x[jj] = ut[(32 * half + jj) * 64 + i] - x[jj];
+            store_halfrow_sw128(sm + ss::UBF, i, half, x);
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        // ---- D1 += [0 ; M] U (A K-major)  and  D2 = K^^T U (A MN-major)   (M = 128, N = 64, K = 64)
+        if (tid == 0) {
+            tc_fence_after();
+            constexpr uint32_t id2 = idesc_bf16(128, 64, false, true);
+            constexpr uint32_t id3 = idesc_bf16(128, 64, true, true);
+#pragma unroll
             for (int s = 0; s < 4; ++s) {
                 const uint64_t bd = smem_desc(sbase + ss::UBF + s * 2048, 8192, 1024, kSwizzle128B);
                 const uint64_t a2 = smem_desc(sb + ss::A2 + s * 32, 16, 1024, kSwizzle128B);
-                const uint64_t a3 = smem_desc(sb + ss::A3 + s * 32, 16, 1024, kSwizzle128B);
-                mma_bf16(tmem, a2, bd, id, 1);
-                mma_bf16(tmem + 64, a3, bd, id, s > 0);
+                const uint64_t a3 = smem_desc(sb + ss::A3 + s * 2048, 8192, 1024, kSwizzle128B);
+                mma_bf16(d1, a2, bd, id2, 1);
+                mma_bf16(tmem + ss::kD2, a3, bd, id3, s > 0);
             }
             mma_commit(bar_mma);
         }
@@ -486,21 +664,13 @@ __global__ void __launch_bounds__(128, 1)
         mma_phase ^= 1;
         if (!ok) break;
         tc_fence_after();
-        if (warp >= 2) {  // O rows = tokens 0..63
-            const int i = tid - 64;
-            const int tok = n * kC + i;
-            float x[64];
-            tmem_ld64(tmem, warp, 0, x);
-            if (tok < T)
-                store_row_bf16_global(o + ((static_cast<size_t>(bi) * T + tok) * Hv + hv) * kD + z * kSlice, x, scale);
-        }
         {
-            float x[64];
-            tmem_ld64(tmem, warp, 64, x);
+            float x[32];
+            tmem_ld_cols<2>(tmem + lane_base + ss::kD2 + 32 * half, x);
             const float gam = reinterpret_cast<const float*>(sm + st * ss::STAGE + ss::GAM)[r];
 #pragma unroll
-            for (int j = 0; j < 64; ++j) S[j] = fmaf(gam, S[j], x[j]);
-            store_row_sw128(sm + ss::SBF, r, S);
+            for (int jj = 0; jj < 32; ++jj) S[jj] = fmaf(gam, S[jj], x[jj]);
+            store_halfrow_sw128(sm + ss::SBF, r, half, S);
         }
         fence_proxy_async_smem();
         tc_fence_before();
@@ -509,14 +679,17 @@ __global__ void __launch_bounds__(128, 1)
     if (!ok) {
         // drain the prefetch of the next chunk if it was issued
         if (tid == 0 && n + 1 < NC) mbar_wait(full + ((n + 1) & 1), ((n + 1) >> 1) & 1, kDefaultWaitNs);
-    } else if (sT_out) {
-        float* dst = sT_out + (static_cast<size_t>(bh) * kD + r) * kD + z * kSlice;
+    } else {
+        if (NC > 0) emit_o(NC - 1);
+        if (sT_out) {
+            float* dst = sT_out + (static_cast<size_t>(bh) * kD + r) * kD + z * kSlice + 32 * half;
 #pragma unroll
-        for (int j = 0; j < 64; j += 4) *reinterpret_cast<float4*>(dst + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
+            for (int j = 0; j < 32; j += 4) *reinterpret_cast<float4*>(dst + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
+        }
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, 128);
+    if (warp == 0) tmem_dealloc(tmem, 256);
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -654,12 +827,12 @@ bool token_map(CUtensorMap* m, const void* p, int B, int T, int H) {
     return make_map(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, p, dims, st, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-// workspace section viewed as (cols, rows, units)
+// workspace section viewed as (cols, rows, units); box (box_cols, box_rows, 1)
 bool ws_map(CUtensorMap* m, const void* p, CUtensorMapDataType dt, int esize, int cols, int rows, int units,
-            int box_rows, CUtensorMapSwizzle sw) {
+            int box_cols, int box_rows, CUtensorMapSwizzle sw) {
     const uint64_t dims[3] = {(uint64_t)cols, (uint64_t)rows, (uint64_t)units};
     const uint64_t st[2] = {(uint64_t)cols * esize, kWsUnit};
-    const uint32_t box[3] = {(uint32_t)cols, (uint32_t)box_rows, 1};
+    const uint32_t box[3] = {(uint32_t)box_cols, (uint32_t)box_rows, 1};
     return make_map(m, dt, 3, p, dims, st, box, sw);
 }
 
@@ -679,33 +852,32 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const v
         !token_map(&fm.v, v, sh.B, sh.T, sh.Hv) || !token_map(&fm.w, w, sh.B, sh.T, sh.Hv))
         return cudaErrorInvalidValue;
     const int units = NC * sh.B * sh.Hv;
-    const uint8_t* wsb = static_cast<const uint8_t*>(ws);
+    uint8_t* wsb = static_cast<uint8_t*>(ws);
+    const auto BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const auto F32 = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    const auto SW = CU_TENSOR_MAP_SWIZZLE_128B;
+    if (!ws_map(&fm.m_st, wsb + kWsM, BF, 2, 64, 64, units, 64, 64, SW) ||
+        !ws_map(&fm.utt_st, wsb + kWsUtT, F32, 4, 64, 128, units, 32, 128, SW))
+        return cudaErrorInvalidValue;
     StateMaps sm_;
-    if (!ws_map(&sm_.wt, wsb + kWsWT, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 64, 128, units, 128,
-                CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !ws_map(&sm_.qbt, wsb + kWsQbT, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 64, 128, units, 128,
-                CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !ws_map(&sm_.kht, wsb + kWsKhT, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 64, 128, units, 128,
-                CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !ws_map(&sm_.m, wsb + kWsM, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 64, 64, units, 64,
-                CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !ws_map(&sm_.utt, wsb + kWsUtT, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, 64, 128, units, kSlice,
-                CU_TENSOR_MAP_SWIZZLE_NONE))
+    if (!ws_map(&sm_.w, wsb + kWsW, BF, 2, 128, 64, units, 64, 64, SW) ||
+        !ws_map(&sm_.qb, wsb + kWsQb, BF, 2, 128, 64, units, 64, 64, SW) ||
+        !ws_map(&sm_.kh, wsb + kWsKh, BF, 2, 128, 64, units, 64, 64, SW) ||
+        !ws_map(&sm_.m, wsb + kWsM, BF, 2, 64, 64, units, 64, 64, SW) ||
+        !ws_map(&sm_.utt, wsb + kWsUtT, F32, 4, 64, 128, units, 64, kSlice, CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
 
-    // The state kernel runs one CTA per SM, so it takes the whole 227 KB: operand descriptors can
-    // then never reach past the CTA's own allocation.
     const size_t f_smem = fs::TOTAL + 1024, s_smem = 232448;
     static_assert(ss::TOTAL + 1024 <= 232448, "state kernel shared memory");
     cudaError_t e = cudaFuncSetAttribute(factors_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)f_smem);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(state_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s_smem);
     if (e != cudaSuccess) return e;
-    factors_tc_kernel<<<dim3(NC, sh.B * sh.Hv), 128, f_smem, s>>>(fm, static_cast<uint8_t*>(ws), sh.Hk, sh.Hv, NC,
+    factors_tc_kernel<<<dim3(NC, sh.B * sh.Hv), fs::kThreads, f_smem, s>>>(fm, static_cast<uint8_t*>(ws), sh.Hk, sh.Hv, NC,
                                                                   wait_ns);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    state_tc_kernel<<<dim3(sh.B * sh.Hv, kD / kSlice), 128, s_smem, s>>>(
+    state_tc_kernel<<<dim3(sh.B * sh.Hv, kD / kSlice), ss::kThreads, s_smem, s>>>(
         sm_, wsb, s0, sT, static_cast<__nv_bfloat16*>(o), sh.T, sh.Hv, NC, scale, wait_ns);
     return cudaGetLastError();
 }
