@@ -61,6 +61,30 @@ def decode_step_bytes(B, Hk, Hv, dk, dv) -> int:
     return 2 * B * Hv * dk * dv * 4 + B * (2 * Hk * dk + Hv * (2 * dk + 2 * dv)) * 2 + B * Hv * dv * 2
 
 
+# ---- multi-GPU host logic (replicas over disjoint sequences; timing reduce only) ------------------
+
+def rank_batch_offset(rank: int, batch_per_rank: int) -> int:
+    """First global batch index of this rank: rank r runs sequences [r*B, (r+1)*B)."""
+    return rank * batch_per_rank
+
+
+def reduce_max(value: float, world: int, device=None) -> float:
+    """Max of `value` over ranks (the slowest rank times the job); identity for one process."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(tokens_per_rank: int, world: int, ms_max: float) -> float:
+    """Whole-job tokens/s: every rank's tokens over the slowest rank's time."""
+    return world * tokens_per_rank / (ms_max * 1e-3)
+
+
 # ---- clocks ------------------------------------------------------------------------------------
 
 class ClockSampler:
@@ -123,7 +147,8 @@ def run_ours(args, rank, world, device):
 
     hbm, tc_burst, tc_sust, peak_kind = peaks()
     wl = synth.WORKLOADS[WORKLOAD]
-    inp = synth.make_inputs(wl)               # host float32 values of bf16 numbers, T + decode tokens
+    # each rank runs its own B sequences (disjoint global batch indices)
+    inp = synth.make_inputs(wl, b0=rank_batch_offset(rank, wl.B))
     T, D = wl.T, wl.decode_steps
     host = {n: synth.to_torch(np.ascontiguousarray(getattr(inp, n)), "bf16").pin_memory()
             for n in ("q", "k", "v", "g", "b", "w")}
@@ -188,13 +213,9 @@ def run_ours(args, rank, world, device):
     chunk_ms = [e[0].elapsed_time(e[1]) for e in events]
     dec_ms = [e[1].elapsed_time(e[2]) for e in events]
     step_ms = [a + b for a, b in zip(chunk_ms, dec_ms)]
-    ms_per_step = sum(step_ms) / len(step_ms)
-    if world > 1:
-        t = torch.tensor([ms_per_step], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_per_step = float(t.item())
+    ms_per_step = reduce_max(sum(step_ms) / len(step_ms), world, device)
     tokens = B * T + B * D
-    value = world * tokens / (ms_per_step * 1e-3)
+    value = job_throughput(tokens, world, ms_per_step)
 
     # roofline of the dominant operation: the chunked forward (factors + state kernels)
     ch_ms = statistics.mean(chunk_ms)
@@ -329,24 +350,21 @@ def end_to_end(g, wl, host, device, args, tokens):
 
 # ---- CPU baseline (the fp64 oracle) --------------------------------------------------------------
 
-def cpu_sample(target_s: float = 12.0, max_tokens: int = 4096):
-    """Time the oracle on one sequence of the workload (all 32 value heads) for a bounded number of
-    tokens, sized to about `target_s` seconds of CPU time. Returns (tokens/s, sample description, threads)."""
+def cpu_sample():
+    """Time the oracle on one full sequence of the bench workload: its 32768-token prefill and 64
+    decode tokens, all 32 value heads (one half of a bench step). Returns (tokens/s, description,
+    threads, seconds)."""
     import oracle
 
     wl = synth.WORKLOADS[WORKLOAD]
     nth = min(oracle.default_threads(), wl.Hv)
-
-    def timed(Ts):
-        inp = synth.make_inputs(wl.with_(B=1), T=Ts)
-        t0 = time.perf_counter()
-        oracle.run_inputs(inp, nthreads=nth)
-        return time.perf_counter() - t0
-
-    t_cal = timed(64)
-    Ts = int(min(max_tokens, max(64, 64 * target_s / max(t_cal, 1e-3))))
-    dt = timed(Ts)
-    return Ts / dt, f"1 sequence x {wl.Hv} value heads x {Ts} tokens of {WORKLOAD} (fp64 recurrent form)", nth, dt
+    inp = synth.make_inputs(wl.with_(B=1))
+    t0 = time.perf_counter()
+    oracle.run_inputs(inp, nthreads=nth)
+    dt = time.perf_counter() - t0
+    Ts = wl.tokens_total
+    return Ts / dt, (f"1 of the {wl.B} sequences of {WORKLOAD}: {wl.T}-token prefill + {wl.decode_steps} "
+                     f"decode tokens, {wl.Hv} value heads (fp64 recurrent form)"), nth, dt
 
 
 def run_reference(args):

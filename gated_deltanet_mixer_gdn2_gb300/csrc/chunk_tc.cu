@@ -40,10 +40,10 @@ constexpr int kSlice = 64;
 constexpr uint32_t kWsW = 0;         // W = T (b.k.e^G)      token-major [64][128] bf16
 constexpr uint32_t kWsQb = 16384;    // q.e^G                token-major [64][128] bf16
 constexpr uint32_t kWsKh = 32768;    // k.e^{G_last - G}     token-major [64][128] bf16
-constexpr uint32_t kWsM = 49152;     // M        [64][64]  bf16
-constexpr uint32_t kWsUtT = 57344;   // U~^T     [128][64] fp32
-constexpr uint32_t kWsGam = 90112;   // e^{G_last} [128] fp32
-constexpr uint32_t kWsUnit = 91136;
+constexpr uint32_t kWsM = 49152;     // M = causal q-k       [64][64] bf16
+constexpr uint32_t kWsT = 57344;     // T = (I + A)^{-1}      [64][64] bf16
+constexpr uint32_t kWsGam = 65536;   // e^{G_last}           [128] fp32
+constexpr uint32_t kWsUnit = 66048;
 
 // ---------------------------------------------------------------------------------------------
 // helpers
@@ -91,18 +91,16 @@ __device__ __forceinline__ void tmem_ld64(uint32_t tmem_base, int warp, int col,
 // kernel 1: per-chunk factors
 
 struct FactorMaps {
-    CUtensorMap q, k, g, b, v, w;  // token tiles (loads)
-    CUtensorMap m_st, utt_st;      // workspace sections written with TMA stores
+    CUtensorMap q, k, g, b;        // token tiles (loads)
+    CUtensorMap m_st, t_st, w_st;  // workspace sections written with TMA stores
 };
 
 namespace fs {  // shared-memory layout of the factor kernel (offsets from a 1024-aligned base)
 constexpr uint32_t A1 = 0;        // [b.k.e^{G-a} ; q.e^{G-a}] 128 x 128, K-major, two 64-wide K blocks
 constexpr uint32_t K = 32768;     // k -> k.e^{a-G} (64 x 128, K-major, two K blocks)
-constexpr uint32_t G = 49152;     // g (prefix pass only), then M staging [64][64] bf16
-constexpr uint32_t V = 65536;     // v -> w.v        (64 tokens x 128, MN-major A operand for M = d_v)
-constexpr uint32_t W = 81920;     // w -> b.k.e^{G}  (64 tokens x 128, MN-major A operand for M = d_k)
-constexpr uint32_t T = 98304;     // token-group sums (fp32 [16][128]), then T = (I + A)^{-1} bf16 64 x 64
-constexpr uint32_t BAR = 106496;  // 2 mbarriers, TMEM base, flag
+constexpr uint32_t G = 49152;     // g -> b.k.e^{G} (64 tokens x 128: MN-major B operand, N = d_k)
+constexpr uint32_t SGS = 65536;   // token-group sums fp32 [16][128]; later M staging [64][64] bf16
+constexpr uint32_t BAR = 73728;   // 2 mbarriers, TMEM base, flag
 constexpr uint32_t CST = BAR + 64;  // per-channel anchor a, e^{a}, e^{G_last - a} (fp32 [3][128])
 constexpr uint32_t TOTAL = CST + 3 * 512;
 // solve scratch (A1/K are dead once A|M has been read): fp32, 16-byte aligned rows of 68
@@ -111,9 +109,11 @@ constexpr uint32_t AF = 0;                       // A [64][68]
 constexpr uint32_t TF = 64 * LDF * 4;            // T [64][68]
 constexpr uint32_t PF = 2 * 64 * LDF * 4;        // products [32][36]
 constexpr int LDP = 36;
-// output staging after the last MMA: W token-major [64][128] bf16 and U~^T [128][64] fp32
+// T = (I + A)^{-1} as bf16 K-major [64][64]; its MMA reads 64 further rows (the first K-block of
+// b.k.e^{G}, finite, result rows discarded)
+constexpr uint32_t TB = 40960;
+// W staging after the last MMA: two 128-byte-swizzled [64 tokens][64 channels] bf16 tiles
 constexpr uint32_t WSTG = 0;
-constexpr uint32_t USTG = 16384;
 constexpr int kThreads = 256;
 }  // namespace fs
 
@@ -144,11 +144,6 @@ __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float (&x)[16 * N16
         for (int i = 0; i < 16; ++i) x[16 * q + i] = __uint_as_float(r[q][i]);
 }
 
-__device__ __forceinline__ void bulk_store(void* gdst, const void* ssrc, uint32_t bytes) {
-    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(reinterpret_cast<uint64_t>(gdst)),
-                 "r"(smem_u32(ssrc)), "r"(bytes)
-                 : "memory");
-}
 __device__ __forceinline__ void tma_store_3d(const void* map, const void* src, int c0, int c1, int c2) {
     asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
                      reinterpret_cast<uint64_t>(map)),
@@ -156,9 +151,9 @@ __device__ __forceinline__ void tma_store_3d(const void* map, const void* src, i
                  : "memory");
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 
-// out[r][c4..c4+3] = sum_k L[r][k] R[k][c4..c4+3] over k in [k0, k1) (fp32 smem, 16-byte rows)
+// sum_k L[k] R[k][c4..c4+3] (fp32 smem, 16-byte aligned rows)
 template <int KN>
 __device__ __forceinline__ float4 row_times(const float* Lrow, const float* R, int ldr, int c4) {
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -187,7 +182,7 @@ __global__ void __launch_bounds__(fs::kThreads, 2)
     float* s_anc = reinterpret_cast<float*>(sm + fs::CST);
     float* s_ea = s_anc + 128;
     float* s_ela = s_anc + 256;
-    float* s_gs = reinterpret_cast<float*>(sm + fs::T);  // [16 token groups][128 channels]
+    float* s_gs = reinterpret_cast<float*>(sm + fs::SGS);  // [16 token groups][128 channels]
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int n = blockIdx.x, bh = blockIdx.y;
@@ -201,7 +196,7 @@ __global__ void __launch_bounds__(fs::kThreads, 2)
         fence_mbar_init();
     }
     if (warp == 0) {
-        tmem_alloc(tmem_slot, 256);
+        tmem_alloc(tmem_slot, 128);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -210,7 +205,7 @@ __global__ void __launch_bounds__(fs::kThreads, 2)
     const uint32_t tmem = *tmem_slot;
 
     if (tid == 0) {
-        mbar_arrive_expect_tx(bar_tma, 6 * 16384);
+        mbar_arrive_expect_tx(bar_tma, 4 * 16384);
         const int t0 = n * kC;
 #pragma unroll
         for (int kb = 0; kb < 2; ++kb) {
@@ -218,8 +213,6 @@ __global__ void __launch_bounds__(fs::kThreads, 2)
             tma_load_4d(sm + fs::A1 + kb * 16384, &maps.b, 64 * kb, hv, t0, bi, bar_tma);
             tma_load_4d(sm + fs::K + kb * 8192, &maps.k, 64 * kb, hk, t0, bi, bar_tma);
             tma_load_4d(sm + fs::G + kb * 8192, &maps.g, 64 * kb, hv, t0, bi, bar_tma);
-            tma_load_4d(sm + fs::V + kb * 8192, &maps.v, 64 * kb, hv, t0, bi, bar_tma);
-            tma_load_4d(sm + fs::W + kb * 8192, &maps.w, 64 * kb, hv, t0, bi, bar_tma);
         }
     }
     bool ok = cta_wait(bar_tma, 0, wait_ns, flag);
@@ -232,8 +225,6 @@ __global__ void __launch_bounds__(fs::kThreads, 2)
         uint8_t* pQ = pB + 8192;
         uint8_t* pK = sm + fs::K + kb * 8192;
         uint8_t* pG = sm + fs::G + kb * 8192;
-        uint8_t* pV = sm + fs::V + kb * 8192;
-        uint8_t* pW = sm + fs::W + kb * 8192;
         auto off = [&](int t) { return t * 128 + ((cj ^ (t & 7)) << 4); };
         float L[4][8];  // inclusive prefix of g within the token group
         {
@@ -287,12 +278,10 @@ __global__ void __launch_bounds__(fs::kThreads, 2)
             for (int r = 0; r < 4; ++r) {
                 const int t = 4 * tg + r;
                 const int o = off(t);
-                float kk[8], qq[8], bb[8], vv[8], wv[8];
+                float kk[8], qq[8], bb[8];
                 unpack8(*reinterpret_cast<const uint4*>(pK + o), kk);
                 unpack8(*reinterpret_cast<const uint4*>(pQ + o), qq);
                 unpack8(*reinterpret_cast<const uint4*>(pB + o), bb);
-                unpack8(*reinterpret_cast<const uint4*>(pV + o), vv);
-                unpack8(*reinterpret_cast<const uint4*>(pW + o), wv);
                 float o_kb[8], o_qa[8], o_kt[8], o_kg[8], qb[8], kh[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
@@ -306,13 +295,11 @@ __global__ void __launch_bounds__(fs::kThreads, 2)
                     o_kg[i] = bk * (e1 * ea[i]);            // b.k.e^{G}
                     qb[i] = qq[i] * (e1 * ea[i]);            // q.e^{G}
                     kh[i] = kk[i] * (e2 * ela[i]);           // k.e^{G_last - G}
-                    wv[i] *= vv[i];
                 }
                 *reinterpret_cast<uint4*>(pB + o) = pack8(o_kb);
                 *reinterpret_cast<uint4*>(pQ + o) = pack8(o_qa);
                 *reinterpret_cast<uint4*>(pK + o) = pack8(o_kt);
-                *reinterpret_cast<uint4*>(pW + o) = pack8(o_kg);   // in place of w (same thread, same chunk)
-                *reinterpret_cast<uint4*>(pV + o) = pack8(wv);
+                *reinterpret_cast<uint4*>(pG + o) = pack8(o_kg);   // in place of g (same thread, same chunk)
                 // decayed q and k, token-major rows of 256 bytes: one 16-byte chunk per thread
                 *reinterpret_cast<uint4*>(unit + kWsQb + t * 256 + j * 16) = pack8(qb);
                 *reinterpret_cast<uint4*>(unit + kWsKh + t * 256 + j * 16) = pack8(kh);
@@ -365,14 +352,15 @@ __global__ void __launch_bounds__(fs::kThreads, 2)
                     float y[8];
 #pragma unroll
                     for (int e = 0; e < 8; ++e) y[e] = (32 * half + 8 * c8 + e <= i) ? x[8 * c8 + e] : 0.f;
-                    *reinterpret_cast<uint4*>(sm + fs::G + i * 128 + (((4 * half + c8) ^ (i & 7)) << 4)) = pack8(y);
+                    *reinterpret_cast<uint4*>(sm + fs::SGS + i * 128 + (((4 * half + c8) ^ (i & 7)) << 4)) = pack8(y);
                 }
             }
         }
         fence_proxy_async_smem();
+        tc_fence_before();
         __syncthreads();
         if (tid == 0) {
-            tma_store_3d(&maps.m_st, sm + fs::G, 0, 0, unit_idx);
+            tma_store_3d(&maps.m_st, sm + fs::SGS, 0, 0, unit_idx);
             bulk_commit();
         }
         // ---- T = (I + A)^{-1}, blocked: (1) the four 16x16 diagonal blocks by forward substitution
@@ -395,7 +383,7 @@ __global__ void __launch_bounds__(fs::kThreads, 2)
         __syncthreads();
         if (tid < 128) {  // Y_i = A_{i+1,i} D_i for diagonal blocks i = 0, 2 (16 x 16 each, 4 columns per thread)
             const int blk = tid >> 6, r = (tid >> 2) & 15, c4 = (tid & 3) * 4;
-            const int i0 = 32 * blk;  // D_i at rows/cols i0..i0+15; A_{i+1,i} at rows i0+16.., cols i0..
+            const int i0 = 32 * blk;
             const float4 y = row_times<16>(AF + (i0 + 16 + r) * fs::LDF + i0, TF + i0 * fs::LDF + i0, fs::LDF, c4);
             *reinterpret_cast<float4*>(PF + (blk * 16 + r) * fs::LDP + c4) = y;
         }
@@ -427,81 +415,84 @@ __global__ void __launch_bounds__(fs::kThreads, 2)
                 const int jc = 8 * c8 + e;
                 y[e] = (jc <= i) ? TF[i * fs::LDF + jc] : 0.f;
             }
-            *reinterpret_cast<uint4*>(sm + fs::T + i * 128 + ((c8 ^ (i & 7)) << 4)) = pack8(y);
+            *reinterpret_cast<uint4*>(sm + fs::TB + i * 128 + ((c8 ^ (i & 7)) << 4)) = pack8(y);
         }
         fence_proxy_async_smem();
         tc_fence_before();
         __syncthreads();
-        // ---- W^T = (b.k.e^G)^T T^T and U~^T = (w.v)^T T^T   (M = 128, N = 64, K = 64)
+        // ---- W = T (b.k.e^G), token-major, as rows 0..63 of [T ; X] (b.k.e^G)   (M = 128, N = 128, K = 64)
         if (tid == 0) {
+            tma_store_3d(&maps.t_st, sm + fs::TB, 0, 0, unit_idx);
+            bulk_commit();
             tc_fence_after();
-            constexpr uint32_t id = idesc_bf16(128, 64, true, false);
+            constexpr uint32_t id = idesc_bf16(128, 128, false, true);
 #pragma unroll
             for (int s = 0; s < 4; ++s) {
-                const uint64_t bd = smem_desc(sbase + fs::T + s * 32, 16, 1024, kSwizzle128B);
-                const uint64_t a1 = smem_desc(sbase + fs::W + s * 2048, 8192, 1024, kSwizzle128B);
-                const uint64_t a2 = smem_desc(sbase + fs::V + s * 2048, 8192, 1024, kSwizzle128B);
-                mma_bf16(tmem + 64, a1, bd, id, s > 0);
-                mma_bf16(tmem + 128, a2, bd, id, s > 0);
+                const uint64_t ad = smem_desc(sbase + fs::TB + s * 32, 16, 1024, kSwizzle128B);
+                const uint64_t bd = smem_desc(sbase + fs::G + s * 2048, 8192, 1024, kSwizzle128B);
+                mma_bf16(tmem, ad, bd, id, s > 0);
             }
             mma_commit(bar_mma);
         }
         ok = cta_wait(bar_mma, 1, wait_ns, flag);
         if (ok) {
             tc_fence_after();
-            const int q4 = warp & 3;
-            const int c = 32 * q4 + lane;
-            float x[64];
-            if (warp < 4) {  // W token-major: column c of [64 tokens][128 channels] bf16
-                tmem_ld_cols<4>(tmem + (static_cast<uint32_t>(32 * q4) << 16) + 64, x);
-                __nv_bfloat16* wst = reinterpret_cast<__nv_bfloat16*>(sm + fs::WSTG);
+            const int q4 = warp & 3, half = warp >> 2;
+            if (q4 < 2) {  // token t = lane row; this thread's 64 channels -> swizzled W staging tile `half`
+                const int t = 32 * q4 + lane;
+                float x[64];
+                tmem_ld_cols<4>(tmem + (static_cast<uint32_t>(32 * q4) << 16) + 64 * half, x);
 #pragma unroll
-                for (int t = 0; t < 64; ++t) wst[t * 128 + c] = __float2bfloat16_rn(x[t]);
-            } else {         // U~^T row c, fp32, as two 128-byte-swizzled [128][32] tiles for TMA stores
-                tmem_ld_cols<4>(tmem + (static_cast<uint32_t>(32 * q4) << 16) + 128, x);
+                for (int c8 = 0; c8 < 8; ++c8) {
+                    float y[8];
 #pragma unroll
-                for (int q = 0; q < 16; ++q)
-                    *reinterpret_cast<float4*>(sm + fs::USTG + (q >> 3) * 16384 + c * 128 + (((q & 7) ^ (c & 7)) << 4)) =
-                        make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
+                    for (int e = 0; e < 8; ++e) y[e] = x[8 * c8 + e];
+                    *reinterpret_cast<uint4*>(sm + fs::WSTG + half * 8192 + t * 128 + ((c8 ^ (t & 7)) << 4)) = pack8(y);
+                }
             }
             fence_proxy_async_smem();
             __syncthreads();
             if (tid == 0) {
-                bulk_store(unit + kWsW, sm + fs::WSTG, 16384);
-                tma_store_3d(&maps.utt_st, sm + fs::USTG, 0, 0, unit_idx);
-                tma_store_3d(&maps.utt_st, sm + fs::USTG + 16384, 32, 0, unit_idx);
+                tma_store_3d(&maps.w_st, sm + fs::WSTG, 0, 0, unit_idx);
+                tma_store_3d(&maps.w_st, sm + fs::WSTG + 8192, 64, 0, unit_idx);
                 bulk_commit();
             }
         }
     }
-    if (tid == 0) bulk_wait_all();
+    if (tid == 0) bulk_wait_read_all();  // staging must be read out before the CTA releases its memory
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, 256);
+    if (warp == 0) tmem_dealloc(tmem, 128);
 }
 
 // ---------------------------------------------------------------------------------------------
 // kernel 2: state chain + output
 
 struct StateMaps {
-    CUtensorMap w, qb, kh, m, utt;
+    CUtensorMap w, qb, kh, m, t;   // workspace sections
+    CUtensorMap v, wg;             // token tiles of v and of the write gate w
 };
 
 namespace ss {
-constexpr uint32_t A1 = 0;          // [W ; Q] K-major, two 64-wide K blocks of [128 rows][128 B]
-constexpr uint32_t A3 = 32768;      // k.e^{G_last-G} token-major = MN-major A for K^^T (two 64-channel blocks)
-constexpr uint32_t A2 = 49152;      // [0 ; M], K-major (rows 0..63 zero)
-constexpr uint32_t UT = 65536;      // U~^T slice, fp32 [64 columns][64 tokens]
-constexpr uint32_t GAM = 81920;     // e^{G_last} fp32 [128]
-constexpr uint32_t STAGE = 82944;
+// one pipeline stage (offsets inside the stage; every tile 1024-byte aligned)
+constexpr uint32_t A1 = 0;          // [W ; Q]: two 64-wide K blocks of [128 rows][128 B], K-major
+constexpr uint32_t KH = 32768;      // k.e^{G_last-G} token-major: MN-major A operand of K^^T (2 blocks)
+constexpr uint32_t MM = 49152;      // M [64][64] K-major; as [X ; M] its first 64 rows are KH's 2nd block
+constexpr uint32_t TT = 57344;      // T [64][64] K-major; as [T ; 0] it is followed by ...
+constexpr uint32_t ZZ = 65536;      // ... 64 rows of zeros (written once)
+constexpr uint32_t VV = 73728;      // v slice [64 tokens][64 columns] (128-byte swizzle)
+constexpr uint32_t WW = 81920;      // w slice
+constexpr uint32_t GAM = 90112;     // e^{G_last} fp32 [128]
+constexpr uint32_t STAGE = 91136;
+constexpr uint32_t TX = 3 * 16384 + 4 * 8192 + 512;   // bytes delivered per stage
 constexpr uint32_t SBF = 2 * STAGE;         // S_n bf16 [128 rows d_k][64], MN-major B operand
 constexpr uint32_t UBF = SBF + 16384;       // U bf16 [64 tokens][64], MN-major B operand
-constexpr uint32_t BAR = UBF + 8192;        // full[2], mma, TMEM base, 3 flags
+constexpr uint32_t WV = UBF + 8192;         // w.v bf16 [64 tokens][64], MN-major B operand
+constexpr uint32_t BAR = WV + 8192;         // full[2], mma, TMEM base, 3 flags
 constexpr uint32_t TOTAL = BAR + 64;
-constexpr uint32_t TX = 16384 * 3 + 8192 + 16384 + 512;
 constexpr int kThreads = 256;
-// TMEM columns: D1 (rows 0-63: W S_n; rows 64-127: Q S_n + M U) double-buffered at 0 and 128,
-// D2 = K^^T U at 64.
+// TMEM columns: D1 (rows 0-63: U = T(w.v) - W S_n; rows 64-127: -(Q S_n + M U)) double-buffered at
+// 0 and 128; D2 = K^^T U at 64.
 __host__ __device__ constexpr uint32_t d1_col(int n) { return (n & 1) ? 128u : 0u; }
 constexpr uint32_t kD2 = 64;
 }  // namespace ss
@@ -547,9 +538,9 @@ __global__ void __launch_bounds__(ss::kThreads, 1)
         tmem_alloc(tmem_slot, 256);
         tmem_relinquish();
     }
-    for (int p = tid; p < 2 * 512; p += ss::kThreads) {  // rows 0..63 of [0 ; M], both stages
+    for (int p = tid; p < 2 * 512; p += ss::kThreads) {  // the zero rows under T, both stages
         const int st = p >> 9, q16 = p & 511;
-        reinterpret_cast<uint4*>(sm + st * ss::STAGE + ss::A2)[q16] = make_uint4(0, 0, 0, 0);
+        reinterpret_cast<uint4*>(sm + st * ss::STAGE + ss::ZZ)[q16] = make_uint4(0, 0, 0, 0);
     }
     float S[32];  // S_n[r][32*half + j], fp32
     {
@@ -579,13 +570,15 @@ __global__ void __launch_bounds__(ss::kThreads, 1)
         for (int kb = 0; kb < 2; ++kb) {
             tma_load_3d(sb + ss::A1 + kb * 16384, &maps.w, 64 * kb, 0, u, full + st);
             tma_load_3d(sb + ss::A1 + kb * 16384 + 8192, &maps.qb, 64 * kb, 0, u, full + st);
-            tma_load_3d(sb + ss::A3 + kb * 8192, &maps.kh, 64 * kb, 0, u, full + st);
+            tma_load_3d(sb + ss::KH + kb * 8192, &maps.kh, 64 * kb, 0, u, full + st);
         }
-        tma_load_3d(sb + ss::A2 + 8192, &maps.m, 0, 0, u, full + st);
-        tma_load_3d(sb + ss::UT, &maps.utt, 0, z * kSlice, u, full + st);
+        tma_load_3d(sb + ss::MM, &maps.m, 0, 0, u, full + st);
+        tma_load_3d(sb + ss::TT, &maps.t, 0, 0, u, full + st);
+        tma_load_4d(sb + ss::VV, &maps.v, z * kSlice, hv, n * kC, bi, full + st);
+        tma_load_4d(sb + ss::WW, &maps.wg, z * kSlice, hv, n * kC, bi, full + st);
         bulk_load(sb + ss::GAM, ws + static_cast<size_t>(u) * kWsUnit + kWsGam, 512, full + st);
     };
-    // O rows of chunk m (tokens 64m..64m+63) from the D1 buffer it was accumulated in
+    // O rows of chunk m (tokens 64m..64m+63): the D1 rows 64..127 it was accumulated in hold -O
     auto emit_o = [&](int m) {
         if (q4 < 2) return;
         const int i = 32 * (q4 - 2) + lane;
@@ -599,7 +592,7 @@ __global__ void __launch_bounds__(ss::kThreads, 1)
             for (int c = 0; c < 4; ++c) {
                 float y[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) y[e] = scale * x[8 * c + e];
+                for (int e = 0; e < 8; ++e) y[e] = -scale * x[8 * c + e];
                 dst[c] = pack8(y);
             }
         }
@@ -611,50 +604,69 @@ __global__ void __launch_bounds__(ss::kThreads, 1)
     int n = 0;
     for (; n < NC && ok; ++n) {
         const int st = n & 1;
+        uint8_t* sbp = sm + st * ss::STAGE;
         const uint32_t sb = sbase + st * ss::STAGE;
         const uint32_t d1 = tmem + ss::d1_col(n);
         if (tid == 0 && n + 1 < NC) issue(n + 1);
         ok = cta_wait(full + st, (n >> 1) & 1, wait_ns, flag + 0);
         if (!ok) break;
-        // ---- D1 = [W ; Q] S_n   (M = 128, N = 64, K = 128; A K-major, B MN-major)
+        {  // w.v for this chunk's 64 x 64 slice: two 16-byte chunks per thread, same swizzled positions
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+                const int item = tid + 256 * h2;  // 512 chunks = 64 rows x 8 chunks
+                const uint32_t off = (item >> 3) * 128 + ((item & 7) << 4);
+                float a[8], bw[8];
+                unpack8(*reinterpret_cast<const uint4*>(sbp + ss::VV + off), a);
+                unpack8(*reinterpret_cast<const uint4*>(sbp + ss::WW + off), bw);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) a[e] *= bw[e];
+                *reinterpret_cast<uint4*>(sm + ss::WV + off) = pack8(a);
+            }
+        }
+        fence_proxy_async_smem();
+        __syncthreads();
+        // ---- D1 = [T ; 0] (w.v)  then  D1 -= [W ; Q] S_n          (M = 128, N = 64)
         if (tid == 0) {
             tc_fence_after();
-            constexpr uint32_t id = idesc_bf16(128, 64, false, true);
+            constexpr uint32_t id0 = idesc_bf16(128, 64, false, true);
+            constexpr uint32_t id1 = idesc_bf16(128, 64, false, true) | kNegateA;
+#pragma unroll
+            for (int s = 0; s < 4; ++s) {
+                const uint64_t ad = smem_desc(sb + ss::TT + s * 32, 16, 1024, kSwizzle128B);
+                const uint64_t bd = smem_desc(sbase + ss::WV + s * 2048, 8192, 1024, kSwizzle128B);
+                mma_bf16(d1, ad, bd, id0, s > 0);
+            }
 #pragma unroll
             for (int s = 0; s < 8; ++s) {
                 const uint64_t ad = smem_desc(sb + ss::A1 + (s >> 2) * 16384 + (s & 3) * 32, 16, 1024, kSwizzle128B);
                 const uint64_t bd = smem_desc(sbase + ss::SBF + s * 2048, 16384, 1024, kSwizzle128B);
-                mma_bf16(d1, ad, bd, id, s > 0);
+                mma_bf16(d1, ad, bd, id1, 1);
             }
             mma_commit(bar_mma);
         }
-        if (n > 0) emit_o(n - 1);  // previous chunk's output, overlapping this MMA
+        if (n > 0) emit_o(n - 1);  // previous chunk's output, overlapping these MMAs
         ok = cta_wait(bar_mma, mma_phase, wait_ns, flag + 1);
         mma_phase ^= 1;
         if (!ok) break;
         tc_fence_after();
-        if (q4 < 2) {  // U = U~ - W S_n for tokens i = 0..63, this thread's 32 columns
-            const int i = r;
+        if (q4 < 2) {  // U rows = tokens 0..63, this thread's 32 columns
             float x[32];
             tmem_ld_cols<2>(d1 + lane_base + 32 * half, x);
-            const float* ut = reinterpret_cast<const float*>(sm + st * ss::STAGE + ss::UT);
-#pragma unroll
-            for (int jj = 0; jj < 32; ++jj) x[jj] = ut[(32 * half + jj) * 64 + i] - x[jj];
-            store_halfrow_sw128(sm + ss::UBF, i, half, x);
+            store_halfrow_sw128(sm + ss::UBF, r, half, x);
         }
         fence_proxy_async_smem();
         tc_fence_before();
         __syncthreads();
-        // ---- D1 += [0 ; M] U (A K-major)  and  D2 = K^^T U (A MN-major)   (M = 128, N = 64, K = 64)
+        // ---- D1 -= [X ; M] U (rows 0..63 are discarded)  and  D2 = K^^T U     (M = 128, N = 64, K = 64)
         if (tid == 0) {
             tc_fence_after();
-            constexpr uint32_t id2 = idesc_bf16(128, 64, false, true);
+            constexpr uint32_t id2 = idesc_bf16(128, 64, false, true) | kNegateA;
             constexpr uint32_t id3 = idesc_bf16(128, 64, true, true);
 #pragma unroll
             for (int s = 0; s < 4; ++s) {
                 const uint64_t bd = smem_desc(sbase + ss::UBF + s * 2048, 8192, 1024, kSwizzle128B);
-                const uint64_t a2 = smem_desc(sb + ss::A2 + s * 32, 16, 1024, kSwizzle128B);
-                const uint64_t a3 = smem_desc(sb + ss::A3 + s * 2048, 8192, 1024, kSwizzle128B);
+                const uint64_t a2 = smem_desc(sb + ss::MM - 8192 + s * 32, 16, 1024, kSwizzle128B);
+                const uint64_t a3 = smem_desc(sb + ss::KH + s * 2048, 8192, 1024, kSwizzle128B);
                 mma_bf16(d1, a2, bd, id2, 1);
                 mma_bf16(tmem + ss::kD2, a3, bd, id3, s > 0);
             }
@@ -667,7 +679,7 @@ __global__ void __launch_bounds__(ss::kThreads, 1)
         {
             float x[32];
             tmem_ld_cols<2>(tmem + lane_base + ss::kD2 + 32 * half, x);
-            const float gam = reinterpret_cast<const float*>(sm + st * ss::STAGE + ss::GAM)[r];
+            const float gam = reinterpret_cast<const float*>(sbp + ss::GAM)[r];
 #pragma unroll
             for (int jj = 0; jj < 32; ++jj) S[jj] = fmaf(gam, S[jj], x[jj]);
             store_halfrow_sw128(sm + ss::SBF, r, half, S);
@@ -706,6 +718,8 @@ __global__ void __launch_bounds__(128, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(sm);
+    const bool negate = (case_id == 4);  // case 4: case 0 with the A operand negated by the descriptor
+    if (negate) case_id = 0;
     uint8_t* sA = sm;
     uint8_t* sB = sm + 32768;
     uint64_t* bar = reinterpret_cast<uint64_t*>(sm + 49152);
@@ -758,7 +772,7 @@ __global__ void __launch_bounds__(128, 1)
     if (ok) {
         if (tid == 0) {
             tc_fence_after();
-            const uint32_t id = idesc_bf16(128, 64, a_mn, b_mn);
+            const uint32_t id = idesc_bf16(128, 64, a_mn, b_mn) | (negate ? kNegateA : 0u);
             for (int s = 0; s < K / 16; ++s) {
                 // K-major: K blocks of 64 are separate R x 128 B regions; step 32 B inside a block.
                 // MN-major: K rows are 128-byte rows; step 16 rows = 2048 B; LBO = next 64-wide MN block.
@@ -846,35 +860,35 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const v
                             const void* w, const float* s0, float* sT, void* o, const ChunkShape& sh, float scale,
                             void* ws, cudaStream_t s, long long wait_ns) {
     const int NC = sh.nchunks();
-    FactorMaps fm;
-    if (!token_map(&fm.q, q, sh.B, sh.T, sh.Hk) || !token_map(&fm.k, k, sh.B, sh.T, sh.Hk) ||
-        !token_map(&fm.g, g, sh.B, sh.T, sh.Hv) || !token_map(&fm.b, b, sh.B, sh.T, sh.Hv) ||
-        !token_map(&fm.v, v, sh.B, sh.T, sh.Hv) || !token_map(&fm.w, w, sh.B, sh.T, sh.Hv))
-        return cudaErrorInvalidValue;
     const int units = NC * sh.B * sh.Hv;
     uint8_t* wsb = static_cast<uint8_t*>(ws);
     const auto BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-    const auto F32 = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
     const auto SW = CU_TENSOR_MAP_SWIZZLE_128B;
-    if (!ws_map(&fm.m_st, wsb + kWsM, BF, 2, 64, 64, units, 64, 64, SW) ||
-        !ws_map(&fm.utt_st, wsb + kWsUtT, F32, 4, 64, 128, units, 32, 128, SW))
+    FactorMaps fm;
+    if (!token_map(&fm.q, q, sh.B, sh.T, sh.Hk) || !token_map(&fm.k, k, sh.B, sh.T, sh.Hk) ||
+        !token_map(&fm.g, g, sh.B, sh.T, sh.Hv) || !token_map(&fm.b, b, sh.B, sh.T, sh.Hv) ||
+        !ws_map(&fm.m_st, wsb + kWsM, BF, 2, 64, 64, units, 64, 64, SW) ||
+        !ws_map(&fm.t_st, wsb + kWsT, BF, 2, 64, 64, units, 64, 64, SW) ||
+        !ws_map(&fm.w_st, wsb + kWsW, BF, 2, 128, 64, units, 64, 64, SW))
         return cudaErrorInvalidValue;
     StateMaps sm_;
     if (!ws_map(&sm_.w, wsb + kWsW, BF, 2, 128, 64, units, 64, 64, SW) ||
         !ws_map(&sm_.qb, wsb + kWsQb, BF, 2, 128, 64, units, 64, 64, SW) ||
         !ws_map(&sm_.kh, wsb + kWsKh, BF, 2, 128, 64, units, 64, 64, SW) ||
         !ws_map(&sm_.m, wsb + kWsM, BF, 2, 64, 64, units, 64, 64, SW) ||
-        !ws_map(&sm_.utt, wsb + kWsUtT, F32, 4, 64, 128, units, 64, kSlice, CU_TENSOR_MAP_SWIZZLE_NONE))
+        !ws_map(&sm_.t, wsb + kWsT, BF, 2, 64, 64, units, 64, 64, SW) ||
+        !token_map(&sm_.v, v, sh.B, sh.T, sh.Hv) || !token_map(&sm_.wg, w, sh.B, sh.T, sh.Hv))
         return cudaErrorInvalidValue;
 
+    // The state kernel runs one CTA per SM, so it takes the whole 227 KB: operand descriptors can
+    // then never reach past the CTA's own allocation.
     const size_t f_smem = fs::TOTAL + 1024, s_smem = 232448;
     static_assert(ss::TOTAL + 1024 <= 232448, "state kernel shared memory");
     cudaError_t e = cudaFuncSetAttribute(factors_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)f_smem);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(state_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s_smem);
     if (e != cudaSuccess) return e;
-    factors_tc_kernel<<<dim3(NC, sh.B * sh.Hv), fs::kThreads, f_smem, s>>>(fm, static_cast<uint8_t*>(ws), sh.Hk, sh.Hv, NC,
-                                                                  wait_ns);
+    factors_tc_kernel<<<dim3(NC, sh.B * sh.Hv), fs::kThreads, f_smem, s>>>(fm, wsb, sh.Hk, sh.Hv, NC, wait_ns);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     state_tc_kernel<<<dim3(sh.B * sh.Hv, kD / kSlice), ss::kThreads, s_smem, s>>>(
@@ -899,8 +913,9 @@ cudaError_t launch_selftest_umma(int case_id, int soft, const void* a_st, const 
     //                        case 1: A 64x128 (K x M),  B 64x64 (N x K)
     //                        case 2: A 128x128 (K x M), B 128x64 (K x N)
     //                        case 3: A 128x64 (M x K),  B 64x64 (K x N)
-    static const int shp[4][4] = {{128, 128, 64, 128}, {64, 128, 64, 64}, {128, 128, 128, 64}, {128, 64, 64, 64}};
-    if (case_id < 0 || case_id > 3) return cudaErrorInvalidValue;
+    static const int shp[5][4] = {{128, 128, 64, 128}, {64, 128, 64, 64}, {128, 128, 128, 64}, {128, 64, 64, 64},
+                                  {128, 128, 64, 128}};
+    if (case_id < 0 || case_id > 4) return cudaErrorInvalidValue;
     const int ar = shp[case_id][0], ac = shp[case_id][1], br = shp[case_id][2], bc = shp[case_id][3];
     SelftestMaps m;
     const uint64_t ad[3] = {(uint64_t)ac, (uint64_t)ar, 1}, as[2] = {(uint64_t)ac * 2, (uint64_t)ac * ar * 2};

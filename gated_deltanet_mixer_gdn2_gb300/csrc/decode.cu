@@ -121,7 +121,9 @@ __global__ void __launch_bounds__(256, 2)
 // 512-byte row per warp instruction); the d_k reductions finish across the 8 warps in shared memory.
 constexpr int kRing = 3;
 constexpr uint32_t kSlab = 128 * 128 * 4;
-constexpr uint32_t kRed = kRing * kSlab;           // [8 warps][2][128] partial r_b, r_q + [8] k.q
+constexpr uint32_t kTokOff = kRing * kSlab;         // per ring slot: q, k, g, b, v, w (128 each)
+constexpr uint32_t kTokSlot = 6 * 128 * 4;          // room for fp32 tokens
+constexpr uint32_t kRed = kTokOff + kRing * kTokSlot;  // [8 warps][2][128] partial r_b, r_q + [8] k.q
 constexpr uint32_t kStreamBar = kRed + 8 * 2 * 128 * 4 + 8 * 4;
 constexpr uint32_t kStreamSmem = kStreamBar + 64;
 
@@ -134,6 +136,25 @@ __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.comm
 template <int N>
 __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory"); }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// Queue the loads of head h into ring slot `slot`: its 64 KB state slab and its six token vectors.
+template <typename Tin>
+__device__ __forceinline__ void stream_issue(uint8_t* smem_s, uint64_t* bar, int slot, int h, const float* state,
+                                             const Tin* q, const Tin* k, const Tin* v, const Tin* g, const Tin* b,
+                                             const Tin* w, int Hk, int Hv) {
+    const int bi = h / Hv, hv = h - bi * Hv, hk = hv / (Hv / Hk);
+    constexpr uint32_t vb = 128 * sizeof(Tin);
+    mbar_arrive_expect_tx(bar, kSlab + 6 * vb);
+    bulk_load(smem_s + slot * kSlab, state + static_cast<size_t>(h) * 16384, kSlab, bar);
+    uint8_t* tk = smem_s + kTokOff + slot * kTokSlot;
+    const size_t kq = (static_cast<size_t>(bi) * Hk + hk) * 128, gv = (static_cast<size_t>(bi) * Hv + hv) * 128;
+    bulk_load(tk + 0 * vb, q + kq, vb, bar);
+    bulk_load(tk + 1 * vb, k + kq, vb, bar);
+    bulk_load(tk + 2 * vb, g + gv, vb, bar);
+    bulk_load(tk + 3 * vb, b + gv, vb, bar);
+    bulk_load(tk + 4 * vb, v + gv, vb, bar);
+    bulk_load(tk + 5 * vb, w + gv, vb, bar);
+}
 
 template <typename Tin>
 __global__ void __launch_bounds__(256, 1)
@@ -152,10 +173,8 @@ __global__ void __launch_bounds__(256, 1)
     if (tid == 0) {
         for (int i = 0; i < kRing; ++i) mbar_init(full + i, 1);
         fence_mbar_init();
-        for (int kk = 0; kk < 2 && kk < count; ++kk) {
-            mbar_arrive_expect_tx(full + kk, kSlab);
-            bulk_load(smem_s + kk * kSlab, state + static_cast<size_t>(first + kk * G) * 16384, kSlab, full + kk);
-        }
+        for (int kk = 0; kk < 2 && kk < count; ++kk)
+            stream_issue(smem_s, full + kk, kk, first + kk * G, state, q, k, v, g, b, w, Hk, Hv);
     }
     __syncthreads();
 
@@ -164,22 +183,7 @@ __global__ void __launch_bounds__(256, 1)
     for (; kk < count; ++kk) {
         const int h = first + kk * G;
         const int bsel = kk % kRing;
-        const int bi = h / Hv, hv = h - bi * Hv, hk = hv / (Hv / Hk);
-        // token vectors: lanes 0..15 hold row 16*warp + lane's q, k, alpha, b.k; every lane its 4 columns of w.v
-        float q_r = 0.f, k_r = 0.f, a_r = 0.f, bk_r = 0.f;
-        if (lane < 16) {
-            const int row = 16 * warp + lane;
-            const size_t kq_i = (static_cast<size_t>(bi) * Hk + hk) * 128 + row;
-            const size_t gb_i = (static_cast<size_t>(bi) * Hv + hv) * 128 + row;
-            q_r = to_f32(q[kq_i]);
-            k_r = to_f32(k[kq_i]);
-            a_r = expf(to_f32(g[gb_i]));
-            bk_r = to_f32(b[gb_i]) * k_r;
-        }
-        const size_t vw_i = (static_cast<size_t>(bi) * Hv + hv) * 128 + 4 * lane;
-        float wv[4];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) wv[c] = to_f32(w[vw_i + c]) * to_f32(v[vw_i + c]);
+        const int bi = h / Hv, hv = h - bi * Hv;
 
         if (tid == 0) {
             const bool got = mbar_wait(full + bsel, (kk / kRing) & 1, wait_ns);
@@ -195,6 +199,21 @@ __global__ void __launch_bounds__(256, 1)
             break;
         }
         mbar_wait(full + bsel, (kk / kRing) & 1, kDefaultWaitNs);
+
+        // token vectors from the ring: lanes 0..15 take row 16*warp + lane's q, k, alpha, b.k;
+        // every lane its 4 columns of w.v
+        const Tin* tk = reinterpret_cast<const Tin*>(smem_s + kTokOff + bsel * kTokSlot);
+        float q_r = 0.f, k_r = 0.f, a_r = 0.f, bk_r = 0.f;
+        if (lane < 16) {
+            const int row = 16 * warp + lane;
+            q_r = to_f32(tk[row]);
+            k_r = to_f32(tk[128 + row]);
+            a_r = expf(to_f32(tk[256 + row]));
+            bk_r = to_f32(tk[384 + row]) * k_r;
+        }
+        float wv[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) wv[c] = to_f32(tk[640 + 4 * lane + c]) * to_f32(tk[512 + 4 * lane + c]);
 
         float* S = reinterpret_cast<float*>(smem_s + bsel * kSlab);
         float4 s[16];
@@ -251,9 +270,7 @@ __global__ void __launch_bounds__(256, 1)
             if (kk + 2 < count) {
                 bulk_wait_read<1>();  // the store of head kk-1 has finished reading its buffer
                 const int nb = (kk + 2) % kRing;
-                mbar_arrive_expect_tx(full + nb, kSlab);
-                bulk_load(smem_s + nb * kSlab, state + static_cast<size_t>(first + (kk + 2) * G) * 16384, kSlab,
-                          full + nb);
+                stream_issue(smem_s, full + nb, nb, first + (kk + 2) * G, state, q, k, v, g, b, w, Hk, Hv);
             }
         }
     }

@@ -180,6 +180,9 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool 
            (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// Instruction-descriptor bit that negates the A operand (D += -A * B).
+constexpr uint32_t kNegateA = 1u << 13;
+
 // Byte offset of element (row, col) of a tile whose rows are 64 bf16 (128 bytes) wide, stored with
 // the 128-byte swizzle that TMA applies: the 16-byte chunk index is XORed with (row mod 8); the
 // tile base must be 1024-byte aligned.

@@ -115,7 +115,7 @@ gdn2_status gdn2_chunk_fwd_path(gdn2_path path, const void* q, const void* k, co
  * the process exits. It allocates nothing.
  *   - Limit: problems whose workspace (gdn2_chunk_fwd_workspace_size) exceeds 33 554 432 bytes
  *     are rejected with GDN2_ERR_WORKSPACE before any work is enqueued (on the tensor-core path,
- *     one 91 136-byte unit per chunk and value head: at most 368 of them).
+ *     one 66 048-byte unit per chunk and value head: at most 508 of them).
  *   - Set-up: the first call on a device looks up the array's device address (with that device
  *     current) and caches it; make that first call before any stream capture.
  *   - Sharing: all calls share the array and it keeps the last call's contents (nothing in it needs
@@ -167,6 +167,7 @@ void gdn2_set_wait_limit(long long ns);
  *   case 1: A [64 (K)][128 (M)],   B [64 (N)][64 (K)]    (A MN-major, B K-major)
  *   case 2: A [128 (K)][128 (M)],  B [128 (K)][64 (N)]   (both MN-major)
  *   case 3: A [128 (M)][64 (K)],   B [64 (K)][64 (N)]    (A K-major, B MN-major)
+ *   case 4: as case 0 with A negated through the instruction descriptor (D = -A * B)
  * soft = 0 stages them with TMA (128-byte swizzle), soft = 1 with ordinary stores using the same
  * swizzle. d_out: [128][64] fp32 device array. Asynchronous on `stream`.
  */

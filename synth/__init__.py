@@ -188,8 +188,12 @@ def _threads() -> int:
     return max(1, min(16, os.cpu_count() or 1))
 
 
-def make_inputs(wl: Workload, T: int | None = None, dtype: str | None = None) -> Inputs:
-    """All token tensors of workload `wl` for T tokens (default: chunk tokens + decode steps)."""
+def make_inputs(wl: Workload, T: int | None = None, dtype: str | None = None, b0: int = 0) -> Inputs:
+    """All token tensors of workload `wl` for T tokens (default: chunk tokens + decode steps).
+
+    b0 offsets the batch indices used for seeding, so that batch element i of the result is batch
+    element b0 + i of a larger batch (how ranks of a multi-GPU run get disjoint sequences).
+    """
     T = wl.tokens_total if T is None else T
     dtype = wl.dtype if dtype is None else dtype
     B, Hk, Hv, dk, dv = wl.B, wl.Hk, wl.Hv, wl.dk, wl.dv
@@ -208,7 +212,7 @@ def make_inputs(wl: Workload, T: int | None = None, dtype: str | None = None) ->
 
     def run(job):
         name, arr, bi, h, d = job
-        arr[bi, :, h, :] = slab(wl.seed, name, bi, h, T, d, dtype, wl.neg_eigval)
+        arr[bi, :, h, :] = slab(wl.seed, name, b0 + bi, h, T, d, dtype, wl.neg_eigval)
 
     with ThreadPoolExecutor(_threads()) as ex:
         list(ex.map(run, jobs))
@@ -217,8 +221,8 @@ def make_inputs(wl: Workload, T: int | None = None, dtype: str | None = None) ->
         s0 = np.empty((B, Hv, dk, dv), np.float32)
         for bi in range(B):
             for h in range(Hv):
-                s0[bi, h] = state_slab(wl.seed, bi, h, dk, dv, wl.s0_std)
-    return Inputs(dtype, s0=s0, meta={"workload": wl.name, "T": T}, **out)
+                s0[bi, h] = state_slab(wl.seed, b0 + bi, h, dk, dv, wl.s0_std)
+    return Inputs(dtype, s0=s0, meta={"workload": wl.name, "T": T, "b0": b0}, **out)
 
 
 def make_head_inputs(wl: Workload, bi: int, hv: int, T: int | None = None) -> Inputs:

@@ -46,10 +46,10 @@ def test_status_strings(g):
 
 
 def test_workspace_sizes(g):
-    # tensor-core path: one 91136-byte unit per (chunk, batch, value head)
-    assert g.gdn2_chunk_fwd_workspace_size(2, 32768, 16, 32, 128, 128, 64, g.GDN2_BF16) == 91136 * 512 * 64
+    # tensor-core path: one 66048-byte unit per (chunk, batch, value head)
+    assert g.gdn2_chunk_fwd_workspace_size(2, 32768, 16, 32, 128, 128, 64, g.GDN2_BF16) == 66048 * 512 * 64
     # ragged tail rounds the chunk count up
-    assert g.gdn2_chunk_fwd_workspace_size(1, 65, 1, 1, 128, 128, 64, g.GDN2_BF16) == 91136 * 2
+    assert g.gdn2_chunk_fwd_workspace_size(1, 65, 1, 1, 128, 128, 64, g.GDN2_BF16) == 66048 * 2
     # fp32 goes to the SIMT path: (3 dk C + C^2 + dv C + dk) floats, rounded to 4
     n = 3 * 64 * 64 + 64 * 64 + 64 * 64 + 64
     assert g.gdn2_chunk_fwd_workspace_size(1, 256, 4, 4, 64, 64, 64, g.GDN2_F32) == 4 * n * 4 * 4

@@ -12,6 +12,7 @@ CASES = {
     1: dict(M=128, N=64, K=64, a_mn=True, b_mn=False),
     2: dict(M=128, N=64, K=128, a_mn=True, b_mn=True),
     3: dict(M=128, N=64, K=64, a_mn=False, b_mn=True),
+    4: dict(M=128, N=64, K=128, a_mn=False, b_mn=False, neg=True),
 }
 
 
@@ -35,6 +36,6 @@ def test_umma_layout(case, soft):
     g.gdn2_selftest_umma(case, soft, at, bt, d)
     torch.cuda.synchronize()
     assert g.gdn2_last_device_status() == g.GDN2_OK
-    ref = A @ B
+    ref = -(A @ B) if c.get("neg") else A @ B
     got = d.cpu().numpy()
     assert np.array_equal(got, ref), f"case {case} soft {soft}: max err {np.nanmax(np.abs(got - ref))}"
