@@ -33,6 +33,23 @@ DECODE_WORKLOAD = "decode_b64"
 FLUSH_BYTES = 256 << 20  # > 129 MB L2
 
 
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one gdn2_chunk_fwd on this
+# workload, from a single-pass ncu capture of factors_tc + state_tc (profiles/traffic_prefill32k.md).
+# Reported only while the tensor-core kernel source is the one that was measured.
+TRAFFIC_RECORD = {"chunk_tc_sha256_16": "80cbe589cc9d18b5", "bytes": 1677608960 + 2112474112 + 3238073600 + 524748800}
+
+
+def recorded_traffic():
+    import hashlib
+
+    path = os.path.join(ROOT, "gated_deltanet_mixer_gdn2_gb300", "csrc", "chunk_tc.cu")
+    try:
+        sha = hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
+    except OSError:
+        return None
+    return TRAFFIC_RECORD["bytes"] if sha == TRAFFIC_RECORD["chunk_tc_sha256_16"] else None
+
+
 def peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -243,7 +260,7 @@ def run_ours(args, rank, world, device):
                    "parallelism": f"replicas{world}" if world > 1 else "single GPU"},
         "roofline": {"kernel": "gdn2_chunk_fwd (factors_tc + state_tc)", "bound": "hbm",
                      "achieved": round(ach_gbs, 1), "peak": hbm, "unit": "GB/s",
-                     "frac": round(ach_gbs / hbm, 4), "traffic": None,
+                     "frac": round(ach_gbs / hbm, 4), "traffic": recorded_traffic(),
                      "algorithmic_bytes": cb, "ms": round(ch_ms, 4), "peak_kind": f"{peak_kind} hbm_gbs",
                      "tflops": round(ach_tf, 1), "tc_frac": round(ach_tf / tc_burst, 4),
                      "tc_peak": tc_burst, "flops": flops},
