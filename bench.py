@@ -325,6 +325,67 @@ def decode_roofline(g, device, hbm):
             "l2": "state 201 MB > L2; 256 back-to-back steps"}
 
 
+def run_variants(device):
+    """Serving decode variants (gdn2_recurrent_update) on the 64-sequence, 48-value-head decode shape:
+    one JSON line each, with the kernel's algorithmic bytes per call against measured HBM bandwidth."""
+    import torch
+
+    import gated_deltanet_mixer_gdn2_gb300 as g
+
+    hbm, _, _, peak_kind = peaks()
+    wl = synth.WORKLOADS[DECODE_WORKLOAD]
+    B, Hk, Hv, dk, dv = wl.B, wl.Hk, wl.Hv, wl.dk, wl.dv
+    gen = torch.Generator(device=device)
+    gen.manual_seed(7)
+
+    def tokens(N):
+        out = []
+        for name, H, d in (("q", Hk, dk), ("k", Hk, dk), ("v", Hv, dv), ("g", Hv, dk), ("b", Hv, dk), ("w", Hv, dv)):
+            x = torch.randn((B, N, H, d), generator=gen, device=device)
+            if name in ("q", "k"):
+                x = x / x.norm(dim=-1, keepdim=True)
+            elif name == "g":
+                x = -torch.nn.functional.softplus(x)
+            elif name in ("b", "w"):
+                x = torch.sigmoid(x)
+            out.append(x.to(torch.bfloat16))
+        return out
+
+    cases = [
+        ("fp32 state, 1 token per call", 1, torch.float32, False),
+        ("fp32 state, 4 tokens per call", 4, torch.float32, False),
+        ("bf16 state, 1 token per call", 1, torch.bfloat16, False),
+        ("fp32 state pool, permuted slot map, 1 token per call", 1, torch.float32, True),
+    ]
+    stream = torch.cuda.current_stream(device)
+    for name, N, sdt, use_slots in cases:
+        n_slots = B + 8 if use_slots else B
+        st = (torch.randn((n_slots, Hv, dk, dv), generator=gen, device=device) * 0.02).to(sdt)
+        slots = torch.randperm(n_slots, generator=gen, device=device)[:B].to(torch.int32) if use_slots else None
+        tk = tokens(N)
+        o = torch.empty((B, N, Hv, dv), dtype=torch.bfloat16, device=device)
+        for _ in range(3):
+            g.gdn2_recurrent_update(*tk, st, o, slots)
+        torch.cuda.synchronize(device)
+        reps = 100
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            g.gdn2_recurrent_update(*tk, st, o, slots)
+        e1.record(stream)
+        torch.cuda.synchronize(device)
+        us = e0.elapsed_time(e1) * 1e3 / reps
+        sbytes = 2 * B * Hv * dk * dv * st.element_size()
+        tbytes = N * (B * (2 * Hk * dk + Hv * (2 * dk + 2 * dv)) * 2 + B * Hv * dv * 2)
+        b = sbytes + tbytes + (B * 4 if use_slots else 0)
+        gbs = b / (us * 1e-6) / 1e9
+        print(json.dumps({"variant": name, "workload": f"{DECODE_WORKLOAD} shape: B={B} H_k={Hk} H_v={Hv} d={dk}",
+                          "us_per_call": round(us, 2), "tokens_per_s": round(B * N / (us * 1e-6), 1),
+                          "bytes_per_call": b, "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
+                          "frac": round(gbs / hbm, 4), "peak_kind": f"{peak_kind} hbm_gbs",
+                          "l2": "state >= 100 MB > L2; 100 back-to-back calls"}), flush=True)
+
+
 def end_to_end(g, wl, host, device, args, tokens):
     """Same step through the public API with host (pinned) buffers: inputs copied in, o copied out."""
     import torch
@@ -449,6 +510,7 @@ def run_profile(spec: str):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--profile", default=None, help="op:workload, e.g. chunk:long_negeig_bf16 (for ncu)")
+    ap.add_argument("--variants", action="store_true", help="measure the serving decode variants instead")
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
@@ -466,6 +528,11 @@ def main():
 
     if args.profile:
         run_profile(args.profile)
+        return
+    if args.variants:
+        import torch
+
+        run_variants(torch.device("cuda", 0))
         return
     if args.impl == "reference":
         if rank == 0:

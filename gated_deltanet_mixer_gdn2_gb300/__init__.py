@@ -24,7 +24,7 @@ EXPORTS = (
     "gdn2_status_string", "gdn2_version", "gdn2_chunk_fwd_workspace_size",
     "gdn2_chunk_fwd_workspace_size_path", "gdn2_chunk_fwd", "gdn2_chunk_fwd_path",
     "gdn2_recurrent_step", "gdn2_last_device_status", "gdn2_set_wait_limit", "gdn2_selftest_umma",
-    "gdn2_chunk_fwd_noalloc",
+    "gdn2_chunk_fwd_noalloc", "gdn2_recurrent_update",
 )
 
 
@@ -53,6 +53,7 @@ def _load() -> ctypes.CDLL:
         "gdn2_set_wait_limit": (None, [L]),
         "gdn2_selftest_umma": (I, [I, I, P, P, P, P]),
         "gdn2_chunk_fwd_noalloc": (I, [P] * 9 + [I] * 7 + [F, I, P]),
+        "gdn2_recurrent_update": (I, [P] * 7 + [I, P, I, P] + [I] * 6 + [F, I, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -162,6 +163,27 @@ def gdn2_recurrent_step(q, k, v, g, b, w, state, o, *, scale=1.0, stream=None):
     st = lib.gdn2_recurrent_step(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(b), _ptr(w), _ptr(state),
                                  _ptr(o), B, Hk, Hv, dk, dv, float(scale), dt, _stream(stream))
     _check(st, "gdn2_recurrent_step")
+    return o
+
+
+def gdn2_recurrent_update(q, k, v, g, b, w, state, o, slots=None, *, scale=1.0, stream=None):
+    """N tokens per call (C ABI gdn2_recurrent_update); updates `state` in place and writes `o`.
+
+    q, k: [B, N, H_k, d_k]; v, w, o: [B, N, H_v, d_v]; g, b: [B, N, H_v, d_k]. state: float32 or
+    bfloat16, [B, H_v, d_k, d_v], or a pool [n_slots, H_v, d_k, d_v] when `slots` (int32 [B]) is given.
+    """
+    import torch
+
+    B, N, Hk, dk = q.shape
+    Hv, dv = v.shape[2], v.shape[3]
+    sdt = _dtype_code(state)
+    n_slots = state.shape[0] if slots is not None else 0
+    if slots is not None and slots.dtype != torch.int32:
+        raise TypeError("slots must be int32")
+    st = lib.gdn2_recurrent_update(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(b), _ptr(w), _ptr(state), sdt,
+                                   _ptr(slots), n_slots, _ptr(o), B, N, Hk, Hv, dk, dv, float(scale),
+                                   _dtype_code(q), _stream(stream))
+    _check(st, "gdn2_recurrent_update")
     return o
 
 

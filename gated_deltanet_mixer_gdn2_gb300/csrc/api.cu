@@ -144,21 +144,30 @@ gdn2_status gdn2_chunk_fwd(const void* q, const void* k, const void* v, const vo
                                dv, C, scale, dt, workspace, ws_bytes, stream);
 }
 
+gdn2_status gdn2_recurrent_update(const void* q, const void* k, const void* v, const void* g, const void* b,
+                                  const void* w, void* state, gdn2_dtype state_dt, const int32_t* slots, int n_slots,
+                                  void* o, int B, int N, int Hk, int Hv, int dk, int dv, float scale, gdn2_dtype dt,
+                                  void* stream) {
+    if (!dtype_ok(dt) || !dtype_ok(state_dt)) return GDN2_ERR_INVALID_ARG;
+    if (B < 0 || N < 0 || Hk <= 0 || Hv <= 0 || dk <= 0 || dv <= 0 || Hv % Hk) return GDN2_ERR_INVALID_ARG;
+    if (slots && n_slots < 0) return GDN2_ERR_INVALID_ARG;
+    if (!(dk == 16 || dk == 32 || dk == 64 || dk == 128) || dv % 16 != 0 || dv > 512) return GDN2_ERR_UNSUPPORTED;
+    if (!sizes_ok(B, N, Hk, Hv, dk, dv)) return GDN2_ERR_UNSUPPORTED;
+    if (B == 0 || N == 0) return GDN2_OK;
+    if (!q || !k || !v || !g || !b || !w || !state || !o) return GDN2_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(g) || !aligned16(b) || !aligned16(w) ||
+        !aligned16(state) || !aligned16(o) || (reinterpret_cast<uintptr_t>(slots) & 3u))
+        return GDN2_ERR_MISALIGNED;
+    const cudaError_t e = launch_recurrent(q, k, v, g, b, w, state, state_dt, slots, n_slots, o, B, N, Hk, Hv, dk,
+                                           dv, scale, dt, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? GDN2_OK : GDN2_ERR_CUDA;
+}
+
 gdn2_status gdn2_recurrent_step(const void* q, const void* k, const void* v, const void* g, const void* b,
                                 const void* w, float* state, void* o, int B, int Hk, int Hv, int dk, int dv,
                                 float scale, gdn2_dtype dt, void* stream) {
-    if (!dtype_ok(dt)) return GDN2_ERR_INVALID_ARG;
-    if (B < 0 || Hk <= 0 || Hv <= 0 || dk <= 0 || dv <= 0 || Hv % Hk) return GDN2_ERR_INVALID_ARG;
-    if (!(dk == 16 || dk == 32 || dk == 64 || dk == 128) || dv % 16 != 0 || dv > 512) return GDN2_ERR_UNSUPPORTED;
-    if (!sizes_ok(B, 1, Hk, Hv, dk, dv)) return GDN2_ERR_UNSUPPORTED;
-    if (B == 0) return GDN2_OK;
-    if (!q || !k || !v || !g || !b || !w || !state || !o) return GDN2_ERR_INVALID_ARG;
-    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(g) || !aligned16(b) || !aligned16(w) ||
-        !aligned16(state) || !aligned16(o))
-        return GDN2_ERR_MISALIGNED;
-    const cudaError_t e = launch_recurrent_step(q, k, v, g, b, w, state, o, B, Hk, Hv, dk, dv, scale, dt,
-                                                static_cast<cudaStream_t>(stream));
-    return e == cudaSuccess ? GDN2_OK : GDN2_ERR_CUDA;
+    return gdn2_recurrent_update(q, k, v, g, b, w, state, GDN2_F32, nullptr, 0, o, B, 1, Hk, Hv, dk, dv, scale, dt,
+                                 stream);
 }
 
 gdn2_status gdn2_last_device_status(void* stream) {

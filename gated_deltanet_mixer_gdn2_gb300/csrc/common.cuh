@@ -48,9 +48,10 @@ int chunk_tc_read_clear_status(cudaStream_t s);
 long long wait_limit_ns();
 
 // Launchers (host side). Return cudaSuccess or the launch error.
-cudaError_t launch_recurrent_step(const void* q, const void* k, const void* v, const void* g, const void* b,
-                                  const void* w, float* state, void* o, int B, int Hk, int Hv, int dk, int dv,
-                                  float scale, gdn2_dtype dt, cudaStream_t s);
+cudaError_t launch_recurrent(const void* q, const void* k, const void* v, const void* g, const void* b,
+                             const void* w, void* state, gdn2_dtype state_dt, const int* slots, int n_slots, void* o,
+                             int B, int N, int Hk, int Hv, int dk, int dv, float scale, gdn2_dtype dt,
+                             cudaStream_t s);
 
 size_t chunk_simt_workspace_bytes(const ChunkShape& sh);
 cudaError_t launch_chunk_simt(const void* q, const void* k, const void* v, const void* g, const void* b,

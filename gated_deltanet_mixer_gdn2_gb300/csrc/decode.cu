@@ -1,16 +1,24 @@
-// decode.cu -- gdn2_recurrent_step: one token against a persistent fp32 state, in place.
+// decode.cu -- the recurrent (token-by-token) mode against a persistent state, updated in place:
+// gdn2_recurrent_step (one token, fp32 state) and gdn2_recurrent_update (N tokens per call, an
+// optional slot map into a pool of states, fp32 or bf16 state storage).
 //
 // Recurrence (burn-gdn2 0.1.5 docs, "Architecture"), regrouped so that the state is read once and
-// written once (the same decay -> erase-read -> delta -> rank-1 update -> readout order as the
-// autoregressive GDN decode described in the llama.cpp GDN decode study):
+// written once per call (the same decay -> erase-read -> delta -> rank-1 update -> readout order as
+// the autoregressive GDN decode described in the llama.cpp GDN decode study):
 //     S' = diag(alpha) S,  r_b = S'^T (b . k),  r_q = S'^T q,  d = w . v - r_b,
 //     S  <- S' + k d^T,    o = scale * (r_q + (k . q) d)          [ = scale * S_new^T q ]
+// With N tokens per call the state stays on chip between tokens; arithmetic is fp32 throughout, a
+// bf16 state is widened on load and rounded (nearest even) once on store.
 //
-// Layout: state [B, H_v, d_k, d_v] fp32 (d_v innermost). The d_v columns evolve independently, so
-// a warp owns 16 columns of one head across all d_k rows: lane = 8 row groups x 4 column groups,
-// each lane holds d_k/8 rows x 4 columns (one 128-bit load / store per row). Reductions over d_k
-// are in-thread over the lane's rows, then warp shuffles across the 8 row groups. No shared
-// memory, no block barrier; every state byte moves HBM -> registers -> HBM exactly once.
+// Layout: state [rows, H_v, d_k, d_v] (d_v innermost), rows = batch or pool slots. The d_v columns
+// evolve independently.
+//   Register kernel: a warp owns 16 columns of one head across all d_k rows: lane = 8 row groups x
+//   4 column groups, each lane holds d_k/8 rows x 4 columns. Reductions over d_k are in-thread, then
+//   warp shuffles across the 8 row groups. No shared memory, no block barrier.
+//   Streaming kernel (d_k = d_v = 128, one token, many heads): a persistent grid walks the heads;
+//   each state slab is bulk-copied into a 3-deep shared-memory ring with its token vectors, updated
+//   in place and bulk-copied back, so that loads of the next two heads and the store of the
+//   previous one are in flight while a head is computed.
 #include "common.cuh"
 #include "ptx.cuh"
 
@@ -20,11 +28,39 @@ namespace {
 
 __device__ int g_status_decode;
 
-template <int DK, typename Tin>
+// ---- state element access: 4 consecutive columns ------------------------------------------------
+
+__device__ __forceinline__ float4 load4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+__device__ __forceinline__ float4 load4(const __nv_bfloat16* p) {
+    const uint2 u = *reinterpret_cast<const uint2*>(p);
+    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+    const float2 c = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+    return make_float4(a.x, a.y, c.x, c.y);
+}
+__device__ __forceinline__ void store4(float* p, float4 x) { *reinterpret_cast<float4*>(p) = x; }
+__device__ __forceinline__ void store4(__nv_bfloat16* p, float4 x) {
+    const __nv_bfloat162 a = __floats2bfloat162_rn(x.x, x.y), c = __floats2bfloat162_rn(x.z, x.w);
+    uint2 u;
+    u.x = *reinterpret_cast<const uint32_t*>(&a);
+    u.y = *reinterpret_cast<const uint32_t*>(&c);
+    *reinterpret_cast<uint2*>(p) = u;
+}
+
+// state row of batch element bi: the slot map (when given) or bi itself; -1 = inactive
+__device__ __forceinline__ int state_row(const int* slots, int n_slots, int bi) {
+    if (!slots) return bi;
+    const int s = slots[bi];
+    return (s >= 0 && s < n_slots) ? s : -1;
+}
+
+// ---- register kernel ----------------------------------------------------------------------------
+
+template <int DK, typename Tin, typename TS>
 __global__ void __launch_bounds__(256, 2)
-    recurrent_step_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* __restrict__ v,
-                          const Tin* __restrict__ g, const Tin* __restrict__ b, const Tin* __restrict__ w,
-                          float* __restrict__ state, Tin* __restrict__ o, int Hk, int Hv, int dv, float scale) {
+    recurrent_reg_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* __restrict__ v,
+                         const Tin* __restrict__ g, const Tin* __restrict__ b, const Tin* __restrict__ w,
+                         TS* __restrict__ state, const int* __restrict__ slots, int n_slots, Tin* __restrict__ o,
+                         int N, int Hk, int Hv, int dv, float scale) {
     constexpr int RPL = DK / 8;  // rows per lane
     const int head = blockIdx.x;
     const int bi = head / Hv;
@@ -36,94 +72,94 @@ __global__ void __launch_bounds__(256, 2)
     const int rg = lane >> 2;
     const int col = blockIdx.y * (blockDim.x >> 1) + warp * 16 + cg * 4;  // 16 columns per warp
     if (col >= dv) return;  // whole warp exits together (dv is a multiple of 16)
+    const int row = state_row(slots, n_slots, bi);
+    if (row < 0) return;    // inactive batch row: nothing read or written
 
-    float* S = state + static_cast<size_t>(head) * DK * dv + col;
+    TS* S = state + (static_cast<size_t>(row) * Hv + hv) * DK * dv + col;
     float4 s[RPL];
 #pragma unroll
-    for (int i = 0; i < RPL; ++i) s[i] = *reinterpret_cast<const float4*>(S + static_cast<size_t>(rg + 8 * i) * dv);
+    for (int i = 0; i < RPL; ++i) s[i] = load4(S + static_cast<size_t>(rg + 8 * i) * dv);
 
-    const Tin* qh = q + (static_cast<size_t>(bi) * Hk + hk) * DK;
-    const Tin* kh = k + (static_cast<size_t>(bi) * Hk + hk) * DK;
-    const Tin* gh = g + (static_cast<size_t>(bi) * Hv + hv) * DK;
-    const Tin* bh = b + (static_cast<size_t>(bi) * Hv + hv) * DK;
+    for (int t = 0; t < N; ++t) {
+        const size_t tk = static_cast<size_t>(bi) * N + t;
+        const Tin* qh = q + (tk * Hk + hk) * DK;
+        const Tin* kh = k + (tk * Hk + hk) * DK;
+        const Tin* gh = g + (tk * Hv + hv) * DK;
+        const Tin* bh = b + (tk * Hv + hv) * DK;
 
-    float4 rb = make_float4(0.f, 0.f, 0.f, 0.f);
-    float4 rq = make_float4(0.f, 0.f, 0.f, 0.f);
-    float kq = 0.f;
+        float4 rb = make_float4(0.f, 0.f, 0.f, 0.f);
+        float4 rq = make_float4(0.f, 0.f, 0.f, 0.f);
+        float kq = 0.f;
 #pragma unroll
-    for (int i = 0; i < RPL; ++i) {
-        const int r = rg + 8 * i;
-        const float a = expf(to_f32(gh[r]));
-        const float kk = to_f32(kh[r]);
-        const float qq = to_f32(qh[r]);
-        const float bk = to_f32(bh[r]) * kk;
-        s[i].x *= a;
-        s[i].y *= a;
-        s[i].z *= a;
-        s[i].w *= a;
-        rb.x = fmaf(s[i].x, bk, rb.x);
-        rb.y = fmaf(s[i].y, bk, rb.y);
-        rb.z = fmaf(s[i].z, bk, rb.z);
-        rb.w = fmaf(s[i].w, bk, rb.w);
-        rq.x = fmaf(s[i].x, qq, rq.x);
-        rq.y = fmaf(s[i].y, qq, rq.y);
-        rq.z = fmaf(s[i].z, qq, rq.z);
-        rq.w = fmaf(s[i].w, qq, rq.w);
-        kq = fmaf(kk, qq, kq);
-    }
-    // sum over the 8 row groups: lanes that differ in bits 2..4
+        for (int i = 0; i < RPL; ++i) {
+            const int r = rg + 8 * i;
+            const float a = expf(to_f32(gh[r]));
+            const float kk = to_f32(kh[r]);
+            const float qq = to_f32(qh[r]);
+            const float bk = to_f32(bh[r]) * kk;
+            s[i].x *= a;
+            s[i].y *= a;
+            s[i].z *= a;
+            s[i].w *= a;
+            rb.x = fmaf(s[i].x, bk, rb.x);
+            rb.y = fmaf(s[i].y, bk, rb.y);
+            rb.z = fmaf(s[i].z, bk, rb.z);
+            rb.w = fmaf(s[i].w, bk, rb.w);
+            rq.x = fmaf(s[i].x, qq, rq.x);
+            rq.y = fmaf(s[i].y, qq, rq.y);
+            rq.z = fmaf(s[i].z, qq, rq.z);
+            rq.w = fmaf(s[i].w, qq, rq.w);
+            kq = fmaf(kk, qq, kq);
+        }
+        // sum over the 8 row groups: lanes that differ in bits 2..4
 #pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-        rb.x += __shfl_xor_sync(0xffffffffu, rb.x, off);
-        rb.y += __shfl_xor_sync(0xffffffffu, rb.y, off);
-        rb.z += __shfl_xor_sync(0xffffffffu, rb.z, off);
-        rb.w += __shfl_xor_sync(0xffffffffu, rb.w, off);
-        rq.x += __shfl_xor_sync(0xffffffffu, rq.x, off);
-        rq.y += __shfl_xor_sync(0xffffffffu, rq.y, off);
-        rq.z += __shfl_xor_sync(0xffffffffu, rq.z, off);
-        rq.w += __shfl_xor_sync(0xffffffffu, rq.w, off);
-        kq += __shfl_xor_sync(0xffffffffu, kq, off);
-    }
+        for (int off = 4; off < 32; off <<= 1) {
+            rb.x += __shfl_xor_sync(0xffffffffu, rb.x, off);
+            rb.y += __shfl_xor_sync(0xffffffffu, rb.y, off);
+            rb.z += __shfl_xor_sync(0xffffffffu, rb.z, off);
+            rb.w += __shfl_xor_sync(0xffffffffu, rb.w, off);
+            rq.x += __shfl_xor_sync(0xffffffffu, rq.x, off);
+            rq.y += __shfl_xor_sync(0xffffffffu, rq.y, off);
+            rq.z += __shfl_xor_sync(0xffffffffu, rq.z, off);
+            rq.w += __shfl_xor_sync(0xffffffffu, rq.w, off);
+            kq += __shfl_xor_sync(0xffffffffu, kq, off);
+        }
 
-    const Tin* vh = v + (static_cast<size_t>(bi) * Hv + hv) * dv + col;
-    const Tin* wh = w + (static_cast<size_t>(bi) * Hv + hv) * dv + col;
-    float4 d;
-    d.x = to_f32(wh[0]) * to_f32(vh[0]) - rb.x;
-    d.y = to_f32(wh[1]) * to_f32(vh[1]) - rb.y;
-    d.z = to_f32(wh[2]) * to_f32(vh[2]) - rb.z;
-    d.w = to_f32(wh[3]) * to_f32(vh[3]) - rb.w;
+        const Tin* vh = v + (tk * Hv + hv) * dv + col;
+        const Tin* wh = w + (tk * Hv + hv) * dv + col;
+        float4 d;
+        d.x = to_f32(wh[0]) * to_f32(vh[0]) - rb.x;
+        d.y = to_f32(wh[1]) * to_f32(vh[1]) - rb.y;
+        d.z = to_f32(wh[2]) * to_f32(vh[2]) - rb.z;
+        d.w = to_f32(wh[3]) * to_f32(vh[3]) - rb.w;
 
-    if (rg == 0) {
-        Tin* oh = o + (static_cast<size_t>(bi) * Hv + hv) * dv + col;
-        oh[0] = from_f32<Tin>(scale * fmaf(kq, d.x, rq.x));
-        oh[1] = from_f32<Tin>(scale * fmaf(kq, d.y, rq.y));
-        oh[2] = from_f32<Tin>(scale * fmaf(kq, d.z, rq.z));
-        oh[3] = from_f32<Tin>(scale * fmaf(kq, d.w, rq.w));
+        if (rg == 0) {
+            Tin* oh = o + (tk * Hv + hv) * dv + col;
+            oh[0] = from_f32<Tin>(scale * fmaf(kq, d.x, rq.x));
+            oh[1] = from_f32<Tin>(scale * fmaf(kq, d.y, rq.y));
+            oh[2] = from_f32<Tin>(scale * fmaf(kq, d.z, rq.z));
+            oh[3] = from_f32<Tin>(scale * fmaf(kq, d.w, rq.w));
+        }
+#pragma unroll
+        for (int i = 0; i < RPL; ++i) {
+            const float kk = to_f32(kh[rg + 8 * i]);  // re-read (L1) rather than hold d_k/8 registers
+            s[i].x = fmaf(kk, d.x, s[i].x);
+            s[i].y = fmaf(kk, d.y, s[i].y);
+            s[i].z = fmaf(kk, d.z, s[i].z);
+            s[i].w = fmaf(kk, d.w, s[i].w);
+        }
     }
 #pragma unroll
-    for (int i = 0; i < RPL; ++i) {
-        const float kk = to_f32(kh[rg + 8 * i]);  // re-read (L1) rather than hold d_k/8 registers
-        float4 t = s[i];
-        t.x = fmaf(kk, d.x, t.x);
-        t.y = fmaf(kk, d.y, t.y);
-        t.z = fmaf(kk, d.z, t.z);
-        t.w = fmaf(kk, d.w, t.w);
-        *reinterpret_cast<float4*>(S + static_cast<size_t>(rg + 8 * i) * dv) = t;
-    }
+    for (int i = 0; i < RPL; ++i) store4(S + static_cast<size_t>(rg + 8 * i) * dv, s[i]);
 }
 
-// ---------------------------------------------------------------------------------------------
-// Streaming variant for d_k = d_v = 128 and many heads: a persistent grid (one CTA per SM) walks
-// the heads h = blockIdx.x, blockIdx.x + gridDim.x, ...; each 64 KB state slab (contiguous) is
-// bulk-copied into a 3-deep shared-memory ring (cp.async.bulk, mbarrier completion), updated in
-// place, and bulk-copied back. Loads for the next two heads and the store of the previous one are
-// in flight while a head is computed. Warp w owns rows 16w..16w+15, lane l columns 4l..4l+3 (one
-// 512-byte row per warp instruction); the d_k reductions finish across the 8 warps in shared memory.
+// ---- streaming kernel (d_k = d_v = 128, one token) ----------------------------------------------
+
 constexpr int kRing = 3;
-constexpr uint32_t kSlab = 128 * 128 * 4;
-constexpr uint32_t kTokOff = kRing * kSlab;         // per ring slot: q, k, g, b, v, w (128 each)
-constexpr uint32_t kTokSlot = 6 * 128 * 4;          // room for fp32 tokens
-constexpr uint32_t kRed = kTokOff + kRing * kTokSlot;  // [8 warps][2][128] partial r_b, r_q + [8] k.q
+constexpr uint32_t kSlabMax = 128 * 128 * 4;
+constexpr uint32_t kTokOff = kRing * kSlabMax;          // per ring slot: q, k, g, b, v, w (128 each)
+constexpr uint32_t kTokSlot = 6 * 128 * 4;              // room for fp32 tokens
+constexpr uint32_t kRed = kTokOff + kRing * kTokSlot;   // [8 warps][2][128] partial r_b, r_q + [8] k.q
 constexpr uint32_t kStreamBar = kRed + 8 * 2 * 128 * 4 + 8 * 4;
 constexpr uint32_t kStreamSmem = kStreamBar + 64;
 
@@ -136,16 +172,26 @@ __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.comm
 template <int N>
 __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory"); }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
 
-// Queue the loads of head h into ring slot `slot`: its 64 KB state slab and its six token vectors.
-template <typename Tin>
-__device__ __forceinline__ void stream_issue(uint8_t* smem_s, uint64_t* bar, int slot, int h, const float* state,
-                                             const Tin* q, const Tin* k, const Tin* v, const Tin* g, const Tin* b,
-                                             const Tin* w, int Hk, int Hv) {
+// Queue the loads of head h into ring slot `slot`: its state slab and its six token vectors. An
+// inactive head (slot map gives no row) completes the slot's barrier phase without loading.
+template <typename Tin, typename TS>
+__device__ __forceinline__ void stream_issue(uint8_t* smem_s, uint64_t* bar, int slot, int h, const TS* state,
+                                             const int* slots, int n_slots, const Tin* q, const Tin* k,
+                                             const Tin* v, const Tin* g, const Tin* b, const Tin* w, int Hk, int Hv) {
+    constexpr uint32_t kSlab = 128 * 128 * sizeof(TS);
     const int bi = h / Hv, hv = h - bi * Hv, hk = hv / (Hv / Hk);
+    const int row = state_row(slots, n_slots, bi);
+    if (row < 0) {
+        mbar_arrive(bar);
+        return;
+    }
     constexpr uint32_t vb = 128 * sizeof(Tin);
     mbar_arrive_expect_tx(bar, kSlab + 6 * vb);
-    bulk_load(smem_s + slot * kSlab, state + static_cast<size_t>(h) * 16384, kSlab, bar);
+    bulk_load(smem_s + slot * kSlabMax, state + (static_cast<size_t>(row) * Hv + hv) * 16384, kSlab, bar);
     uint8_t* tk = smem_s + kTokOff + slot * kTokSlot;
     const size_t kq = (static_cast<size_t>(bi) * Hk + hk) * 128, gv = (static_cast<size_t>(bi) * Hv + hv) * 128;
     bulk_load(tk + 0 * vb, q + kq, vb, bar);
@@ -156,12 +202,13 @@ __device__ __forceinline__ void stream_issue(uint8_t* smem_s, uint64_t* bar, int
     bulk_load(tk + 5 * vb, w + gv, vb, bar);
 }
 
-template <typename Tin>
+template <typename Tin, typename TS>
 __global__ void __launch_bounds__(256, 1)
-    recurrent_step_stream_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* __restrict__ v,
-                                 const Tin* __restrict__ g, const Tin* __restrict__ b, const Tin* __restrict__ w,
-                                 float* __restrict__ state, Tin* __restrict__ o, int nheads, int Hk, int Hv,
-                                 float scale, long long wait_ns) {
+    recurrent_stream_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* __restrict__ v,
+                            const Tin* __restrict__ g, const Tin* __restrict__ b, const Tin* __restrict__ w,
+                            TS* __restrict__ state, const int* __restrict__ slots, int n_slots,
+                            Tin* __restrict__ o, int nheads, int Hk, int Hv, float scale, long long wait_ns) {
+    constexpr uint32_t kSlab = 128 * 128 * sizeof(TS);
     extern __shared__ __align__(128) uint8_t smem_s[];
     float* red = reinterpret_cast<float*>(smem_s + kRed);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem_s + kStreamBar);
@@ -174,7 +221,7 @@ __global__ void __launch_bounds__(256, 1)
         for (int i = 0; i < kRing; ++i) mbar_init(full + i, 1);
         fence_mbar_init();
         for (int kk = 0; kk < 2 && kk < count; ++kk)
-            stream_issue(smem_s, full + kk, kk, first + kk * G, state, q, k, v, g, b, w, Hk, Hv);
+            stream_issue(smem_s, full + kk, kk, first + kk * G, state, slots, n_slots, q, k, v, g, b, w, Hk, Hv);
     }
     __syncthreads();
 
@@ -184,6 +231,7 @@ __global__ void __launch_bounds__(256, 1)
         const int h = first + kk * G;
         const int bsel = kk % kRing;
         const int bi = h / Hv, hv = h - bi * Hv;
+        const int row = state_row(slots, n_slots, bi);
 
         if (tid == 0) {
             const bool got = mbar_wait(full + bsel, (kk / kRing) & 1, wait_ns);
@@ -200,77 +248,81 @@ __global__ void __launch_bounds__(256, 1)
         }
         mbar_wait(full + bsel, (kk / kRing) & 1, kDefaultWaitNs);
 
-        // token vectors from the ring: lanes 0..15 take row 16*warp + lane's q, k, alpha, b.k;
-        // every lane its 4 columns of w.v
-        const Tin* tk = reinterpret_cast<const Tin*>(smem_s + kTokOff + bsel * kTokSlot);
-        float q_r = 0.f, k_r = 0.f, a_r = 0.f, bk_r = 0.f;
-        if (lane < 16) {
-            const int row = 16 * warp + lane;
-            q_r = to_f32(tk[row]);
-            k_r = to_f32(tk[128 + row]);
-            a_r = expf(to_f32(tk[256 + row]));
-            bk_r = to_f32(tk[384 + row]) * k_r;
-        }
-        float wv[4];
+        if (row >= 0) {
+            // token vectors from the ring: lanes 0..15 take row 16*warp + lane's q, k, alpha, b.k;
+            // every lane its 4 columns of w.v
+            const Tin* tk = reinterpret_cast<const Tin*>(smem_s + kTokOff + bsel * kTokSlot);
+            float q_r = 0.f, k_r = 0.f, a_r = 0.f, bk_r = 0.f;
+            if (lane < 16) {
+                const int rr = 16 * warp + lane;
+                q_r = to_f32(tk[rr]);
+                k_r = to_f32(tk[128 + rr]);
+                a_r = expf(to_f32(tk[256 + rr]));
+                bk_r = to_f32(tk[384 + rr]) * k_r;
+            }
+            float wv[4];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) wv[c] = to_f32(tk[640 + 4 * lane + c]) * to_f32(tk[512 + 4 * lane + c]);
+            for (int c = 0; c < 4; ++c) wv[c] = to_f32(tk[640 + 4 * lane + c]) * to_f32(tk[512 + 4 * lane + c]);
 
-        float* S = reinterpret_cast<float*>(smem_s + bsel * kSlab);
-        float4 s[16];
-        float4 rb = make_float4(0.f, 0.f, 0.f, 0.f), rq = make_float4(0.f, 0.f, 0.f, 0.f);
-        float kq = k_r * q_r;
+            TS* S = reinterpret_cast<TS*>(smem_s + bsel * kSlabMax);
+            float4 s[16];
+            float4 rb = make_float4(0.f, 0.f, 0.f, 0.f), rq = make_float4(0.f, 0.f, 0.f, 0.f);
+            float kq = k_r * q_r;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const float ai = __shfl_sync(0xffffffffu, a_r, i);
-            const float bki = __shfl_sync(0xffffffffu, bk_r, i);
-            const float qi = __shfl_sync(0xffffffffu, q_r, i);
-            float4 t = reinterpret_cast<const float4*>(S + (16 * warp + i) * 128)[lane];
-            t.x *= ai; t.y *= ai; t.z *= ai; t.w *= ai;
-            s[i] = t;
-            rb.x = fmaf(t.x, bki, rb.x); rb.y = fmaf(t.y, bki, rb.y); rb.z = fmaf(t.z, bki, rb.z); rb.w = fmaf(t.w, bki, rb.w);
-            rq.x = fmaf(t.x, qi, rq.x); rq.y = fmaf(t.y, qi, rq.y); rq.z = fmaf(t.z, qi, rq.z); rq.w = fmaf(t.w, qi, rq.w);
-        }
+            for (int i = 0; i < 16; ++i) {
+                const float ai = __shfl_sync(0xffffffffu, a_r, i);
+                const float bki = __shfl_sync(0xffffffffu, bk_r, i);
+                const float qi = __shfl_sync(0xffffffffu, q_r, i);
+                float4 t = load4(S + (16 * warp + i) * 128 + 4 * lane);
+                t.x *= ai; t.y *= ai; t.z *= ai; t.w *= ai;
+                s[i] = t;
+                rb.x = fmaf(t.x, bki, rb.x); rb.y = fmaf(t.y, bki, rb.y); rb.z = fmaf(t.z, bki, rb.z); rb.w = fmaf(t.w, bki, rb.w);
+                rq.x = fmaf(t.x, qi, rq.x); rq.y = fmaf(t.y, qi, rq.y); rq.z = fmaf(t.z, qi, rq.z); rq.w = fmaf(t.w, qi, rq.w);
+            }
 #pragma unroll
-        for (int off = 8; off > 0; off >>= 1) kq += __shfl_xor_sync(0xffffffffu, kq, off);  // lanes 0..15 hold rows
-        reinterpret_cast<float4*>(red + (warp * 2 + 0) * 128)[lane] = rb;
-        reinterpret_cast<float4*>(red + (warp * 2 + 1) * 128)[lane] = rq;
-        if (lane == 0) red[8 * 2 * 128 + warp] = kq;
-        __syncthreads();
-        rb = make_float4(0.f, 0.f, 0.f, 0.f);
-        rq = make_float4(0.f, 0.f, 0.f, 0.f);
-        kq = 0.f;
+            for (int off = 8; off > 0; off >>= 1) kq += __shfl_xor_sync(0xffffffffu, kq, off);  // lanes 0..15 hold rows
+            reinterpret_cast<float4*>(red + (warp * 2 + 0) * 128)[lane] = rb;
+            reinterpret_cast<float4*>(red + (warp * 2 + 1) * 128)[lane] = rq;
+            if (lane == 0) red[8 * 2 * 128 + warp] = kq;
+            __syncthreads();
+            rb = make_float4(0.f, 0.f, 0.f, 0.f);
+            rq = make_float4(0.f, 0.f, 0.f, 0.f);
+            kq = 0.f;
 #pragma unroll
-        for (int w8 = 0; w8 < 8; ++w8) {
-            const float4 x = reinterpret_cast<const float4*>(red + (w8 * 2 + 0) * 128)[lane];
-            const float4 y = reinterpret_cast<const float4*>(red + (w8 * 2 + 1) * 128)[lane];
-            rb.x += x.x; rb.y += x.y; rb.z += x.z; rb.w += x.w;
-            rq.x += y.x; rq.y += y.y; rq.z += y.z; rq.w += y.w;
-            kq += red[8 * 2 * 128 + w8];
-        }
-        const float d0 = wv[0] - rb.x, d1 = wv[1] - rb.y, d2 = wv[2] - rb.z, d3 = wv[3] - rb.w;
-        if (warp == 0) {
-            Tin* oh = o + (static_cast<size_t>(bi) * Hv + hv) * 128 + 4 * lane;
-            oh[0] = from_f32<Tin>(scale * fmaf(kq, d0, rq.x));
-            oh[1] = from_f32<Tin>(scale * fmaf(kq, d1, rq.y));
-            oh[2] = from_f32<Tin>(scale * fmaf(kq, d2, rq.z));
-            oh[3] = from_f32<Tin>(scale * fmaf(kq, d3, rq.w));
-        }
+            for (int w8 = 0; w8 < 8; ++w8) {
+                const float4 x = reinterpret_cast<const float4*>(red + (w8 * 2 + 0) * 128)[lane];
+                const float4 y = reinterpret_cast<const float4*>(red + (w8 * 2 + 1) * 128)[lane];
+                rb.x += x.x; rb.y += x.y; rb.z += x.z; rb.w += x.w;
+                rq.x += y.x; rq.y += y.y; rq.z += y.z; rq.w += y.w;
+                kq += red[8 * 2 * 128 + w8];
+            }
+            const float d0 = wv[0] - rb.x, d1 = wv[1] - rb.y, d2 = wv[2] - rb.z, d3 = wv[3] - rb.w;
+            if (warp == 0) {
+                Tin* oh = o + (static_cast<size_t>(bi) * Hv + hv) * 128 + 4 * lane;
+                oh[0] = from_f32<Tin>(scale * fmaf(kq, d0, rq.x));
+                oh[1] = from_f32<Tin>(scale * fmaf(kq, d1, rq.y));
+                oh[2] = from_f32<Tin>(scale * fmaf(kq, d2, rq.z));
+                oh[3] = from_f32<Tin>(scale * fmaf(kq, d3, rq.w));
+            }
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const float ki = __shfl_sync(0xffffffffu, k_r, i);
-            float4 t = s[i];
-            t.x = fmaf(ki, d0, t.x); t.y = fmaf(ki, d1, t.y); t.z = fmaf(ki, d2, t.z); t.w = fmaf(ki, d3, t.w);
-            reinterpret_cast<float4*>(S + (16 * warp + i) * 128)[lane] = t;
+            for (int i = 0; i < 16; ++i) {
+                const float ki = __shfl_sync(0xffffffffu, k_r, i);
+                float4 t = s[i];
+                t.x = fmaf(ki, d0, t.x); t.y = fmaf(ki, d1, t.y); t.z = fmaf(ki, d2, t.z); t.w = fmaf(ki, d3, t.w);
+                store4(S + (16 * warp + i) * 128 + 4 * lane, t);
+            }
+            fence_proxy_async_smem();
         }
-        fence_proxy_async_smem();
         __syncthreads();
         if (tid == 0) {
-            bulk_store(state + static_cast<size_t>(h) * 16384, S, kSlab);
-            bulk_commit();
+            if (row >= 0)
+                bulk_store(state + (static_cast<size_t>(row) * Hv + hv) * 16384, smem_s + bsel * kSlabMax, kSlab);
+            bulk_commit();  // an empty group for an inactive head keeps the group count in step
             if (kk + 2 < count) {
                 bulk_wait_read<1>();  // the store of head kk-1 has finished reading its buffer
                 const int nb = (kk + 2) % kRing;
-                stream_issue(smem_s, full + nb, nb, first + (kk + 2) * G, state, q, k, v, g, b, w, Hk, Hv);
+                stream_issue(smem_s, full + nb, nb, first + (kk + 2) * G, state, slots, n_slots, q, k, v, g, b, w,
+                             Hk, Hv);
             }
         }
     }
@@ -284,9 +336,10 @@ __global__ void __launch_bounds__(256, 1)
 
 int g_num_sms = 0;
 
-template <typename Tin>
+template <typename Tin, typename TS>
 cudaError_t launch_t(const void* q, const void* k, const void* v, const void* g, const void* b, const void* w,
-                     float* state, void* o, int B, int Hk, int Hv, int dk, int dv, float scale, cudaStream_t s) {
+                     void* state, const int* slots, int n_slots, void* o, int B, int N, int Hk, int Hv, int dk,
+                     int dv, float scale, cudaStream_t s) {
     if (g_num_sms == 0) {
         int dev = 0;
         if (cudaGetDevice(&dev) != cudaSuccess ||
@@ -294,13 +347,14 @@ cudaError_t launch_t(const void* q, const void* k, const void* v, const void* g,
             g_num_sms = 1;
     }
     const long long heads = static_cast<long long>(B) * Hv;
-    if (dk == 128 && dv == 128 && heads >= 4LL * g_num_sms) {
-        cudaError_t e = cudaFuncSetAttribute(recurrent_step_stream_kernel<Tin>,
+    TS* st = static_cast<TS*>(state);
+    if (N == 1 && dk == 128 && dv == 128 && heads >= 4LL * g_num_sms) {
+        cudaError_t e = cudaFuncSetAttribute(recurrent_stream_kernel<Tin, TS>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kStreamSmem);
         if (e != cudaSuccess) return e;
-        recurrent_step_stream_kernel<Tin><<<g_num_sms, 256, kStreamSmem, s>>>(
+        recurrent_stream_kernel<Tin, TS><<<g_num_sms, 256, kStreamSmem, s>>>(
             static_cast<const Tin*>(q), static_cast<const Tin*>(k), static_cast<const Tin*>(v),
-            static_cast<const Tin*>(g), static_cast<const Tin*>(b), static_cast<const Tin*>(w), state,
+            static_cast<const Tin*>(g), static_cast<const Tin*>(b), static_cast<const Tin*>(w), st, slots, n_slots,
             static_cast<Tin*>(o), static_cast<int>(heads), Hk, Hv, scale, wait_limit_ns());
         return cudaGetLastError();
     }
@@ -312,10 +366,10 @@ cudaError_t launch_t(const void* q, const void* k, const void* v, const void* g,
     const dim3 block(32 * (dv >= cols ? wpc : dv / 16));
 #define GDN2_DECODE_CASE(DKV)                                                                              \
     case DKV:                                                                                              \
-        recurrent_step_kernel<DKV, Tin><<<grid, block, 0, s>>>(                                            \
+        recurrent_reg_kernel<DKV, Tin, TS><<<grid, block, 0, s>>>(                                         \
             static_cast<const Tin*>(q), static_cast<const Tin*>(k), static_cast<const Tin*>(v),            \
-            static_cast<const Tin*>(g), static_cast<const Tin*>(b), static_cast<const Tin*>(w), state,     \
-            static_cast<Tin*>(o), Hk, Hv, dv, scale);                                                      \
+            static_cast<const Tin*>(g), static_cast<const Tin*>(b), static_cast<const Tin*>(w), st, slots, \
+            n_slots, static_cast<Tin*>(o), N, Hk, Hv, dv, scale);                                          \
         break;
     switch (dk) {
         GDN2_DECODE_CASE(16)
@@ -331,12 +385,21 @@ cudaError_t launch_t(const void* q, const void* k, const void* v, const void* g,
 
 }  // namespace
 
-cudaError_t launch_recurrent_step(const void* q, const void* k, const void* v, const void* g, const void* b,
-                                  const void* w, float* state, void* o, int B, int Hk, int Hv, int dk, int dv,
-                                  float scale, gdn2_dtype dt, cudaStream_t s) {
-    if (dt == GDN2_BF16)
-        return launch_t<__nv_bfloat16>(q, k, v, g, b, w, state, o, B, Hk, Hv, dk, dv, scale, s);
-    return launch_t<float>(q, k, v, g, b, w, state, o, B, Hk, Hv, dk, dv, scale, s);
+cudaError_t launch_recurrent(const void* q, const void* k, const void* v, const void* g, const void* b,
+                             const void* w, void* state, gdn2_dtype state_dt, const int* slots, int n_slots, void* o,
+                             int B, int N, int Hk, int Hv, int dk, int dv, float scale, gdn2_dtype dt,
+                             cudaStream_t s) {
+    if (dt == GDN2_BF16) {
+        if (state_dt == GDN2_BF16)
+            return launch_t<__nv_bfloat16, __nv_bfloat16>(q, k, v, g, b, w, state, slots, n_slots, o, B, N, Hk, Hv,
+                                                           dk, dv, scale, s);
+        return launch_t<__nv_bfloat16, float>(q, k, v, g, b, w, state, slots, n_slots, o, B, N, Hk, Hv, dk, dv,
+                                              scale, s);
+    }
+    if (state_dt == GDN2_BF16)
+        return launch_t<float, __nv_bfloat16>(q, k, v, g, b, w, state, slots, n_slots, o, B, N, Hk, Hv, dk, dv,
+                                              scale, s);
+    return launch_t<float, float>(q, k, v, g, b, w, state, slots, n_slots, o, B, N, Hk, Hv, dk, dv, scale, s);
 }
 
 int decode_read_clear_status(cudaStream_t s) {

@@ -144,6 +144,31 @@ gdn2_status gdn2_recurrent_step(const void* q, const void* k, const void* v, con
                                 void* stream);
 
 /*
+ * gdn2_recurrent_update -- the recurrent mode for serving: N tokens per call against persistent
+ * states, optionally addressed through a slot map into a pool, with fp32 or bf16 state storage.
+ * The same per-token recurrence as gdn2_recurrent_step, applied to tokens 0..N-1 in order; the
+ * state is read once and written once per call (it stays on chip between the call's tokens). This
+ * serves the serving-side items the llama.cpp GDN decode study names: a recurrent state cache
+ * whose entries are read and written every step, more than one token per step, and a bf16 state.
+ *
+ *   q, k    [B, N, H_k, d_k] dt;   v, w, o [B, N, H_v, d_v] dt;   g, b [B, N, H_v, d_k] dt
+ *   state   slots == NULL: [B, H_v, d_k, d_v] of state_dt, row b for batch element b;
+ *           slots != NULL: a pool [n_slots, H_v, d_k, d_v] of state_dt; batch element b uses pool
+ *           row slots[b] (int32 device array of B entries). A slot outside [0, n_slots) marks the
+ *           element inactive: its state, its o rows and every other pool row are left untouched.
+ *           Active elements must name distinct slots (two elements on one slot race).
+ *   state_dt  GDN2_F32, or GDN2_BF16: widened to fp32 on load, rounded to nearest even on store.
+ *
+ * Supported: d_k in {16, 32, 64, 128}; d_v a multiple of 16 up to 512. B == 0 or N == 0 is a no-op.
+ * gdn2_recurrent_step(...) equals gdn2_recurrent_update(..., GDN2_F32, NULL, 0, ..., N = 1, ...).
+ */
+gdn2_status gdn2_recurrent_update(const void* q, const void* k, const void* v, const void* g,
+                                  const void* b, const void* w, void* state, gdn2_dtype state_dt,
+                                  const int32_t* slots, int n_slots, void* o, int B, int N,
+                                  int Hk, int Hv, int dk, int dv, float scale, gdn2_dtype dt,
+                                  void* stream);
+
+/*
  * gdn2_last_device_status -- synchronises `stream`, then reads and clears the device status word
  * of the current device. Returns GDN2_OK, GDN2_ERR_TIMEOUT (a kernel gave up a bounded wait since
  * the last call) or GDN2_ERR_CUDA (the synchronisation itself failed).

@@ -117,3 +117,16 @@ def test_product_path_does_not_touch_the_oracle():
                 src = open(os.path.join(dirpath, f)).read()
                 assert "oracle" not in src.lower(), f"{f} mentions the oracle"
                 assert "import synth" not in src and "from synth" not in src
+
+
+def test_recurrent_update_argument_errors(g):
+    P = ctypes.c_void_p(0x10000)
+    f = lambda sdt=0, slots=None, n_slots=0, B=1, N=2, dk=128, dv=128, dt=1, p=P: g.lib.gdn2_recurrent_update(
+        p, p, p, p, p, p, p, sdt, slots, n_slots, p, B, N, 1, 1, dk, dv, 1.0, dt, None)
+    assert f(sdt=5) == g.GDN2_ERR_INVALID_ARG
+    assert f(N=-1) == g.GDN2_ERR_INVALID_ARG
+    assert f(slots=ctypes.c_void_p(0x20000), n_slots=-1) == g.GDN2_ERR_INVALID_ARG
+    assert f(slots=ctypes.c_void_p(0x20002), n_slots=4) == g.GDN2_ERR_MISALIGNED
+    assert f(dk=48) == g.GDN2_ERR_UNSUPPORTED
+    assert f(p=None) == g.GDN2_ERR_INVALID_ARG
+    assert f(N=0, p=None) == g.GDN2_OK
