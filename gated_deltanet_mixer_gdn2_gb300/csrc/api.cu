@@ -184,7 +184,7 @@ void gdn2_set_wait_limit(long long ns) { g_wait_ns.store(ns < 0 ? kDefaultWaitNs
 
 gdn2_status gdn2_selftest_umma(int case_id, int soft, const void* a_storage, const void* b_storage, float* d_out,
                                void* stream) {
-    if (case_id < 0 || case_id > 4 || !a_storage || !b_storage || !d_out) return GDN2_ERR_INVALID_ARG;
+    if (case_id < 0 || case_id > 7 || !a_storage || !b_storage || !d_out) return GDN2_ERR_INVALID_ARG;
     if (!aligned16(a_storage) || !aligned16(b_storage) || !aligned16(d_out)) return GDN2_ERR_MISALIGNED;
     const cudaError_t e = launch_selftest_umma(case_id, soft, a_storage, b_storage, d_out,
                                                static_cast<cudaStream_t>(stream), wait_limit_ns());

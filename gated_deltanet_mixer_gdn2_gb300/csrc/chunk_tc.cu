@@ -6,21 +6,17 @@
 // log-decay of the chunk per key channel:
 //     A = tril_{-1}(K_bar K_til^T),  M = tril_0(Q_anc K_til^T)           [one M=128 MMA, stacked]
 //         with K_bar = b.k.e^{G-a}, Q_anc = q.e^{G-a}, K_til = k.e^{a-G} and a per-channel anchor
-//         a = (min G + max G)/2, so that every factor stays within e^{+-range/2}
+//         a = (G_0 + G_last)/2, so that every factor stays within e^{+-range/2}
 //     T = (I + A)^{-1}                                                   [fp32, blocked forward substitution]
-//     W^T = (b.k.e^{G})^T T^T,  U~^T = (w.v)^T T^T                        [two M=128 MMAs]
-//     U = U~ - W S_n;  O = (q.e^{G}) S_n + M U;  S_{n+1} = e^{G_last} . S_n + (k.e^{G_last-G})^T U
+//     W = T (b.k.e^{G})                                                  [M=128 MMA]
+//     U = T (w.v) - W S_n;  O = (q.e^{G}) S_n + M U;  S_{n+1} = e^{G_last} . S_n + (k.e^{G_last-G})^T U
 //
-// Kernel 1 "factors" (grid: chunks x heads; 128 threads; 2 CTAs/SM): TMA loads the six token
-// tiles of one chunk, one pass over the chunk computes the decayed operands, tcgen05 forms A|M,
-// CUDA cores invert (I + A), tcgen05 forms W^T and U~^T; results go to the workspace.
-// Kernel 2 "state" (grid: heads x d_v halves; 128 threads; sequential over chunks): TMA double-
-// buffers the chunk factors; the state slice lives in registers (fp32, one d_k row per thread =
-// one TMEM lane) with a bf16 copy in shared memory as the MMA operand; per chunk two MMA rounds:
-// [W; Q]·S_n -> U -> {[0; M]·U, K^^T·U}.
-//
-// Every barrier wait is bounded; on expiry the CTA records a timeout in the device status word,
-// drains its own copies / MMAs, frees TMEM and returns.
+// Kernel 1 "factors" (grid: chunks x heads; 256 threads; 3 CTAs/SM): TMA loads q, k, g, b of one
+// chunk, one pass computes the decayed operands, tcgen05 forms A|M, CUDA cores invert (I + A),
+// tcgen05 forms W; -W, q.e^G, k.e^{G_last-G}, M, T and e^{G_last} go to the workspace.
+// Kernel 2 "state" (grid: batch x value heads; warp-specialised; sequential over chunks): the same
+// recurrence transposed, with d_v as the 128-row side of every product, so that the state S^T and
+// U^T are tensor-memory A operands and only the chunk factors are read from shared memory.
 #include <cuda.h>
 
 #include "common.cuh"
@@ -34,10 +30,9 @@ __device__ int g_status_tc;
 
 constexpr int kC = 64;
 constexpr int kD = 128;
-constexpr int kSlice = 64;
 
 // workspace unit (one chunk of one value head), bytes
-constexpr uint32_t kWsW = 0;         // W = T (b.k.e^G)      token-major [64][128] bf16
+constexpr uint32_t kWsW = 0;         // -W = -T (b.k.e^G)    token-major [64][128] bf16
 constexpr uint32_t kWsQb = 16384;    // q.e^G                token-major [64][128] bf16
 constexpr uint32_t kWsKh = 32768;    // k.e^{G_last - G}     token-major [64][128] bf16
 constexpr uint32_t kWsM = 49152;     // M = causal q-k       [64][64] bf16
@@ -152,6 +147,7 @@ __device__ __forceinline__ void tma_store_3d(const void* map, const void* src, i
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // sum_k L[k] R[k][c4..c4+3] (fp32 smem, 16-byte aligned rows)
 template <int KN>
@@ -169,7 +165,7 @@ __device__ __forceinline__ float4 row_times(const float* Lrow, const float* R, i
     return acc;
 }
 
-__global__ void __launch_bounds__(fs::kThreads, 2)
+__global__ void __launch_bounds__(fs::kThreads, 3)
     factors_tc_kernel(const __grid_constant__ FactorMaps maps, uint8_t* __restrict__ ws, int Hk, int Hv, int NC,
                       long long wait_ns) {
     extern __shared__ uint8_t smem_raw[];
@@ -242,12 +238,14 @@ __global__ void __launch_bounds__(fs::kThreads, 2)
         __syncthreads();
         if (tid < 128) {  // exclusive prefix over the 16 token groups, per channel
             const int c = tid;
+            float part[16];
+#pragma unroll
+            for (int q = 0; q < 16; ++q) part[q] = s_gs[q * 128 + c];  // all loads first
             float run = 0.f;
 #pragma unroll
             for (int q = 0; q < 16; ++q) {
-                const float x = s_gs[q * 128 + c];
                 s_gs[q * 128 + c] = run;
-                run += x;
+                run += part[q];
             }
             const float g0 = __bfloat162float(
                 *reinterpret_cast<const __nv_bfloat16*>(sm + fs::G + (c >> 6) * 8192 + sw128_off(0, c & 63)));
@@ -446,7 +444,7 @@ __global__ void __launch_bounds__(fs::kThreads, 2)
                 for (int c8 = 0; c8 < 8; ++c8) {
                     float y[8];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) y[e] = x[8 * c8 + e];
+                    for (int e = 0; e < 8; ++e) y[e] = -x[8 * c8 + e];  // stored negated
                     *reinterpret_cast<uint4*>(sm + fs::WSTG + half * 8192 + t * 128 + ((c8 ^ (t & 7)) << 4)) = pack8(y);
                 }
             }
@@ -471,245 +469,479 @@ __global__ void __launch_bounds__(fs::kThreads, 2)
 struct StateMaps {
     CUtensorMap w, qb, kh, m, t;   // workspace sections
     CUtensorMap v, wg;             // token tiles of v and of the write gate w
+    CUtensorMap o_st;              // output, stored in [64 tokens][32 d_v] tiles
 };
 
 namespace ss {
-// one pipeline stage (offsets inside the stage; every tile 1024-byte aligned)
-constexpr uint32_t A1 = 0;          // [W ; Q]: two 64-wide K blocks of [128 rows][128 B], K-major
-constexpr uint32_t KH = 32768;      // k.e^{G_last-G} token-major: MN-major A operand of K^^T (2 blocks)
-constexpr uint32_t MM = 49152;      // M [64][64] K-major; as [X ; M] its first 64 rows are KH's 2nd block
-constexpr uint32_t TT = 57344;      // T [64][64] K-major; as [T ; 0] it is followed by ...
-constexpr uint32_t ZZ = 65536;      // ... 64 rows of zeros (written once)
-constexpr uint32_t VV = 73728;      // v slice [64 tokens][64 columns] (128-byte swizzle)
-constexpr uint32_t WW = 81920;      // w slice
-constexpr uint32_t GAM = 90112;     // e^{G_last} fp32 [128]
-constexpr uint32_t STAGE = 91136;
-constexpr uint32_t TX = 3 * 16384 + 4 * 8192 + 512;   // bytes delivered per stage
-constexpr uint32_t SBF = 2 * STAGE;         // S_n bf16 [128 rows d_k][64], MN-major B operand
-constexpr uint32_t UBF = SBF + 16384;       // U bf16 [64 tokens][64], MN-major B operand
-constexpr uint32_t WV = UBF + 8192;         // w.v bf16 [64 tokens][64], MN-major B operand
-constexpr uint32_t BAR = WV + 8192;         // full[2], mma, TMEM base, 3 flags
-constexpr uint32_t TOTAL = BAR + 64;
-constexpr int kThreads = 256;
-// TMEM columns: D1 (rows 0-63: U = T(w.v) - W S_n; rows 64-127: -(Q S_n + M U)) double-buffered at
-// 0 and 128; D2 = K^^T U at 64.
-__host__ __device__ constexpr uint32_t d1_col(int n) { return (n & 1) ? 128u : 0u; }
-constexpr uint32_t kD2 = 64;
+// Two rings of two slots in shared memory (every tile 1024-byte aligned). "big" holds what the
+// products of chunk n read during step n; "pre" holds what is used one step ahead (w.v, T, the
+// chunk decay), so each slot is released as soon as its last reader is done.
+constexpr uint32_t A1 = 0;          // big: [-W ; Q], two 64-wide K (d_k) blocks of [128 rows (token)][128 B]
+constexpr uint32_t KH = 32768;      // big: k.e^{G_last-G} token-major, two 64-wide d_k blocks (MN-major B)
+constexpr uint32_t MM = 49152;      // big: M [64 tokens][64 tokens] (K-major B)
+constexpr uint32_t BIG = 57344;     // big slot size
+constexpr uint32_t TT = 0;          // pre: T [64][64] (K-major B)
+constexpr uint32_t VV = 8192;       // pre: v tile [64 tokens][128 d_v] as two 64-wide blocks; w.v in place
+constexpr uint32_t WW = 24576;      // pre: w tile, same layout
+constexpr uint32_t GAM = 40960;     // pre: e^{G_last} fp32 [128]
+constexpr uint32_t PRE = 41984;     // pre slot size
+constexpr uint32_t TX_BIG = 2 * 16384 + 16384 + 8192;
+constexpr uint32_t TX_PRE = 8192 + 2 * 16384 + 512;
+constexpr uint32_t BIG0 = 0, PRE0 = 2 * BIG;
+constexpr uint32_t GAMC = PRE0 + 2 * PRE;   // per chain warp copies of e^{G_last}: [2][8 warps][64] fp32
+constexpr uint32_t OST = GAMC + 4096;       // output staging: [4 warps][64 tokens][32 d_v] bf16
+constexpr uint32_t BAR = OST + 16384;       // mbarriers, TMEM base, error flag
+constexpr uint32_t TOTAL = BAR + 256;
+constexpr int kChainWarps = 8;              // warps 0-7: w.v, U and state read-outs
+constexpr int kOutWarps = 4;                // warps 8-11: output read-out
+constexpr int kProducer = 12, kIssuer = 13;
+constexpr int kThreads = 14 * 32;
+// TMEM columns. D_UO[b] (b = chunk parity): columns 0-63 U^T = (w.v)^T T^T - S^T W^T, 64-127
+// O^T = S^T Q^T + U^T M^T. D_S holds e^{G_last} . S_n^T before U^T K^ is added to it, S_{n+1}^T
+// after. Then the bf16 A operands S^T (d_k packed two per column) and U^T (tokens packed).
+constexpr uint32_t kDuo = 0, kDs = 256, kAs = 384, kAu = 448;
 }  // namespace ss
 
-// Write 32 values as half `half` (16-byte chunks 4*half .. 4*half+3) of 128-byte swizzled row `row`.
-__device__ __forceinline__ void store_halfrow_sw128(uint8_t* tile, int row, int half, const float (&x)[32]) {
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-        float y[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) y[e] = x[8 * c + e];
-        *reinterpret_cast<uint4*>(tile + row * 128 + (((4 * half + c) ^ (row & 7)) << 4)) = pack8(y);
+__device__ __forceinline__ void mbar_arrive1(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// Bounded wait that also gives up as soon as another role has recorded a failure in *err.
+__device__ __forceinline__ bool mbar_wait_or_abort(uint64_t* bar, uint32_t parity, long long limit_ns,
+                                                   volatile int* err) {
+    if (limit_ns <= 0) return false;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t it = 0;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 63) == 63) {
+            if (*err) return false;
+            if ((long long)(globaltimer_ns() - t0) > limit_ns) return false;
+        }
     }
 }
 
+__device__ __forceinline__ void note_failure(volatile int* err) {
+    if (!*err) {
+        record_timeout();
+        *err = 1;
+    }
+}
+
+// Warp-uniform wait: lane 0 polls (and records a timeout), the verdict is broadcast, and every lane
+// then observes the completed phase itself.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, long long limit_ns, volatile int* err) {
+    int ok = 0;
+    if ((threadIdx.x & 31) == 0) {
+        ok = mbar_wait_or_abort(bar, parity, limit_ns, err) ? 1 : 0;
+        if (!ok) note_failure(err);
+    }
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (ok) mbar_wait(bar, parity, kDefaultWaitNs);
+    return ok != 0;
+}
+
+__device__ __forceinline__ void tmem_st_f32x16(uint32_t taddr, const float* x) {
+    uint32_t r[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(x[i]);
+    tmem_st16(taddr, r);
+}
+
+// 32 fp32 values -> 16 columns of bf16 pairs (lower index in the low half)
+__device__ __forceinline__ void tmem_st_bf16x32(uint32_t taddr, const float* x) {
+    uint32_t r[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) r[i] = pack_bf16x2(x[2 * i], x[2 * i + 1]);
+    tmem_st16(taddr, r);
+}
+
+__device__ __forceinline__ void tma_store_4d(const void* map, const void* src, int c0, int c1, int c2, int c3) {
+    asm volatile("cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+                 : "memory");
+}
+
+// The chunk recurrence in transposed form, one CTA per (batch, value head): with S^T (d_v x d_k) and
+// per chunk n the factors of the workspace,
+//   U^T = (w.v)^T T^T - S_n^T W^T,   O^T = S_n^T Q^T + U^T M^T,   S_{n+1}^T = S_n^T diag(e^{G_last}) + U^T K^.
+// d_v is the 128-row M dimension of every product, so S^T and U^T (bf16 copies in tensor memory)
+// are the A operands and only the factors are read from shared memory; the fp32 state stays in the
+// tensor-memory accumulator of U^T K^. The dependent chain per chunk is
+//   S_n^T -> [S^T W^T | S^T Q^T] -> U^T -> + U^T K^ -> S_{n+1}^T;
+// w.v, (w.v)^T T^T, U^T M^T, the decay of the accumulator and the output run beside it. Roles: a
+// TMA warp keeps both slots of both rings in flight, an MMA warp issues (one lane), eight chain warps
+// form w.v and read U and the state, four warps read the output. They hand over through mbarriers; every wait is
+// bounded.
 __global__ void __launch_bounds__(ss::kThreads, 1)
     state_tc_kernel(const __grid_constant__ StateMaps maps, const uint8_t* __restrict__ ws,
-                    const float* __restrict__ s0, float* __restrict__ sT_out, __nv_bfloat16* __restrict__ o, int T,
-                    int Hv, int NC, float scale, long long wait_ns) {
+                    const float* __restrict__ s0, float* __restrict__ sT_out, int Hv, int NC, float scale,
+                    long long wait_ns) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(sm);
-    uint64_t* full = reinterpret_cast<uint64_t*>(sm + ss::BAR);
-    uint64_t* bar_mma = full + 2;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + ss::BAR + 24);
-    int* flag = reinterpret_cast<int*>(sm + ss::BAR + 28);  // 3 slots: one per wait site, so that a
-                                                            // slot is never rewritten before all read it
+    uint64_t* full_big = reinterpret_cast<uint64_t*>(sm + ss::BAR);  // [2] big slot landed
+    uint64_t* empty_big = full_big + 2;                              // [2] big slot consumed
+    uint64_t* full_pre = full_big + 4;                               // [2] pre slot landed
+    uint64_t* empty_pre = full_big + 6;                              // [2] pre slot consumed
+    uint64_t* wv_ready = full_big + 8;                               // [2] w.v formed (per chunk parity)
+    uint64_t* o_free = full_big + 10;                                // [2] O^T columns of D_UO[b] zeroed
+    uint64_t* o_done = full_big + 12;                                // [2] O^T of D_UO[b] complete
+    uint64_t* mma1_done = full_big + 14;                             // S^T W^T, S^T Q^T complete
+    uint64_t* s_done = full_big + 15;                                // U^T K^ complete
+    uint64_t* u_ready = full_big + 16;                               // U^T written, D_S decayed (8 warps)
+    uint64_t* s_ready = full_big + 17;                               // S^T written (8 chain warps)
+    uint64_t* drain = full_big + 18;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + ss::BAR + 224);
+    volatile int* err = reinterpret_cast<volatile int*>(sm + ss::BAR + 228);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int q4 = warp & 3, half = warp >> 2;  // TMEM lane quarter, column half
-    const int bh = blockIdx.x, z = blockIdx.y;
+    const int bh = blockIdx.x;
     const int bi = bh / Hv, hv = bh - bi * Hv;
-    const int r = 32 * q4 + lane;  // d_k row of the state (= TMEM lane) owned by this thread
-    const uint32_t lane_base = static_cast<uint32_t>(32 * q4) << 16;
 
     if (tid == 0) {
-        mbar_init(full, 1);
-        mbar_init(full + 1, 1);
-        mbar_init(bar_mma, 1);
+        for (int i = 0; i < 8; ++i) mbar_init(full_big + i, 1);
+        mbar_init(wv_ready, ss::kChainWarps);
+        mbar_init(wv_ready + 1, ss::kChainWarps);
+        mbar_init(o_free, ss::kOutWarps);
+        mbar_init(o_free + 1, ss::kOutWarps);
+        mbar_init(o_done, 1);
+        mbar_init(o_done + 1, 1);
+        mbar_init(mma1_done, 1);
+        mbar_init(s_done, 1);
+        mbar_init(u_ready, ss::kChainWarps);
+        mbar_init(s_ready, ss::kChainWarps);
+        mbar_init(drain, 1);
+        *err = 0;
         fence_mbar_init();
     }
     if (warp == 0) {
-        tmem_alloc(tmem_slot, 256);
+        tmem_alloc(tmem_slot, 512);
         tmem_relinquish();
     }
-    for (int p = tid; p < 2 * 512; p += ss::kThreads) {  // the zero rows under T, both stages
-        const int st = p >> 9, q16 = p & 511;
-        reinterpret_cast<uint4*>(sm + st * ss::STAGE + ss::ZZ)[q16] = make_uint4(0, 0, 0, 0);
-    }
-    float S[32];  // S_n[r][32*half + j], fp32
-    {
-        const float* src = s0 ? s0 + (static_cast<size_t>(bh) * kD + r) * kD + z * kSlice + 32 * half : nullptr;
-#pragma unroll
-        for (int j = 0; j < 32; j += 4) {
-            const float4 t4 = src ? *reinterpret_cast<const float4*>(src + j) : make_float4(0.f, 0.f, 0.f, 0.f);
-            S[j] = t4.x;
-            S[j + 1] = t4.y;
-            S[j + 2] = t4.z;
-            S[j + 3] = t4.w;
-        }
-        store_halfrow_sw128(sm + ss::SBF, r, half, S);
-    }
-    fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    auto issue = [&](int n) {
-        const int st = n & 1;
-        uint8_t* sb = sm + st * ss::STAGE;
-        const int u = bh * NC + n;
-        mbar_arrive_expect_tx(full + st, ss::TX);
+    if (warp == ss::kProducer) {
+        // ================================ TMA warp ================================
+        // order of need: pre(0), then big(m), pre(m+1)
+        int big_issued = -1, pre_issued = -1;
+        if (lane == 0) {
+            auto issue_pre = [&](int m) -> bool {
+                const int st = m & 1;
+                if (m >= 2 && !mbar_wait_or_abort(empty_pre + st, ((m >> 1) + 1) & 1, wait_ns, err)) return false;
+                uint8_t* sb = sm + ss::PRE0 + st * ss::PRE;
+                const int u = bh * NC + m;
+                mbar_arrive_expect_tx(full_pre + st, ss::TX_PRE);
+                tma_load_3d(sb + ss::TT, &maps.t, 0, 0, u, full_pre + st);
 #pragma unroll
-        for (int kb = 0; kb < 2; ++kb) {
-            tma_load_3d(sb + ss::A1 + kb * 16384, &maps.w, 64 * kb, 0, u, full + st);
-            tma_load_3d(sb + ss::A1 + kb * 16384 + 8192, &maps.qb, 64 * kb, 0, u, full + st);
-            tma_load_3d(sb + ss::KH + kb * 8192, &maps.kh, 64 * kb, 0, u, full + st);
+                for (int kb = 0; kb < 2; ++kb) {
+                    tma_load_4d(sb + ss::VV + kb * 8192, &maps.v, 64 * kb, hv, m * kC, bi, full_pre + st);
+                    tma_load_4d(sb + ss::WW + kb * 8192, &maps.wg, 64 * kb, hv, m * kC, bi, full_pre + st);
+                }
+                bulk_load(sb + ss::GAM, ws + static_cast<size_t>(u) * kWsUnit + kWsGam, 512, full_pre + st);
+                pre_issued = m;
+                return true;
+            };
+            auto issue_big = [&](int m) -> bool {
+                const int st = m & 1;
+                if (m >= 2 && !mbar_wait_or_abort(empty_big + st, ((m >> 1) + 1) & 1, wait_ns, err)) return false;
+                uint8_t* sb = sm + ss::BIG0 + st * ss::BIG;
+                const int u = bh * NC + m;
+                mbar_arrive_expect_tx(full_big + st, ss::TX_BIG);
+#pragma unroll
+                for (int kb = 0; kb < 2; ++kb) {
+                    tma_load_3d(sb + ss::A1 + kb * 16384, &maps.w, 64 * kb, 0, u, full_big + st);
+                    tma_load_3d(sb + ss::A1 + kb * 16384 + 8192, &maps.qb, 64 * kb, 0, u, full_big + st);
+                    tma_load_3d(sb + ss::KH + kb * 8192, &maps.kh, 64 * kb, 0, u, full_big + st);
+                }
+                tma_load_3d(sb + ss::MM, &maps.m, 0, 0, u, full_big + st);
+                big_issued = m;
+                return true;
+            };
+            bool go = NC > 0 && issue_pre(0);
+            for (int m = 0; go && m < NC; ++m) go = issue_big(m) && (m + 1 >= NC || issue_pre(m + 1));
+            if (!go && NC > 0) note_failure(err);
+            // every load this warp issued has landed before the block releases its shared memory
+            for (int m = big_issued - 1; m <= big_issued; ++m)
+                if (m >= 0) mbar_wait(full_big + (m & 1), (m >> 1) & 1, kDefaultWaitNs);
+            for (int m = pre_issued - 1; m <= pre_issued; ++m)
+                if (m >= 0) mbar_wait(full_pre + (m & 1), (m >> 1) & 1, kDefaultWaitNs);
         }
-        tma_load_3d(sb + ss::MM, &maps.m, 0, 0, u, full + st);
-        tma_load_3d(sb + ss::TT, &maps.t, 0, 0, u, full + st);
-        tma_load_4d(sb + ss::VV, &maps.v, z * kSlice, hv, n * kC, bi, full + st);
-        tma_load_4d(sb + ss::WW, &maps.wg, z * kSlice, hv, n * kC, bi, full + st);
-        bulk_load(sb + ss::GAM, ws + static_cast<size_t>(u) * kWsUnit + kWsGam, 512, full + st);
-    };
-    // O rows of chunk m (tokens 64m..64m+63): the D1 rows 64..127 it was accumulated in hold -O
-    auto emit_o = [&](int m) {
-        if (q4 < 2) return;
-        const int i = 32 * (q4 - 2) + lane;
-        const int tok = m * kC + i;
-        float x[32];
-        tmem_ld_cols<2>(tmem + lane_base + ss::d1_col(m) + 32 * half, x);
-        if (tok < T) {
-            uint4* dst = reinterpret_cast<uint4*>(o + ((static_cast<size_t>(bi) * T + tok) * Hv + hv) * kD +
-                                                  z * kSlice + 32 * half);
+    } else if (warp == ss::kIssuer) {
+        // ================================ MMA warp ================================
+        // Tensor-pipe order per step n: S^T[-W;Q]^T (n) | (w.v)^T T^T (n+1) | U^T K^ (n) | U^T M^T (n):
+        // the two products off the chain fill the gaps while U and the state are read out.
+        if (lane == 0) {
+            constexpr uint32_t id_uo = idesc_bf16(128, 128, false, false);  // S^T [-W ; Q]^T
+            constexpr uint32_t id_s = idesc_bf16(128, 128, false, true);    // U^T K^
+            constexpr uint32_t id_o = idesc_bf16(128, 64, false, false);    // U^T M^T
+            constexpr uint32_t id_0 = idesc_bf16(128, 64, true, false);     // (w.v)^T T^T
+            auto desc = [&](uint32_t off, uint32_t lbo) { return smem_desc(sbase + off, lbo, 1024, kSwizzle128B); };
+            // D_UO[m&1] columns 0-63 = (w.v)^T T^T, once w.v of chunk m has been formed
+            auto mma0_ready = [&](int m) {
+                return mbar_try_wait(wv_ready + (m & 1), (m >> 1) & 1) && mbar_try_wait(full_pre + (m & 1), (m >> 1) & 1);
+            };
+            auto mma0 = [&](int m) -> bool {
+                const int st = m & 1;
+                if (!mbar_wait_or_abort(wv_ready + st, (m >> 1) & 1, wait_ns, err) ||
+                    !mbar_wait_or_abort(full_pre + st, (m >> 1) & 1, wait_ns, err))
+                    return false;
+                tc_fence_after();
+                const uint32_t pre = ss::PRE0 + st * ss::PRE;
+                const uint64_t a = desc(pre + ss::VV, 8192), b = desc(pre + ss::TT, 16);
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                float y[8];
+                for (int s = 0; s < 4; ++s)
+                    mma_bf16(tmem + ss::kDuo + 128 * st, a + (s * 2048 >> 4), b + (s * 32 >> 4), id_0, s > 0);
+                mma_commit(empty_pre + st);
+                return true;
+            };
+            bool run = NC > 0 && mma0(0);
+            for (int n = 0; run && n < NC; ++n) {
+                const int st = n & 1;
+                const uint32_t duo = tmem + ss::kDuo + 128 * st;
+                const uint32_t big = ss::BIG0 + st * ss::BIG;
+                if (!mbar_wait_or_abort(o_free + st, (n >> 1) & 1, wait_ns, err) ||
+                    !mbar_wait_or_abort(full_big + st, (n >> 1) & 1, wait_ns, err) ||
+                    !mbar_wait_or_abort(s_ready, n & 1, wait_ns, err)) {
+                    run = false;
+                    break;
+                }
+                tc_fence_after();
+                {
+                    const uint64_t b = desc(big + ss::A1, 16);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) y[e] = -scale * x[8 * c + e];
-                dst[c] = pack8(y);
+                    for (int s = 0; s < 8; ++s)  // K = d_k: two 64-wide blocks of 16 KB
+                        mma_bf16_ts(duo, tmem + ss::kAs + 8 * s, b + (((s >> 2) * 16384 + (s & 3) * 32) >> 4), id_uo, 1);
+                }
+                mma_commit(mma1_done);
+                // (w.v)^T T^T of the next chunk goes in now if its w.v is ready, else after U^T M^T
+                bool next0 = n + 1 < NC;
+                if (next0 && mma0_ready(n + 1)) {
+                    if (!mma0(n + 1)) {
+                        run = false;
+                        break;
+                    }
+                    next0 = false;
+                }
+                if (!mbar_wait_or_abort(u_ready, n & 1, wait_ns, err)) {
+                    run = false;
+                    break;
+                }
+                tc_fence_after();
+                {
+                    const uint64_t bk = desc(big + ss::KH, 8192), bm = desc(big + ss::MM, 16);
+#pragma unroll
+                    for (int s = 0; s < 4; ++s)  // K = tokens; accumulates onto e^{G_last} . S_n^T
+                        mma_bf16_ts(tmem + ss::kDs, tmem + ss::kAu + 8 * s, bk + (s * 2048 >> 4), id_s, 1);
+                    mma_commit(s_done);
+#pragma unroll
+                    for (int s = 0; s < 4; ++s)
+                        mma_bf16_ts(duo + 64, tmem + ss::kAu + 8 * s, bm + (s * 32 >> 4), id_o, 1);
+                    mma_commit(o_done + st);
+                    mma_commit(empty_big + st);
+                }
+                if (next0 && !mma0(n + 1)) {
+                    run = false;
+                    break;
+                }
+            }
+            if (!run && NC > 0) note_failure(err);
+            // all issued MMAs complete before TMEM and shared memory are released
+            mma_commit(drain);
+            mbar_wait(drain, 0, kDefaultWaitNs);
+        }
+    } else if (warp >= ss::kChainWarps) {
+        // ======================= output read-out (warps 8-11) =======================
+        const int q4 = warp & 3;  // TMEM lane quarter = d_v rows 32*q4 ..
+        const uint32_t lane_base = static_cast<uint32_t>(32 * q4) << 16;
+        uint8_t* stg = sm + ss::OST + q4 * 4096;  // [64 tokens][32 d_v] bf16, 64-byte rows
+        bool ok = NC > 0;
+        if (ok) {
+            float z[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) z[i] = 0.f;
+#pragma unroll
+            for (int b = 0; b < 2; ++b)
+#pragma unroll
+                for (int c = 0; c < 64; c += 16) tmem_st_f32x16(tmem + lane_base + ss::kDuo + 128 * b + 64 + c, z);
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive1(o_free);
+                mbar_arrive1(o_free + 1);
             }
         }
-    };
-    if (tid == 0 && NC > 0) issue(0);
-
-    uint32_t mma_phase = 0;
-    bool ok = true;
-    int n = 0;
-    for (; n < NC && ok; ++n) {
-        const int st = n & 1;
-        uint8_t* sbp = sm + st * ss::STAGE;
-        const uint32_t sb = sbase + st * ss::STAGE;
-        const uint32_t d1 = tmem + ss::d1_col(n);
-        if (tid == 0 && n + 1 < NC) issue(n + 1);
-        ok = cta_wait(full + st, (n >> 1) & 1, wait_ns, flag + 0);
-        if (!ok) break;
-        {  // w.v for this chunk's 64 x 64 slice: two 16-byte chunks per thread, same swizzled positions
+        for (int m = 0; ok && m < NC; ++m) {
+            const int st = m & 1;
+            if (!(ok = warp_wait(o_done + st, (m >> 1) & 1, wait_ns, err))) break;
+            tc_fence_after();
+            if (lane == 0) bulk_wait_read_all();  // the previous chunk's store has read the staging
+            __syncwarp();
 #pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2) {
-                const int item = tid + 256 * h2;  // 512 chunks = 64 rows x 8 chunks
-                const uint32_t off = (item >> 3) * 128 + ((item & 7) << 4);
+            for (int c0 = 0; c0 < 64; c0 += 32) {
+                float x[32];
+                tmem_ld_cols<2>(tmem + lane_base + ss::kDuo + 128 * st + 64 + c0, x);
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    *reinterpret_cast<__nv_bfloat16*>(stg + (c0 + j) * 64 + lane * 2) = __float2bfloat16_rn(scale * x[j]);
+            }
+            {
+                float z[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) z[i] = 0.f;
+#pragma unroll
+                for (int c = 0; c < 64; c += 16) tmem_st_f32x16(tmem + lane_base + ss::kDuo + 128 * st + 64 + c, z);
+                tmem_st_wait();
+                tc_fence_before();
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive1(o_free + st);
+                // rows past T are clipped by the tensor map
+                tma_store_4d(&maps.o_st, stg, 32 * q4, hv, m * kC, bi);
+                bulk_commit();
+            }
+        }
+        if (lane == 0) bulk_wait_all();  // the output is written before the block retires
+    } else {
+        // ================== w.v, U and state read-outs (warps 0-7) ==================
+        const int q4 = warp & 3, half = warp >> 2;  // TMEM lane quarter; column half
+        const int v = 32 * q4 + lane;                // d_v row (= TMEM lane)
+        const uint32_t lane_base = static_cast<uint32_t>(32 * q4) << 16;
+        auto arrive = [&](uint64_t* bar) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive1(bar);
+        };
+        // e^{G_last} of chunk m for this warp's 64 d_k columns, and w.v in place of v (both tiles
+        // carry the same swizzle, so the product is position-wise)
+        auto take_pre = [&](int m) {
+            const int st = m & 1;
+            uint8_t* sbp = sm + ss::PRE0 + st * ss::PRE;
+            float* gc = reinterpret_cast<float*>(sm + ss::GAMC) + (st * ss::kChainWarps + warp) * 64;
+            const float* gs = reinterpret_cast<const float*>(sbp + ss::GAM) + 64 * half;
+            gc[lane] = gs[lane];
+            gc[lane + 32] = gs[lane + 32];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint32_t off = (tid + 256 * i) * 16;  // 1024 chunks of 16 bytes
                 float a[8], bw[8];
                 unpack8(*reinterpret_cast<const uint4*>(sbp + ss::VV + off), a);
                 unpack8(*reinterpret_cast<const uint4*>(sbp + ss::WW + off), bw);
 #pragma unroll
                 for (int e = 0; e < 8; ++e) a[e] *= bw[e];
-                *reinterpret_cast<uint4*>(sm + ss::WV + off) = pack8(a);
+                *reinterpret_cast<uint4*>(sbp + ss::VV + off) = pack8(a);
             }
+            fence_proxy_async_smem();
+            arrive(wv_ready + st);
+        };
+        // D_S = e^{G_last(m)} . S^T (x holds this thread's 64 columns of S^T)
+        auto decay_into_ds = [&](int m, float (&x)[64]) {
+            const float4* g4 = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(sm + ss::GAMC) +
+                                                               ((m & 1) * ss::kChainWarps + warp) * 64);
+#pragma unroll
+            for (int j4 = 0; j4 < 16; ++j4) {
+                const float4 gg = g4[j4];
+                x[4 * j4] *= gg.x;
+                x[4 * j4 + 1] *= gg.y;
+                x[4 * j4 + 2] *= gg.z;
+                x[4 * j4 + 3] *= gg.w;
+            }
+#pragma unroll
+            for (int c = 0; c < 64; c += 16) tmem_st_f32x16(tmem + lane_base + ss::kDs + 64 * half + c, x + c);
+        };
+        bool ok = NC > 0;
+        if (ok && (ok = warp_wait(full_pre, 0, wait_ns, err))) {
+            take_pre(0);
+            float x[64];
+            const float* src = s0 ? s0 + (static_cast<size_t>(bh) * kD + 64 * half) * kD + v : nullptr;
+#pragma unroll
+            for (int j = 0; j < 64; ++j) x[j] = src ? src[j * kD] : 0.f;
+            tmem_st_bf16x32(tmem + lane_base + ss::kAs + 32 * half, x);
+            tmem_st_bf16x32(tmem + lane_base + ss::kAs + 32 * half + 16, x + 32);
+            decay_into_ds(0, x);
+            tmem_st_wait();
+            tc_fence_before();
+            arrive(s_ready);
         }
-        fence_proxy_async_smem();
-        __syncthreads();
-        // ---- D1 = [T ; 0] (w.v)  then  D1 -= [W ; Q] S_n          (M = 128, N = 64)
-        if (tid == 0) {
+        for (int n = 0; ok && n < NC; ++n) {
+            const int st = n & 1;
+            // w.v of chunk n+1 while S^T [-W ; Q]^T of chunk n runs, if its slot has landed
+            bool pre_done = n + 1 >= NC;
+            if (!pre_done) {
+                int ready = 0;
+                if (lane == 0) ready = mbar_try_wait(full_pre + ((n + 1) & 1), ((n + 1) >> 1) & 1) ? 1 : 0;
+                if (__shfl_sync(0xffffffffu, ready, 0)) {
+                    mbar_wait(full_pre + ((n + 1) & 1), ((n + 1) >> 1) & 1, kDefaultWaitNs);
+                    take_pre(n + 1);
+                    pre_done = true;
+                }
+            }
+            if (!(ok = warp_wait(mma1_done, n & 1, wait_ns, err))) break;
             tc_fence_after();
-            constexpr uint32_t id0 = idesc_bf16(128, 64, false, true);
-            constexpr uint32_t id1 = idesc_bf16(128, 64, false, true) | kNegateA;
-#pragma unroll
-            for (int s = 0; s < 4; ++s) {
-                const uint64_t ad = smem_desc(sb + ss::TT + s * 32, 16, 1024, kSwizzle128B);
-                const uint64_t bd = smem_desc(sbase + ss::WV + s * 2048, 8192, 1024, kSwizzle128B);
-                mma_bf16(d1, ad, bd, id0, s > 0);
+            {  // U^T: this thread's 32 token columns -> bf16 A operand
+                float x[32];
+                tmem_ld_cols<2>(tmem + lane_base + ss::kDuo + 128 * st + 32 * half, x);
+                tmem_st_bf16x32(tmem + lane_base + ss::kAu + 16 * half, x);
+                tmem_st_wait();
+                tc_fence_before();
+                arrive(u_ready);
             }
-#pragma unroll
-            for (int s = 0; s < 8; ++s) {
-                const uint64_t ad = smem_desc(sb + ss::A1 + (s >> 2) * 16384 + (s & 3) * 32, 16, 1024, kSwizzle128B);
-                const uint64_t bd = smem_desc(sbase + ss::SBF + s * 2048, 16384, 1024, kSwizzle128B);
-                mma_bf16(d1, ad, bd, id1, 1);
+            if (!pre_done) {
+                if (!(ok = warp_wait(full_pre + ((n + 1) & 1), ((n + 1) >> 1) & 1, wait_ns, err))) break;
+                take_pre(n + 1);
             }
-            mma_commit(bar_mma);
-        }
-        if (n > 0) emit_o(n - 1);  // previous chunk's output, overlapping these MMAs
-        ok = cta_wait(bar_mma, mma_phase, wait_ns, flag + 1);
-        mma_phase ^= 1;
-        if (!ok) break;
-        tc_fence_after();
-        if (q4 < 2) {  // U rows = tokens 0..63, this thread's 32 columns
-            float x[32];
-            tmem_ld_cols<2>(d1 + lane_base + 32 * half, x);
-            store_halfrow_sw128(sm + ss::UBF, r, half, x);
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        // ---- D1 -= [X ; M] U (rows 0..63 are discarded)  and  D2 = K^^T U     (M = 128, N = 64, K = 64)
-        if (tid == 0) {
+            if (!(ok = warp_wait(s_done, n & 1, wait_ns, err))) break;
             tc_fence_after();
-            constexpr uint32_t id2 = idesc_bf16(128, 64, false, true) | kNegateA;
-            constexpr uint32_t id3 = idesc_bf16(128, 64, true, true);
+            float x[64];  // S_{n+1}^T, this thread's 64 d_k columns
+            tmem_ld_cols<4>(tmem + lane_base + ss::kDs + 64 * half, x);
+            tmem_st_bf16x32(tmem + lane_base + ss::kAs + 32 * half, x);
+            tmem_st_bf16x32(tmem + lane_base + ss::kAs + 32 * half + 16, x + 32);
+            tmem_st_wait();
+            tc_fence_before();
+            arrive(s_ready);
+            if (n + 1 < NC) {
+                decay_into_ds(n + 1, x);  // ordered before U^T K^ of chunk n+1 by the next U hand-off
+                tmem_st_wait();
+                tc_fence_before();
+            } else if (sT_out) {
+                float* dst = sT_out + (static_cast<size_t>(bh) * kD + 64 * half) * kD + v;
 #pragma unroll
-            for (int s = 0; s < 4; ++s) {
-                const uint64_t bd = smem_desc(sbase + ss::UBF + s * 2048, 8192, 1024, kSwizzle128B);
-                const uint64_t a2 = smem_desc(sb + ss::MM - 8192 + s * 32, 16, 1024, kSwizzle128B);
-                const uint64_t a3 = smem_desc(sb + ss::KH + s * 2048, 8192, 1024, kSwizzle128B);
-                mma_bf16(d1, a2, bd, id2, 1);
-                mma_bf16(tmem + ss::kD2, a3, bd, id3, s > 0);
+                for (int j = 0; j < 64; ++j) dst[j * kD] = x[j];
             }
-            mma_commit(bar_mma);
-        }
-        ok = cta_wait(bar_mma, mma_phase, wait_ns, flag + 2);
-        mma_phase ^= 1;
-        if (!ok) break;
-        tc_fence_after();
-        {
-            float x[32];
-            tmem_ld_cols<2>(tmem + lane_base + ss::kD2 + 32 * half, x);
-            const float gam = reinterpret_cast<const float*>(sbp + ss::GAM)[r];
-#pragma unroll
-            for (int jj = 0; jj < 32; ++jj) S[jj] = fmaf(gam, S[jj], x[jj]);
-            store_halfrow_sw128(sm + ss::SBF, r, half, S);
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncthreads();
-    }
-    if (!ok) {
-        // drain the prefetch of the next chunk if it was issued
-        if (tid == 0 && n + 1 < NC) mbar_wait(full + ((n + 1) & 1), ((n + 1) >> 1) & 1, kDefaultWaitNs);
-    } else {
-        if (NC > 0) emit_o(NC - 1);
-        if (sT_out) {
-            float* dst = sT_out + (static_cast<size_t>(bh) * kD + r) * kD + z * kSlice + 32 * half;
-#pragma unroll
-            for (int j = 0; j < 32; j += 4) *reinterpret_cast<float4*>(dst + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
         }
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, 256);
+    if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
 // ---------------------------------------------------------------------------------------------
-// UMMA layout self-test: one M=128, N=64 product with the operand layouts the kernels above use.
+// UMMA layout self-test: one M=128 product with the operand layouts the kernels above use.
 
 struct SelftestMaps {
     CUtensorMap a, b;
 };
+
+// Storage shapes (rows x cols of the row-major device arrays), N and K of each case; see
+// gdn2_selftest_umma in the public header.
+struct SelftestShape {
+    int a_rows, a_cols, b_rows, b_cols, N, K;
+    bool a_mn, b_mn, a_tmem;
+};
+__host__ __device__ constexpr SelftestShape selftest_shape(int c) {
+    return c == 1   ? SelftestShape{64, 128, 64, 64, 64, 64, true, false, false}
+           : c == 2 ? SelftestShape{128, 128, 128, 64, 64, 128, true, true, false}
+           : c == 3 ? SelftestShape{128, 64, 64, 64, 64, 64, false, true, false}
+           : c == 5 ? SelftestShape{128, 64, 64, 64, 64, 64, false, false, true}
+           : c == 6 ? SelftestShape{128, 64, 64, 128, 128, 64, false, true, true}
+           : c == 7 ? SelftestShape{128, 128, 128, 128, 128, 128, false, false, true}
+                    : SelftestShape{128, 128, 64, 128, 64, 128, false, false, false};  // cases 0 and 4
+}
 
 __global__ void __launch_bounds__(128, 1)
     selftest_umma_kernel(const __grid_constant__ SelftestMaps maps, int case_id, int soft,
@@ -719,21 +951,14 @@ __global__ void __launch_bounds__(128, 1)
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(sm);
     const bool negate = (case_id == 4);  // case 4: case 0 with the A operand negated by the descriptor
-    if (negate) case_id = 0;
+    const SelftestShape sh = selftest_shape(case_id);
     uint8_t* sA = sm;
     uint8_t* sB = sm + 32768;
-    uint64_t* bar = reinterpret_cast<uint64_t*>(sm + 49152);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + 49152 + 16);
-    int* flag = reinterpret_cast<int*>(sm + 49152 + 20);
+    uint64_t* bar = reinterpret_cast<uint64_t*>(sm + 65536);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + 65536 + 16);
+    int* flag = reinterpret_cast<int*>(sm + 65536 + 20);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    // storage shapes (rows x cols) per case, see launch_selftest
-    const int a_rows = (case_id == 0 || case_id == 2) ? 128 : (case_id == 1 ? 64 : 128);
-    const int a_cols = (case_id == 3) ? 64 : 128;
-    const int b_rows = (case_id == 0 || case_id == 1) ? 64 : (case_id == 2 ? 128 : 64);
-    const int b_cols = (case_id == 0) ? 128 : 64;
-    const bool a_mn = (case_id == 1 || case_id == 2);
-    const bool b_mn = (case_id == 2 || case_id == 3);
-    const int K = (case_id == 0 || case_id == 2) ? 128 : 64;
+    constexpr uint32_t kAcol = 128;  // TMEM column of an A operand held in tensor memory
 
     if (tid == 0) {
         mbar_init(bar, 1);
@@ -741,46 +966,69 @@ __global__ void __launch_bounds__(128, 1)
         fence_mbar_init();
     }
     if (warp == 0) {
-        tmem_alloc(tmem_slot, 64);
+        tmem_alloc(tmem_slot, 256);
         tmem_relinquish();
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    const uint32_t lane_base = static_cast<uint32_t>(32 * warp) << 16;
+    if (sh.a_tmem) {  // row 32*warp + lane of A, K bf16 values packed two per column
+        const uint32_t* src = reinterpret_cast<const uint32_t*>(a_st + (32 * warp + lane) * sh.a_cols);
+        for (int c0 = 0; c0 < sh.a_cols / 2; c0 += 16) {
+            uint32_t r[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) r[i] = src[c0 + i];
+            tmem_st16(tmem + lane_base + kAcol + c0, r);
+        }
+        tmem_st_wait();
+    }
     // a storage of R rows x (64 * nb) columns becomes nb blocks of R x 128 B (block j = columns 64j..)
     bool ok = true;
     if (soft) {
-        for (int p = tid; p < a_rows * a_cols; p += 128) {
-            const int rr = p / a_cols, cc = p % a_cols;
-            *reinterpret_cast<__nv_bfloat16*>(sA + (cc >> 6) * (a_rows * 128) + sw128_off(rr, cc & 63)) = a_st[p];
-        }
-        for (int p = tid; p < b_rows * b_cols; p += 128) {
-            const int rr = p / b_cols, cc = p % b_cols;
-            *reinterpret_cast<__nv_bfloat16*>(sB + (cc >> 6) * (b_rows * 128) + sw128_off(rr, cc & 63)) = b_st[p];
+        if (!sh.a_tmem)
+            for (int p = tid; p < sh.a_rows * sh.a_cols; p += 128) {
+                const int rr = p / sh.a_cols, cc = p % sh.a_cols;
+                *reinterpret_cast<__nv_bfloat16*>(sA + (cc >> 6) * (sh.a_rows * 128) + sw128_off(rr, cc & 63)) =
+                    a_st[p];
+            }
+        for (int p = tid; p < sh.b_rows * sh.b_cols; p += 128) {
+            const int rr = p / sh.b_cols, cc = p % sh.b_cols;
+            *reinterpret_cast<__nv_bfloat16*>(sB + (cc >> 6) * (sh.b_rows * 128) + sw128_off(rr, cc & 63)) = b_st[p];
         }
         fence_proxy_async_smem();
+        tc_fence_before();
         __syncthreads();
     } else {
+        tc_fence_before();
+        __syncthreads();
         if (tid == 0) {
-            mbar_arrive_expect_tx(bar, (a_rows * a_cols + b_rows * b_cols) * 2);
-            for (int j = 0; j < a_cols / 64; ++j) tma_load_3d(sA + j * a_rows * 128, &maps.a, 64 * j, 0, 0, bar);
-            for (int j = 0; j < b_cols / 64; ++j) tma_load_3d(sB + j * b_rows * 128, &maps.b, 64 * j, 0, 0, bar);
+            mbar_arrive_expect_tx(bar, ((sh.a_tmem ? 0 : sh.a_rows * sh.a_cols) + sh.b_rows * sh.b_cols) * 2);
+            if (!sh.a_tmem)
+                for (int j = 0; j < sh.a_cols / 64; ++j) tma_load_3d(sA + j * sh.a_rows * 128, &maps.a, 64 * j, 0, 0, bar);
+            for (int j = 0; j < sh.b_cols / 64; ++j) tma_load_3d(sB + j * sh.b_rows * 128, &maps.b, 64 * j, 0, 0, bar);
         }
         ok = cta_wait(bar, 0, wait_ns, flag);
     }
     if (ok) {
         if (tid == 0) {
             tc_fence_after();
-            const uint32_t id = idesc_bf16(128, 64, a_mn, b_mn) | (negate ? kNegateA : 0u);
-            for (int s = 0; s < K / 16; ++s) {
+            const uint32_t id = idesc_bf16(128, sh.N, sh.a_mn, sh.b_mn) | (negate ? kNegateA : 0u);
+            for (int s = 0; s < sh.K / 16; ++s) {
                 // K-major: K blocks of 64 are separate R x 128 B regions; step 32 B inside a block.
                 // MN-major: K rows are 128-byte rows; step 16 rows = 2048 B; LBO = next 64-wide MN block.
-                const uint32_t aoff = a_mn ? s * 2048 : (s >> 2) * (a_rows * 128) + (s & 3) * 32;
-                const uint32_t boff = b_mn ? s * 2048 : (s >> 2) * (b_rows * 128) + (s & 3) * 32;
-                const uint64_t ad = smem_desc(sbase + aoff, a_mn ? a_rows * 128 : 16, 1024, kSwizzle128B);
-                const uint64_t bd = smem_desc(sbase + 32768 + boff, b_mn ? b_rows * 128 : 16, 1024, kSwizzle128B);
-                mma_bf16(tmem, ad, bd, id, s > 0);
+                // Tensor memory: 16 K values are 8 columns.
+                const uint32_t boff = sh.b_mn ? s * 2048 : (s >> 2) * (sh.b_rows * 128) + (s & 3) * 32;
+                const uint64_t bd =
+                    smem_desc(sbase + 32768 + boff, sh.b_mn ? sh.b_rows * 128 : 16, 1024, kSwizzle128B);
+                if (sh.a_tmem) {
+                    mma_bf16_ts(tmem, tmem + kAcol + 8 * s, bd, id, s > 0);
+                } else {
+                    const uint32_t aoff = sh.a_mn ? s * 2048 : (s >> 2) * (sh.a_rows * 128) + (s & 3) * 32;
+                    const uint64_t ad = smem_desc(sbase + aoff, sh.a_mn ? sh.a_rows * 128 : 16, 1024, kSwizzle128B);
+                    mma_bf16(tmem, ad, bd, id, s > 0);
+                }
             }
             mma_commit(bar + 1);
         }
@@ -788,13 +1036,15 @@ __global__ void __launch_bounds__(128, 1)
     }
     if (ok) {
         tc_fence_after();
-        float x[64];
-        tmem_ld64(tmem, warp, 0, x);
-        for (int j = 0; j < 64; ++j) d_out[(32 * warp + lane) * 64 + j] = x[j];
+        for (int c0 = 0; c0 < sh.N; c0 += 64) {
+            float x[64];
+            tmem_ld64(tmem, warp, c0, x);
+            for (int j = 0; j < 64; ++j) d_out[(32 * warp + lane) * sh.N + c0 + j] = x[j];
+        }
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, 64);
+    if (warp == 0) tmem_dealloc(tmem, 256);
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -841,6 +1091,14 @@ bool token_map(CUtensorMap* m, const void* p, int B, int T, int H) {
     return make_map(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, p, dims, st, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
+// output [B, T, H, 128] bf16 viewed as (d, H, T, B); box (32, 1, 64, 1), plain rows of 64 bytes
+bool out_map(CUtensorMap* m, const void* p, int B, int T, int H) {
+    const uint64_t dims[4] = {kD, (uint64_t)H, (uint64_t)T, (uint64_t)B};
+    const uint64_t st[3] = {kD * 2, (uint64_t)H * kD * 2, (uint64_t)T * H * kD * 2};
+    const uint32_t box[4] = {32, 1, kC, 1};
+    return make_map(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, p, dims, st, box, CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
 // workspace section viewed as (cols, rows, units); box (box_cols, box_rows, 1)
 bool ws_map(CUtensorMap* m, const void* p, CUtensorMapDataType dt, int esize, int cols, int rows, int units,
             int box_cols, int box_rows, CUtensorMapSwizzle sw) {
@@ -877,7 +1135,8 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const v
         !ws_map(&sm_.kh, wsb + kWsKh, BF, 2, 128, 64, units, 64, 64, SW) ||
         !ws_map(&sm_.m, wsb + kWsM, BF, 2, 64, 64, units, 64, 64, SW) ||
         !ws_map(&sm_.t, wsb + kWsT, BF, 2, 64, 64, units, 64, 64, SW) ||
-        !token_map(&sm_.v, v, sh.B, sh.T, sh.Hv) || !token_map(&sm_.wg, w, sh.B, sh.T, sh.Hv))
+        !token_map(&sm_.v, v, sh.B, sh.T, sh.Hv) || !token_map(&sm_.wg, w, sh.B, sh.T, sh.Hv) ||
+        !out_map(&sm_.o_st, o, sh.B, sh.T, sh.Hv))
         return cudaErrorInvalidValue;
 
     // The state kernel runs one CTA per SM, so it takes the whole 227 KB: operand descriptors can
@@ -891,8 +1150,8 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const v
     factors_tc_kernel<<<dim3(NC, sh.B * sh.Hv), fs::kThreads, f_smem, s>>>(fm, wsb, sh.Hk, sh.Hv, NC, wait_ns);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    state_tc_kernel<<<dim3(sh.B * sh.Hv, kD / kSlice), ss::kThreads, s_smem, s>>>(
-        sm_, wsb, s0, sT, static_cast<__nv_bfloat16*>(o), sh.T, sh.Hv, NC, scale, wait_ns);
+    state_tc_kernel<<<dim3(sh.B * sh.Hv), ss::kThreads, s_smem, s>>>(sm_, wsb, s0, sT, sh.Hv, NC, scale,
+                                                                      wait_ns);
     return cudaGetLastError();
 }
 
@@ -909,14 +1168,9 @@ int chunk_tc_read_clear_status(cudaStream_t s) {
 
 cudaError_t launch_selftest_umma(int case_id, int soft, const void* a_st, const void* b_st, float* d_out,
                                  cudaStream_t s, long long wait_ns) {
-    // storage (rows x cols): case 0: A 128x128 (M x K), B 64x128 (N x K)
-    //                        case 1: A 64x128 (K x M),  B 64x64 (N x K)
-    //                        case 2: A 128x128 (K x M), B 128x64 (K x N)
-    //                        case 3: A 128x64 (M x K),  B 64x64 (K x N)
-    static const int shp[5][4] = {{128, 128, 64, 128}, {64, 128, 64, 64}, {128, 128, 128, 64}, {128, 64, 64, 64},
-                                  {128, 128, 64, 128}};
-    if (case_id < 0 || case_id > 4) return cudaErrorInvalidValue;
-    const int ar = shp[case_id][0], ac = shp[case_id][1], br = shp[case_id][2], bc = shp[case_id][3];
+    if (case_id < 0 || case_id > 7) return cudaErrorInvalidValue;
+    const SelftestShape sh = selftest_shape(case_id);
+    const int ar = sh.a_rows, ac = sh.a_cols, br = sh.b_rows, bc = sh.b_cols;
     SelftestMaps m;
     const uint64_t ad[3] = {(uint64_t)ac, (uint64_t)ar, 1}, as[2] = {(uint64_t)ac * 2, (uint64_t)ac * ar * 2};
     const uint64_t bdm[3] = {(uint64_t)bc, (uint64_t)br, 1}, bs[2] = {(uint64_t)bc * 2, (uint64_t)bc * br * 2};

@@ -185,16 +185,20 @@ gdn2_status gdn2_last_device_status(void* stream);
 void gdn2_set_wait_limit(long long ns);
 
 /*
- * gdn2_selftest_umma -- diagnostics: one tcgen05 product D[128][64] = A * B (bf16 in, fp32 out)
- * with the shared-memory operand layouts the tensor-core chunked kernels use, so that a test can
- * check them against a host matrix product. The operands are row-major bf16 device arrays:
- *   case 0: A [128 (M)][128 (K)],  B [64 (N)][128 (K)]   (both K-major)
- *   case 1: A [64 (K)][128 (M)],   B [64 (N)][64 (K)]    (A MN-major, B K-major)
- *   case 2: A [128 (K)][128 (M)],  B [128 (K)][64 (N)]   (both MN-major)
- *   case 3: A [128 (M)][64 (K)],   B [64 (K)][64 (N)]    (A K-major, B MN-major)
+ * gdn2_selftest_umma -- diagnostics: one tcgen05 product D[128][N] = A * B (bf16 in, fp32 out)
+ * with the operand layouts the tensor-core chunked kernels use, so that a test can check them
+ * against a host matrix product. The operands are row-major bf16 device arrays:
+ *   case 0: A [128 (M)][128 (K)],  B [64 (N)][128 (K)]   (both K-major), N = 64
+ *   case 1: A [64 (K)][128 (M)],   B [64 (N)][64 (K)]    (A MN-major, B K-major), N = 64
+ *   case 2: A [128 (K)][128 (M)],  B [128 (K)][64 (N)]   (both MN-major), N = 64
+ *   case 3: A [128 (M)][64 (K)],   B [64 (K)][64 (N)]    (A K-major, B MN-major), N = 64
  *   case 4: as case 0 with A negated through the instruction descriptor (D = -A * B)
- * soft = 0 stages them with TMA (128-byte swizzle), soft = 1 with ordinary stores using the same
- * swizzle. d_out: [128][64] fp32 device array. Asynchronous on `stream`.
+ *   case 5: A [128 (M)][64 (K)] in tensor memory, B [64 (N)][64 (K)] K-major, N = 64
+ *   case 6: A [128 (M)][64 (K)] in tensor memory, B [64 (K)][128 (N)] MN-major, N = 128
+ *   case 7: A [128 (M)][128 (K)] in tensor memory, B [128 (N)][128 (K)] K-major, N = 128
+ * soft = 0 stages the shared-memory operands with TMA (128-byte swizzle), soft = 1 with ordinary
+ * stores using the same swizzle; an A operand in tensor memory is written with tcgen05.st.
+ * d_out: [128][N] fp32 device array. Asynchronous on `stream`.
  */
 gdn2_status gdn2_selftest_umma(int case_id, int soft, const void* a_storage, const void* b_storage,
                                float* d_out, void* stream);

@@ -1,5 +1,6 @@
-"""tcgen05 operand layouts: one M=128, N=64 product per layout combination the chunked kernels use,
-staged by TMA (128-byte swizzle) and by ordinary stores with the same swizzle, against numpy.
+"""tcgen05 operand layouts: one M=128 product per layout combination the chunked kernels use, with
+shared-memory operands staged by TMA (128-byte swizzle) and by ordinary stores with the same
+swizzle, and A operands held in tensor memory, against numpy.
 Values are small multiples of 1/8, so every product and sum is exact in fp32."""
 import numpy as np
 import pytest
@@ -13,6 +14,10 @@ CASES = {
     2: dict(M=128, N=64, K=128, a_mn=True, b_mn=True),
     3: dict(M=128, N=64, K=64, a_mn=False, b_mn=True),
     4: dict(M=128, N=64, K=128, a_mn=False, b_mn=False, neg=True),
+    # A read from tensor memory (row-major M x K storage, written with tcgen05.st)
+    5: dict(M=128, N=64, K=64, a_mn=False, b_mn=False),
+    6: dict(M=128, N=128, K=64, a_mn=False, b_mn=True),
+    7: dict(M=128, N=128, K=128, a_mn=False, b_mn=False),
 }
 
 
@@ -32,7 +37,7 @@ def test_umma_layout(case, soft):
     dev = torch.device("cuda")
     at = torch.tensor(np.ascontiguousarray(a_st), dtype=torch.bfloat16, device=dev)
     bt = torch.tensor(np.ascontiguousarray(b_st), dtype=torch.bfloat16, device=dev)
-    d = torch.full((128, 64), float("nan"), dtype=torch.float32, device=dev)
+    d = torch.full((128, c["N"]), float("nan"), dtype=torch.float32, device=dev)
     g.gdn2_selftest_umma(case, soft, at, bt, d)
     torch.cuda.synchronize()
     assert g.gdn2_last_device_status() == g.GDN2_OK
