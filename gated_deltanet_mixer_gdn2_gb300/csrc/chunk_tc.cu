@@ -473,33 +473,39 @@ struct StateMaps {
 };
 
 namespace ss {
-// Two rings of two slots in shared memory (every tile 1024-byte aligned). "big" holds what the
-// products of chunk n read during step n; "pre" holds what is used one step ahead (w.v, T, the
-// chunk decay), so each slot is released as soon as its last reader is done.
-constexpr uint32_t A1 = 0;          // big: [-W ; Q], two 64-wide K (d_k) blocks of [128 rows (token)][128 B]
+// Shared memory (every tile 1024-byte aligned): two rings of two slots, "big" for what the products
+// of chunk n read during step n, "pre" for what is used one step ahead (w.v, the chunk decay), so
+// each slot is released as soon as its last reader is done; the T tiles of the two chunk parities
+// sit around one zero tile.
+constexpr uint32_t A1 = 0;          // big: [-W ; Q] (even chunks) or [Q ; -W] (odd chunks): two 64-wide
+                                    //      K (d_k) blocks of [128 rows (token)][128 B]
 constexpr uint32_t KH = 32768;      // big: k.e^{G_last-G} token-major, two 64-wide d_k blocks (MN-major B)
 constexpr uint32_t MM = 49152;      // big: M [64 tokens][64 tokens] (K-major B)
 constexpr uint32_t BIG = 57344;     // big slot size
-constexpr uint32_t TT = 0;          // pre: T [64][64] (K-major B)
-constexpr uint32_t VV = 8192;       // pre: v tile [64 tokens][128 d_v] as two 64-wide blocks; w.v in place
-constexpr uint32_t WW = 24576;      // pre: w tile, same layout
-constexpr uint32_t GAM = 40960;     // pre: e^{G_last} fp32 [128]
-constexpr uint32_t PRE = 41984;     // pre slot size
+constexpr uint32_t VV = 0;          // pre: v tile [64 tokens][128 d_v] as two 64-wide blocks; w.v in place
+constexpr uint32_t WW = 16384;      // pre: w tile, same layout
+constexpr uint32_t GAM = 32768;     // pre: e^{G_last} fp32 [128]
+constexpr uint32_t PRE = 33792;     // pre slot size
 constexpr uint32_t TX_BIG = 2 * 16384 + 16384 + 8192;
 constexpr uint32_t TX_PRE = 8192 + 2 * 16384 + 512;
-constexpr uint32_t BIG0 = 0, PRE0 = 2 * BIG;
-constexpr uint32_t GAMC = PRE0 + 2 * PRE;   // per chain warp copies of e^{G_last}: [2][8 warps][64] fp32
-constexpr uint32_t OST = GAMC + 4096;       // output staging: [4 warps][64 tokens][32 d_v] bf16
+constexpr uint32_t BIG0 = 0;
+constexpr uint32_t TZ = 2 * BIG;            // T (even chunk) | zeros | T (odd chunk), [64][64] bf16 each:
+                                            // as N = 128 K-major B operands, [T ; 0] and [0 ; T]
+constexpr uint32_t PRE0 = TZ + 3 * 8192;
+constexpr uint32_t GAMC = PRE0 + 2 * PRE;   // copies of e^{G_last}: [4 chunks][128] fp32
+constexpr uint32_t OST = GAMC + 2048;       // output staging: [4 warps][64 tokens][32 d_v] bf16
 constexpr uint32_t BAR = OST + 16384;       // mbarriers, TMEM base, error flag
 constexpr uint32_t TOTAL = BAR + 256;
-constexpr int kChainWarps = 8;              // warps 0-7: w.v, U and state read-outs
-constexpr int kOutWarps = 4;                // warps 8-11: output read-out
+constexpr int kChainWarps = 8;              // warps 0-7: U and state read-outs
+constexpr int kOutWarps = 4;                // warps 8-11: output read-out, w.v
 constexpr int kProducer = 12, kIssuer = 13;
 constexpr int kThreads = 14 * 32;
-// TMEM columns. D_UO[b] (b = chunk parity): columns 0-63 U^T = (w.v)^T T^T - S^T W^T, 64-127
-// O^T = S^T Q^T + U^T M^T. D_S holds e^{G_last} . S_n^T before U^T K^ is added to it, S_{n+1}^T
-// after. Then the bf16 A operands S^T (d_k packed two per column) and U^T (tokens packed).
+// TMEM columns. D_UO[b] (b = chunk parity) holds U^T = (w.v)^T T^T - S^T W^T in columns 64b..64b+63
+// and O^T = S^T Q^T + U^T M^T in the other 64. D_S holds e^{G_last} . S_n^T before U^T K^ is added
+// to it, S_{n+1}^T after. Then the bf16 A operands S^T (d_k packed two per column) and U^T.
 constexpr uint32_t kDuo = 0, kDs = 256, kAs = 384, kAu = 448;
+__host__ __device__ constexpr uint32_t u_col(int b) { return 128u * b + 64u * b; }
+__host__ __device__ constexpr uint32_t o_col(int b) { return 128u * b + 64u * (1 - b); }
 }  // namespace ss
 
 __device__ __forceinline__ void mbar_arrive1(uint64_t* bar) {
@@ -510,13 +516,12 @@ __device__ __forceinline__ void mbar_arrive1(uint64_t* bar) {
 __device__ __forceinline__ bool mbar_wait_or_abort(uint64_t* bar, uint32_t parity, long long limit_ns,
                                                    volatile int* err) {
     if (limit_ns <= 0) return false;
+    if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
-    for (uint32_t it = 0;; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 63) == 63) {
-            if (*err) return false;
-            if ((long long)(globaltimer_ns() - t0) > limit_ns) return false;
-        }
+    for (;;) {
+        if (mbar_try_wait_sleep(bar, parity, kWaitHintNs)) return true;
+        if (*err) return false;
+        if ((long long)(globaltimer_ns() - t0) > limit_ns) return false;
     }
 }
 
@@ -571,7 +576,7 @@ __device__ __forceinline__ void tma_store_4d(const void* map, const void* src, i
 //   S_n^T -> [S^T W^T | S^T Q^T] -> U^T -> + U^T K^ -> S_{n+1}^T;
 // w.v, (w.v)^T T^T, U^T M^T, the decay of the accumulator and the output run beside it. Roles: a
 // TMA warp keeps both slots of both rings in flight, an MMA warp issues (one lane), eight chain warps
-// form w.v and read U and the state, four warps read the output. They hand over through mbarriers; every wait is
+// read U and the state, four warps form w.v and read the output. They hand over through mbarriers; every wait is
 // bounded.
 __global__ void __launch_bounds__(ss::kThreads, 1)
     state_tc_kernel(const __grid_constant__ StateMaps maps, const uint8_t* __restrict__ ws,
@@ -585,7 +590,7 @@ __global__ void __launch_bounds__(ss::kThreads, 1)
     uint64_t* full_pre = full_big + 4;                               // [2] pre slot landed
     uint64_t* empty_pre = full_big + 6;                              // [2] pre slot consumed
     uint64_t* wv_ready = full_big + 8;                               // [2] w.v formed (per chunk parity)
-    uint64_t* o_free = full_big + 10;                                // [2] O^T columns of D_UO[b] zeroed
+    uint64_t* o_free = full_big + 10;                                // [2] O^T columns of D_UO[b] read
     uint64_t* o_done = full_big + 12;                                // [2] O^T of D_UO[b] complete
     uint64_t* mma1_done = full_big + 14;                             // S^T W^T, S^T Q^T complete
     uint64_t* s_done = full_big + 15;                                // U^T K^ complete
@@ -601,8 +606,8 @@ __global__ void __launch_bounds__(ss::kThreads, 1)
 
     if (tid == 0) {
         for (int i = 0; i < 8; ++i) mbar_init(full_big + i, 1);
-        mbar_init(wv_ready, ss::kChainWarps);
-        mbar_init(wv_ready + 1, ss::kChainWarps);
+        mbar_init(wv_ready, ss::kOutWarps);
+        mbar_init(wv_ready + 1, ss::kOutWarps);
         mbar_init(o_free, ss::kOutWarps);
         mbar_init(o_free + 1, ss::kOutWarps);
         mbar_init(o_done, 1);
@@ -619,6 +624,9 @@ __global__ void __launch_bounds__(ss::kThreads, 1)
         tmem_alloc(tmem_slot, 512);
         tmem_relinquish();
     }
+    for (int p = tid; p < 512; p += ss::kThreads)
+        reinterpret_cast<uint4*>(sm + ss::TZ + 8192)[p] = make_uint4(0, 0, 0, 0);
+    fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -635,7 +643,7 @@ __global__ void __launch_bounds__(ss::kThreads, 1)
                 uint8_t* sb = sm + ss::PRE0 + st * ss::PRE;
                 const int u = bh * NC + m;
                 mbar_arrive_expect_tx(full_pre + st, ss::TX_PRE);
-                tma_load_3d(sb + ss::TT, &maps.t, 0, 0, u, full_pre + st);
+                tma_load_3d(sm + ss::TZ + 16384 * st, &maps.t, 0, 0, u, full_pre + st);
 #pragma unroll
                 for (int kb = 0; kb < 2; ++kb) {
                     tma_load_4d(sb + ss::VV + kb * 8192, &maps.v, 64 * kb, hv, m * kC, bi, full_pre + st);
@@ -653,8 +661,8 @@ __global__ void __launch_bounds__(ss::kThreads, 1)
                 mbar_arrive_expect_tx(full_big + st, ss::TX_BIG);
 #pragma unroll
                 for (int kb = 0; kb < 2; ++kb) {
-                    tma_load_3d(sb + ss::A1 + kb * 16384, &maps.w, 64 * kb, 0, u, full_big + st);
-                    tma_load_3d(sb + ss::A1 + kb * 16384 + 8192, &maps.qb, 64 * kb, 0, u, full_big + st);
+                    tma_load_3d(sb + ss::A1 + kb * 16384 + 8192 * st, &maps.w, 64 * kb, 0, u, full_big + st);
+                    tma_load_3d(sb + ss::A1 + kb * 16384 + 8192 * (1 - st), &maps.qb, 64 * kb, 0, u, full_big + st);
                     tma_load_3d(sb + ss::KH + kb * 8192, &maps.kh, 64 * kb, 0, u, full_big + st);
                 }
                 tma_load_3d(sb + ss::MM, &maps.m, 0, 0, u, full_big + st);
@@ -672,26 +680,30 @@ __global__ void __launch_bounds__(ss::kThreads, 1)
         }
     } else if (warp == ss::kIssuer) {
         // ================================ MMA warp ================================
-        // Tensor-pipe order per step n: S^T[-W;Q]^T (n) | (w.v)^T T^T (n+1) | U^T K^ (n) | U^T M^T (n):
-        // the two products off the chain fill the gaps while U and the state are read out.
+        // Tensor-pipe order per step n: S^T[-W;Q]^T (n) | (w.v)^T T^T (n+1) if ready | U^T K^ (n) |
+        // U^T M^T (n) | (w.v)^T T^T (n+1) otherwise: the products off the chain fill the gaps while
+        // U and the state are read out.
         if (lane == 0) {
             constexpr uint32_t id_uo = idesc_bf16(128, 128, false, false);  // S^T [-W ; Q]^T
             constexpr uint32_t id_s = idesc_bf16(128, 128, false, true);    // U^T K^
             constexpr uint32_t id_o = idesc_bf16(128, 64, false, false);    // U^T M^T
-            constexpr uint32_t id_0 = idesc_bf16(128, 64, true, false);     // (w.v)^T T^T
+            constexpr uint32_t id_0 = idesc_bf16(128, 128, true, false);    // (w.v)^T [T ; 0]^T
             auto desc = [&](uint32_t off, uint32_t lbo) { return smem_desc(sbase + off, lbo, 1024, kSwizzle128B); };
-            // D_UO[m&1] columns 0-63 = (w.v)^T T^T, once w.v of chunk m has been formed
+            // D_UO[m&1] = (w.v)^T T^T in the U columns and 0 in the O columns, once w.v of chunk m is
+            // formed and the output of chunk m-2 has been read
             auto mma0_ready = [&](int m) {
-                return mbar_try_wait(wv_ready + (m & 1), (m >> 1) & 1) && mbar_try_wait(full_pre + (m & 1), (m >> 1) & 1);
+                const int st = m & 1, ph = (m >> 1) & 1;
+                return mbar_test_wait(wv_ready + st, ph) && mbar_test_wait(full_pre + st, ph) &&
+                       mbar_test_wait(o_free + st, ph);
             };
             auto mma0 = [&](int m) -> bool {
-                const int st = m & 1;
-                if (!mbar_wait_or_abort(wv_ready + st, (m >> 1) & 1, wait_ns, err) ||
-                    !mbar_wait_or_abort(full_pre + st, (m >> 1) & 1, wait_ns, err))
+                const int st = m & 1, ph = (m >> 1) & 1;
+                if (!mbar_wait_or_abort(wv_ready + st, ph, wait_ns, err) ||
+                    !mbar_wait_or_abort(full_pre + st, ph, wait_ns, err) ||
+                    !mbar_wait_or_abort(o_free + st, ph, wait_ns, err))
                     return false;
                 tc_fence_after();
-                const uint32_t pre = ss::PRE0 + st * ss::PRE;
-                const uint64_t a = desc(pre + ss::VV, 8192), b = desc(pre + ss::TT, 16);
+                const uint64_t a = desc(ss::PRE0 + st * ss::PRE + ss::VV, 8192), b = desc(ss::TZ + 8192 * st, 16);
 #pragma unroll
                 for (int s = 0; s < 4; ++s)
                     mma_bf16(tmem + ss::kDuo + 128 * st, a + (s * 2048 >> 4), b + (s * 32 >> 4), id_0, s > 0);
@@ -701,10 +713,8 @@ __global__ void __launch_bounds__(ss::kThreads, 1)
             bool run = NC > 0 && mma0(0);
             for (int n = 0; run && n < NC; ++n) {
                 const int st = n & 1;
-                const uint32_t duo = tmem + ss::kDuo + 128 * st;
                 const uint32_t big = ss::BIG0 + st * ss::BIG;
-                if (!mbar_wait_or_abort(o_free + st, (n >> 1) & 1, wait_ns, err) ||
-                    !mbar_wait_or_abort(full_big + st, (n >> 1) & 1, wait_ns, err) ||
+                if (!mbar_wait_or_abort(full_big + st, (n >> 1) & 1, wait_ns, err) ||
                     !mbar_wait_or_abort(s_ready, n & 1, wait_ns, err)) {
                     run = false;
                     break;
@@ -714,10 +724,10 @@ __global__ void __launch_bounds__(ss::kThreads, 1)
                     const uint64_t b = desc(big + ss::A1, 16);
 #pragma unroll
                     for (int s = 0; s < 8; ++s)  // K = d_k: two 64-wide blocks of 16 KB
-                        mma_bf16_ts(duo, tmem + ss::kAs + 8 * s, b + (((s >> 2) * 16384 + (s & 3) * 32) >> 4), id_uo, 1);
+                        mma_bf16_ts(tmem + ss::kDuo + 128 * st, tmem + ss::kAs + 8 * s,
+                                    b + (((s >> 2) * 16384 + (s & 3) * 32) >> 4), id_uo, 1);
                 }
                 mma_commit(mma1_done);
-                // (w.v)^T T^T of the next chunk goes in now if its w.v is ready, else after U^T M^T
                 bool next0 = n + 1 < NC;
                 if (next0 && mma0_ready(n + 1)) {
                     if (!mma0(n + 1)) {
@@ -739,7 +749,7 @@ __global__ void __launch_bounds__(ss::kThreads, 1)
                     mma_commit(s_done);
 #pragma unroll
                     for (int s = 0; s < 4; ++s)
-                        mma_bf16_ts(duo + 64, tmem + ss::kAu + 8 * s, bm + (s * 32 >> 4), id_o, 1);
+                        mma_bf16_ts(tmem + ss::kDuo + ss::o_col(st), tmem + ss::kAu + 8 * s, bm + (s * 32 >> 4), id_o, 1);
                     mma_commit(o_done + st);
                     mma_commit(empty_big + st);
                 }
@@ -754,81 +764,22 @@ __global__ void __launch_bounds__(ss::kThreads, 1)
             mbar_wait(drain, 0, kDefaultWaitNs);
         }
     } else if (warp >= ss::kChainWarps) {
-        // ======================= output read-out (warps 8-11) =======================
+        // ================== output read-out and w.v (warps 8-11) ===================
         const int q4 = warp & 3;  // TMEM lane quarter = d_v rows 32*q4 ..
+        const int otid = tid - 32 * ss::kChainWarps;  // 0..127
         const uint32_t lane_base = static_cast<uint32_t>(32 * q4) << 16;
         uint8_t* stg = sm + ss::OST + q4 * 4096;  // [64 tokens][32 d_v] bf16, 64-byte rows
-        bool ok = NC > 0;
-        if (ok) {
-            float z[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) z[i] = 0.f;
-#pragma unroll
-            for (int b = 0; b < 2; ++b)
-#pragma unroll
-                for (int c = 0; c < 64; c += 16) tmem_st_f32x16(tmem + lane_base + ss::kDuo + 128 * b + 64 + c, z);
-            tmem_st_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) {
-                mbar_arrive1(o_free);
-                mbar_arrive1(o_free + 1);
-            }
-        }
-        for (int m = 0; ok && m < NC; ++m) {
+        // e^{G_last} of chunk m (kept for the state read-out after the slot is refilled), and w.v in
+        // place of v (both tiles carry the same swizzle, so the product is position-wise)
+        auto take_pre = [&](int m) -> bool {
             const int st = m & 1;
-            if (!(ok = warp_wait(o_done + st, (m >> 1) & 1, wait_ns, err))) break;
-            tc_fence_after();
-            if (lane == 0) bulk_wait_read_all();  // the previous chunk's store has read the staging
-            __syncwarp();
-#pragma unroll
-            for (int c0 = 0; c0 < 64; c0 += 32) {
-                float x[32];
-                tmem_ld_cols<2>(tmem + lane_base + ss::kDuo + 128 * st + 64 + c0, x);
-#pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    *reinterpret_cast<__nv_bfloat16*>(stg + (c0 + j) * 64 + lane * 2) = __float2bfloat16_rn(scale * x[j]);
-            }
-            {
-                float z[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) z[i] = 0.f;
-#pragma unroll
-                for (int c = 0; c < 64; c += 16) tmem_st_f32x16(tmem + lane_base + ss::kDuo + 128 * st + 64 + c, z);
-                tmem_st_wait();
-                tc_fence_before();
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-                mbar_arrive1(o_free + st);
-                // rows past T are clipped by the tensor map
-                tma_store_4d(&maps.o_st, stg, 32 * q4, hv, m * kC, bi);
-                bulk_commit();
-            }
-        }
-        if (lane == 0) bulk_wait_all();  // the output is written before the block retires
-    } else {
-        // ================== w.v, U and state read-outs (warps 0-7) ==================
-        const int q4 = warp & 3, half = warp >> 2;  // TMEM lane quarter; column half
-        const int v = 32 * q4 + lane;                // d_v row (= TMEM lane)
-        const uint32_t lane_base = static_cast<uint32_t>(32 * q4) << 16;
-        auto arrive = [&](uint64_t* bar) {
-            __syncwarp();
-            if (lane == 0) mbar_arrive1(bar);
-        };
-        // e^{G_last} of chunk m for this warp's 64 d_k columns, and w.v in place of v (both tiles
-        // carry the same swizzle, so the product is position-wise)
-        auto take_pre = [&](int m) {
-            const int st = m & 1;
+            if (!warp_wait(full_pre + st, (m >> 1) & 1, wait_ns, err)) return false;
             uint8_t* sbp = sm + ss::PRE0 + st * ss::PRE;
-            float* gc = reinterpret_cast<float*>(sm + ss::GAMC) + (st * ss::kChainWarps + warp) * 64;
-            const float* gs = reinterpret_cast<const float*>(sbp + ss::GAM) + 64 * half;
-            gc[lane] = gs[lane];
-            gc[lane + 32] = gs[lane + 32];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const uint32_t off = (tid + 256 * i) * 16;  // 1024 chunks of 16 bytes
+            reinterpret_cast<float*>(sm + ss::GAMC)[(m & 3) * 128 + otid] =
+                reinterpret_cast<const float*>(sbp + ss::GAM)[otid];
+#pragma unroll 4
+            for (int i = 0; i < 8; ++i) {
+                const uint32_t off = (otid + 128 * i) * 16;  // 1024 chunks of 16 bytes
                 float a[8], bw[8];
                 unpack8(*reinterpret_cast<const uint4*>(sbp + ss::VV + off), a);
                 unpack8(*reinterpret_cast<const uint4*>(sbp + ss::WW + off), bw);
@@ -837,12 +788,59 @@ __global__ void __launch_bounds__(ss::kThreads, 1)
                 *reinterpret_cast<uint4*>(sbp + ss::VV + off) = pack8(a);
             }
             fence_proxy_async_smem();
-            arrive(wv_ready + st);
+            __syncwarp();
+            if (lane == 0) mbar_arrive1(wv_ready + st);
+            return true;
         };
-        // D_S = e^{G_last(m)} . S^T (x holds this thread's 64 columns of S^T)
-        auto decay_into_ds = [&](int m, float (&x)[64]) {
+        bool ok = NC > 0;
+        if (ok) {
+            if (lane == 0) {  // nothing to read before the first two chunks
+                mbar_arrive1(o_free);
+                mbar_arrive1(o_free + 1);
+            }
+            ok = take_pre(0) && (NC < 2 || take_pre(1));
+        }
+        for (int m = 0; ok && m < NC; ++m) {
+            const int st = m & 1;
+            if (!(ok = warp_wait(o_done + st, (m >> 1) & 1, wait_ns, err))) break;
+            tc_fence_after();
+            if (lane == 0) bulk_wait_read_all();  // the previous chunk's store has read the staging
+            __syncwarp();
+            {
+                float x[64];
+                tmem_ld_cols<4>(tmem + lane_base + ss::kDuo + ss::o_col(st), x);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive1(o_free + st);
+#pragma unroll
+                for (int j = 0; j < 64; ++j)
+                    *reinterpret_cast<__nv_bfloat16*>(stg + j * 64 + lane * 2) = __float2bfloat16_rn(scale * x[j]);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                // rows past T are clipped by the tensor map
+                tma_store_4d(&maps.o_st, stg, 32 * q4, hv, m * kC, bi);
+                bulk_commit();
+            }
+            if (m + 2 < NC && !(ok = take_pre(m + 2))) break;
+        }
+        if (lane == 0) bulk_wait_all();  // the output is written before the block retires
+    } else {
+        // ===================== U and state read-outs (warps 0-7) =====================
+        const int q4 = warp & 3, half = warp >> 2;  // TMEM lane quarter; column half
+        const int v = 32 * q4 + lane;                // d_v row (= TMEM lane)
+        const uint32_t lane_base = static_cast<uint32_t>(32 * q4) << 16;
+        auto arrive = [&](uint64_t* bar) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive1(bar);
+        };
+        // D_S = e^{G_last(m)} . S^T for this thread's 64 columns (the copy of the decay is in place
+        // once w.v of chunk m has been formed)
+        auto decay_into_ds = [&](int m, float (&x)[64]) -> bool {
+            if (!warp_wait(wv_ready + (m & 1), (m >> 1) & 1, wait_ns, err)) return false;
             const float4* g4 = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(sm + ss::GAMC) +
-                                                               ((m & 1) * ss::kChainWarps + warp) * 64);
+                                                               (m & 3) * 128 + 64 * half);
 #pragma unroll
             for (int j4 = 0; j4 < 16; ++j4) {
                 const float4 gg = g4[j4];
@@ -853,47 +851,32 @@ __global__ void __launch_bounds__(ss::kThreads, 1)
             }
 #pragma unroll
             for (int c = 0; c < 64; c += 16) tmem_st_f32x16(tmem + lane_base + ss::kDs + 64 * half + c, x + c);
+            tmem_st_wait();
+            tc_fence_before();
+            return true;
         };
         bool ok = NC > 0;
-        if (ok && (ok = warp_wait(full_pre, 0, wait_ns, err))) {
-            take_pre(0);
+        if (ok) {
             float x[64];
             const float* src = s0 ? s0 + (static_cast<size_t>(bh) * kD + 64 * half) * kD + v : nullptr;
 #pragma unroll
             for (int j = 0; j < 64; ++j) x[j] = src ? src[j * kD] : 0.f;
             tmem_st_bf16x32(tmem + lane_base + ss::kAs + 32 * half, x);
             tmem_st_bf16x32(tmem + lane_base + ss::kAs + 32 * half + 16, x + 32);
-            decay_into_ds(0, x);
-            tmem_st_wait();
-            tc_fence_before();
-            arrive(s_ready);
+            ok = decay_into_ds(0, x);
+            if (ok) arrive(s_ready);
         }
         for (int n = 0; ok && n < NC; ++n) {
             const int st = n & 1;
-            // w.v of chunk n+1 while S^T [-W ; Q]^T of chunk n runs, if its slot has landed
-            bool pre_done = n + 1 >= NC;
-            if (!pre_done) {
-                int ready = 0;
-                if (lane == 0) ready = mbar_try_wait(full_pre + ((n + 1) & 1), ((n + 1) >> 1) & 1) ? 1 : 0;
-                if (__shfl_sync(0xffffffffu, ready, 0)) {
-                    mbar_wait(full_pre + ((n + 1) & 1), ((n + 1) >> 1) & 1, kDefaultWaitNs);
-                    take_pre(n + 1);
-                    pre_done = true;
-                }
-            }
             if (!(ok = warp_wait(mma1_done, n & 1, wait_ns, err))) break;
             tc_fence_after();
             {  // U^T: this thread's 32 token columns -> bf16 A operand
                 float x[32];
-                tmem_ld_cols<2>(tmem + lane_base + ss::kDuo + 128 * st + 32 * half, x);
+                tmem_ld_cols<2>(tmem + lane_base + ss::kDuo + ss::u_col(st) + 32 * half, x);
                 tmem_st_bf16x32(tmem + lane_base + ss::kAu + 16 * half, x);
                 tmem_st_wait();
                 tc_fence_before();
                 arrive(u_ready);
-            }
-            if (!pre_done) {
-                if (!(ok = warp_wait(full_pre + ((n + 1) & 1), ((n + 1) >> 1) & 1, wait_ns, err))) break;
-                take_pre(n + 1);
             }
             if (!(ok = warp_wait(s_done, n & 1, wait_ns, err))) break;
             tc_fence_after();
@@ -905,9 +888,8 @@ __global__ void __launch_bounds__(ss::kThreads, 1)
             tc_fence_before();
             arrive(s_ready);
             if (n + 1 < NC) {
-                decay_into_ds(n + 1, x);  // ordered before U^T K^ of chunk n+1 by the next U hand-off
-                tmem_st_wait();
-                tc_fence_before();
+                // ordered before U^T K^ of chunk n+1 by the next U hand-off
+                if (!(ok = decay_into_ds(n + 1, x))) break;
             } else if (sT_out) {
                 float* dst = sT_out + (static_cast<size_t>(bh) * kD + 64 * half) * kD + v;
 #pragma unroll
