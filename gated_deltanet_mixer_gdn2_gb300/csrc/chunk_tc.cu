@@ -474,9 +474,9 @@ struct StateMaps {
 
 namespace ss {
 // Shared memory (every tile 1024-byte aligned): two rings of two slots, "big" for what the products
-// of chunk n read during step n, "pre" for what is used one step ahead (w.v, the chunk decay), so
-// each slot is released as soon as its last reader is done; the T tiles of the two chunk parities
-// sit around one zero tile.
+// of chunk n read during step n, "pre" for what is used one step ahead (w.v), so each slot is
+// released as soon as its last reader is done; the T tiles of the two chunk parities sit around one
+// zero tile; the chunk decays have a ring of four of their own.
 constexpr uint32_t A1 = 0;          // big: [-W ; Q] (even chunks) or [Q ; -W] (odd chunks): two 64-wide
                                     //      K (d_k) blocks of [128 rows (token)][128 B]
 constexpr uint32_t KH = 32768;      // big: k.e^{G_last-G} token-major, two 64-wide d_k blocks (MN-major B)
@@ -484,15 +484,14 @@ constexpr uint32_t MM = 49152;      // big: M [64 tokens][64 tokens] (K-major B)
 constexpr uint32_t BIG = 57344;     // big slot size
 constexpr uint32_t VV = 0;          // pre: v tile [64 tokens][128 d_v] as two 64-wide blocks; w.v in place
 constexpr uint32_t WW = 16384;      // pre: w tile, same layout
-constexpr uint32_t GAM = 32768;     // pre: e^{G_last} fp32 [128]
-constexpr uint32_t PRE = 33792;     // pre slot size
+constexpr uint32_t PRE = 32768;     // pre slot size
 constexpr uint32_t TX_BIG = 2 * 16384 + 16384 + 8192;
-constexpr uint32_t TX_PRE = 8192 + 2 * 16384 + 512;
+constexpr uint32_t TX_PRE = 8192 + 2 * 16384;
 constexpr uint32_t BIG0 = 0;
 constexpr uint32_t TZ = 2 * BIG;            // T (even chunk) | zeros | T (odd chunk), [64][64] bf16 each:
                                             // as N = 128 K-major B operands, [T ; 0] and [0 ; T]
 constexpr uint32_t PRE0 = TZ + 3 * 8192;
-constexpr uint32_t GAMC = PRE0 + 2 * PRE;   // copies of e^{G_last}: [4 chunks][128] fp32
+constexpr uint32_t GAMC = PRE0 + 2 * PRE;   // ring of e^{G_last}: [4 chunks][128] fp32, own barriers
 constexpr uint32_t OST = GAMC + 2048;       // output staging: [4 warps][64 tokens][32 d_v] bf16
 constexpr uint32_t BAR = OST + 16384;       // mbarriers, TMEM base, error flag
 constexpr uint32_t TOTAL = BAR + 256;
@@ -597,6 +596,7 @@ __global__ void __launch_bounds__(ss::kThreads, 1)
     uint64_t* u_ready = full_big + 16;                               // U^T written, D_S decayed (8 warps)
     uint64_t* s_ready = full_big + 17;                               // S^T written (8 chain warps)
     uint64_t* drain = full_big + 18;
+    uint64_t* gam_full = full_big + 19;                              // [4] e^{G_last} of chunk m landed
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + ss::BAR + 224);
     volatile int* err = reinterpret_cast<volatile int*>(sm + ss::BAR + 228);
 
@@ -617,6 +617,7 @@ __global__ void __launch_bounds__(ss::kThreads, 1)
         mbar_init(u_ready, ss::kChainWarps);
         mbar_init(s_ready, ss::kChainWarps);
         mbar_init(drain, 1);
+        for (int i = 0; i < 4; ++i) mbar_init(gam_full + i, 1);
         *err = 0;
         fence_mbar_init();
     }
@@ -649,7 +650,10 @@ __global__ void __launch_bounds__(ss::kThreads, 1)
                     tma_load_4d(sb + ss::VV + kb * 8192, &maps.v, 64 * kb, hv, m * kC, bi, full_pre + st);
                     tma_load_4d(sb + ss::WW + kb * 8192, &maps.wg, 64 * kb, hv, m * kC, bi, full_pre + st);
                 }
-                bulk_load(sb + ss::GAM, ws + static_cast<size_t>(u) * kWsUnit + kWsGam, 512, full_pre + st);
+                // the decay of chunk m-4 has been applied once pre(m-2) was consumed
+                mbar_arrive_expect_tx(gam_full + (m & 3), 512);
+                bulk_load(sm + ss::GAMC + (m & 3) * 512, ws + static_cast<size_t>(u) * kWsUnit + kWsGam, 512,
+                          gam_full + (m & 3));
                 pre_issued = m;
                 return true;
             };
@@ -677,6 +681,8 @@ __global__ void __launch_bounds__(ss::kThreads, 1)
                 if (m >= 0) mbar_wait(full_big + (m & 1), (m >> 1) & 1, kDefaultWaitNs);
             for (int m = pre_issued - 1; m <= pre_issued; ++m)
                 if (m >= 0) mbar_wait(full_pre + (m & 1), (m >> 1) & 1, kDefaultWaitNs);
+            for (int m = pre_issued - 3; m <= pre_issued; ++m)
+                if (m >= 0) mbar_wait(gam_full + (m & 3), (m >> 2) & 1, kDefaultWaitNs);
         }
     } else if (warp == ss::kIssuer) {
         // ================================ MMA warp ================================
@@ -769,15 +775,12 @@ __global__ void __launch_bounds__(ss::kThreads, 1)
         const int otid = tid - 32 * ss::kChainWarps;  // 0..127
         const uint32_t lane_base = static_cast<uint32_t>(32 * q4) << 16;
         uint8_t* stg = sm + ss::OST + q4 * 4096;  // [64 tokens][32 d_v] bf16, 64-byte rows
-        // e^{G_last} of chunk m (kept for the state read-out after the slot is refilled), and w.v in
-        // place of v (both tiles carry the same swizzle, so the product is position-wise)
+        // w.v in place of v (both tiles carry the same swizzle, so the product is position-wise)
         auto take_pre = [&](int m) -> bool {
             const int st = m & 1;
             if (!warp_wait(full_pre + st, (m >> 1) & 1, wait_ns, err)) return false;
             uint8_t* sbp = sm + ss::PRE0 + st * ss::PRE;
-            reinterpret_cast<float*>(sm + ss::GAMC)[(m & 3) * 128 + otid] =
-                reinterpret_cast<const float*>(sbp + ss::GAM)[otid];
-#pragma unroll 4
+#pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const uint32_t off = (otid + 128 * i) * 16;  // 1024 chunks of 16 bytes
                 float a[8], bw[8];
@@ -835,10 +838,9 @@ __global__ void __launch_bounds__(ss::kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive1(bar);
         };
-        // D_S = e^{G_last(m)} . S^T for this thread's 64 columns (the copy of the decay is in place
-        // once w.v of chunk m has been formed)
+        // D_S = e^{G_last(m)} . S^T for this thread's 64 columns
         auto decay_into_ds = [&](int m, float (&x)[64]) -> bool {
-            if (!warp_wait(wv_ready + (m & 1), (m >> 1) & 1, wait_ns, err)) return false;
+            if (!warp_wait(gam_full + (m & 3), (m >> 2) & 1, wait_ns, err)) return false;
             const float4* g4 = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(sm + ss::GAMC) +
                                                                (m & 3) * 128 + 64 * half);
 #pragma unroll
