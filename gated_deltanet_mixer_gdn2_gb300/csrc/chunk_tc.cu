@@ -257,7 +257,7 @@ __global__ void __launch_bounds__(fs::kThreads, 3)
         }
         __syncthreads();
         {
-            float pre[8], anc[8], ea[8], ela[8];
+            float pa[8], ea[8], ela[8];  // per channel: G_{group start} - a, e^{a}, e^{G_last - a}
             {
                 const float4* p4 = reinterpret_cast<const float4*>(s_gs + tg * 128 + 8 * j);
                 const float4* a4 = reinterpret_cast<const float4*>(s_anc + 8 * j);
@@ -266,41 +266,52 @@ __global__ void __launch_bounds__(fs::kThreads, 3)
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     const float4 pp = p4[h], aa = a4[h], ee = e4[h], ll = l4[h];
-                    pre[4 * h] = pp.x; pre[4 * h + 1] = pp.y; pre[4 * h + 2] = pp.z; pre[4 * h + 3] = pp.w;
-                    anc[4 * h] = aa.x; anc[4 * h + 1] = aa.y; anc[4 * h + 2] = aa.z; anc[4 * h + 3] = aa.w;
+                    pa[4 * h] = pp.x - aa.x; pa[4 * h + 1] = pp.y - aa.y; pa[4 * h + 2] = pp.z - aa.z; pa[4 * h + 3] = pp.w - aa.w;
                     ea[4 * h] = ee.x; ea[4 * h + 1] = ee.y; ea[4 * h + 2] = ee.z; ea[4 * h + 3] = ee.w;
                     ela[4 * h] = ll.x; ela[4 * h + 1] = ll.y; ela[4 * h + 2] = ll.z; ela[4 * h + 3] = ll.w;
                 }
             }
+            // each output is formed and stored before the next one, so that few values are live
 #pragma unroll
             for (int r = 0; r < 4; ++r) {
                 const int t = 4 * tg + r;
                 const int o = off(t);
-                float kk[8], qq[8], bb[8];
-                unpack8(*reinterpret_cast<const uint4*>(pK + o), kk);
-                unpack8(*reinterpret_cast<const uint4*>(pQ + o), qq);
-                unpack8(*reinterpret_cast<const uint4*>(pB + o), bb);
-                float o_kb[8], o_qa[8], o_kt[8], o_kg[8], qb[8], kh[8];
+                float e1[8], e2[8], kk[8], y[8];
+                {
+                    float bb[8];
+                    unpack8(*reinterpret_cast<const uint4*>(pK + o), kk);
+                    unpack8(*reinterpret_cast<const uint4*>(pB + o), bb);
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const float Gi = pre[i] + L[r][i];
-                    const float e1 = __expf(Gi - anc[i]);   // e^{G - a}
-                    const float e2 = __expf(anc[i] - Gi);   // e^{a - G}
-                    const float bk = bb[i] * kk[i];
-                    o_kb[i] = bk * e1;
-                    o_qa[i] = qq[i] * e1;
-                    o_kt[i] = kk[i] * e2;
-                    o_kg[i] = bk * (e1 * ea[i]);            // b.k.e^{G}
-                    qb[i] = qq[i] * (e1 * ea[i]);            // q.e^{G}
-                    kh[i] = kk[i] * (e2 * ela[i]);           // k.e^{G_last - G}
+                    for (int i = 0; i < 8; ++i) {
+                        const float d = pa[i] + L[r][i];   // G - a
+                        e1[i] = __expf(d);                 // e^{G - a}
+                        e2[i] = __expf(-d);                // e^{a - G}
+                        bb[i] *= kk[i];                    // b.k
+                    }
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) y[i] = bb[i] * e1[i];
+                    *reinterpret_cast<uint4*>(pB + o) = pack8(y);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) y[i] = bb[i] * (e1[i] * ea[i]);  // b.k.e^{G}
+                    *reinterpret_cast<uint4*>(pG + o) = pack8(y);   // in place of g (same thread, same chunk)
                 }
-                *reinterpret_cast<uint4*>(pB + o) = pack8(o_kb);
-                *reinterpret_cast<uint4*>(pQ + o) = pack8(o_qa);
-                *reinterpret_cast<uint4*>(pK + o) = pack8(o_kt);
-                *reinterpret_cast<uint4*>(pG + o) = pack8(o_kg);   // in place of g (same thread, same chunk)
-                // decayed q and k, token-major rows of 256 bytes: one 16-byte chunk per thread
-                *reinterpret_cast<uint4*>(unit + kWsQb + t * 256 + j * 16) = pack8(qb);
-                *reinterpret_cast<uint4*>(unit + kWsKh + t * 256 + j * 16) = pack8(kh);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) y[i] = kk[i] * e2[i];
+                *reinterpret_cast<uint4*>(pK + o) = pack8(y);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) y[i] = kk[i] * (e2[i] * ela[i]);      // k.e^{G_last - G}
+                *reinterpret_cast<uint4*>(unit + kWsKh + t * 256 + j * 16) = pack8(y);
+                {
+                    float qq[8];
+                    unpack8(*reinterpret_cast<const uint4*>(pQ + o), qq);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) y[i] = qq[i] * e1[i];
+                    *reinterpret_cast<uint4*>(pQ + o) = pack8(y);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) y[i] = qq[i] * (e1[i] * ea[i]);  // q.e^{G}
+                    // decayed q and k, token-major rows of 256 bytes: one 16-byte chunk per thread
+                    *reinterpret_cast<uint4*>(unit + kWsQb + t * 256 + j * 16) = pack8(y);
+                }
             }
         }
         fence_proxy_async_smem();
@@ -438,14 +449,18 @@ __global__ void __launch_bounds__(fs::kThreads, 3)
             const int q4 = warp & 3, half = warp >> 2;
             if (q4 < 2) {  // token t = lane row; this thread's 64 channels -> swizzled W staging tile `half`
                 const int t = 32 * q4 + lane;
-                float x[64];
-                tmem_ld_cols<4>(tmem + (static_cast<uint32_t>(32 * q4) << 16) + 64 * half, x);
 #pragma unroll
-                for (int c8 = 0; c8 < 8; ++c8) {
-                    float y[8];
+                for (int c0 = 0; c0 < 2; ++c0) {
+                    float x[32];
+                    tmem_ld_cols<2>(tmem + (static_cast<uint32_t>(32 * q4) << 16) + 64 * half + 32 * c0, x);
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) y[e] = -x[8 * c8 + e];  // stored negated
-                    *reinterpret_cast<uint4*>(sm + fs::WSTG + half * 8192 + t * 128 + ((c8 ^ (t & 7)) << 4)) = pack8(y);
+                    for (int c4 = 0; c4 < 4; ++c4) {
+                        const int c8 = 4 * c0 + c4;
+                        float y[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) y[e] = -x[8 * c4 + e];  // stored negated
+                        *reinterpret_cast<uint4*>(sm + fs::WSTG + half * 8192 + t * 128 + ((c8 ^ (t & 7)) << 4)) = pack8(y);
+                    }
                 }
             }
             fence_proxy_async_smem();
