@@ -34,9 +34,9 @@ FLUSH_BYTES = 256 << 20  # > 129 MB L2
 
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one gdn2_chunk_fwd on this
-# workload, from a single-pass ncu capture of factors_tc + state_tc (profiles/traffic_prefill32k.md).
-# Reported only while the tensor-core kernel source is the one that was measured.
-TRAFFIC_RECORD = {"chunk_tc_sha256_16": "80cbe589cc9d18b5", "bytes": 1677608960 + 2112474112 + 3238073600 + 524748800}
+# workload, from a single-pass ncu capture of factors_tc + state_tc. Reported only while the
+# tensor-core kernel source is the one that was measured.
+TRAFFIC_RECORD = {"chunk_tc_sha256_16": "39f86be5734abf68", "bytes": 1725676032 + 2194833664 + 3238155776 + 523586304}
 
 
 def recorded_traffic():
