@@ -24,7 +24,7 @@ EXPORTS = (
     "gdn2_status_string", "gdn2_version", "gdn2_chunk_fwd_workspace_size",
     "gdn2_chunk_fwd_workspace_size_path", "gdn2_chunk_fwd", "gdn2_chunk_fwd_path",
     "gdn2_recurrent_step", "gdn2_last_device_status", "gdn2_set_wait_limit", "gdn2_selftest_umma",
-    "gdn2_chunk_fwd_noalloc", "gdn2_recurrent_update",
+    "gdn2_chunk_fwd_noalloc", "gdn2_recurrent_update", "gdn2_fg2_inputs",
 )
 
 
@@ -54,6 +54,7 @@ def _load() -> ctypes.CDLL:
         "gdn2_selftest_umma": (I, [I, I, P, P, P, P]),
         "gdn2_chunk_fwd_noalloc": (I, [P] * 9 + [I] * 7 + [F, I, P]),
         "gdn2_recurrent_update": (I, [P] * 7 + [I, P, I, P] + [I] * 6 + [F, I, P]),
+        "gdn2_fg2_inputs": (I, [P] * 7 + [I] * 5 + [I, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -185,6 +186,33 @@ def gdn2_recurrent_update(q, k, v, g, b, w, state, o, slots=None, *, scale=1.0, 
                                    _dtype_code(q), _stream(stream))
     _check(st, "gdn2_recurrent_update")
     return o
+
+
+def gdn2_fg2_inputs(q, k, beta, q_out, k_out, b_out, w_out, *, stream=None):
+    """FG^2-GDN inputs for the GDN-2 core (C ABI gdn2_fg2_inputs): writes q_out, k_out = sqrt(beta).k,
+    b_out = 1, w_out = sqrt(beta), all per value head.
+
+    q, k: [B, T, H_k, d] (or [B, H_k, d] for decode tokens); beta and the outputs: [B, T, H_v, d]
+    (or [B, H_v, d]).
+    """
+    if q.dim() == 3:
+        B, Hk, d = q.shape
+        T, Hv = 1, beta.shape[1]
+    else:
+        B, T, Hk, d = q.shape
+        Hv = beta.shape[2]
+    st = lib.gdn2_fg2_inputs(_ptr(q), _ptr(k), _ptr(beta), _ptr(q_out), _ptr(k_out), _ptr(b_out), _ptr(w_out),
+                             B, T, Hk, Hv, d, _dtype_code(q), _stream(stream))
+    _check(st, "gdn2_fg2_inputs")
+    return q_out, k_out, b_out, w_out
+
+
+def fg2_inputs(q, k, beta, *, stream=None):
+    """Returns (q_out, k_out, b_out, w_out) for running FG^2-GDN on the GDN-2 core (H_k = H_v)."""
+    import torch
+
+    outs = [torch.empty(beta.shape, dtype=q.dtype, device=q.device) for _ in range(4)]
+    return gdn2_fg2_inputs(q, k, beta, *outs, stream=stream)
 
 
 def gdn2_last_device_status(stream=None) -> int:

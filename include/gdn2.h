@@ -185,6 +185,28 @@ gdn2_status gdn2_last_device_status(void* stream);
 void gdn2_set_wait_limit(long long ns);
 
 /*
+ * gdn2_fg2_inputs -- FG^2-GDN as GDN-2 inputs ("FG^2-GDN: Enhancing Long-Context Gated Delta
+ * Networks with Doubly Fine-Grained Control", section 2.A, "FG2-GDN: Tasa de Aprendizaje
+ * Vectorial"). FG^2-GDN absorbs a per-channel learning rate beta_t (d values, >= 0) into key and
+ * value, k~ = sqrt(beta) . k and v~ = sqrt(beta) . v, and updates
+ *     S_t = (I - k~ k~^T) Diag(alpha_t) S_{t-1} + k~ v~^T.
+ * That is the GDN-2 recurrence with k <- sqrt(beta) . k, b <- 1, w <- sqrt(beta) (d_k = d_v = d).
+ * This call writes, for every value head h: q_out = q of key head floor(h * H_k / H_v),
+ * k_out = sqrt(beta) . (that head's k), b_out = 1, w_out = sqrt(beta). Then run gdn2_chunk_fwd or
+ * gdn2_recurrent_update with H_k = H_v on (q_out, k_out, v, g, b_out, w_out).
+ *
+ * q, k: [B, T, H_k, d]; beta: [B, T, H_v, d]; q_out, k_out, b_out, w_out: [B, T, H_v, d] (caller-
+ * owned device buffers, distinct from the inputs); all of dtype dt. For decode tokens [B, H, d]
+ * pass T = 1. d must be a multiple of 8; pointers 16-byte aligned. beta < 0 is not checked (its
+ * square root is NaN). Asynchronous on `stream`.
+ * Errors: GDN2_ERR_INVALID_ARG (dtype, sizes <= 0 or negative, H_v % H_k, null pointer),
+ * GDN2_ERR_UNSUPPORTED (d % 8, too large), GDN2_ERR_MISALIGNED, GDN2_ERR_CUDA (launch failed).
+ */
+gdn2_status gdn2_fg2_inputs(const void* q, const void* k, const void* beta, void* q_out, void* k_out,
+                            void* b_out, void* w_out, int B, int T, int Hk, int Hv, int d, gdn2_dtype dt,
+                            void* stream);
+
+/*
  * gdn2_selftest_umma -- diagnostics: one tcgen05 product D[128][N] = A * B (bf16 in, fp32 out)
  * with the operand layouts the tensor-core chunked kernels use, so that a test can check them
  * against a host matrix product. The operands are row-major bf16 device arrays:

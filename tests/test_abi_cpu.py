@@ -130,3 +130,16 @@ def test_recurrent_update_argument_errors(g):
     assert f(dk=48) == g.GDN2_ERR_UNSUPPORTED
     assert f(p=None) == g.GDN2_ERR_INVALID_ARG
     assert f(N=0, p=None) == g.GDN2_OK
+
+
+def test_fg2_inputs_argument_errors(g):
+    P = lambda a: ctypes.c_void_p(a) if a else None
+    f = lambda ptr=0x10000, B=1, T=4, Hk=1, Hv=2, d=128, dt=1: g.lib.gdn2_fg2_inputs(
+        *(P(ptr),) * 7, B, T, Hk, Hv, d, dt, None)
+    assert f(B=0) == g.GDN2_OK                                   # nothing to do, nothing launched
+    assert f(ptr=0) == g.GDN2_ERR_INVALID_ARG
+    assert f(Hk=3, Hv=4) == g.GDN2_ERR_INVALID_ARG
+    assert f(dt=5) == g.GDN2_ERR_INVALID_ARG
+    assert f(T=-1) == g.GDN2_ERR_INVALID_ARG
+    assert f(d=12) == g.GDN2_ERR_UNSUPPORTED
+    assert f(ptr=0x10008) == g.GDN2_ERR_MISALIGNED
