@@ -244,6 +244,7 @@ def run_ours(args, rank, world, device):
     d_ms = statistics.mean(dec_ms) / D
 
     decode_line = decode_roofline(g, device, hbm) if rank == 0 and not args.no_decode_workload else None
+    next_rows = next_rows_rooflines(g, device, hbm, wl) if rank == 0 and not args.no_decode_workload else None
 
     # end to end through the public API with host buffers (inputs H2D, results D2H every step)
     e2e = None
@@ -274,6 +275,8 @@ def run_ours(args, rank, world, device):
     }
     if decode_line:
         line["decode"] = decode_line
+    if next_rows:
+        line["next_rows"] = next_rows
     if e2e:
         line["e2e"] = e2e
     return line
@@ -319,10 +322,64 @@ def decode_roofline(g, device, hbm):
     us = e0.elapsed_time(e1) * 1e3 / (reps * steps)
     b = decode_step_bytes(B, Hk, Hv, dk, dv)
     gbs = b / (us * 1e-6) / 1e9
-    return {"workload": f"{DECODE_WORKLOAD}: {wl.description}", "kernel": "recurrent_step_kernel",
+    return {"workload": f"{DECODE_WORKLOAD}: {wl.description}", "kernel": "recurrent_stream_kernel (gdn2_recurrent_step)",
             "us_per_step": round(us, 2), "bytes_per_step": b, "achieved": round(gbs, 1), "peak": hbm,
             "unit": "GB/s", "frac": round(gbs / hbm, 4), "bound": "hbm",
             "l2": "state 201 MB > L2; 256 back-to-back steps"}
+
+
+def next_rows_rooflines(g, device, hbm, wl):
+    """The widened rows on the bench workload's shapes, each HBM-bound: the fused mixer prologue and
+    epilogue, and the FG^2-GDN input transform. Algorithmic bytes = every tensor read once and
+    written once; inputs are GBs (> L2), timed with CUDA events over back-to-back calls."""
+    import torch
+
+    B, T, Hk, Hv, d = wl.B, wl.T, wl.Hk, wl.Hv, wl.dk
+    bf = torch.bfloat16
+    gen = torch.Generator(device=device)
+    gen.manual_seed(1234)
+    rnd = lambda *s: torch.randn(s, generator=gen, device=device).to(bf)
+    xq, xk, xv = rnd(B, T, Hk, d), rnd(B, T, Hk, d), rnd(B, T, Hv, d)
+    ag, ab, aw = rnd(B, T, Hv, d), rnd(B, T, Hv, d), rnd(B, T, Hv, d)
+    cw = [torch.randn((n, 4), generator=gen, device=device) * 0.5 for n in (Hk * d, Hk * d, Hv * d)]
+    states = [torch.zeros((B, 3, n), device=device) for n in (Hk * d, Hk * d, Hv * d)]
+    outs = [torch.empty_like(t) for t in (xq, xk, xv, ag, ab, aw)]
+    z, o = rnd(B, T, Hv, d), rnd(B, T, Hv, d)
+    wt = torch.ones(d, device=device)
+    y = torch.empty_like(o)
+    f_outs = [torch.empty((B, T, Hv, d), dtype=bf, device=device) for _ in range(4)]
+    stream = torch.cuda.current_stream(device)
+    tok = B * T
+    e = 2  # bytes per bf16 element
+    calls = {
+        "mixer_prologue": (lambda: g.gdn2_mixer_prologue(xq, xk, xv, *cw, ag, ab, aw, *outs, states=states),
+                           2 * tok * (2 * Hk * d + 4 * Hv * d) * e + sum(c.numel() for c in cw) * 4
+                           + 2 * sum(s_.numel() for s_ in states) * 4,
+                           "gdn2_mixer_prologue (prologue_kernel + conv_state_kernel)"),
+        "mixer_epilogue": (lambda: g.gdn2_mixer_epilogue(o, z, wt, y), 3 * tok * Hv * d * e + d * 4,
+                           "gdn2_mixer_epilogue (epilogue_kernel)"),
+        "fg2_inputs": (lambda: g.gdn2_fg2_inputs(xq, xk, ag, *f_outs), (2 * Hk + 5 * Hv) * tok * d * e,
+                       "gdn2_fg2_inputs (fg2_inputs_kernel)"),
+    }
+    res = {}
+    for name, (fn, nbytes, kernel) in calls.items():
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize(device)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = 5
+        e0.record(stream)
+        for _ in range(reps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize(device)
+        ms = e0.elapsed_time(e1) / reps
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        res[name] = {"kernel": kernel, "ms": round(ms, 4), "algorithmic_bytes": int(nbytes),
+                     "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s", "frac": round(gbs / hbm, 4),
+                     "bound": "hbm"}
+    res["shape"] = f"B={B} T={T} H_k={Hk} H_v={Hv} d={d} bf16 (the bench workload's token tensors)"
+    return res
 
 
 def run_variants(device):

@@ -24,7 +24,8 @@ EXPORTS = (
     "gdn2_status_string", "gdn2_version", "gdn2_chunk_fwd_workspace_size",
     "gdn2_chunk_fwd_workspace_size_path", "gdn2_chunk_fwd", "gdn2_chunk_fwd_path",
     "gdn2_recurrent_step", "gdn2_last_device_status", "gdn2_set_wait_limit", "gdn2_selftest_umma",
-    "gdn2_chunk_fwd_noalloc", "gdn2_recurrent_update", "gdn2_fg2_inputs",
+    "gdn2_chunk_fwd_noalloc", "gdn2_recurrent_update", "gdn2_fg2_inputs", "gdn2_mixer_prologue",
+    "gdn2_mixer_epilogue",
 )
 
 
@@ -55,6 +56,8 @@ def _load() -> ctypes.CDLL:
         "gdn2_chunk_fwd_noalloc": (I, [P] * 9 + [I] * 7 + [F, I, P]),
         "gdn2_recurrent_update": (I, [P] * 7 + [I, P, I, P] + [I] * 6 + [F, I, P]),
         "gdn2_fg2_inputs": (I, [P] * 7 + [I] * 5 + [I, P]),
+        "gdn2_mixer_prologue": (I, [P] * 18 + [I] * 7 + [I, P]),
+        "gdn2_mixer_epilogue": (I, [P, P, P, F, P] + [I] * 4 + [I, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -213,6 +216,40 @@ def fg2_inputs(q, k, beta, *, stream=None):
 
     outs = [torch.empty(beta.shape, dtype=q.dtype, device=q.device) for _ in range(4)]
     return gdn2_fg2_inputs(q, k, beta, *outs, stream=stream)
+
+
+def gdn2_mixer_prologue(xq, xk, xv, conv_q, conv_k, conv_v, ag, ab, aw, q, k, v, g, b, w, states=None, *,
+                        neg_eigval=False, stream=None):
+    """ShortConv + L2 norm + gate activations (C ABI gdn2_mixer_prologue). Shapes as the core's
+    inputs ([B, T, H, d], or [B, H, d] for one decode token); conv weights fp32 [H * d, 4];
+    `states`: None or (state_q, state_k, state_v) fp32 [B, 3, H * d] tensors (each may be None),
+    updated in place."""
+    if xq.dim() == 3:
+        B, Hk, dk = xq.shape
+        T, Hv, dv = 1, xv.shape[1], xv.shape[2]
+    else:
+        B, T, Hk, dk = xq.shape
+        Hv, dv = xv.shape[2], xv.shape[3]
+    sq, sk, sv = states if states is not None else (None, None, None)
+    st = lib.gdn2_mixer_prologue(*(_ptr(t) for t in (xq, xk, xv, conv_q, conv_k, conv_v, ag, ab, aw, sq, sk, sv,
+                                                    q, k, v, g, b, w)),
+                                 B, T, Hk, Hv, dk, dv, int(bool(neg_eigval)), _dtype_code(xq), _stream(stream))
+    _check(st, "gdn2_mixer_prologue")
+    return q, k, v, g, b, w
+
+
+def gdn2_mixer_epilogue(o, z, weight, y, *, eps=1e-5, stream=None):
+    """Gated RMSNorm with a SiLU gate (C ABI gdn2_mixer_epilogue); o, z, y: [B, T, H_v, d_v] (or
+    [B, H_v, d_v]); weight: fp32 [d_v]."""
+    if o.dim() == 3:
+        B, Hv, dv = o.shape
+        T = 1
+    else:
+        B, T, Hv, dv = o.shape
+    st = lib.gdn2_mixer_epilogue(_ptr(o), _ptr(z), _ptr(weight), float(eps), _ptr(y), B, T, Hv, dv,
+                                 _dtype_code(o), _stream(stream))
+    _check(st, "gdn2_mixer_epilogue")
+    return y
 
 
 def gdn2_last_device_status(stream=None) -> int:

@@ -13,41 +13,6 @@
 namespace gdn2 {
 namespace {
 
-template <typename T>
-struct Vec8;
-template <>
-struct Vec8<float> {
-    using Raw = float4[2];
-    __device__ static void load(const float* p, float (&x)[8]) {
-        const float4 a = reinterpret_cast<const float4*>(p)[0], b = reinterpret_cast<const float4*>(p)[1];
-        x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
-    }
-    __device__ static void store(float* p, const float (&x)[8]) {
-        reinterpret_cast<float4*>(p)[0] = make_float4(x[0], x[1], x[2], x[3]);
-        reinterpret_cast<float4*>(p)[1] = make_float4(x[4], x[5], x[6], x[7]);
-    }
-};
-template <>
-struct Vec8<__nv_bfloat16> {
-    __device__ static void load(const __nv_bfloat16* p, float (&x)[8]) {
-        const uint4 u = *reinterpret_cast<const uint4*>(p);
-        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float2 f = __bfloat1622float2(h[i]);
-            x[2 * i] = f.x;
-            x[2 * i + 1] = f.y;
-        }
-    }
-    __device__ static void store(__nv_bfloat16* p, const float (&x)[8]) {
-        uint4 u;
-        __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(x[2 * i], x[2 * i + 1]);
-        *reinterpret_cast<uint4*>(p) = u;
-    }
-};
-
 // One thread per 8 consecutive channels of one (row, value head); grid-stride.
 template <typename T>
 __global__ void __launch_bounds__(256) fg2_inputs_kernel(const T* __restrict__ q, const T* __restrict__ k,

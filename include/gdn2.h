@@ -207,6 +207,41 @@ gdn2_status gdn2_fg2_inputs(const void* q, const void* k, const void* beta, void
                             void* stream);
 
 /*
+ * gdn2_mixer_prologue -- the token-mixer steps between the projections and the core, in one pass
+ * (burn-gdn2 0.1.5 docs, "Architecture": projections -> ShortConv -> L2-Norm -> core; configuration
+ * table: use_short_conv, allow_neg_eigval "b x 2"; llama.cpp GDN decode study, sections 1-2: conv
+ * kernel 4, a carried state of the previous 3 samples):
+ *   q = L2norm(conv(xq)), k = L2norm(conv(xk)), v = conv(xv), with the depthwise causal conv
+ *       conv(x)_t[c] = sum_{j=0..3} W[c][j] x_{t-3+j}[c]   (samples before the call from the state)
+ *       and L2norm(x) = x / sqrt(sum x^2 + 1e-6) per (token, head);
+ *   g = -softplus(ag), b = sigmoid(ab) (x 2 when neg_eigval != 0), w = sigmoid(aw).
+ * xq, xk: [B, T, H_k, d_k]; xv: [B, T, H_v, d_v]; ag, ab: [B, T, H_v, d_k]; aw: [B, T, H_v, d_v];
+ * conv_q, conv_k: fp32 [H_k * d_k][4]; conv_v: fp32 [H_v * d_v][4] (tap 3 = current token).
+ * state_q / state_k / state_v: fp32 conv states [B][3][channels] (x_{-3}, x_{-2}, x_{-1}), read and then
+ * replaced by the last 3 samples of [state, x]; NULL = zeros in, nothing written. Outputs q, k, v, g,
+ * b, w in the core's layout, token dtype dt; they must not overlap the inputs. d_k, d_v in
+ * {16, 32, 64, 128, 256}; pointers 16-byte aligned. For decode tokens pass T = 1.
+ * Errors: GDN2_ERR_INVALID_ARG (dtype, sizes, H_v % H_k, null required pointer), GDN2_ERR_UNSUPPORTED
+ * (head size, too large), GDN2_ERR_MISALIGNED, GDN2_ERR_CUDA. Asynchronous on `stream`.
+ */
+gdn2_status gdn2_mixer_prologue(const void* xq, const void* xk, const void* xv, const float* conv_q,
+                                const float* conv_k, const float* conv_v, const void* ag, const void* ab,
+                                const void* aw, float* state_q, float* state_k, float* state_v, void* q, void* k,
+                                void* v, void* g, void* b, void* w, int B, int T, int Hk, int Hv, int dk, int dv,
+                                int neg_eigval, gdn2_dtype dt, void* stream);
+
+/*
+ * gdn2_mixer_epilogue -- gated RMSNorm with a SiLU gate after the core (burn-gdn2 0.1.5 docs,
+ * "Architecture": Gated RMS Norm <- SiLU Gate; configuration table: norm_eps 1e-5):
+ *   y = o / sqrt(mean_{d_v}(o^2) + eps) * weight * silu(z),  silu(z) = z / (1 + e^{-z}),
+ * per (token, value head). o, z, y: [B, T, H_v, d_v] of dtype dt (y may alias o); weight: fp32
+ * [d_v]. d_v in {16, 32, 64, 128, 256}; pointers 16-byte aligned. Errors as gdn2_mixer_prologue
+ * (eps < 0 or NaN is GDN2_ERR_INVALID_ARG).
+ */
+gdn2_status gdn2_mixer_epilogue(const void* o, const void* z, const float* weight, float eps, void* y, int B,
+                                int T, int Hv, int dv, gdn2_dtype dt, void* stream);
+
+/*
  * gdn2_selftest_umma -- diagnostics: one tcgen05 product D[128][N] = A * B (bf16 in, fp32 out)
  * with the operand layouts the tensor-core chunked kernels use, so that a test can check them
  * against a host matrix product. The operands are row-major bf16 device arrays:

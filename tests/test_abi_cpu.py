@@ -143,3 +143,24 @@ def test_fg2_inputs_argument_errors(g):
     assert f(T=-1) == g.GDN2_ERR_INVALID_ARG
     assert f(d=12) == g.GDN2_ERR_UNSUPPORTED
     assert f(ptr=0x10008) == g.GDN2_ERR_MISALIGNED
+
+
+def test_mixer_argument_errors(g):
+    P = lambda a: ctypes.c_void_p(a) if a else None
+    pro = lambda ptr=0x10000, B=1, T=4, Hk=1, Hv=2, dk=128, dv=128, dt=1, st=0: g.lib.gdn2_mixer_prologue(
+        *(P(ptr),) * 9, *(P(st),) * 3, *(P(ptr),) * 6, B, T, Hk, Hv, dk, dv, 0, dt, None)
+    assert pro(T=0) == g.GDN2_OK
+    assert pro(ptr=0) == g.GDN2_ERR_INVALID_ARG
+    assert pro(Hk=3, Hv=4) == g.GDN2_ERR_INVALID_ARG
+    assert pro(dt=3) == g.GDN2_ERR_INVALID_ARG
+    assert pro(dk=96) == g.GDN2_ERR_UNSUPPORTED
+    assert pro(ptr=0x10004) == g.GDN2_ERR_MISALIGNED
+    assert pro(st=0x10008) == g.GDN2_ERR_MISALIGNED
+    epi = lambda ptr=0x10000, eps=1e-5, dv=128, B=1: g.lib.gdn2_mixer_epilogue(
+        P(ptr), P(ptr), P(ptr), eps, P(ptr), B, 4, 2, dv, 1, None)
+    assert epi(B=0) == g.GDN2_OK
+    assert epi(ptr=0) == g.GDN2_ERR_INVALID_ARG
+    assert epi(eps=-1.0) == g.GDN2_ERR_INVALID_ARG
+    assert epi(eps=float("nan")) == g.GDN2_ERR_INVALID_ARG
+    assert epi(dv=48) == g.GDN2_ERR_UNSUPPORTED
+    assert epi(ptr=0x10002) == g.GDN2_ERR_MISALIGNED
