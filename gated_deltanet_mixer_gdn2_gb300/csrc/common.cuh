@@ -44,6 +44,11 @@ struct Vec8<float> {
         reinterpret_cast<float4*>(p)[0] = make_float4(x[0], x[1], x[2], x[3]);
         reinterpret_cast<float4*>(p)[1] = make_float4(x[4], x[5], x[6], x[7]);
     }
+    // through the read-only (non-coherent) path: only for data the kernel does not write
+    __device__ static void load_ro(const float* p, float (&x)[8]) {
+        const float4 a = __ldg(reinterpret_cast<const float4*>(p)), b = __ldg(reinterpret_cast<const float4*>(p) + 1);
+        x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+    }
 };
 template <>
 struct Vec8<__nv_bfloat16> {
@@ -63,6 +68,17 @@ struct Vec8<__nv_bfloat16> {
 #pragma unroll
         for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(x[2 * i], x[2 * i + 1]);
         *reinterpret_cast<uint4*>(p) = u;
+    }
+    // through the read-only (non-coherent) path: only for data the kernel does not write
+    __device__ static void load_ro(const __nv_bfloat16* p, float (&x)[8]) {
+        const uint4 u = __ldg(reinterpret_cast<const uint4*>(p));
+        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 f = __bfloat1622float2(h[i]);
+            x[2 * i] = f.x;
+            x[2 * i + 1] = f.y;
+        }
     }
 };
 
