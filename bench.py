@@ -378,6 +378,35 @@ def next_rows_rooflines(g, device, hbm, wl):
         res[name] = {"kernel": kernel, "ms": round(ms, 4), "algorithmic_bytes": int(nbytes),
                      "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s", "frac": round(gbs / hbm, 4),
                      "bound": "hbm"}
+    # backward (recurrent form, fp32 SIMT): bound by fp32 arithmetic on the B*H_v SMs it occupies
+    tk = [rnd(B, T, Hk, d), rnd(B, T, Hk, d)]
+    tk[0] = (tk[0].float() / tk[0].float().norm(dim=-1, keepdim=True)).to(bf)
+    tk[1] = (tk[1].float() / tk[1].float().norm(dim=-1, keepdim=True)).to(bf)
+    vv, do_ = rnd(B, T, Hv, d), rnd(B, T, Hv, d)
+    gg = (-torch.nn.functional.softplus(torch.randn((B, T, Hv, d), generator=gen, device=device))).to(bf)
+    bb = torch.sigmoid(torch.randn((B, T, Hv, d), generator=gen, device=device)).to(bf)
+    ww = torch.sigmoid(torch.randn((B, T, Hv, d), generator=gen, device=device)).to(bf)
+    grads = [torch.empty_like(t) for t in (tk[0], tk[1], vv, gg, bb, ww)]
+    wsb = g.lib.gdn2_backward_workspace_size(B, T, Hk, Hv, d, d, g.GDN2_BF16)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=device)
+    fn = lambda: g.gdn2_backward(tk[0], tk[1], vv, gg, bb, ww, do_, *grads, workspace=ws)
+    fn()
+    torch.cuda.synchronize(device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(2):
+        fn()
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    ms = e0.elapsed_time(e1) / 2
+    flops = 26 * d * d * tok * Hv   # forward (4 d^2 FMA) + backward (9 d^2 FMA) per token and head
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    peak_tf = sms * 128 * 2 * 2.07e9 / 1e12          # fp32 lanes x FMA x max SM clock
+    ach = flops / (ms * 1e-3) / 1e12
+    res["backward"] = {"kernel": "gdn2_backward (backward_kernel + group_sum_kernel)", "ms": round(ms, 3),
+                       "algorithmic_flops": int(flops), "achieved": round(ach, 2), "peak": round(peak_tf, 1),
+                       "unit": "TFLOP/s", "frac": round(ach / peak_tf, 4), "bound": "alu",
+                       "note": f"one CTA per (batch, value head): {B * Hv} of {sms} SMs busy"}
     res["shape"] = f"B={B} T={T} H_k={Hk} H_v={Hv} d={d} bf16 (the bench workload's token tensors)"
     return res
 

@@ -242,6 +242,26 @@ gdn2_status gdn2_mixer_epilogue(const void* o, const void* z, const float* weigh
                                 int T, int Hv, int dv, gdn2_dtype dt, void* stream);
 
 /*
+ * gdn2_backward -- gradients of the core (dq, dk, dv, dg, db, dw and the initial state) for the
+ * recurrence of the burn-gdn2 0.1.5 docs ("Architecture"), given the upstream gradient d_o of o
+ * and optionally d_final_state of S_T: the gradients of sum(o * d_o) + sum(S_T * d_final_state).
+ * Exact reverse mode of the per-token recurrence in fp32 (not the chunked form): a forward sweep
+ * keeps the state at every 32nd token in the workspace, each stretch of 32 tokens is recomputed and
+ * walked backward; one CTA per (batch, value head). The forward outputs are not needed.
+ * q, k, dq, dk: [B, T, H_k, d_k]; v, w, d_o, dv, dw: [B, T, H_v, d_v]; g, b, dg, db: [B, T, H_v, d_k]
+ * (all dtype dt); initial_state, d_final_state, d_initial_state: fp32 [B, H_v, d_k, d_v] or NULL
+ * (zeros / not written). dq and dk of a key head sum its value heads. d_k = d_v = 128.
+ * workspace: gdn2_backward_workspace_size(...) bytes of device memory, 16-byte aligned.
+ * Errors: as gdn2_chunk_fwd. Asynchronous on `stream`.
+ */
+size_t gdn2_backward_workspace_size(int B, int T, int Hk, int Hv, int dk, int dv, gdn2_dtype dt);
+gdn2_status gdn2_backward(const void* q, const void* k, const void* v, const void* g, const void* b, const void* w,
+                          const float* initial_state, const void* d_o, const float* d_final_state, void* dq,
+                          void* dk, void* dv, void* dg, void* db, void* dw, float* d_initial_state, int B, int T,
+                          int Hk, int Hv, int dk_, int dv_, float scale, gdn2_dtype dt, void* workspace,
+                          size_t ws_bytes, void* stream);
+
+/*
  * gdn2_selftest_umma -- diagnostics: one tcgen05 product D[128][N] = A * B (bf16 in, fp32 out)
  * with the operand layouts the tensor-core chunked kernels use, so that a test can check them
  * against a host matrix product. The operands are row-major bf16 device arrays:

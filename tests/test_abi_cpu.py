@@ -164,3 +164,20 @@ def test_mixer_argument_errors(g):
     assert epi(eps=float("nan")) == g.GDN2_ERR_INVALID_ARG
     assert epi(dv=48) == g.GDN2_ERR_UNSUPPORTED
     assert epi(ptr=0x10002) == g.GDN2_ERR_MISALIGNED
+
+
+def test_backward_argument_errors(g):
+    P = lambda a: ctypes.c_void_p(a) if a else None
+    f = lambda ptr=0x10000, B=1, T=4, Hk=1, Hv=2, dk=128, dv=128, dt=1, ws=0x10000, wsb=1 << 40: g.lib.gdn2_backward(
+        *(P(ptr),) * 6, None, P(ptr), None, *(P(ptr),) * 6, None, B, T, Hk, Hv, dk, dv, 1.0, dt, P(ws), wsb, None)
+    assert f(ptr=0) == g.GDN2_ERR_INVALID_ARG
+    assert f(Hk=3, Hv=4) == g.GDN2_ERR_INVALID_ARG
+    assert f(dt=4) == g.GDN2_ERR_INVALID_ARG
+    assert f(dk=64, dv=64) == g.GDN2_ERR_UNSUPPORTED
+    assert f(ptr=0x10004) == g.GDN2_ERR_MISALIGNED
+    assert f(ws=0) == g.GDN2_ERR_WORKSPACE
+    assert f(wsb=16) == g.GDN2_ERR_WORKSPACE
+    n = g.lib.gdn2_backward_workspace_size(2, 100, 1, 2, 128, 128, 1)
+    st, ck = 128 * 128 * 4, (100 + 31) // 32 + 1
+    assert n >= 4 * ck * st + 4 * 32 * st + 2 * 2 * 100 * 2 * 128 * 4
+    assert g.lib.gdn2_backward_workspace_size(2, 100, 1, 2, 64, 64, 1) == 0
