@@ -487,14 +487,16 @@ def end_to_end(g, wl, host, device, args, tokens):
         t.numel() * t.element_size() for t in hdec.values())
     d2h = o_h.numel() * 2 + od_h.numel() * 2
 
+    from gated_deltanet_mixer_gdn2_gb300.host_stream import chunk_fwd_from_host
+
     def step():
-        d = {n: t.to(device, non_blocking=True) for n, t in hpre.items()}
+        # prefill streamed in segments (uploads, kernels and downloads overlap), then the decode tokens
+        st = chunk_fwd_from_host(*(hpre[n] for n in ("q", "k", "v", "g", "b", "w")), o_h, None, C=wl.C, segment_tokens=4096,
+                                 device=device, stream=stream)
         dd = {n: t.to(device, non_blocking=True) for n, t in hdec.items()}
-        o, st = g.chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["b"], d["w"], None)
         outs = []
         for i in range(D):
             outs.append(g.recurrent_step(*(dd[n][i] for n in ("q", "k", "v", "g", "b", "w")), st))
-        o_h.copy_(o, non_blocking=True)
         od_h.copy_(torch.stack(outs, dim=1), non_blocking=True)
 
     for _ in range(2):
