@@ -564,7 +564,8 @@ def run_reference(args):
 
 def run_profile(spec: str):
     """One operation of one workload, twice (the second call is the one to capture with ncu -s 1).
-    spec: 'chunk:<workload>' or 'decode:<workload>'."""
+    spec: 'chunk:<workload>', 'decode:<workload>' or 'next:<workload>' (prologue, epilogue, FG2 transform,
+    backward on that workload's shapes)."""
     import torch
 
     import gated_deltanet_mixer_gdn2_gb300 as g
@@ -579,6 +580,13 @@ def run_profile(spec: str):
         s0 = None if inp.s0 is None else torch.from_numpy(inp.s0).to(device)
         for _ in range(2):
             g.chunk_fwd(q, k, v, gg, b, w, s0, C=wl.C)
+    elif op == "next":
+        # the widened rows on the given workload's token shapes (one call each after a warm-up call)
+        from types import SimpleNamespace
+
+        hbm = peaks()[0]
+        res = next_rows_rooflines(g, device, hbm, SimpleNamespace(B=wl.B, T=wl.T, Hk=wl.Hk, Hv=wl.Hv, dk=wl.dk))
+        print(json.dumps({k: (v["ms"] if isinstance(v, dict) else v) for k, v in res.items()}))
     elif op == "decode":
         inp = synth.make_inputs(wl, T=2)
         st = torch.from_numpy(inp.s0).to(device)
