@@ -149,20 +149,35 @@ __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.comm
 __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
-// sum_k L[k] R[k][c4..c4+3] (fp32 smem, 16-byte aligned rows)
-template <int KN>
-__device__ __forceinline__ float4 row_times(const float* Lrow, const float* R, int ldr, int c4) {
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+// acc[i][c] += sum_{k = 4 g0}^{4 g1 - 1} L[i][k] R[k][c] for a 4 x 4 register tile (fp32 smem, 16-byte aligned
+// rows ldl / ldr floats apart). Each 16-byte load feeds 16 FMAs; k runs upwards, one FMA per term.
+__device__ __forceinline__ void tile4_times(const float* L, int ldl, const float* R, int ldr, int g0, int g1,
+                                            float (&acc)[4][4]) {
+#pragma unroll 2
+    for (int g = g0; g < g1; ++g) {
+        float4 l[4], r[4];
 #pragma unroll
-    for (int k = 0; k < KN; ++k) {
-        const float a = Lrow[k];
-        const float4 b = *reinterpret_cast<const float4*>(R + k * ldr + c4);
-        acc.x = fmaf(a, b.x, acc.x);
-        acc.y = fmaf(a, b.y, acc.y);
-        acc.z = fmaf(a, b.z, acc.z);
-        acc.w = fmaf(a, b.w, acc.w);
+        for (int i = 0; i < 4; ++i) l[i] = *reinterpret_cast<const float4*>(L + i * ldl + 4 * g);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) r[j] = *reinterpret_cast<const float4*>(R + (4 * g + j) * ldr);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float a[4] = {l[i].x, l[i].y, l[i].z, l[i].w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                acc[i][0] = fmaf(a[j], r[j].x, acc[i][0]);
+                acc[i][1] = fmaf(a[j], r[j].y, acc[i][1]);
+                acc[i][2] = fmaf(a[j], r[j].z, acc[i][2]);
+                acc[i][3] = fmaf(a[j], r[j].w, acc[i][3]);
+            }
+        }
     }
-    return acc;
+}
+__device__ __forceinline__ void tile4_store(float* D, int ldd, const float (&acc)[4][4], float sgn) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        *reinterpret_cast<float4*>(D + i * ldd) =
+            make_float4(sgn * acc[i][0], sgn * acc[i][1], sgn * acc[i][2], sgn * acc[i][3]);
 }
 
 __global__ void __launch_bounds__(fs::kThreads, 3)
@@ -390,30 +405,34 @@ __global__ void __launch_bounds__(fs::kThreads, 3)
             for (int i = 0; i < 16; ++i) TF[(base + i) * fs::LDF + base + jj] = x[i];
         }
         __syncthreads();
-        if (tid < 128) {  // Y_i = A_{i+1,i} D_i for diagonal blocks i = 0, 2 (16 x 16 each, 4 columns per thread)
-            const int blk = tid >> 6, r = (tid >> 2) & 15, c4 = (tid & 3) * 4;
-            const int i0 = 32 * blk;
-            const float4 y = row_times<16>(AF + (i0 + 16 + r) * fs::LDF + i0, TF + i0 * fs::LDF + i0, fs::LDF, c4);
-            *reinterpret_cast<float4*>(PF + (blk * 16 + r) * fs::LDP + c4) = y;
+        // Products below run as 4 x 4 register tiles. A skipped k-range multiplies entries of a lower
+        // triangular factor that are exactly zero, so bounds stay warp-uniform and the sums are unchanged.
+        if (warp < 2 && lane < 16) {  // Y_i = A_{i+1,i} D_i for diagonal blocks i = 0, 2 (warp = block)
+            const int i0 = 32 * warp, r0 = 4 * (lane >> 2), c0 = 4 * (lane & 3);
+            float acc[4][4] = {};
+            tile4_times(AF + (i0 + 16 + r0) * fs::LDF + i0, fs::LDF, TF + i0 * fs::LDF + i0 + c0, fs::LDF, 0, 4, acc);
+            tile4_store(PF + (16 * warp + r0) * fs::LDP + c0, fs::LDP, acc, 1.f);
         }
         __syncthreads();
-        if (tid < 128) {  // T_{i+1,i} = -D_{i+1} Y_i
-            const int blk = tid >> 6, r = (tid >> 2) & 15, c4 = (tid & 3) * 4;
-            const int i1 = 32 * blk + 16;
-            const float4 y = row_times<16>(TF + (i1 + r) * fs::LDF + i1, PF + (blk * 16) * fs::LDP, fs::LDP, c4);
-            *reinterpret_cast<float4*>(TF + (i1 + r) * fs::LDF + i1 - 16 + c4) = make_float4(-y.x, -y.y, -y.z, -y.w);
+        if (warp < 2 && lane < 16) {  // T_{i+1,i} = -D_{i+1} Y_i
+            const int i1 = 32 * warp + 16, r0 = 4 * (lane >> 2), c0 = 4 * (lane & 3);
+            float acc[4][4] = {};
+            tile4_times(TF + (i1 + r0) * fs::LDF + i1, fs::LDF, PF + 16 * warp * fs::LDP + c0, fs::LDP, 0, 4, acc);
+            tile4_store(TF + (i1 + r0) * fs::LDF + i1 - 16 + c0, fs::LDF, acc, -1.f);
         }
         __syncthreads();
-        {  // X = A_10 T_00 (32 x 32; rows 32.., cols 0..31), one float4 per thread
-            const int r = tid >> 3, c4 = (tid & 7) * 4;
-            const float4 y = row_times<32>(AF + (32 + r) * fs::LDF, TF, fs::LDF, c4);
-            *reinterpret_cast<float4*>(PF + r * fs::LDP + c4) = y;
+        if (warp < 2) {  // X = A_10 T_00 (32 x 32): warp w takes columns 16w.., where T_00 is zero above row 16w
+            const int r0 = 4 * (lane >> 2), c0 = 16 * warp + 4 * (lane & 3);
+            float acc[4][4] = {};
+            tile4_times(AF + (32 + r0) * fs::LDF, fs::LDF, TF + c0, fs::LDF, 4 * warp, 8, acc);
+            tile4_store(PF + r0 * fs::LDP + c0, fs::LDP, acc, 1.f);
         }
         __syncthreads();
-        {  // T_10 = -T_11 X
-            const int r = tid >> 3, c4 = (tid & 7) * 4;
-            const float4 y = row_times<32>(TF + (32 + r) * fs::LDF + 32, PF, fs::LDP, c4);
-            *reinterpret_cast<float4*>(TF + (32 + r) * fs::LDF + c4) = make_float4(-y.x, -y.y, -y.z, -y.w);
+        if (warp < 2) {  // T_10 = -T_11 X: warp w takes rows 16w.., where T_11 is zero right of column 16w + 15
+            const int r0 = 16 * warp + 4 * (lane >> 3), c0 = 4 * (lane & 7);
+            float acc[4][4] = {};
+            tile4_times(TF + (32 + r0) * fs::LDF + 32, fs::LDF, PF + c0, fs::LDP, 0, 4 * (warp + 1), acc);
+            tile4_store(TF + (32 + r0) * fs::LDF + c0, fs::LDF, acc, -1.f);
         }
         __syncthreads();
         for (int p = tid; p < 64 * 8; p += fs::kThreads) {  // bf16 T, K-major rows (one 16-byte chunk per item)
