@@ -14,9 +14,10 @@
 // Kernel 1 "factors" (grid: chunks x heads; 256 threads; 3 CTAs/SM): TMA loads q, k, g, b of one
 // chunk, one pass computes the decayed operands, tcgen05 forms A|M, CUDA cores invert (I + A),
 // tcgen05 forms W; -W, q.e^G, k.e^{G_last-G}, M, T and e^{G_last} go to the workspace.
-// Kernel 2 "state" (grid: batch x value heads; warp-specialised; sequential over chunks): the same
-// recurrence transposed, with d_v as the 128-row side of every product, so that the state S^T and
-// U^T are tensor-memory A operands and only the chunk factors are read from shared memory.
+// Kernel 2 "state" (grid: 2 x batch x value heads; warp-specialised; sequential over chunks): the
+// columns of S evolve independently, so each CTA runs the recurrence for 64 of the d_v columns with
+// the fp32 state in registers, 128-row products over tokens or d_k, and the bf16 state and U as
+// shared-memory operands.
 #include <cuda.h>
 
 #include "common.cuh"
@@ -503,42 +504,43 @@ __global__ void __launch_bounds__(fs::kThreads, 3)
 struct StateMaps {
     CUtensorMap w, qb, kh, m, t;   // workspace sections
     CUtensorMap v, wg;             // token tiles of v and of the write gate w
-    CUtensorMap o_st;              // output, stored in [64 tokens][32 d_v] tiles
+    CUtensorMap o_st;              // output, stored in [32 tokens][64 d_v] tiles (128-byte swizzle)
 };
 
 namespace ss {
 // Shared memory (every tile 1024-byte aligned): two rings of two slots, "big" for what the products
-// of chunk n read during step n, "pre" for what is used one step ahead (w.v), so each slot is
-// released as soon as its last reader is done; the T tiles of the two chunk parities sit around one
-// zero tile; the chunk decays have a ring of four of their own.
-constexpr uint32_t A1 = 0;          // big: [-W ; Q] (even chunks) or [Q ; -W] (odd chunks): two 64-wide
-                                    //      K (d_k) blocks of [128 rows (token)][128 B]
-constexpr uint32_t KH = 32768;      // big: k.e^{G_last-G} token-major, two 64-wide d_k blocks (MN-major B)
-constexpr uint32_t MM = 49152;      // big: M [64 tokens][64 tokens] (K-major B)
+// of chunk n read during step n, "pre" for what is used one step ahead (T and w.v), so each slot is
+// released as soon as its last reader is done; the chunk decays have a ring of four of their own.
+constexpr uint32_t A1 = 0;          // big: [-W ; Q] as a 128-row K-major A operand: two 64-wide d_k
+                                    //      blocks of [128 rows (token)][128 B]
+constexpr uint32_t KH = 32768;      // big: k.e^{G_last-G} token-major, two 64-wide d_k blocks
+                                    //      (MN-major A operand, M = d_k)
+constexpr uint32_t MM = 49152;      // big: M [64 tokens][64 tokens], K-major. The 8 KB before it are the
+                                    //      upper half of the A operand of M U; those product rows fall on
+                                    //      U rows that have been read already.
 constexpr uint32_t BIG = 57344;     // big slot size
-constexpr uint32_t VV = 0;          // pre: v tile [64 tokens][128 d_v] as two 64-wide blocks; w.v in place
-constexpr uint32_t WW = 16384;      // pre: w tile, same layout
+constexpr uint32_t TT = 0;          // pre: T [64][64] K-major followed by 8 KB of zeros: A operand [T ; 0]
+constexpr uint32_t VV = 16384;      // pre: this CTA's 64 v columns [64 tokens][64]; w.v in place (MN-major B)
+constexpr uint32_t WW = 24576;      // pre: the same columns of w
 constexpr uint32_t PRE = 32768;     // pre slot size
-constexpr uint32_t TX_BIG = 2 * 16384 + 16384 + 8192;
-constexpr uint32_t TX_PRE = 8192 + 2 * 16384;
+constexpr uint32_t TX_BIG = 7 * 8192;
+constexpr uint32_t TX_PRE = 3 * 8192;
 constexpr uint32_t BIG0 = 0;
-constexpr uint32_t TZ = 2 * BIG;            // T (even chunk) | zeros | T (odd chunk), [64][64] bf16 each:
-                                            // as N = 128 K-major B operands, [T ; 0] and [0 ; T]
-constexpr uint32_t PRE0 = TZ + 3 * 8192;
-constexpr uint32_t GAMC = PRE0 + 2 * PRE;   // ring of e^{G_last}: [4 chunks][128] fp32, own barriers
-constexpr uint32_t OST = GAMC + 2048;       // output staging: [4 warps][64 tokens][32 d_v] bf16
-constexpr uint32_t BAR = OST + 16384;       // mbarriers, TMEM base, error flag
+constexpr uint32_t PRE0 = 2 * BIG;
+constexpr uint32_t SB = PRE0 + 2 * PRE;  // bf16 S_n [128 d_k][64 d_v] (MN-major B operand)
+constexpr uint32_t UB = SB + 16384;      // bf16 U [64 tokens][64 d_v] (MN-major B operand)
+constexpr uint32_t OST = UB + 8192;      // output staging [2 warps][32 tokens][64 d_v] bf16, 128-byte swizzle
+constexpr uint32_t GAMC = OST + 8192;    // ring of e^{G_last}: [4 chunks][128] fp32, own barriers
+constexpr uint32_t BAR = GAMC + 2048;    // mbarriers, TMEM base, error flag
 constexpr uint32_t TOTAL = BAR + 256;
-constexpr int kChainWarps = 8;              // warps 0-7: U and state read-outs
-constexpr int kOutWarps = 4;                // warps 8-11: output read-out, w.v
+constexpr int kChainWarps = 8;           // warps 0-7: U and state read-outs, decay
+constexpr int kOutWarps = 4;             // warps 8-11: w.v; warps 10-11 also read the output
+constexpr int kOutReaders = 2;
 constexpr int kProducer = 12, kIssuer = 13;
 constexpr int kThreads = 14 * 32;
-// TMEM columns. D_UO[b] (b = chunk parity) holds U^T = (w.v)^T T^T - S^T W^T in columns 64b..64b+63
-// and O^T = S^T Q^T + U^T M^T in the other 64. D_S holds e^{G_last} . S_n^T before U^T K^ is added
-// to it, S_{n+1}^T after. Then the bf16 A operands S^T (d_k packed two per column) and U^T.
-constexpr uint32_t kDuo = 0, kDs = 256, kAs = 384, kAu = 448;
-__host__ __device__ constexpr uint32_t u_col(int b) { return 128u * b + 64u * b; }
-__host__ __device__ constexpr uint32_t o_col(int b) { return 128u * b + 64u * (1 - b); }
+// TMEM columns (lane = product row). D_UO[b] (b = chunk parity): lanes 0-63 hold U = T (w.v) - W S_n,
+// lanes 64-127 O = Q S_n + M U. D_S receives K^T U (lane = d_k row).
+constexpr uint32_t kDuo = 0, kDs = 128, kCols = 256;
 }  // namespace ss
 
 __device__ __forceinline__ void mbar_arrive1(uint64_t* bar) {
@@ -578,19 +580,15 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, long l
     return ok != 0;
 }
 
-__device__ __forceinline__ void tmem_st_f32x16(uint32_t taddr, const float* x) {
-    uint32_t r[16];
+// 32 fp32 values -> bf16 into four 16-byte chunks (c0..c0+3) of a 128-byte-swizzled row
+__device__ __forceinline__ void st_row_bf16x32(uint8_t* tile, int row, int c0, const float* x) {
 #pragma unroll
-    for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(x[i]);
-    tmem_st16(taddr, r);
-}
-
-// 32 fp32 values -> 16 columns of bf16 pairs (lower index in the low half)
-__device__ __forceinline__ void tmem_st_bf16x32(uint32_t taddr, const float* x) {
-    uint32_t r[16];
+    for (int c = 0; c < 4; ++c) {
+        float y[8];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) r[i] = pack_bf16x2(x[2 * i], x[2 * i + 1]);
-    tmem_st16(taddr, r);
+        for (int e = 0; e < 8; ++e) y[e] = x[8 * c + e];
+        *reinterpret_cast<uint4*>(tile + row * 128 + (((c0 + c) ^ (row & 7)) << 4)) = pack8(y);
+    }
 }
 
 __device__ __forceinline__ void tma_store_4d(const void* map, const void* src, int c0, int c1, int c2, int c3) {
@@ -600,16 +598,19 @@ __device__ __forceinline__ void tma_store_4d(const void* map, const void* src, i
                  : "memory");
 }
 
-// The chunk recurrence in transposed form, one CTA per (batch, value head): with S^T (d_v x d_k) and
-// per chunk n the factors of the workspace,
-//   U^T = (w.v)^T T^T - S_n^T W^T,   O^T = S_n^T Q^T + U^T M^T,   S_{n+1}^T = S_n^T diag(e^{G_last}) + U^T K^.
-// d_v is the 128-row M dimension of every product, so S^T and U^T (bf16 copies in tensor memory)
-// are the A operands and only the factors are read from shared memory; the fp32 state stays in the
-// tensor-memory accumulator of U^T K^. The dependent chain per chunk is
-//   S_n^T -> [S^T W^T | S^T Q^T] -> U^T -> + U^T K^ -> S_{n+1}^T;
-// w.v, (w.v)^T T^T, U^T M^T, the decay of the accumulator and the output run beside it. Roles: a
-// TMA warp keeps both slots of both rings in flight, an MMA warp issues (one lane), eight chain warps
-// read U and the state, four warps form w.v and read the output. They hand over through mbarriers; every wait is
+// The chunk recurrence for 64 of the d_v columns, two CTAs per (batch, value head): the columns of S
+// evolve independently, so each CTA keeps its d_k x 64 slice of the state. Per chunk n, with the
+// factors of the workspace,
+//   U = T (w.v) - W S_n,   O = Q S_n + M U,   S_{n+1} = diag(e^{G_last}) S_n + K^T U.
+// Every product has the 128 rows of M = 128: the token rows of [T ; 0], [-W ; Q] and [. ; M] put U and
+// O into the two lane halves of one accumulator, and d_k is the row side of K^T U. The fp32 state
+// stays in the registers of the eight chain warps (one d_k row, 32 columns per thread), where the
+// decay is one scalar per row and K^T U is added from tensor memory; its bf16 copy and U are the B
+// operands in shared memory. The dependent chain per chunk is
+//   S_n -> [-W ; Q] S_n -> U -> + K^T U -> S_{n+1};
+// w.v, T (w.v), M U, the decay and the output run beside it. Roles: a TMA warp keeps both slots of
+// both rings in flight, an MMA warp issues (one lane), eight chain warps read U and the state, four
+// warps form w.v and two of them read the output. They hand over through mbarriers; every wait is
 // bounded.
 __global__ void __launch_bounds__(ss::kThreads, 1)
     state_tc_kernel(const __grid_constant__ StateMaps maps, const uint8_t* __restrict__ ws,
@@ -623,32 +624,32 @@ __global__ void __launch_bounds__(ss::kThreads, 1)
     uint64_t* full_pre = full_big + 4;                               // [2] pre slot landed
     uint64_t* empty_pre = full_big + 6;                              // [2] pre slot consumed
     uint64_t* wv_ready = full_big + 8;                               // [2] w.v formed (per chunk parity)
-    uint64_t* o_free = full_big + 10;                                // [2] O^T columns of D_UO[b] read
-    uint64_t* o_done = full_big + 12;                                // [2] O^T of D_UO[b] complete
-    uint64_t* mma1_done = full_big + 14;                             // S^T W^T, S^T Q^T complete
-    uint64_t* s_done = full_big + 15;                                // U^T K^ complete
-    uint64_t* u_ready = full_big + 16;                               // U^T written, D_S decayed (8 warps)
-    uint64_t* s_ready = full_big + 17;                               // S^T written (8 chain warps)
+    uint64_t* o_free = full_big + 10;                                // [2] O lanes of D_UO[b] read
+    uint64_t* o_done = full_big + 12;                                // [2] O of D_UO[b] complete
+    uint64_t* mma1_done = full_big + 14;                             // [-W ; Q] S_n complete
+    uint64_t* s_done = full_big + 15;                                // K^T U complete
+    uint64_t* u_ready = full_big + 16;                               // U written (4 warps)
+    uint64_t* s_ready = full_big + 17;                               // bf16 S_n written (8 chain warps)
     uint64_t* drain = full_big + 18;
     uint64_t* gam_full = full_big + 19;                              // [4] e^{G_last} of chunk m landed
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + ss::BAR + 224);
     volatile int* err = reinterpret_cast<volatile int*>(sm + ss::BAR + 228);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int bh = blockIdx.x;
+    const int bh = blockIdx.x >> 1, hc = blockIdx.x & 1;  // (batch, value head), d_v column half
     const int bi = bh / Hv, hv = bh - bi * Hv;
 
     if (tid == 0) {
         for (int i = 0; i < 8; ++i) mbar_init(full_big + i, 1);
         mbar_init(wv_ready, ss::kOutWarps);
         mbar_init(wv_ready + 1, ss::kOutWarps);
-        mbar_init(o_free, ss::kOutWarps);
-        mbar_init(o_free + 1, ss::kOutWarps);
+        mbar_init(o_free, ss::kOutReaders);
+        mbar_init(o_free + 1, ss::kOutReaders);
         mbar_init(o_done, 1);
         mbar_init(o_done + 1, 1);
         mbar_init(mma1_done, 1);
         mbar_init(s_done, 1);
-        mbar_init(u_ready, ss::kChainWarps);
+        mbar_init(u_ready, ss::kChainWarps / 2);
         mbar_init(s_ready, ss::kChainWarps);
         mbar_init(drain, 1);
         for (int i = 0; i < 4; ++i) mbar_init(gam_full + i, 1);
@@ -656,11 +657,11 @@ __global__ void __launch_bounds__(ss::kThreads, 1)
         fence_mbar_init();
     }
     if (warp == 0) {
-        tmem_alloc(tmem_slot, 512);
+        tmem_alloc(tmem_slot, ss::kCols);
         tmem_relinquish();
     }
-    for (int p = tid; p < 512; p += ss::kThreads)
-        reinterpret_cast<uint4*>(sm + ss::TZ + 8192)[p] = make_uint4(0, 0, 0, 0);
+    for (int p = tid; p < 2 * 512; p += ss::kThreads)  // the zero halves of [T ; 0] in both pre slots
+        reinterpret_cast<uint4*>(sm + ss::PRE0 + (p >> 9) * ss::PRE + ss::TT + 8192)[p & 511] = make_uint4(0, 0, 0, 0);
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
@@ -678,12 +679,9 @@ __global__ void __launch_bounds__(ss::kThreads, 1)
                 uint8_t* sb = sm + ss::PRE0 + st * ss::PRE;
                 const int u = bh * NC + m;
                 mbar_arrive_expect_tx(full_pre + st, ss::TX_PRE);
-                tma_load_3d(sm + ss::TZ + 16384 * st, &maps.t, 0, 0, u, full_pre + st);
-#pragma unroll
-                for (int kb = 0; kb < 2; ++kb) {
-                    tma_load_4d(sb + ss::VV + kb * 8192, &maps.v, 64 * kb, hv, m * kC, bi, full_pre + st);
-                    tma_load_4d(sb + ss::WW + kb * 8192, &maps.wg, 64 * kb, hv, m * kC, bi, full_pre + st);
-                }
+                tma_load_3d(sb + ss::TT, &maps.t, 0, 0, u, full_pre + st);
+                tma_load_4d(sb + ss::VV, &maps.v, 64 * hc, hv, m * kC, bi, full_pre + st);
+                tma_load_4d(sb + ss::WW, &maps.wg, 64 * hc, hv, m * kC, bi, full_pre + st);
                 // the decay of chunk m-4 has been applied once pre(m-2) was consumed
                 mbar_arrive_expect_tx(gam_full + (m & 3), 512);
                 bulk_load(sm + ss::GAMC + (m & 3) * 512, ws + static_cast<size_t>(u) * kWsUnit + kWsGam, 512,
@@ -699,8 +697,8 @@ __global__ void __launch_bounds__(ss::kThreads, 1)
                 mbar_arrive_expect_tx(full_big + st, ss::TX_BIG);
 #pragma unroll
                 for (int kb = 0; kb < 2; ++kb) {
-                    tma_load_3d(sb + ss::A1 + kb * 16384 + 8192 * st, &maps.w, 64 * kb, 0, u, full_big + st);
-                    tma_load_3d(sb + ss::A1 + kb * 16384 + 8192 * (1 - st), &maps.qb, 64 * kb, 0, u, full_big + st);
+                    tma_load_3d(sb + ss::A1 + kb * 16384, &maps.w, 64 * kb, 0, u, full_big + st);
+                    tma_load_3d(sb + ss::A1 + kb * 16384 + 8192, &maps.qb, 64 * kb, 0, u, full_big + st);
                     tma_load_3d(sb + ss::KH + kb * 8192, &maps.kh, 64 * kb, 0, u, full_big + st);
                 }
                 tma_load_3d(sb + ss::MM, &maps.m, 0, 0, u, full_big + st);
@@ -720,22 +718,14 @@ __global__ void __launch_bounds__(ss::kThreads, 1)
         }
     } else if (warp == ss::kIssuer) {
         // ================================ MMA warp ================================
-        // Tensor-pipe order per step n: S^T[-W;Q]^T (n) | (w.v)^T T^T (n+1) if ready | U^T K^ (n) |
-        // U^T M^T (n) | (w.v)^T T^T (n+1) otherwise: the products off the chain fill the gaps while
-        // U and the state are read out.
+        // Tensor-pipe order per step n: [-W ; Q] S_n | K^T U (n) | M U (n) | T (w.v) (n+1): the
+        // products off the chain run while the state is read out.
         if (lane == 0) {
-            constexpr uint32_t id_uo = idesc_bf16(128, 128, false, false);  // S^T [-W ; Q]^T
-            constexpr uint32_t id_s = idesc_bf16(128, 128, false, true);    // U^T K^
-            constexpr uint32_t id_o = idesc_bf16(128, 64, false, false);    // U^T M^T
-            constexpr uint32_t id_0 = idesc_bf16(128, 128, true, false);    // (w.v)^T [T ; 0]^T
+            constexpr uint32_t id_k = idesc_bf16(128, 64, false, true);  // K-major A, MN-major B
+            constexpr uint32_t id_s = idesc_bf16(128, 64, true, true);   // K^T U: MN-major A and B
             auto desc = [&](uint32_t off, uint32_t lbo) { return smem_desc(sbase + off, lbo, 1024, kSwizzle128B); };
-            // D_UO[m&1] = (w.v)^T T^T in the U columns and 0 in the O columns, once w.v of chunk m is
-            // formed and the output of chunk m-2 has been read
-            auto mma0_ready = [&](int m) {
-                const int st = m & 1, ph = (m >> 1) & 1;
-                return mbar_test_wait(wv_ready + st, ph) && mbar_test_wait(full_pre + st, ph) &&
-                       mbar_test_wait(o_free + st, ph);
-            };
+            const uint64_t b_s = desc(ss::SB, 16384), b_u = desc(ss::UB, 8192);
+            // D_UO[m&1] = [T ; 0] (w.v), once w.v of chunk m is formed and the output of chunk m-2 read
             auto mma0 = [&](int m) -> bool {
                 const int st = m & 1, ph = (m >> 1) & 1;
                 if (!mbar_wait_or_abort(wv_ready + st, ph, wait_ns, err) ||
@@ -743,10 +733,11 @@ __global__ void __launch_bounds__(ss::kThreads, 1)
                     !mbar_wait_or_abort(o_free + st, ph, wait_ns, err))
                     return false;
                 tc_fence_after();
-                const uint64_t a = desc(ss::PRE0 + st * ss::PRE + ss::VV, 8192), b = desc(ss::TZ + 8192 * st, 16);
+                const uint32_t pre = ss::PRE0 + st * ss::PRE;
+                const uint64_t a = desc(pre + ss::TT, 16), b = desc(pre + ss::VV, 8192);
 #pragma unroll
-                for (int s = 0; s < 4; ++s)
-                    mma_bf16(tmem + ss::kDuo + 128 * st, a + (s * 2048 >> 4), b + (s * 32 >> 4), id_0, s > 0);
+                for (int s = 0; s < 4; ++s)  // K = tokens
+                    mma_bf16(tmem + ss::kDuo + 64 * st, a + (s * 32 >> 4), b + (s * 2048 >> 4), id_k, s > 0);
                 mma_commit(empty_pre + st);
                 return true;
             };
@@ -761,39 +752,31 @@ __global__ void __launch_bounds__(ss::kThreads, 1)
                 }
                 tc_fence_after();
                 {
-                    const uint64_t b = desc(big + ss::A1, 16);
+                    const uint64_t a = desc(big + ss::A1, 16);
 #pragma unroll
                     for (int s = 0; s < 8; ++s)  // K = d_k: two 64-wide blocks of 16 KB
-                        mma_bf16_ts(tmem + ss::kDuo + 128 * st, tmem + ss::kAs + 8 * s,
-                                    b + (((s >> 2) * 16384 + (s & 3) * 32) >> 4), id_uo, 1);
+                        mma_bf16(tmem + ss::kDuo + 64 * st, a + (((s >> 2) * 16384 + (s & 3) * 32) >> 4),
+                                 b_s + (s * 2048 >> 4), id_k, 1);
                 }
                 mma_commit(mma1_done);
-                bool next0 = n + 1 < NC;
-                if (next0 && mma0_ready(n + 1)) {
-                    if (!mma0(n + 1)) {
-                        run = false;
-                        break;
-                    }
-                    next0 = false;
-                }
                 if (!mbar_wait_or_abort(u_ready, n & 1, wait_ns, err)) {
                     run = false;
                     break;
                 }
                 tc_fence_after();
                 {
-                    const uint64_t bk = desc(big + ss::KH, 8192), bm = desc(big + ss::MM, 16);
+                    const uint64_t ak = desc(big + ss::KH, 8192), am = desc(big + ss::MM - 8192, 16);
 #pragma unroll
-                    for (int s = 0; s < 4; ++s)  // K = tokens; accumulates onto e^{G_last} . S_n^T
-                        mma_bf16_ts(tmem + ss::kDs, tmem + ss::kAu + 8 * s, bk + (s * 2048 >> 4), id_s, 1);
+                    for (int s = 0; s < 4; ++s)  // K = tokens
+                        mma_bf16(tmem + ss::kDs, ak + (s * 2048 >> 4), b_u + (s * 2048 >> 4), id_s, s > 0);
                     mma_commit(s_done);
 #pragma unroll
                     for (int s = 0; s < 4; ++s)
-                        mma_bf16_ts(tmem + ss::kDuo + ss::o_col(st), tmem + ss::kAu + 8 * s, bm + (s * 32 >> 4), id_o, 1);
+                        mma_bf16(tmem + ss::kDuo + 64 * st, am + (s * 32 >> 4), b_u + (s * 2048 >> 4), id_k, 1);
                     mma_commit(o_done + st);
                     mma_commit(empty_big + st);
                 }
-                if (next0 && !mma0(n + 1)) {
+                if (n + 1 < NC && !mma0(n + 1)) {
                     run = false;
                     break;
                 }
@@ -804,19 +787,20 @@ __global__ void __launch_bounds__(ss::kThreads, 1)
             mbar_wait(drain, 0, kDefaultWaitNs);
         }
     } else if (warp >= ss::kChainWarps) {
-        // ================== output read-out and w.v (warps 8-11) ===================
-        const int q4 = warp & 3;  // TMEM lane quarter = d_v rows 32*q4 ..
+        // ============== w.v (warps 8-11) and output read-out (warps 10-11) ==============
+        const int q4 = warp & 3;                      // TMEM lane quarter
+        const bool reader = q4 >= 2;                  // lanes 64-127: O rows = tokens 32 (q4 - 2) ..
         const int otid = tid - 32 * ss::kChainWarps;  // 0..127
         const uint32_t lane_base = static_cast<uint32_t>(32 * q4) << 16;
-        uint8_t* stg = sm + ss::OST + q4 * 4096;  // [64 tokens][32 d_v] bf16, 64-byte rows
+        uint8_t* stg = sm + ss::OST + (q4 & 1) * 4096;  // [32 tokens][64 d_v] bf16, 128-byte swizzle
         // w.v in place of v (both tiles carry the same swizzle, so the product is position-wise)
         auto take_pre = [&](int m) -> bool {
             const int st = m & 1;
             if (!warp_wait(full_pre + st, (m >> 1) & 1, wait_ns, err)) return false;
             uint8_t* sbp = sm + ss::PRE0 + st * ss::PRE;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const uint32_t off = (otid + 128 * i) * 16;  // 1024 chunks of 16 bytes
+            for (int i = 0; i < 4; ++i) {
+                const uint32_t off = (otid + 128 * i) * 16;  // 512 chunks of 16 bytes
                 float a[8], bw[8];
                 unpack8(*reinterpret_cast<const uint4*>(sbp + ss::VV + off), a);
                 unpack8(*reinterpret_cast<const uint4*>(sbp + ss::WW + off), bw);
@@ -831,7 +815,7 @@ __global__ void __launch_bounds__(ss::kThreads, 1)
         };
         bool ok = NC > 0;
         if (ok) {
-            if (lane == 0) {  // nothing to read before the first two chunks
+            if (reader && lane == 0) {  // nothing to read before the first two chunks
                 mbar_arrive1(o_free);
                 mbar_arrive1(o_free + 1);
             }
@@ -839,103 +823,106 @@ __global__ void __launch_bounds__(ss::kThreads, 1)
         }
         for (int m = 0; ok && m < NC; ++m) {
             const int st = m & 1;
-            if (!(ok = warp_wait(o_done + st, (m >> 1) & 1, wait_ns, err))) break;
-            tc_fence_after();
-            if (lane == 0) bulk_wait_read_all();  // the previous chunk's store has read the staging
-            __syncwarp();
-            {
+            if (reader) {
+                if (!(ok = warp_wait(o_done + st, (m >> 1) & 1, wait_ns, err))) break;
+                tc_fence_after();
+                if (lane == 0) bulk_wait_read_all();  // the previous chunk's store has read the staging
+                __syncwarp();
                 float x[64];
-                tmem_ld_cols<4>(tmem + lane_base + ss::kDuo + ss::o_col(st), x);
+                tmem_ld_cols<4>(tmem + lane_base + ss::kDuo + 64 * st, x);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive1(o_free + st);
 #pragma unroll
-                for (int j = 0; j < 64; ++j)
-                    *reinterpret_cast<__nv_bfloat16*>(stg + j * 64 + lane * 2) = __float2bfloat16_rn(scale * x[j]);
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-                // rows past T are clipped by the tensor map
-                tma_store_4d(&maps.o_st, stg, 32 * q4, hv, m * kC, bi);
-                bulk_commit();
+                for (int j = 0; j < 64; ++j) x[j] *= scale;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) st_row_bf16x32(stg, lane, 4 * h, x + 32 * h);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    // rows past T are clipped by the tensor map
+                    tma_store_4d(&maps.o_st, stg, 64 * hc, hv, m * kC + 32 * (q4 - 2), bi);
+                    bulk_commit();
+                }
             }
             if (m + 2 < NC && !(ok = take_pre(m + 2))) break;
         }
-        if (lane == 0) bulk_wait_all();  // the output is written before the block retires
+        if (reader && lane == 0) bulk_wait_all();  // the output is written before the block retires
     } else {
-        // ===================== U and state read-outs (warps 0-7) =====================
-        const int q4 = warp & 3, half = warp >> 2;  // TMEM lane quarter; column half
-        const int v = 32 * q4 + lane;                // d_v row (= TMEM lane)
+        // ============= U and state read-outs, decay (warps 0-7) =============
+        // Each thread keeps its row and 32 columns of the fp32 state in registers, already multiplied
+        // by the next chunk's decay; the tensor core only forms K^T U.
+        const int q4 = warp & 3, half = warp >> 2;  // TMEM lane quarter; 32-column half of the 64
+        const bool u_reader = q4 < 2;               // lanes 0-63 of D_UO hold U
+        const int r = 32 * q4 + lane;               // d_k row of D_S (= TMEM lane); token row of U
         const uint32_t lane_base = static_cast<uint32_t>(32 * q4) << 16;
         auto arrive = [&](uint64_t* bar) {
             __syncwarp();
             if (lane == 0) mbar_arrive1(bar);
         };
-        // D_S = e^{G_last(m)} . S^T for this thread's 64 columns
-        auto decay_into_ds = [&](int m, float (&x)[64]) -> bool {
+        auto decay = [&](int m, float (&x)[32]) -> bool {  // x = e^{G_last(m)} . x for this thread's row
             if (!warp_wait(gam_full + (m & 3), (m >> 2) & 1, wait_ns, err)) return false;
-            const float4* g4 = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(sm + ss::GAMC) +
-                                                               (m & 3) * 128 + 64 * half);
+            const float gg = reinterpret_cast<const float*>(sm + ss::GAMC)[(m & 3) * 128 + r];
 #pragma unroll
-            for (int j4 = 0; j4 < 16; ++j4) {
-                const float4 gg = g4[j4];
-                x[4 * j4] *= gg.x;
-                x[4 * j4 + 1] *= gg.y;
-                x[4 * j4 + 2] *= gg.z;
-                x[4 * j4 + 3] *= gg.w;
-            }
-#pragma unroll
-            for (int c = 0; c < 64; c += 16) tmem_st_f32x16(tmem + lane_base + ss::kDs + 64 * half + c, x + c);
-            tmem_st_wait();
-            tc_fence_before();
+            for (int j = 0; j < 32; ++j) x[j] *= gg;
             return true;
         };
+        uint8_t* sbt = sm + ss::SB;
+        uint8_t* ubt = sm + ss::UB;
+        const size_t srow = (static_cast<size_t>(bh) * kD + r) * kD + 64 * hc + 32 * half;
+        float sx[32];  // e^{G_last(n)} . S_n
         bool ok = NC > 0;
         if (ok) {
-            float x[64];
-            const float* src = s0 ? s0 + (static_cast<size_t>(bh) * kD + 64 * half) * kD + v : nullptr;
 #pragma unroll
-            for (int j = 0; j < 64; ++j) x[j] = src ? src[j * kD] : 0.f;
-            tmem_st_bf16x32(tmem + lane_base + ss::kAs + 32 * half, x);
-            tmem_st_bf16x32(tmem + lane_base + ss::kAs + 32 * half + 16, x + 32);
-            ok = decay_into_ds(0, x);
-            if (ok) arrive(s_ready);
+            for (int j4 = 0; j4 < 8; ++j4) {
+                const float4 f = s0 ? reinterpret_cast<const float4*>(s0 + srow)[j4] : make_float4(0.f, 0.f, 0.f, 0.f);
+                sx[4 * j4] = f.x;
+                sx[4 * j4 + 1] = f.y;
+                sx[4 * j4 + 2] = f.z;
+                sx[4 * j4 + 3] = f.w;
+            }
+            st_row_bf16x32(sbt, r, 4 * half, sx);
+            fence_proxy_async_smem();
+            arrive(s_ready);
+            ok = decay(0, sx);
         }
         for (int n = 0; ok && n < NC; ++n) {
             const int st = n & 1;
-            if (!(ok = warp_wait(mma1_done, n & 1, wait_ns, err))) break;
-            tc_fence_after();
-            {  // U^T: this thread's 32 token columns -> bf16 A operand
-                float x[32];
-                tmem_ld_cols<2>(tmem + lane_base + ss::kDuo + ss::u_col(st) + 32 * half, x);
-                tmem_st_bf16x32(tmem + lane_base + ss::kAu + 16 * half, x);
-                tmem_st_wait();
+            if (u_reader) {
+                if (!(ok = warp_wait(mma1_done, n & 1, wait_ns, err))) break;
+                tc_fence_after();
+                float x[32];  // U: token row r, this thread's 32 columns -> bf16 B operand
+                tmem_ld_cols<2>(tmem + lane_base + ss::kDuo + 64 * st + 32 * half, x);
+                st_row_bf16x32(ubt, r, 4 * half, x);
+                fence_proxy_async_smem();
                 tc_fence_before();
                 arrive(u_ready);
             }
             if (!(ok = warp_wait(s_done, n & 1, wait_ns, err))) break;
             tc_fence_after();
-            float x[64];  // S_{n+1}^T, this thread's 64 d_k columns
-            tmem_ld_cols<4>(tmem + lane_base + ss::kDs + 64 * half, x);
-            tmem_st_bf16x32(tmem + lane_base + ss::kAs + 32 * half, x);
-            tmem_st_bf16x32(tmem + lane_base + ss::kAs + 32 * half + 16, x + 32);
-            tmem_st_wait();
+            {
+                float x[32];  // K^T U: d_k row r, this thread's 32 columns
+                tmem_ld_cols<2>(tmem + lane_base + ss::kDs + 32 * half, x);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) sx[j] += x[j];  // S_{n+1}
+            }
+            st_row_bf16x32(sbt, r, 4 * half, sx);
+            fence_proxy_async_smem();
             tc_fence_before();
             arrive(s_ready);
             if (n + 1 < NC) {
-                // ordered before U^T K^ of chunk n+1 by the next U hand-off
-                if (!(ok = decay_into_ds(n + 1, x))) break;
+                if (!(ok = decay(n + 1, sx))) break;
             } else if (sT_out) {
-                float* dst = sT_out + (static_cast<size_t>(bh) * kD + 64 * half) * kD + v;
+                float4* dst = reinterpret_cast<float4*>(sT_out + srow);
 #pragma unroll
-                for (int j = 0; j < 64; ++j) dst[j * kD] = x[j];
+                for (int j4 = 0; j4 < 8; ++j4)
+                    dst[j4] = make_float4(sx[4 * j4], sx[4 * j4 + 1], sx[4 * j4 + 2], sx[4 * j4 + 3]);
             }
         }
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, 512);
+    if (warp == 0) tmem_dealloc(tmem, ss::kCols);
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -1109,12 +1096,12 @@ bool token_map(CUtensorMap* m, const void* p, int B, int T, int H) {
     return make_map(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, p, dims, st, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-// output [B, T, H, 128] bf16 viewed as (d, H, T, B); box (32, 1, 64, 1), plain rows of 64 bytes
+// output [B, T, H, 128] bf16 viewed as (d, H, T, B); box (64, 1, 32, 1), 128-byte swizzle
 bool out_map(CUtensorMap* m, const void* p, int B, int T, int H) {
     const uint64_t dims[4] = {kD, (uint64_t)H, (uint64_t)T, (uint64_t)B};
     const uint64_t st[3] = {kD * 2, (uint64_t)H * kD * 2, (uint64_t)T * H * kD * 2};
-    const uint32_t box[4] = {32, 1, kC, 1};
-    return make_map(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, p, dims, st, box, CU_TENSOR_MAP_SWIZZLE_NONE);
+    const uint32_t box[4] = {64, 1, 32, 1};
+    return make_map(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, p, dims, st, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 // workspace section viewed as (cols, rows, units); box (box_cols, box_rows, 1)
@@ -1168,7 +1155,7 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const v
     factors_tc_kernel<<<dim3(NC, sh.B * sh.Hv), fs::kThreads, f_smem, s>>>(fm, wsb, sh.Hk, sh.Hv, NC, wait_ns);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    state_tc_kernel<<<dim3(sh.B * sh.Hv), ss::kThreads, s_smem, s>>>(sm_, wsb, s0, sT, sh.Hv, NC, scale,
+    state_tc_kernel<<<dim3(2 * sh.B * sh.Hv), ss::kThreads, s_smem, s>>>(sm_, wsb, s0, sT, sh.Hv, NC, scale,
                                                                       wait_ns);
     return cudaGetLastError();
 }
