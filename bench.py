@@ -355,7 +355,7 @@ def next_rows_rooflines(g, device, hbm, wl):
         "mixer_prologue": (lambda: g.gdn2_mixer_prologue(xq, xk, xv, *cw, ag, ab, aw, *outs, states=states),
                            2 * tok * (2 * Hk * d + 4 * Hv * d) * e + sum(c.numel() for c in cw) * 4
                            + 2 * sum(s_.numel() for s_ in states) * 4,
-                           "gdn2_mixer_prologue (prologue_kernel + gates_kernel + conv_state_kernel)"),
+                           "gdn2_mixer_prologue (conv_tile_kernel + gates_kernel + conv_state_kernel)"),
         "mixer_epilogue": (lambda: g.gdn2_mixer_epilogue(o, z, wt, y), 3 * tok * Hv * d * e + d * 4,
                            "gdn2_mixer_epilogue (epilogue_kernel)"),
         "fg2_inputs": (lambda: g.gdn2_fg2_inputs(xq, xk, ag, *f_outs), (2 * Hk + 5 * Hv) * tok * d * e,

@@ -52,7 +52,8 @@ def _run_prologue(g, xs, ws, gates, states, dtype, neg, t0=0, t1=None):
     return outs
 
 
-@pytest.mark.parametrize("dtype,d,neg", [("bf16", 128, False), ("bf16", 128, True), ("f32", 64, False)])
+@pytest.mark.parametrize("dtype,d,neg", [("bf16", 128, False), ("bf16", 128, True), ("f32", 64, False),
+                                         ("bf16", 256, False), ("f32", 16, True), ("bf16", 32, False)])
 def test_prologue_parity(g, dtype, d, neg):
     import torch
 
