@@ -10,19 +10,21 @@ from tests import gpu_helpers as H
 pytestmark = pytest.mark.gpu
 
 
-def test_segments_match_one_call():
+@pytest.mark.parametrize("T,segment_tokens", [(1000, 192), (3000, 1024)])
+def test_segments_match_one_call(T, segment_tokens):
     import torch
 
     import gated_deltanet_mixer_gdn2_gb300 as g
     from gated_deltanet_mixer_gdn2_gb300.host_stream import chunk_fwd_from_host
 
-    wl = synth.Workload("hs", B=2, T=1000, Hk=2, Hv=4, dk=128, dv=128, dtype="bf16", seed=3, s0_std=0.02)
+    wl = synth.Workload("hs", B=2, T=T, Hk=2, Hv=4, dk=128, dv=128, dtype="bf16", seed=3, s0_std=0.02)
     inp = synth.make_inputs(wl)
     host = [synth.to_torch(np.ascontiguousarray(getattr(inp, n)), "bf16", "cpu").pin_memory()
             for n in ("q", "k", "v", "g", "b", "w")]
-    o_h = torch.empty((2, 1000, 4, 128), dtype=torch.bfloat16).pin_memory()
+    o_h = torch.empty((2, T, 4, 128), dtype=torch.bfloat16).pin_memory()
     s0 = H.state_to_device(inp.s0)
-    st = chunk_fwd_from_host(*host, o_h, s0, segment_tokens=192)   # 6 segments, the last one ragged
+    # (1000, 192): 6 segments, the last one ragged; (3000, 1024): 512, 1024, 952, 512 (ramp + ragged middle)
+    st = chunk_fwd_from_host(*host, o_h, s0, segment_tokens=segment_tokens)
     torch.cuda.synchronize()
     o_ref, s_ref = g.chunk_fwd(*(t.cuda() for t in host), s0)
     torch.cuda.synchronize()
