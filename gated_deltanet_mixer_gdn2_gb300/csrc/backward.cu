@@ -9,25 +9,29 @@
 //     dL/dS_{t-1} = diag(alpha) (G - beta x^T) + scale q_{t-1} do_{t-1}^T.
 // The walk back needs S_{t-1} for every t: the states at every kChk-th token are saved in a first
 // forward sweep, and each stretch of kChk tokens is recomputed into a scratch buffer (L2-sized)
-// before it is walked backward. One CTA per (batch, value head) holds the 128 x 128 fp32 state and
-// its gradient in registers: warp w owns 16 columns, lane = 8 row groups x 4 column groups, 16 rows
-// x 4 columns per thread. Column sums (over d_k) are in-thread plus shuffles; row sums (over d_v)
-// go through shared memory. q and k gradients are formed per value head and summed over each key
-// head's group by a second kernel. Arithmetic is fp32.
+// before it is walked backward. The columns of S (and of its gradient) evolve independently, so two
+// CTAs per (batch, value head) each hold 64 of the d_v columns of the fp32 state and its gradient in
+// registers: warp w owns 8 columns, lane = 16 row groups x 2 column groups, 8 rows x 4 columns per
+// thread. Column sums (over d_k) are in-thread plus shuffles; row sums (over d_v) go through shared
+// memory and leave the CTA as fp32 partial sums (they are linear in the columns): a second kernel
+// adds the two halves, and for q and k also the value heads of each key head's group, in a fixed
+// order. Arithmetic is fp32.
 #include "common.cuh"
 
 namespace gdn2 {
 namespace {
 
 constexpr int kD = 128;
+constexpr int kCols = 64;     // d_v columns per CTA
 constexpr int kChk = 32;      // checkpoint interval = tokens recomputed at a time
 constexpr int kThreads = 256;
+constexpr int kParts = 2 * kCols / 4;  // row-sum partials per row inside a CTA: 8 warps x 2 column groups
 
 struct BwdArgs {
     const void *q, *k, *v, *g, *b, *w, *dout;
     const float* s0;      // nullable
     const float* dsT;     // nullable
-    float *dq_ws, *dk_ws; // [B, T, H_v, 128] fp32
+    float* part;          // [4 sums][2 halves][B, T, H_v, 128] fp32: dq, dk, db, dg partial sums
     void *dv, *dg, *db, *dw;
     float* ds0;           // nullable
     float *ckpt, *scratch;
@@ -85,19 +89,20 @@ __device__ void stage_tokens(const BwdArgs& a, int bi, int hv, int t_lo, int n, 
     }
 }
 
-// sum over the 8 row groups of a warp (lanes differing in bits 2..4)
+// sum over the 16 row groups of a warp (lanes differing in bits 1..4)
 __device__ __forceinline__ float col_sum(float x) {
+    x += __shfl_xor_sync(0xffffffffu, x, 2);
     x += __shfl_xor_sync(0xffffffffu, x, 4);
     x += __shfl_xor_sync(0xffffffffu, x, 8);
     x += __shfl_xor_sync(0xffffffffu, x, 16);
     return x;
 }
 
-// one forward token on this thread's 16 x 4 tile
-__device__ __forceinline__ void forward_step(float (&S)[16][4], const Tok& tk, int r0, int c0) {
+// one forward token on this thread's 8 x 4 tile (c0: global d_v column)
+__device__ __forceinline__ void forward_step(float (&S)[8][4], const Tok& tk, int r0, int c0) {
     float r[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
+    for (int i = 0; i < 8; ++i) {
         const float al = tk.alpha[r0 + i], be = tk.beta[r0 + i];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -109,24 +114,25 @@ __device__ __forceinline__ void forward_step(float (&S)[16][4], const Tok& tk, i
 #pragma unroll
     for (int j = 0; j < 4; ++j) d[j] = tk.u[c0 + j] - col_sum(r[j]);
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
+    for (int i = 0; i < 8; ++i) {
         const float kk = tk.k[r0 + i];
 #pragma unroll
         for (int j = 0; j < 4; ++j) S[i][j] = fmaf(kk, d[j], S[i][j]);
     }
 }
 
-__device__ __forceinline__ void tile_load(float (&S)[16][4], const float* base, int r0, int c0) {
+// ld: row stride of the stored matrix (kD for [d_k][d_v] states, kCols for this CTA's compact copies)
+__device__ __forceinline__ void tile_load(float (&S)[8][4], const float* base, int ld, int r0, int c0) {
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        const float4 x = *reinterpret_cast<const float4*>(base + (r0 + i) * kD + c0);
+    for (int i = 0; i < 8; ++i) {
+        const float4 x = *reinterpret_cast<const float4*>(base + (r0 + i) * ld + c0);
         S[i][0] = x.x; S[i][1] = x.y; S[i][2] = x.z; S[i][3] = x.w;
     }
 }
-__device__ __forceinline__ void tile_store(const float (&S)[16][4], float* base, int r0, int c0) {
+__device__ __forceinline__ void tile_store(const float (&S)[8][4], float* base, int ld, int r0, int c0) {
 #pragma unroll
-    for (int i = 0; i < 16; ++i)
-        *reinterpret_cast<float4*>(base + (r0 + i) * kD + c0) = make_float4(S[i][0], S[i][1], S[i][2], S[i][3]);
+    for (int i = 0; i < 8; ++i)
+        *reinterpret_cast<float4*>(base + (r0 + i) * ld + c0) = make_float4(S[i][0], S[i][1], S[i][2], S[i][3]);
 }
 
 template <typename T>
@@ -134,29 +140,33 @@ __global__ void __launch_bounds__(kThreads, 1) backward_kernel(const __grid_cons
     extern __shared__ float4 smem_f4[];
     float* smem = reinterpret_cast<float*>(smem_f4);
     Tok* tks = reinterpret_cast<Tok*>(smem);                       // [kBatch] staged tokens
-    float* red = smem + kBatch * sizeof(Tok) / sizeof(float);      // [8 warps][4 column groups][4 sums][128 rows]
-    float* xcol = red + 8 * 4 * 4 * kD;                            // x = G^T k per column [128]
-    float* sdot = xcol + kD;                                       // [8 warps][4 column groups] partial delta . do
+    float* red = smem + kBatch * sizeof(Tok) / sizeof(float);      // [kParts][4 sums][128 rows]
+    float* xcol = red + kParts * 4 * kD;                           // x = G^T k per column of this CTA [64]
+    float* sdot = xcol + kCols;                                    // [kParts] partial delta . do
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int rg = lane >> 2, cg = lane & 3;
-    const int r0 = 16 * rg, c0 = 16 * warp + 4 * cg;
-    const int bh = blockIdx.x, bi = bh / a.Hv, hv = bh - bi * a.Hv;
+    const int rg = lane >> 1, cg = lane & 1;
+    const int r0 = 8 * rg, lc = 8 * warp + 4 * cg;  // first row; first column within the CTA's 64
+    const int bh = blockIdx.x >> 1, hc = blockIdx.x & 1;
+    const int c0 = kCols * hc + lc;                  // first column within d_v
+    const int bi = bh / a.Hv, hv = bh - bi * a.Hv;
     const int nT = a.T;
     const int nchk = (nT + kChk - 1) / kChk;
-    float* ckpt = a.ckpt + static_cast<size_t>(bh) * (nchk + 1) * kD * kD;
-    float* scratch = a.scratch + static_cast<size_t>(bh) * kChk * kD * kD;
+    const size_t st = static_cast<size_t>(kD) * kCols;  // floats per compact [d_k][64] state copy
+    float* ckpt = a.ckpt + static_cast<size_t>(blockIdx.x) * (nchk + 1) * st;
+    float* scratch = a.scratch + static_cast<size_t>(blockIdx.x) * kChk * st;
+    const size_t sbase = static_cast<size_t>(bh) * kD * kD;  // this head's [d_k][d_v] state
 
     // ---- forward sweep: save the state at every kChk-th token
-    float S[16][4];
-    if (a.s0) tile_load(S, a.s0 + static_cast<size_t>(bh) * kD * kD, r0, c0);
+    float S[8][4];
+    if (a.s0) tile_load(S, a.s0 + sbase, kD, r0, c0);
     else {
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
+        for (int i = 0; i < 8; ++i)
 #pragma unroll
             for (int j = 0; j < 4; ++j) S[i][j] = 0.f;
     }
-    tile_store(S, ckpt, r0, c0);
+    tile_store(S, ckpt, kCols, r0, lc);
     for (int tb = 0; tb < nT; tb += kBatch) {
         const int n = min(kBatch, nT - tb);
         __syncthreads();
@@ -165,31 +175,31 @@ __global__ void __launch_bounds__(kThreads, 1) backward_kernel(const __grid_cons
         for (int j = 0; j < n; ++j) {
             const int t = tb + j;
             forward_step(S, tks[j], r0, c0);
-            if ((t + 1) % kChk == 0 && t + 1 < nT)
-                tile_store(S, ckpt + static_cast<size_t>((t + 1) / kChk) * kD * kD, r0, c0);
+            if ((t + 1) % kChk == 0 && t + 1 < nT) tile_store(S, ckpt + static_cast<size_t>((t + 1) / kChk) * st, kCols, r0, lc);
         }
     }
 
     // ---- backward sweep
-    float G[16][4];  // dL/dS after the token being processed (before its own readout term)
-    if (a.dsT) tile_load(G, a.dsT + static_cast<size_t>(bh) * kD * kD, r0, c0);
+    float G[8][4];  // dL/dS after the token being processed (before its own readout term)
+    if (a.dsT) tile_load(G, a.dsT + sbase, kD, r0, c0);
     else {
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
+        for (int i = 0; i < 8; ++i)
 #pragma unroll
             for (int j = 0; j < 4; ++j) G[i][j] = 0.f;
     }
+    const size_t nsum = static_cast<size_t>(a.B) * nT * a.Hv * kD;  // elements of one partial-sum array
     for (int c = nchk - 1; c >= 0; --c) {
         const int t0 = c * kChk, t1 = min(nT, t0 + kChk);
         // recompute the states before tokens t0 .. t1-1 into the scratch
-        tile_load(S, ckpt + static_cast<size_t>(c) * kD * kD, r0, c0);
+        tile_load(S, ckpt + static_cast<size_t>(c) * st, kCols, r0, lc);
         for (int tb = t0; tb < t1; tb += kBatch) {
             const int n = min(kBatch, t1 - tb);
             __syncthreads();
             stage_tokens<T>(a, bi, hv, tb, n, tks);
             __syncthreads();
             for (int j = 0; j < n; ++j) {
-                tile_store(S, scratch + static_cast<size_t>(tb + j - t0) * kD * kD, r0, c0);
+                tile_store(S, scratch + static_cast<size_t>(tb + j - t0) * st, kCols, r0, lc);
                 if (tb + j + 1 < t1) forward_step(S, tks[j], r0, c0);
             }
         }
@@ -202,11 +212,11 @@ __global__ void __launch_bounds__(kThreads, 1) backward_kernel(const __grid_cons
                 const int t = tb + j;
                 const Tok& tk = tks[j];
                 __syncthreads();  // staged tokens visible; the previous token's reductions have been read
-                float (&Sp)[16][4] = S;  // state before token t
-                tile_load(Sp, scratch + static_cast<size_t>(t - t0) * kD * kD, r0, c0);
+                float (&Sp)[8][4] = S;  // state before token t
+                tile_load(Sp, scratch + static_cast<size_t>(t - t0) * st, kCols, r0, lc);
                 // G += scale q do^T (readout of token t)
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
+                for (int i = 0; i < 8; ++i) {
                     const float qs = a.scale * tk.q[r0 + i];
 #pragma unroll
                     for (int jj = 0; jj < 4; ++jj) G[i][jj] = fmaf(qs, tk.dO[c0 + jj], G[i][jj]);
@@ -214,7 +224,7 @@ __global__ void __launch_bounds__(kThreads, 1) backward_kernel(const __grid_cons
                 // column sums: x = G^T k, r = P^T beta with P = alpha . S_prev
                 float x[4] = {0.f, 0.f, 0.f, 0.f}, r[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
+                for (int i = 0; i < 8; ++i) {
                     const float kk = tk.k[r0 + i], pb = tk.alpha[r0 + i] * tk.beta[r0 + i];
 #pragma unroll
                     for (int jj = 0; jj < 4; ++jj) {
@@ -232,14 +242,14 @@ __global__ void __launch_bounds__(kThreads, 1) backward_kernel(const __grid_cons
                 }
                 if (rg == 0) {
 #pragma unroll
-                    for (int jj = 0; jj < 4; ++jj) xcol[c0 + jj] = x[jj];
-                    sdot[warp * 4 + cg] = sd;
+                    for (int jj = 0; jj < 4; ++jj) xcol[lc + jj] = x[jj];
+                    sdot[warp * 2 + cg] = sd;
                 }
                 // row sums over this thread's 4 columns: G delta, P x, P do, (G - beta x^T) . S_prev;
                 // then G <- alpha (G - beta x^T), the gradient for the state before token t
-                float* rd = red + (warp * 4 + cg) * 4 * kD;
+                float* rd = red + (warp * 2 + cg) * 4 * kD;
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
+                for (int i = 0; i < 8; ++i) {
                     const int row = r0 + i;
                     const float al = tk.alpha[row], be = tk.beta[row];
                     float s_a = 0.f, s_c = 0.f, s_e = 0.f, s_f = 0.f;
@@ -261,10 +271,11 @@ __global__ void __launch_bounds__(kThreads, 1) backward_kernel(const __grid_cons
                 __syncthreads();
                 const size_t vh = ((static_cast<size_t>(bi) * nT + t) * a.Hv + hv) * kD;
                 if (tid < kD) {
+                    // this half's share of dk, dq, db, dg (linear in the columns)
                     const int row = tid;
                     float s_a = 0.f, s_c = 0.f, s_e = 0.f, s_f = 0.f, s_d = 0.f;
 #pragma unroll 4
-                    for (int p = 0; p < 32; ++p) {
+                    for (int p = 0; p < kParts; ++p) {
                         const float* rp = red + p * 4 * kD;
                         s_a += rp[row];
                         s_c += rp[kD + row];
@@ -274,31 +285,34 @@ __global__ void __launch_bounds__(kThreads, 1) backward_kernel(const __grid_cons
                     }
                     const float kk = tk.k[row], bb = tk.b[row];
                     const float dbeta = -s_c;
-                    a.dk_ws[vh + row] = s_a + bb * dbeta;
-                    a.dq_ws[vh + row] = a.scale * (s_e + kk * s_d);
-                    static_cast<T*>(a.db)[vh + row] = from_f32<T>(kk * dbeta);
-                    static_cast<T*>(a.dg)[vh + row] = from_f32<T>(tk.alpha[row] * s_f);
-                } else {
-                    const int col = tid - kD;
+                    float* pp = a.part + static_cast<size_t>(hc) * nsum + vh + row;
+                    pp[0] = a.scale * (s_e + kk * s_d);  // dq
+                    pp[2 * nsum] = s_a + bb * dbeta;     // dk
+                    pp[4 * nsum] = kk * dbeta;           // db
+                    pp[6 * nsum] = tk.alpha[row] * s_f;  // dg
+                } else if (tid < kD + kCols) {
+                    const int col = tid - kD, gc = kCols * hc + col;
                     const float xx = xcol[col];
-                    static_cast<T*>(a.dv)[vh + col] = from_f32<T>(tk.w[col] * xx);
-                    static_cast<T*>(a.dw)[vh + col] = from_f32<T>(tk.v[col] * xx);
+                    static_cast<T*>(a.dv)[vh + gc] = from_f32<T>(tk.w[gc] * xx);
+                    static_cast<T*>(a.dw)[vh + gc] = from_f32<T>(tk.v[gc] * xx);
                 }
             }
         }
     }
-    if (a.ds0) tile_store(G, a.ds0 + static_cast<size_t>(bh) * kD * kD, r0, c0);
+    if (a.ds0) tile_store(G, a.ds0 + sbase, kD, r0, c0);
 }
 
-// dq, dk of key head h_k = sums over the value heads of its group
+// dq, dk of key head h_k = sums over the two column halves and the value heads of its group; db, dg =
+// sums over the two halves. part = [dq, dk, db, dg][half][B, T, H_v, 128].
 template <typename T>
-__global__ void __launch_bounds__(256) group_sum_kernel(const float* __restrict__ dq_ws, const float* __restrict__ dk_ws,
-                                                       T* __restrict__ dq, T* __restrict__ dk, long long rows, int Hk,
-                                                       int Hv) {
+__global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ part, T* __restrict__ dq,
+                                                     T* __restrict__ dk, T* __restrict__ db, T* __restrict__ dg,
+                                                     long long rows, int Hk, int Hv) {
     const int group = Hv / Hk;
-    const long long n = rows * Hk * kD;
-    for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n;
-         i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const size_t nsum = static_cast<size_t>(rows) * Hv * kD;
+    const long long nk = rows * Hk * kD, nv = rows * Hv * kD;
+    const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+    for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < nk; i += stride) {
         const int c = static_cast<int>(i % kD);
         const long long rh = i / kD;
         const int hk = static_cast<int>(rh % Hk);
@@ -306,27 +320,29 @@ __global__ void __launch_bounds__(256) group_sum_kernel(const float* __restrict_
         float sq = 0.f, sk = 0.f;
         for (int m = 0; m < group; ++m) {
             const size_t src = ((static_cast<size_t>(r) * Hv) + hk * group + m) * kD + c;
-            sq += dq_ws[src];
-            sk += dk_ws[src];
+            sq += part[src] + part[nsum + src];
+            sk += part[2 * nsum + src] + part[3 * nsum + src];
         }
         dq[i] = from_f32<T>(sq);
         dk[i] = from_f32<T>(sk);
     }
+    for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < nv; i += stride) {
+        db[i] = from_f32<T>(part[4 * nsum + i] + part[5 * nsum + i]);
+        dg[i] = from_f32<T>(part[6 * nsum + i] + part[7 * nsum + i]);
+    }
 }
 
 struct BwdLayout {
-    size_t ckpt, scratch, dq, dk, total;
+    size_t ckpt, scratch, part, total;
 };
 BwdLayout bwd_layout(int B, int T, int Hv) {
-    const size_t heads = static_cast<size_t>(B) * Hv, st = static_cast<size_t>(kD) * kD * 4;
+    const size_t ctas = static_cast<size_t>(B) * Hv * 2, st = static_cast<size_t>(kD) * kCols * 4;
     const size_t nchk = (T + kChk - 1) / kChk;
     BwdLayout L;
     L.ckpt = 0;
-    L.scratch = align_up(heads * (nchk + 1) * st, 256);
-    L.dq = align_up(L.scratch + heads * kChk * st, 256);
-    const size_t g = static_cast<size_t>(B) * T * Hv * kD * 4;
-    L.dk = align_up(L.dq + g, 256);
-    L.total = align_up(L.dk + g, 256);
+    L.scratch = align_up(ctas * (nchk + 1) * st, 256);
+    L.part = align_up(L.scratch + ctas * kChk * st, 256);
+    L.total = align_up(L.part + 8 * static_cast<size_t>(B) * T * Hv * kD * 4, 256);
     return L;
 }
 
@@ -382,31 +398,31 @@ gdn2_status gdn2_backward(const void* q, const void* k, const void* v, const voi
     BwdArgs a;
     a.q = q; a.k = k; a.v = v; a.g = g; a.b = b; a.w = w; a.dout = d_o;
     a.s0 = initial_state; a.dsT = d_final_state;
-    a.dq_ws = reinterpret_cast<float*>(ws + L.dq);
-    a.dk_ws = reinterpret_cast<float*>(ws + L.dk);
+    a.part = reinterpret_cast<float*>(ws + L.part);
     a.dv = dv; a.dg = dg; a.db = db; a.dw = dw; a.ds0 = d_initial_state;
     a.ckpt = reinterpret_cast<float*>(ws + L.ckpt);
     a.scratch = reinterpret_cast<float*>(ws + L.scratch);
     a.B = B; a.T = T; a.Hk = Hk; a.Hv = Hv; a.scale = scale;
-    const size_t smem = kBatch * sizeof(Tok) + (8 * 4 * 4 * kD + kD + 32) * sizeof(float);
+    const size_t smem = kBatch * sizeof(Tok) + (kParts * 4 * kD + kCols + kParts) * sizeof(float);
     cudaError_t e;
     const long long rows = static_cast<long long>(B) * T;
-    const long long n = rows * Hk * kD;
+    const long long n = rows * Hv * kD;
     const int gs = static_cast<int>(n / 256 + 1 < 4096 ? n / 256 + 1 : 4096);
     if (dt == GDN2_BF16) {
         e = cudaFuncSetAttribute(backward_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return GDN2_ERR_CUDA;
-        backward_kernel<__nv_bfloat16><<<B * Hv, kThreads, smem, s>>>(a);
+        backward_kernel<__nv_bfloat16><<<2 * B * Hv, kThreads, smem, s>>>(a);
         if (cudaGetLastError() != cudaSuccess) return GDN2_ERR_CUDA;
-        group_sum_kernel<__nv_bfloat16><<<gs, 256, 0, s>>>(a.dq_ws, a.dk_ws, static_cast<__nv_bfloat16*>(dq),
-                                                           static_cast<__nv_bfloat16*>(dk), rows, Hk, Hv);
+        combine_kernel<__nv_bfloat16><<<gs, 256, 0, s>>>(a.part, static_cast<__nv_bfloat16*>(dq),
+                                                         static_cast<__nv_bfloat16*>(dk), static_cast<__nv_bfloat16*>(db),
+                                                         static_cast<__nv_bfloat16*>(dg), rows, Hk, Hv);
     } else {
         e = cudaFuncSetAttribute(backward_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return GDN2_ERR_CUDA;
-        backward_kernel<float><<<B * Hv, kThreads, smem, s>>>(a);
+        backward_kernel<float><<<2 * B * Hv, kThreads, smem, s>>>(a);
         if (cudaGetLastError() != cudaSuccess) return GDN2_ERR_CUDA;
-        group_sum_kernel<float><<<gs, 256, 0, s>>>(a.dq_ws, a.dk_ws, static_cast<float*>(dq), static_cast<float*>(dk),
-                                                   rows, Hk, Hv);
+        combine_kernel<float><<<gs, 256, 0, s>>>(a.part, static_cast<float*>(dq), static_cast<float*>(dk),
+                                                 static_cast<float*>(db), static_cast<float*>(dg), rows, Hk, Hv);
     }
     return cudaGetLastError() == cudaSuccess ? GDN2_OK : GDN2_ERR_CUDA;
 }

@@ -247,7 +247,8 @@ gdn2_status gdn2_mixer_epilogue(const void* o, const void* z, const float* weigh
  * and optionally d_final_state of S_T: the gradients of sum(o * d_o) + sum(S_T * d_final_state).
  * Exact reverse mode of the per-token recurrence in fp32 (not the chunked form): a forward sweep
  * keeps the state at every 32nd token in the workspace, each stretch of 32 tokens is recomputed and
- * walked backward; one CTA per (batch, value head). The forward outputs are not needed.
+ * walked backward; two CTAs per (batch, value head), 64 columns of d_v each, whose sums over d_v
+ * (for dq, dk, db, dg) a second kernel adds in a fixed order. The forward outputs are not needed.
  * q, k, dq, dk: [B, T, H_k, d_k]; v, w, d_o, dv, dw: [B, T, H_v, d_v]; g, b, dg, db: [B, T, H_v, d_k]
  * (all dtype dt); initial_state, d_final_state, d_initial_state: fp32 [B, H_v, d_k, d_v] or NULL
  * (zeros / not written). dq and dk of a key head sum its value heads. d_k = d_v = 128.
