@@ -203,7 +203,10 @@ __global__ void __launch_bounds__(kThreads, 1) backward_kernel(const __grid_cons
                 if (tb + j + 1 < t1) forward_step(S, tks[j], r0, c0);
             }
         }
-        // walk back, kBatch tokens staged at a time (highest first)
+        // walk back, kBatch tokens staged at a time (highest first); the state before the next token
+        // is loaded from the scratch one token ahead
+        float Sn[8][4];
+        tile_load(Sn, scratch + static_cast<size_t>(t1 - 1 - t0) * st, kCols, r0, lc);
         for (int te = t1; te > t0; te -= kBatch) {
             const int tb = max(t0, te - kBatch), n = te - tb;
             __syncthreads();
@@ -213,7 +216,11 @@ __global__ void __launch_bounds__(kThreads, 1) backward_kernel(const __grid_cons
                 const Tok& tk = tks[j];
                 __syncthreads();  // staged tokens visible; the previous token's reductions have been read
                 float (&Sp)[8][4] = S;  // state before token t
-                tile_load(Sp, scratch + static_cast<size_t>(t - t0) * st, kCols, r0, lc);
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+#pragma unroll
+                    for (int jj = 0; jj < 4; ++jj) Sp[i][jj] = Sn[i][jj];
+                if (t - 1 >= t0) tile_load(Sn, scratch + static_cast<size_t>(t - 1 - t0) * st, kCols, r0, lc);
                 // G += scale q do^T (readout of token t)
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
