@@ -150,19 +150,19 @@ __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.comm
 __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
-// acc[i][c] += sum_{k = 4 g0}^{4 g1 - 1} L[i][k] R[k][c] for a 4 x 4 register tile (fp32 smem, 16-byte aligned
-// rows ldl / ldr floats apart). Each 16-byte load feeds 16 FMAs; k runs upwards, one FMA per term.
-__device__ __forceinline__ void tile4_times(const float* L, int ldl, const float* R, int ldr, int g0, int g1,
-                                            float (&acc)[4][4]) {
+// acc[i][c] += sum_{k = 4 g0}^{4 g1 - 1} L[i][k] R[k][c] for a 2 x 4 register tile (fp32 smem, 16-byte
+// aligned rows ldl / ldr floats apart); k runs upwards, one FMA per term.
+__device__ __forceinline__ void tile24_times(const float* L, int ldl, const float* R, int ldr, int g0, int g1,
+                                             float (&acc)[2][4]) {
 #pragma unroll 2
     for (int g = g0; g < g1; ++g) {
-        float4 l[4], r[4];
+        float4 l[2], r[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) l[i] = *reinterpret_cast<const float4*>(L + i * ldl + 4 * g);
+        for (int i = 0; i < 2; ++i) l[i] = *reinterpret_cast<const float4*>(L + i * ldl + 4 * g);
 #pragma unroll
         for (int j = 0; j < 4; ++j) r[j] = *reinterpret_cast<const float4*>(R + (4 * g + j) * ldr);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
+        for (int i = 0; i < 2; ++i) {
             const float a[4] = {l[i].x, l[i].y, l[i].z, l[i].w};
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
@@ -174,11 +174,10 @@ __device__ __forceinline__ void tile4_times(const float* L, int ldl, const float
         }
     }
 }
-__device__ __forceinline__ void tile4_store(float* D, int ldd, const float (&acc)[4][4], float sgn) {
+__device__ __forceinline__ void tile24_store(float* D, int ldd, const float (&acc)[2][4], float sgn) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
-        *reinterpret_cast<float4*>(D + i * ldd) =
-            make_float4(sgn * acc[i][0], sgn * acc[i][1], sgn * acc[i][2], sgn * acc[i][3]);
+    for (int i = 0; i < 2; ++i)
+        *reinterpret_cast<float4*>(D + i * ldd) = make_float4(sgn * acc[i][0], sgn * acc[i][1], sgn * acc[i][2], sgn * acc[i][3]);
 }
 
 __global__ void __launch_bounds__(fs::kThreads, 3)
@@ -406,34 +405,36 @@ __global__ void __launch_bounds__(fs::kThreads, 3)
             for (int i = 0; i < 16; ++i) TF[(base + i) * fs::LDF + base + jj] = x[i];
         }
         __syncthreads();
-        // Products below run as 4 x 4 register tiles. A skipped k-range multiplies entries of a lower
-        // triangular factor that are exactly zero, so bounds stay warp-uniform and the sums are unchanged.
-        if (warp < 2 && lane < 16) {  // Y_i = A_{i+1,i} D_i for diagonal blocks i = 0, 2 (warp = block)
-            const int i0 = 32 * warp, r0 = 4 * (lane >> 2), c0 = 4 * (lane & 3);
-            float acc[4][4] = {};
-            tile4_times(AF + (i0 + 16 + r0) * fs::LDF + i0, fs::LDF, TF + i0 * fs::LDF + i0 + c0, fs::LDF, 0, 4, acc);
-            tile4_store(PF + (16 * warp + r0) * fs::LDP + c0, fs::LDP, acc, 1.f);
+        // Products below run as 2 x 4 register tiles (each 16-byte load feeds 8 FMAs; 64 or 128 threads
+        // share a product, which measured faster than 4 x 4 tiles on fewer threads or 1 x 4 on all 8
+        // warps). A skipped k-range multiplies entries of a lower triangular factor that are exactly
+        // zero, so bounds stay warp-uniform and the sums are unchanged.
+        if (warp < 2) {  // Y_i = A_{i+1,i} D_i for diagonal blocks i = 0, 2 (warp = block, 2 x 4 tiles)
+            const int i0 = 32 * warp, r0 = 2 * (lane >> 2), c0 = 4 * (lane & 3);
+            float acc[2][4] = {};
+            tile24_times(AF + (i0 + 16 + r0) * fs::LDF + i0, fs::LDF, TF + i0 * fs::LDF + i0 + c0, fs::LDF, 0, 4, acc);
+            tile24_store(PF + (16 * warp + r0) * fs::LDP + c0, fs::LDP, acc, 1.f);
         }
         __syncthreads();
-        if (warp < 2 && lane < 16) {  // T_{i+1,i} = -D_{i+1} Y_i
-            const int i1 = 32 * warp + 16, r0 = 4 * (lane >> 2), c0 = 4 * (lane & 3);
-            float acc[4][4] = {};
-            tile4_times(TF + (i1 + r0) * fs::LDF + i1, fs::LDF, PF + 16 * warp * fs::LDP + c0, fs::LDP, 0, 4, acc);
-            tile4_store(TF + (i1 + r0) * fs::LDF + i1 - 16 + c0, fs::LDF, acc, -1.f);
+        if (warp < 2) {  // T_{i+1,i} = -D_{i+1} Y_i
+            const int i1 = 32 * warp + 16, r0 = 2 * (lane >> 2), c0 = 4 * (lane & 3);
+            float acc[2][4] = {};
+            tile24_times(TF + (i1 + r0) * fs::LDF + i1, fs::LDF, PF + 16 * warp * fs::LDP + c0, fs::LDP, 0, 4, acc);
+            tile24_store(TF + (i1 + r0) * fs::LDF + i1 - 16 + c0, fs::LDF, acc, -1.f);
         }
         __syncthreads();
-        if (warp < 2) {  // X = A_10 T_00 (32 x 32): warp w takes columns 16w.., where T_00 is zero above row 16w
-            const int r0 = 4 * (lane >> 2), c0 = 16 * warp + 4 * (lane & 3);
-            float acc[4][4] = {};
-            tile4_times(AF + (32 + r0) * fs::LDF, fs::LDF, TF + c0, fs::LDF, 4 * warp, 8, acc);
-            tile4_store(PF + r0 * fs::LDP + c0, fs::LDP, acc, 1.f);
+        if (warp < 4) {  // X = A_10 T_00: warp w takes columns 8w.. (2 x 4 tiles)
+            const int r0 = 2 * (lane >> 1), c0 = 8 * warp + 4 * (lane & 1);
+            float acc[2][4] = {};
+            tile24_times(AF + (32 + r0) * fs::LDF, fs::LDF, TF + c0, fs::LDF, 2 * warp, 8, acc);
+            tile24_store(PF + r0 * fs::LDP + c0, fs::LDP, acc, 1.f);
         }
         __syncthreads();
-        if (warp < 2) {  // T_10 = -T_11 X: warp w takes rows 16w.., where T_11 is zero right of column 16w + 15
-            const int r0 = 16 * warp + 4 * (lane >> 3), c0 = 4 * (lane & 7);
-            float acc[4][4] = {};
-            tile4_times(TF + (32 + r0) * fs::LDF + 32, fs::LDF, PF + c0, fs::LDP, 0, 4 * (warp + 1), acc);
-            tile4_store(TF + (32 + r0) * fs::LDF + c0, fs::LDF, acc, -1.f);
+        if (warp < 4) {  // T_10 = -T_11 X: warp w takes rows 8w.. (2 x 4 tiles)
+            const int r0 = 8 * warp + 2 * (lane >> 3), c0 = 4 * (lane & 7);
+            float acc[2][4] = {};
+            tile24_times(TF + (32 + r0) * fs::LDF + 32, fs::LDF, PF + c0, fs::LDP, 0, 2 * (warp + 1), acc);
+            tile24_store(TF + (32 + r0) * fs::LDF + c0, fs::LDF, acc, -1.f);
         }
         __syncthreads();
         for (int p = tid; p < 64 * 8; p += fs::kThreads) {  // bf16 T, K-major rows (one 16-byte chunk per item)
