@@ -72,6 +72,22 @@ def test_prologue_parity(g, dtype, d, neg):
         assert np.array_equal(got.cpu().numpy().astype(np.float64), want)   # copies of stored samples
 
 
+@pytest.mark.parametrize("B,T", [(3, 2), (1, 129), (2, 256)])
+def test_prologue_tile_edges(g, B, T):
+    """The conv works on 128-token tiles with a 3-sample halo: sequences shorter than the halo, one
+    token past a tile, and whole tiles across several batch rows."""
+    import torch
+
+    rng = np.random.default_rng(100 + T)
+    Hk, Hv, d = 1, 2, 128
+    xs, ws, gates, states = _raw(rng, B, T, Hk, Hv, d, d, "bf16")
+    outs = _run_prologue(g, xs, ws, gates, [_f32dev(s) for s in states], "bf16", False)
+    torch.cuda.synchronize()
+    ref = mixer.prologue(*xs, *ws, *gates, states=states)
+    for name, got, want in zip("qkvgbw", outs, ref[:6]):
+        assert max_rel_err(H.to_np(got), want) < 1e-2, (name, T)
+
+
 def test_prologue_state_chaining_is_exact(g):
     """One call over 70 tokens equals calls over 33, 1 and 36 tokens that carry the conv state."""
     import torch
