@@ -36,7 +36,7 @@ FLUSH_BYTES = 256 << 20  # > 129 MB L2
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one gdn2_chunk_fwd on this
 # workload, from a single-pass ncu capture of factors_tc + state_tc. Reported only while the
 # tensor-core kernel source is the one that was measured.
-TRAFFIC_RECORD = {"chunk_tc_sha256_16": "b7dd8ab9dc67c586", "bytes": 1736506368 + 2217438464 + 3247258624 + 523793408}
+TRAFFIC_RECORD = {"chunk_tc_sha256_16": "ddb383fe32ca4778", "bytes": 1732167936 + 2190468608 + 3254820096 + 523984384}
 
 
 def recorded_traffic():
