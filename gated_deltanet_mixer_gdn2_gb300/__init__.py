@@ -26,6 +26,7 @@ EXPORTS = (
     "gdn2_recurrent_step", "gdn2_last_device_status", "gdn2_set_wait_limit", "gdn2_selftest_umma",
     "gdn2_chunk_fwd_noalloc", "gdn2_recurrent_update", "gdn2_fg2_inputs", "gdn2_mixer_prologue",
     "gdn2_mixer_epilogue", "gdn2_backward_workspace_size", "gdn2_backward",
+    "gdn2_backward_recurrent_workspace_size", "gdn2_backward_recurrent",
 )
 
 
@@ -60,6 +61,8 @@ def _load() -> ctypes.CDLL:
         "gdn2_mixer_epilogue": (I, [P, P, P, F, P] + [I] * 4 + [I, P]),
         "gdn2_backward_workspace_size": (Z, [I] * 6 + [I]),
         "gdn2_backward": (I, [P] * 16 + [I] * 6 + [F, I, P, Z, P]),
+        "gdn2_backward_recurrent_workspace_size": (Z, [I] * 6 + [I]),
+        "gdn2_backward_recurrent": (I, [P] * 16 + [I] * 6 + [F, I, P, Z, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -255,33 +258,37 @@ def gdn2_mixer_epilogue(o, z, weight, y, *, eps=1e-5, stream=None):
 
 
 def gdn2_backward(q, k, v, g, b, w, d_o, dq, dk, dv, dg, db, dw, initial_state=None, d_final_state=None,
-                  d_initial_state=None, *, scale=1.0, workspace=None, stream=None):
-    """Gradients of the core (C ABI gdn2_backward); writes dq, dk, dv, dg, db, dw and, if given,
-    d_initial_state. Shapes as gdn2_chunk_fwd's inputs; states fp32 [B, H_v, d_k, d_v]."""
+                  d_initial_state=None, *, scale=1.0, workspace=None, stream=None, recurrent=False):
+    """Gradients of the core (C ABI gdn2_backward, or gdn2_backward_recurrent when `recurrent`);
+    writes dq, dk, dv, dg, db, dw and, if given, d_initial_state. Shapes as gdn2_chunk_fwd's
+    inputs; states fp32 [B, H_v, d_k, d_v]."""
     import torch
 
     B, T, Hk, dk_ = q.shape
     Hv, dv_ = v.shape[2], v.shape[3]
     dt = _dtype_code(q)
-    need = lib.gdn2_backward_workspace_size(B, T, Hk, Hv, dk_, dv_, dt)
+    size_fn = lib.gdn2_backward_recurrent_workspace_size if recurrent else lib.gdn2_backward_workspace_size
+    fn = lib.gdn2_backward_recurrent if recurrent else lib.gdn2_backward
+    need = size_fn(B, T, Hk, Hv, dk_, dv_, dt)
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
-    st = lib.gdn2_backward(*(_ptr(t) for t in (q, k, v, g, b, w, initial_state, d_o, d_final_state, dq, dk, dv, dg,
-                                               db, dw, d_initial_state)),
-                           B, T, Hk, Hv, dk_, dv_, float(scale), dt, _ptr(workspace), workspace.numel(),
-                           _stream(stream))
-    _check(st, "gdn2_backward")
+    st = fn(*(_ptr(t) for t in (q, k, v, g, b, w, initial_state, d_o, d_final_state, dq, dk, dv, dg, db, dw,
+                                d_initial_state)),
+            B, T, Hk, Hv, dk_, dv_, float(scale), dt, _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(st, "gdn2_backward_recurrent" if recurrent else "gdn2_backward")
     return dq, dk, dv, dg, db, dw
 
 
-def backward(q, k, v, g, b, w, d_o, initial_state=None, d_final_state=None, *, scale=1.0, stream=None):
+def backward(q, k, v, g, b, w, d_o, initial_state=None, d_final_state=None, *, scale=1.0, stream=None,
+             recurrent=False):
     """Returns (dq, dk, dv, dg, db, dw, d_initial_state)."""
     import torch
 
     outs = [torch.empty_like(t) for t in (q, k, v, g, b, w)]
     B, Hv, dk_, dv_ = q.shape[0], v.shape[2], q.shape[3], v.shape[3]
     ds0 = torch.empty((B, Hv, dk_, dv_), dtype=torch.float32, device=q.device)
-    gdn2_backward(q, k, v, g, b, w, d_o, *outs, initial_state, d_final_state, ds0, scale=scale, stream=stream)
+    gdn2_backward(q, k, v, g, b, w, d_o, *outs, initial_state, d_final_state, ds0, scale=scale, stream=stream,
+                  recurrent=recurrent)
     return (*outs, ds0)
 
 

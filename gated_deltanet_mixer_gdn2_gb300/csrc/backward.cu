@@ -363,22 +363,19 @@ bool bwd_shape_ok(int B, int T, int Hk, int Hv, int dk, int dv) {
 
 using namespace gdn2;
 
-extern "C" {
+namespace {
 
-size_t gdn2_backward_workspace_size(int B, int T, int Hk, int Hv, int dk, int dv, gdn2_dtype dt) {
-    if ((dt != GDN2_F32 && dt != GDN2_BF16) || !bwd_shape_ok(B, T, Hk, Hv, dk, dv) || B == 0 || T == 0) return 0;
-    return bwd_layout(B, T, Hv).total;
-}
-
-gdn2_status gdn2_backward(const void* q, const void* k, const void* v, const void* g, const void* b, const void* w,
-                          const float* initial_state, const void* d_o, const float* d_final_state, void* dq, void* dk,
-                          void* dv, void* dg, void* db, void* dw, float* d_initial_state, int B, int T, int Hk, int Hv,
-                          int d_k, int d_v, float scale, gdn2_dtype dt, void* workspace, size_t ws_bytes,
-                          void* stream) {
+// Checks shared by both entry points; handles the empty sequence (dS0 = dS_T). Returns GDN2_OK with
+// *done = false when the caller should launch.
+gdn2_status check_and_trivial(const void* q, const void* k, const void* v, const void* g, const void* b, const void* w,
+                              const float* initial_state, const void* d_o, const float* d_final_state, void* dq,
+                              void* dk, void* dv, void* dg, void* db, void* dw, float* d_initial_state, int B, int T,
+                              int Hk, int Hv, int d_k, int d_v, gdn2_dtype dt, void* workspace, size_t ws_bytes,
+                              size_t need, cudaStream_t s, bool* done) {
+    *done = true;
     if (dt != GDN2_F32 && dt != GDN2_BF16) return GDN2_ERR_INVALID_ARG;
     if (B < 0 || T < 0 || Hk <= 0 || Hv <= 0 || d_k <= 0 || d_v <= 0 || Hv % Hk) return GDN2_ERR_INVALID_ARG;
     if (!bwd_shape_ok(B, T, Hk, Hv, d_k, d_v)) return GDN2_ERR_UNSUPPORTED;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
     const size_t state_bytes = sizeof(float) * static_cast<size_t>(B) * Hv * d_k * d_v;
     if (B == 0 || T == 0) {  // no tokens: dS0 = dS_T
         if (d_initial_state && state_bytes) {
@@ -398,9 +395,57 @@ gdn2_status gdn2_backward(const void* q, const void* k, const void* v, const voi
     if ((initial_state && !aligned16(initial_state)) || (d_final_state && !aligned16(d_final_state)) ||
         (d_initial_state && !aligned16(d_initial_state)))
         return GDN2_ERR_MISALIGNED;
-    const BwdLayout L = bwd_layout(B, T, Hv);
-    if (!workspace || ws_bytes < L.total) return GDN2_ERR_WORKSPACE;
+    if (!workspace || ws_bytes < need) return GDN2_ERR_WORKSPACE;
     if (!aligned16(workspace)) return GDN2_ERR_MISALIGNED;
+    *done = false;
+    return GDN2_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t gdn2_backward_workspace_size(int B, int T, int Hk, int Hv, int dk, int dv, gdn2_dtype dt) {
+    if ((dt != GDN2_F32 && dt != GDN2_BF16) || !bwd_shape_ok(B, T, Hk, Hv, dk, dv) || B == 0 || T == 0) return 0;
+    return backward_chunked_workspace_bytes(B, T, Hv);
+}
+
+gdn2_status gdn2_backward(const void* q, const void* k, const void* v, const void* g, const void* b, const void* w,
+                          const float* initial_state, const void* d_o, const float* d_final_state, void* dq, void* dk,
+                          void* dv, void* dg, void* db, void* dw, float* d_initial_state, int B, int T, int Hk, int Hv,
+                          int d_k, int d_v, float scale, gdn2_dtype dt, void* workspace, size_t ws_bytes,
+                          void* stream) {
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    bool done;
+    const size_t need = bwd_shape_ok(B, T, Hk, Hv, d_k, d_v) && B > 0 && T > 0 ? backward_chunked_workspace_bytes(B, T, Hv) : 0;
+    const gdn2_status st = check_and_trivial(q, k, v, g, b, w, initial_state, d_o, d_final_state, dq, dk, dv, dg, db,
+                                             dw, d_initial_state, B, T, Hk, Hv, d_k, d_v, dt, workspace, ws_bytes, need,
+                                             s, &done);
+    if (done) return st;
+    return launch_backward_chunked(q, k, v, g, b, w, initial_state, d_o, d_final_state, dq, dk, dv, dg, db, dw,
+                                   d_initial_state, B, T, Hk, Hv, scale, dt, workspace, s) == cudaSuccess
+               ? GDN2_OK
+               : GDN2_ERR_CUDA;
+}
+
+size_t gdn2_backward_recurrent_workspace_size(int B, int T, int Hk, int Hv, int dk, int dv, gdn2_dtype dt) {
+    if ((dt != GDN2_F32 && dt != GDN2_BF16) || !bwd_shape_ok(B, T, Hk, Hv, dk, dv) || B == 0 || T == 0) return 0;
+    return bwd_layout(B, T, Hv).total;
+}
+
+gdn2_status gdn2_backward_recurrent(const void* q, const void* k, const void* v, const void* g, const void* b,
+                                    const void* w, const float* initial_state, const void* d_o,
+                                    const float* d_final_state, void* dq, void* dk, void* dv, void* dg, void* db,
+                                    void* dw, float* d_initial_state, int B, int T, int Hk, int Hv, int d_k, int d_v,
+                                    float scale, gdn2_dtype dt, void* workspace, size_t ws_bytes, void* stream) {
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    bool done;
+    const size_t need = bwd_shape_ok(B, T, Hk, Hv, d_k, d_v) && B > 0 && T > 0 ? bwd_layout(B, T, Hv).total : 0;
+    const gdn2_status st = check_and_trivial(q, k, v, g, b, w, initial_state, d_o, d_final_state, dq, dk, dv, dg, db,
+                                             dw, d_initial_state, B, T, Hk, Hv, d_k, d_v, dt, workspace, ws_bytes, need,
+                                             s, &done);
+    if (done) return st;
+    const BwdLayout L = bwd_layout(B, T, Hv);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     BwdArgs a;
     a.q = q; a.k = k; a.v = v; a.g = g; a.b = b; a.w = w; a.dout = d_o;

@@ -25,26 +25,12 @@ namespace {
 
 __device__ int g_status_simt;
 
-struct SimtWs {
-    int dk, dv, C;
-    __host__ __device__ size_t unit_floats() const {
-        size_t n = 3 * (size_t)dk * C + (size_t)C * C + (size_t)dv * C + dk;
-        return (n + 3) & ~size_t(3);
-    }
-    __host__ __device__ size_t off_wt() const { return 0; }
-    __host__ __device__ size_t off_qbt() const { return (size_t)dk * C; }
-    __host__ __device__ size_t off_kht() const { return 2 * (size_t)dk * C; }
-    __host__ __device__ size_t off_m() const { return 3 * (size_t)dk * C; }
-    __host__ __device__ size_t off_utt() const { return 3 * (size_t)dk * C + (size_t)C * C; }
-    __host__ __device__ size_t off_gam() const { return 3 * (size_t)dk * C + (size_t)C * C + (size_t)dv * C; }
-};
-
 template <typename Tin>
 __global__ void __launch_bounds__(256) factors_simt_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k,
                                                            const Tin* __restrict__ v, const Tin* __restrict__ g,
                                                            const Tin* __restrict__ b, const Tin* __restrict__ w,
-                                                           float* __restrict__ ws, int T, int Hk, int Hv, int dk,
-                                                           int dv, int C) {
+                                                           float* __restrict__ ws, float* __restrict__ t_out, int T,
+                                                           int Hk, int Hv, int dk, int dv, int C) {
     extern __shared__ float smem[];
     const int n = blockIdx.x;                // chunk
     const int bh = blockIdx.y;               // bi * Hv + hv
@@ -155,13 +141,19 @@ __global__ void __launch_bounds__(256) factors_simt_kernel(const Tin* __restrict
         for (int j = 0; j <= i; ++j) acc = fmaf(sT[i * (C + 1) + j], sQ[j * LDQ + c], acc);
         u[L.off_utt() + p] = acc;
     }
+    if (t_out)  // T = (I + A)^{-1} [C][C] for the gradients
+        for (int p = tid; p < C * C; p += nt) {
+            const int i = p / C, j = p - i * C;
+            t_out[((size_t)bh * NC + n) * C * C + p] = sT[i * (C + 1) + j];
+        }
 }
 
 constexpr int kSlice = 16;
 
 template <typename Tin>
 __global__ void __launch_bounds__(256) state_simt_kernel(const float* __restrict__ ws, const float* __restrict__ s0,
-                                                         float* __restrict__ sT_out, Tin* __restrict__ o, int T,
+                                                         float* __restrict__ sT_out, Tin* __restrict__ o,
+                                                         float* __restrict__ s_save, float* __restrict__ u_save, int T,
                                                          int Hv, int dk, int dv, int C, int NC, float scale) {
     extern __shared__ float smem[];
     const int bh = blockIdx.x;
@@ -194,6 +186,11 @@ __global__ void __launch_bounds__(256) state_simt_kernel(const float* __restrict
         for (int p = tid; p < C * C; p += nt) sM[p] = u[L.off_m() + p];
         for (int p = tid; p < kSlice * C; p += nt) sUt[p] = u[L.off_utt() + (size_t)col0 * C + p];
         for (int p = tid; p < dk; p += nt) sGam[p] = u[L.off_gam() + p];
+        if (s_save)  // S_n, the state entering the chunk, for the gradients
+            for (int p = tid; p < dk * kSlice; p += nt) {
+                const int c = p / kSlice, j = p - c * kSlice;
+                s_save[(((size_t)bh * NC + n) * dk + c) * dv + col0 + j] = sS[p];
+            }
         __syncthreads();
         // U = U~ - W S_n ;  P = (q . e^{G}) S_n
         for (int p = tid; p < C * kSlice; p += nt) {
@@ -206,13 +203,14 @@ __global__ void __launch_bounds__(256) state_simt_kernel(const float* __restrict
             }
             sU[p] = sUt[j * C + i] - ws_;
             sP[p] = qs;
+            if (u_save) u_save[(((size_t)bh * NC + n) * C + i) * dv + col0 + j] = sU[p];
         }
         __syncthreads();
         // O = P + M U ;  S_{n+1} = diag(e^{G_last}) S_n + K^^T U
         for (int p = tid; p < C * kSlice; p += nt) {
             const int i = p / kSlice, j = p - i * kSlice;
             const int tok = n * C + i;
-            if (tok < T) {
+            if (o && tok < T) {
                 float acc = sP[p];
                 for (int l = 0; l <= i; ++l) acc = fmaf(sM[i * C + l], sU[l * kSlice + j], acc);
                 o[(((size_t)bi * T + tok) * Hv + hv) * dv + col0 + j] = from_f32<Tin>(scale * acc);
@@ -244,7 +242,8 @@ size_t state_smem(int dk, int C) {
 
 template <typename Tin>
 cudaError_t launch_t(const void* q, const void* k, const void* v, const void* g, const void* b, const void* w,
-                     const float* s0, float* sT, void* o, const ChunkShape& sh, float scale, void* ws, cudaStream_t s) {
+                     const float* s0, float* sT, void* o, const ChunkShape& sh, float scale, void* ws, cudaStream_t s,
+                     float* t_out = nullptr, float* s_save = nullptr, float* u_save = nullptr) {
     const int NC = sh.nchunks();
     const size_t f_smem = factors_smem(sh.dk, sh.dv, sh.C);
     const size_t s_smem = state_smem(sh.dk, sh.C);
@@ -256,11 +255,12 @@ cudaError_t launch_t(const void* q, const void* k, const void* v, const void* g,
     factors_simt_kernel<Tin><<<dim3(NC, sh.B * sh.Hv), 256, f_smem, s>>>(
         static_cast<const Tin*>(q), static_cast<const Tin*>(k), static_cast<const Tin*>(v),
         static_cast<const Tin*>(g), static_cast<const Tin*>(b), static_cast<const Tin*>(w), static_cast<float*>(ws),
-        sh.T, sh.Hk, sh.Hv, sh.dk, sh.dv, sh.C);
+        t_out, sh.T, sh.Hk, sh.Hv, sh.dk, sh.dv, sh.C);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     state_simt_kernel<Tin><<<dim3(sh.B * sh.Hv, sh.dv / kSlice), 256, s_smem, s>>>(
-        static_cast<const float*>(ws), s0, sT, static_cast<Tin*>(o), sh.T, sh.Hv, sh.dk, sh.dv, sh.C, NC, scale);
+        static_cast<const float*>(ws), s0, sT, static_cast<Tin*>(o), s_save, u_save, sh.T, sh.Hv, sh.dk, sh.dv, sh.C,
+        NC, scale);
     return cudaGetLastError();
 }
 
@@ -276,6 +276,14 @@ cudaError_t launch_chunk_simt(const void* q, const void* k, const void* v, const
                               gdn2_dtype dt, void* ws, cudaStream_t s) {
     if (dt == GDN2_BF16) return launch_t<__nv_bfloat16>(q, k, v, g, b, w, s0, sT, o, sh, scale, ws, s);
     return launch_t<float>(q, k, v, g, b, w, s0, sT, o, sh, scale, ws, s);
+}
+
+cudaError_t launch_chunk_simt_saving(const void* q, const void* k, const void* v, const void* g, const void* b,
+                                     const void* w, const float* s0, const ChunkShape& sh, gdn2_dtype dt, void* ws,
+                                     float* t_out, float* s_save, float* u_save, cudaStream_t s) {
+    if (dt == GDN2_BF16)
+        return launch_t<__nv_bfloat16>(q, k, v, g, b, w, s0, nullptr, nullptr, sh, 1.f, ws, s, t_out, s_save, u_save);
+    return launch_t<float>(q, k, v, g, b, w, s0, nullptr, nullptr, sh, 1.f, ws, s, t_out, s_save, u_save);
 }
 
 int chunk_simt_read_clear_status(cudaStream_t) {

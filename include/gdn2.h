@@ -245,10 +245,14 @@ gdn2_status gdn2_mixer_epilogue(const void* o, const void* z, const float* weigh
  * gdn2_backward -- gradients of the core (dq, dk, dv, dg, db, dw and the initial state) for the
  * recurrence of the burn-gdn2 0.1.5 docs ("Architecture"), given the upstream gradient d_o of o
  * and optionally d_final_state of S_T: the gradients of sum(o * d_o) + sum(S_T * d_final_state).
- * Exact reverse mode of the per-token recurrence in fp32 (not the chunked form): a forward sweep
- * keeps the state at every 32nd token in the workspace, each stretch of 32 tokens is recomputed and
- * walked backward; two CTAs per (batch, value head), 64 columns of d_v each, whose sums over d_v
- * (for dq, dk, db, dg) a second kernel adds in a fixed order. The forward outputs are not needed.
+ * Reverse mode of the chunked (WY / UT) form of the same recurrence ("Gated Delta Networks:
+ * Improving Mamba2 with Delta Rule", section 3.3), in fp32 with chunks of 32 tokens, in four
+ * launches: a forward chain that keeps each chunk's starting state S_n, its U and its T =
+ * (I + A)^-1 in the workspace; a backward chain over the chunks that keeps dS_(n+1) and dU; one CTA
+ * per (chunk, batch, value head) that forms every per-token gradient of its chunk from those; and
+ * a pass that adds the value heads of each key head for dq and dk in a fixed order. The forward
+ * outputs are not needed. Gates enter only as ratios exp(G_t - G_s) with t >= s, so no
+ * intermediate overflows for any g <= 0.
  * q, k, dq, dk: [B, T, H_k, d_k]; v, w, d_o, dv, dw: [B, T, H_v, d_v]; g, b, dg, db: [B, T, H_v, d_k]
  * (all dtype dt); initial_state, d_final_state, d_initial_state: fp32 [B, H_v, d_k, d_v] or NULL
  * (zeros / not written). dq and dk of a key head sum its value heads. d_k = d_v = 128.
@@ -261,6 +265,23 @@ gdn2_status gdn2_backward(const void* q, const void* k, const void* v, const voi
                           void* dk, void* dv, void* dg, void* db, void* dw, float* d_initial_state, int B, int T,
                           int Hk, int Hv, int dk_, int dv_, float scale, gdn2_dtype dt, void* workspace,
                           size_t ws_bytes, void* stream);
+
+/*
+ * gdn2_backward_recurrent -- the same gradients as gdn2_backward (same arguments, layouts and
+ * errors) by exact reverse mode of the per-token recurrence in fp32, without the chunked form: a
+ * forward sweep keeps the state at every 32nd token in the workspace, each stretch of 32 tokens is
+ * recomputed and walked backward; two CTAs per (batch, value head), 64 columns of d_v each, whose
+ * sums over d_v (for dq, dk, db, dg) a second kernel adds in a fixed order. Slower than the chunked
+ * path; it shares none of its arithmetic and serves as an independent cross-check at lengths the
+ * host reference cannot reach. workspace: gdn2_backward_recurrent_workspace_size(...) bytes.
+ */
+size_t gdn2_backward_recurrent_workspace_size(int B, int T, int Hk, int Hv, int dk, int dv, gdn2_dtype dt);
+gdn2_status gdn2_backward_recurrent(const void* q, const void* k, const void* v, const void* g, const void* b,
+                                    const void* w, const float* initial_state, const void* d_o,
+                                    const float* d_final_state, void* dq, void* dk, void* dv, void* dg, void* db,
+                                    void* dw, float* d_initial_state, int B, int T, int Hk, int Hv, int dk_,
+                                    int dv_, float scale, gdn2_dtype dt, void* workspace, size_t ws_bytes,
+                                    void* stream);
 
 /*
  * gdn2_selftest_umma -- diagnostics: one tcgen05 product D[128][N] = A * B (bf16 in, fp32 out)

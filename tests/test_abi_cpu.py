@@ -166,9 +166,11 @@ def test_mixer_argument_errors(g):
     assert epi(ptr=0x10002) == g.GDN2_ERR_MISALIGNED
 
 
-def test_backward_argument_errors(g):
+@pytest.mark.parametrize("entry", ["gdn2_backward", "gdn2_backward_recurrent"])
+def test_backward_argument_errors(g, entry):
     P = lambda a: ctypes.c_void_p(a) if a else None
-    f = lambda ptr=0x10000, B=1, T=4, Hk=1, Hv=2, dk=128, dv=128, dt=1, ws=0x10000, wsb=1 << 40: g.lib.gdn2_backward(
+    fn = getattr(g.lib, entry)
+    f = lambda ptr=0x10000, B=1, T=4, Hk=1, Hv=2, dk=128, dv=128, dt=1, ws=0x10000, wsb=1 << 40: fn(
         *(P(ptr),) * 6, None, P(ptr), None, *(P(ptr),) * 6, None, B, T, Hk, Hv, dk, dv, 1.0, dt, P(ws), wsb, None)
     assert f(ptr=0) == g.GDN2_ERR_INVALID_ARG
     assert f(Hk=3, Hv=4) == g.GDN2_ERR_INVALID_ARG
@@ -177,7 +179,16 @@ def test_backward_argument_errors(g):
     assert f(ptr=0x10004) == g.GDN2_ERR_MISALIGNED
     assert f(ws=0) == g.GDN2_ERR_WORKSPACE
     assert f(wsb=16) == g.GDN2_ERR_WORKSPACE
+    size = getattr(g.lib, entry + "_workspace_size")
+    assert size(2, 100, 1, 2, 64, 64, 1) == 0
+    assert size(2, 0, 1, 2, 128, 128, 1) == 0
+
+
+def test_backward_workspace_sizes(g):
     n = g.lib.gdn2_backward_workspace_size(2, 100, 1, 2, 128, 128, 1)
-    st, ck = 128 * 128 * 4, (100 + 31) // 32 + 1
-    assert n >= 4 * ck * st + 4 * 32 * st + 8 * 2 * 100 * 2 * 128 * 4   # + 4 fp32 partial sums x 2 halves
-    assert g.lib.gdn2_backward_workspace_size(2, 100, 1, 2, 64, 64, 1) == 0
+    units = 2 * 2 * ((100 + 31) // 32)   # (batch, value head, 32-token chunk)
+    # per unit: S entering and dS leaving the chunk, U and dU, T; then fp32 dq and dk per value head
+    assert n >= units * (2 * 128 * 128 + 2 * 32 * 128 + 32 * 32) * 4 + 2 * 2 * 100 * 2 * 128 * 4
+    r = g.lib.gdn2_backward_recurrent_workspace_size(2, 100, 1, 2, 128, 128, 1)
+    # one fp32 state per 32-token stretch for each (batch, value head)
+    assert r >= units * 128 * 128 * 4

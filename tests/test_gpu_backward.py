@@ -1,6 +1,7 @@
-"""Gradients of the core on the GPU (gdn2_backward) against the fp64 autograd oracle
-(oracle/backward.py): bf16 and fp32 token tensors, grouped heads, a ragged tail of the 32-token
-recompute stretches, an initial state and an upstream final-state gradient."""
+"""Gradients of the core on the GPU against the fp64 autograd oracle (oracle/backward.py): the
+chunked path (gdn2_backward) and the per-token recurrent path (gdn2_backward_recurrent), bf16 and
+fp32 token tensors, grouped heads, a ragged last chunk, an initial state and an upstream
+final-state gradient; at lengths the oracle cannot reach, the two paths against each other."""
 import numpy as np
 import pytest
 
@@ -21,8 +22,9 @@ def g():
     return mod
 
 
-@pytest.mark.parametrize("dtype,T,with_ds", [("bf16", 77, True), ("f32", 45, False)])
-def test_backward_parity(g, dtype, T, with_ds):
+@pytest.mark.parametrize("recurrent", [False, True], ids=["chunked", "recurrent"])
+@pytest.mark.parametrize("dtype,T,with_ds", [("bf16", 77, True), ("f32", 45, False), ("f32", 64, True)])
+def test_backward_parity(g, dtype, T, with_ds, recurrent):
     import torch
 
     wl = synth.Workload("bwd", B=2, T=T, Hk=1, Hv=2, dk=128, dv=128, dtype=dtype, seed=21 + T, s0_std=0.02)
@@ -34,7 +36,7 @@ def test_backward_parity(g, dtype, T, with_ds):
     ts = [dev(getattr(inp, n)) for n in ("q", "k", "v", "g", "b", "w")]
     s0 = H.state_to_device(inp.s0)
     dsd = H.state_to_device(ds_t) if with_ds else None
-    outs = g.backward(*ts, dev(d_o), s0, dsd)
+    outs = g.backward(*ts, dev(d_o), s0, dsd, recurrent=recurrent)
     torch.cuda.synchronize()
     assert g.gdn2_last_device_status() == g.GDN2_OK
     ref = oback.gradients(inp.q, inp.k, inp.v, inp.g, inp.b, inp.w, inp.s0, d_o, ds_t)
@@ -52,3 +54,27 @@ def test_backward_empty_sequence_passes_the_state_gradient(g):
     g.gdn2_backward(x, x, x, x, x, x, x, x, x, x, x, x, x, None, ds, ds0)
     torch.cuda.synchronize()
     assert torch.equal(ds0, ds)
+
+
+@pytest.mark.parametrize("T,Hk,Hv", [(2050, 1, 2), (700, 2, 4)])
+def test_backward_chunked_matches_recurrent_on_long_sequences(g, T, Hk, Hv):
+    """Two fp32 computations of the same gradients that share no arithmetic: they agree to the
+    rounding of fp32 sums over thousands of tokens."""
+    import torch
+
+    wl = synth.Workload("bwd-long", B=1, T=T, Hk=Hk, Hv=Hv, dk=128, dv=128, dtype="f32", seed=3 + T, s0_std=0.02)
+    inp = synth.make_inputs(wl)
+    rng = np.random.default_rng(T)
+    d_o = rng.standard_normal((1, T, Hv, 128)).astype(np.float32)
+    ds_t = (0.1 * rng.standard_normal((1, Hv, 128, 128))).astype(np.float32)
+    dev = lambda a: synth.to_torch(np.ascontiguousarray(a), "f32", "cuda")
+    ts = [dev(getattr(inp, n)) for n in ("q", "k", "v", "g", "b", "w")]
+    s0, dsd = H.state_to_device(inp.s0), H.state_to_device(ds_t)
+    a = g.backward(*ts, dev(d_o), s0, dsd)
+    r = g.backward(*ts, dev(d_o), s0, dsd, recurrent=True)
+    torch.cuda.synchronize()
+    assert g.gdn2_last_device_status() == g.GDN2_OK
+    for name, x, y in zip(("dq", "dk", "dv", "dg", "db", "dw", "ds0"), a, r):
+        assert torch.isfinite(x).all(), name
+        e = max_rel_err(H.to_np(x), H.to_np(y).astype(np.float64))
+        assert e < 1e-3, (name, e)
