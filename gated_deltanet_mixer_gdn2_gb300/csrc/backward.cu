@@ -25,7 +25,7 @@ constexpr int kD = 128;
 constexpr int kCols = 64;     // d_v columns per CTA
 constexpr int kChk = 32;      // checkpoint interval = tokens recomputed at a time
 constexpr int kThreads = 256;
-constexpr int kParts = 2 * kCols / 4;  // row-sum partials per row inside a CTA: 8 warps x 2 column groups
+constexpr int kParts = 2 * (kThreads / 32);  // row-sum partials per row inside a CTA: one per (warp, column group)
 
 struct BwdArgs {
     const void *q, *k, *v, *g, *b, *w, *dout;

@@ -16,7 +16,8 @@
 //
 // Four launches: the fp32 forward keeping T, S_n and U per chunk; the chain over chunks in reverse
 // (adjoint_kernel: heads x 16-column slices, like the forward's state kernel); the local gradients of
-// every (chunk, head) in parallel (grad_kernel); the sums of dq, dk over each key head's group.
+// every (chunk, head) in parallel (grad_kernel, one 512-thread CTA per SM, register-tiled products);
+// the sums of dq, dk over each key head's group.
 #include <type_traits>
 
 #include "common.cuh"
@@ -27,8 +28,6 @@ namespace {
 constexpr int kD = 128;       // d_k = d_v
 constexpr int kCb = 32;       // chunk of the backward
 constexpr int kSl = 16;       // d_v columns per adjoint CTA
-constexpr int kLD = kD + 1;   // padded row of [C][d] and [d][d] shared arrays
-constexpr int kLC = kCb + 1;  // padded row of [C][C] shared arrays
 
 // dS and dU over the chunks in reverse: dU_n = M_n^T dO~_n + K^_n dS_{n+1};
 // dS_n = G_n dS_{n+1} + Q_bar_n^T dO~_n - W_n^T dU_n. Keeps dS_{n+1} and dU_n of every chunk.
@@ -104,217 +103,500 @@ __global__ void __launch_bounds__(256) adjoint_kernel(const float* __restrict__ 
         }
 }
 
-// The local gradients of one (chunk, head). Thread = channel c and the tokens t0, t0 + 2, .., t0 + 30.
+// ---- grad_kernel: every per-token gradient of one (chunk, head), one CTA of 512 threads per SM
+constexpr int kGT = 512;          // threads
+constexpr int kLS = 132;          // padded row of its [*][128] arrays (16-byte aligned rows)
+constexpr int kLQ = 36;           // padded row of its [32][32] arrays
+constexpr int kSlot = kCb * kLS;  // one [32][128] array
+
+namespace gk {  // shared-memory map (floats); arrays that are dead by the time another is written share room
+constexpr int slot(int i) { return i * kSlot; }
+constexpr int DS = 0, SS = kD * kLS;  // dS_{n+1}, S_n [128][kLS]: slots 0-3 and 4-7 while the big products run
+constexpr int DKH = slot(0), DQB = slot(1), DW = slot(2), XX = slot(2), U0 = slot(3), KB = slot(3), G = slot(4),
+              K = slot(5), BETA = slot(6), Q = slot(7);
+constexpr int U = slot(8), DKB = slot(8), DU = slot(9), ZV = slot(9), DO = slot(10), YY = slot(10);
+constexpr int TM = slot(11);                  // T [32][kLQ]
+constexpr int DT = TM + kCb * kLQ;            // dT
+constexpr int PP = DT + kCb * kLQ;            // T^T dT
+constexpr int DA = PP + kCb * kLQ, DAT = DA + kCb * kLQ, DM = DAT + kCb * kLQ, DMT = DM + kCb * kLQ;
+constexpr int DGP = DMT + kCb * kLQ;          // [4][128] partial rowsums of dS' . S
+constexpr int DGL = DGP + 4 * kD;             // [4][128] partial sums of dK^ . K^
+constexpr int TOTAL = DGL + 4 * kD;
+}  // namespace gk
+
+__device__ __forceinline__ float4 lds4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+__device__ __forceinline__ void sts4(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
+__device__ __forceinline__ float dot4(float4 a, float4 b, float acc) {
+    return fmaf(a.w, b.w, fmaf(a.z, b.z, fmaf(a.y, b.y, fmaf(a.x, b.x, acc))));
+}
+__device__ __forceinline__ void cp_async16(float* smem, const float* gmem) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(smem))),
+                 "l"(gmem)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// waits until at most n of this thread's most recent groups are in flight (n folds to a constant when unrolled)
+__device__ __forceinline__ void cp_async_wait(int n) {
+    switch (n) {
+        case 0: asm volatile("cp.async.wait_group 0;" ::: "memory"); break;
+        case 1: asm volatile("cp.async.wait_group 1;" ::: "memory"); break;
+        case 2: asm volatile("cp.async.wait_group 2;" ::: "memory"); break;
+        case 3: asm volatile("cp.async.wait_group 3;" ::: "memory"); break;
+        case 4: asm volatile("cp.async.wait_group 4;" ::: "memory"); break;
+        case 5: asm volatile("cp.async.wait_group 5;" ::: "memory"); break;
+        case 6: asm volatile("cp.async.wait_group 6;" ::: "memory"); break;
+        default: asm volatile("cp.async.wait_group 7;" ::: "memory"); break;
+    }
+}
+// four consecutive elements of a token tensor as fp32
 template <typename Tin>
-__global__ void __launch_bounds__(256) grad_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k,
-                                                   const Tin* __restrict__ v, const Tin* __restrict__ g,
-                                                   const Tin* __restrict__ b, const Tin* __restrict__ w,
-                                                   const Tin* __restrict__ dO, const float* __restrict__ ws,
-                                                   const float* __restrict__ t_ws, const float* __restrict__ s_save,
-                                                   const float* __restrict__ u_save, const float* __restrict__ ds_save,
-                                                   const float* __restrict__ du_save, float* __restrict__ dq_ws,
-                                                   float* __restrict__ dk_ws, Tin* __restrict__ dv, Tin* __restrict__ dg,
-                                                   Tin* __restrict__ db, Tin* __restrict__ dw, int T, int Hk, int Hv,
-                                                   float scale) {
-    extern __shared__ float smem[];
+__device__ __forceinline__ float4 ld4_tok(const Tin* p) {
+    if constexpr (sizeof(Tin) == 4) {
+        return *reinterpret_cast<const float4*>(p);
+    } else {
+        const uint2 u = *reinterpret_cast<const uint2*>(p);
+        const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+        const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+        return make_float4(a.x, a.y, b.x, b.y);
+    }
+}
+template <typename Tin>
+__device__ __forceinline__ void st4_tok(Tin* p, float4 x) {
+    if constexpr (sizeof(Tin) == 4) {
+        *reinterpret_cast<float4*>(p) = x;
+    } else {
+        const __nv_bfloat162 a = __floats2bfloat162_rn(x.x, x.y), b = __floats2bfloat162_rn(x.z, x.w);
+        uint2 u;
+        u.x = *reinterpret_cast<const uint32_t*>(&a);
+        u.y = *reinterpret_cast<const uint32_t*>(&b);
+        *reinterpret_cast<uint2*>(p) = u;
+    }
+}
+
+// The local gradients of one (chunk n, batch-head bh), given S_n, dS_{n+1}, U, dU and T of the chunk:
+//   1. dK^ = U dS'^T, dQ_bar = dO~ S^T, dW = -dU S^T, dgamma = rowsum(dS' . S)  (K = d_v, register tiles of
+//      2 tokens x 4 channels; S and dS' arrive in eight 16-column groups that the products consume in order)
+//   2. dM = tril(dO~ U^T), dT = dU U0^T + dW K_bar^T, dK_bar = T^T dW, dU0 = T^T dU (-> dv, dw)
+//   3. P = T^T dT, dA = -strict_tril(P T^T)
+//   4. the pair terms X, Y (thread = channel and block of 8 tokens t) and Z + V (block of 8 tokens s), each
+//      factor e^{G_t - G_s} of two tokens in different blocks split at a block edge r between them into
+//      e^{G_t - G_r} e^{G_r - G_s}, both <= 1, so the sums over the other block are plain products
+//   5. dq, dk (fp32, per value head), db and dg = reverse cumulative sum of dG plus dG_last.
+template <typename Tin>
+__global__ void __launch_bounds__(kGT, 1) grad_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k,
+                                                      const Tin* __restrict__ v, const Tin* __restrict__ g,
+                                                      const Tin* __restrict__ b, const Tin* __restrict__ w,
+                                                      const Tin* __restrict__ dO, const float* __restrict__ t_ws,
+                                                      const float* __restrict__ s_save, const float* __restrict__ u_save,
+                                                      const float* __restrict__ ds_save,
+                                                      const float* __restrict__ du_save, float* __restrict__ dq_ws,
+                                                      float* __restrict__ dk_ws, Tin* __restrict__ dv,
+                                                      Tin* __restrict__ dg, Tin* __restrict__ db, Tin* __restrict__ dw,
+                                                      int T, int Hk, int Hv, float scale) {
+    extern __shared__ __align__(16) float sm[];
     const int n = blockIdx.x, bh = blockIdx.y, NC = gridDim.x;
     const int bi = bh / Hv, hv = bh - bi * Hv, hk = hv / (Hv / Hk);
     const int tid = threadIdx.x;
-    const int c = tid & (kD - 1), t0 = tid >> 7;
-    constexpr int kM = kCb / 2;  // tokens per thread
-    float* sG = smem;                 // [C][kLD] cumulative log-decay, later dG
-    float* sQ = sG + kCb * kLD;       // q
-    float* sK = sQ + kCb * kLD;       // k
-    float* sBeta = sK + kCb * kLD;    // b.k
-    float* sDO = sBeta + kCb * kLD;   // scale . do
-    float* sU = sDO + kCb * kLD;      // U
-    float* sDU = sU + kCb * kLD;      // dU
-    float* sX = sDU + kCb * kLD;      // w.v, later K_bar
-    float* sBig = sX + kCb * kLD;     // [kD][kLD]: dS_{n+1}, then S_n, then dW [C][kLD]
-    float* sT = sBig + kD * kLD;      // [C][kLC]
-    float* sM = sT + kCb * kLC;
-    float* sdM = sM + kCb * kLC;
-    float* sdT = sdM + kCb * kLC;
-    float* sdA = sdT + kCb * kLC;
-    float* sP = sdA + kCb * kLC;      // T^T dT, later the two halves of the dG_last sums
-    const SimtWs L{kD, kD, kCb};
     const size_t unit = (size_t)bh * NC + n;
+    auto vrow = [&](int t) { return (((size_t)bi * T + n * kCb + t) * Hv + hv) * kD; };   // v-like token row
+    auto krow = [&](int t) { return (((size_t)bi * T + n * kCb + t) * Hk + hk) * kD; };   // k-like token row
+    const int nvalid = min(kCb, T - n * kCb);
 
-    // ---- inputs of the chunk
-#pragma unroll 4
-    for (int m = 0; m < kM; ++m) {
-        const int t = t0 + 2 * m, tok = n * kCb + t;
-        float qq = 0.f, kk = 0.f, bb = 0.f, gg = 0.f, oo = 0.f, uu0 = 0.f;
-        if (tok < T) {
-            const size_t kq = (((size_t)bi * T + tok) * Hk + hk) * kD + c;
-            const size_t vh = (((size_t)bi * T + tok) * Hv + hv) * kD + c;
-            qq = to_f32(q[kq]);
-            kk = to_f32(k[kq]);
-            bb = to_f32(b[vh]);
-            gg = to_f32(g[vh]);
-            oo = scale * to_f32(dO[vh]);
-            uu0 = to_f32(w[vh]) * to_f32(v[vh]);
+    // ---- group 0: U, dU, T and the first 16 columns of S, dS'; groups 1-7: the other columns
+    {
+        const float* Ug = u_save + unit * kCb * kD;
+        const float* DUg = du_save + unit * kCb * kD;
+        for (int i = tid; i < kCb * kD / 4; i += kGT) {
+            const int t = i >> 5, c4 = 4 * (i & 31);
+            cp_async16(sm + gk::U + t * kLS + c4, Ug + t * kD + c4);
+            cp_async16(sm + gk::DU + t * kLS + c4, DUg + t * kD + c4);
         }
-        sQ[t * kLD + c] = qq;
-        sK[t * kLD + c] = kk;
-        sBeta[t * kLD + c] = bb * kk;
-        sG[t * kLD + c] = gg;
-        sDO[t * kLD + c] = oo;
-        sX[t * kLD + c] = uu0;
-        sU[t * kLD + c] = u_save[(unit * kCb + t) * kD + c];
-        sDU[t * kLD + c] = du_save[(unit * kCb + t) * kD + c];
+        if (tid < kCb * kCb / 4) {
+            const int r = tid >> 3, c4 = 4 * (tid & 7);
+            cp_async16(sm + gk::TM + r * kLQ + c4, t_ws + unit * kCb * kCb + r * kCb + c4);
+        }
+        const float* Sg = s_save + unit * kD * kD;
+        const float* DSg = ds_save + unit * kD * kD;
+#pragma unroll
+        for (int jb = 0; jb < 8; ++jb) {
+#pragma unroll
+            for (int m = 0; m < 2; ++m) {
+                const int id = tid + kGT * m;            // 2 matrices x 128 rows x 4 pieces of 16 bytes
+                const int row = (id >> 2) & (kD - 1), c4 = 16 * jb + 4 * (id & 3);
+                if (id < 512)
+                    cp_async16(sm + gk::DS + row * kLS + c4, DSg + row * kD + c4);
+                else
+                    cp_async16(sm + gk::SS + row * kLS + c4, Sg + row * kD + c4);
+            }
+            cp_async_commit();
+        }
     }
-    for (int p = tid; p < kCb * kCb; p += 256) {
-        const int i = p / kCb, j = p - i * kCb;
-        sT[i * kLC + j] = t_ws[unit * kCb * kCb + p];
-        sM[i * kLC + j] = ws[unit * L.unit_floats() + L.off_m() + p];
+    // scaled dO with ordinary loads while the copies fly (zero past the end of the sequence)
+    {
+        const int t = tid >> 4, c8 = 8 * (tid & 15);
+        float x[8];
+        if (t < nvalid) {
+            Vec8<Tin>::load(dO + vrow(t) + c8, x);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) x[i] = 0.f;
+        }
+        sts4(sm + gk::DO + t * kLS + c8, make_float4(scale * x[0], scale * x[1], scale * x[2], scale * x[3]));
+        sts4(sm + gk::DO + t * kLS + c8 + 4, make_float4(scale * x[4], scale * x[5], scale * x[6], scale * x[7]));
     }
-    const float* S = s_save + unit * kD * kD;
-    const float* dS = ds_save + unit * kD * kD;
-    float dgam = 0.f;  // rowsum(dS' . S) for channel c (threads below 128)
-    if (tid < kD)
-        for (int j = 0; j < kD; ++j) dgam = fmaf(dS[(size_t)c * kD + j], S[(size_t)c * kD + j], dgam);
-    for (int p = tid; p < kD * kD; p += 256) sBig[(p >> 7) * kLD + (p & (kD - 1))] = dS[p];
+
+    // ---- 1. the products with S and dS' (contraction over d_v)
+    const int warp = tid >> 5, lane = tid & 31;
+    const int cb = 32 * (warp & 3) + (lane & 7);   // channels cb + 8r, r = 0..3
+    const int ta = 8 * (warp >> 2) + (lane >> 3);  // tokens ta, ta + 4
+    float aKh[2][4], aQb[2][4], aW[2][4], dgp[4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        dgp[r] = 0.f;
+#pragma unroll
+        for (int i = 0; i < 2; ++i) aKh[i][r] = aQb[i][r] = aW[i][r] = 0.f;
+    }
+#pragma unroll
+    for (int jb = 0; jb < 8; ++jb) {
+        cp_async_wait(7 - jb);
+        __syncthreads();
+#pragma unroll
+        for (int jq = 0; jq < 4; ++jq) {
+            const int j = 16 * jb + 4 * jq;
+            float4 u4[2], du4[2], o4[2], s4[4], ds4[4];
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                u4[i] = lds4(sm + gk::U + (ta + 4 * i) * kLS + j);
+                du4[i] = lds4(sm + gk::DU + (ta + 4 * i) * kLS + j);
+                o4[i] = lds4(sm + gk::DO + (ta + 4 * i) * kLS + j);
+            }
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                s4[r] = lds4(sm + gk::SS + (cb + 8 * r) * kLS + j);
+                ds4[r] = lds4(sm + gk::DS + (cb + 8 * r) * kLS + j);
+            }
+#pragma unroll
+            for (int i = 0; i < 2; ++i)
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    aKh[i][r] = dot4(u4[i], ds4[r], aKh[i][r]);
+                    aQb[i][r] = dot4(o4[i], s4[r], aQb[i][r]);
+                    aW[i][r] = dot4(du4[i], s4[r], aW[i][r]);
+                }
+            if (jq == (warp >> 2))  // each row of warps takes one quarter of the columns of the rowsum
+#pragma unroll
+                for (int r = 0; r < 4; ++r) dgp[r] = dot4(ds4[r], s4[r], dgp[r]);
+        }
+    }
+    __syncthreads();  // S, dS' read out: their room takes the per-token arrays
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const int o = (ta + 4 * i) * kLS + cb + 8 * r;
+            sm[gk::DKH + o] = aKh[i][r];
+            sm[gk::DQB + o] = aQb[i][r];
+            sm[gk::DW + o] = -aW[i][r];
+        }
+    if ((lane >> 3) == 0)
+#pragma unroll
+        for (int r = 0; r < 4; ++r) sm[gk::DGP + (warp >> 2) * kD + cb + 8 * r] = dgp[r];
+    {   // token inputs: U0 = w.v, g, k, b.k, q (zero past the end of the sequence)
+        const int t = tid >> 4, c8 = 8 * (tid & 15);
+        float xw[8], xv[8], xg[8], xk[8], xb[8], xq[8];
+        if (t < nvalid) {
+            Vec8<Tin>::load(w + vrow(t) + c8, xw);
+            Vec8<Tin>::load(v + vrow(t) + c8, xv);
+            Vec8<Tin>::load(g + vrow(t) + c8, xg);
+            Vec8<Tin>::load(b + vrow(t) + c8, xb);
+            Vec8<Tin>::load(k + krow(t) + c8, xk);
+            Vec8<Tin>::load(q + krow(t) + c8, xq);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) xw[i] = xv[i] = xg[i] = xk[i] = xb[i] = xq[i] = 0.f;
+        }
+        const int o = t * kLS + c8;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int i = 4 * h;
+            sts4(sm + gk::U0 + o + i, make_float4(xw[i] * xv[i], xw[i + 1] * xv[i + 1], xw[i + 2] * xv[i + 2],
+                                                  xw[i + 3] * xv[i + 3]));
+            sts4(sm + gk::G + o + i, make_float4(xg[i], xg[i + 1], xg[i + 2], xg[i + 3]));
+            sts4(sm + gk::K + o + i, make_float4(xk[i], xk[i + 1], xk[i + 2], xk[i + 3]));
+            sts4(sm + gk::BETA + o + i, make_float4(xb[i] * xk[i], xb[i + 1] * xk[i + 1], xb[i + 2] * xk[i + 2],
+                                                    xb[i + 3] * xk[i + 3]));
+            sts4(sm + gk::Q + o + i, make_float4(xq[i], xq[i + 1], xq[i + 2], xq[i + 3]));
+        }
+    }
     __syncthreads();
-    if (tid < kD) {  // inclusive cumulative log-decay per channel
+
+    // ---- 2. dM = tril(dO~ U^T) (threads 0-255), dT1 = dU U0^T (256-511): 2 x 2 tiles over d_v; warps 0-3 first
+    //      form the cumulative log-decay G per channel
+    if (tid < kD) {
         float acc = 0.f;
         for (int t = 0; t < kCb; ++t) {
-            acc += sG[t * kLD + c];
-            sG[t * kLD + c] = acc;
+            acc += sm[gk::G + t * kLS + tid];
+            sm[gk::G + t * kLS + tid] = acc;
         }
     }
-    __syncthreads();
-    const float Glast = sG[(kCb - 1) * kLD + c];
-    // ---- dK^ = U dS'^T
-    float dKh[kM];
-#pragma unroll
-    for (int m = 0; m < kM; ++m) dKh[m] = 0.f;
-    for (int j = 0; j < kD; ++j) {
-        const float x = sBig[c * kLD + j];
-#pragma unroll
-        for (int m = 0; m < kM; ++m) dKh[m] = fmaf(sU[(t0 + 2 * m) * kLD + j], x, dKh[m]);
-    }
-    __syncthreads();
-    for (int p = tid; p < kD * kD; p += 256) sBig[(p >> 7) * kLD + (p & (kD - 1))] = S[p];
-    __syncthreads();
-    // ---- dQ_bar = dO~ S^T, dW = -dU S^T
-    float dQb[kM], dW[kM];
-#pragma unroll
-    for (int m = 0; m < kM; ++m) dQb[m] = dW[m] = 0.f;
-    for (int j = 0; j < kD; ++j) {
-        const float x = sBig[c * kLD + j];
-#pragma unroll
-        for (int m = 0; m < kM; ++m) {
-            dQb[m] = fmaf(sDO[(t0 + 2 * m) * kLD + j], x, dQb[m]);
-            dW[m] = fmaf(-sDU[(t0 + 2 * m) * kLD + j], x, dW[m]);
-        }
-    }
-    __syncthreads();
-#pragma unroll
-    for (int m = 0; m < kM; ++m) sBig[(t0 + 2 * m) * kLD + c] = dW[m];  // dW [C][kLD]
-    __syncthreads();
-    // ---- dM = tril(dO~ U^T), dT = dU U0^T (then + dW K_bar^T)
-    for (int p = tid; p < kCb * kCb; p += 256) {
-        const int t = p / kCb, s = p - t * kCb;
-        float am = 0.f, at = 0.f;
-        for (int j = 0; j < kD; ++j) {
-            am = fmaf(sDO[t * kLD + j], sU[s * kLD + j], am);
-            at = fmaf(sDU[t * kLD + j], sX[s * kLD + j], at);
-        }
-        sdM[t * kLC + s] = s <= t ? am : 0.f;
-        sdT[t * kLC + s] = at;
-    }
-    __syncthreads();
-#pragma unroll
-    for (int m = 0; m < kM; ++m) {  // K_bar = b.k.e^G in place of w.v
-        const int t = t0 + 2 * m;
-        sX[t * kLD + c] = sBeta[t * kLD + c] * expf(sG[t * kLD + c]);
-    }
-    __syncthreads();
-    for (int p = tid; p < kCb * kCb; p += 256) {
-        const int t = p / kCb, s = p - t * kCb;
-        float at = sdT[t * kLC + s];
-        for (int j = 0; j < kD; ++j) at = fmaf(sBig[t * kLD + j], sX[s * kLD + j], at);
-        sdT[t * kLC + s] = at;
-    }
-    __syncthreads();
-    // ---- dU0 = T^T dU (-> dv, dw), dK_bar = T^T dW;  P = T^T dT
-    float dKb[kM];
+    const int prod = tid >> 8, tile = tid & 255;
+    const int tp = tile >> 4, sp = tile & 15;  // tokens {tp, tp + 16} x {sp, sp + 16}
+    float pt[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+    {
+        const float* A = sm + (prod ? gk::DU : gk::DO);
+        const float* Bm = sm + (prod ? gk::U0 : gk::U);
 #pragma unroll 4
-    for (int m = 0; m < kM; ++m) {
-        const int t = t0 + 2 * m, tok = n * kCb + t;
-        float du0 = 0.f, dkb = 0.f;
-        for (int s = t; s < kCb; ++s) {
-            const float ts = sT[s * kLC + t];
-            du0 = fmaf(ts, sDU[s * kLD + c], du0);
-            dkb = fmaf(ts, sBig[s * kLD + c], dkb);
-        }
-        dKb[m] = dkb;
-        if (tok < T) {
-            const size_t vh = (((size_t)bi * T + tok) * Hv + hv) * kD + c;
-            dv[vh] = from_f32<Tin>(to_f32(w[vh]) * du0);
-            dw[vh] = from_f32<Tin>(to_f32(v[vh]) * du0);
+        for (int j = 0; j < kD; j += 4) {
+            const float4 a0 = lds4(A + tp * kLS + j), a1 = lds4(A + (tp + 16) * kLS + j);
+            const float4 b0 = lds4(Bm + sp * kLS + j), b1 = lds4(Bm + (sp + 16) * kLS + j);
+            pt[0][0] = dot4(a0, b0, pt[0][0]);
+            pt[1][0] = dot4(a1, b0, pt[1][0]);
+            pt[1][1] = dot4(a1, b1, pt[1][1]);
+            if (prod) pt[0][1] = dot4(a0, b1, pt[0][1]);  // above the diagonal for dM
         }
     }
-    for (int p = tid; p < kCb * kCb; p += 256) {
-        const int t = p / kCb, s = p - t * kCb;
-        float acc = 0.f;
-        for (int r = t; r < kCb; ++r) acc = fmaf(sT[r * kLC + t], sdT[r * kLC + s], acc);
-        sP[t * kLC + s] = acc;
+    if (prod == 0)
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int t = tp + 16 * i, s2 = sp + 16 * j;
+                const float x = s2 <= t ? pt[i][j] : 0.f;
+                sm[gk::DM + t * kLQ + s2] = x;
+                sm[gk::DMT + s2 * kLQ + t] = x;
+            }
+    __syncthreads();
+    {   // K_bar = b.k.e^G in place of U0
+        const int t = tid >> 4, c8 = 8 * (tid & 15);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int o = t * kLS + c8 + i;
+            sm[gk::KB + o] = sm[gk::BETA + o] * __expf(sm[gk::G + o]);
+        }
     }
     __syncthreads();
-    for (int p = tid; p < kCb * kCb; p += 256) {  // dA = -strict_tril(P T^T)
-        const int t = p / kCb, s = p - t * kCb;
-        float acc = 0.f;
-        if (s < t)
-            for (int r = 0; r <= s; ++r) acc = fmaf(sP[t * kLC + r], sT[s * kLC + r], acc);
-        sdA[t * kLC + s] = -acc;
+
+    // ---- dT = dT1 + dW K_bar^T (threads 256-511); dK_bar = T^T dW, dU0 = T^T dU -> dv, dw (threads 0-255)
+    if (prod) {
+#pragma unroll 4
+        for (int c = 0; c < kD; c += 4) {
+            const float4 a0 = lds4(sm + gk::DW + tp * kLS + c), a1 = lds4(sm + gk::DW + (tp + 16) * kLS + c);
+            const float4 b0 = lds4(sm + gk::KB + sp * kLS + c), b1 = lds4(sm + gk::KB + (sp + 16) * kLS + c);
+            pt[0][0] = dot4(a0, b0, pt[0][0]);
+            pt[0][1] = dot4(a0, b1, pt[0][1]);
+            pt[1][0] = dot4(a1, b0, pt[1][0]);
+            pt[1][1] = dot4(a1, b1, pt[1][1]);
+        }
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+#pragma unroll
+            for (int j = 0; j < 2; ++j) sm[gk::DT + (tp + 16 * i) * kLQ + sp + 16 * j] = pt[i][j];
+    } else {
+        const int c0 = 4 * (tile & 31), tq = tile >> 5;  // tokens tq + 8i, i = 0..3
+        float4 aKb[4], aU0[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) aKb[i] = aU0[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int sg = 0; sg < 4; ++sg)
+#pragma unroll 4
+            for (int ss = 0; ss < 8; ++ss) {
+                const int s2 = 8 * sg + ss;
+                const float4 w4 = lds4(sm + gk::DW + s2 * kLS + c0), u4 = lds4(sm + gk::DU + s2 * kLS + c0);
+#pragma unroll
+                for (int i = 0; i <= sg; ++i) {  // T[s][t] = 0 for t > s
+                    const float tt = sm[gk::TM + s2 * kLQ + tq + 8 * i];
+                    aKb[i].x = fmaf(tt, w4.x, aKb[i].x); aKb[i].y = fmaf(tt, w4.y, aKb[i].y);
+                    aKb[i].z = fmaf(tt, w4.z, aKb[i].z); aKb[i].w = fmaf(tt, w4.w, aKb[i].w);
+                    aU0[i].x = fmaf(tt, u4.x, aU0[i].x); aU0[i].y = fmaf(tt, u4.y, aU0[i].y);
+                    aU0[i].z = fmaf(tt, u4.z, aU0[i].z); aU0[i].w = fmaf(tt, u4.w, aU0[i].w);
+                }
+            }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int t = tq + 8 * i;
+            sts4(sm + gk::DKB + t * kLS + c0, aKb[i]);
+            if (t < nvalid) {
+                const float4 w4 = ld4_tok(w + vrow(t) + c0), v4 = ld4_tok(v + vrow(t) + c0);
+                const float4 d = aU0[i];
+                st4_tok(dv + vrow(t) + c0, make_float4(w4.x * d.x, w4.y * d.y, w4.z * d.z, w4.w * d.w));
+                st4_tok(dw + vrow(t) + c0, make_float4(v4.x * d.x, v4.y * d.y, v4.z * d.z, v4.w * d.w));
+            }
+        }
     }
     __syncthreads();
-    // ---- the A and M terms pair by pair, then everything back to the inputs
-    float dG[kM], dKhKh = 0.f;
-#pragma unroll 2
-    for (int m = 0; m < kM; ++m) {
-        const int t = t0 + 2 * m, tok = n * kCb + t;
-        const float Gt = sG[t * kLD + c];
-        float X = 0.f, Y = sdM[t * kLC + t] * sK[t * kLD + c], Z = 0.f, V = sdM[t * kLC + t] * sQ[t * kLD + c];
-        for (int s = 0; s < t; ++s) {
-            const float e = expf(Gt - sG[s * kLD + c]);  // e^{G_t - G_s} <= 1
-            const float ks = sK[s * kLD + c] * e;
-            X = fmaf(sdA[t * kLC + s], ks, X);
-            Y = fmaf(sdM[t * kLC + s], ks, Y);
+
+    // ---- 3. P = T^T dT, dA = -strict_tril(P T^T): thread = row t and columns s, s + 16
+    const int rt = tid >> 4, rs = tid & 15;
+    {
+        float p0 = 0.f, p1 = 0.f;
+        for (int r = rt; r < kCb; ++r) {
+            const float tt = sm[gk::TM + r * kLQ + rt];
+            p0 = fmaf(tt, sm[gk::DT + r * kLQ + rs], p0);
+            p1 = fmaf(tt, sm[gk::DT + r * kLQ + rs + 16], p1);
         }
-        for (int u = t + 1; u < kCb; ++u) {
-            const float e = expf(sG[u * kLD + c] - Gt);  // e^{G_u - G_t} <= 1
-            Z = fmaf(sdA[u * kLC + t], sBeta[u * kLD + c] * e, Z);
-            V = fmaf(sdM[u * kLC + t], sQ[u * kLD + c] * e, V);
-        }
-        const float eG = expf(Gt), eH = expf(Glast - Gt);
-        const float qq = sQ[t * kLD + c], kk = sK[t * kLD + c], be = sBeta[t * kLD + c];
-        const float Qb = qq * eG, Kh = kk * eH, Kb = sX[t * kLD + c];
-        const float dbeta = dKb[m] * eG + X;
-        dG[m] = dQb[m] * Qb + dKb[m] * Kb - dKh[m] * Kh + be * X + qq * Y - kk * (Z + V);
-        dKhKh = fmaf(dKh[m], Kh, dKhKh);
-        if (tok < T) {
-            const size_t vh = (((size_t)bi * T + tok) * Hv + hv) * kD + c;
-            const float bb = to_f32(b[vh]);
-            dq_ws[vh] = dQb[m] * eG + Y;
-            dk_ws[vh] = dKh[m] * eH + Z + V + dbeta * bb;
-            db[vh] = from_f32<Tin>(dbeta * kk);
-        }
+        sm[gk::PP + rt * kLQ + rs] = p0;
+        sm[gk::PP + rt * kLQ + rs + 16] = p1;
     }
-    // dg_t = sum_{s >= t} dG_s + dG_last, dG_last = sum_t dK^.K^ + dgamma . e^{G_last}
     __syncthreads();
 #pragma unroll
-    for (int m = 0; m < kM; ++m) sG[(t0 + 2 * m) * kLD + c] = dG[m];  // sG is no longer read
-    sP[t0 * kD + c] = dKhKh;
+    for (int h = 0; h < 2; ++h) {
+        const int s2 = rs + 16 * h;
+        float a = 0.f;
+        if (s2 < rt)
+            for (int r = 0; r <= s2; ++r) a = fmaf(sm[gk::PP + rt * kLQ + r], sm[gk::TM + s2 * kLQ + r], a);
+        sm[gk::DA + rt * kLQ + s2] = -a;
+        sm[gk::DAT + s2 * kLQ + rt] = -a;
+    }
     __syncthreads();
-    if (tid < kD) {
-        float run = sP[c] + sP[kD + c] + dgam * expf(Glast);  // dG_last
+
+    // ---- 4. pair terms. Thread = channel c, half h: blocks {0, 3} (h = 0) or {1, 2}; side 0 forms X, Y of
+    //      its blocks' tokens, side 1 forms Z + V
+    {
+        const int c = tid & (kD - 1), h = (tid >> 7) & 1, side = tid >> 8;
+        const float* sG = sm + gk::G + c;
+        const float* sK = sm + gk::K + c;
+        const float* sB = sm + gk::BETA + c;
+        const float* sQ = sm + gk::Q + c;
+#pragma unroll 1
+        for (int rep = 0; rep < 2; ++rep) {
+            const int blk = h ? 1 + rep : 3 * rep;
+            const int t0 = 8 * blk;
+            float Gb[8], xb[8], A1[8], A2[8];
+            if (side == 0) {  // X_t = sum_{s<t} dA_ts k_s e^{G_t-G_s};  Y_t = sum_{s<=t} dM_ts k_s e^{G_t-G_s}
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    Gb[i] = sG[(t0 + i) * kLS];
+                    xb[i] = sK[(t0 + i) * kLS];
+                    A1[i] = 0.f;
+                    A2[i] = sm[gk::DM + (t0 + i) * kLQ + t0 + i] * xb[i];
+                }
+                if (blk > 0) {  // s in earlier blocks, split at r = t0: e^{G_t - G_r} e^{G_r - G_s}
+                    float ax[8], ay[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) ax[i] = ay[i] = 0.f;
+                    const float Gr = Gb[0];
+#pragma unroll 2
+                    for (int s2 = 0; s2 < t0; ++s2) {
+                        const float ks = sK[s2 * kLS] * __expf(Gr - sG[s2 * kLS]);
+                        const float4 a0 = lds4(sm + gk::DAT + s2 * kLQ + t0), a1 = lds4(sm + gk::DAT + s2 * kLQ + t0 + 4);
+                        const float4 m0 = lds4(sm + gk::DMT + s2 * kLQ + t0), m1 = lds4(sm + gk::DMT + s2 * kLQ + t0 + 4);
+                        ax[0] = fmaf(a0.x, ks, ax[0]); ax[1] = fmaf(a0.y, ks, ax[1]);
+                        ax[2] = fmaf(a0.z, ks, ax[2]); ax[3] = fmaf(a0.w, ks, ax[3]);
+                        ax[4] = fmaf(a1.x, ks, ax[4]); ax[5] = fmaf(a1.y, ks, ax[5]);
+                        ax[6] = fmaf(a1.z, ks, ax[6]); ax[7] = fmaf(a1.w, ks, ax[7]);
+                        ay[0] = fmaf(m0.x, ks, ay[0]); ay[1] = fmaf(m0.y, ks, ay[1]);
+                        ay[2] = fmaf(m0.z, ks, ay[2]); ay[3] = fmaf(m0.w, ks, ay[3]);
+                        ay[4] = fmaf(m1.x, ks, ay[4]); ay[5] = fmaf(m1.y, ks, ay[5]);
+                        ay[6] = fmaf(m1.z, ks, ay[6]); ay[7] = fmaf(m1.w, ks, ay[7]);
+                    }
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const float et = __expf(Gb[i] - Gr);
+                        A1[i] = fmaf(et, ax[i], A1[i]);
+                        A2[i] = fmaf(et, ay[i], A2[i]);
+                    }
+                }
+#pragma unroll
+                for (int i = 1; i < 8; ++i)  // s in the same block, s < t
+#pragma unroll
+                    for (int j = 0; j < i; ++j) {
+                        const float ks = xb[j] * __expf(Gb[i] - Gb[j]);
+                        A1[i] = fmaf(sm[gk::DA + (t0 + i) * kLQ + t0 + j], ks, A1[i]);
+                        A2[i] = fmaf(sm[gk::DM + (t0 + i) * kLQ + t0 + j], ks, A2[i]);
+                    }
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    sm[gk::XX + (t0 + i) * kLS + c] = A1[i];
+                    sm[gk::YY + (t0 + i) * kLS + c] = A2[i];
+                }
+            } else {  // Z_s = sum_{u>s} dA_us b_u k_u e^{G_u-G_s};  V_s = sum_{u>=s} dM_us q_u e^{G_u-G_s}
+                float qb[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    Gb[i] = sG[(t0 + i) * kLS];
+                    xb[i] = sB[(t0 + i) * kLS];
+                    qb[i] = sQ[(t0 + i) * kLS];
+                    A1[i] = 0.f;
+                    A2[i] = sm[gk::DM + (t0 + i) * kLQ + t0 + i] * qb[i];
+                }
+                if (blk < 3) {  // u in later blocks, split at r = t0 + 7: e^{G_u - G_r} e^{G_r - G_s}
+                    float az[8], av[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) az[i] = av[i] = 0.f;
+                    const float Gr = Gb[7];
+#pragma unroll 2
+                    for (int u2 = t0 + 8; u2 < kCb; ++u2) {
+                        const float eu = __expf(sG[u2 * kLS] - Gr);
+                        const float bu = sB[u2 * kLS] * eu, qu = sQ[u2 * kLS] * eu;
+                        const float4 a0 = lds4(sm + gk::DA + u2 * kLQ + t0), a1 = lds4(sm + gk::DA + u2 * kLQ + t0 + 4);
+                        const float4 m0 = lds4(sm + gk::DM + u2 * kLQ + t0), m1 = lds4(sm + gk::DM + u2 * kLQ + t0 + 4);
+                        az[0] = fmaf(a0.x, bu, az[0]); az[1] = fmaf(a0.y, bu, az[1]);
+                        az[2] = fmaf(a0.z, bu, az[2]); az[3] = fmaf(a0.w, bu, az[3]);
+                        az[4] = fmaf(a1.x, bu, az[4]); az[5] = fmaf(a1.y, bu, az[5]);
+                        az[6] = fmaf(a1.z, bu, az[6]); az[7] = fmaf(a1.w, bu, az[7]);
+                        av[0] = fmaf(m0.x, qu, av[0]); av[1] = fmaf(m0.y, qu, av[1]);
+                        av[2] = fmaf(m0.z, qu, av[2]); av[3] = fmaf(m0.w, qu, av[3]);
+                        av[4] = fmaf(m1.x, qu, av[4]); av[5] = fmaf(m1.y, qu, av[5]);
+                        av[6] = fmaf(m1.z, qu, av[6]); av[7] = fmaf(m1.w, qu, av[7]);
+                    }
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const float es = __expf(Gr - Gb[i]);
+                        A1[i] = fmaf(es, az[i], A1[i]);
+                        A2[i] = fmaf(es, av[i], A2[i]);
+                    }
+                }
+#pragma unroll
+                for (int i = 0; i < 7; ++i)  // u in the same block, u > s
+#pragma unroll
+                    for (int j = i + 1; j < 8; ++j) {
+                        const float e = __expf(Gb[j] - Gb[i]);
+                        A1[i] = fmaf(sm[gk::DA + (t0 + j) * kLQ + t0 + i], xb[j] * e, A1[i]);
+                        A2[i] = fmaf(sm[gk::DM + (t0 + j) * kLQ + t0 + i], qb[j] * e, A2[i]);
+                    }
+#pragma unroll
+                for (int i = 0; i < 8; ++i) sm[gk::ZV + (t0 + i) * kLS + c] = A1[i] + A2[i];
+            }
+        }
+    }
+    __syncthreads();
+
+    // ---- 5. back to the inputs: thread = channel c, block of 8 tokens
+    {
+        const int c = tid & (kD - 1), blk = tid >> 7;
+        const float Glast = sm[gk::G + (kCb - 1) * kLS + c];
+        float dkk = 0.f;
+#pragma unroll 2
+        for (int i = 0; i < 8; ++i) {
+            const int t = 8 * blk + i, o = t * kLS + c;
+            const float G = sm[gk::G + o], eG = __expf(G), eH = __expf(Glast - G);
+            const float qq = sm[gk::Q + o], kk = sm[gk::K + o], be = sm[gk::BETA + o], kb = sm[gk::KB + o];
+            const float dqb = sm[gk::DQB + o], dkb = sm[gk::DKB + o], dkh = sm[gk::DKH + o];
+            const float x = sm[gk::XX + o], y = sm[gk::YY + o], zv = sm[gk::ZV + o];
+            const float dbeta = fmaf(dkb, eG, x);
+            const float dGt = dqb * qq * eG + dkb * kb - dkh * kk * eH + be * x + qq * y - kk * zv;
+            dkk = fmaf(dkh, kk * eH, dkk);
+            sm[gk::DQB + o] = dGt;  // dQ_bar of (t, c) is no longer needed
+            if (t < nvalid) {
+                const size_t vh = vrow(t) + c;
+                const float bb = to_f32(b[vh]);
+                dq_ws[vh] = fmaf(dqb, eG, y);
+                dk_ws[vh] = fmaf(dkh, eH, zv) + dbeta * bb;
+                db[vh] = from_f32<Tin>(dbeta * kk);
+            }
+        }
+        sm[gk::DGL + blk * kD + c] = dkk;
+    }
+    __syncthreads();
+    if (tid < kD) {  // dg_t = sum_{s >= t} dG_s + dG_last, dG_last = sum_t dK^.K^ + rowsum(dS'.S) e^{G_last}
+        const int c = tid;
+        const float Glast = sm[gk::G + (kCb - 1) * kLS + c];
+        const float dgam = (sm[gk::DGP + c] + sm[gk::DGP + kD + c]) + (sm[gk::DGP + 2 * kD + c] + sm[gk::DGP + 3 * kD + c]);
+        float run = (sm[gk::DGL + c] + sm[gk::DGL + kD + c]) + (sm[gk::DGL + 2 * kD + c] + sm[gk::DGL + 3 * kD + c]);
+        run = fmaf(dgam, __expf(Glast), run);
         for (int t = kCb - 1; t >= 0; --t) {
-            run += sG[t * kLD + c];
-            const int tok = n * kCb + t;
-            if (tok < T) dg[(((size_t)bi * T + tok) * Hv + hv) * kD + c] = from_f32<Tin>(run);
+            run += sm[gk::DQB + t * kLS + c];
+            if (t < nvalid) dg[vrow(t) + c] = from_f32<Tin>(run);
         }
     }
 }
@@ -382,7 +664,7 @@ cudaError_t launch_t(const void* q, const void* k, const void* v, const void* g,
                                              simt, t_ws, s_save, u_save, s);
     if (e != cudaSuccess) return e;
     const size_t a_smem = sizeof(float) * ((size_t)kD * kSl + 3 * (size_t)kD * kCb + kCb * kCb + kD + 2 * kCb * kSl);
-    const size_t g_smem = sizeof(float) * (8 * (size_t)kCb * kLD + (size_t)kD * kLD + 6 * (size_t)kCb * kLC);
+    const size_t g_smem = sizeof(float) * (size_t)gk::TOTAL;
     e = cudaFuncSetAttribute(adjoint_kernel<Tin>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)a_smem);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(grad_kernel<Tin>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)g_smem);
@@ -390,9 +672,9 @@ cudaError_t launch_t(const void* q, const void* k, const void* v, const void* g,
     adjoint_kernel<Tin><<<dim3(B * Hv, kD / kSl), 256, a_smem, s>>>(simt, static_cast<const Tin*>(d_o), dsT, ds0,
                                                                     ds_save, du_save, T, Hv, NC, scale);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    grad_kernel<Tin><<<dim3(NC, B * Hv), 256, g_smem, s>>>(
+    grad_kernel<Tin><<<dim3(NC, B * Hv), kGT, g_smem, s>>>(
         static_cast<const Tin*>(q), static_cast<const Tin*>(k), static_cast<const Tin*>(v), static_cast<const Tin*>(g),
-        static_cast<const Tin*>(b), static_cast<const Tin*>(w), static_cast<const Tin*>(d_o), simt, t_ws, s_save, u_save,
+        static_cast<const Tin*>(b), static_cast<const Tin*>(w), static_cast<const Tin*>(d_o), t_ws, s_save, u_save,
         ds_save, du_save, dq_ws, dk_ws, static_cast<Tin*>(dv), static_cast<Tin*>(dg), static_cast<Tin*>(db),
         static_cast<Tin*>(dw), T, Hk, Hv, scale);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
