@@ -27,114 +27,35 @@ namespace {
 
 constexpr int kD = 128;       // d_k = d_v
 constexpr int kCb = 32;       // chunk of the backward
-constexpr int kSl = 16;       // d_v columns per adjoint CTA
 
-// dS and dU over the chunks in reverse: dU_n = M_n^T dO~_n + K^_n dS_{n+1};
-// dS_n = G_n dS_{n+1} + Q_bar_n^T dO~_n - W_n^T dU_n. Keeps dS_{n+1} and dU_n of every chunk.
-template <typename Tin>
-__global__ void __launch_bounds__(256) adjoint_kernel(const float* __restrict__ ws, const Tin* __restrict__ dO,
-                                                      const float* __restrict__ dsT, float* __restrict__ ds0,
-                                                      float* __restrict__ ds_save, float* __restrict__ du_save, int T,
-                                                      int Hv, int NC, float scale) {
-    extern __shared__ float smem[];
-    const int bh = blockIdx.x, bi = bh / Hv, hv = bh - bi * Hv;
-    const int col0 = blockIdx.y * kSl;
-    const int tid = threadIdx.x, nt = blockDim.x;
-    float* sR = smem;                 // [kD][kSl] dS
-    float* sWT = sR + kD * kSl;       // [kD][C]
-    float* sQb = sWT + kD * kCb;      // [kD][C]
-    float* sKh = sQb + kD * kCb;      // [kD][C]
-    float* sM = sKh + kD * kCb;       // [C][C]
-    float* sGam = sM + kCb * kCb;     // [kD]
-    float* sDO = sGam + kD;           // [C][kSl]
-    float* sDU = sDO + kCb * kSl;     // [C][kSl]
-    const SimtWs L{kD, kD, kCb};
-
-    for (int p = tid; p < kD * kSl; p += nt) {
-        const int c = p / kSl, j = p - c * kSl;
-        sR[p] = dsT ? dsT[((size_t)bh * kD + c) * kD + col0 + j] : 0.f;
-    }
-    for (int n = NC - 1; n >= 0; --n) {
-        const float* u = ws + ((size_t)bh * NC + n) * L.unit_floats();
-        __syncthreads();
-        for (int p = tid; p < kD * kCb; p += nt) {
-            sWT[p] = u[L.off_wt() + p];
-            sQb[p] = u[L.off_qbt() + p];
-            sKh[p] = u[L.off_kht() + p];
-        }
-        for (int p = tid; p < kCb * kCb; p += nt) sM[p] = u[L.off_m() + p];
-        for (int p = tid; p < kD; p += nt) sGam[p] = u[L.off_gam() + p];
-        for (int p = tid; p < kCb * kSl; p += nt) {
-            const int i = p / kSl, j = p - i * kSl;
-            const int tok = n * kCb + i;
-            sDO[p] = tok < T ? scale * to_f32(dO[(((size_t)bi * T + tok) * Hv + hv) * kD + col0 + j]) : 0.f;
-        }
-        float* dsn = ds_save + ((size_t)bh * NC + n) * kD * kD;
-        for (int p = tid; p < kD * kSl; p += nt) {
-            const int c = p / kSl, j = p - c * kSl;
-            dsn[(size_t)c * kD + col0 + j] = sR[p];  // dS_{n+1}
-        }
-        __syncthreads();
-        float* dun = du_save + ((size_t)bh * NC + n) * kCb * kD;
-        for (int p = tid; p < kCb * kSl; p += nt) {
-            const int i = p / kSl, j = p - i * kSl;
-            float acc = 0.f;
-            for (int l = i; l < kCb; ++l) acc = fmaf(sM[l * kCb + i], sDO[l * kSl + j], acc);
-            for (int c = 0; c < kD; ++c) acc = fmaf(sKh[c * kCb + i], sR[c * kSl + j], acc);
-            sDU[p] = acc;
-            dun[(size_t)i * kD + col0 + j] = acc;
-        }
-        __syncthreads();
-        for (int p = tid; p < kD * kSl; p += nt) {
-            const int c = p / kSl, j = p - c * kSl;
-            float acc = sGam[c] * sR[p];
-            for (int i = 0; i < kCb; ++i) {
-                acc = fmaf(sQb[c * kCb + i], sDO[i * kSl + j], acc);
-                acc = fmaf(-sWT[c * kCb + i], sDU[i * kSl + j], acc);
-            }
-            sR[p] = acc;
-        }
-    }
-    __syncthreads();
-    if (ds0)
-        for (int p = tid; p < kD * kSl; p += nt) {
-            const int c = p / kSl, j = p - c * kSl;
-            ds0[((size_t)bh * kD + c) * kD + col0 + j] = sR[p];
-        }
-}
-
-// ---- grad_kernel: every per-token gradient of one (chunk, head), one CTA of 512 threads per SM
-constexpr int kGT = 512;          // threads
-constexpr int kLS = 132;          // padded row of its [*][128] arrays (16-byte aligned rows)
-constexpr int kLQ = 36;           // padded row of its [32][32] arrays
-constexpr int kSlot = kCb * kLS;  // one [32][128] array
-
-namespace gk {  // shared-memory map (floats); arrays that are dead by the time another is written share room
-constexpr int slot(int i) { return i * kSlot; }
-constexpr int DS = 0, SS = kD * kLS;  // dS_{n+1}, S_n [128][kLS]: slots 0-3 and 4-7 while the big products run
-constexpr int DKH = slot(0), DQB = slot(1), DW = slot(2), XX = slot(2), U0 = slot(3), KB = slot(3), G = slot(4),
-              K = slot(5), BETA = slot(6), Q = slot(7);
-constexpr int U = slot(8), DKB = slot(8), DU = slot(9), ZV = slot(9), DO = slot(10), YY = slot(10);
-constexpr int TM = slot(11);                  // T [32][kLQ]
-constexpr int DT = TM + kCb * kLQ;            // dT
-constexpr int PP = DT + kCb * kLQ;            // T^T dT
-constexpr int DA = PP + kCb * kLQ, DAT = DA + kCb * kLQ, DM = DAT + kCb * kLQ, DMT = DM + kCb * kLQ;
-constexpr int DGP = DMT + kCb * kLQ;          // [4][128] partial rowsums of dS' . S
-constexpr int DGL = DGP + 4 * kD;             // [4][128] partial sums of dK^ . K^
-constexpr int TOTAL = DGL + 4 * kD;
-}  // namespace gk
+// ---- the two chains over chunks: one CTA of 512 threads per (batch-head, 64 columns of d_v), the
+// 128 x 64 state slice in registers (4 x 4 per thread) with a copy in shared memory for the products
+// that contract over d_k; the next chunk's factors arrive by cp.async while this chunk is processed.
+constexpr int kCT = 512;        // threads of a chain CTA
+constexpr int kSl = 64;         // d_v columns per chain CTA
+constexpr int kLJ = kSl + 4;    // padded row of [*][64] slices
+constexpr int kLW = kD + 4;     // padded row of [32][128] factor rows
+constexpr int kLM = kCb + 4;    // padded row of [32][32]
 
 __device__ __forceinline__ float4 lds4(const float* p) { return *reinterpret_cast<const float4*>(p); }
 __device__ __forceinline__ void sts4(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
 __device__ __forceinline__ float dot4(float4 a, float4 b, float acc) {
     return fmaf(a.w, b.w, fmaf(a.z, b.z, fmaf(a.y, b.y, fmaf(a.x, b.x, acc))));
 }
-__device__ __forceinline__ void cp_async16(float* smem, const float* gmem) {
+__device__ __forceinline__ float comp(float4 v, int i) { return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w; }
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(smem))),
                  "l"(gmem)
                  : "memory");
 }
+// 16 bytes, or zeros when !valid (nothing is read then)
+__device__ __forceinline__ void cp_async16_zfill(void* smem, const void* gmem, bool valid) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(smem))),
+                 "l"(gmem), "r"(valid ? 16 : 0)
+                 : "memory");
+}
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 // waits until at most n of this thread's most recent groups are in flight (n folds to a constant when unrolled)
 __device__ __forceinline__ void cp_async_wait(int n) {
     switch (n) {
@@ -148,7 +69,7 @@ __device__ __forceinline__ void cp_async_wait(int n) {
         default: asm volatile("cp.async.wait_group 7;" ::: "memory"); break;
     }
 }
-// four consecutive elements of a token tensor as fp32
+// four consecutive elements of a token tensor (global or shared) as fp32
 template <typename Tin>
 __device__ __forceinline__ float4 ld4_tok(const Tin* p) {
     if constexpr (sizeof(Tin) == 4) {
@@ -172,6 +93,327 @@ __device__ __forceinline__ void st4_tok(Tin* p, float4 x) {
         *reinterpret_cast<uint2*>(p) = u;
     }
 }
+
+// Thread roles shared by both chains.
+//  Rows-of-C products (out [32][64], contraction over d_k = 128): thread = 4 x 4 tile (iq, jq) and one
+//  quarter kq of the contraction (c = 16m + 4kq + 0..3); the quarters are added by a butterfly over the
+//  four lanes of a tile that leaves row 4iq + kq in lane kq.
+//  State products (out [128][64], contraction over the 32 tokens): thread = 4 x 4 tile (cq, jq), which
+//  is also the register-resident part of the state it owns.
+struct ChainRoles {
+    int kq, iq, jq1;  // rows-of-C tile
+    int cq, jq2;      // state tile
+    __device__ ChainRoles(int tid) {
+        const int warp = tid >> 5, lane = tid & 31, tl = lane >> 2;
+        kq = lane & 3;
+        iq = 2 * (warp & 3) + (tl & 1);
+        jq1 = 4 * (warp >> 2) + (tl >> 1);
+        cq = 8 * (warp & 3) + (lane & 7);
+        jq2 = 4 * (warp >> 2) + (lane >> 3);
+    }
+};
+
+// a[ii][jj] summed over the four lanes kq of a tile; returns row kq
+__device__ __forceinline__ float4 quarter_sum(float (&a)[4][4], int kq) {
+    const bool hi = kq & 2;
+    float keep[2][4];
+#pragma unroll
+    for (int r = 0; r < 2; ++r)
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+            const float mine_lo = a[r][jj], mine_hi = a[2 + r][jj];
+            const float send = hi ? mine_lo : mine_hi;
+            keep[r][jj] = (hi ? mine_hi : mine_lo) + __shfl_xor_sync(0xffffffffu, send, 2);
+        }
+    const bool odd = kq & 1;
+    float out[4];
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj) {
+        const float send = odd ? keep[0][jj] : keep[1][jj];
+        out[jj] = (odd ? keep[1][jj] : keep[0][jj]) + __shfl_xor_sync(0xffffffffu, send, 1);
+    }
+    return make_float4(out[0], out[1], out[2], out[3]);
+}
+
+namespace fc {  // shared-memory map of save_chain_kernel (floats)
+constexpr int S = 0;                          // S_n [128][kLJ]
+constexpr int U = S + kD * kLJ;               // U [32][kLJ]
+constexpr int BUF = U + kCb * kLJ;            // two factor buffers
+constexpr int W = 0, KH = W + kCb * kLW, UT = KH + kCb * kLW, GAM = UT + kCb * kLJ, BUF_FLOATS = GAM + kD;
+constexpr int TOTAL = BUF + 2 * BUF_FLOATS;
+}  // namespace fc
+
+// Forward chain keeping, for every chunk n, S_n (the state entering it) and U_n = U~_n - W_n S_n; with
+// the token-major factors of factors_simt_kernel:  S_{n+1} = diag(e^{G_last}) S_n + K^_n^T U_n.
+__global__ void __launch_bounds__(kCT, 1) save_chain_kernel(const float* __restrict__ ws, const float* __restrict__ s0,
+                                                           float* __restrict__ s_save, float* __restrict__ u_save,
+                                                           int NC) {
+    extern __shared__ __align__(16) float sm[];
+    const int bh = blockIdx.x, col0 = blockIdx.y * kSl, tid = threadIdx.x;
+    const SimtWs L{kD, kD, kCb};
+    const ChainRoles R(tid);
+    auto prefetch = [&](int n, float* buf) {
+        const float* u = ws + ((size_t)bh * NC + n) * L.unit_floats();
+        for (int i = tid; i < 2 * kCb * (kD / 4); i += kCT) {  // W, K^ rows
+            const int m = i >> 10, r = (i >> 5) & (kCb - 1), c4 = 4 * (i & 31);
+            cp_async16(buf + (m ? fc::KH : fc::W) + r * kLW + c4, u + (m ? L.off_kht() : L.off_wt()) + r * kD + c4);
+        }
+        {   // this CTA's columns of U~, and e^{G_last}
+            const int r = tid >> 4, c4 = 4 * (tid & 15);
+            cp_async16(buf + fc::UT + r * kLJ + c4, u + L.off_utt() + r * kD + col0 + c4);
+        }
+        if (tid < kD / 4) cp_async16(buf + fc::GAM + 4 * tid, u + L.off_gam() + 4 * tid);
+        cp_async_commit();
+    };
+    float S[4][4];  // rows 4cq + r, columns 4jq2 + jj of this CTA's slice
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        const float4 x = s0 ? *reinterpret_cast<const float4*>(s0 + ((size_t)bh * kD + 4 * R.cq + r) * kD + col0 + 4 * R.jq2)
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+        S[r][0] = x.x; S[r][1] = x.y; S[r][2] = x.z; S[r][3] = x.w;
+        sts4(sm + fc::S + (4 * R.cq + r) * kLJ + 4 * R.jq2, x);
+    }
+    prefetch(0, sm + fc::BUF);
+    cp_async_wait_all();
+    __syncthreads();
+    for (int n = 0; n < NC; ++n) {
+        const float* buf = sm + fc::BUF + (n & 1) * fc::BUF_FLOATS;
+        const size_t unit = (size_t)bh * NC + n;
+#pragma unroll
+        for (int r = 0; r < 4; ++r)  // S_n
+            *reinterpret_cast<float4*>(s_save + (unit * kD + 4 * R.cq + r) * kD + col0 + 4 * R.jq2) =
+                make_float4(S[r][0], S[r][1], S[r][2], S[r][3]);
+        if (n + 1 < NC) prefetch(n + 1, sm + fc::BUF + ((n + 1) & 1) * fc::BUF_FLOATS);
+        // U = U~ - W S_n (contraction over d_k)
+        {
+            float a[4][4];
+#pragma unroll
+            for (int ii = 0; ii < 4; ++ii)
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) a[ii][jj] = 0.f;
+#pragma unroll 4
+            for (int m = 0; m < 8; ++m) {
+                const int c0 = 16 * m + 4 * R.kq;
+                float4 wv[4], sv[4];
+#pragma unroll
+                for (int ii = 0; ii < 4; ++ii) wv[ii] = lds4(buf + fc::W + (4 * R.iq + ii) * kLW + c0);
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) sv[cc] = lds4(sm + fc::S + (c0 + cc) * kLJ + 4 * R.jq1);
+#pragma unroll
+                for (int ii = 0; ii < 4; ++ii) {
+                    a[ii][0] = fmaf(wv[ii].x, sv[0].x, fmaf(wv[ii].y, sv[1].x, fmaf(wv[ii].z, sv[2].x, fmaf(wv[ii].w, sv[3].x, a[ii][0]))));
+                    a[ii][1] = fmaf(wv[ii].x, sv[0].y, fmaf(wv[ii].y, sv[1].y, fmaf(wv[ii].z, sv[2].y, fmaf(wv[ii].w, sv[3].y, a[ii][1]))));
+                    a[ii][2] = fmaf(wv[ii].x, sv[0].z, fmaf(wv[ii].y, sv[1].z, fmaf(wv[ii].z, sv[2].z, fmaf(wv[ii].w, sv[3].z, a[ii][2]))));
+                    a[ii][3] = fmaf(wv[ii].x, sv[0].w, fmaf(wv[ii].y, sv[1].w, fmaf(wv[ii].z, sv[2].w, fmaf(wv[ii].w, sv[3].w, a[ii][3]))));
+                }
+            }
+            const float4 ws4 = quarter_sum(a, R.kq);
+            const int i = 4 * R.iq + R.kq;
+            const float4 ut = lds4(buf + fc::UT + i * kLJ + 4 * R.jq1);
+            const float4 uu = make_float4(ut.x - ws4.x, ut.y - ws4.y, ut.z - ws4.z, ut.w - ws4.w);
+            sts4(sm + fc::U + i * kLJ + 4 * R.jq1, uu);
+            *reinterpret_cast<float4*>(u_save + (unit * kCb + i) * kD + col0 + 4 * R.jq1) = uu;
+        }
+        __syncthreads();
+        // S_{n+1} = diag(e^{G_last}) S_n + K^^T U (contraction over the chunk's tokens)
+        {
+            const float4 gm = lds4(buf + fc::GAM + 4 * R.cq);
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) S[r][jj] *= comp(gm, r);
+#pragma unroll 4
+            for (int i = 0; i < kCb; ++i) {
+                const float4 kv = lds4(buf + fc::KH + i * kLW + 4 * R.cq);
+                const float4 uv = lds4(sm + fc::U + i * kLJ + 4 * R.jq2);
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    const float kr = comp(kv, r);
+                    S[r][0] = fmaf(kr, uv.x, S[r][0]);
+                    S[r][1] = fmaf(kr, uv.y, S[r][1]);
+                    S[r][2] = fmaf(kr, uv.z, S[r][2]);
+                    S[r][3] = fmaf(kr, uv.w, S[r][3]);
+                }
+            }
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+                sts4(sm + fc::S + (4 * R.cq + r) * kLJ + 4 * R.jq2, make_float4(S[r][0], S[r][1], S[r][2], S[r][3]));
+        }
+        cp_async_wait_all();
+        __syncthreads();
+    }
+}
+
+namespace ac {  // shared-memory map of adjoint_kernel (floats)
+constexpr int R = 0;                          // dS_{n+1} [128][kLJ]
+constexpr int DU = R + kD * kLJ;              // dU [32][kLJ]
+constexpr int BUF = DU + kCb * kLJ;           // two buffers of factors and dO rows
+constexpr int KH = 0, QB = KH + kCb * kLW, W = QB + kCb * kLW, M = W + kCb * kLW, GAM = M + kCb * kLM,
+              DO = GAM + kD, BUF_FLOATS = DO + kCb * kLJ;   // dO rows: 272 bytes each whatever the dtype
+constexpr int TOTAL = BUF + 2 * BUF_FLOATS;
+}  // namespace ac
+
+// dS and dU over the chunks in reverse, with dO~ = scale dO:
+//     dU_n = M_n^T dO~_n + K^_n dS_{n+1},   dS_n = diag(e^{G_last}) dS_{n+1} + Q_bar_n^T dO~_n - W_n^T dU_n,
+// keeping dS_{n+1} and dU_n of every chunk and writing dS_0.
+template <typename Tin>
+__global__ void __launch_bounds__(kCT, 1) adjoint_kernel(const float* __restrict__ ws, const Tin* __restrict__ dO,
+                                                        const float* __restrict__ dsT, float* __restrict__ ds0,
+                                                        float* __restrict__ ds_save, float* __restrict__ du_save,
+                                                        int T, int Hv, int NC, float scale) {
+    extern __shared__ __align__(16) float sm[];
+    const int bh = blockIdx.x, bi = bh / Hv, hv = bh - bi * Hv, col0 = blockIdx.y * kSl, tid = threadIdx.x;
+    const SimtWs L{kD, kD, kCb};
+    const ChainRoles R(tid);
+    constexpr int kPieces = kSl * (int)sizeof(Tin) / 16;  // 16-byte pieces of one dO row slice
+    auto prefetch = [&](int n, float* buf) {
+        const float* u = ws + ((size_t)bh * NC + n) * L.unit_floats();
+        for (int i = tid; i < 3 * kCb * (kD / 4); i += kCT) {  // K^, Q_bar, W rows
+            const int m = i >> 10, r = (i >> 5) & (kCb - 1), c4 = 4 * (i & 31);
+            const int dst = m == 0 ? ac::KH : m == 1 ? ac::QB : ac::W;
+            const size_t src = m == 0 ? L.off_kht() : m == 1 ? L.off_qbt() : L.off_wt();
+            cp_async16(buf + dst + r * kLW + c4, u + src + r * kD + c4);
+        }
+        if (tid < kCb * kCb / 4) {
+            const int r = tid >> 3, c4 = 4 * (tid & 7);
+            cp_async16(buf + ac::M + r * kLM + c4, u + L.off_m() + r * kCb + c4);
+        } else if (tid < kCb * kCb / 4 + kD / 4) {
+            const int c4 = 4 * (tid - kCb * kCb / 4);
+            cp_async16(buf + ac::GAM + c4, u + L.off_gam() + c4);
+        }
+        if (tid < kCb * kPieces) {  // dO rows of the chunk, zeros past the end of the sequence
+            const int r = tid / kPieces, pc = tid - r * kPieces, tok = n * kCb + r;
+            const bool valid = tok < T;
+            const Tin* src = dO + (((size_t)bi * T + (valid ? tok : 0)) * Hv + hv) * kD + col0 + pc * (16 / (int)sizeof(Tin));
+            cp_async16_zfill(reinterpret_cast<char*>(buf + ac::DO + r * kLJ) + 16 * pc, src, valid);
+        }
+        cp_async_commit();
+    };
+    float G[4][4];  // dS_{n+1}: rows 4cq + r, columns 4jq2 + jj of this CTA's slice
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        const float4 x = dsT ? *reinterpret_cast<const float4*>(dsT + ((size_t)bh * kD + 4 * R.cq + r) * kD + col0 + 4 * R.jq2)
+                             : make_float4(0.f, 0.f, 0.f, 0.f);
+        G[r][0] = x.x; G[r][1] = x.y; G[r][2] = x.z; G[r][3] = x.w;
+        sts4(sm + ac::R + (4 * R.cq + r) * kLJ + 4 * R.jq2, x);
+    }
+    prefetch(NC - 1, sm + ac::BUF + ((NC - 1) & 1) * ac::BUF_FLOATS);
+    cp_async_wait_all();
+    __syncthreads();
+    for (int n = NC - 1; n >= 0; --n) {
+        const float* buf = sm + ac::BUF + (n & 1) * ac::BUF_FLOATS;
+        const Tin* sDO = reinterpret_cast<const Tin*>(buf + ac::DO);
+        constexpr int kRowT = kLJ * 4 / (int)sizeof(Tin);  // dO row stride in elements
+        const size_t unit = (size_t)bh * NC + n;
+#pragma unroll
+        for (int r = 0; r < 4; ++r)  // dS_{n+1}
+            *reinterpret_cast<float4*>(ds_save + (unit * kD + 4 * R.cq + r) * kD + col0 + 4 * R.jq2) =
+                make_float4(G[r][0], G[r][1], G[r][2], G[r][3]);
+        if (n > 0) prefetch(n - 1, sm + ac::BUF + ((n - 1) & 1) * ac::BUF_FLOATS);
+        // dU = M^T dO~ + K^ dS_{n+1}
+        {
+            float a[4][4], am[4][4];
+#pragma unroll
+            for (int ii = 0; ii < 4; ++ii)
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) a[ii][jj] = am[ii][jj] = 0.f;
+#pragma unroll 4
+            for (int m = 0; m < 8; ++m) {
+                const int c0 = 16 * m + 4 * R.kq;
+                float4 kv[4], rv[4];
+#pragma unroll
+                for (int ii = 0; ii < 4; ++ii) kv[ii] = lds4(buf + ac::KH + (4 * R.iq + ii) * kLW + c0);
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) rv[cc] = lds4(sm + ac::R + (c0 + cc) * kLJ + 4 * R.jq1);
+#pragma unroll
+                for (int ii = 0; ii < 4; ++ii) {
+                    a[ii][0] = fmaf(kv[ii].x, rv[0].x, fmaf(kv[ii].y, rv[1].x, fmaf(kv[ii].z, rv[2].x, fmaf(kv[ii].w, rv[3].x, a[ii][0]))));
+                    a[ii][1] = fmaf(kv[ii].x, rv[0].y, fmaf(kv[ii].y, rv[1].y, fmaf(kv[ii].z, rv[2].y, fmaf(kv[ii].w, rv[3].y, a[ii][1]))));
+                    a[ii][2] = fmaf(kv[ii].x, rv[0].z, fmaf(kv[ii].y, rv[1].z, fmaf(kv[ii].z, rv[2].z, fmaf(kv[ii].w, rv[3].z, a[ii][2]))));
+                    a[ii][3] = fmaf(kv[ii].x, rv[0].w, fmaf(kv[ii].y, rv[1].w, fmaf(kv[ii].z, rv[2].w, fmaf(kv[ii].w, rv[3].w, a[ii][3]))));
+                }
+            }
+#pragma unroll
+            for (int m = 0; m < 8; ++m) {  // tokens l = 4m + kq; M[l][i] = 0 for l < i
+                const int l = 4 * m + R.kq;
+                const float4 mv = lds4(buf + ac::M + l * kLM + 4 * R.iq);
+                const float4 ov = ld4_tok(sDO + l * kRowT + 4 * R.jq1);
+#pragma unroll
+                for (int ii = 0; ii < 4; ++ii) {
+                    const float mi = comp(mv, ii);
+                    am[ii][0] = fmaf(mi, ov.x, am[ii][0]);
+                    am[ii][1] = fmaf(mi, ov.y, am[ii][1]);
+                    am[ii][2] = fmaf(mi, ov.z, am[ii][2]);
+                    am[ii][3] = fmaf(mi, ov.w, am[ii][3]);
+                }
+            }
+#pragma unroll
+            for (int ii = 0; ii < 4; ++ii)
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) a[ii][jj] = fmaf(scale, am[ii][jj], a[ii][jj]);
+            const float4 du = quarter_sum(a, R.kq);
+            const int i = 4 * R.iq + R.kq;
+            sts4(sm + ac::DU + i * kLJ + 4 * R.jq1, du);
+            *reinterpret_cast<float4*>(du_save + (unit * kCb + i) * kD + col0 + 4 * R.jq1) = du;
+        }
+        __syncthreads();
+        // dS_n = diag(e^{G_last}) dS_{n+1} + Q_bar^T dO~ - W^T dU
+        {
+            const float4 gm = lds4(buf + ac::GAM + 4 * R.cq);
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) G[r][jj] *= comp(gm, r);
+#pragma unroll 4
+            for (int i = 0; i < kCb; ++i) {
+                const float4 qv = lds4(buf + ac::QB + i * kLW + 4 * R.cq);
+                const float4 wv = lds4(buf + ac::W + i * kLW + 4 * R.cq);
+                float4 ov = ld4_tok(sDO + i * kRowT + 4 * R.jq2);
+                ov = make_float4(scale * ov.x, scale * ov.y, scale * ov.z, scale * ov.w);
+                const float4 dv = lds4(sm + ac::DU + i * kLJ + 4 * R.jq2);
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    const float qr = comp(qv, r), wr = -comp(wv, r);
+                    G[r][0] = fmaf(qr, ov.x, fmaf(wr, dv.x, G[r][0]));
+                    G[r][1] = fmaf(qr, ov.y, fmaf(wr, dv.y, G[r][1]));
+                    G[r][2] = fmaf(qr, ov.z, fmaf(wr, dv.z, G[r][2]));
+                    G[r][3] = fmaf(qr, ov.w, fmaf(wr, dv.w, G[r][3]));
+                }
+            }
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+                sts4(sm + ac::R + (4 * R.cq + r) * kLJ + 4 * R.jq2, make_float4(G[r][0], G[r][1], G[r][2], G[r][3]));
+        }
+        cp_async_wait_all();
+        __syncthreads();
+    }
+    if (ds0)
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+            *reinterpret_cast<float4*>(ds0 + ((size_t)bh * kD + 4 * R.cq + r) * kD + col0 + 4 * R.jq2) =
+                make_float4(G[r][0], G[r][1], G[r][2], G[r][3]);
+}
+
+// ---- grad_kernel: every per-token gradient of one (chunk, head), one CTA of 512 threads per SM
+constexpr int kGT = 512;          // threads
+constexpr int kLS = 132;          // padded row of its [*][128] arrays (16-byte aligned rows)
+constexpr int kLQ = 36;           // padded row of its [32][32] arrays
+constexpr int kSlot = kCb * kLS;  // one [32][128] array
+
+namespace gk {  // shared-memory map (floats); arrays that are dead by the time another is written share room
+constexpr int slot(int i) { return i * kSlot; }
+constexpr int DS = 0, SS = kD * kLS;  // dS_{n+1}, S_n [128][kLS]: slots 0-3 and 4-7 while the big products run
+constexpr int DKH = slot(0), DQB = slot(1), DW = slot(2), XX = slot(2), U0 = slot(3), KB = slot(3), G = slot(4),
+              K = slot(5), BETA = slot(6), Q = slot(7);
+constexpr int U = slot(8), DKB = slot(8), DU = slot(9), ZV = slot(9), DO = slot(10), YY = slot(10);
+constexpr int TM = slot(11);                  // T [32][kLQ]
+constexpr int DT = TM + kCb * kLQ;            // dT
+constexpr int PP = DT + kCb * kLQ;            // T^T dT
+constexpr int DA = PP + kCb * kLQ, DAT = DA + kCb * kLQ, DM = DAT + kCb * kLQ, DMT = DM + kCb * kLQ;
+constexpr int DGP = DMT + kCb * kLQ;          // [4][128] partial rowsums of dS' . S
+constexpr int DGL = DGP + 4 * kD;             // [4][128] partial sums of dK^ . K^
+constexpr int TOTAL = DGL + 4 * kD;
+}  // namespace gk
 
 // The local gradients of one (chunk n, batch-head bh), given S_n, dS_{n+1}, U, dU and T of the chunk:
 //   1. dK^ = U dS'^T, dQ_bar = dO~ S^T, dW = -dU S^T, dgamma = rowsum(dS' . S)  (K = d_v, register tiles of
@@ -660,17 +902,21 @@ cudaError_t launch_t(const void* q, const void* k, const void* v, const void* g,
     float* du_save = reinterpret_cast<float*>(ws + L.du);
     float* dq_ws = reinterpret_cast<float*>(ws + L.dq);
     float* dk_ws = reinterpret_cast<float*>(ws + L.dk);
-    cudaError_t e = launch_chunk_simt_saving(q, k, v, g, b, w, s0, sh, std::is_same<Tin, float>::value ? GDN2_F32 : GDN2_BF16,
-                                             simt, t_ws, s_save, u_save, s);
+    cudaError_t e = launch_factors_simt(q, k, v, g, b, w, sh, std::is_same<Tin, float>::value ? GDN2_F32 : GDN2_BF16,
+                                        simt, t_ws, /*token_major=*/true, s);
     if (e != cudaSuccess) return e;
-    const size_t a_smem = sizeof(float) * ((size_t)kD * kSl + 3 * (size_t)kD * kCb + kCb * kCb + kD + 2 * kCb * kSl);
+    const size_t c_smem = sizeof(float) * (size_t)fc::TOTAL, a_smem = sizeof(float) * (size_t)ac::TOTAL;
     const size_t g_smem = sizeof(float) * (size_t)gk::TOTAL;
+    e = cudaFuncSetAttribute(save_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)c_smem);
+    if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(adjoint_kernel<Tin>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)a_smem);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(grad_kernel<Tin>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)g_smem);
     if (e != cudaSuccess) return e;
-    adjoint_kernel<Tin><<<dim3(B * Hv, kD / kSl), 256, a_smem, s>>>(simt, static_cast<const Tin*>(d_o), dsT, ds0,
-                                                                    ds_save, du_save, T, Hv, NC, scale);
+    save_chain_kernel<<<dim3(B * Hv, kD / kSl), kCT, c_smem, s>>>(simt, s0, s_save, u_save, NC);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    adjoint_kernel<Tin><<<dim3(B * Hv, kD / kSl), kCT, a_smem, s>>>(simt, static_cast<const Tin*>(d_o), dsT, ds0,
+                                                                   ds_save, du_save, T, Hv, NC, scale);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     grad_kernel<Tin><<<dim3(NC, B * Hv), kGT, g_smem, s>>>(
         static_cast<const Tin*>(q), static_cast<const Tin*>(k), static_cast<const Tin*>(v), static_cast<const Tin*>(g),

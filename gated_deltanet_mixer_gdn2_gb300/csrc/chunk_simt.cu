@@ -30,7 +30,7 @@ __global__ void __launch_bounds__(256) factors_simt_kernel(const Tin* __restrict
                                                            const Tin* __restrict__ v, const Tin* __restrict__ g,
                                                            const Tin* __restrict__ b, const Tin* __restrict__ w,
                                                            float* __restrict__ ws, float* __restrict__ t_out, int T,
-                                                           int Hk, int Hv, int dk, int dv, int C) {
+                                                           int Hk, int Hv, int dk, int dv, int C, int imajor) {
     extern __shared__ float smem[];
     const int n = blockIdx.x;                // chunk
     const int bh = blockIdx.y;               // bi * Hv + hv
@@ -105,9 +105,11 @@ __global__ void __launch_bounds__(256) factors_simt_kernel(const Tin* __restrict
             sT[i * (C + 1) + j] = -acc;
         }
     }
-    // decayed q and k (transposed, [d_k][C]) for the state kernel; b . k . e^{G} in place
+    // decayed q and k ([d_k][C], or [C][d_k] when imajor) for the state kernel; b . k . e^{G} in place
     for (int p = tid; p < dk * C; p += nt) {
-        const int c = p / C, i = p - c * C;
+        int c, i;
+        if (imajor) i = p / dk, c = p - i * dk;
+        else c = p / C, i = p - c * C;
         const float Gi = sG[i * LD + c];
         u[L.off_qbt() + p] = sQ[i * LDQ + c] * expf(Gi);
         u[L.off_kht() + p] = sK[i * LD + c] * expf(sG[(C - 1) * LD + c] - Gi);
@@ -128,15 +130,20 @@ __global__ void __launch_bounds__(256) factors_simt_kernel(const Tin* __restrict
         sQ[t * LDQ + c] = x;
     }
     __syncthreads();
-    // W^T [d_k][C] = (T X)^T with X = b . k . e^{G};  U~^T [d_v][C] = (T (w . v))^T
+    // W^T [d_k][C] = (T X)^T with X = b . k . e^{G};  U~^T [d_v][C] = (T (w . v))^T  (W [C][d_k] and
+    // U~ [C][d_v] when imajor)
     for (int p = tid; p < dk * C; p += nt) {
-        const int c = p / C, i = p - c * C;
+        int c, i;
+        if (imajor) i = p / dk, c = p - i * dk;
+        else c = p / C, i = p - c * C;
         float acc = 0.f;
         for (int j = 0; j <= i; ++j) acc = fmaf(sT[i * (C + 1) + j], sBK[j * LD + c], acc);
         u[L.off_wt() + p] = acc;
     }
     for (int p = tid; p < dv * C; p += nt) {
-        const int c = p / C, i = p - c * C;
+        int c, i;
+        if (imajor) i = p / dv, c = p - i * dv;
+        else c = p / C, i = p - c * C;
         float acc = 0.f;
         for (int j = 0; j <= i; ++j) acc = fmaf(sT[i * (C + 1) + j], sQ[j * LDQ + c], acc);
         u[L.off_utt() + p] = acc;
@@ -152,8 +159,7 @@ constexpr int kSlice = 16;
 
 template <typename Tin>
 __global__ void __launch_bounds__(256) state_simt_kernel(const float* __restrict__ ws, const float* __restrict__ s0,
-                                                         float* __restrict__ sT_out, Tin* __restrict__ o,
-                                                         float* __restrict__ s_save, float* __restrict__ u_save, int T,
+                                                         float* __restrict__ sT_out, Tin* __restrict__ o, int T,
                                                          int Hv, int dk, int dv, int C, int NC, float scale) {
     extern __shared__ float smem[];
     const int bh = blockIdx.x;
@@ -186,11 +192,6 @@ __global__ void __launch_bounds__(256) state_simt_kernel(const float* __restrict
         for (int p = tid; p < C * C; p += nt) sM[p] = u[L.off_m() + p];
         for (int p = tid; p < kSlice * C; p += nt) sUt[p] = u[L.off_utt() + (size_t)col0 * C + p];
         for (int p = tid; p < dk; p += nt) sGam[p] = u[L.off_gam() + p];
-        if (s_save)  // S_n, the state entering the chunk, for the gradients
-            for (int p = tid; p < dk * kSlice; p += nt) {
-                const int c = p / kSlice, j = p - c * kSlice;
-                s_save[(((size_t)bh * NC + n) * dk + c) * dv + col0 + j] = sS[p];
-            }
         __syncthreads();
         // U = U~ - W S_n ;  P = (q . e^{G}) S_n
         for (int p = tid; p < C * kSlice; p += nt) {
@@ -203,14 +204,13 @@ __global__ void __launch_bounds__(256) state_simt_kernel(const float* __restrict
             }
             sU[p] = sUt[j * C + i] - ws_;
             sP[p] = qs;
-            if (u_save) u_save[(((size_t)bh * NC + n) * C + i) * dv + col0 + j] = sU[p];
         }
         __syncthreads();
         // O = P + M U ;  S_{n+1} = diag(e^{G_last}) S_n + K^^T U
         for (int p = tid; p < C * kSlice; p += nt) {
             const int i = p / kSlice, j = p - i * kSlice;
             const int tok = n * C + i;
-            if (o && tok < T) {
+            if (tok < T) {
                 float acc = sP[p];
                 for (int l = 0; l <= i; ++l) acc = fmaf(sM[i * C + l], sU[l * kSlice + j], acc);
                 o[(((size_t)bi * T + tok) * Hv + hv) * dv + col0 + j] = from_f32<Tin>(scale * acc);
@@ -241,26 +241,30 @@ size_t state_smem(int dk, int C) {
 }
 
 template <typename Tin>
-cudaError_t launch_t(const void* q, const void* k, const void* v, const void* g, const void* b, const void* w,
-                     const float* s0, float* sT, void* o, const ChunkShape& sh, float scale, void* ws, cudaStream_t s,
-                     float* t_out = nullptr, float* s_save = nullptr, float* u_save = nullptr) {
-    const int NC = sh.nchunks();
+cudaError_t launch_factors_t(const void* q, const void* k, const void* v, const void* g, const void* b, const void* w,
+                             const ChunkShape& sh, void* ws, float* t_out, int imajor, cudaStream_t s) {
     const size_t f_smem = factors_smem(sh.dk, sh.dv, sh.C);
-    const size_t s_smem = state_smem(sh.dk, sh.C);
     cudaError_t e = cudaFuncSetAttribute(factors_simt_kernel<Tin>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)f_smem);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(state_simt_kernel<Tin>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s_smem);
-    if (e != cudaSuccess) return e;
-    factors_simt_kernel<Tin><<<dim3(NC, sh.B * sh.Hv), 256, f_smem, s>>>(
+    factors_simt_kernel<Tin><<<dim3(sh.nchunks(), sh.B * sh.Hv), 256, f_smem, s>>>(
         static_cast<const Tin*>(q), static_cast<const Tin*>(k), static_cast<const Tin*>(v),
         static_cast<const Tin*>(g), static_cast<const Tin*>(b), static_cast<const Tin*>(w), static_cast<float*>(ws),
-        t_out, sh.T, sh.Hk, sh.Hv, sh.dk, sh.dv, sh.C);
-    e = cudaGetLastError();
+        t_out, sh.T, sh.Hk, sh.Hv, sh.dk, sh.dv, sh.C, imajor);
+    return cudaGetLastError();
+}
+
+template <typename Tin>
+cudaError_t launch_t(const void* q, const void* k, const void* v, const void* g, const void* b, const void* w,
+                     const float* s0, float* sT, void* o, const ChunkShape& sh, float scale, void* ws, cudaStream_t s) {
+    const int NC = sh.nchunks();
+    const size_t s_smem = state_smem(sh.dk, sh.C);
+    cudaError_t e = launch_factors_t<Tin>(q, k, v, g, b, w, sh, ws, nullptr, 0, s);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(state_simt_kernel<Tin>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s_smem);
     if (e != cudaSuccess) return e;
     state_simt_kernel<Tin><<<dim3(sh.B * sh.Hv, sh.dv / kSlice), 256, s_smem, s>>>(
-        static_cast<const float*>(ws), s0, sT, static_cast<Tin*>(o), s_save, u_save, sh.T, sh.Hv, sh.dk, sh.dv, sh.C,
-        NC, scale);
+        static_cast<const float*>(ws), s0, sT, static_cast<Tin*>(o), sh.T, sh.Hv, sh.dk, sh.dv, sh.C, NC, scale);
     return cudaGetLastError();
 }
 
@@ -278,12 +282,12 @@ cudaError_t launch_chunk_simt(const void* q, const void* k, const void* v, const
     return launch_t<float>(q, k, v, g, b, w, s0, sT, o, sh, scale, ws, s);
 }
 
-cudaError_t launch_chunk_simt_saving(const void* q, const void* k, const void* v, const void* g, const void* b,
-                                     const void* w, const float* s0, const ChunkShape& sh, gdn2_dtype dt, void* ws,
-                                     float* t_out, float* s_save, float* u_save, cudaStream_t s) {
-    if (dt == GDN2_BF16)
-        return launch_t<__nv_bfloat16>(q, k, v, g, b, w, s0, nullptr, nullptr, sh, 1.f, ws, s, t_out, s_save, u_save);
-    return launch_t<float>(q, k, v, g, b, w, s0, nullptr, nullptr, sh, 1.f, ws, s, t_out, s_save, u_save);
+cudaError_t launch_factors_simt(const void* q, const void* k, const void* v, const void* g, const void* b,
+                                const void* w, const ChunkShape& sh, gdn2_dtype dt, void* ws, float* t_out,
+                                bool token_major, cudaStream_t s) {
+    const int im = token_major ? 1 : 0;
+    if (dt == GDN2_BF16) return launch_factors_t<__nv_bfloat16>(q, k, v, g, b, w, sh, ws, t_out, im, s);
+    return launch_factors_t<float>(q, k, v, g, b, w, sh, ws, t_out, im, s);
 }
 
 int chunk_simt_read_clear_status(cudaStream_t) {

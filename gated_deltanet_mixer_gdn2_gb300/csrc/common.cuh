@@ -104,9 +104,9 @@ cudaError_t launch_recurrent(const void* q, const void* k, const void* v, const 
                              int B, int N, int Hk, int Hv, int dk, int dv, float scale, gdn2_dtype dt,
                              cudaStream_t s);
 
-// Per-unit fp32 workspace of the CUDA-core chunked forward (chunk_simt.cu), read by the chunked
-// backward (backward_chunk.cu): W^T, (q.e^G)^T, (k.e^{G_last-G})^T [d_k][C], M [C][C], U~^T [d_v][C],
-// e^{G_last} [d_k].
+// Per-unit fp32 workspace of the CUDA-core chunked forward (chunk_simt.cu), also read by the chunked
+// backward (backward_chunk.cu): W, q.e^G, k.e^{G_last-G} ([d_k][C], or token-major [C][d_k]), M [C][C],
+// U~ ([d_v][C], or token-major [C][d_v]), e^{G_last} [d_k].
 struct SimtWs {
     int dk, dv, C;
     __host__ __device__ size_t unit_floats() const {
@@ -122,18 +122,17 @@ struct SimtWs {
 };
 
 size_t chunk_simt_workspace_bytes(const ChunkShape& sh);
-// As launch_chunk_simt without the output, also writing T = (I + A)^{-1} per unit [C][C] (t_out), the
-// state entering every chunk [B*H_v][NC][d_k][d_v] (s_save) and U of every chunk [B*H_v][NC][C][d_v]
-// (u_save).
+// The state-independent factors of every chunk into ws (layout SimtWs; token-major when token_major),
+// and, when t_out is given, T = (I + A)^{-1} per unit [C][C].
+cudaError_t launch_factors_simt(const void* q, const void* k, const void* v, const void* g, const void* b,
+                                const void* w, const ChunkShape& sh, gdn2_dtype dt, void* ws, float* t_out,
+                                bool token_major, cudaStream_t s);
 // Chunked backward (backward_chunk.cu): workspace bytes and the launches; d_k = d_v = 128.
 size_t backward_chunked_workspace_bytes(int B, int T, int Hv);
 cudaError_t launch_backward_chunked(const void* q, const void* k, const void* v, const void* g, const void* b,
                                     const void* w, const float* s0, const void* d_o, const float* dsT, void* dq,
                                     void* dk, void* dv, void* dg, void* db, void* dw, float* ds0, int B, int T, int Hk,
                                     int Hv, float scale, gdn2_dtype dt, void* ws, cudaStream_t s);
-cudaError_t launch_chunk_simt_saving(const void* q, const void* k, const void* v, const void* g, const void* b,
-                                     const void* w, const float* s0, const ChunkShape& sh, gdn2_dtype dt, void* ws,
-                                     float* t_out, float* s_save, float* u_save, cudaStream_t s);
 cudaError_t launch_chunk_simt(const void* q, const void* k, const void* v, const void* g, const void* b,
                               const void* w, const float* s0, float* sT, void* o, const ChunkShape& sh, float scale,
                               gdn2_dtype dt, void* ws, cudaStream_t s);
