@@ -25,12 +25,15 @@ namespace {
 
 __device__ int g_status_simt;
 
-template <typename Tin>
+// kDK, kDV, kC: the sizes as compile-time constants, or 0 to take them from the arguments
+template <typename Tin, int kDK, int kDV, int kC>
 __global__ void __launch_bounds__(256) factors_simt_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k,
                                                            const Tin* __restrict__ v, const Tin* __restrict__ g,
                                                            const Tin* __restrict__ b, const Tin* __restrict__ w,
                                                            float* __restrict__ ws, float* __restrict__ t_out, int T,
-                                                           int Hk, int Hv, int dk, int dv, int C, int imajor) {
+                                                           int Hk, int Hv, int dk_arg, int dv_arg, int C_arg,
+                                                           int imajor) {
+    const int dk = kDK ? kDK : dk_arg, dv = kDV ? kDV : dv_arg, C = kC ? kC : C_arg;
     extern __shared__ float smem[];
     const int n = blockIdx.x;                // chunk
     const int bh = blockIdx.y;               // bi * Hv + hv
@@ -46,6 +49,7 @@ __global__ void __launch_bounds__(256) factors_simt_kernel(const Tin* __restrict
     float* sQ = sBK + C * LD;                // [C][LDQ]  q, later w . v
     float* sA = sQ + C * LDQ;                // [C][C+1]
     float* sT = sA + C * (C + 1);            // [C][C+1]
+    float* sX = sQ;                          // [16][C] block products of the inverse (q is read out by then)
 
     const SimtWs L{dk, dv, C};
     float* u = ws + ((size_t)bh * NC + n) * L.unit_floats();
@@ -75,31 +79,43 @@ __global__ void __launch_bounds__(256) factors_simt_kernel(const Tin* __restrict
             acc += sG[t * LD + c];
             sG[t * LD + c] = acc;
         }
-        u[L.off_gam() + c] = expf(acc);
+        u[L.off_gam() + c] = __expf(acc);
     }
     __syncthreads();
-    // erase interaction A (strictly lower) and causal q-k M (lower incl. diagonal)
+    // erase interaction A (strictly lower) and causal q-k M (lower incl. diagonal): one thread per pair
+    // (i, j <= i), the pairs numbered along the lower triangle so that no lane idles above the diagonal
     float* Mws = u + L.off_m();
     for (int p = tid; p < C * C; p += nt) {
         const int i = p / C, j = p - i * C;
+        sT[i * (C + 1) + j] = 0.f;
+        if (j > i) {
+            sA[i * (C + 1) + j] = 0.f;
+            Mws[p] = 0.f;
+        }
+    }
+    for (int p = tid; p < C * (C + 1) / 2; p += nt) {
+        int i = static_cast<int>((sqrtf(8.f * p + 1.f) - 1.f) * 0.5f);
+        while ((i + 1) * (i + 2) / 2 <= p) ++i;
+        while (i * (i + 1) / 2 > p) --i;
+        const int j = p - i * (i + 1) / 2;
         float a = 0.f, m = 0.f;
-        if (j <= i) {
-            for (int c = 0; c < dk; ++c) {
-                const float e = expf(sG[i * LD + c] - sG[j * LD + c]);
-                const float kj = sK[j * LD + c] * e;
-                a = fmaf(sBK[i * LD + c], kj, a);
-                m = fmaf(sQ[i * LDQ + c], kj, m);
-            }
+        for (int c = 0; c < dk; ++c) {
+            const float e = __expf(sG[i * LD + c] - sG[j * LD + c]);  // G_i - G_j <= 0
+            const float kj = sK[j * LD + c] * e;
+            a = fmaf(sBK[i * LD + c], kj, a);
+            m = fmaf(sQ[i * LDQ + c], kj, m);
         }
         sA[i * (C + 1) + j] = (j < i) ? a : 0.f;
-        Mws[p] = (j <= i) ? m : 0.f;
+        Mws[i * C + j] = m;
     }
     __syncthreads();
-    // T = (I + A)^{-1}: thread j solves column j by forward substitution
-    for (int j = tid; j < C; j += nt) {
-        for (int i = 0; i < j; ++i) sT[i * (C + 1) + j] = 0.f;
+    // T = (I + A)^{-1} (unit lower triangular) by 16 x 16 blocks: each diagonal block by forward
+    // substitution (thread = column), then the block rows r in order,
+    //     T_rs = -T_rr X_rs,   X_rs = sum_{s <= l < r} A_rl T_ls   (blocks s < r)
+    if (tid < C) {
+        const int j = tid, top = j & ~15;
         sT[j * (C + 1) + j] = 1.f;
-        for (int i = j + 1; i < C; ++i) {
+        for (int i = j + 1; i < top + 16; ++i) {
             float acc = 0.f;
             for (int l = j; l < i; ++l) acc = fmaf(sA[i * (C + 1) + l], sT[l * (C + 1) + j], acc);
             sT[i * (C + 1) + j] = -acc;
@@ -111,13 +127,29 @@ __global__ void __launch_bounds__(256) factors_simt_kernel(const Tin* __restrict
         if (imajor) i = p / dk, c = p - i * dk;
         else c = p / C, i = p - c * C;
         const float Gi = sG[i * LD + c];
-        u[L.off_qbt() + p] = sQ[i * LDQ + c] * expf(Gi);
-        u[L.off_kht() + p] = sK[i * LD + c] * expf(sG[(C - 1) * LD + c] - Gi);
+        u[L.off_qbt() + p] = sQ[i * LDQ + c] * __expf(Gi);
+        u[L.off_kht() + p] = sK[i * LD + c] * __expf(sG[(C - 1) * LD + c] - Gi);
     }
     __syncthreads();
+    for (int r = 16; r < C; r += 16) {
+        for (int p = tid; p < 16 * r; p += nt) {  // X: rows r .. r+15, columns 0 .. r-1
+            const int ii = p / r, jj = p - ii * r;
+            float acc = 0.f;
+            for (int l = jj; l < r; ++l) acc = fmaf(sA[(r + ii) * (C + 1) + l], sT[l * (C + 1) + jj], acc);
+            sX[p] = acc;
+        }
+        __syncthreads();
+        for (int p = tid; p < 16 * r; p += nt) {
+            const int ii = p / r, jj = p - ii * r;
+            float acc = 0.f;
+            for (int m2 = 0; m2 <= ii; ++m2) acc = fmaf(sT[(r + ii) * (C + 1) + r + m2], sX[m2 * r + jj], acc);
+            sT[(r + ii) * (C + 1) + jj] = -acc;
+        }
+        __syncthreads();
+    }
     for (int idx = tid; idx < C * dk; idx += nt) {
         const int t = idx / dk, c = idx - t * dk;
-        sBK[t * LD + c] *= expf(sG[t * LD + c]);
+        sBK[t * LD + c] *= __expf(sG[t * LD + c]);
     }
     for (int idx = tid; idx < C * dv; idx += nt) {
         const int t = idx / dv, c = idx - t * dv;
@@ -240,18 +272,29 @@ size_t state_smem(int dk, int C) {
                             2 * (size_t)C * kSlice);
 }
 
-template <typename Tin>
-cudaError_t launch_factors_t(const void* q, const void* k, const void* v, const void* g, const void* b, const void* w,
-                             const ChunkShape& sh, void* ws, float* t_out, int imajor, cudaStream_t s) {
+template <typename Tin, int kDK, int kDV, int kC>
+cudaError_t launch_factors_shape(const void* q, const void* k, const void* v, const void* g, const void* b,
+                                 const void* w, const ChunkShape& sh, void* ws, float* t_out, int imajor,
+                                 cudaStream_t s) {
     const size_t f_smem = factors_smem(sh.dk, sh.dv, sh.C);
-    cudaError_t e = cudaFuncSetAttribute(factors_simt_kernel<Tin>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)f_smem);
+    cudaError_t e = cudaFuncSetAttribute(factors_simt_kernel<Tin, kDK, kDV, kC>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)f_smem);
     if (e != cudaSuccess) return e;
-    factors_simt_kernel<Tin><<<dim3(sh.nchunks(), sh.B * sh.Hv), 256, f_smem, s>>>(
+    factors_simt_kernel<Tin, kDK, kDV, kC><<<dim3(sh.nchunks(), sh.B * sh.Hv), 256, f_smem, s>>>(
         static_cast<const Tin*>(q), static_cast<const Tin*>(k), static_cast<const Tin*>(v),
         static_cast<const Tin*>(g), static_cast<const Tin*>(b), static_cast<const Tin*>(w), static_cast<float*>(ws),
         t_out, sh.T, sh.Hk, sh.Hv, sh.dk, sh.dv, sh.C, imajor);
     return cudaGetLastError();
+}
+
+template <typename Tin>
+cudaError_t launch_factors_t(const void* q, const void* k, const void* v, const void* g, const void* b, const void* w,
+                             const ChunkShape& sh, void* ws, float* t_out, int imajor, cudaStream_t s) {
+    if (sh.dk == 128 && sh.dv == 128 && sh.C == 32)
+        return launch_factors_shape<Tin, 128, 128, 32>(q, k, v, g, b, w, sh, ws, t_out, imajor, s);
+    if (sh.dk == 128 && sh.dv == 128 && sh.C == 64)
+        return launch_factors_shape<Tin, 128, 128, 64>(q, k, v, g, b, w, sh, ws, t_out, imajor, s);
+    return launch_factors_shape<Tin, 0, 0, 0>(q, k, v, g, b, w, sh, ws, t_out, imajor, s);
 }
 
 template <typename Tin>
