@@ -378,7 +378,7 @@ def next_rows_rooflines(g, device, hbm, wl):
         res[name] = {"kernel": kernel, "ms": round(ms, 4), "algorithmic_bytes": int(nbytes),
                      "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s", "frac": round(gbs / hbm, 4),
                      "bound": "hbm"}
-    # backward (recurrent form, fp32 SIMT): bound by fp32 arithmetic on the 2*B*H_v SMs it occupies
+    # backward (chunked WY form in fp32 on CUDA cores, 32-token chunks): bound by fp32 arithmetic
     tk = [rnd(B, T, Hk, d), rnd(B, T, Hk, d)]
     tk[0] = (tk[0].float() / tk[0].float().norm(dim=-1, keepdim=True)).to(bf)
     tk[1] = (tk[1].float() / tk[1].float().norm(dim=-1, keepdim=True)).to(bf)
@@ -403,10 +403,12 @@ def next_rows_rooflines(g, device, hbm, wl):
     sms = torch.cuda.get_device_properties(device).multi_processor_count
     peak_tf = sms * 128 * 2 * 2.07e9 / 1e12          # fp32 lanes x FMA x max SM clock
     ach = flops / (ms * 1e-3) / 1e12
-    res["backward"] = {"kernel": "gdn2_backward (backward_kernel + combine_kernel)", "ms": round(ms, 3),
+    res["backward"] = {"kernel": "gdn2_backward (factors_simt_kernel + save_chain_kernel + adjoint_kernel + "
+                                 "grad_kernel + group_sum2_kernel)", "ms": round(ms, 3),
                        "algorithmic_flops": int(flops), "achieved": round(ach, 2), "peak": round(peak_tf, 1),
                        "unit": "TFLOP/s", "frac": round(ach / peak_tf, 4), "bound": "alu",
-                       "note": f"two CTAs per (batch, value head), 64 d_v columns each: {min(2 * B * Hv, sms)} of {sms} SMs busy"}
+                       "note": (f"factors and per-chunk gradients: one CTA per (chunk, head); the two chains over "
+                                f"chunks: two CTAs per (batch, value head), {min(2 * B * Hv, sms)} of {sms} SMs")}
     res["shape"] = f"B={B} T={T} H_k={Hk} H_v={Hv} d={d} bf16 (the bench workload's token tensors)"
     return res
 
