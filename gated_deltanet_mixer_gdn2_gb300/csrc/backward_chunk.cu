@@ -35,7 +35,7 @@ constexpr int kCT = 512;        // threads of a chain CTA
 constexpr int kSl = 64;         // d_v columns per chain CTA
 constexpr int kLJ = kSl + 4;    // padded row of [*][64] slices
 constexpr int kLW = kD + 4;     // padded row of [32][128] factor rows
-constexpr int kLM = kCb + 4;    // padded row of [32][32]
+constexpr int kLM = kCb + 4;    // padded row of [*][32] arrays (channel-major factors, M)
 
 __device__ __forceinline__ float4 lds4(const float* p) { return *reinterpret_cast<const float4*>(p); }
 __device__ __forceinline__ void sts4(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
@@ -94,69 +94,77 @@ __device__ __forceinline__ void st4_tok(Tin* p, float4 x) {
     }
 }
 
-// Thread roles shared by both chains.
-//  Rows-of-C products (out [32][64], contraction over d_k = 128): thread = 4 x 4 tile (iq, jq) and one
-//  quarter kq of the contraction (c = 16m + 4kq + 0..3); the quarters are added by a butterfly over the
-//  four lanes of a tile that leaves row 4iq + kq in lane kq.
-//  State products (out [128][64], contraction over the 32 tokens): thread = 4 x 4 tile (cq, jq), which
-//  is also the register-resident part of the state it owns.
+// Thread roles shared by both chains (16 warps). A shared load that every lane of a half-warp makes
+// from one address costs half the wavefronts per value of one whose address differs per lane, so each
+// product takes 8 values of one operand from half-warp-uniform addresses and 4 of the other per lane:
+//  state products (out [128][64] += sum over the 32 tokens): warp w takes channels 8w .. 8w+7, lane
+//    (kh = lane >> 4, jl = lane & 15) columns 4jl .. 4jl+3 over the tokens of parity kh; one exchange
+//    adds the two parities and leaves rows 8w + 4kh .. +3 with the lane: its part of the state;
+//  rows products (out [32][64], contraction over d_k): tokens 8(w & 3) .. +7, columns 4jl .. +3, d_k
+//    slice ks = 2(w >> 2) + kh of 16 channels; one exchange adds the two slices of a warp, shared
+//    memory the four warp groups (in a fixed order).
 struct ChainRoles {
-    int kq, iq, jq1;  // rows-of-C tile
-    int cq, jq2;      // state tile
-    __device__ ChainRoles(int tid) {
-        const int warp = tid >> 5, lane = tid & 31, tl = lane >> 2;
-        kq = lane & 3;
-        iq = 2 * (warp & 3) + (tl & 1);
-        jq1 = 4 * (warp >> 2) + (tl >> 1);
-        cq = 8 * (warp & 3) + (lane & 7);
-        jq2 = 4 * (warp >> 2) + (lane >> 3);
+    int w, kh, jl, iset, ks;
+    __device__ explicit ChainRoles(int tid) {
+        w = tid >> 5;
+        kh = (tid >> 4) & 1;
+        jl = tid & 15;
+        iset = w & 3;
+        ks = 2 * (w >> 2) + kh;
     }
 };
 
-// a[ii][jj] summed over the four lanes kq of a tile; returns row kq
-__device__ __forceinline__ float4 quarter_sum(float (&a)[4][4], int kq) {
-    const bool hi = kq & 2;
-    float keep[2][4];
+// a (8 rows x 4 columns) plus the other half-warp's a; rows 4kh .. 4kh+3 of the sum land in b
+__device__ __forceinline__ void half_sum(const float (&a)[8][4], int kh, float (&b)[4][4]) {
 #pragma unroll
-    for (int r = 0; r < 2; ++r)
+    for (int r = 0; r < 4; ++r)
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj) {
-            const float mine_lo = a[r][jj], mine_hi = a[2 + r][jj];
-            const float send = hi ? mine_lo : mine_hi;
-            keep[r][jj] = (hi ? mine_hi : mine_lo) + __shfl_xor_sync(0xffffffffu, send, 2);
+            const float lo = a[r][jj], hi = a[4 + r][jj];
+            b[r][jj] = (kh ? hi : lo) + __shfl_xor_sync(0xffffffffu, kh ? lo : hi, 16);
         }
-    const bool odd = kq & 1;
-    float out[4];
+}
+
+// a[r][jj] += x[r] * y[jj] for 8 x values given as two float4
+__device__ __forceinline__ void outer8x4(float (&a)[8][4], float4 x0, float4 x1, float4 y) {
+    const float xs[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
 #pragma unroll
-    for (int jj = 0; jj < 4; ++jj) {
-        const float send = odd ? keep[0][jj] : keep[1][jj];
-        out[jj] = (odd ? keep[1][jj] : keep[0][jj]) + __shfl_xor_sync(0xffffffffu, send, 1);
+    for (int r = 0; r < 8; ++r) {
+        a[r][0] = fmaf(xs[r], y.x, a[r][0]);
+        a[r][1] = fmaf(xs[r], y.y, a[r][1]);
+        a[r][2] = fmaf(xs[r], y.z, a[r][2]);
+        a[r][3] = fmaf(xs[r], y.w, a[r][3]);
     }
-    return make_float4(out[0], out[1], out[2], out[3]);
 }
 
 namespace fc {  // shared-memory map of save_chain_kernel (floats)
 constexpr int S = 0;                          // S_n [128][kLJ]
 constexpr int U = S + kD * kLJ;               // U [32][kLJ]
-constexpr int BUF = U + kCb * kLJ;            // two factor buffers
-constexpr int W = 0, KH = W + kCb * kLW, UT = KH + kCb * kLW, GAM = UT + kCb * kLJ, BUF_FLOATS = GAM + kD;
+constexpr int RED = U + kCb * kLJ;            // [4][32][64] partial rows products of the warp groups
+constexpr int BUF = RED + 4 * kCb * kSl;      // two factor buffers
+constexpr int WT = 0, KH = WT + kD * kLM, UT = KH + kCb * kLW, GAM = UT + kCb * kLJ, BUF_FLOATS = GAM + kD;
 constexpr int TOTAL = BUF + 2 * BUF_FLOATS;
 }  // namespace fc
 
-// Forward chain keeping, for every chunk n, S_n (the state entering it) and U_n = U~_n - W_n S_n; with
-// the token-major factors of factors_simt_kernel:  S_{n+1} = diag(e^{G_last}) S_n + K^_n^T U_n.
+// Forward chain keeping, for every chunk n, S_n (the state entering it) and U_n = U~_n - W_n S_n:
+//     S_{n+1} = diag(e^{G_last}) S_n + K^_n^T U_n.
 __global__ void __launch_bounds__(kCT, 1) save_chain_kernel(const float* __restrict__ ws, const float* __restrict__ s0,
                                                            float* __restrict__ s_save, float* __restrict__ u_save,
                                                            int NC) {
     extern __shared__ __align__(16) float sm[];
     const int bh = blockIdx.x, col0 = blockIdx.y * kSl, tid = threadIdx.x;
-    const SimtWs L{kD, kD, kCb};
+    const SimtWs L{kD, kD, kCb, true};
     const ChainRoles R(tid);
+    const int c_own = 8 * R.w + 4 * R.kh;  // first of the lane's four state rows
     auto prefetch = [&](int n, float* buf) {
         const float* u = ws + ((size_t)bh * NC + n) * L.unit_floats();
-        for (int i = tid; i < 2 * kCb * (kD / 4); i += kCT) {  // W, K^ rows
-            const int m = i >> 10, r = (i >> 5) & (kCb - 1), c4 = 4 * (i & 31);
-            cp_async16(buf + (m ? fc::KH : fc::W) + r * kLW + c4, u + (m ? L.off_kht() : L.off_wt()) + r * kD + c4);
+        for (int i = tid; i < kD * (kCb / 4); i += kCT) {  // W^T [d_k][C]
+            const int r = i >> 3, c4 = 4 * (i & 7);
+            cp_async16(buf + fc::WT + r * kLM + c4, u + L.off_wt2() + r * kCb + c4);
+        }
+        for (int i = tid; i < kCb * (kD / 4); i += kCT) {  // K^ [C][d_k]
+            const int r = i >> 5, c4 = 4 * (i & 31);
+            cp_async16(buf + fc::KH + r * kLW + c4, u + L.off_kht() + r * kD + c4);
         }
         {   // this CTA's columns of U~, and e^{G_last}
             const int r = tid >> 4, c4 = 4 * (tid & 15);
@@ -165,79 +173,73 @@ __global__ void __launch_bounds__(kCT, 1) save_chain_kernel(const float* __restr
         if (tid < kD / 4) cp_async16(buf + fc::GAM + 4 * tid, u + L.off_gam() + 4 * tid);
         cp_async_commit();
     };
-    float S[4][4];  // rows 4cq + r, columns 4jq2 + jj of this CTA's slice
+    float S[4][4];  // rows c_own + r, columns 4jl + jj of this CTA's slice
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
-        const float4 x = s0 ? *reinterpret_cast<const float4*>(s0 + ((size_t)bh * kD + 4 * R.cq + r) * kD + col0 + 4 * R.jq2)
+        const float4 x = s0 ? *reinterpret_cast<const float4*>(s0 + ((size_t)bh * kD + c_own + r) * kD + col0 + 4 * R.jl)
                             : make_float4(0.f, 0.f, 0.f, 0.f);
         S[r][0] = x.x; S[r][1] = x.y; S[r][2] = x.z; S[r][3] = x.w;
-        sts4(sm + fc::S + (4 * R.cq + r) * kLJ + 4 * R.jq2, x);
+        sts4(sm + fc::S + (c_own + r) * kLJ + 4 * R.jl, x);
     }
     prefetch(0, sm + fc::BUF);
     cp_async_wait_all();
     __syncthreads();
+    const int fi = tid >> 4, fj = 4 * (tid & 15);  // the (row, column quad) each thread finishes
     for (int n = 0; n < NC; ++n) {
         const float* buf = sm + fc::BUF + (n & 1) * fc::BUF_FLOATS;
         const size_t unit = (size_t)bh * NC + n;
 #pragma unroll
         for (int r = 0; r < 4; ++r)  // S_n
-            *reinterpret_cast<float4*>(s_save + (unit * kD + 4 * R.cq + r) * kD + col0 + 4 * R.jq2) =
+            *reinterpret_cast<float4*>(s_save + (unit * kD + c_own + r) * kD + col0 + 4 * R.jl) =
                 make_float4(S[r][0], S[r][1], S[r][2], S[r][3]);
         if (n + 1 < NC) prefetch(n + 1, sm + fc::BUF + ((n + 1) & 1) * fc::BUF_FLOATS);
-        // U = U~ - W S_n (contraction over d_k)
-        {
-            float a[4][4];
-#pragma unroll
-            for (int ii = 0; ii < 4; ++ii)
-#pragma unroll
-                for (int jj = 0; jj < 4; ++jj) a[ii][jj] = 0.f;
+        {   // W S_n over this lane's 16 channels
+            float a[8][4] = {};
 #pragma unroll 4
-            for (int m = 0; m < 8; ++m) {
-                const int c0 = 16 * m + 4 * R.kq;
-                float4 wv[4], sv[4];
-#pragma unroll
-                for (int ii = 0; ii < 4; ++ii) wv[ii] = lds4(buf + fc::W + (4 * R.iq + ii) * kLW + c0);
-#pragma unroll
-                for (int cc = 0; cc < 4; ++cc) sv[cc] = lds4(sm + fc::S + (c0 + cc) * kLJ + 4 * R.jq1);
-#pragma unroll
-                for (int ii = 0; ii < 4; ++ii) {
-                    a[ii][0] = fmaf(wv[ii].x, sv[0].x, fmaf(wv[ii].y, sv[1].x, fmaf(wv[ii].z, sv[2].x, fmaf(wv[ii].w, sv[3].x, a[ii][0]))));
-                    a[ii][1] = fmaf(wv[ii].x, sv[0].y, fmaf(wv[ii].y, sv[1].y, fmaf(wv[ii].z, sv[2].y, fmaf(wv[ii].w, sv[3].y, a[ii][1]))));
-                    a[ii][2] = fmaf(wv[ii].x, sv[0].z, fmaf(wv[ii].y, sv[1].z, fmaf(wv[ii].z, sv[2].z, fmaf(wv[ii].w, sv[3].z, a[ii][2]))));
-                    a[ii][3] = fmaf(wv[ii].x, sv[0].w, fmaf(wv[ii].y, sv[1].w, fmaf(wv[ii].z, sv[2].w, fmaf(wv[ii].w, sv[3].w, a[ii][3]))));
-                }
+            for (int cc = 0; cc < 16; ++cc) {
+                const int c = 16 * R.ks + cc;
+                const float* wt = buf + fc::WT + c * kLM + 8 * R.iset;
+                outer8x4(a, lds4(wt), lds4(wt + 4), lds4(sm + fc::S + c * kLJ + 4 * R.jl));
             }
-            const float4 ws4 = quarter_sum(a, R.kq);
-            const int i = 4 * R.iq + R.kq;
-            const float4 ut = lds4(buf + fc::UT + i * kLJ + 4 * R.jq1);
-            const float4 uu = make_float4(ut.x - ws4.x, ut.y - ws4.y, ut.z - ws4.z, ut.w - ws4.w);
-            sts4(sm + fc::U + i * kLJ + 4 * R.jq1, uu);
-            *reinterpret_cast<float4*>(u_save + (unit * kCb + i) * kD + col0 + 4 * R.jq1) = uu;
+            float b[4][4];
+            half_sum(a, R.kh, b);
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+                sts4(sm + fc::RED + ((R.w >> 2) * kCb + 8 * R.iset + 4 * R.kh + r) * kSl + 4 * R.jl,
+                     make_float4(b[r][0], b[r][1], b[r][2], b[r][3]));
         }
         __syncthreads();
-        // S_{n+1} = diag(e^{G_last}) S_n + K^^T U (contraction over the chunk's tokens)
-        {
-            const float4 gm = lds4(buf + fc::GAM + 4 * R.cq);
+        {   // U = U~ - W S_n
+            float4 t = lds4(sm + fc::RED + fi * kSl + fj);
 #pragma unroll
-            for (int r = 0; r < 4; ++r)
-#pragma unroll
-                for (int jj = 0; jj < 4; ++jj) S[r][jj] *= comp(gm, r);
-#pragma unroll 4
-            for (int i = 0; i < kCb; ++i) {
-                const float4 kv = lds4(buf + fc::KH + i * kLW + 4 * R.cq);
-                const float4 uv = lds4(sm + fc::U + i * kLJ + 4 * R.jq2);
-#pragma unroll
-                for (int r = 0; r < 4; ++r) {
-                    const float kr = comp(kv, r);
-                    S[r][0] = fmaf(kr, uv.x, S[r][0]);
-                    S[r][1] = fmaf(kr, uv.y, S[r][1]);
-                    S[r][2] = fmaf(kr, uv.z, S[r][2]);
-                    S[r][3] = fmaf(kr, uv.w, S[r][3]);
-                }
+            for (int g2 = 1; g2 < 4; ++g2) {
+                const float4 x = lds4(sm + fc::RED + (g2 * kCb + fi) * kSl + fj);
+                t.x += x.x; t.y += x.y; t.z += x.z; t.w += x.w;
             }
+            const float4 ut = lds4(buf + fc::UT + fi * kLJ + fj);
+            const float4 uu = make_float4(ut.x - t.x, ut.y - t.y, ut.z - t.z, ut.w - t.w);
+            sts4(sm + fc::U + fi * kLJ + fj, uu);
+            *reinterpret_cast<float4*>(u_save + (unit * kCb + fi) * kD + col0 + fj) = uu;
+        }
+        __syncthreads();
+        {   // S_{n+1} = diag(e^{G_last}) S_n + K^^T U
+            float a[8][4] = {};
+#pragma unroll 4
+            for (int m = 0; m < kCb / 2; ++m) {
+                const int i = 2 * m + R.kh;
+                const float* kh = buf + fc::KH + i * kLW + 8 * R.w;
+                outer8x4(a, lds4(kh), lds4(kh + 4), lds4(sm + fc::U + i * kLJ + 4 * R.jl));
+            }
+            float b[4][4];
+            half_sum(a, R.kh, b);
+            const float4 gm = lds4(buf + fc::GAM + c_own);
 #pragma unroll
-            for (int r = 0; r < 4; ++r)
-                sts4(sm + fc::S + (4 * R.cq + r) * kLJ + 4 * R.jq2, make_float4(S[r][0], S[r][1], S[r][2], S[r][3]));
+            for (int r = 0; r < 4; ++r) {
+                const float gr = comp(gm, r);
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) S[r][jj] = fmaf(gr, S[r][jj], b[r][jj]);
+                sts4(sm + fc::S + (c_own + r) * kLJ + 4 * R.jl, make_float4(S[r][0], S[r][1], S[r][2], S[r][3]));
+            }
         }
         cp_async_wait_all();
         __syncthreads();
@@ -247,8 +249,9 @@ __global__ void __launch_bounds__(kCT, 1) save_chain_kernel(const float* __restr
 namespace ac {  // shared-memory map of adjoint_kernel (floats)
 constexpr int R = 0;                          // dS_{n+1} [128][kLJ]
 constexpr int DU = R + kD * kLJ;              // dU [32][kLJ]
-constexpr int BUF = DU + kCb * kLJ;           // two buffers of factors and dO rows
-constexpr int KH = 0, QB = KH + kCb * kLW, W = QB + kCb * kLW, M = W + kCb * kLW, GAM = M + kCb * kLM,
+constexpr int RED = DU + kCb * kLJ;           // [4][32][64] partial rows products of the warp groups
+constexpr int BUF = RED + 4 * kCb * kSl;      // two buffers of factors and dO rows
+constexpr int KHT = 0, QB = KHT + kD * kLM, W = QB + kCb * kLW, M = W + kCb * kLW, GAM = M + kCb * kLM,
               DO = GAM + kD, BUF_FLOATS = DO + kCb * kLJ;   // dO rows: 272 bytes each whatever the dtype
 constexpr int TOTAL = BUF + 2 * BUF_FLOATS;
 }  // namespace ac
@@ -263,16 +266,20 @@ __global__ void __launch_bounds__(kCT, 1) adjoint_kernel(const float* __restrict
                                                         int T, int Hv, int NC, float scale) {
     extern __shared__ __align__(16) float sm[];
     const int bh = blockIdx.x, bi = bh / Hv, hv = bh - bi * Hv, col0 = blockIdx.y * kSl, tid = threadIdx.x;
-    const SimtWs L{kD, kD, kCb};
+    const SimtWs L{kD, kD, kCb, true};
     const ChainRoles R(tid);
+    const int c_own = 8 * R.w + 4 * R.kh;
     constexpr int kPieces = kSl * (int)sizeof(Tin) / 16;  // 16-byte pieces of one dO row slice
+    constexpr int kRowT = kLJ * 4 / (int)sizeof(Tin);      // dO row stride in elements
     auto prefetch = [&](int n, float* buf) {
         const float* u = ws + ((size_t)bh * NC + n) * L.unit_floats();
-        for (int i = tid; i < 3 * kCb * (kD / 4); i += kCT) {  // K^, Q_bar, W rows
+        for (int i = tid; i < kD * (kCb / 4); i += kCT) {  // K^^T [d_k][C]
+            const int r = i >> 3, c4 = 4 * (i & 7);
+            cp_async16(buf + ac::KHT + r * kLM + c4, u + L.off_kht2() + r * kCb + c4);
+        }
+        for (int i = tid; i < 2 * kCb * (kD / 4); i += kCT) {  // Q_bar, W [C][d_k]
             const int m = i >> 10, r = (i >> 5) & (kCb - 1), c4 = 4 * (i & 31);
-            const int dst = m == 0 ? ac::KH : m == 1 ? ac::QB : ac::W;
-            const size_t src = m == 0 ? L.off_kht() : m == 1 ? L.off_qbt() : L.off_wt();
-            cp_async16(buf + dst + r * kLW + c4, u + src + r * kD + c4);
+            cp_async16(buf + (m ? ac::W : ac::QB) + r * kLW + c4, u + (m ? L.off_wt() : L.off_qbt()) + r * kD + c4);
         }
         if (tid < kCb * kCb / 4) {
             const int r = tid >> 3, c4 = 4 * (tid & 7);
@@ -289,100 +296,86 @@ __global__ void __launch_bounds__(kCT, 1) adjoint_kernel(const float* __restrict
         }
         cp_async_commit();
     };
-    float G[4][4];  // dS_{n+1}: rows 4cq + r, columns 4jq2 + jj of this CTA's slice
+    float G[4][4];  // dS_{n+1}: rows c_own + r, columns 4jl + jj of this CTA's slice
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
-        const float4 x = dsT ? *reinterpret_cast<const float4*>(dsT + ((size_t)bh * kD + 4 * R.cq + r) * kD + col0 + 4 * R.jq2)
+        const float4 x = dsT ? *reinterpret_cast<const float4*>(dsT + ((size_t)bh * kD + c_own + r) * kD + col0 + 4 * R.jl)
                              : make_float4(0.f, 0.f, 0.f, 0.f);
         G[r][0] = x.x; G[r][1] = x.y; G[r][2] = x.z; G[r][3] = x.w;
-        sts4(sm + ac::R + (4 * R.cq + r) * kLJ + 4 * R.jq2, x);
+        sts4(sm + ac::R + (c_own + r) * kLJ + 4 * R.jl, x);
     }
     prefetch(NC - 1, sm + ac::BUF + ((NC - 1) & 1) * ac::BUF_FLOATS);
     cp_async_wait_all();
     __syncthreads();
+    const int fi = tid >> 4, fj = 4 * (tid & 15);
     for (int n = NC - 1; n >= 0; --n) {
         const float* buf = sm + ac::BUF + (n & 1) * ac::BUF_FLOATS;
         const Tin* sDO = reinterpret_cast<const Tin*>(buf + ac::DO);
-        constexpr int kRowT = kLJ * 4 / (int)sizeof(Tin);  // dO row stride in elements
         const size_t unit = (size_t)bh * NC + n;
 #pragma unroll
         for (int r = 0; r < 4; ++r)  // dS_{n+1}
-            *reinterpret_cast<float4*>(ds_save + (unit * kD + 4 * R.cq + r) * kD + col0 + 4 * R.jq2) =
+            *reinterpret_cast<float4*>(ds_save + (unit * kD + c_own + r) * kD + col0 + 4 * R.jl) =
                 make_float4(G[r][0], G[r][1], G[r][2], G[r][3]);
         if (n > 0) prefetch(n - 1, sm + ac::BUF + ((n - 1) & 1) * ac::BUF_FLOATS);
-        // dU = M^T dO~ + K^ dS_{n+1}
-        {
-            float a[4][4], am[4][4];
-#pragma unroll
-            for (int ii = 0; ii < 4; ++ii)
-#pragma unroll
-                for (int jj = 0; jj < 4; ++jj) a[ii][jj] = am[ii][jj] = 0.f;
+        {   // K^ dS_{n+1} over this lane's 16 channels, M^T dO~ over its 4 tokens
+            float a[8][4] = {};
 #pragma unroll 4
-            for (int m = 0; m < 8; ++m) {
-                const int c0 = 16 * m + 4 * R.kq;
-                float4 kv[4], rv[4];
-#pragma unroll
-                for (int ii = 0; ii < 4; ++ii) kv[ii] = lds4(buf + ac::KH + (4 * R.iq + ii) * kLW + c0);
-#pragma unroll
-                for (int cc = 0; cc < 4; ++cc) rv[cc] = lds4(sm + ac::R + (c0 + cc) * kLJ + 4 * R.jq1);
-#pragma unroll
-                for (int ii = 0; ii < 4; ++ii) {
-                    a[ii][0] = fmaf(kv[ii].x, rv[0].x, fmaf(kv[ii].y, rv[1].x, fmaf(kv[ii].z, rv[2].x, fmaf(kv[ii].w, rv[3].x, a[ii][0]))));
-                    a[ii][1] = fmaf(kv[ii].x, rv[0].y, fmaf(kv[ii].y, rv[1].y, fmaf(kv[ii].z, rv[2].y, fmaf(kv[ii].w, rv[3].y, a[ii][1]))));
-                    a[ii][2] = fmaf(kv[ii].x, rv[0].z, fmaf(kv[ii].y, rv[1].z, fmaf(kv[ii].z, rv[2].z, fmaf(kv[ii].w, rv[3].z, a[ii][2]))));
-                    a[ii][3] = fmaf(kv[ii].x, rv[0].w, fmaf(kv[ii].y, rv[1].w, fmaf(kv[ii].z, rv[2].w, fmaf(kv[ii].w, rv[3].w, a[ii][3]))));
-                }
+            for (int cc = 0; cc < 16; ++cc) {
+                const int c = 16 * R.ks + cc;
+                const float* kt = buf + ac::KHT + c * kLM + 8 * R.iset;
+                outer8x4(a, lds4(kt), lds4(kt + 4), lds4(sm + ac::R + c * kLJ + 4 * R.jl));
             }
 #pragma unroll
-            for (int m = 0; m < 8; ++m) {  // tokens l = 4m + kq; M[l][i] = 0 for l < i
-                const int l = 4 * m + R.kq;
-                const float4 mv = lds4(buf + ac::M + l * kLM + 4 * R.iq);
-                const float4 ov = ld4_tok(sDO + l * kRowT + 4 * R.jq1);
-#pragma unroll
-                for (int ii = 0; ii < 4; ++ii) {
-                    const float mi = comp(mv, ii);
-                    am[ii][0] = fmaf(mi, ov.x, am[ii][0]);
-                    am[ii][1] = fmaf(mi, ov.y, am[ii][1]);
-                    am[ii][2] = fmaf(mi, ov.z, am[ii][2]);
-                    am[ii][3] = fmaf(mi, ov.w, am[ii][3]);
-                }
+            for (int ll = 0; ll < 4; ++ll) {  // M[l][i] = 0 for l < i
+                const int l = 4 * R.ks + ll;
+                const float* mr = buf + ac::M + l * kLM + 8 * R.iset;
+                float4 ov = ld4_tok(sDO + l * kRowT + 4 * R.jl);
+                ov = make_float4(scale * ov.x, scale * ov.y, scale * ov.z, scale * ov.w);
+                outer8x4(a, lds4(mr), lds4(mr + 4), ov);
             }
+            float b[4][4];
+            half_sum(a, R.kh, b);
 #pragma unroll
-            for (int ii = 0; ii < 4; ++ii)
-#pragma unroll
-                for (int jj = 0; jj < 4; ++jj) a[ii][jj] = fmaf(scale, am[ii][jj], a[ii][jj]);
-            const float4 du = quarter_sum(a, R.kq);
-            const int i = 4 * R.iq + R.kq;
-            sts4(sm + ac::DU + i * kLJ + 4 * R.jq1, du);
-            *reinterpret_cast<float4*>(du_save + (unit * kCb + i) * kD + col0 + 4 * R.jq1) = du;
+            for (int r = 0; r < 4; ++r)
+                sts4(sm + ac::RED + ((R.w >> 2) * kCb + 8 * R.iset + 4 * R.kh + r) * kSl + 4 * R.jl,
+                     make_float4(b[r][0], b[r][1], b[r][2], b[r][3]));
         }
         __syncthreads();
-        // dS_n = diag(e^{G_last}) dS_{n+1} + Q_bar^T dO~ - W^T dU
-        {
-            const float4 gm = lds4(buf + ac::GAM + 4 * R.cq);
+        {   // dU
+            float4 t = lds4(sm + ac::RED + fi * kSl + fj);
 #pragma unroll
-            for (int r = 0; r < 4; ++r)
-#pragma unroll
-                for (int jj = 0; jj < 4; ++jj) G[r][jj] *= comp(gm, r);
-#pragma unroll 4
-            for (int i = 0; i < kCb; ++i) {
-                const float4 qv = lds4(buf + ac::QB + i * kLW + 4 * R.cq);
-                const float4 wv = lds4(buf + ac::W + i * kLW + 4 * R.cq);
-                float4 ov = ld4_tok(sDO + i * kRowT + 4 * R.jq2);
-                ov = make_float4(scale * ov.x, scale * ov.y, scale * ov.z, scale * ov.w);
-                const float4 dv = lds4(sm + ac::DU + i * kLJ + 4 * R.jq2);
-#pragma unroll
-                for (int r = 0; r < 4; ++r) {
-                    const float qr = comp(qv, r), wr = -comp(wv, r);
-                    G[r][0] = fmaf(qr, ov.x, fmaf(wr, dv.x, G[r][0]));
-                    G[r][1] = fmaf(qr, ov.y, fmaf(wr, dv.y, G[r][1]));
-                    G[r][2] = fmaf(qr, ov.z, fmaf(wr, dv.z, G[r][2]));
-                    G[r][3] = fmaf(qr, ov.w, fmaf(wr, dv.w, G[r][3]));
-                }
+            for (int g2 = 1; g2 < 4; ++g2) {
+                const float4 x = lds4(sm + ac::RED + (g2 * kCb + fi) * kSl + fj);
+                t.x += x.x; t.y += x.y; t.z += x.z; t.w += x.w;
             }
+            sts4(sm + ac::DU + fi * kLJ + fj, t);
+            *reinterpret_cast<float4*>(du_save + (unit * kCb + fi) * kD + col0 + fj) = t;
+        }
+        __syncthreads();
+        {   // dS_n = diag(e^{G_last}) dS_{n+1} + Q_bar^T dO~ - W^T dU
+            float a[8][4] = {};
+#pragma unroll 2
+            for (int m = 0; m < kCb / 2; ++m) {
+                const int i = 2 * m + R.kh;
+                const float* qb = buf + ac::QB + i * kLW + 8 * R.w;
+                const float* wr = buf + ac::W + i * kLW + 8 * R.w;
+                float4 ov = ld4_tok(sDO + i * kRowT + 4 * R.jl);
+                ov = make_float4(scale * ov.x, scale * ov.y, scale * ov.z, scale * ov.w);
+                float4 dv = lds4(sm + ac::DU + i * kLJ + 4 * R.jl);
+                dv = make_float4(-dv.x, -dv.y, -dv.z, -dv.w);
+                outer8x4(a, lds4(qb), lds4(qb + 4), ov);
+                outer8x4(a, lds4(wr), lds4(wr + 4), dv);
+            }
+            float b[4][4];
+            half_sum(a, R.kh, b);
+            const float4 gm = lds4(buf + ac::GAM + c_own);
 #pragma unroll
-            for (int r = 0; r < 4; ++r)
-                sts4(sm + ac::R + (4 * R.cq + r) * kLJ + 4 * R.jq2, make_float4(G[r][0], G[r][1], G[r][2], G[r][3]));
+            for (int r = 0; r < 4; ++r) {
+                const float gr = comp(gm, r);
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) G[r][jj] = fmaf(gr, G[r][jj], b[r][jj]);
+                sts4(sm + ac::R + (c_own + r) * kLJ + 4 * R.jl, make_float4(G[r][0], G[r][1], G[r][2], G[r][3]));
+            }
         }
         cp_async_wait_all();
         __syncthreads();
@@ -390,7 +383,7 @@ __global__ void __launch_bounds__(kCT, 1) adjoint_kernel(const float* __restrict
     if (ds0)
 #pragma unroll
         for (int r = 0; r < 4; ++r)
-            *reinterpret_cast<float4*>(ds0 + ((size_t)bh * kD + 4 * R.cq + r) * kD + col0 + 4 * R.jq2) =
+            *reinterpret_cast<float4*>(ds0 + ((size_t)bh * kD + c_own + r) * kD + col0 + 4 * R.jl) =
                 make_float4(G[r][0], G[r][1], G[r][2], G[r][3]);
 }
 
@@ -875,7 +868,7 @@ ChunkBwdLayout chunk_bwd_layout(int B, int T, int Hv) {
     const size_t units = (size_t)sh.nchunks() * B * Hv, tok = (size_t)B * T * Hv * kD * 4;
     ChunkBwdLayout L;
     L.simt = 0;
-    L.t = align_up(chunk_simt_workspace_bytes(sh), 256);
+    L.t = align_up(chunk_simt_workspace_bytes(sh, /*token_major=*/true), 256);
     L.s = align_up(L.t + units * kCb * kCb * 4, 256);
     L.u = align_up(L.s + units * kD * kD * 4, 256);
     L.ds = align_up(L.u + units * kCb * kD * 4, 256);

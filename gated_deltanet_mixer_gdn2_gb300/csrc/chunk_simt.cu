@@ -51,7 +51,7 @@ __global__ void __launch_bounds__(256) factors_simt_kernel(const Tin* __restrict
     float* sT = sA + C * (C + 1);            // [C][C+1]
     float* sX = sQ;                          // [16][C] block products of the inverse (q is read out by then)
 
-    const SimtWs L{dk, dv, C};
+    const SimtWs L{dk, dv, C, imajor != 0};
     float* u = ws + ((size_t)bh * NC + n) * L.unit_floats();
 
     for (int idx = tid; idx < C * dk; idx += nt) {
@@ -130,6 +130,11 @@ __global__ void __launch_bounds__(256) factors_simt_kernel(const Tin* __restrict
         u[L.off_qbt() + p] = sQ[i * LDQ + c] * __expf(Gi);
         u[L.off_kht() + p] = sK[i * LD + c] * __expf(sG[(C - 1) * LD + c] - Gi);
     }
+    if (imajor)  // channel-major copy of k.e^{G_last-G}
+        for (int p = tid; p < dk * C; p += nt) {
+            const int c = p / C, i = p - c * C;
+            u[L.off_kht2() + p] = sK[i * LD + c] * __expf(sG[(C - 1) * LD + c] - sG[i * LD + c]);
+        }
     __syncthreads();
     for (int r = 16; r < C; r += 16) {
         for (int p = tid; p < 16 * r; p += nt) {  // X: rows r .. r+15, columns 0 .. r-1
@@ -171,6 +176,7 @@ __global__ void __launch_bounds__(256) factors_simt_kernel(const Tin* __restrict
         float acc = 0.f;
         for (int j = 0; j <= i; ++j) acc = fmaf(sT[i * (C + 1) + j], sBK[j * LD + c], acc);
         u[L.off_wt() + p] = acc;
+        if (imajor) sK[i * LD + c] = acc;  // k is read out: W for its channel-major copy
     }
     for (int p = tid; p < dv * C; p += nt) {
         int c, i;
@@ -179,6 +185,13 @@ __global__ void __launch_bounds__(256) factors_simt_kernel(const Tin* __restrict
         float acc = 0.f;
         for (int j = 0; j <= i; ++j) acc = fmaf(sT[i * (C + 1) + j], sQ[j * LDQ + c], acc);
         u[L.off_utt() + p] = acc;
+    }
+    if (imajor) {
+        __syncthreads();
+        for (int p = tid; p < dk * C; p += nt) {
+            const int c = p / C, i = p - c * C;
+            u[L.off_wt2() + p] = sK[i * LD + c];
+        }
     }
     if (t_out)  // T = (I + A)^{-1} [C][C] for the gradients
         for (int p = tid; p < C * C; p += nt) {
@@ -313,8 +326,8 @@ cudaError_t launch_t(const void* q, const void* k, const void* v, const void* g,
 
 }  // namespace
 
-size_t chunk_simt_workspace_bytes(const ChunkShape& sh) {
-    const SimtWs L{sh.dk, sh.dv, sh.C};
+size_t chunk_simt_workspace_bytes(const ChunkShape& sh, bool token_major) {
+    const SimtWs L{sh.dk, sh.dv, sh.C, token_major};
     return sizeof(float) * L.unit_floats() * (size_t)sh.nchunks() * sh.B * sh.Hv;
 }
 

@@ -106,12 +106,15 @@ cudaError_t launch_recurrent(const void* q, const void* k, const void* v, const 
 
 // Per-unit fp32 workspace of the CUDA-core chunked forward (chunk_simt.cu), also read by the chunked
 // backward (backward_chunk.cu): W, q.e^G, k.e^{G_last-G} ([d_k][C], or token-major [C][d_k]), M [C][C],
-// U~ ([d_v][C], or token-major [C][d_v]), e^{G_last} [d_k].
+// U~ ([d_v][C], or token-major [C][d_v]), e^{G_last} [d_k]; with both layouts (ext), channel-major
+// copies of W and k.e^{G_last-G} [d_k][C] follow.
 struct SimtWs {
     int dk, dv, C;
+    bool ext = false;
     __host__ __device__ size_t unit_floats() const {
         size_t n = 3 * (size_t)dk * C + (size_t)C * C + (size_t)dv * C + dk;
-        return (n + 3) & ~size_t(3);
+        n = (n + 3) & ~size_t(3);
+        return ext ? n + 2 * (size_t)dk * C : n;
     }
     __host__ __device__ size_t off_wt() const { return 0; }
     __host__ __device__ size_t off_qbt() const { return (size_t)dk * C; }
@@ -119,11 +122,14 @@ struct SimtWs {
     __host__ __device__ size_t off_m() const { return 3 * (size_t)dk * C; }
     __host__ __device__ size_t off_utt() const { return 3 * (size_t)dk * C + (size_t)C * C; }
     __host__ __device__ size_t off_gam() const { return 3 * (size_t)dk * C + (size_t)C * C + (size_t)dv * C; }
+    __host__ __device__ size_t off_wt2() const { return ((off_gam() + dk) + 3) & ~size_t(3); }
+    __host__ __device__ size_t off_kht2() const { return off_wt2() + (size_t)dk * C; }
 };
 
-size_t chunk_simt_workspace_bytes(const ChunkShape& sh);
-// The state-independent factors of every chunk into ws (layout SimtWs; token-major when token_major),
-// and, when t_out is given, T = (I + A)^{-1} per unit [C][C].
+size_t chunk_simt_workspace_bytes(const ChunkShape& sh, bool token_major = false);
+// The state-independent factors of every chunk into ws (layout SimtWs; token-major plus the
+// channel-major copies of W and k.e^{G_last-G} when token_major), and, when t_out is given,
+// T = (I + A)^{-1} per unit [C][C].
 cudaError_t launch_factors_simt(const void* q, const void* k, const void* v, const void* g, const void* b,
                                 const void* w, const ChunkShape& sh, gdn2_dtype dt, void* ws, float* t_out,
                                 bool token_major, cudaStream_t s);
