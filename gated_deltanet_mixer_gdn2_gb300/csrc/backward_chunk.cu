@@ -403,14 +403,15 @@ constexpr int TM = slot(11);                  // T [32][kLQ]
 constexpr int DT = TM + kCb * kLQ;            // dT
 constexpr int PP = DT + kCb * kLQ;            // T^T dT
 constexpr int DA = PP + kCb * kLQ, DAT = DA + kCb * kLQ, DM = DAT + kCb * kLQ, DMT = DM + kCb * kLQ;
-constexpr int DGP = DMT + kCb * kLQ;          // [4][128] partial rowsums of dS' . S
-constexpr int DGL = DGP + 4 * kD;             // [4][128] partial sums of dK^ . K^
-constexpr int TOTAL = DGL + 4 * kD;
+constexpr int DGP = DMT + kCb * kLQ;          // [128] rowsum(dS' . S)
+constexpr int DGL = DGP + kD;                 // [4][128] partial sums of dK^ . K^
+constexpr int DBT = DGL + 4 * kD;             // [4][128] sums of dG over each block of 8 tokens
+constexpr int TOTAL = DBT + 4 * kD;
 }  // namespace gk
 
 // The local gradients of one (chunk n, batch-head bh), given S_n, dS_{n+1}, U, dU and T of the chunk:
 //   1. dK^ = U dS'^T, dQ_bar = dO~ S^T, dW = -dU S^T, dgamma = rowsum(dS' . S)  (K = d_v, register tiles of
-//      2 tokens x 4 channels; S and dS' arrive in eight 16-column groups that the products consume in order)
+//      8 channels x 4 tokens; S and dS' arrive in eight 16-column groups that the products consume in order)
 //   2. dM = tril(dO~ U^T), dT = dU U0^T + dW K_bar^T, dK_bar = T^T dW, dU0 = T^T dU (-> dv, dw)
 //   3. P = T^T dT, dA = -strict_tril(P T^T)
 //   4. the pair terms X, Y (thread = channel and block of 8 tokens t) and Z + V (block of 8 tokens s), each
@@ -437,7 +438,13 @@ __global__ void __launch_bounds__(kGT, 1) grad_kernel(const Tin* __restrict__ q,
     auto krow = [&](int t) { return (((size_t)bi * T + n * kCb + t) * Hk + hk) * kD; };   // k-like token row
     const int nvalid = min(kCb, T - n * kCb);
 
-    // ---- group 0: U, dU, T and the first 16 columns of S, dS'; groups 1-7: the other columns
+    float4 do4[2];  // this thread's dO elements, in flight ahead of the copies
+#pragma unroll
+    for (int pass = 0; pass < 2; ++pass) {
+        const int t = (tid >> 5) + 16 * pass;
+        do4[pass] = t < nvalid ? ld4_tok(dO + vrow(t) + 4 * (tid & 31)) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    // ---- U, dU, T, then S and dS' in eight groups of 16 columns
     {
         const float* Ug = u_save + unit * kCb * kD;
         const float* DUg = du_save + unit * kCb * kD;
@@ -450,117 +457,114 @@ __global__ void __launch_bounds__(kGT, 1) grad_kernel(const Tin* __restrict__ q,
             const int r = tid >> 3, c4 = 4 * (tid & 7);
             cp_async16(sm + gk::TM + r * kLQ + c4, t_ws + unit * kCb * kCb + r * kCb + c4);
         }
-        const float* Sg = s_save + unit * kD * kD;
-        const float* DSg = ds_save + unit * kD * kD;
-#pragma unroll
-        for (int jb = 0; jb < 8; ++jb) {
-#pragma unroll
-            for (int m = 0; m < 2; ++m) {
-                const int id = tid + kGT * m;            // 2 matrices x 128 rows x 4 pieces of 16 bytes
-                const int row = (id >> 2) & (kD - 1), c4 = 16 * jb + 4 * (id & 3);
-                if (id < 512)
-                    cp_async16(sm + gk::DS + row * kLS + c4, DSg + row * kD + c4);
-                else
-                    cp_async16(sm + gk::SS + row * kLS + c4, Sg + row * kD + c4);
-            }
-            cp_async_commit();
-        }
     }
-    // scaled dO with ordinary loads while the copies fly (zero past the end of the sequence)
-    {
-        const int t = tid >> 4, c8 = 8 * (tid & 15);
-        float x[8];
-        if (t < nvalid) {
-            Vec8<Tin>::load(dO + vrow(t) + c8, x);
-        } else {
+    const float* Sg = s_save + unit * kD * kD;
+    const float* DSg = ds_save + unit * kD * kD;
+    auto issue_block = [&](int jb) {  // columns 16jb .. 16jb+15 of S and dS'
 #pragma unroll
-            for (int i = 0; i < 8; ++i) x[i] = 0.f;
+        for (int m = 0; m < 2; ++m) {
+            const int id = tid + kGT * m;  // 2 matrices x 128 rows x 4 pieces of 16 bytes
+            const int row = (id >> 2) & (kD - 1), c4 = 16 * jb + 4 * (id & 3);
+            if (id < 512)
+                cp_async16(sm + gk::DS + row * kLS + c4, DSg + row * kD + c4);
+            else
+                cp_async16(sm + gk::SS + row * kLS + c4, Sg + row * kD + c4);
         }
-        sts4(sm + gk::DO + t * kLS + c8, make_float4(scale * x[0], scale * x[1], scale * x[2], scale * x[3]));
-        sts4(sm + gk::DO + t * kLS + c8 + 4, make_float4(scale * x[4], scale * x[5], scale * x[6], scale * x[7]));
+    };
+#pragma unroll
+    for (int jb = 0; jb < 8; ++jb) {  // all in flight at once (measured faster than a few groups ahead)
+        issue_block(jb);
+        cp_async_commit();  // group 0 also carries U, dU and T
+    }
+    {   // scaled dO, loaded before the copies were queued (zero past the end of the sequence)
+        const int c4 = 4 * (tid & 31);
+#pragma unroll
+        for (int pass = 0; pass < 2; ++pass)
+            sts4(sm + gk::DO + ((tid >> 5) + 16 * pass) * kLS + c4,
+                 make_float4(scale * do4[pass].x, scale * do4[pass].y, scale * do4[pass].z, scale * do4[pass].w));
     }
 
-    // ---- 1. the products with S and dS' (contraction over d_v)
-    const int warp = tid >> 5, lane = tid & 31;
-    const int cb = 32 * (warp & 3) + (lane & 7);   // channels cb + 8r, r = 0..3
-    const int ta = 8 * (warp >> 2) + (lane >> 3);  // tokens ta, ta + 4
-    float aKh[2][4], aQb[2][4], aW[2][4], dgp[4];
+    // ---- 1. dK^ = U dS'^T (warps 0-3), dQ_bar = dO~ S^T (4-7), dW = -dU S^T (8-11), contraction over d_v:
+    //      a quarter-warp takes 8 channels 4 apart (one shared address per quarter, the four quarters in
+    //      different banks), its lanes 4 tokens each;
+    //      warps 12-15 form rowsum(dS' . S)
+    {
+        const int warp = tid >> 5, lane = tid & 31, prod = warp >> 2;
+        const int c0 = 32 * (warp & 3) + (lane >> 3), tq = lane & 7;  // channels c0 + 4i, tokens tq + 8i
+        const float* Am = sm + (prod == 0 ? gk::DS : gk::SS) + c0 * kLS;
+        const float* Bm = sm + (prod == 0 ? gk::U : prod == 1 ? gk::DO : gk::DU) + tq * kLS;
+        float acc[8][4] = {};
+        float dgam = 0.f;
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
-        dgp[r] = 0.f;
-#pragma unroll
-        for (int i = 0; i < 2; ++i) aKh[i][r] = aQb[i][r] = aW[i][r] = 0.f;
-    }
-#pragma unroll
-    for (int jb = 0; jb < 8; ++jb) {
-        cp_async_wait(7 - jb);
-        __syncthreads();
-#pragma unroll
-        for (int jq = 0; jq < 4; ++jq) {
-            const int j = 16 * jb + 4 * jq;
-            float4 u4[2], du4[2], o4[2], s4[4], ds4[4];
-#pragma unroll
-            for (int i = 0; i < 2; ++i) {
-                u4[i] = lds4(sm + gk::U + (ta + 4 * i) * kLS + j);
-                du4[i] = lds4(sm + gk::DU + (ta + 4 * i) * kLS + j);
-                o4[i] = lds4(sm + gk::DO + (ta + 4 * i) * kLS + j);
-            }
-#pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                s4[r] = lds4(sm + gk::SS + (cb + 8 * r) * kLS + j);
-                ds4[r] = lds4(sm + gk::DS + (cb + 8 * r) * kLS + j);
-            }
-#pragma unroll
-            for (int i = 0; i < 2; ++i)
-#pragma unroll
-                for (int r = 0; r < 4; ++r) {
-                    aKh[i][r] = dot4(u4[i], ds4[r], aKh[i][r]);
-                    aQb[i][r] = dot4(o4[i], s4[r], aQb[i][r]);
-                    aW[i][r] = dot4(du4[i], s4[r], aW[i][r]);
+        for (int jb = 0; jb < 8; ++jb) {
+            cp_async_wait(7 - jb);  // groups 0 .. jb have landed
+            __syncthreads();
+            if (jb == 4) {  // the token inputs read after the products: into L2 now, one 128-byte line each
+                constexpr int kLines = kD * (int)sizeof(Tin) / 128;  // lines per token row
+                for (int i = tid; i < 6 * kCb * kLines; i += kGT) {
+                    const int ten = i / (kCb * kLines), row = (i / kLines) % kCb, line = i % kLines;
+                    if (row < nvalid) {
+                        const Tin* base = ten == 0 ? w : ten == 1 ? v : ten == 2 ? g : ten == 3 ? b : ten == 4 ? k : q;
+                        const size_t off = (ten >= 4 ? krow(row) : vrow(row)) + line * (128 / (int)sizeof(Tin));
+                        asm volatile("prefetch.global.L2 [%0];" ::"l"(base + off));
+                    }
                 }
-            if (jq == (warp >> 2))  // each row of warps takes one quarter of the columns of the rowsum
+            }
+            if (prod < 3) {
 #pragma unroll
-                for (int r = 0; r < 4; ++r) dgp[r] = dot4(ds4[r], s4[r], dgp[r]);
+                for (int jq = 0; jq < 4; ++jq) {
+                    const int j = 16 * jb + 4 * jq;
+                    float4 av[8], bv[4];
+#pragma unroll
+                    for (int ci = 0; ci < 8; ++ci) av[ci] = lds4(Am + 4 * ci * kLS + j);
+#pragma unroll
+                    for (int ti = 0; ti < 4; ++ti) bv[ti] = lds4(Bm + 8 * ti * kLS + j);
+#pragma unroll
+                    for (int ci = 0; ci < 8; ++ci)
+#pragma unroll
+                        for (int ti = 0; ti < 4; ++ti) acc[ci][ti] = dot4(av[ci], bv[ti], acc[ci][ti]);
+                }
+            } else {
+                const int c = tid - 3 * 128;
+#pragma unroll
+                for (int jq = 0; jq < 4; ++jq) {
+                    const int j = 16 * jb + 4 * jq;
+                    dgam = dot4(lds4(sm + gk::DS + c * kLS + j), lds4(sm + gk::SS + c * kLS + j), dgam);
+                }
+            }
+        }
+        __syncthreads();  // S, dS' read out: their room takes the per-token arrays
+        if (prod < 3) {
+            float* dst = sm + (prod == 0 ? gk::DKH : prod == 1 ? gk::DQB : gk::DW);
+            const float sg = prod == 2 ? -1.f : 1.f;
+#pragma unroll
+            for (int ci = 0; ci < 8; ++ci)
+#pragma unroll
+                for (int ti = 0; ti < 4; ++ti) dst[(tq + 8 * ti) * kLS + c0 + 4 * ci] = sg * acc[ci][ti];
+        } else {
+            sm[gk::DGP + tid - 3 * 128] = dgam;
         }
     }
-    __syncthreads();  // S, dS' read out: their room takes the per-token arrays
-#pragma unroll
-    for (int i = 0; i < 2; ++i)
-#pragma unroll
-        for (int r = 0; r < 4; ++r) {
-            const int o = (ta + 4 * i) * kLS + cb + 8 * r;
-            sm[gk::DKH + o] = aKh[i][r];
-            sm[gk::DQB + o] = aQb[i][r];
-            sm[gk::DW + o] = -aW[i][r];
-        }
-    if ((lane >> 3) == 0)
-#pragma unroll
-        for (int r = 0; r < 4; ++r) sm[gk::DGP + (warp >> 2) * kD + cb + 8 * r] = dgp[r];
     {   // token inputs: U0 = w.v, g, k, b.k, q (zero past the end of the sequence)
-        const int t = tid >> 4, c8 = 8 * (tid & 15);
-        float xw[8], xv[8], xg[8], xk[8], xb[8], xq[8];
-        if (t < nvalid) {
-            Vec8<Tin>::load(w + vrow(t) + c8, xw);
-            Vec8<Tin>::load(v + vrow(t) + c8, xv);
-            Vec8<Tin>::load(g + vrow(t) + c8, xg);
-            Vec8<Tin>::load(b + vrow(t) + c8, xb);
-            Vec8<Tin>::load(k + krow(t) + c8, xk);
-            Vec8<Tin>::load(q + krow(t) + c8, xq);
-        } else {
+        const int c4 = 4 * (tid & 31);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) xw[i] = xv[i] = xg[i] = xk[i] = xb[i] = xq[i] = 0.f;
-        }
-        const int o = t * kLS + c8;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int i = 4 * h;
-            sts4(sm + gk::U0 + o + i, make_float4(xw[i] * xv[i], xw[i + 1] * xv[i + 1], xw[i + 2] * xv[i + 2],
-                                                  xw[i + 3] * xv[i + 3]));
-            sts4(sm + gk::G + o + i, make_float4(xg[i], xg[i + 1], xg[i + 2], xg[i + 3]));
-            sts4(sm + gk::K + o + i, make_float4(xk[i], xk[i + 1], xk[i + 2], xk[i + 3]));
-            sts4(sm + gk::BETA + o + i, make_float4(xb[i] * xk[i], xb[i + 1] * xk[i + 1], xb[i + 2] * xk[i + 2],
-                                                    xb[i + 3] * xk[i + 3]));
-            sts4(sm + gk::Q + o + i, make_float4(xq[i], xq[i + 1], xq[i + 2], xq[i + 3]));
+        for (int pass = 0; pass < 2; ++pass) {
+            const int t = (tid >> 5) + 16 * pass;
+            float4 xw = make_float4(0.f, 0.f, 0.f, 0.f), xv = xw, xg = xw, xk = xw, xb = xw, xq = xw;
+            if (t < nvalid) {
+                xw = ld4_tok(w + vrow(t) + c4);
+                xv = ld4_tok(v + vrow(t) + c4);
+                xg = ld4_tok(g + vrow(t) + c4);
+                xb = ld4_tok(b + vrow(t) + c4);
+                xk = ld4_tok(k + krow(t) + c4);
+                xq = ld4_tok(q + krow(t) + c4);
+            }
+            const int o = t * kLS + c4;
+            sts4(sm + gk::U0 + o, make_float4(xw.x * xv.x, xw.y * xv.y, xw.z * xv.z, xw.w * xv.w));
+            sts4(sm + gk::G + o, xg);
+            sts4(sm + gk::K + o, xk);
+            sts4(sm + gk::BETA + o, make_float4(xb.x * xk.x, xb.y * xk.y, xb.z * xk.z, xb.w * xk.w));
+            sts4(sm + gk::Q + o, xq);
         }
     }
     __syncthreads();
@@ -602,11 +606,13 @@ __global__ void __launch_bounds__(kGT, 1) grad_kernel(const Tin* __restrict__ q,
             }
     __syncthreads();
     {   // K_bar = b.k.e^G in place of U0
-        const int t = tid >> 4, c8 = 8 * (tid & 15);
+        const int c4 = 4 * (tid & 31);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int o = t * kLS + c8 + i;
-            sm[gk::KB + o] = sm[gk::BETA + o] * __expf(sm[gk::G + o]);
+        for (int pass = 0; pass < 2; ++pass) {
+            const int o = ((tid >> 5) + 16 * pass) * kLS + c4;
+            const float4 be = lds4(sm + gk::BETA + o), gg = lds4(sm + gk::G + o);
+            sts4(sm + gk::KB + o, make_float4(be.x * __expf(gg.x), be.y * __expf(gg.y), be.z * __expf(gg.z),
+                                              be.w * __expf(gg.w)));
         }
     }
     __syncthreads();
@@ -796,12 +802,19 @@ __global__ void __launch_bounds__(kGT, 1) grad_kernel(const Tin* __restrict__ q,
     }
     __syncthreads();
 
-    // ---- 5. back to the inputs: thread = channel c, block of 8 tokens
+    // ---- 5. back to the inputs: thread = channel c, block of 8 tokens; then dg_t = sum_{s >= t} dG_s +
+    //      dG_last, dG_last = sum_t dK^.K^ + rowsum(dS'.S) e^{G_last}, from suffix sums inside each block
+    //      plus the totals of the later blocks
     {
         const int c = tid & (kD - 1), blk = tid >> 7;
         const float Glast = sm[gk::G + (kCb - 1) * kLS + c];
-        float dkk = 0.f;
-#pragma unroll 2
+        float dkk = 0.f, dGb[8], bb[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int t = 8 * blk + i;
+            bb[i] = t < nvalid ? to_f32(b[vrow(t) + c]) : 0.f;
+        }
+#pragma unroll
         for (int i = 0; i < 8; ++i) {
             const int t = 8 * blk + i, o = t * kLS + c;
             const float G = sm[gk::G + o], eG = __expf(G), eH = __expf(Glast - G);
@@ -809,29 +822,31 @@ __global__ void __launch_bounds__(kGT, 1) grad_kernel(const Tin* __restrict__ q,
             const float dqb = sm[gk::DQB + o], dkb = sm[gk::DKB + o], dkh = sm[gk::DKH + o];
             const float x = sm[gk::XX + o], y = sm[gk::YY + o], zv = sm[gk::ZV + o];
             const float dbeta = fmaf(dkb, eG, x);
-            const float dGt = dqb * qq * eG + dkb * kb - dkh * kk * eH + be * x + qq * y - kk * zv;
+            dGb[i] = dqb * qq * eG + dkb * kb - dkh * kk * eH + be * x + qq * y - kk * zv;
             dkk = fmaf(dkh, kk * eH, dkk);
-            sm[gk::DQB + o] = dGt;  // dQ_bar of (t, c) is no longer needed
             if (t < nvalid) {
                 const size_t vh = vrow(t) + c;
-                const float bb = to_f32(b[vh]);
                 dq_ws[vh] = fmaf(dqb, eG, y);
-                dk_ws[vh] = fmaf(dkh, eH, zv) + dbeta * bb;
+                dk_ws[vh] = fmaf(dkh, eH, zv) + dbeta * bb[i];
                 db[vh] = from_f32<Tin>(dbeta * kk);
             }
         }
+        float run = 0.f;
+#pragma unroll
+        for (int i = 7; i >= 0; --i) {
+            run += dGb[i];
+            dGb[i] = run;
+        }
         sm[gk::DGL + blk * kD + c] = dkk;
-    }
-    __syncthreads();
-    if (tid < kD) {  // dg_t = sum_{s >= t} dG_s + dG_last, dG_last = sum_t dK^.K^ + rowsum(dS'.S) e^{G_last}
-        const int c = tid;
-        const float Glast = sm[gk::G + (kCb - 1) * kLS + c];
-        const float dgam = (sm[gk::DGP + c] + sm[gk::DGP + kD + c]) + (sm[gk::DGP + 2 * kD + c] + sm[gk::DGP + 3 * kD + c]);
-        float run = (sm[gk::DGL + c] + sm[gk::DGL + kD + c]) + (sm[gk::DGL + 2 * kD + c] + sm[gk::DGL + 3 * kD + c]);
-        run = fmaf(dgam, __expf(Glast), run);
-        for (int t = kCb - 1; t >= 0; --t) {
-            run += sm[gk::DQB + t * kLS + c];
-            if (t < nvalid) dg[vrow(t) + c] = from_f32<Tin>(run);
+        sm[gk::DBT + blk * kD + c] = run;
+        __syncthreads();
+        float off = (sm[gk::DGL + c] + sm[gk::DGL + kD + c]) + (sm[gk::DGL + 2 * kD + c] + sm[gk::DGL + 3 * kD + c]);
+        off = fmaf(sm[gk::DGP + c], __expf(Glast), off);
+        for (int b2 = 3; b2 > blk; --b2) off += sm[gk::DBT + b2 * kD + c];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int t = 8 * blk + i;
+            if (t < nvalid) dg[vrow(t) + c] = from_f32<Tin>(dGb[i] + off);
         }
     }
 }
