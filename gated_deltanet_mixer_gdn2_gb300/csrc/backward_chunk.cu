@@ -11,13 +11,16 @@
 //     dU  = M^T dO~ + K^ dS'                dS = G dS' + Q_bar^T dO~ - W^T dU      (the chain over chunks)
 //     dQ_bar = dO~ S^T   dW = -dU S^T   dK^ = U dS'^T   dgamma = rowsum(dS' . S)   dM = tril(dO~ U^T)
 //     dT = dU U0^T + dW K_bar^T   dU0 = T^T dU   dK_bar = T^T dW   dA = -strict_tril(T^T dT T^T)
-// and through the elementwise factors to dq, dk, db, dg, dv, dw; the terms of A and M are taken pair
-// by pair with e^{G_t - G_s} <= 1, so no factor can overflow whatever the decays.
+// and through the elementwise factors to dq, dk, db, dg, dv, dw; every exponential factor of A and M is
+// <= 1, so no factor can overflow whatever the decays.
 //
-// Four launches: the fp32 forward keeping T, S_n and U per chunk; the chain over chunks in reverse
-// (adjoint_kernel: heads x 16-column slices, like the forward's state kernel); the local gradients of
-// every (chunk, head) in parallel (grad_kernel, one 512-thread CTA per SM, register-tiled products);
-// the sums of dq, dk over each key head's group.
+// Five launches: the state-independent factors of every chunk (factors_simt_kernel in token-major form,
+// plus T); the chain over chunks forward (save_chain_kernel: keeps S_n and U_n) and in reverse
+// (adjoint_kernel: keeps dS_{n+1} and dU_n), each one CTA per (batch-head, 64 columns of d_v) with its
+// state slice in registers; the per-token gradients of every (chunk, head) in parallel (grad_kernel,
+// one 512-thread CTA per SM); the sums of dq, dk over each key head's group. Within a chunk the pair
+// factors e^{G_t - G_s} of tokens in different 8-token blocks are split at a block edge into two
+// factors <= 1.
 #include <type_traits>
 
 #include "common.cuh"

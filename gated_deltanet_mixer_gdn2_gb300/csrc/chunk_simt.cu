@@ -16,6 +16,9 @@
 //           state and stores it in the workspace: W^T, (q . e^{G})^T, (k . e^{G_last - G})^T [d_k x C],
 //           M [C x C], U~^T [d_v x C], e^{G_last} [d_k];
 //   state   (grid: heads x 16-column slices of d_v, sequential over chunks) carries S_n and writes o.
+// For the chunked backward the factor kernel writes the same quantities token-major ([C x d]) and adds
+// channel-major copies of W and k . e^{G_last - G}; there the chains of backward_chunk.cu replace the
+// state kernel.
 // Padding: tokens past T read as zeros (k = q = b = v = w = 0, g = 0), which leaves S unchanged.
 #include "common.cuh"
 

@@ -246,11 +246,11 @@ gdn2_status gdn2_mixer_epilogue(const void* o, const void* z, const float* weigh
  * recurrence of the burn-gdn2 0.1.5 docs ("Architecture"), given the upstream gradient d_o of o
  * and optionally d_final_state of S_T: the gradients of sum(o * d_o) + sum(S_T * d_final_state).
  * Reverse mode of the chunked (WY / UT) form of the same recurrence ("Gated Delta Networks:
- * Improving Mamba2 with Delta Rule", section 3.3), in fp32 with chunks of 32 tokens, in four
- * launches: a forward chain that keeps each chunk's starting state S_n, its U and its T =
- * (I + A)^-1 in the workspace; a backward chain over the chunks that keeps dS_(n+1) and dU; one CTA
- * per (chunk, batch, value head) that forms every per-token gradient of its chunk from those; and
- * a pass that adds the value heads of each key head for dq and dk in a fixed order. The forward
+ * Improving Mamba2 with Delta Rule", section 3.3), in fp32 with chunks of 32 tokens, in five
+ * launches: the state-independent factors of every chunk (with T = (I + A)^-1); a forward chain
+ * that keeps each chunk's starting state S_n and its U; a backward chain that keeps dS_(n+1) and dU;
+ * one CTA per (chunk, batch, value head) that forms every per-token gradient of its chunk from those;
+ * and a pass that adds the value heads of each key head for dq and dk in a fixed order. The forward
  * outputs are not needed. Gates enter only as ratios exp(G_t - G_s) with t >= s, so no
  * intermediate overflows for any g <= 0.
  * q, k, dq, dk: [B, T, H_k, d_k]; v, w, d_o, dv, dw: [B, T, H_v, d_v]; g, b, dg, db: [B, T, H_v, d_k]
