@@ -57,22 +57,40 @@ __global__ void __launch_bounds__(256) factors_simt_kernel(const Tin* __restrict
     const SimtWs L{dk, dv, C, imajor != 0};
     float* u = ws + ((size_t)bh * NC + n) * L.unit_floats();
 
-    for (int idx = tid; idx < C * dk; idx += nt) {
-        const int t = idx / dk, c = idx - t * dk;
+    {   // w and v are read after the inverse: into L2 now, one 128-byte line per thread
+        const int lines = (dv * (int)sizeof(Tin) + 127) / 128, per = 128 / (int)sizeof(Tin);
+        for (int i = tid; i < 2 * C * lines; i += nt) {
+            const int ten = i / (C * lines), t = (i / lines) % C, line = i % lines;
+            if (t0 + t < T) {
+                const Tin* base = ten ? v : w;
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(base + (((size_t)bi * T + t0 + t) * Hv + hv) * dv + line * per));
+            }
+        }
+    }
+    // eight consecutive channels per load (d_k, d_v are multiples of 16, so rows stay 16-byte aligned)
+#pragma unroll 2
+    for (int idx = tid; idx < C * dk / 8; idx += nt) {
+        const int t = idx / (dk / 8), c = 8 * (idx - t * (dk / 8));
         const int tok = t0 + t;
-        float gg = 0.f, kk = 0.f, bb = 0.f, qq = 0.f;
+        float gg[8], kk[8], bb[8], qq[8];
         if (tok < T) {
             const size_t kq_i = (((size_t)bi * T + tok) * Hk + hk) * dk + c;
             const size_t gb_i = (((size_t)bi * T + tok) * Hv + hv) * dk + c;
-            gg = to_f32(g[gb_i]);
-            bb = to_f32(b[gb_i]);
-            kk = to_f32(k[kq_i]);
-            qq = to_f32(q[kq_i]);
+            Vec8<Tin>::load(g + gb_i, gg);
+            Vec8<Tin>::load(b + gb_i, bb);
+            Vec8<Tin>::load(k + kq_i, kk);
+            Vec8<Tin>::load(q + kq_i, qq);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) gg[i] = kk[i] = bb[i] = qq[i] = 0.f;
         }
-        sG[t * LD + c] = gg;
-        sK[t * LD + c] = kk;
-        sBK[t * LD + c] = bb * kk;
-        sQ[t * LDQ + c] = qq;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            sG[t * LD + c + i] = gg[i];
+            sK[t * LD + c + i] = kk[i];
+            sBK[t * LD + c + i] = bb[i] * kk[i];
+            sQ[t * LDQ + c + i] = qq[i];
+        }
     }
     __syncthreads();
     // inclusive cumulative log-decay per key channel, and the chunk decay e^{G_last}
@@ -159,15 +177,21 @@ __global__ void __launch_bounds__(256) factors_simt_kernel(const Tin* __restrict
         const int t = idx / dk, c = idx - t * dk;
         sBK[t * LD + c] *= __expf(sG[t * LD + c]);
     }
-    for (int idx = tid; idx < C * dv; idx += nt) {
-        const int t = idx / dv, c = idx - t * dv;
+#pragma unroll 2
+    for (int idx = tid; idx < C * dv / 8; idx += nt) {
+        const int t = idx / (dv / 8), c = 8 * (idx - t * (dv / 8));
         const int tok = t0 + t;
-        float x = 0.f;
+        float ww[8], vv[8];
         if (tok < T) {
             const size_t vw_i = (((size_t)bi * T + tok) * Hv + hv) * dv + c;
-            x = to_f32(w[vw_i]) * to_f32(v[vw_i]);
+            Vec8<Tin>::load(w + vw_i, ww);
+            Vec8<Tin>::load(v + vw_i, vv);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) ww[i] = vv[i] = 0.f;
         }
-        sQ[t * LDQ + c] = x;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) sQ[t * LDQ + c + i] = ww[i] * vv[i];
     }
     __syncthreads();
     // W^T [d_k][C] = (T X)^T with X = b . k . e^{G};  U~^T [d_v][C] = (T (w . v))^T  (W [C][d_k] and
