@@ -28,9 +28,12 @@ namespace {
 
 __device__ int g_status_simt;
 
+// 9 warps: the 528 pairs of A and M for C = 32 take at most two rounds of the block
+constexpr int kFactorThreads = 288;
+
 // kDK, kDV, kC: the sizes as compile-time constants, or 0 to take them from the arguments
 template <typename Tin, int kDK, int kDV, int kC>
-__global__ void __launch_bounds__(256) factors_simt_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k,
+__global__ void __launch_bounds__(kFactorThreads) factors_simt_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k,
                                                            const Tin* __restrict__ v, const Tin* __restrict__ g,
                                                            const Tin* __restrict__ b, const Tin* __restrict__ w,
                                                            float* __restrict__ ws, float* __restrict__ t_out, int T,
@@ -194,24 +197,38 @@ __global__ void __launch_bounds__(256) factors_simt_kernel(const Tin* __restrict
         for (int i = 0; i < 8; ++i) sQ[t * LDQ + c + i] = ww[i] * vv[i];
     }
     __syncthreads();
-    // W^T [d_k][C] = (T X)^T with X = b . k . e^{G};  U~^T [d_v][C] = (T (w . v))^T  (W [C][d_k] and
-    // U~ [C][d_v] when imajor)
-    for (int p = tid; p < dk * C; p += nt) {
-        int c, i;
-        if (imajor) i = p / dk, c = p - i * dk;
-        else c = p / C, i = p - c * C;
-        float acc = 0.f;
-        for (int j = 0; j <= i; ++j) acc = fmaf(sT[i * (C + 1) + j], sBK[j * LD + c], acc);
-        u[L.off_wt() + p] = acc;
-        if (imajor) sK[i * LD + c] = acc;  // k is read out: W for its channel-major copy
-    }
-    for (int p = tid; p < dv * C; p += nt) {
-        int c, i;
-        if (imajor) i = p / dv, c = p - i * dv;
-        else c = p / C, i = p - c * C;
-        float acc = 0.f;
-        for (int j = 0; j <= i; ++j) acc = fmaf(sT[i * (C + 1) + j], sQ[j * LDQ + c], acc);
-        u[L.off_utt() + p] = acc;
+    // W = T X with X = b . k . e^{G}, and U~ = T (w . v), stored [C][d] when imajor, else transposed:
+    // thread = channel c and the rows i, C-1-i together (four independent sums; the j loop runs to the
+    // longer row, T being zero above its diagonal)
+    {
+        const int dm = dk > dv ? dk : dv;
+        for (int p = tid; p < dm * (C / 2); p += nt) {
+            const int ip = p / dm, c = p - ip * dm;
+            const int i1 = ip, i2 = C - 1 - ip;
+            const bool hw = c < dk, hu = c < dv;
+            float w1 = 0.f, w2 = 0.f, u1 = 0.f, u2 = 0.f;
+#pragma unroll 4
+            for (int j = 0; j <= i2; ++j) {
+                const float t1 = sT[i1 * (C + 1) + j], t2 = sT[i2 * (C + 1) + j];
+                const float x = hw ? sBK[j * LD + c] : 0.f, y = hu ? sQ[j * LDQ + c] : 0.f;
+                w1 = fmaf(t1, x, w1);
+                w2 = fmaf(t2, x, w2);
+                u1 = fmaf(t1, y, u1);
+                u2 = fmaf(t2, y, u2);
+            }
+            if (hw) {
+                u[L.off_wt() + (imajor ? (size_t)i1 * dk + c : (size_t)c * C + i1)] = w1;
+                u[L.off_wt() + (imajor ? (size_t)i2 * dk + c : (size_t)c * C + i2)] = w2;
+                if (imajor) {  // k is read out: W for its channel-major copy
+                    sK[i1 * LD + c] = w1;
+                    sK[i2 * LD + c] = w2;
+                }
+            }
+            if (hu) {
+                u[L.off_utt() + (imajor ? (size_t)i1 * dv + c : (size_t)c * C + i1)] = u1;
+                u[L.off_utt() + (imajor ? (size_t)i2 * dv + c : (size_t)c * C + i2)] = u2;
+            }
+        }
     }
     if (imajor) {
         __syncthreads();
@@ -320,7 +337,7 @@ cudaError_t launch_factors_shape(const void* q, const void* k, const void* v, co
     cudaError_t e = cudaFuncSetAttribute(factors_simt_kernel<Tin, kDK, kDV, kC>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)f_smem);
     if (e != cudaSuccess) return e;
-    factors_simt_kernel<Tin, kDK, kDV, kC><<<dim3(sh.nchunks(), sh.B * sh.Hv), 256, f_smem, s>>>(
+    factors_simt_kernel<Tin, kDK, kDV, kC><<<dim3(sh.nchunks(), sh.B * sh.Hv), kFactorThreads, f_smem, s>>>(
         static_cast<const Tin*>(q), static_cast<const Tin*>(k), static_cast<const Tin*>(v),
         static_cast<const Tin*>(g), static_cast<const Tin*>(b), static_cast<const Tin*>(w), static_cast<float*>(ws),
         t_out, sh.T, sh.Hk, sh.Hv, sh.dk, sh.dv, sh.C, imajor);
