@@ -136,17 +136,24 @@ __global__ void __launch_bounds__(kFactorThreads) factors_simt_kernel(const Tin*
     // T = (I + A)^{-1} (unit lower triangular) by 16 x 16 blocks: each diagonal block by forward
     // substitution (thread = column), then the block rows r in order,
     //     T_rs = -T_rr X_rs,   X_rs = sum_{s <= l < r} A_rl T_ls   (blocks s < r)
-    if (tid < C) {
-        const int j = tid, top = j & ~15;
-        sT[j * (C + 1) + j] = 1.f;
-        for (int i = j + 1; i < top + 16; ++i) {
+    if (tid < C) {  // column j of its diagonal block, kept in registers
+        const int j = tid, top = j & ~15, jl = j & 15;
+        float tc[16];
+#pragma unroll
+        for (int r = 0; r < 16; ++r) tc[r] = r == jl ? 1.f : 0.f;
+#pragma unroll
+        for (int r = 1; r < 16; ++r) {
             float acc = 0.f;
-            for (int l = j; l < i; ++l) acc = fmaf(sA[i * (C + 1) + l], sT[l * (C + 1) + j], acc);
-            sT[i * (C + 1) + j] = -acc;
+#pragma unroll
+            for (int l = 0; l < r; ++l) acc = fmaf(sA[(top + r) * (C + 1) + top + l], tc[l], acc);
+            if (r > jl) tc[r] = -acc;  // rows above j stay 0, row j stays 1
         }
+#pragma unroll
+        for (int r = 0; r < 16; ++r) sT[(top + r) * (C + 1) + j] = tc[r];
     }
-    // decayed q and k ([d_k][C], or [C][d_k] when imajor) for the state kernel; b . k . e^{G} in place
-    for (int p = tid; p < dk * C; p += nt) {
+    // decayed q and k ([d_k][C], or [C][d_k] when imajor) for the state kernel, by the threads that do not
+    // solve; b . k . e^{G} in place
+    for (int p = tid - C; p >= 0 && p < dk * C; p += nt - C) {
         int c, i;
         if (imajor) i = p / dk, c = p - i * dk;
         else c = p / C, i = p - c * C;
@@ -155,7 +162,7 @@ __global__ void __launch_bounds__(kFactorThreads) factors_simt_kernel(const Tin*
         u[L.off_kht() + p] = sK[i * LD + c] * __expf(sG[(C - 1) * LD + c] - Gi);
     }
     if (imajor)  // channel-major copy of k.e^{G_last-G}
-        for (int p = tid; p < dk * C; p += nt) {
+        for (int p = tid - C; p >= 0 && p < dk * C; p += nt - C) {
             const int c = p / C, i = p - c * C;
             u[L.off_kht2() + p] = sK[i * LD + c] * __expf(sG[(C - 1) * LD + c] - sG[i * LD + c]);
         }
