@@ -2,6 +2,8 @@
 chunked path (gdn2_backward) and the per-token recurrent path (gdn2_backward_recurrent), bf16 and
 fp32 token tensors, grouped heads, a ragged last chunk, an initial state and an upstream
 final-state gradient; at lengths the oracle cannot reach, the two paths against each other."""
+import dataclasses
+
 import numpy as np
 import pytest
 
@@ -23,7 +25,7 @@ def g():
 
 
 @pytest.mark.parametrize("recurrent", [False, True], ids=["chunked", "recurrent"])
-@pytest.mark.parametrize("dtype,T,with_ds", [("bf16", 77, True), ("f32", 45, False), ("f32", 64, True)])
+@pytest.mark.parametrize("dtype,T,with_ds", [("bf16", 77, True), ("f32", 45, False), ("f32", 64, True), ("f32", 5, True)])
 def test_backward_parity(g, dtype, T, with_ds, recurrent):
     import torch
 
@@ -78,3 +80,33 @@ def test_backward_chunked_matches_recurrent_on_long_sequences(g, T, Hk, Hv):
         assert torch.isfinite(x).all(), name
         e = max_rel_err(H.to_np(x), H.to_np(y).astype(np.float64))
         assert e < 1e-3, (name, e)
+
+
+@pytest.mark.parametrize("decay", ["strong", "none"])
+def test_backward_extreme_decays(g, decay):
+    """Gates far from the synthetic recipe: log-decays near -3 per token (products of the pair factors
+    underflow inside a 32-token chunk) and no decay at all (every factor is 1)."""
+    import torch
+
+    T = 70
+    wl = synth.Workload("bwd-decay", B=1, T=T, Hk=1, Hv=2, dk=128, dv=128, dtype="f32", seed=7, s0_std=0.02)
+    inp = synth.make_inputs(wl)
+    rng = np.random.default_rng(11)
+    if decay == "strong":
+        gg = -np.log1p(np.exp(rng.normal(3.0, 1.0, inp.g.shape)))
+    else:
+        gg = np.zeros(inp.g.shape)
+    inp = dataclasses.replace(inp, g=gg.astype(np.float32).astype(np.float64))
+    d_o = rng.standard_normal((1, T, 2, 128)).astype(np.float32).astype(np.float64)
+    ds_t = (0.1 * rng.standard_normal((1, 2, 128, 128))).astype(np.float32).astype(np.float64)
+    dev = lambda a: synth.to_torch(np.ascontiguousarray(a), "f32", "cuda")
+    ts = [dev(getattr(inp, n)) for n in ("q", "k", "v", "g", "b", "w")]
+    outs = g.backward(*ts, dev(d_o), H.state_to_device(inp.s0), H.state_to_device(ds_t))
+    torch.cuda.synchronize()
+    assert g.gdn2_last_device_status() == g.GDN2_OK
+    ref = oback.gradients(inp.q, inp.k, inp.v, inp.g, inp.b, inp.w, inp.s0, d_o, ds_t)
+    for name, got in zip(("dq", "dk", "dv", "dg", "db", "dw", "ds0"), outs):
+        x = H.to_np(got)
+        assert np.isfinite(x).all(), name
+        e = max_rel_err(x, ref[name])
+        assert e < TOL["f32"], (name, e)
