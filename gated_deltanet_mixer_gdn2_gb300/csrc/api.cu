@@ -51,6 +51,9 @@ bool sizes_ok(long long B, long long T, long long Hk, long long Hv, long long dk
     return el < (1LL << 46);
 }
 
+// The chunked kernels put (batch, value head) on the grid's second dimension (at most 65535).
+bool grid_ok(long long B, long long Hv) { return B * Hv <= 65535; }
+
 size_t ws_size(gdn2_path path, const ChunkShape& sh, gdn2_dtype dt) {
     if (sh.B <= 0 || sh.T <= 0) return 0;
     const gdn2_path p = resolve(path, sh, dt);
@@ -84,7 +87,7 @@ int gdn2_version(void) { return 100; }
 size_t gdn2_chunk_fwd_workspace_size_path(gdn2_path path, int B, int T, int Hk, int Hv, int dk, int dv, int C,
                                           gdn2_dtype dt) {
     if (!dtype_ok(dt) || B < 0 || T < 0 || Hk <= 0 || Hv <= 0 || dk <= 0 || dv <= 0 || C <= 0 || Hv % Hk) return 0;
-    if (!sizes_ok(B, T, Hk, Hv, dk, dv)) return 0;
+    if (!sizes_ok(B, T, Hk, Hv, dk, dv) || !grid_ok(B, Hv)) return 0;
     return ws_size(path, ChunkShape{B, T, Hk, Hv, dk, dv, C}, dt);
 }
 
@@ -100,7 +103,7 @@ gdn2_status gdn2_chunk_fwd_path(gdn2_path path, const void* q, const void* k, co
         return GDN2_ERR_INVALID_ARG;
     if (B < 0 || T < 0 || Hk <= 0 || Hv <= 0 || dk <= 0 || dv <= 0 || C <= 0 || Hv % Hk)
         return GDN2_ERR_INVALID_ARG;
-    if (!sizes_ok(B, T, Hk, Hv, dk, dv)) return GDN2_ERR_UNSUPPORTED;
+    if (!sizes_ok(B, T, Hk, Hv, dk, dv) || !grid_ok(B, Hv)) return GDN2_ERR_UNSUPPORTED;
     const ChunkShape sh{B, T, Hk, Hv, dk, dv, C};
     const gdn2_path p = resolve(path, sh, dt);
     if (p == GDN2_PATH_AUTO) return GDN2_ERR_UNSUPPORTED;

@@ -354,8 +354,9 @@ BwdLayout bwd_layout(int B, int T, int Hv) {
 }
 
 bool bwd_shape_ok(int B, int T, int Hk, int Hv, int dk, int dv) {
+    // (batch, value head) is the second grid dimension of the per-chunk kernels (at most 65535)
     return B >= 0 && T >= 0 && Hk > 0 && Hv > 0 && Hv % Hk == 0 && dk == kD && dv == kD &&
-           static_cast<long long>(B) * T * Hv < (1LL << 31) / kD;
+           static_cast<long long>(B) * T * Hv < (1LL << 31) / kD && static_cast<long long>(B) * Hv <= 65535;
 }
 
 }  // namespace

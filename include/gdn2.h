@@ -89,7 +89,7 @@ size_t gdn2_chunk_fwd_workspace_size_path(gdn2_path path, int B, int T, int Hk, 
  * T need not be a multiple of C (the last chunk is padded with tokens that leave the state
  * unchanged). T == 0 or B == 0 is valid: o is untouched and final_state receives initial_state (or
  * zeros). Supported: d_k, d_v multiples of 16 in [16, 128] (SIMT, fp32 or bf16); bf16 with
- * d_k = d_v = 128 and C = 64 (TCGEN05). Within one chunk the per-channel cumulative log-decay must
+ * d_k = d_v = 128 and C = 64 (TCGEN05); B * H_v <= 65535 (GDN2_ERR_UNSUPPORTED beyond). Within one chunk the per-channel cumulative log-decay must
  * span less than about 160 (alpha above about exp(-2.5) per token on average) on the TCGEN05 path;
  * beyond that its decay factors leave the fp32 exponent range.
  */
@@ -255,7 +255,8 @@ gdn2_status gdn2_mixer_epilogue(const void* o, const void* z, const float* weigh
  * intermediate overflows for any g <= 0.
  * q, k, dq, dk: [B, T, H_k, d_k]; v, w, d_o, dv, dw: [B, T, H_v, d_v]; g, b, dg, db: [B, T, H_v, d_k]
  * (all dtype dt); initial_state, d_final_state, d_initial_state: fp32 [B, H_v, d_k, d_v] or NULL
- * (zeros / not written). dq and dk of a key head sum its value heads. d_k = d_v = 128.
+ * (zeros / not written). dq and dk of a key head sum its value heads. d_k = d_v = 128,
+ * B * H_v <= 65535 (GDN2_ERR_UNSUPPORTED otherwise).
  * workspace: gdn2_backward_workspace_size(...) bytes of device memory, 16-byte aligned.
  * Errors: as gdn2_chunk_fwd. Asynchronous on `stream`.
  */

@@ -76,6 +76,8 @@ def test_chunk_argument_errors(g):
     assert _chunk(g, C=48) == g.GDN2_ERR_UNSUPPORTED
     assert _chunk(g, path=2, dt=0) == g.GDN2_ERR_UNSUPPORTED           # tensor cores need bf16
     assert _chunk(g, path=2, dk=64, dv=64) == g.GDN2_ERR_UNSUPPORTED
+    assert _chunk(g, B=32768, T=1, Hv=4) == g.GDN2_ERR_UNSUPPORTED     # B * H_v beyond the grid's y range
+    assert g.lib.gdn2_chunk_fwd_workspace_size(32768, 1, 1, 4, 128, 128, 64, 1) == 0
     assert _chunk(g, ptr=0x10008) == g.GDN2_ERR_MISALIGNED
     assert _chunk(g, ws=0) == g.GDN2_ERR_WORKSPACE
     assert _chunk(g, wsb=100) == g.GDN2_ERR_WORKSPACE
@@ -179,8 +181,10 @@ def test_backward_argument_errors(g, entry):
     assert f(ptr=0x10004) == g.GDN2_ERR_MISALIGNED
     assert f(ws=0) == g.GDN2_ERR_WORKSPACE
     assert f(wsb=16) == g.GDN2_ERR_WORKSPACE
+    assert f(B=32768, T=1, Hv=4) == g.GDN2_ERR_UNSUPPORTED  # (batch, value head) beyond the grid's y range
     size = getattr(g.lib, entry + "_workspace_size")
     assert size(2, 100, 1, 2, 64, 64, 1) == 0
+    assert size(32768, 1, 1, 4, 128, 128, 1) == 0
     assert size(2, 0, 1, 2, 128, 128, 1) == 0
 
 
