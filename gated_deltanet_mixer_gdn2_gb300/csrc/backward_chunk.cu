@@ -498,8 +498,8 @@ __global__ void __launch_bounds__(kGT, 1) grad_kernel(const Tin* __restrict__ q,
         const float* Bm = sm + (prod == 0 ? gk::U : prod == 1 ? gk::DO : gk::DU) + tq * kLS;
         float acc[8][4] = {};
         float dgam = 0.f;
-#pragma unroll
-        for (int jb = 0; jb < 8; ++jb) {
+#pragma unroll 1
+        for (int jb = 0; jb < 8; ++jb) {  // kept rolled: the body is large (instruction-fetch stalls)
             cp_async_wait(7 - jb);  // groups 0 .. jb have landed
             __syncthreads();
             if (jb == 4) {  // the token inputs read after the products: into L2 now, one 128-byte line each
