@@ -110,3 +110,36 @@ def test_backward_extreme_decays(g, decay):
         assert np.isfinite(x).all(), name
         e = max_rel_err(x, ref[name])
         assert e < TOL["f32"], (name, e)
+
+
+def test_backward_chunked_matches_recurrent_at_the_bench_shape(g):
+    """The bench workload's shapes (B 2, T 32768, H_k 16, H_v 32, bf16 tensors): the chunked path against
+    the per-token recurrent path, two fp32 computations that share no arithmetic; errors are normwise
+    over each whole output, computed on the device."""
+    import torch
+
+    B, T, Hk, Hv, d = 2, 32768, 16, 32, 128
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(2024)
+    rnd = lambda *s: torch.randn(s, generator=gen, device="cuda")
+    bf = torch.bfloat16
+    q = torch.nn.functional.normalize(rnd(B, T, Hk, d), dim=-1).to(bf)
+    k = torch.nn.functional.normalize(rnd(B, T, Hk, d), dim=-1).to(bf)
+    v, d_o = rnd(B, T, Hv, d).to(bf), rnd(B, T, Hv, d).to(bf)
+    gg = (-torch.nn.functional.softplus(rnd(B, T, Hv, d))).to(bf)
+    bb = torch.sigmoid(rnd(B, T, Hv, d)).to(bf)
+    ww = torch.sigmoid(rnd(B, T, Hv, d)).to(bf)
+    s0 = 0.02 * rnd(B, Hv, d, d)
+    ds_t = 0.1 * rnd(B, Hv, d, d)
+    a = g.backward(q, k, v, gg, bb, ww, d_o, s0, ds_t)
+    torch.cuda.synchronize()
+    assert g.gdn2_last_device_status() == g.GDN2_OK
+    r = g.backward(q, k, v, gg, bb, ww, d_o, s0, ds_t, recurrent=True)
+    torch.cuda.synchronize()
+    assert g.gdn2_last_device_status() == g.GDN2_OK
+    for name, x, y in zip(("dq", "dk", "dv", "dg", "db", "dw", "ds0"), a, r):
+        x, y = x.float(), y.float()
+        assert torch.isfinite(x).all(), name
+        e = ((x - y).abs().max() / y.abs().max()).item()
+        print(f"{name}: {e:.2e}")
+        assert e < 1e-2, (name, e)
