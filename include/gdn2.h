@@ -245,8 +245,8 @@ gdn2_status gdn2_mixer_epilogue(const void* o, const void* z, const float* weigh
  * gdn2_backward -- gradients of the core (dq, dk, dv, dg, db, dw and the initial state) for the
  * recurrence of the burn-gdn2 0.1.5 docs ("Architecture"), given the upstream gradient d_o of o
  * and optionally d_final_state of S_T: the gradients of sum(o * d_o) + sum(S_T * d_final_state).
- * Reverse mode of the chunked (WY / UT) form of the same recurrence ("Gated Delta Networks:
- * Improving Mamba2 with Delta Rule", section 3.3), in fp32 with chunks of 32 tokens, in five
+ * Reverse mode of the chunked WY form of the same recurrence (burn-gdn2 0.1.5 docs, "chunked WY
+ * decomposition (training)"), in fp32 with chunks of 32 tokens, in five
  * launches: the state-independent factors of every chunk (with T = (I + A)^-1); a forward chain
  * that keeps each chunk's starting state S_n and its U; a backward chain that keeps dS_(n+1) and dU;
  * one CTA per (chunk, batch, value head) that forms every per-token gradient of its chunk from those;
