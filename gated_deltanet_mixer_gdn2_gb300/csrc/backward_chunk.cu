@@ -21,6 +21,7 @@
 // one 512-thread CTA per SM); the sums of dq, dk over each key head's group. Within a chunk the pair
 // factors e^{G_t - G_s} of tokens in different 8-token blocks are split at a block edge into two
 // factors <= 1.
+#include <mutex>
 #include <type_traits>
 
 #include "common.cuh"
@@ -878,6 +879,27 @@ __global__ void __launch_bounds__(256) group_sum2_kernel(const float* __restrict
     }
 }
 
+// A second stream per device for the backward chain, which runs beside the forward chain (both only
+// read the factors and write disjoint buffers), between a fork and a join event on the caller's stream.
+constexpr int kMaxDevices = 64;
+struct SideStream {
+    cudaStream_t stream = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+};
+std::mutex g_side_mu;
+SideStream g_side[kMaxDevices];
+
+cudaError_t side_stream(int dev, SideStream** out) {
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    SideStream& x = g_side[dev];
+    cudaError_t e;
+    if (!x.stream && (e = cudaStreamCreateWithFlags(&x.stream, cudaStreamNonBlocking)) != cudaSuccess) return e;
+    if (!x.fork && (e = cudaEventCreateWithFlags(&x.fork, cudaEventDisableTiming)) != cudaSuccess) return e;
+    if (!x.join && (e = cudaEventCreateWithFlags(&x.join, cudaEventDisableTiming)) != cudaSuccess) return e;
+    *out = &x;
+    return cudaSuccess;
+}
+
 struct ChunkBwdLayout {
     size_t simt, t, s, u, ds, du, dq, dk, total;
 };
@@ -924,11 +946,24 @@ cudaError_t launch_t(const void* q, const void* k, const void* v, const void* g,
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(grad_kernel<Tin>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)g_smem);
     if (e != cudaSuccess) return e;
-    save_chain_kernel<<<dim3(B * Hv, kD / kSl), kCT, c_smem, s>>>(simt, s0, s_save, u_save, NC);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    adjoint_kernel<Tin><<<dim3(B * Hv, kD / kSl), kCT, a_smem, s>>>(simt, static_cast<const Tin*>(d_o), dsT, ds0,
-                                                                   ds_save, du_save, T, Hv, NC, scale);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    {   // the two chains side by side: the forward one on the caller's stream, the backward one on the side
+        // stream between a fork and a join (the enqueueing is serialised per process so that the events
+        // can be reused)
+        int dev = 0;
+        if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+        std::lock_guard<std::mutex> lock(g_side_mu);
+        SideStream* side = nullptr;
+        if ((e = side_stream(dev, &side)) != cudaSuccess) return e;
+        if ((e = cudaEventRecord(side->fork, s)) != cudaSuccess) return e;
+        if ((e = cudaStreamWaitEvent(side->stream, side->fork, 0)) != cudaSuccess) return e;
+        save_chain_kernel<<<dim3(B * Hv, kD / kSl), kCT, c_smem, s>>>(simt, s0, s_save, u_save, NC);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        adjoint_kernel<Tin><<<dim3(B * Hv, kD / kSl), kCT, a_smem, side->stream>>>(
+            simt, static_cast<const Tin*>(d_o), dsT, ds0, ds_save, du_save, T, Hv, NC, scale);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        if ((e = cudaEventRecord(side->join, side->stream)) != cudaSuccess) return e;
+        if ((e = cudaStreamWaitEvent(s, side->join, 0)) != cudaSuccess) return e;
+    }
     grad_kernel<Tin><<<dim3(NC, B * Hv), kGT, g_smem, s>>>(
         static_cast<const Tin*>(q), static_cast<const Tin*>(k), static_cast<const Tin*>(v), static_cast<const Tin*>(g),
         static_cast<const Tin*>(b), static_cast<const Tin*>(w), static_cast<const Tin*>(d_o), t_ws, s_save, u_save,

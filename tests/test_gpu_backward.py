@@ -143,3 +143,39 @@ def test_backward_chunked_matches_recurrent_at_the_bench_shape(g):
         e = ((x - y).abs().max() / y.abs().max()).item()
         print(f"{name}: {e:.2e}")
         assert e < 1e-2, (name, e)
+
+
+def test_backward_in_a_cuda_graph(g):
+    """The chunked backward forks its second chain onto a side stream and joins it back: captured in a
+    CUDA graph and replayed, it gives the same gradients as the eager call."""
+    import torch
+
+    T = 100
+    wl = synth.Workload("bwd-graph", B=1, T=T, Hk=1, Hv=2, dk=128, dv=128, dtype="bf16", seed=9, s0_std=0.02)
+    inp = synth.make_inputs(wl)
+    dev = lambda a: synth.to_torch(np.ascontiguousarray(a), "bf16", "cuda")
+    ts = [dev(getattr(inp, n)) for n in ("q", "k", "v", "g", "b", "w")]
+    d_o = dev(np.random.default_rng(1).standard_normal((1, T, 2, 128)))
+    s0 = H.state_to_device(inp.s0)
+    eager = g.backward(*ts, d_o, s0)
+    torch.cuda.synchronize()
+    outs = [torch.empty_like(t) for t in ts]
+    ds0 = torch.empty_like(s0)
+    ws = torch.empty(g.lib.gdn2_backward_workspace_size(1, T, 1, 2, 128, 128, g.GDN2_BF16), dtype=torch.uint8,
+                     device="cuda")
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(stream):  # warm-up outside the capture
+        g.gdn2_backward(*ts, d_o, *outs, s0, None, ds0, workspace=ws, stream=stream)
+    torch.cuda.current_stream().wait_stream(stream)
+    torch.cuda.synchronize()
+    for o in outs:
+        o.zero_()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        g.gdn2_backward(*ts, d_o, *outs, s0, None, ds0, workspace=ws, stream=torch.cuda.current_stream())
+    graph.replay()
+    torch.cuda.synchronize()
+    assert g.gdn2_last_device_status() == g.GDN2_OK
+    for name, x, y in zip(("dq", "dk", "dv", "dg", "db", "dw", "ds0"), (*outs, ds0), eager):
+        assert torch.equal(x, y), name
