@@ -89,9 +89,10 @@ size_t gdn2_chunk_fwd_workspace_size_path(gdn2_path path, int B, int T, int Hk, 
  * T need not be a multiple of C (the last chunk is padded with tokens that leave the state
  * unchanged). T == 0 or B == 0 is valid: o is untouched and final_state receives initial_state (or
  * zeros). Supported: d_k, d_v multiples of 16 in [16, 128] (SIMT, fp32 or bf16); bf16 with
- * d_k = d_v = 128 and C = 64 (TCGEN05); B * H_v <= 65535 (GDN2_ERR_UNSUPPORTED beyond). Within one chunk the per-channel cumulative log-decay must
- * span less than about 160 (alpha above about exp(-2.5) per token on average) on the TCGEN05 path;
- * beyond that its decay factors leave the fp32 exponent range.
+ * d_k = d_v = 128 and C = 64 (TCGEN05); B * H_v <= 65535 (GDN2_ERR_UNSUPPORTED beyond). Within one
+ * chunk the per-channel cumulative log-decay must span less than about 160 (alpha above about
+ * exp(-2.5) per token on average) on the TCGEN05 path; beyond that its decay factors leave the fp32
+ * exponent range.
  */
 gdn2_status gdn2_chunk_fwd(const void* q, const void* k, const void* v, const void* g,
                            const void* b, const void* w, const float* initial_state,
@@ -258,7 +259,10 @@ gdn2_status gdn2_mixer_epilogue(const void* o, const void* z, const float* weigh
  * (zeros / not written). dq and dk of a key head sum its value heads. d_k = d_v = 128,
  * B * H_v <= 65535 (GDN2_ERR_UNSUPPORTED otherwise).
  * workspace: gdn2_backward_workspace_size(...) bytes of device memory, 16-byte aligned.
- * Errors: as gdn2_chunk_fwd. Asynchronous on `stream`.
+ * Errors: as gdn2_chunk_fwd. Asynchronous on `stream`: the backward chain runs on a library-owned
+ * stream of the current device between an event recorded on `stream` and one that `stream` then
+ * waits for, so the call stays ordered on `stream` and can be captured in a CUDA graph (enqueueing
+ * from several host threads is serialised inside the library).
  */
 size_t gdn2_backward_workspace_size(int B, int T, int Hk, int Hv, int dk, int dv, gdn2_dtype dt);
 gdn2_status gdn2_backward(const void* q, const void* k, const void* v, const void* g, const void* b, const void* w,
