@@ -261,8 +261,9 @@ gdn2_status gdn2_mixer_epilogue(const void* o, const void* z, const float* weigh
  * workspace: gdn2_backward_workspace_size(...) bytes of device memory, 16-byte aligned.
  * Errors: as gdn2_chunk_fwd. Asynchronous on `stream`: the backward chain runs on a library-owned
  * stream of the current device between an event recorded on `stream` and one that `stream` then
- * waits for, so the call stays ordered on `stream` and can be captured in a CUDA graph (enqueueing
- * from several host threads is serialised inside the library).
+ * waits for, so the call stays ordered on `stream` and can be captured in a CUDA graph (the first
+ * call on a device creates that stream and its events: make it before capturing). Enqueueing from
+ * several host threads is serialised inside the library.
  */
 size_t gdn2_backward_workspace_size(int B, int T, int Hk, int Hv, int dk, int dv, gdn2_dtype dt);
 gdn2_status gdn2_backward(const void* q, const void* k, const void* v, const void* g, const void* b, const void* w,
