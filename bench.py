@@ -73,6 +73,12 @@ def chunk_flops(wl) -> int:
     return wl.B * wl.T * wl.Hv * (wl.C * (3 * wl.dk + 2 * wl.dv) + 6 * wl.dk * wl.dv)
 
 
+def backward_flops(tokens: int, Hv: int, d: int) -> int:
+    """Flops the backward is counted at: the recurrent form's forward (4 d^2 FMA) and backward (9 d^2 FMA)
+    per token and value head, 2 flops per FMA."""
+    return 26 * d * d * tokens * Hv
+
+
 def decode_step_bytes(B, Hk, Hv, dk, dv) -> int:
     """State read + write, token inputs, output; bf16 tokens, fp32 state."""
     return 2 * B * Hv * dk * dv * 4 + B * (2 * Hk * dk + Hv * (2 * dk + 2 * dv)) * 2 + B * Hv * dv * 2
@@ -416,7 +422,7 @@ def next_rows_rooflines(g, device, hbm, wl):
     e1.record(stream)
     torch.cuda.synchronize(device)
     ms = e0.elapsed_time(e1) / 2
-    flops = 26 * d * d * tok * Hv   # forward (4 d^2 FMA) + backward (9 d^2 FMA) per token and head
+    flops = backward_flops(tok, Hv, d)
     sms = torch.cuda.get_device_properties(device).multi_processor_count
     peak_tf = sms * 128 * 2 * 2.07e9 / 1e12          # fp32 lanes x FMA x max SM clock
     ach = flops / (ms * 1e-3) / 1e12
