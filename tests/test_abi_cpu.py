@@ -39,6 +39,30 @@ def test_every_declared_symbol_is_exported(g):
     assert set(g.EXPORTS) == set(_declared_functions())
 
 
+def _declared_arity():
+    """Parameter count of every prototype in include/gdn2.h."""
+    src = open(os.path.join(ROOT, "include", "gdn2.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", "", src)
+    out = {}
+    for m in re.finditer(r"\b(gdn2_[a-z0-9_]+)\s*\(", src):
+        depth, i = 1, m.end()
+        while depth:
+            depth += {"(": 1, ")": -1}.get(src[i], 0)
+            i += 1
+        params = src[m.end():i - 1].strip()
+        if src[i:].lstrip().startswith(";"):  # a prototype, not a use inside another declaration
+            out[m.group(1)] = 0 if params in ("", "void") else params.count(",") + 1
+    return out
+
+
+def test_binding_signatures_match_the_header(g):
+    arity = _declared_arity()
+    assert set(arity) == set(g.EXPORTS)
+    for fn, n in arity.items():
+        assert len(getattr(g.lib, fn).argtypes) == n, (fn, n, len(getattr(g.lib, fn).argtypes))
+
+
 def test_status_strings(g):
     for s in range(0, -7, -1):
         assert g.status_string(s) and g.status_string(s) != "unknown status"
