@@ -20,6 +20,15 @@
 // channel-major copies of W and k . e^{G_last - G}; there the chains of backward_chunk.cu replace the
 // state kernel.
 // Padding: tokens past T read as zeros (k = q = b = v = w = 0, g = 0), which leaves S unchanged.
+//
+// Decay factors over the whole domain alpha in [0, 1] (g = log alpha in [-inf, 0]): g is first
+// clamped at -100 (alpha = e^{-100} ~ 4e-44, which no fp32 result can tell from 0), so a full reset
+// (g = -inf) stays finite. The exponent of every factor is then formed from 16-token blocks of the
+// chunk: L_t = the inclusive prefix of g within t's block, S_B = the sum over block B. For tokens
+// i >= j in blocks I >= J,
+//     G_i - G_j = L_i - L_j + W_IJ,    W_IJ = S_J + sum_{J < B < I} S_B   (0 when I = J),
+// so no exponent is the difference of two long prefixes: values stay small unless the factor itself
+// is negligible, and no factor can overflow (every exponent is <= 0).
 #include "common.cuh"
 
 namespace gdn2 {
@@ -49,13 +58,18 @@ __global__ void __launch_bounds__(kFactorThreads) factors_simt_kernel(const Tin*
     const int tid = threadIdx.x, nt = blockDim.x;
     const int LD = dk + 1;
     const int LDQ = (dk > dv ? dk : dv) + 1;
-    float* sG = smem;                        // [C][LD]   cumulative log-decay
+    const int nb = C / 16;                   // 16-token blocks of the chunk
+    float* sG = smem;                        // [C][LD]   g, then L: inclusive prefix within the 16-token block
     float* sK = sG + C * LD;                 // [C][LD]   k
     float* sBK = sK + C * LD;                // [C][LD]   b . k, later b . k . e^{G}
     float* sQ = sBK + C * LD;                // [C][LDQ]  q, later w . v
     float* sA = sQ + C * LDQ;                // [C][C+1]
     float* sT = sA + C * (C + 1);            // [C][C+1]
     float* sX = sQ;                          // [16][C] block products of the inverse (q is read out by then)
+    float* sS = sT + C * (C + 1);            // [nb][dk]  block sums S_B
+    float* sPre = sS + nb * dk;              // [nb][dk]  sum of the blocks before B (G at the start of B)
+    float* sSuf = sPre + nb * dk;            // [nb][dk]  sum of the blocks after B
+    float* sW = sSuf + nb * dk;              // [1 + nb(nb-1)/2][dk]  W_IJ (row 0: zeros, for I = J)
 
     const SimtWs L{dk, dv, C, imajor != 0};
     float* u = ws + ((size_t)bh * NC + n) * L.unit_floats();
@@ -96,14 +110,36 @@ __global__ void __launch_bounds__(kFactorThreads) factors_simt_kernel(const Tin*
         }
     }
     __syncthreads();
-    // inclusive cumulative log-decay per key channel, and the chunk decay e^{G_last}
+    // per key channel: L (prefix within each 16-token block) of the clamped gates, the block sums,
+    // the sums before / after each block and between block pairs, and the chunk decay e^{G_last}
     for (int c = tid; c < dk; c += nt) {
-        float acc = 0.f;
-        for (int t = 0; t < C; ++t) {
-            acc += sG[t * LD + c];
-            sG[t * LD + c] = acc;
+        for (int B = 0; B < nb; ++B) {
+            float acc = 0.f;
+            for (int t = 16 * B; t < 16 * B + 16; ++t) {
+                acc += fmaxf(sG[t * LD + c], kGateFloor);
+                sG[t * LD + c] = acc;
+            }
+            sS[B * dk + c] = acc;
         }
-        u[L.off_gam() + c] = __expf(acc);
+        float pre = 0.f;
+        for (int B = 0; B < nb; ++B) {
+            sPre[B * dk + c] = pre;
+            pre += sS[B * dk + c];
+        }
+        float suf = 0.f;
+        for (int B = nb - 1; B >= 0; --B) {
+            sSuf[B * dk + c] = suf;
+            suf += sS[B * dk + c];
+        }
+        sW[c] = 0.f;
+        for (int I = 1; I < nb; ++I) {
+            float z = 0.f;  // sum of the blocks strictly between J and I
+            for (int J = I - 1; J >= 0; --J) {
+                sW[(1 + I * (I - 1) / 2 + J) * dk + c] = sS[J * dk + c] + z;
+                z += sS[J * dk + c];
+            }
+        }
+        u[L.off_gam() + c] = __expf(pre);
     }
     __syncthreads();
     // erase interaction A (strictly lower) and causal q-k M (lower incl. diagonal): one thread per pair
@@ -122,9 +158,11 @@ __global__ void __launch_bounds__(kFactorThreads) factors_simt_kernel(const Tin*
         while ((i + 1) * (i + 2) / 2 <= p) ++i;
         while (i * (i + 1) / 2 > p) --i;
         const int j = p - i * (i + 1) / 2;
+        const int I = i >> 4, J = j >> 4;
+        const float* wr = sW + (I == J ? 0 : 1 + I * (I - 1) / 2 + J) * dk;
         float a = 0.f, m = 0.f;
         for (int c = 0; c < dk; ++c) {
-            const float e = __expf(sG[i * LD + c] - sG[j * LD + c]);  // G_i - G_j <= 0
+            const float e = __expf(sG[i * LD + c] - sG[j * LD + c] + wr[c]);  // G_i - G_j <= 0
             const float kj = sK[j * LD + c] * e;
             a = fmaf(sBK[i * LD + c], kj, a);
             m = fmaf(sQ[i * LDQ + c], kj, m);
@@ -157,14 +195,15 @@ __global__ void __launch_bounds__(kFactorThreads) factors_simt_kernel(const Tin*
         int c, i;
         if (imajor) i = p / dk, c = p - i * dk;
         else c = p / C, i = p - c * C;
-        const float Gi = sG[i * LD + c];
-        u[L.off_qbt() + p] = sQ[i * LDQ + c] * __expf(Gi);
-        u[L.off_kht() + p] = sK[i * LD + c] * __expf(sG[(C - 1) * LD + c] - Gi);
+        const float Li = sG[i * LD + c];
+        const int Bi = i >> 4;
+        u[L.off_qbt() + p] = sQ[i * LDQ + c] * __expf(Li + sPre[Bi * dk + c]);                        // e^{G_i}
+        u[L.off_kht() + p] = sK[i * LD + c] * __expf(sS[Bi * dk + c] - Li + sSuf[Bi * dk + c]);     // e^{G_last - G_i}
     }
     if (imajor)  // channel-major copy of k.e^{G_last-G}
         for (int p = tid - C; p >= 0 && p < dk * C; p += nt - C) {
-            const int c = p / C, i = p - c * C;
-            u[L.off_kht2() + p] = sK[i * LD + c] * __expf(sG[(C - 1) * LD + c] - sG[i * LD + c]);
+            const int c = p / C, i = p - c * C, Bi = i >> 4;
+            u[L.off_kht2() + p] = sK[i * LD + c] * __expf(sS[Bi * dk + c] - sG[i * LD + c] + sSuf[Bi * dk + c]);
         }
     __syncthreads();
     for (int r = 16; r < C; r += 16) {
@@ -185,7 +224,7 @@ __global__ void __launch_bounds__(kFactorThreads) factors_simt_kernel(const Tin*
     }
     for (int idx = tid; idx < C * dk; idx += nt) {
         const int t = idx / dk, c = idx - t * dk;
-        sBK[t * LD + c] *= __expf(sG[t * LD + c]);
+        sBK[t * LD + c] *= __expf(sG[t * LD + c] + sPre[(t >> 4) * dk + c]);
     }
 #pragma unroll 2
     for (int idx = tid; idx < C * dv / 8; idx += nt) {
@@ -328,8 +367,9 @@ __global__ void __launch_bounds__(256) state_simt_kernel(const float* __restrict
 }
 
 size_t factors_smem(int dk, int dv, int C) {
-    const int LD = dk + 1, LDQ = (dk > dv ? dk : dv) + 1;
-    return sizeof(float) * ((size_t)3 * C * LD + (size_t)C * LDQ + 2 * (size_t)C * (C + 1));
+    const int LD = dk + 1, LDQ = (dk > dv ? dk : dv) + 1, nb = C / 16;
+    const size_t blk = (size_t)(3 * nb + 1 + nb * (nb - 1) / 2) * dk;  // S, before, after, W
+    return sizeof(float) * ((size_t)3 * C * LD + (size_t)C * LDQ + 2 * (size_t)C * (C + 1) + blk);
 }
 size_t state_smem(int dk, int C) {
     return sizeof(float) * ((size_t)dk * kSlice + 3 * (size_t)dk * C + (size_t)C * C + (size_t)kSlice * C + dk +

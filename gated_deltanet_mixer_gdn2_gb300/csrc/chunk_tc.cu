@@ -14,6 +14,11 @@
 // Kernel 1 "factors" (grid: chunks x heads; 256 threads; 3 CTAs/SM): TMA loads q, k, g, b of one
 // chunk, one pass computes the decayed operands, tcgen05 forms A|M, CUDA cores invert (I + A),
 // tcgen05 forms W; -W, q.e^G, k.e^{G_last-G}, M, T and e^{G_last} go to the workspace.
+// The gates are floored at kGateFloor (alpha = e^{-100}: a full reset, g = -inf, stays finite). A
+// chunk in which some channel's log-decay spans more than kSpanAnchored cannot use one anchor per
+// channel (its factors would leave bf16's range): kernel 1 lists it and kernel 1b "exact" forms that
+// unit on CUDA cores with one factor e^{G_i - G_j} <= 1 per entry, so the whole domain alpha in
+// [0, 1] is covered.
 // Kernel 2 "state" (grid: 2 x batch x value heads; warp-specialised; sequential over chunks): the
 // columns of S evolve independently, so each CTA runs the recurrence for 64 of the d_v columns with
 // the fp32 state in registers, 128-row products over tokens or d_k, and the bf16 state and U as
@@ -31,6 +36,12 @@ __device__ int g_status_tc;
 
 constexpr int kC = 64;
 constexpr int kD = 128;
+
+// Largest per-channel span G_0 - G_last of the (floored) cumulative log-decay within one chunk that
+// the anchored operands take: every factor then lies in [e^-60, e^60], far inside bf16's range
+// (operands down to |x| ~ 1e-12 keep their value after the e^-60 scaling). Wider chunks go to the
+// exact kernel.
+constexpr float kSpanAnchored = 120.f;
 
 // workspace unit (one chunk of one value head), bytes
 constexpr uint32_t kWsW = 0;         // -W = -T (b.k.e^G)    token-major [64][128] bf16
@@ -180,9 +191,64 @@ __device__ __forceinline__ void tile24_store(float* D, int ldd, const float (&ac
         *reinterpret_cast<float4*>(D + i * ldd) = make_float4(sgn * acc[i][0], sgn * acc[i][1], sgn * acc[i][2], sgn * acc[i][3]);
 }
 
+// T = (I + A)^{-1} for a strictly lower triangular 64 x 64 A (fp32 shared memory, rows LDF floats
+// apart; T's scratch must hold zeros above its diagonal blocks on entry), by blocks: (1) the four
+// 16x16 diagonal blocks by forward substitution (warps 0-3, one column per lane); (2) the two 16x16
+// blocks below them inside each 32x32 diagonal block, T_{i+1,i} = -D_{i+1} A_{i+1,i} D_i; (3) the
+// 32x32 block below the diagonal, T_10 = -T_11 A_10 T_00. Called by all 256 threads of the block;
+// PF is a [32][LDP] fp32 scratch.
+__device__ __forceinline__ void invert_unit_lower64(const float* AF, float* TF, float* PF, int warp, int lane) {
+    if (warp < 4 && lane < 16) {
+        const int base = 16 * warp, jj = lane;
+        float x[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            float s = 0.f;
+#pragma unroll
+            for (int l = 0; l < i; ++l) s = fmaf(AF[(base + i) * fs::LDF + base + l], x[l], s);
+            x[i] = (i == jj) ? 1.f : ((i < jj) ? 0.f : -s);
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) TF[(base + i) * fs::LDF + base + jj] = x[i];
+    }
+    __syncthreads();
+    // Products below run as 2 x 4 register tiles (each 16-byte load feeds 8 FMAs; 64 or 128 threads
+    // share a product, which measured faster than 4 x 4 tiles on fewer threads or 1 x 4 on all 8
+    // warps). A skipped k-range multiplies entries of a lower triangular factor that are exactly
+    // zero, so bounds stay warp-uniform and the sums are unchanged.
+    if (warp < 2) {  // Y_i = A_{i+1,i} D_i for diagonal blocks i = 0, 2 (warp = block, 2 x 4 tiles)
+        const int i0 = 32 * warp, r0 = 2 * (lane >> 2), c0 = 4 * (lane & 3);
+        float acc[2][4] = {};
+        tile24_times(AF + (i0 + 16 + r0) * fs::LDF + i0, fs::LDF, TF + i0 * fs::LDF + i0 + c0, fs::LDF, 0, 4, acc);
+        tile24_store(PF + (16 * warp + r0) * fs::LDP + c0, fs::LDP, acc, 1.f);
+    }
+    __syncthreads();
+    if (warp < 2) {  // T_{i+1,i} = -D_{i+1} Y_i
+        const int i1 = 32 * warp + 16, r0 = 2 * (lane >> 2), c0 = 4 * (lane & 3);
+        float acc[2][4] = {};
+        tile24_times(TF + (i1 + r0) * fs::LDF + i1, fs::LDF, PF + 16 * warp * fs::LDP + c0, fs::LDP, 0, 4, acc);
+        tile24_store(TF + (i1 + r0) * fs::LDF + i1 - 16 + c0, fs::LDF, acc, -1.f);
+    }
+    __syncthreads();
+    if (warp < 4) {  // X = A_10 T_00: warp w takes columns 8w.. (2 x 4 tiles)
+        const int r0 = 2 * (lane >> 1), c0 = 8 * warp + 4 * (lane & 1);
+        float acc[2][4] = {};
+        tile24_times(AF + (32 + r0) * fs::LDF, fs::LDF, TF + c0, fs::LDF, 2 * warp, 8, acc);
+        tile24_store(PF + r0 * fs::LDP + c0, fs::LDP, acc, 1.f);
+    }
+    __syncthreads();
+    if (warp < 4) {  // T_10 = -T_11 X: warp w takes rows 8w.. (2 x 4 tiles)
+        const int r0 = 8 * warp + 2 * (lane >> 3), c0 = 4 * (lane & 7);
+        float acc[2][4] = {};
+        tile24_times(TF + (32 + r0) * fs::LDF + 32, fs::LDF, PF + c0, fs::LDP, 0, 2 * (warp + 1), acc);
+        tile24_store(TF + (32 + r0) * fs::LDF + c0, fs::LDF, acc, -1.f);
+    }
+    __syncthreads();
+}
+
 __global__ void __launch_bounds__(fs::kThreads, 3)
-    factors_tc_kernel(const __grid_constant__ FactorMaps maps, uint8_t* __restrict__ ws, int Hk, int Hv, int NC,
-                      long long wait_ns) {
+    factors_tc_kernel(const __grid_constant__ FactorMaps maps, uint8_t* __restrict__ ws, int* __restrict__ exact_list,
+                      int Hk, int Hv, int NC, long long wait_ns) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(sm);
@@ -244,13 +310,14 @@ __global__ void __launch_bounds__(fs::kThreads, 3)
             for (int r = 0; r < 4; ++r) {
                 unpack8(*reinterpret_cast<const uint4*>(pG + off(4 * tg + r)), x);
 #pragma unroll
-                for (int i = 0; i < 8; ++i) L[r][i] = (r ? L[r - 1][i] : 0.f) + x[i];
+                for (int i = 0; i < 8; ++i) L[r][i] = (r ? L[r - 1][i] : 0.f) + fmaxf(x[i], kGateFloor);
             }
             float4* dst = reinterpret_cast<float4*>(s_gs + tg * 128 + 8 * j);
             dst[0] = make_float4(L[3][0], L[3][1], L[3][2], L[3][3]);
             dst[1] = make_float4(L[3][4], L[3][5], L[3][6], L[3][7]);
         }
         __syncthreads();
+        bool wide = false;  // this channel's log-decay spans more than the anchored form can hold
         if (tid < 128) {  // exclusive prefix over the 16 token groups, per channel
             const int c = tid;
             float part[16];
@@ -262,15 +329,22 @@ __global__ void __launch_bounds__(fs::kThreads, 3)
                 s_gs[q * 128 + c] = run;
                 run += part[q];
             }
-            const float g0 = __bfloat162float(
-                *reinterpret_cast<const __nv_bfloat16*>(sm + fs::G + (c >> 6) * 8192 + sw128_off(0, c & 63)));
+            const float g0 = fmaxf(__bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(
+                                       sm + fs::G + (c >> 6) * 8192 + sw128_off(0, c & 63))),
+                                   kGateFloor);
             const float a = 0.5f * (g0 + run);  // G_0 and G_last bracket G when log-decays are <= 0
+            wide = g0 - run > kSpanAnchored;
             s_anc[c] = a;
             s_ea[c] = __expf(a);
             s_ela[c] = __expf(run - a);
             reinterpret_cast<float*>(unit + kWsGam)[c] = __expf(run);
         }
-        __syncthreads();
+        // A channel whose log-decay spans more than kSpanAnchored would need factors beyond
+        // e^{+-kSpanAnchored/2}: the exact kernel forms this unit instead (it is listed and skipped).
+        const bool exact = __syncthreads_or(wide) != 0;
+        if (exact && tid == 0) exact_list[1 + atomicAdd(exact_list, 1)] = unit_idx;
+        if (exact) ok = false;
+        if (!exact) {
         {
             float pa[8], ea[8], ela[8];  // per channel: G_{group start} - a, e^{a}, e^{G_last - a}
             {
@@ -345,6 +419,7 @@ __global__ void __launch_bounds__(fs::kThreads, 3)
             mma_commit(bar_mma);
         }
         ok = cta_wait(bar_mma, 0, wait_ns, flag);
+        }
     }
     if (ok) {
         tc_fence_after();
@@ -387,56 +462,7 @@ __global__ void __launch_bounds__(fs::kThreads, 3)
             tma_store_3d(&maps.m_st, sm + fs::SGS, 0, 0, unit_idx);
             bulk_commit();
         }
-        // ---- T = (I + A)^{-1}, blocked: (1) the four 16x16 diagonal blocks by forward substitution
-        //      (warps 0-3, one column per lane); (2) the two 16x16 blocks below them inside each
-        //      32x32 diagonal block, T_{i+1,i} = -D_{i+1} A_{i+1,i} D_i; (3) the 32x32 block below
-        //      the diagonal, T_10 = -T_11 A_10 T_00.
-        if (warp < 4 && lane < 16) {
-            const int base = 16 * warp, jj = lane;
-            float x[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                float s = 0.f;
-#pragma unroll
-                for (int l = 0; l < i; ++l) s = fmaf(AF[(base + i) * fs::LDF + base + l], x[l], s);
-                x[i] = (i == jj) ? 1.f : ((i < jj) ? 0.f : -s);
-            }
-#pragma unroll
-            for (int i = 0; i < 16; ++i) TF[(base + i) * fs::LDF + base + jj] = x[i];
-        }
-        __syncthreads();
-        // Products below run as 2 x 4 register tiles (each 16-byte load feeds 8 FMAs; 64 or 128 threads
-        // share a product, which measured faster than 4 x 4 tiles on fewer threads or 1 x 4 on all 8
-        // warps). A skipped k-range multiplies entries of a lower triangular factor that are exactly
-        // zero, so bounds stay warp-uniform and the sums are unchanged.
-        if (warp < 2) {  // Y_i = A_{i+1,i} D_i for diagonal blocks i = 0, 2 (warp = block, 2 x 4 tiles)
-            const int i0 = 32 * warp, r0 = 2 * (lane >> 2), c0 = 4 * (lane & 3);
-            float acc[2][4] = {};
-            tile24_times(AF + (i0 + 16 + r0) * fs::LDF + i0, fs::LDF, TF + i0 * fs::LDF + i0 + c0, fs::LDF, 0, 4, acc);
-            tile24_store(PF + (16 * warp + r0) * fs::LDP + c0, fs::LDP, acc, 1.f);
-        }
-        __syncthreads();
-        if (warp < 2) {  // T_{i+1,i} = -D_{i+1} Y_i
-            const int i1 = 32 * warp + 16, r0 = 2 * (lane >> 2), c0 = 4 * (lane & 3);
-            float acc[2][4] = {};
-            tile24_times(TF + (i1 + r0) * fs::LDF + i1, fs::LDF, PF + 16 * warp * fs::LDP + c0, fs::LDP, 0, 4, acc);
-            tile24_store(TF + (i1 + r0) * fs::LDF + i1 - 16 + c0, fs::LDF, acc, -1.f);
-        }
-        __syncthreads();
-        if (warp < 4) {  // X = A_10 T_00: warp w takes columns 8w.. (2 x 4 tiles)
-            const int r0 = 2 * (lane >> 1), c0 = 8 * warp + 4 * (lane & 1);
-            float acc[2][4] = {};
-            tile24_times(AF + (32 + r0) * fs::LDF, fs::LDF, TF + c0, fs::LDF, 2 * warp, 8, acc);
-            tile24_store(PF + r0 * fs::LDP + c0, fs::LDP, acc, 1.f);
-        }
-        __syncthreads();
-        if (warp < 4) {  // T_10 = -T_11 X: warp w takes rows 8w.. (2 x 4 tiles)
-            const int r0 = 8 * warp + 2 * (lane >> 3), c0 = 4 * (lane & 7);
-            float acc[2][4] = {};
-            tile24_times(TF + (32 + r0) * fs::LDF + 32, fs::LDF, PF + c0, fs::LDP, 0, 2 * (warp + 1), acc);
-            tile24_store(TF + (32 + r0) * fs::LDF + c0, fs::LDF, acc, -1.f);
-        }
-        __syncthreads();
+        invert_unit_lower64(AF, TF, PF, warp, lane);
         for (int p = tid; p < 64 * 8; p += fs::kThreads) {  // bf16 T, K-major rows (one 16-byte chunk per item)
             const int i = p >> 3, c8 = p & 7;
             float y[8];
@@ -497,6 +523,169 @@ __global__ void __launch_bounds__(fs::kThreads, 3)
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, 128);
+}
+
+// ---------------------------------------------------------------------------------------------
+// kernel 1b: exact factors of the units whose decay spans more than the anchored form holds
+//
+// Same outputs as the factor kernel (the workspace unit: -W, q.e^G, k.e^{G_last-G}, M, T, e^{G_last}),
+// formed in fp32 on CUDA cores without any anchor: every entry of A and M takes its own factor
+// e^{G_i - G_j} (i >= j, at most 1), every other factor is e^{G} or e^{G_last - G} (at most 1), so
+// nothing can overflow whatever the decay, and a full reset (g = -inf, floored at kGateFloor) gives
+// factors that are exactly or negligibly 0. A persistent grid walks the list the factor kernel
+// wrote (count, then unit indices).
+
+namespace xs {  // shared memory of the exact kernel (fp32 unless noted)
+constexpr int LD = 132;                           // token rows of 128 channels, padded
+constexpr uint32_t G = 0;                         // [64][LD] inclusive cumulative log-decay (floored)
+constexpr uint32_t BK = G + 64 * LD * 4;          // [64][LD] b.k, later b.k.e^G
+constexpr uint32_t Q = BK + 64 * LD * 4;          // [64][LD] q
+constexpr uint32_t K = Q + 64 * LD * 4;           // [64][LD] k
+constexpr uint32_t AF = K + 64 * LD * 4;          // [64][LDF] A (strictly lower)
+constexpr uint32_t MF = AF + 64 * fs::LDF * 4;    // [64][LDF] M (lower incl. the diagonal)
+constexpr uint32_t TF = MF + 64 * fs::LDF * 4;    // [64][LDF] T
+constexpr uint32_t PF = TF + 64 * fs::LDF * 4;    // [32][LDP] inverse scratch
+constexpr uint32_t TOTAL = PF + 32 * fs::LDP * 4;
+constexpr int kThreads = 256;
+}  // namespace xs
+
+__global__ void __launch_bounds__(xs::kThreads, 1)
+    factors_exact_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
+                         const __nv_bfloat16* __restrict__ g, const __nv_bfloat16* __restrict__ b,
+                         uint8_t* __restrict__ ws, const int* __restrict__ exact_list, int T, int Hk, int Hv, int NC) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+    float* sG = reinterpret_cast<float*>(sm + xs::G);
+    float* sBK = reinterpret_cast<float*>(sm + xs::BK);
+    float* sQ = reinterpret_cast<float*>(sm + xs::Q);
+    float* sK = reinterpret_cast<float*>(sm + xs::K);
+    float* AF = reinterpret_cast<float*>(sm + xs::AF);
+    float* MF = reinterpret_cast<float*>(sm + xs::MF);
+    float* TF = reinterpret_cast<float*>(sm + xs::TF);
+    float* PF = reinterpret_cast<float*>(sm + xs::PF);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int count = exact_list[0];
+
+    for (int li = blockIdx.x; li < count; li += gridDim.x) {
+        const int unit_idx = exact_list[1 + li];
+        const int bh = unit_idx / NC, n = unit_idx - bh * NC;
+        const int bi = bh / Hv, hv = bh - bi * Hv, hk = hv / (Hv / Hk);
+        uint8_t* unit = ws + static_cast<size_t>(unit_idx) * kWsUnit;
+        __syncthreads();  // the previous unit's shared-memory readers are done
+        // token tiles (zeros past T), 8 channels per item
+        for (int p = tid; p < 64 * 16; p += xs::kThreads) {
+            const int t = p >> 4, c = 8 * (p & 15), tok = n * kC + t;
+            float gg[8], bb[8], kk[8], qq[8];
+            if (tok < T) {
+                const size_t kq = ((static_cast<size_t>(bi) * T + tok) * Hk + hk) * kD + c;
+                const size_t gb = ((static_cast<size_t>(bi) * T + tok) * Hv + hv) * kD + c;
+                unpack8(*reinterpret_cast<const uint4*>(g + gb), gg);
+                unpack8(*reinterpret_cast<const uint4*>(b + gb), bb);
+                unpack8(*reinterpret_cast<const uint4*>(k + kq), kk);
+                unpack8(*reinterpret_cast<const uint4*>(q + kq), qq);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) gg[i] = bb[i] = kk[i] = qq[i] = 0.f;
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                sG[t * xs::LD + c + i] = fmaxf(gg[i], kGateFloor);
+                sBK[t * xs::LD + c + i] = bb[i] * kk[i];
+                sK[t * xs::LD + c + i] = kk[i];
+                sQ[t * xs::LD + c + i] = qq[i];
+            }
+        }
+        for (int p = tid; p < 64 * fs::LDF; p += xs::kThreads) {
+            AF[p] = 0.f;
+            MF[p] = 0.f;
+            TF[p] = 0.f;
+        }
+        __syncthreads();
+        if (tid < 128) {  // inclusive cumulative log-decay of channel tid, and e^{G_last}
+            float run = 0.f;
+            for (int t = 0; t < kC; ++t) {
+                run += sG[t * xs::LD + tid];
+                sG[t * xs::LD + tid] = run;
+            }
+            reinterpret_cast<float*>(unit + kWsGam)[tid] = __expf(run);
+        }
+        __syncthreads();
+        // A (j < i) and M (j <= i): one thread per pair, pairs numbered along the lower triangle
+        for (int p = tid; p < kC * (kC + 1) / 2; p += xs::kThreads) {
+            int i = static_cast<int>((sqrtf(8.f * p + 1.f) - 1.f) * 0.5f);
+            while ((i + 1) * (i + 2) / 2 <= p) ++i;
+            while (i * (i + 1) / 2 > p) --i;
+            const int j = p - i * (i + 1) / 2;
+            const float4* gi = reinterpret_cast<const float4*>(sG + i * xs::LD);
+            const float4* gj = reinterpret_cast<const float4*>(sG + j * xs::LD);
+            const float4* bki = reinterpret_cast<const float4*>(sBK + i * xs::LD);
+            const float4* qi = reinterpret_cast<const float4*>(sQ + i * xs::LD);
+            const float4* kj = reinterpret_cast<const float4*>(sK + j * xs::LD);
+            float a = 0.f, m = 0.f;
+#pragma unroll 4
+            for (int c4 = 0; c4 < 32; ++c4) {
+                const float4 Gi = gi[c4], Gj = gj[c4], B4 = bki[c4], Q4 = qi[c4], K4 = kj[c4];
+                const float f0 = K4.x * __expf(Gi.x - Gj.x), f1 = K4.y * __expf(Gi.y - Gj.y);
+                const float f2 = K4.z * __expf(Gi.z - Gj.z), f3 = K4.w * __expf(Gi.w - Gj.w);
+                a = fmaf(B4.x, f0, fmaf(B4.y, f1, fmaf(B4.z, f2, fmaf(B4.w, f3, a))));
+                m = fmaf(Q4.x, f0, fmaf(Q4.y, f1, fmaf(Q4.z, f2, fmaf(Q4.w, f3, m))));
+            }
+            if (j < i) AF[i * fs::LDF + j] = a;
+            MF[i * fs::LDF + j] = m;
+        }
+        __syncthreads();
+        invert_unit_lower64(AF, TF, PF, warp, lane);
+        // b.k.e^{G}, then W = T (b.k.e^G): thread = (token row i, 4 channels), the row's T entries shared
+        // by the warp
+        for (int p = tid; p < 64 * 32; p += xs::kThreads) {
+            const int t = p >> 5, c = 4 * (p & 31);
+            float4* x = reinterpret_cast<float4*>(sBK + t * xs::LD + c);
+            const float4 G4 = *reinterpret_cast<const float4*>(sG + t * xs::LD + c);
+            float4 v = *x;
+            v.x *= __expf(G4.x); v.y *= __expf(G4.y); v.z *= __expf(G4.z); v.w *= __expf(G4.w);
+            *x = v;
+        }
+        __syncthreads();
+        for (int p = tid; p < 64 * 16; p += xs::kThreads) {
+            const int i = p >> 4, c = 8 * (p & 15);
+            float acc[8] = {};
+            for (int l = 0; l <= i; ++l) {
+                const float tl = TF[i * fs::LDF + l];
+                const float4 x0 = *reinterpret_cast<const float4*>(sBK + l * xs::LD + c);
+                const float4 x1 = *reinterpret_cast<const float4*>(sBK + l * xs::LD + c + 4);
+                acc[0] = fmaf(tl, x0.x, acc[0]); acc[1] = fmaf(tl, x0.y, acc[1]);
+                acc[2] = fmaf(tl, x0.z, acc[2]); acc[3] = fmaf(tl, x0.w, acc[3]);
+                acc[4] = fmaf(tl, x1.x, acc[4]); acc[5] = fmaf(tl, x1.y, acc[5]);
+                acc[6] = fmaf(tl, x1.z, acc[6]); acc[7] = fmaf(tl, x1.w, acc[7]);
+            }
+            float y[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) y[e] = -acc[e];  // stored negated
+            *reinterpret_cast<uint4*>(unit + kWsW + i * 256 + c * 2) = pack8(y);
+            // decayed q and k of the same token and channels
+            float qb[8], kh[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const float Gi = sG[i * xs::LD + c + e];
+                qb[e] = sQ[i * xs::LD + c + e] * __expf(Gi);
+                kh[e] = sK[i * xs::LD + c + e] * __expf(sG[(kC - 1) * xs::LD + c + e] - Gi);
+            }
+            *reinterpret_cast<uint4*>(unit + kWsQb + i * 256 + c * 2) = pack8(qb);
+            *reinterpret_cast<uint4*>(unit + kWsKh + i * 256 + c * 2) = pack8(kh);
+        }
+        // M and T as bf16 [64][64] rows (zeros above their diagonals)
+        for (int p = tid; p < 64 * 8; p += xs::kThreads) {
+            const int i = p >> 3, c = 8 * (p & 7);
+            float ym[8], yt[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                ym[e] = (c + e <= i) ? MF[i * fs::LDF + c + e] : 0.f;
+                yt[e] = (c + e <= i) ? TF[i * fs::LDF + c + e] : 0.f;
+            }
+            *reinterpret_cast<uint4*>(unit + kWsM + i * 128 + c * 2) = pack8(ym);
+            *reinterpret_cast<uint4*>(unit + kWsT + i * 128 + c * 2) = pack8(yt);
+        }
+    }
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -1116,8 +1305,11 @@ bool ws_map(CUtensorMap* m, const void* p, CUtensorMapDataType dt, int esize, in
 
 }  // namespace
 
+// Workspace: the 66 048-byte units, (batch . value head, chunk) order, then the list of units that
+// the exact kernel forms: a count and up to one int32 index per unit.
 size_t chunk_tc_workspace_bytes(const ChunkShape& sh) {
-    return static_cast<size_t>(kWsUnit) * sh.nchunks() * sh.B * sh.Hv;
+    const size_t units = static_cast<size_t>(sh.nchunks()) * sh.B * sh.Hv;
+    return static_cast<size_t>(kWsUnit) * units + align_up(sizeof(int) * (units + 1), 256);
 }
 
 cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const void* g, const void* b,
@@ -1147,13 +1339,28 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const v
 
     // The state kernel runs one CTA per SM, so it takes the whole 227 KB: operand descriptors can
     // then never reach past the CTA's own allocation.
-    const size_t f_smem = fs::TOTAL + 1024, s_smem = 232448;
+    const size_t f_smem = fs::TOTAL + 1024, x_smem = xs::TOTAL + 128, s_smem = 232448;
     static_assert(ss::TOTAL + 1024 <= 232448, "state kernel shared memory");
+    static_assert(xs::TOTAL + 128 <= 232448, "exact factor kernel shared memory");
     cudaError_t e = cudaFuncSetAttribute(factors_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)f_smem);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(factors_exact_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)x_smem);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(state_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s_smem);
     if (e != cudaSuccess) return e;
-    factors_tc_kernel<<<dim3(NC, sh.B * sh.Hv), fs::kThreads, f_smem, s>>>(fm, wsb, sh.Hk, sh.Hv, NC, wait_ns);
+    int dev = 0, nsm = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    int* exact_list = reinterpret_cast<int*>(wsb + static_cast<size_t>(kWsUnit) * units);
+    if ((e = cudaMemsetAsync(exact_list, 0, sizeof(int), s)) != cudaSuccess) return e;
+    factors_tc_kernel<<<dim3(NC, sh.B * sh.Hv), fs::kThreads, f_smem, s>>>(fm, wsb, exact_list, sh.Hk, sh.Hv, NC,
+                                                                         wait_ns);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    factors_exact_kernel<<<units < nsm ? units : nsm, xs::kThreads, x_smem, s>>>(
+        static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
+        static_cast<const __nv_bfloat16*>(g), static_cast<const __nv_bfloat16*>(b), wsb, exact_list, sh.T, sh.Hk,
+        sh.Hv, NC);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     state_tc_kernel<<<dim3(2 * sh.B * sh.Hv), ss::kThreads, s_smem, s>>>(sm_, wsb, s0, sT, sh.Hv, NC, scale,

@@ -17,6 +17,11 @@ constexpr long long kDefaultWaitNs = 2000000000LL;
 // Device status bits (one word per translation unit, read and cleared by the host).
 constexpr int kStatusTimeout = 1;
 
+// Floor applied to the log-decay g by the chunked kernels: alpha = e^{-100} ~ 3.7e-44 is below
+// every fp32 quantity those kernels form from it, so a full reset (g = -inf, alpha = 0) gives the
+// same results while every cumulative sum of gates stays finite.
+constexpr float kGateFloor = -100.f;
+
 template <typename T>
 __device__ __forceinline__ float to_f32(T x);
 template <>

@@ -16,10 +16,11 @@
 // address is then passed to the existing chunked-forward launchers like any workspace pointer.
 // Nothing here calls cudaMalloc, cudaFree or an allocating library routine.
 //
-// Sharing: every call uses the same array and the array keeps the last call's contents. The
-// kernels overwrite every workspace byte they read within a call, so nothing needs clearing; but
-// calls whose kernels overlap on the GPU (different streams, or different host threads on one
-// device) race on the array.
+// Sharing: every call uses the same array and the array keeps the last call's contents. Within a
+// call the kernels write every workspace byte before they read it, except the tensor-core path's
+// count of chunks for its exact kernel, which the launcher clears on the call's stream first; so
+// the caller clears nothing. Calls whose kernels overlap on the GPU (different streams, or
+// different host threads on one device) race on the array.
 #include <mutex>
 
 #include "common.cuh"

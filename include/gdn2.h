@@ -19,9 +19,10 @@
  *   - Token dtype: GDN2_F32 (float) or GDN2_BF16 (bfloat16) for q, k, v, g, b, w and o. States
  *     are always fp32. Arithmetic is fp32 (the bf16 chunked path feeds bf16 operands to the
  *     tensor cores with fp32 accumulation).
- *   - g is log(alpha) (expected <= 0, not checked); b is the erase gate after its activation, with
- *     values in (0, 2) when negative eigenvalues are allowed (the caller doubles it); w is the write
- *     gate after its activation.
+ *   - g is log(alpha) with alpha in [0, 1]: g <= 0, -inf included (a full reset of that key
+ *     channel; not checked). b is the erase gate after its activation, with values in (0, 2) when
+ *     negative eigenvalues are allowed (the caller doubles it); w is the write gate after its
+ *     activation.
  *   - Streams: `stream` is a cudaStream_t passed as void* (NULL = legacy default stream). Every
  *     entry point only enqueues work: it returns without synchronising the host.
  *   - Errors: entry points never abort, trap or print. Argument errors are detected on the host
@@ -83,16 +84,23 @@ size_t gdn2_chunk_fwd_workspace_size_path(gdn2_path path, int B, int T, int Hk, 
  *   final_state    [B, H_v, d_k, d_v] fp32, may be NULL (not written); may alias initial_state
  *   o              [B, T, H_v, d_v]  dt (output)
  *   C              chunk length: 64 on the tensor-core path; 16, 32 or 64 on the SIMT path
- *   workspace      device buffer of at least gdn2_chunk_fwd_workspace_size(...) bytes, 256-byte
- *                  aligned; its contents on entry are ignored and on return are unspecified
+ *   workspace      device buffer of at least gdn2_chunk_fwd_workspace_size(...) bytes, 16-byte
+ *                  aligned (GDN2_ERR_MISALIGNED otherwise); its contents on entry are ignored and
+ *                  on return are unspecified, except as noted below for the TCGEN05 path
  *
  * T need not be a multiple of C (the last chunk is padded with tokens that leave the state
  * unchanged). T == 0 or B == 0 is valid: o is untouched and final_state receives initial_state (or
  * zeros). Supported: d_k, d_v multiples of 16 in [16, 128] (SIMT, fp32 or bf16); bf16 with
- * d_k = d_v = 128 and C = 64 (TCGEN05); B * H_v <= 65535 (GDN2_ERR_UNSUPPORTED beyond). Within one
- * chunk the per-channel cumulative log-decay must span less than about 160 (alpha above about
- * exp(-2.5) per token on average) on the TCGEN05 path; beyond that its decay factors leave the fp32
- * exponent range.
+ * d_k = d_v = 128 and C = 64 (TCGEN05); B * H_v <= 65535 (GDN2_ERR_UNSUPPORTED beyond).
+ *
+ * Decay domain: any alpha in [0, 1] on both paths, including alpha = 0 (g = -inf) and decays that
+ * forget a whole chunk. Both paths floor g at -100 (alpha = e^-100 ~ 4e-44, indistinguishable from
+ * 0 in fp32) and form every decay factor so that it cannot overflow. On the TCGEN05 path a
+ * (chunk, value head) whose per-channel log-decay spans more than 120 within the chunk (more than
+ * about 1.9 per token on average) is formed by an exact CUDA-core kernel instead of the tensor-core
+ * factor kernel: same results, slower for those chunks. Diagnostic: after the call completes, the
+ * int32 at byte offset 66048 * ceil(T / 64) * B * H_v of the workspace holds the number of such
+ * chunks.
  */
 gdn2_status gdn2_chunk_fwd(const void* q, const void* k, const void* v, const void* g,
                            const void* b, const void* w, const float* initial_state,
@@ -119,8 +127,9 @@ gdn2_status gdn2_chunk_fwd_path(gdn2_path path, const void* q, const void* k, co
  *     one 66 048-byte unit per chunk and value head: at most 508 of them).
  *   - Set-up: the first call on a device looks up the array's device address (with that device
  *     current) and caches it; make that first call before any stream capture.
- *   - Sharing: all calls share the array and it keeps the last call's contents (nothing in it needs
- *     to start at zero); calls whose kernels overlap on the GPU race on it.
+ *   - Sharing: all calls share the array and it keeps the last call's contents (the call itself
+ *     clears, on its stream, the one word that must start at zero); calls whose kernels overlap on
+ *     the GPU race on it.
  * Other arguments, errors and results: as gdn2_chunk_fwd (AUTO path).
  */
 gdn2_status gdn2_chunk_fwd_noalloc(const void* q, const void* k, const void* v, const void* g,

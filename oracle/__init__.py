@@ -106,3 +106,18 @@ def max_rel_err(x, ref) -> float:
     if den == 0.0:
         return num
     return num / den
+
+
+def max_rel_err_elementwise(x, ref, floor_frac: float = 1e-3) -> float:
+    """Largest element-by-element relative error max_i |x_i - ref_i| / max(|ref_i|, floor), with the
+    floor floor_frac * max|ref| (so elements near zero are measured against a small fraction of the
+    tensor's scale rather than against themselves)."""
+    x = np.asarray(x, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    if not ref.size:
+        return 0.0
+    scale = float(np.max(np.abs(ref)))
+    if scale == 0.0:
+        return float(np.max(np.abs(x - ref)))
+    den = np.maximum(np.abs(ref), floor_frac * scale)
+    return float(np.max(np.abs(x - ref) / den))

@@ -10,6 +10,13 @@ Recipe. Each (workload seed, tensor, batch index, head) slab has its own numpy P
   q, k  ~ N(0,1), L2-normalised over d_k per (token, head)        [B, T, H_k, d_k]
   v     ~ N(0,1)                                                    [B, T, H_v, d_v]
   g     = -softplus(N(0,1))   (log alpha, one per key channel)      [B, T, H_v, d_k]
+          decay variants (the whole domain alpha in [0, 1]):
+            "strong": -softplus(N(3,1)) (about -3 per token, a 64-token chunk spans ~195)
+            "bursts": the standard draw, plus runs of 8 tokens at g = -20 starting at each
+                      (token, channel) with probability 1/8192 (about one run per 64 x 128
+                      chunk, so chunks with and without a run alternate)
+            "reset":  the standard draw, plus g = -inf (alpha = 0) at each (token, channel)
+                      with probability 1/32 and on every channel of tokens t = 50 (mod 97)
   b     = sigmoid(N(0,1)); 2*sigmoid(N(0,1)) when negative
           eigenvalues are allowed (the "b x 2" option)              [B, T, H_v, d_k]
   w     = sigmoid(N(0,1))                                           [B, T, H_v, d_v]
@@ -27,7 +34,8 @@ from dataclasses import dataclass, field, replace
 
 import numpy as np
 
-_TENSOR_ID = {"q": 1, "k": 2, "v": 3, "g": 4, "b": 5, "w": 6, "s0": 7}
+_TENSOR_ID = {"q": 1, "k": 2, "v": 3, "g": 4, "b": 5, "w": 6, "s0": 7, "g_extra": 8}
+DECAYS = ("standard", "strong", "bursts", "reset")
 
 
 @dataclass(frozen=True)
@@ -48,6 +56,7 @@ class Workload:
     neg_eigval: bool = False
     decode_steps: int = 0  # single-token steps after the chunked forward
     description: str = ""
+    decay: str = "standard"  # distribution of g (see DECAYS and the module docstring)
 
     @property
     def tokens_total(self) -> int:
@@ -122,15 +131,37 @@ def _sigmoid(x):
     return 0.5 * (1.0 + np.tanh(0.5 * x))
 
 
+def _decay_slab(x: np.ndarray, decay: str, seed: int, bi: int, h: int) -> np.ndarray:
+    """g = log alpha from the standard-normal draw x [T, d] for one decay variant."""
+    if decay == "strong":
+        return -_softplus(x + 3.0)
+    g = -_softplus(x)
+    if decay == "standard":
+        return g
+    T, d = x.shape
+    u = _rng(seed, "g_extra", bi, h).random((T, d))
+    if decay == "bursts":
+        start = u < 1.0 / 8192.0
+        burst = np.zeros((T, d), bool)
+        for s in range(8):
+            burst[s:] |= start[:T - s]
+        return np.where(burst, -20.0, g)
+    if decay == "reset":
+        g = np.where(u < 1.0 / 32.0, -np.inf, g)
+        g[np.arange(T) % 97 == 50] = -np.inf
+        return g
+    raise ValueError(decay)
+
+
 def slab(seed: int, name: str, bi: int, h: int, T: int, d: int, dtype: str,
-         neg_eigval: bool = False) -> np.ndarray:
+         neg_eigval: bool = False, decay: str = "standard") -> np.ndarray:
     """One [T, d] slab of token tensor `name` for batch index bi and head h (float32 values)."""
     x = _rng(seed, name, bi, h).standard_normal((T, d))
     if name in ("q", "k"):
         nrm = np.sqrt(np.sum(x * x, axis=1, keepdims=True))
         x = x / np.where(nrm > 0, nrm, 1.0)
     elif name == "g":
-        x = -_softplus(x)
+        x = _decay_slab(x, decay, seed, bi, h)
     elif name == "b":
         x = _sigmoid(x) * (2.0 if neg_eigval else 1.0)
     elif name == "w":
@@ -212,7 +243,7 @@ def make_inputs(wl: Workload, T: int | None = None, dtype: str | None = None, b0
 
     def run(job):
         name, arr, bi, h, d = job
-        arr[bi, :, h, :] = slab(wl.seed, name, b0 + bi, h, T, d, dtype, wl.neg_eigval)
+        arr[bi, :, h, :] = slab(wl.seed, name, b0 + bi, h, T, d, dtype, wl.neg_eigval, wl.decay)
 
     with ThreadPoolExecutor(_threads()) as ex:
         list(ex.map(run, jobs))
@@ -232,7 +263,7 @@ def make_head_inputs(wl: Workload, bi: int, hv: int, T: int | None = None) -> In
     """
     T = wl.tokens_total if T is None else T
     hk = hv // (wl.Hv // wl.Hk)
-    f = lambda name, h, d: slab(wl.seed, name, bi, h, T, d, wl.dtype, wl.neg_eigval)[None, :, None, :]
+    f = lambda name, h, d: slab(wl.seed, name, bi, h, T, d, wl.dtype, wl.neg_eigval, wl.decay)[None, :, None, :]
     s0 = None
     if wl.s0_std > 0:
         s0 = state_slab(wl.seed, bi, hv, wl.dk, wl.dv, wl.s0_std)[None, None]

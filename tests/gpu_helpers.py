@@ -14,6 +14,33 @@ def tol_for(dtype: str) -> float:
     return BF16_TOL if dtype == "bf16" else F32_TOL
 
 
+def check(name: str, got, ref, tol: float, head_axis: int | None = 2) -> str:
+    """Parity of a CUDA result with the oracle's: finite, normwise max relative error <= tol over the
+    whole tensor and, when head_axis is given, over every (batch, head) slice on its own (a bad head
+    of small magnitude cannot hide under the others). Returns a one-line report that also gives the
+    elementwise relative error with a floor of 1e-3 * max|ref| (reported, not bounded: near-zero
+    elements of bf16 results carry the rounding of much larger ones)."""
+    import oracle
+
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert got.shape == ref.shape, f"{name}: shape {got.shape} != {ref.shape}"
+    assert np.isfinite(got).all(), f"{name}: non-finite values"
+    err = oracle.max_rel_err(got, ref)
+    ele = oracle.max_rel_err_elementwise(got, ref)
+    assert err <= tol, f"{name}: max rel err {err:.3e} > {tol:.1e} (elementwise {ele:.3e})"
+    worst = 0.0
+    if head_axis is not None and got.ndim == 4:
+        g2 = np.moveaxis(got, head_axis, 1)
+        r2 = np.moveaxis(ref, head_axis, 1)
+        for bi in range(g2.shape[0]):
+            for h in range(g2.shape[1]):
+                e = oracle.max_rel_err(g2[bi, h], r2[bi, h])
+                assert e <= tol, f"{name}: head ({bi}, {h}) max rel err {e:.3e} > {tol:.1e}"
+                worst = max(worst, e)
+    return f"{name}: normwise {err:.2e}, worst head {worst:.2e}, elementwise (floor 1e-3 max) {ele:.2e}"
+
+
 def upload(inp: synth.Inputs, t0: int, t1: int, device="cuda"):
     """Token tensors for tokens [t0, t1) as device tensors of the storage dtype."""
     sl = lambda a: np.ascontiguousarray(a[:, t0:t1])

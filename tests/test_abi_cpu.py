@@ -70,10 +70,15 @@ def test_status_strings(g):
 
 
 def test_workspace_sizes(g):
-    # tensor-core path: one 66048-byte unit per (chunk, batch, value head)
-    assert g.gdn2_chunk_fwd_workspace_size(2, 32768, 16, 32, 128, 128, 64, g.GDN2_BF16) == 66048 * 512 * 64
+    # tensor-core path: one 66048-byte unit per (chunk, batch, value head), then the exact kernel's list
+    # (a count and one int32 per unit, rounded up to 256 bytes)
+    tail = lambda units: -(-4 * (units + 1) // 256) * 256
+    assert g.gdn2_chunk_fwd_workspace_size(2, 32768, 16, 32, 128, 128, 64, g.GDN2_BF16) == \
+        66048 * 512 * 64 + tail(512 * 64)
     # ragged tail rounds the chunk count up
-    assert g.gdn2_chunk_fwd_workspace_size(1, 65, 1, 1, 128, 128, 64, g.GDN2_BF16) == 66048 * 2
+    assert g.gdn2_chunk_fwd_workspace_size(1, 65, 1, 1, 128, 128, 64, g.GDN2_BF16) == 66048 * 2 + 256
+    # the no-alloc entry point's 32 MiB array holds exactly 508 units and their list
+    assert 66048 * 508 + tail(508) == 32 << 20
     # fp32 goes to the SIMT path: (3 dk C + C^2 + dv C + dk) floats, rounded to 4
     n = 3 * 64 * 64 + 64 * 64 + 64 * 64 + 64
     assert g.gdn2_chunk_fwd_workspace_size(1, 256, 4, 4, 64, 64, 64, g.GDN2_F32) == 4 * n * 4 * 4

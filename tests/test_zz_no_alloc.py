@@ -5,7 +5,8 @@ serving loop must not call cudaMalloc / cudaFree, which can block or synchronise
 the library offers a chunked forward that uses its own fixed 32 MiB device array instead of a
 caller workspace. This test calls that entry point directly through the C ABI, twice in a row with
 different problems, and checks each result against the workspace entry point on the same inputs
-(same tolerance as the parity tests). It lives in a file of its own that pytest collects last.
+and against the fp64 oracle (same tolerance as the parity tests). It lives in a file of its own that
+pytest collects last.
 """
 import ctypes
 
@@ -58,6 +59,9 @@ def test_noalloc_matches_workspace_entry_point(first, second):
         assert oracle.max_rel_err(H.to_np(o), H.to_np(o_ref)) <= tol
         assert oracle.max_rel_err(sT.cpu().numpy(), s_ref.cpu().numpy()) <= tol
         assert np.isfinite(H.to_np(o)).all()
+        o_or, s_or = oracle.run_inputs(inp)
+        H.check("o (no-alloc) vs oracle", H.to_np(o), o_or, tol)
+        H.check("state (no-alloc) vs oracle", sT.cpu().numpy(), s_or, tol, head_axis=1)
 
 
 def test_noalloc_rejects_problems_beyond_its_array():
