@@ -16,13 +16,14 @@ cudaError_t launch_selftest_umma(int case_id, int soft, const void* a_st, const 
 
 namespace {
 
+// Tensor-core path: d_k = 128; the state kernel runs one CTA per 64 columns of d_v.
 bool tc_shape(const ChunkShape& sh, gdn2_dtype dt) {
-    return dt == GDN2_BF16 && sh.dk == 128 && sh.dv == 128 && sh.C == 64;
+    return dt == GDN2_BF16 && sh.dk == 128 && sh.dv % 64 == 0 && sh.dv >= 64 && sh.dv <= 512 && sh.C == 64;
 }
 
 bool simt_shape(const ChunkShape& sh) {
-    auto okd = [](int d) { return d >= 16 && d <= 128 && d % 16 == 0; };
-    return okd(sh.dk) && okd(sh.dv) && (sh.C == 16 || sh.C == 32 || sh.C == 64);
+    auto okd = [](int d, int hi) { return d >= 16 && d <= hi && d % 16 == 0; };
+    return okd(sh.dk, 128) && okd(sh.dv, 256) && (sh.C == 16 || sh.C == 32 || sh.C == 64);
 }
 
 // Resolve AUTO; returns GDN2_PATH_AUTO when the requested path cannot run this shape.

@@ -1,5 +1,5 @@
 // chunk_tc.cu -- chunked forward on the 5th-generation tensor cores (tcgen05 + TMA + TMEM), bf16
-// inputs, d_k = d_v = 128, chunk C = 64.
+// inputs, d_k = 128, d_v a multiple of 64 (up to 512), chunk C = 64.
 //
 // Same chunked WY / UT form as the SIMT path (burn-gdn2 0.1.5 docs: "chunked WY decomposition
 // (training)"); per chunk of C tokens entering with state S_n, G_i = inclusive cumulative
@@ -80,6 +80,42 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<const uint32_t*>(&v);
 }
 
+
+// Packed fp32x2 arithmetic (two channels per instruction) and bf16 pair conversions.
+constexpr float kLog2e = 1.4426950408889634f;
+__device__ __forceinline__ uint64_t f32x2(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f32x2_split(uint64_t a, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(a));
+}
+__device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+__device__ __forceinline__ float ex2_approx(float x) {  // 2^x, the hardware approximation
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+// two bf16 (low half = first) -> fp32 pair: a bf16 is the upper half of its fp32
+__device__ __forceinline__ uint64_t bf16x2_widen(uint32_t u) {
+    return f32x2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
+}
+// fp32 pair -> two bf16 (round to nearest even), first value in the low half
+__device__ __forceinline__ uint32_t bf16x2_narrow(uint64_t a) {
+    float lo, hi;
+    f32x2_split(a, lo, hi);
+    return pack_bf16x2(lo, hi);
+}
 
 // 64 fp32 columns of this warp's TMEM lanes starting at column `col`.
 __device__ __forceinline__ void tmem_ld64(uint32_t tmem_base, int warp, int col, float (&x)[64]) {
@@ -346,7 +382,8 @@ __global__ void __launch_bounds__(fs::kThreads, 3)
         if (exact) ok = false;
         if (!exact) {
         {
-            float pa[8], ea[8], ela[8];  // per channel: G_{group start} - a, e^{a}, e^{G_last - a}
+            // per channel: (G_{group start} - a) log2(e), e^{a}, e^{G_last - a}, as channel pairs
+            uint64_t pa2[4], ea2[4], ela2[4];
             {
                 const float4* p4 = reinterpret_cast<const float4*>(s_gs + tg * 128 + 8 * j);
                 const float4* a4 = reinterpret_cast<const float4*>(s_anc + 8 * j);
@@ -355,51 +392,72 @@ __global__ void __launch_bounds__(fs::kThreads, 3)
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     const float4 pp = p4[h], aa = a4[h], ee = e4[h], ll = l4[h];
-                    pa[4 * h] = pp.x - aa.x; pa[4 * h + 1] = pp.y - aa.y; pa[4 * h + 2] = pp.z - aa.z; pa[4 * h + 3] = pp.w - aa.w;
-                    ea[4 * h] = ee.x; ea[4 * h + 1] = ee.y; ea[4 * h + 2] = ee.z; ea[4 * h + 3] = ee.w;
-                    ela[4 * h] = ll.x; ela[4 * h + 1] = ll.y; ela[4 * h + 2] = ll.z; ela[4 * h + 3] = ll.w;
+                    pa2[2 * h] = f32x2((pp.x - aa.x) * kLog2e, (pp.y - aa.y) * kLog2e);
+                    pa2[2 * h + 1] = f32x2((pp.z - aa.z) * kLog2e, (pp.w - aa.w) * kLog2e);
+                    ea2[2 * h] = f32x2(ee.x, ee.y);
+                    ea2[2 * h + 1] = f32x2(ee.z, ee.w);
+                    ela2[2 * h] = f32x2(ll.x, ll.y);
+                    ela2[2 * h + 1] = f32x2(ll.z, ll.w);
                 }
             }
-            // each output is formed and stored before the next one, so that few values are live
+            const uint64_t log2e2 = f32x2(kLog2e, kLog2e);
+            // each output is formed and stored before the next one, so that few values are live;
+            // products run on channel pairs (packed fp32x2), bf16 inputs widen by shifts
 #pragma unroll
             for (int r = 0; r < 4; ++r) {
                 const int t = 4 * tg + r;
                 const int o = off(t);
-                float e1[8], e2[8], kk[8], y[8];
+                uint64_t e1[4], e2[4], kk[4], bk[4];
+                uint32_t y[4];
                 {
-                    float bb[8];
-                    unpack8(*reinterpret_cast<const uint4*>(pK + o), kk);
-                    unpack8(*reinterpret_cast<const uint4*>(pB + o), bb);
+                    const uint4 ku = *reinterpret_cast<const uint4*>(pK + o);
+                    const uint4 bu = *reinterpret_cast<const uint4*>(pB + o);
+                    const uint32_t kw[4] = {ku.x, ku.y, ku.z, ku.w}, bw[4] = {bu.x, bu.y, bu.z, bu.w};
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const float d = pa[i] + L[r][i];   // G - a
-                        e1[i] = __expf(d);                 // e^{G - a}
-                        e2[i] = __expf(-d);                // e^{a - G}
-                        bb[i] *= kk[i];                    // b.k
+                    for (int i = 0; i < 4; ++i) {
+                        // (G - a) log2(e) for channels 2i, 2i+1 of this token
+                        const uint64_t d = fma_f32x2(f32x2(L[r][2 * i], L[r][2 * i + 1]), log2e2, pa2[i]);
+                        float d0, d1;
+                        f32x2_split(d, d0, d1);
+                        e1[i] = f32x2(ex2_approx(d0), ex2_approx(d1));      // e^{G - a}
+                        e2[i] = f32x2(ex2_approx(-d0), ex2_approx(-d1));    // e^{a - G}
+                        kk[i] = bf16x2_widen(kw[i]);
+                        bk[i] = mul_f32x2(bf16x2_widen(bw[i]), kk[i]);      // b.k
                     }
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) y[i] = bb[i] * e1[i];
-                    *reinterpret_cast<uint4*>(pB + o) = pack8(y);
+                    for (int i = 0; i < 4; ++i) {
+                        const uint64_t kb_ = mul_f32x2(bk[i], e1[i]);       // b.k.e^{G-a}
+                        y[i] = bf16x2_narrow(kb_);
+                        bk[i] = mul_f32x2(kb_, ea2[i]);                     // b.k.e^{G}
+                    }
+                    *reinterpret_cast<uint4*>(pB + o) = make_uint4(y[0], y[1], y[2], y[3]);
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) y[i] = bb[i] * (e1[i] * ea[i]);  // b.k.e^{G}
-                    *reinterpret_cast<uint4*>(pG + o) = pack8(y);   // in place of g (same thread, same chunk)
+                    for (int i = 0; i < 4; ++i) y[i] = bf16x2_narrow(bk[i]);
+                    *reinterpret_cast<uint4*>(pG + o) = make_uint4(y[0], y[1], y[2], y[3]);  // in place of g
                 }
 #pragma unroll
-                for (int i = 0; i < 8; ++i) y[i] = kk[i] * e2[i];
-                *reinterpret_cast<uint4*>(pK + o) = pack8(y);
+                for (int i = 0; i < 4; ++i) {
+                    kk[i] = mul_f32x2(kk[i], e2[i]);                        // k.e^{a-G}
+                    y[i] = bf16x2_narrow(kk[i]);
+                }
+                *reinterpret_cast<uint4*>(pK + o) = make_uint4(y[0], y[1], y[2], y[3]);
 #pragma unroll
-                for (int i = 0; i < 8; ++i) y[i] = kk[i] * (e2[i] * ela[i]);      // k.e^{G_last - G}
-                *reinterpret_cast<uint4*>(unit + kWsKh + t * 256 + j * 16) = pack8(y);
+                for (int i = 0; i < 4; ++i) y[i] = bf16x2_narrow(mul_f32x2(kk[i], ela2[i]));  // k.e^{G_last - G}
+                *reinterpret_cast<uint4*>(unit + kWsKh + t * 256 + j * 16) = make_uint4(y[0], y[1], y[2], y[3]);
                 {
-                    float qq[8];
-                    unpack8(*reinterpret_cast<const uint4*>(pQ + o), qq);
+                    const uint4 qu = *reinterpret_cast<const uint4*>(pQ + o);
+                    const uint32_t qw[4] = {qu.x, qu.y, qu.z, qu.w};
+                    uint64_t qq[4];
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) y[i] = qq[i] * e1[i];
-                    *reinterpret_cast<uint4*>(pQ + o) = pack8(y);
+                    for (int i = 0; i < 4; ++i) {
+                        qq[i] = mul_f32x2(bf16x2_widen(qw[i]), e1[i]);      // q.e^{G-a}
+                        y[i] = bf16x2_narrow(qq[i]);
+                    }
+                    *reinterpret_cast<uint4*>(pQ + o) = make_uint4(y[0], y[1], y[2], y[3]);
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) y[i] = qq[i] * (e1[i] * ea[i]);  // q.e^{G}
+                    for (int i = 0; i < 4; ++i) y[i] = bf16x2_narrow(mul_f32x2(qq[i], ea2[i]));  // q.e^{G}
                     // decayed q and k, token-major rows of 256 bytes: one 16-byte chunk per thread
-                    *reinterpret_cast<uint4*>(unit + kWsQb + t * 256 + j * 16) = pack8(y);
+                    *reinterpret_cast<uint4*>(unit + kWsQb + t * 256 + j * 16) = make_uint4(y[0], y[1], y[2], y[3]);
                 }
             }
         }
@@ -723,11 +781,11 @@ constexpr uint32_t OST = UB + 8192;      // output staging [2 warps][32 tokens][
 constexpr uint32_t GAMC = OST + 8192;    // ring of e^{G_last}: [4 chunks][128] fp32, own barriers
 constexpr uint32_t BAR = GAMC + 2048;    // mbarriers, TMEM base, error flag
 constexpr uint32_t TOTAL = BAR + 256;
-constexpr int kChainWarps = 8;           // warps 0-7: U and state read-outs, decay
-constexpr int kOutWarps = 4;             // warps 8-11: w.v; warps 10-11 also read the output
+constexpr int kChainWarps = 4;           // warps 0-3: U and state read-outs, decay (64 columns each)
+constexpr int kOutWarps = 4;             // warps 4-7: w.v; warps 6-7 also read the output
 constexpr int kOutReaders = 2;
-constexpr int kProducer = 12, kIssuer = 13;
-constexpr int kThreads = 14 * 32;
+constexpr int kProducer = 8, kIssuer = 9;
+constexpr int kThreads = 10 * 32;
 // TMEM columns (lane = product row). D_UO[b] (b = chunk parity): lanes 0-63 hold U = T (w.v) - W S_n,
 // lanes 64-127 O = Q S_n + M U. D_S receives K^T U (lane = d_k row).
 constexpr uint32_t kDuo = 0, kDs = 128, kCols = 256;
@@ -788,23 +846,23 @@ __device__ __forceinline__ void tma_store_4d(const void* map, const void* src, i
                  : "memory");
 }
 
-// The chunk recurrence for 64 of the d_v columns, two CTAs per (batch, value head): the columns of S
+// The chunk recurrence for 64 of the d_v columns, d_v / 64 CTAs per (batch, value head): the columns of S
 // evolve independently, so each CTA keeps its d_k x 64 slice of the state. Per chunk n, with the
 // factors of the workspace,
 //   U = T (w.v) - W S_n,   O = Q S_n + M U,   S_{n+1} = diag(e^{G_last}) S_n + K^T U.
 // Every product has the 128 rows of M = 128: the token rows of [T ; 0], [-W ; Q] and [. ; M] put U and
 // O into the two lane halves of one accumulator, and d_k is the row side of K^T U. The fp32 state
-// stays in the registers of the eight chain warps (one d_k row, 32 columns per thread), where the
+// stays in the registers of the four chain warps (one d_k row, all 64 columns per thread), where the
 // decay is one scalar per row and K^T U is added from tensor memory; its bf16 copy and U are the B
 // operands in shared memory. The dependent chain per chunk is
 //   S_n -> [-W ; Q] S_n -> U -> + K^T U -> S_{n+1};
 // w.v, T (w.v), M U, the decay and the output run beside it. Roles: a TMA warp keeps both slots of
-// both rings in flight, an MMA warp issues (one lane), eight chain warps read U and the state, four
+// both rings in flight, an MMA warp issues (one lane), four chain warps read U and the state, four
 // warps form w.v and two of them read the output. They hand over through mbarriers; every wait is
 // bounded.
 __global__ void __launch_bounds__(ss::kThreads, 1)
     state_tc_kernel(const __grid_constant__ StateMaps maps, const uint8_t* __restrict__ ws,
-                    const float* __restrict__ s0, float* __restrict__ sT_out, int Hv, int NC, float scale,
+                    const float* __restrict__ s0, float* __restrict__ sT_out, int Hv, int dv, int NC, float scale,
                     long long wait_ns) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -818,15 +876,16 @@ __global__ void __launch_bounds__(ss::kThreads, 1)
     uint64_t* o_done = full_big + 12;                                // [2] O of D_UO[b] complete
     uint64_t* mma1_done = full_big + 14;                             // [-W ; Q] S_n complete
     uint64_t* s_done = full_big + 15;                                // K^T U complete
-    uint64_t* u_ready = full_big + 16;                               // U written (4 warps)
-    uint64_t* s_ready = full_big + 17;                               // bf16 S_n written (8 chain warps)
+    uint64_t* u_ready = full_big + 16;                               // U written (2 warps)
+    uint64_t* s_ready = full_big + 17;                               // bf16 S_n written (4 chain warps)
     uint64_t* drain = full_big + 18;
     uint64_t* gam_full = full_big + 19;                              // [4] e^{G_last} of chunk m landed
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + ss::BAR + 224);
     volatile int* err = reinterpret_cast<volatile int*>(sm + ss::BAR + 228);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int bh = blockIdx.x >> 1, hc = blockIdx.x & 1;  // (batch, value head), d_v column half
+    const int nslice = dv >> 6;                           // 64-column slices of d_v
+    const int bh = blockIdx.x / nslice, hc = blockIdx.x - bh * nslice;  // (batch, value head), d_v slice
     const int bi = bh / Hv, hv = bh - bi * Hv;
 
     if (tid == 0) {
@@ -977,7 +1036,7 @@ __global__ void __launch_bounds__(ss::kThreads, 1)
             mbar_wait(drain, 0, kDefaultWaitNs);
         }
     } else if (warp >= ss::kChainWarps) {
-        // ============== w.v (warps 8-11) and output read-out (warps 10-11) ==============
+        // ============== w.v (warps 4-7) and output read-out (warps 6-7) ==============
         const int q4 = warp & 3;                      // TMEM lane quarter
         const bool reader = q4 >= 2;                  // lanes 64-127: O rows = tokens 32 (q4 - 2) ..
         const int otid = tid - 32 * ss::kChainWarps;  // 0..127
@@ -1039,10 +1098,12 @@ __global__ void __launch_bounds__(ss::kThreads, 1)
         }
         if (reader && lane == 0) bulk_wait_all();  // the output is written before the block retires
     } else {
-        // ============= U and state read-outs, decay (warps 0-7) =============
-        // Each thread keeps its row and 32 columns of the fp32 state in registers, already multiplied
-        // by the next chunk's decay; the tensor core only forms K^T U.
-        const int q4 = warp & 3, half = warp >> 2;  // TMEM lane quarter; 32-column half of the 64
+        // ============= U and state read-outs, decay (warps 0-3) =============
+        // Each thread keeps its row and the CTA's 64 columns of the fp32 state in registers, already
+        // multiplied by the next chunk's decay; the tensor core only forms K^T U. One warp per TMEM
+        // lane quarter: measured faster than two or four warps per quarter with fewer columns each,
+        // since every extra warp is one more arrival on the barriers the MMA warp waits for.
+        const int q4 = warp & 3;                    // TMEM lane quarter; all 64 columns
         const bool u_reader = q4 < 2;               // lanes 0-63 of D_UO hold U
         const int r = 32 * q4 + lane;               // d_k row of D_S (= TMEM lane); token row of U
         const uint32_t lane_base = static_cast<uint32_t>(32 * q4) << 16;
@@ -1050,28 +1111,29 @@ __global__ void __launch_bounds__(ss::kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive1(bar);
         };
-        auto decay = [&](int m, float (&x)[32]) -> bool {  // x = e^{G_last(m)} . x for this thread's row
+        auto decay = [&](int m, float (&x)[64]) -> bool {  // x = e^{G_last(m)} . x for this thread's row
             if (!warp_wait(gam_full + (m & 3), (m >> 2) & 1, wait_ns, err)) return false;
             const float gg = reinterpret_cast<const float*>(sm + ss::GAMC)[(m & 3) * 128 + r];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) x[j] *= gg;
+            for (int j = 0; j < 64; ++j) x[j] *= gg;
             return true;
         };
         uint8_t* sbt = sm + ss::SB;
         uint8_t* ubt = sm + ss::UB;
-        const size_t srow = (static_cast<size_t>(bh) * kD + r) * kD + 64 * hc + 32 * half;
-        float sx[32];  // e^{G_last(n)} . S_n
+        const size_t srow = (static_cast<size_t>(bh) * kD + r) * dv + 64 * hc;
+        float sx[64];  // e^{G_last(n)} . S_n
         bool ok = NC > 0;
         if (ok) {
 #pragma unroll
-            for (int j4 = 0; j4 < 8; ++j4) {
+            for (int j4 = 0; j4 < 16; ++j4) {
                 const float4 f = s0 ? reinterpret_cast<const float4*>(s0 + srow)[j4] : make_float4(0.f, 0.f, 0.f, 0.f);
                 sx[4 * j4] = f.x;
                 sx[4 * j4 + 1] = f.y;
                 sx[4 * j4 + 2] = f.z;
                 sx[4 * j4 + 3] = f.w;
             }
-            st_row_bf16x32(sbt, r, 4 * half, sx);
+            st_row_bf16x32(sbt, r, 0, sx);
+            st_row_bf16x32(sbt, r, 4, sx + 32);
             fence_proxy_async_smem();
             arrive(s_ready);
             ok = decay(0, sx);
@@ -1081,9 +1143,10 @@ __global__ void __launch_bounds__(ss::kThreads, 1)
             if (u_reader) {
                 if (!(ok = warp_wait(mma1_done, n & 1, wait_ns, err))) break;
                 tc_fence_after();
-                float x[32];  // U: token row r, this thread's 32 columns -> bf16 B operand
-                tmem_ld_cols<2>(tmem + lane_base + ss::kDuo + 64 * st + 32 * half, x);
-                st_row_bf16x32(ubt, r, 4 * half, x);
+                float x[64];  // U: token row r, all 64 columns -> bf16 B operand
+                tmem_ld_cols<4>(tmem + lane_base + ss::kDuo + 64 * st, x);
+                st_row_bf16x32(ubt, r, 0, x);
+                st_row_bf16x32(ubt, r, 4, x + 32);
                 fence_proxy_async_smem();
                 tc_fence_before();
                 arrive(u_ready);
@@ -1091,12 +1154,13 @@ __global__ void __launch_bounds__(ss::kThreads, 1)
             if (!(ok = warp_wait(s_done, n & 1, wait_ns, err))) break;
             tc_fence_after();
             {
-                float x[32];  // K^T U: d_k row r, this thread's 32 columns
-                tmem_ld_cols<2>(tmem + lane_base + ss::kDs + 32 * half, x);
+                float x[64];  // K^T U: d_k row r, all 64 columns
+                tmem_ld_cols<4>(tmem + lane_base + ss::kDs, x);
 #pragma unroll
-                for (int j = 0; j < 32; ++j) sx[j] += x[j];  // S_{n+1}
+                for (int j = 0; j < 64; ++j) sx[j] += x[j];  // S_{n+1}
             }
-            st_row_bf16x32(sbt, r, 4 * half, sx);
+            st_row_bf16x32(sbt, r, 0, sx);
+            st_row_bf16x32(sbt, r, 4, sx + 32);
             fence_proxy_async_smem();
             tc_fence_before();
             arrive(s_ready);
@@ -1105,7 +1169,7 @@ __global__ void __launch_bounds__(ss::kThreads, 1)
             } else if (sT_out) {
                 float4* dst = reinterpret_cast<float4*>(sT_out + srow);
 #pragma unroll
-                for (int j4 = 0; j4 < 8; ++j4)
+                for (int j4 = 0; j4 < 16; ++j4)
                     dst[j4] = make_float4(sx[4 * j4], sx[4 * j4 + 1], sx[4 * j4 + 2], sx[4 * j4 + 3]);
             }
         }
@@ -1278,18 +1342,18 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base
              CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// token tensor [B, T, H, 128] bf16 viewed as (d, H, T, B); box (64, 1, 64, 1)
-bool token_map(CUtensorMap* m, const void* p, int B, int T, int H) {
-    const uint64_t dims[4] = {kD, (uint64_t)H, (uint64_t)T, (uint64_t)B};
-    const uint64_t st[3] = {kD * 2, (uint64_t)H * kD * 2, (uint64_t)T * H * kD * 2};
+// token tensor [B, T, H, d] bf16 (d = 128 unless given) viewed as (d, H, T, B); box (64, 1, 64, 1)
+bool token_map(CUtensorMap* m, const void* p, int B, int T, int H, int d = kD) {
+    const uint64_t dims[4] = {(uint64_t)d, (uint64_t)H, (uint64_t)T, (uint64_t)B};
+    const uint64_t st[3] = {(uint64_t)d * 2, (uint64_t)H * d * 2, (uint64_t)T * H * d * 2};
     const uint32_t box[4] = {64, 1, kC, 1};
     return make_map(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, p, dims, st, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-// output [B, T, H, 128] bf16 viewed as (d, H, T, B); box (64, 1, 32, 1), 128-byte swizzle
-bool out_map(CUtensorMap* m, const void* p, int B, int T, int H) {
-    const uint64_t dims[4] = {kD, (uint64_t)H, (uint64_t)T, (uint64_t)B};
-    const uint64_t st[3] = {kD * 2, (uint64_t)H * kD * 2, (uint64_t)T * H * kD * 2};
+// output [B, T, H, d_v] bf16 viewed as (d_v, H, T, B); box (64, 1, 32, 1), 128-byte swizzle
+bool out_map(CUtensorMap* m, const void* p, int B, int T, int H, int dv) {
+    const uint64_t dims[4] = {(uint64_t)dv, (uint64_t)H, (uint64_t)T, (uint64_t)B};
+    const uint64_t st[3] = {(uint64_t)dv * 2, (uint64_t)H * dv * 2, (uint64_t)T * H * dv * 2};
     const uint32_t box[4] = {64, 1, 32, 1};
     return make_map(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, p, dims, st, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
@@ -1333,8 +1397,8 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const v
         !ws_map(&sm_.kh, wsb + kWsKh, BF, 2, 128, 64, units, 64, 64, SW) ||
         !ws_map(&sm_.m, wsb + kWsM, BF, 2, 64, 64, units, 64, 64, SW) ||
         !ws_map(&sm_.t, wsb + kWsT, BF, 2, 64, 64, units, 64, 64, SW) ||
-        !token_map(&sm_.v, v, sh.B, sh.T, sh.Hv) || !token_map(&sm_.wg, w, sh.B, sh.T, sh.Hv) ||
-        !out_map(&sm_.o_st, o, sh.B, sh.T, sh.Hv))
+        !token_map(&sm_.v, v, sh.B, sh.T, sh.Hv, sh.dv) || !token_map(&sm_.wg, w, sh.B, sh.T, sh.Hv, sh.dv) ||
+        !out_map(&sm_.o_st, o, sh.B, sh.T, sh.Hv, sh.dv))
         return cudaErrorInvalidValue;
 
     // The state kernel runs one CTA per SM, so it takes the whole 227 KB: operand descriptors can
@@ -1363,8 +1427,8 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const v
         sh.Hv, NC);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    state_tc_kernel<<<dim3(2 * sh.B * sh.Hv), ss::kThreads, s_smem, s>>>(sm_, wsb, s0, sT, sh.Hv, NC, scale,
-                                                                      wait_ns);
+    state_tc_kernel<<<dim3((sh.dv / 64) * sh.B * sh.Hv), ss::kThreads, s_smem, s>>>(sm_, wsb, s0, sT, sh.Hv, sh.dv,
+                                                                                  NC, scale, wait_ns);
     return cudaGetLastError();
 }
 

@@ -86,6 +86,9 @@ def test_workspace_sizes(g):
     assert g.gdn2_chunk_fwd_workspace_size(1, 10, 3, 4, 64, 64, 64, g.GDN2_F32) == 0        # Hv % Hk
     assert g.gdn2_chunk_fwd_workspace_size(1, 10, 4, 4, 72, 64, 64, g.GDN2_F32) == 0        # dk % 16
     assert g.gdn2_chunk_fwd_workspace_size(1, 10, 4, 4, 64, 64, 64, g.GDN2_BF16, "tcgen05") == 0
+    # the tensor-core units hold d_k-side factors only: the same workspace for every d_v
+    for dv in (64, 256, 512):
+        assert g.gdn2_chunk_fwd_workspace_size(1, 65, 1, 1, 128, dv, 64, g.GDN2_BF16) == 66048 * 2 + 256
 
 
 def _chunk(g, path=0, B=1, T=8, Hk=1, Hv=1, dk=128, dv=128, C=64, dt=1, ptr=0x10000, ws=None, wsb=1 << 30,
@@ -105,6 +108,9 @@ def test_chunk_argument_errors(g):
     assert _chunk(g, C=48) == g.GDN2_ERR_UNSUPPORTED
     assert _chunk(g, path=2, dt=0) == g.GDN2_ERR_UNSUPPORTED           # tensor cores need bf16
     assert _chunk(g, path=2, dk=64, dv=64) == g.GDN2_ERR_UNSUPPORTED
+    assert _chunk(g, path=2, dv=96) == g.GDN2_ERR_UNSUPPORTED           # tensor cores: d_v in 64-column slices
+    assert _chunk(g, path=2, dv=576) == g.GDN2_ERR_UNSUPPORTED
+    assert _chunk(g, path=1, dv=272) == g.GDN2_ERR_UNSUPPORTED          # SIMT: d_v up to 256
     assert _chunk(g, B=32768, T=1, Hv=4) == g.GDN2_ERR_UNSUPPORTED     # B * H_v beyond the grid's y range
     assert g.lib.gdn2_chunk_fwd_workspace_size(32768, 1, 1, 4, 128, 128, 64, 1) == 0
     assert _chunk(g, ptr=0x10008) == g.GDN2_ERR_MISALIGNED

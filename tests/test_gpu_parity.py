@@ -284,3 +284,27 @@ def test_decode_writes_stay_in_bounds(g, B, Hk, Hv):
     o_ref, s_ref = oracle.run_inputs(inp)
     _check("o", H.to_np(torch.stack(outs, dim=1)), o_ref, H.BF16_TOL)
     _check("state", st.cpu().numpy(), s_ref, H.BF16_TOL)
+
+
+# ---------------------------------------------------------------------------------------------
+# value dimensions other than d_k (expand_v): the tensor-core path runs d_v / 64 state CTAs per head
+
+@pytest.mark.parametrize("dv,Hk,Hv,T", [(256, 1, 2, 200), (64, 2, 2, 130), (192, 1, 3, 64), (512, 1, 1, 70)])
+def test_chunk_tc_value_dims(g, dv, Hk, Hv, T):
+    wl = synth.Workload("t", B=2, T=T, Hk=Hk, Hv=Hv, dk=128, dv=dv, dtype="bf16", seed=50 + dv, s0_std=0.02)
+    inp = synth.make_inputs(wl)
+    o, st = H.run_chunk(g, inp, path="tcgen05")
+    o_ref, s_ref = oracle.run_inputs(inp)
+    _check("o", o, o_ref, H.BF16_TOL)
+    _check("state", st.cpu().numpy(), s_ref, H.BF16_TOL)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_chunk_simt_value_dim_256(g, dtype):
+    wl = synth.Workload("t", B=1, T=150, Hk=1, Hv=2, dk=64, dv=256, C=32, dtype=dtype, seed=57, s0_std=0.02)
+    inp = synth.make_inputs(wl)
+    o, st = H.run_chunk(g, inp, C=32, path="simt")
+    o_ref, s_ref = oracle.run_inputs(inp)
+    tol = H.tol_for(dtype)
+    _check("o", o, o_ref, tol)
+    _check("state", st.cpu().numpy(), s_ref, tol)
