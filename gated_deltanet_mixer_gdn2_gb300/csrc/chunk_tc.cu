@@ -75,47 +75,7 @@ __device__ __forceinline__ bool cta_wait(uint64_t* bar, uint32_t parity, long lo
     return ok;
 }
 
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<const uint32_t*>(&v);
-}
 
-
-// Packed fp32x2 arithmetic (two channels per instruction) and bf16 pair conversions.
-constexpr float kLog2e = 1.4426950408889634f;
-__device__ __forceinline__ uint64_t f32x2(float lo, float hi) {
-    uint64_t r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-    return r;
-}
-__device__ __forceinline__ void f32x2_split(uint64_t a, float& lo, float& hi) {
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(a));
-}
-__device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b) {
-    uint64_t r;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-    return r;
-}
-__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
-    uint64_t r;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
-    return r;
-}
-__device__ __forceinline__ float ex2_approx(float x) {  // 2^x, the hardware approximation
-    float r;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
-    return r;
-}
-// two bf16 (low half = first) -> fp32 pair: a bf16 is the upper half of its fp32
-__device__ __forceinline__ uint64_t bf16x2_widen(uint32_t u) {
-    return f32x2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
-}
-// fp32 pair -> two bf16 (round to nearest even), first value in the low half
-__device__ __forceinline__ uint32_t bf16x2_narrow(uint64_t a) {
-    float lo, hi;
-    f32x2_split(a, lo, hi);
-    return pack_bf16x2(lo, hi);
-}
 
 // 64 fp32 columns of this warp's TMEM lanes starting at column `col`.
 __device__ __forceinline__ void tmem_ld64(uint32_t tmem_base, int warp, int col, float (&x)[64]) {

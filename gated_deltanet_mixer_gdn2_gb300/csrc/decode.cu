@@ -15,10 +15,12 @@
 //   Register kernel: a warp owns 16 columns of one head across all d_k rows: lane = 8 row groups x
 //   4 column groups, each lane holds d_k/8 rows x 4 columns. Reductions over d_k are in-thread, then
 //   warp shuffles across the 8 row groups. No shared memory, no block barrier.
-//   Streaming kernel (d_k = d_v = 128, one token, many heads): a persistent grid walks the heads;
-//   each state slab is bulk-copied into a 3-deep shared-memory ring with its token vectors, updated
-//   in place and bulk-copied back, so that loads of the next two heads and the store of the
-//   previous one are in flight while a head is computed.
+//   Streaming kernel (d_k = d_v = 128, up to 4 tokens per call, many heads): a persistent grid walks
+//   the heads; each state slab is bulk-copied into a shared-memory ring with the call's token
+//   vectors, carried through the tokens in registers and bulk-copied back, so that the loads of the
+//   next heads and the store of the previous one are in flight while a head is computed. The ring
+//   takes as many slots as fit: 3 with fp32 state, 5-6 with bf16 state (a bf16 slab is half the
+//   bytes, so twice as many heads keep the HBM busy).
 #include "common.cuh"
 #include "ptx.cuh"
 
@@ -153,15 +155,32 @@ __global__ void __launch_bounds__(256, 2)
     for (int i = 0; i < RPL; ++i) store4(S + static_cast<size_t>(rg + 8 * i) * dv, s[i]);
 }
 
-// ---- streaming kernel (d_k = d_v = 128, one token) ----------------------------------------------
+// ---- streaming kernel (d_k = d_v = 128, up to kStreamTokens tokens per call) --------------------
 
-constexpr int kRing = 3;
-constexpr uint32_t kSlabMax = 128 * 128 * 4;
-constexpr uint32_t kTokOff = kRing * kSlabMax;          // per ring slot: q, k, g, b, v, w (128 each)
-constexpr uint32_t kTokSlot = 6 * 128 * 4;              // room for fp32 tokens
-constexpr uint32_t kRed = kTokOff + kRing * kTokSlot;   // [8 warps][2][128] partial r_b, r_q + [8] k.q
-constexpr uint32_t kStreamBar = kRed + 8 * 2 * 128 * 4 + 8 * 4;
-constexpr uint32_t kStreamSmem = kStreamBar + 64;
+constexpr int kStreamTokens = 4;
+constexpr uint32_t kStreamSmemBlock = 232448;  // largest dynamic shared memory of one CTA
+constexpr uint32_t kStreamSmemSM = 233472;     // shared memory of one SM (each resident CTA reserves 1 KB)
+
+// Ring geometry for one (token type, state type, tokens per call, CTAs per SM): a slot holds a state
+// slab and the call's token vectors; as many slots as fit in the CTA's share (at most 8). bf16 slabs
+// are half the bytes: with two CTAs per SM, two heads are computed at once and each CTA still keeps
+// two heads loading ahead.
+template <typename Tin, typename TS, int NT, int CPS>
+struct StreamRing {
+    static constexpr uint32_t smem = CPS == 1 ? kStreamSmemBlock : (kStreamSmemSM / CPS - 1024) / 128 * 128;
+    static constexpr int parities = NT > 1 ? 2 : 1;            // reduction buffers (alternate per token)
+    static constexpr uint32_t red_bytes = parities * (8 * 2 * 128 + 8) * 4;  // [8 warps][r_b | r_q][128] + [8] k.q
+    static constexpr uint32_t slab = 128 * 128 * sizeof(TS);
+    static constexpr uint32_t tok = NT * 6 * 128 * sizeof(Tin);
+    static constexpr uint32_t slot = (slab + tok + 127) / 128 * 128;
+    // per token and d_k row: (alpha, alpha, b.k, b.k, q, q, k, k) fp32, plus the token's 8 partial k.q
+    static constexpr uint32_t rows_bytes = NT > 1 ? NT * (128 * 32 + 32) : 0;
+    static constexpr uint32_t avail = smem - red_bytes - rows_bytes - 256;
+    static constexpr int depth = avail / slot > 8 ? 8 : (int)(avail / slot);
+    static constexpr uint32_t red_off = depth * slot;
+    static constexpr uint32_t rows_off = red_off + red_bytes;
+    static constexpr uint32_t bar_off = (rows_off + rows_bytes + 7) / 8 * 8;
+};
 
 __device__ __forceinline__ void bulk_store(void* gdst, const void* ssrc, uint32_t bytes) {
     asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(reinterpret_cast<uint64_t>(gdst)),
@@ -176,13 +195,13 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
-// Queue the loads of head h into ring slot `slot`: its state slab and its six token vectors. An
+// Queue the loads of head h into ring slot `slot`: its state slab and the N tokens' six vectors. An
 // inactive head (slot map gives no row) completes the slot's barrier phase without loading.
-template <typename Tin, typename TS>
-__device__ __forceinline__ void stream_issue(uint8_t* smem_s, uint64_t* bar, int slot, int h, const TS* state,
+template <typename Tin, typename TS, int NT, int CPS>
+__device__ __forceinline__ void stream_issue(uint8_t* smem_s, uint64_t* bar, int slot, int h, int N, const TS* state,
                                              const int* slots, int n_slots, const Tin* q, const Tin* k,
                                              const Tin* v, const Tin* g, const Tin* b, const Tin* w, int Hk, int Hv) {
-    constexpr uint32_t kSlab = 128 * 128 * sizeof(TS);
+    using R = StreamRing<Tin, TS, NT, CPS>;
     const int bi = h / Hv, hv = h - bi * Hv, hk = hv / (Hv / Hk);
     const int row = state_row(slots, n_slots, bi);
     if (row < 0) {
@@ -190,38 +209,54 @@ __device__ __forceinline__ void stream_issue(uint8_t* smem_s, uint64_t* bar, int
         return;
     }
     constexpr uint32_t vb = 128 * sizeof(Tin);
-    mbar_arrive_expect_tx(bar, kSlab + 6 * vb);
-    bulk_load(smem_s + slot * kSlabMax, state + (static_cast<size_t>(row) * Hv + hv) * 16384, kSlab, bar);
-    uint8_t* tk = smem_s + kTokOff + slot * kTokSlot;
-    const size_t kq = (static_cast<size_t>(bi) * Hk + hk) * 128, gv = (static_cast<size_t>(bi) * Hv + hv) * 128;
-    bulk_load(tk + 0 * vb, q + kq, vb, bar);
-    bulk_load(tk + 1 * vb, k + kq, vb, bar);
-    bulk_load(tk + 2 * vb, g + gv, vb, bar);
-    bulk_load(tk + 3 * vb, b + gv, vb, bar);
-    bulk_load(tk + 4 * vb, v + gv, vb, bar);
-    bulk_load(tk + 5 * vb, w + gv, vb, bar);
+    mbar_arrive_expect_tx(bar, R::slab + 6 * vb * N);
+    uint8_t* sl = smem_s + slot * R::slot;
+    bulk_load(sl, state + (static_cast<size_t>(row) * Hv + hv) * 16384, R::slab, bar);
+    for (int t = 0; t < N; ++t) {
+        uint8_t* tk = sl + R::slab + t * 6 * vb;
+        const size_t tt = static_cast<size_t>(bi) * N + t;
+        const size_t kq = (tt * Hk + hk) * 128, gv = (tt * Hv + hv) * 128;
+        bulk_load(tk + 0 * vb, q + kq, vb, bar);
+        bulk_load(tk + 1 * vb, k + kq, vb, bar);
+        bulk_load(tk + 2 * vb, g + gv, vb, bar);
+        bulk_load(tk + 3 * vb, b + gv, vb, bar);
+        bulk_load(tk + 4 * vb, v + gv, vb, bar);
+        bulk_load(tk + 5 * vb, w + gv, vb, bar);
+    }
 }
 
-template <typename Tin, typename TS>
-__global__ void __launch_bounds__(256, 1)
+// Persistent grid over the heads, one CTA per SM, 8 warps: a ring of state slabs (with the tokens of
+// the call) keeps the next depth-1 heads loading and the previous head's store in flight while one
+// head is updated. Per head, thread (warp, lane) holds rows 16 warp .. 16 warp + 15 x columns
+// 4 lane .. 4 lane + 3 of the state in registers across the N tokens; per token the reductions over
+// d_k go in-thread, then across warps through a shared buffer of the token's parity (one block
+// barrier per token).
+template <typename Tin, typename TS, int NT, int CPS>
+__global__ void __launch_bounds__(256, CPS)
     recurrent_stream_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* __restrict__ v,
                             const Tin* __restrict__ g, const Tin* __restrict__ b, const Tin* __restrict__ w,
                             TS* __restrict__ state, const int* __restrict__ slots, int n_slots,
-                            Tin* __restrict__ o, int nheads, int Hk, int Hv, float scale, long long wait_ns) {
-    constexpr uint32_t kSlab = 128 * 128 * sizeof(TS);
+                            Tin* __restrict__ o, int nheads, int N, int Hk, int Hv, float scale, long long wait_ns) {
+    using R = StreamRing<Tin, TS, NT, CPS>;
+    static_assert(R::depth >= 1, "stream ring needs a slot");
+    static_assert(R::bar_off + 8 * 8 + 16 <= R::smem, "stream kernel shared memory");
+    // ring slots; heads loading ahead (with a single slot, the next head loads once the previous
+    // store has read the slot, and the other CTA of the SM covers that gap)
+    constexpr int D = R::depth, P = D > 1 ? D - 1 : 1;
     extern __shared__ __align__(128) uint8_t smem_s[];
-    float* red = reinterpret_cast<float*>(smem_s + kRed);
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem_s + kStreamBar);
-    int* flag = reinterpret_cast<int*>(smem_s + kStreamBar + 32);
+    float* red = reinterpret_cast<float*>(smem_s + R::red_off);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem_s + R::bar_off);
+    int* flag = reinterpret_cast<int*>(smem_s + R::bar_off + 8 * 8);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int G = gridDim.x, first = blockIdx.x;
     const int count = first < nheads ? (nheads - first + G - 1) / G : 0;
 
     if (tid == 0) {
-        for (int i = 0; i < kRing; ++i) mbar_init(full + i, 1);
+        for (int i = 0; i < D; ++i) mbar_init(full + i, 1);
         fence_mbar_init();
-        for (int kk = 0; kk < 2 && kk < count; ++kk)
-            stream_issue(smem_s, full + kk, kk, first + kk * G, state, slots, n_slots, q, k, v, g, b, w, Hk, Hv);
+        for (int kk = 0; kk < P && kk < count; ++kk)
+            stream_issue<Tin, TS, NT, CPS>(smem_s, full + kk, kk, first + kk * G, N, state, slots, n_slots, q, k,
+                                           v, g, b, w, Hk, Hv);
     }
     __syncthreads();
 
@@ -229,15 +264,16 @@ __global__ void __launch_bounds__(256, 1)
     bool ok = true;
     for (; kk < count; ++kk) {
         const int h = first + kk * G;
-        const int bsel = kk % kRing;
+        const int bsel = kk % D;
+        const uint32_t par = (kk / D) & 1;
         const int bi = h / Hv, hv = h - bi * Hv;
         const int row = state_row(slots, n_slots, bi);
 
         if (tid == 0) {
-            const bool got = mbar_wait(full + bsel, (kk / kRing) & 1, wait_ns);
+            const bool got = mbar_wait(full + bsel, par, wait_ns);
             if (!got) {
                 atomicOr(&g_status_decode, kStatusTimeout);
-                mbar_wait(full + bsel, (kk / kRing) & 1, kDefaultWaitNs);
+                mbar_wait(full + bsel, par, kDefaultWaitNs);
             }
             *flag = got ? 1 : 0;
         }
@@ -246,12 +282,12 @@ __global__ void __launch_bounds__(256, 1)
             ok = false;
             break;
         }
-        mbar_wait(full + bsel, (kk / kRing) & 1, kDefaultWaitNs);
+        mbar_wait(full + bsel, par, kDefaultWaitNs);
 
-        if (row >= 0) {
-            // token vectors from the ring: lanes 0..15 take row 16*warp + lane's q, k, alpha, b.k;
-            // every lane its 4 columns of w.v
-            const Tin* tk = reinterpret_cast<const Tin*>(smem_s + kTokOff + bsel * kTokSlot);
+        if (NT == 1 && row >= 0) {
+            // one token: lanes 0..15 take row 16 warp + lane's q, k, alpha, b.k and pass them round
+            // the warp by shuffles; every lane its 4 columns of w.v
+            const Tin* tk = reinterpret_cast<const Tin*>(smem_s + bsel * R::slot + R::slab);
             float q_r = 0.f, k_r = 0.f, a_r = 0.f, bk_r = 0.f;
             if (lane < 16) {
                 const int rr = 16 * warp + lane;
@@ -263,8 +299,7 @@ __global__ void __launch_bounds__(256, 1)
             float wv[4];
 #pragma unroll
             for (int c = 0; c < 4; ++c) wv[c] = to_f32(tk[640 + 4 * lane + c]) * to_f32(tk[512 + 4 * lane + c]);
-
-            TS* S = reinterpret_cast<TS*>(smem_s + bsel * kSlabMax);
+            TS* S = reinterpret_cast<TS*>(smem_s + bsel * R::slot);
             float4 s[16];
             float4 rb = make_float4(0.f, 0.f, 0.f, 0.f), rq = make_float4(0.f, 0.f, 0.f, 0.f);
             float kq = k_r * q_r;
@@ -313,25 +348,150 @@ __global__ void __launch_bounds__(256, 1)
             }
             fence_proxy_async_smem();
         }
+        if (NT > 1 && row >= 0) {
+            // Several tokens. Per token, this warp's 16 d_k rows' scalars (alpha, b.k, q, k), each duplicated into an
+            // fp32 pair for the packed arithmetic below, and their part of k.q; a warp only reads its
+            // own rows, so no block barrier (the k.q parts are read after the token's barrier).
+            const uint8_t* tkb = smem_s + bsel * R::slot + R::slab;
+            float* rows = reinterpret_cast<float*>(smem_s + R::rows_off);
+            // (lane l takes entry p0 + l: token (p0 + l) / 16, row 16 warp + l mod 16). Every lane runs
+            // every trip, since the shuffles need the whole warp; lanes past the last entry add 0.
+            for (int p0 = 0; p0 < 16 * N; p0 += 32) {
+                const int p = p0 + lane, t = p >> 4, rr = 16 * warp + (p & 15);
+                const bool on = p < 16 * N;
+                float kq = 0.f;
+                if (on) {
+                    const Tin* tk = reinterpret_cast<const Tin*>(tkb) + t * 6 * 128;
+                    const float qq = to_f32(tk[rr]), kk = to_f32(tk[128 + rr]);
+                    const float a = expf(to_f32(tk[256 + rr])), bk = to_f32(tk[384 + rr]) * kk;
+                    float4* dst = reinterpret_cast<float4*>(rows + t * (128 * 8 + 8) + rr * 8);
+                    dst[0] = make_float4(a, a, bk, bk);
+                    dst[1] = make_float4(qq, qq, kk, kk);
+                    kq = kk * qq;
+                }
+#pragma unroll
+                for (int off = 8; off > 0; off >>= 1) kq += __shfl_xor_sync(0xffffffffu, kq, off);  // 16-lane halves
+                if (on && (lane & 15) == 0) rows[t * (128 * 8 + 8) + 128 * 8 + warp] = kq;
+            }
+            __syncwarp();
+            // thread (warp, lane): rows 16 warp .. 16 warp + 15, columns 4 lane .. 4 lane + 3, as two
+            // fp32 pairs per row
+            TS* S = reinterpret_cast<TS*>(smem_s + bsel * R::slot);
+            uint64_t s[16][2];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const float4 x = load4(S + (16 * warp + i) * 128 + 4 * lane);
+                s[i][0] = f32x2(x.x, x.y);
+                s[i][1] = f32x2(x.z, x.w);
+            }
+            for (int t = 0; t < N; ++t) {
+                const Tin* tk = reinterpret_cast<const Tin*>(tkb) + t * 6 * 128;
+                const float* rt_rows = rows + t * (128 * 8 + 8);
+                uint64_t wv[2];
+                {
+                    float v4[4], w4[4];
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        v4[c] = to_f32(tk[512 + 4 * lane + c]);
+                        w4[c] = to_f32(tk[640 + 4 * lane + c]);
+                    }
+                    wv[0] = mul_f32x2(f32x2(w4[0], w4[1]), f32x2(v4[0], v4[1]));
+                    wv[1] = mul_f32x2(f32x2(w4[2], w4[3]), f32x2(v4[2], v4[3]));
+                }
+                uint64_t rb[2] = {0, 0}, rq[2] = {0, 0};  // +0.0f pairs
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const ulonglong2 ab = *reinterpret_cast<const ulonglong2*>(rt_rows + (16 * warp + i) * 8);
+                    const uint64_t qp = *reinterpret_cast<const uint64_t*>(rt_rows + (16 * warp + i) * 8 + 4);
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        s[i][h] = mul_f32x2(s[i][h], ab.x);          // alpha
+                        rb[h] = fma_f32x2(s[i][h], ab.y, rb[h]);     // b.k
+                        rq[h] = fma_f32x2(s[i][h], qp, rq[h]);       // q
+                    }
+                }
+                float* rt = red + (t % R::parities) * (8 * 2 * 128 + 8);
+                reinterpret_cast<ulonglong2*>(rt + (warp * 2 + 0) * 128)[lane] = make_ulonglong2(rb[0], rb[1]);
+                reinterpret_cast<ulonglong2*>(rt + (warp * 2 + 1) * 128)[lane] = make_ulonglong2(rq[0], rq[1]);
+                __syncthreads();
+                rb[0] = rb[1] = rq[0] = rq[1] = 0;
+#pragma unroll
+                for (int w8 = 0; w8 < 8; ++w8) {
+                    const ulonglong2 x = reinterpret_cast<const ulonglong2*>(rt + (w8 * 2 + 0) * 128)[lane];
+                    const ulonglong2 y = reinterpret_cast<const ulonglong2*>(rt + (w8 * 2 + 1) * 128)[lane];
+                    rb[0] = add_f32x2(rb[0], x.x);
+                    rb[1] = add_f32x2(rb[1], x.y);
+                    rq[0] = add_f32x2(rq[0], y.x);
+                    rq[1] = add_f32x2(rq[1], y.y);
+                }
+                const float4 kqa = *reinterpret_cast<const float4*>(rt_rows + 128 * 8);
+                const float4 kqb = *reinterpret_cast<const float4*>(rt_rows + 128 * 8 + 4);
+                const float kq = ((kqa.x + kqa.y) + (kqa.z + kqa.w)) + ((kqb.x + kqb.y) + (kqb.z + kqb.w));
+                const uint64_t d[2] = {sub_f32x2(wv[0], rb[0]), sub_f32x2(wv[1], rb[1])};
+                if (warp == 0) {
+                    const uint64_t kq2 = f32x2(kq, kq), sc2 = f32x2(scale, scale);
+                    float ov[4];
+                    f32x2_split(mul_f32x2(sc2, fma_f32x2(kq2, d[0], rq[0])), ov[0], ov[1]);
+                    f32x2_split(mul_f32x2(sc2, fma_f32x2(kq2, d[1], rq[1])), ov[2], ov[3]);
+                    Tin* oh = o + ((static_cast<size_t>(bi) * N + t) * Hv + hv) * 128 + 4 * lane;
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) oh[c] = from_f32<Tin>(ov[c]);
+                }
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const uint64_t kp = *reinterpret_cast<const uint64_t*>(rt_rows + (16 * warp + i) * 8 + 6);
+                    s[i][0] = fma_f32x2(kp, d[0], s[i][0]);
+                    s[i][1] = fma_f32x2(kp, d[1], s[i][1]);
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                float x0, x1, x2, x3;
+                f32x2_split(s[i][0], x0, x1);
+                f32x2_split(s[i][1], x2, x3);
+                store4(S + (16 * warp + i) * 128 + 4 * lane, make_float4(x0, x1, x2, x3));
+            }
+            fence_proxy_async_smem();
+        }
         __syncthreads();
         if (tid == 0) {
             if (row >= 0)
-                bulk_store(state + (static_cast<size_t>(row) * Hv + hv) * 16384, smem_s + bsel * kSlabMax, kSlab);
+                bulk_store(state + (static_cast<size_t>(row) * Hv + hv) * 16384, smem_s + bsel * R::slot, R::slab);
             bulk_commit();  // an empty group for an inactive head keeps the group count in step
-            if (kk + 2 < count) {
-                bulk_wait_read<1>();  // the store of head kk-1 has finished reading its buffer
-                const int nb = (kk + 2) % kRing;
-                stream_issue(smem_s, full + nb, nb, first + (kk + 2) * G, state, slots, n_slots, q, k, v, g, b, w,
-                             Hk, Hv);
+            if (kk + P < count) {
+                if (D > 1) bulk_wait_read<1>();  // the store of head kk-1 has finished reading the slot it leaves
+                else bulk_wait_read<0>();        // single slot: the store of head kk has read it
+                const int nb = (kk + P) % D;
+                stream_issue<Tin, TS, NT, CPS>(smem_s, full + nb, nb, first + (kk + P) * G, N, state, slots, n_slots,
+                                               q, k, v, g, b, w, Hk, Hv);
             }
         }
     }
     if (tid == 0) {
         if (!ok)  // drain the loads already issued for heads after kk
-            for (int j = kk + 1; j < kk + 2 && j < count; ++j) mbar_wait(full + j % kRing, (j / kRing) & 1, kDefaultWaitNs);
+            for (int j = kk + 1; j < kk + P && j < count; ++j) mbar_wait(full + j % D, (j / D) & 1, kDefaultWaitNs);
         bulk_wait_all();
     }
     __syncthreads();
+}
+
+template <typename Tin, typename TS, int NT>
+cudaError_t launch_stream(const void* q, const void* k, const void* v, const void* g, const void* b, const void* w,
+                          TS* st, const int* slots, int n_slots, void* o, long long heads, int N, int Hk, int Hv,
+                          float scale, int nsm, cudaStream_t s) {
+    // Two CTAs per SM when each still gets a ring of three slots (bf16 state), or, with several tokens
+    // per call (a head's compute is then long next to its copies), when each gets one slot at all.
+    constexpr int depth2 = StreamRing<Tin, TS, NT, 2>::avail / StreamRing<Tin, TS, NT, 2>::slot;
+    constexpr int CPS = (depth2 >= 3 || (NT > 1 && depth2 >= 1)) ? 2 : 1;
+    using R = StreamRing<Tin, TS, NT, CPS>;
+    cudaError_t e = cudaFuncSetAttribute(recurrent_stream_kernel<Tin, TS, NT, CPS>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)R::smem);
+    if (e != cudaSuccess) return e;
+    recurrent_stream_kernel<Tin, TS, NT, CPS><<<CPS * nsm, 256, R::smem, s>>>(
+        static_cast<const Tin*>(q), static_cast<const Tin*>(k), static_cast<const Tin*>(v),
+        static_cast<const Tin*>(g), static_cast<const Tin*>(b), static_cast<const Tin*>(w), st, slots, n_slots,
+        static_cast<Tin*>(o), static_cast<int>(heads), N, Hk, Hv, scale, wait_limit_ns());
+    return cudaGetLastError();
 }
 
 int g_num_sms = 0;
@@ -348,15 +508,12 @@ cudaError_t launch_t(const void* q, const void* k, const void* v, const void* g,
     }
     const long long heads = static_cast<long long>(B) * Hv;
     TS* st = static_cast<TS*>(state);
-    if (N == 1 && dk == 128 && dv == 128 && heads >= 4LL * g_num_sms) {
-        cudaError_t e = cudaFuncSetAttribute(recurrent_stream_kernel<Tin, TS>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kStreamSmem);
-        if (e != cudaSuccess) return e;
-        recurrent_stream_kernel<Tin, TS><<<g_num_sms, 256, kStreamSmem, s>>>(
-            static_cast<const Tin*>(q), static_cast<const Tin*>(k), static_cast<const Tin*>(v),
-            static_cast<const Tin*>(g), static_cast<const Tin*>(b), static_cast<const Tin*>(w), st, slots, n_slots,
-            static_cast<Tin*>(o), static_cast<int>(heads), Hk, Hv, scale, wait_limit_ns());
-        return cudaGetLastError();
+    if (N <= kStreamTokens && dk == 128 && dv == 128 && heads >= 4LL * g_num_sms) {
+        if (N == 1)
+            return launch_stream<Tin, TS, 1>(q, k, v, g, b, w, st, slots, n_slots, o, heads, N, Hk, Hv, scale,
+                                             g_num_sms, s);
+        return launch_stream<Tin, TS, kStreamTokens>(q, k, v, g, b, w, st, slots, n_slots, o, heads, N, Hk, Hv,
+                                                     scale, g_num_sms, s);
     }
     // register kernel: 8 warps (128 columns) per CTA when there are many heads, 2 warps (32
     // columns) otherwise so that small batches still spread over the SMs

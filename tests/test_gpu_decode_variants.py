@@ -124,3 +124,29 @@ def test_bf16_state_many_steps(g, B):
         o_ref, s_ref = oracle.run_inputs(sub)
         assert _err(o_gpu[bi:bi + 1, :, hv:hv + 1], o_ref) < H.BF16_TOL
         assert _err(st[bi, hv].float().cpu().numpy(), s_ref[0, 0]) < H.BF16_TOL
+
+
+@pytest.mark.parametrize("N,state_dt,tok_dt", [(2, "f32", "bf16"), (4, "f32", "bf16"), (4, "bf16", "bf16"),
+                                               (3, "bf16", "f32"), (4, "f32", "f32"), (5, "f32", "bf16")])
+def test_streaming_kernel_tokens_and_state_types(g, N, state_dt, tok_dt):
+    """160 x 4 = 640 heads: the streaming kernel (several tokens per call with the state held between
+    them, up to 4; N = 5 takes the register kernel), fp32 or bf16 state, fp32 or bf16 tokens, against
+    the oracle on every head."""
+    import torch
+
+    wl = synth.Workload("t", B=160, T=N, Hk=2, Hv=4, dk=128, dv=128, dtype=tok_dt, seed=70 + N, s0_std=0.02)
+    inp = synth.make_inputs(wl)
+    if state_dt == "bf16":
+        inp.s0 = synth.round_to(inp.s0.astype(np.float64), "bf16")
+    q, k, v, gg, b, w = _dev(inp)
+    st = H.state_to_device(inp.s0)
+    if state_dt == "bf16":
+        st = st.to(torch.bfloat16)
+    o = torch.full_like(v, float("nan"))
+    g.gdn2_recurrent_update(q, k, v, gg, b, w, st, o)
+    torch.cuda.synchronize()
+    assert g.gdn2_last_device_status() == g.GDN2_OK
+    o_ref, s_ref = oracle.run_inputs(inp)
+    tol = H.BF16_TOL if (tok_dt == "bf16" or state_dt == "bf16") else H.F32_TOL
+    H.check("o", H.to_np(o), o_ref, tol)
+    H.check("state", st.float().cpu().numpy(), s_ref, tol, head_axis=1)
