@@ -16,9 +16,11 @@ cudaError_t launch_selftest_umma(int case_id, int soft, const void* a_st, const 
 
 namespace {
 
-// Tensor-core path: d_k = 128; the state kernel runs one CTA per 64 columns of d_v.
+// Tensor-core path: d_k = 128, or 64 run as 128 with zero channels; the state kernel runs one CTA per
+// 64 columns of d_v.
 bool tc_shape(const ChunkShape& sh, gdn2_dtype dt) {
-    return dt == GDN2_BF16 && sh.dk == 128 && sh.dv % 64 == 0 && sh.dv >= 64 && sh.dv <= 512 && sh.C == 64;
+    return dt == GDN2_BF16 && (sh.dk == 128 || sh.dk == 64) && sh.dv % 64 == 0 && sh.dv >= 64 && sh.dv <= 512 &&
+           sh.C == 64;
 }
 
 bool simt_shape(const ChunkShape& sh) {

@@ -570,7 +570,8 @@ constexpr int kThreads = 256;
 __global__ void __launch_bounds__(xs::kThreads, 1)
     factors_exact_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
                          const __nv_bfloat16* __restrict__ g, const __nv_bfloat16* __restrict__ b,
-                         uint8_t* __restrict__ ws, const int* __restrict__ exact_list, int T, int Hk, int Hv, int NC) {
+                         uint8_t* __restrict__ ws, const int* __restrict__ exact_list, int T, int Hk, int Hv, int NC,
+                         int dk) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
     float* sG = reinterpret_cast<float*>(sm + xs::G);
@@ -594,9 +595,9 @@ __global__ void __launch_bounds__(xs::kThreads, 1)
         for (int p = tid; p < 64 * 16; p += xs::kThreads) {
             const int t = p >> 4, c = 8 * (p & 15), tok = n * kC + t;
             float gg[8], bb[8], kk[8], qq[8];
-            if (tok < T) {
-                const size_t kq = ((static_cast<size_t>(bi) * T + tok) * Hk + hk) * kD + c;
-                const size_t gb = ((static_cast<size_t>(bi) * T + tok) * Hv + hv) * kD + c;
+            if (tok < T && c < dk) {  // channels past d_k (d_k = 64) are zero: they leave the state unchanged
+                const size_t kq = ((static_cast<size_t>(bi) * T + tok) * Hk + hk) * dk + c;
+                const size_t gb = ((static_cast<size_t>(bi) * T + tok) * Hv + hv) * dk + c;
                 unpack8(*reinterpret_cast<const uint4*>(g + gb), gg);
                 unpack8(*reinterpret_cast<const uint4*>(b + gb), bb);
                 unpack8(*reinterpret_cast<const uint4*>(k + kq), kk);
@@ -822,8 +823,8 @@ __device__ __forceinline__ void tma_store_4d(const void* map, const void* src, i
 // bounded.
 __global__ void __launch_bounds__(ss::kThreads, 1)
     state_tc_kernel(const __grid_constant__ StateMaps maps, const uint8_t* __restrict__ ws,
-                    const float* __restrict__ s0, float* __restrict__ sT_out, int Hv, int dv, int NC, float scale,
-                    long long wait_ns) {
+                    const float* __restrict__ s0, float* __restrict__ sT_out, int Hv, int dk, int dv, int NC,
+                    float scale, long long wait_ns) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(sm);
@@ -1080,13 +1081,17 @@ __global__ void __launch_bounds__(ss::kThreads, 1)
         };
         uint8_t* sbt = sm + ss::SB;
         uint8_t* ubt = sm + ss::UB;
-        const size_t srow = (static_cast<size_t>(bh) * kD + r) * dv + 64 * hc;
+        // with d_k = 64 the rows 64..127 are zero padding: they start at 0 and stay there (their keys
+        // are zero and their decay is 1), and are neither read from S0 nor written to S_T
+        const bool real_row = r < dk;
+        const size_t srow = (static_cast<size_t>(bh) * dk + (real_row ? r : 0)) * dv + 64 * hc;
         float sx[64];  // e^{G_last(n)} . S_n
         bool ok = NC > 0;
         if (ok) {
 #pragma unroll
             for (int j4 = 0; j4 < 16; ++j4) {
-                const float4 f = s0 ? reinterpret_cast<const float4*>(s0 + srow)[j4] : make_float4(0.f, 0.f, 0.f, 0.f);
+                const float4 f = (s0 && real_row) ? reinterpret_cast<const float4*>(s0 + srow)[j4]
+                                                  : make_float4(0.f, 0.f, 0.f, 0.f);
                 sx[4 * j4] = f.x;
                 sx[4 * j4 + 1] = f.y;
                 sx[4 * j4 + 2] = f.z;
@@ -1126,7 +1131,7 @@ __global__ void __launch_bounds__(ss::kThreads, 1)
             arrive(s_ready);
             if (n + 1 < NC) {
                 if (!(ok = decay(n + 1, sx))) break;
-            } else if (sT_out) {
+            } else if (sT_out && real_row) {
                 float4* dst = reinterpret_cast<float4*>(sT_out + srow);
 #pragma unroll
                 for (int j4 = 0; j4 < 16; ++j4)
@@ -1345,8 +1350,9 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const v
     const auto BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     const auto SW = CU_TENSOR_MAP_SWIZZLE_128B;
     FactorMaps fm;
-    if (!token_map(&fm.q, q, sh.B, sh.T, sh.Hk) || !token_map(&fm.k, k, sh.B, sh.T, sh.Hk) ||
-        !token_map(&fm.g, g, sh.B, sh.T, sh.Hv) || !token_map(&fm.b, b, sh.B, sh.T, sh.Hv) ||
+    // d_k = 64: the maps declare 64 channels, so the second 64-channel box of every tile reads as zeros
+    if (!token_map(&fm.q, q, sh.B, sh.T, sh.Hk, sh.dk) || !token_map(&fm.k, k, sh.B, sh.T, sh.Hk, sh.dk) ||
+        !token_map(&fm.g, g, sh.B, sh.T, sh.Hv, sh.dk) || !token_map(&fm.b, b, sh.B, sh.T, sh.Hv, sh.dk) ||
         !ws_map(&fm.m_st, wsb + kWsM, BF, 2, 64, 64, units, 64, 64, SW) ||
         !ws_map(&fm.t_st, wsb + kWsT, BF, 2, 64, 64, units, 64, 64, SW) ||
         !ws_map(&fm.w_st, wsb + kWsW, BF, 2, 128, 64, units, 64, 64, SW))
@@ -1384,11 +1390,11 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const v
     factors_exact_kernel<<<units < nsm ? units : nsm, xs::kThreads, x_smem, s>>>(
         static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k),
         static_cast<const __nv_bfloat16*>(g), static_cast<const __nv_bfloat16*>(b), wsb, exact_list, sh.T, sh.Hk,
-        sh.Hv, NC);
+        sh.Hv, NC, sh.dk);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    state_tc_kernel<<<dim3((sh.dv / 64) * sh.B * sh.Hv), ss::kThreads, s_smem, s>>>(sm_, wsb, s0, sT, sh.Hv, sh.dv,
-                                                                                  NC, scale, wait_ns);
+    state_tc_kernel<<<dim3((sh.dv / 64) * sh.B * sh.Hv), ss::kThreads, s_smem, s>>>(sm_, wsb, s0, sT, sh.Hv, sh.dk,
+                                                                                  sh.dv, NC, scale, wait_ns);
     return cudaGetLastError();
 }
 

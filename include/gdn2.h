@@ -52,8 +52,8 @@ typedef enum gdn2_status {
 
 typedef enum gdn2_dtype { GDN2_F32 = 0, GDN2_BF16 = 1 } gdn2_dtype;
 
-/* Kernel family used by the chunked forward. AUTO picks TCGEN05 for bf16 with d_k = 128, d_v a
- * multiple of 64 (up to 512) and C = 64, and SIMT otherwise. */
+/* Kernel family used by the chunked forward. AUTO picks TCGEN05 for bf16 with d_k = 128 or 64, d_v
+ * a multiple of 64 (up to 512) and C = 64, and SIMT otherwise. */
 typedef enum gdn2_path { GDN2_PATH_AUTO = 0, GDN2_PATH_SIMT = 1, GDN2_PATH_TCGEN05 = 2 } gdn2_path;
 
 /* Human-readable name of a status code (static string, never NULL). */
@@ -91,9 +91,10 @@ size_t gdn2_chunk_fwd_workspace_size_path(gdn2_path path, int B, int T, int Hk, 
  * T need not be a multiple of C (the last chunk is padded with tokens that leave the state
  * unchanged). T == 0 or B == 0 is valid: o is untouched and final_state receives initial_state (or
  * zeros). Supported: d_k a multiple of 16 in [16, 128] and d_v a multiple of 16 in [16, 256]
- * (SIMT, fp32 or bf16); bf16 with d_k = 128, d_v a multiple of 64 in [64, 512] and C = 64 (TCGEN05,
- * which AUTO picks for those shapes; d_v = 256 is the configuration table's expand_v = 2 at
- * head_dim 128); B * H_v <= 65535 (GDN2_ERR_UNSUPPORTED beyond).
+ * (SIMT, fp32 or bf16); bf16 with d_k = 128 or 64, d_v a multiple of 64 in [64, 512] and C = 64
+ * (TCGEN05, which AUTO picks for those shapes; d_v = 256 is the configuration table's expand_v = 2
+ * at head_dim 128; d_k = 64 runs as d_k = 128 whose upper 64 key channels are zero, so it costs
+ * what d_k = 128 costs); B * H_v <= 65535 (GDN2_ERR_UNSUPPORTED beyond).
  *
  * Decay domain: any alpha in [0, 1] on both paths, including alpha = 0 (g = -inf) and decays that
  * forget a whole chunk. Both paths floor g at -100 (alpha = e^-100 ~ 4e-44, indistinguishable from

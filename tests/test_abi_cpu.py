@@ -85,7 +85,9 @@ def test_workspace_sizes(g):
     assert g.gdn2_chunk_fwd_workspace_size(1, 0, 4, 4, 64, 64, 64, g.GDN2_F32) == 0
     assert g.gdn2_chunk_fwd_workspace_size(1, 10, 3, 4, 64, 64, 64, g.GDN2_F32) == 0        # Hv % Hk
     assert g.gdn2_chunk_fwd_workspace_size(1, 10, 4, 4, 72, 64, 64, g.GDN2_F32) == 0        # dk % 16
-    assert g.gdn2_chunk_fwd_workspace_size(1, 10, 4, 4, 64, 64, 64, g.GDN2_BF16, "tcgen05") == 0
+    assert g.gdn2_chunk_fwd_workspace_size(1, 10, 4, 4, 32, 64, 64, g.GDN2_BF16, "tcgen05") == 0
+    # d_k = 64 runs as d_k = 128 with zero channels: the same units
+    assert g.gdn2_chunk_fwd_workspace_size(1, 10, 4, 4, 64, 64, 64, g.GDN2_BF16, "tcgen05") == 66048 * 4 + 256
     # the tensor-core units hold d_k-side factors only: the same workspace for every d_v
     for dv in (64, 256, 512):
         assert g.gdn2_chunk_fwd_workspace_size(1, 65, 1, 1, 128, dv, 64, g.GDN2_BF16) == 66048 * 2 + 256
@@ -107,7 +109,7 @@ def test_chunk_argument_errors(g):
     assert _chunk(g, dk=72) == g.GDN2_ERR_UNSUPPORTED
     assert _chunk(g, C=48) == g.GDN2_ERR_UNSUPPORTED
     assert _chunk(g, path=2, dt=0) == g.GDN2_ERR_UNSUPPORTED           # tensor cores need bf16
-    assert _chunk(g, path=2, dk=64, dv=64) == g.GDN2_ERR_UNSUPPORTED
+    assert _chunk(g, path=2, dk=32, dv=64) == g.GDN2_ERR_UNSUPPORTED    # tensor cores: d_k 128 or 64
     assert _chunk(g, path=2, dv=96) == g.GDN2_ERR_UNSUPPORTED           # tensor cores: d_v in 64-column slices
     assert _chunk(g, path=2, dv=576) == g.GDN2_ERR_UNSUPPORTED
     assert _chunk(g, path=1, dv=272) == g.GDN2_ERR_UNSUPPORTED          # SIMT: d_v up to 256

@@ -308,3 +308,16 @@ def test_chunk_simt_value_dim_256(g, dtype):
     tol = H.tol_for(dtype)
     _check("o", o, o_ref, tol)
     _check("state", st.cpu().numpy(), s_ref, tol)
+
+
+@pytest.mark.parametrize("dv,decay,s0", [(64, "standard", True), (128, "standard", False), (64, "reset", True)])
+def test_chunk_tc_head_dim_64(g, dv, decay, s0):
+    """head_dim 64 (the burn-gdn2 Quick start's shape) on the tensor-core path: d_k = 64 runs as
+    d_k = 128 with zero channels; ragged T, grouped heads, an initial state and the exact kernel."""
+    wl = synth.Workload("t", B=2, T=170, Hk=1, Hv=2, dk=64, dv=dv, dtype="bf16", seed=60 + dv,
+                        s0_std=0.02 if s0 else 0.0, decay=decay)
+    inp = synth.make_inputs(wl)
+    o, st = H.run_chunk(g, inp, path="tcgen05")
+    o_ref, s_ref = oracle.run_inputs(inp)
+    _check("o", o, o_ref, H.BF16_TOL)
+    _check("state", st.cpu().numpy(), s_ref, H.BF16_TOL)
