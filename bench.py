@@ -495,6 +495,68 @@ def run_variants(device):
                           "bytes_per_call": b, "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
                           "frac": round(gbs / hbm, 4), "peak_kind": f"{peak_kind} hbm_gbs",
                           "l2": "state >= 100 MB > L2; 100 back-to-back calls"}), flush=True)
+    run_mixer_step_variants(device, hbm, peak_kind)
+
+
+def run_mixer_step_variants(device, hbm, peak_kind):
+    """The whole mixer around the core for one decode token: gdn2_mixer_decode_step (one launch) against
+    gdn2_mixer_prologue + gdn2_recurrent_step + gdn2_mixer_epilogue (five launches), at the decode
+    workload's batch and at batch 1; 100 back-to-back calls of each."""
+    import torch
+
+    import gated_deltanet_mixer_gdn2_gb300 as g
+
+    wl = synth.WORKLOADS[DECODE_WORKLOAD]
+    Hk, Hv, d = wl.Hk, wl.Hv, wl.dk
+    gen = torch.Generator(device=device)
+    gen.manual_seed(11)
+    bf = torch.bfloat16
+    for B in (wl.B, 1):
+        rn = lambda *s: torch.randn(s, generator=gen, device=device)
+        xq, xk, xv = rn(B, 1, Hk, d).to(bf), rn(B, 1, Hk, d).to(bf), rn(B, 1, Hv, d).to(bf)
+        ag, ab, aw, z = rn(B, 1, Hv, d).to(bf), rn(B, 1, Hv, d).to(bf), rn(B, 1, Hv, d).to(bf), rn(B, Hv, d).to(bf)
+        cw = [0.5 * rn(n, 4) for n in (Hk * d, Hk * d, Hv * d)]
+        cs = [rn(B, 3, n) for n in (Hk * d, Hk * d, Hv * d)]
+        st = 0.02 * rn(B, Hv, d, d)
+        wt = torch.ones(d, device=device)
+        y = torch.empty((B, Hv, d), dtype=bf, device=device)
+        outs = [torch.empty_like(t) for t in (xq, xk, xv, ag, ab, aw)]
+        o = torch.empty((B, Hv, d), dtype=bf, device=device)
+
+        def fused():
+            g.gdn2_mixer_decode_step(xq[:, 0], xk[:, 0], xv[:, 0], *cw, ag[:, 0], ab[:, 0], aw[:, 0], st, z, wt, y,
+                                     states=cs)
+
+        def separate():
+            g.gdn2_mixer_prologue(xq, xk, xv, *cw, ag, ab, aw, *outs, states=cs)
+            g.gdn2_recurrent_step(*(t[:, 0] for t in outs), st, o)
+            g.gdn2_mixer_epilogue(o[:, None], z[:, None], wt, y[:, None])
+
+        stream = torch.cuda.current_stream(device)
+        res = {}
+        for name, fn in (("fused", fused), ("separate", separate)):
+            for _ in range(3):
+                fn()
+            torch.cuda.synchronize(device)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(100):
+                fn()
+            e1.record(stream)
+            torch.cuda.synchronize(device)
+            res[name] = e0.elapsed_time(e1) * 1e3 / 100
+        # bytes of the fused step: core state read + written, conv states read + written, the token's
+        # vectors in and y out, the conv weights
+        b = (2 * B * Hv * d * d * 4 + 2 * B * 3 * (2 * Hk + Hv) * d * 4 + B * (2 * Hk + 5 * Hv) * d * 2
+             + (2 * Hk + Hv) * d * 16 + d * 4)
+        gbs = b / (res["fused"] * 1e-6) / 1e9
+        print(json.dumps({"variant": f"mixer decode step (conv + L2 norm + gates + core + gated RMSNorm), B={B}",
+                          "workload": f"{DECODE_WORKLOAD} heads: H_k={Hk} H_v={Hv} d={d}, bf16 tokens, fp32 state",
+                          "us_per_call_fused": round(res["fused"], 2), "launches_fused": 1,
+                          "us_per_call_separate": round(res["separate"], 2), "launches_separate": 5,
+                          "bytes_per_call": b, "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
+                          "frac": round(gbs / hbm, 4), "peak_kind": f"{peak_kind} hbm_gbs",
+                          "l2": "100 back-to-back calls"}), flush=True)
 
 
 def end_to_end(g, wl, host, device, args, tokens):

@@ -26,7 +26,7 @@ EXPORTS = (
     "gdn2_recurrent_step", "gdn2_last_device_status", "gdn2_set_wait_limit", "gdn2_selftest_umma",
     "gdn2_chunk_fwd_noalloc", "gdn2_recurrent_update", "gdn2_fg2_inputs", "gdn2_mixer_prologue",
     "gdn2_mixer_epilogue", "gdn2_backward_workspace_size", "gdn2_backward",
-    "gdn2_backward_recurrent_workspace_size", "gdn2_backward_recurrent",
+    "gdn2_backward_recurrent_workspace_size", "gdn2_backward_recurrent", "gdn2_mixer_decode_step",
 )
 
 
@@ -63,6 +63,7 @@ def _load() -> ctypes.CDLL:
         "gdn2_backward": (I, [P] * 16 + [I] * 6 + [F, I, P, Z, P]),
         "gdn2_backward_recurrent_workspace_size": (Z, [I] * 6 + [I]),
         "gdn2_backward_recurrent": (I, [P] * 16 + [I] * 6 + [F, I, P, Z, P]),
+        "gdn2_mixer_decode_step": (I, [P] * 15 + [F, P] + [I] * 6 + [F, I, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -327,3 +328,23 @@ def recurrent_step(q, k, v, g, b, w, state, *, scale=1.0, stream=None):
 
     o = torch.empty(v.shape, dtype=q.dtype, device=q.device)
     return gdn2_recurrent_step(q, k, v, g, b, w, state, o, scale=scale, stream=stream)
+
+
+def gdn2_mixer_decode_step(xq, xk, xv, conv_q, conv_k, conv_v, ag, ab, aw, state, z, weight, y, *,
+                           states=(None, None, None), eps=1e-5, neg_eigval=False, scale=1.0, stream=None):
+    """One decode token of the whole mixer (C ABI gdn2_mixer_decode_step): conv + L2 norm + gates,
+    the recurrent update of `state` (in place) and the gated RMSNorm into `y`.
+
+    xq, xk: [B, H_k, d_k]; xv, z, y: [B, H_v, d_v]; ag, ab: [B, H_v, d_k]; aw: [B, H_v, d_v] (one dtype);
+    conv_*: float32 [channels, 4]; states: float32 conv states [B, 3, channels] or None (updated in
+    place); state: float32 [B, H_v, d_k, d_v]; weight: float32 [d_v].
+    """
+    B, Hk, dk = xq.shape
+    Hv, dv = xv.shape[1], xv.shape[2]
+    sq, sk, sv = states
+    st = lib.gdn2_mixer_decode_step(_ptr(xq), _ptr(xk), _ptr(xv), _ptr(conv_q), _ptr(conv_k), _ptr(conv_v),
+                                    _ptr(ag), _ptr(ab), _ptr(aw), _ptr(sq), _ptr(sk), _ptr(sv), _ptr(state),
+                                    _ptr(z), _ptr(weight), float(eps), _ptr(y), B, Hk, Hv, dk, dv,
+                                    int(bool(neg_eigval)), float(scale), _dtype_code(xq), _stream(stream))
+    _check(st, "gdn2_mixer_decode_step")
+    return y

@@ -255,6 +255,34 @@ gdn2_status gdn2_mixer_epilogue(const void* o, const void* z, const float* weigh
                                 int T, int Hv, int dv, gdn2_dtype dt, void* stream);
 
 /*
+ * gdn2_mixer_decode_step -- one decode token of the whole token mixer around the core in one launch
+ * (burn-gdn2 0.1.5 docs, "Architecture": projections -> ShortConv -> L2-Norm -> Fused Recurrent ->
+ * Gated RMS Norm <- SiLU Gate; the llama.cpp GDN decode study, section 4, suggests fusing the conv and
+ * the gated norm into the delta-net step): the operations of gdn2_mixer_prologue (T = 1),
+ * gdn2_recurrent_step and gdn2_mixer_epilogue in sequence, with q, k, v, the gates and o kept on chip.
+ *   xq, xk            [B, H_k, d_k] dt  projections of the token (before the conv)
+ *   xv                [B, H_v, d_v] dt
+ *   conv_q, conv_k    fp32 [H_k * d_k][4]; conv_v fp32 [H_v * d_v][4] (tap 3 = current token)
+ *   ag, ab            [B, H_v, d_k] dt  gate pre-activations (g = -softplus(ag), b = sigmoid(ab),
+ *   aw                [B, H_v, d_v] dt   x 2 when neg_eigval != 0, w = sigmoid(aw))
+ *   state_q, state_k  fp32 conv states [B][3][H_k * d_k]; state_v [B][3][H_v * d_v]: read, then
+ *                     replaced by the last 3 samples; NULL = zeros in, nothing written
+ *   state             fp32 core state [B, H_v, d_k, d_v], read and written in place
+ *   z                 [B, H_v, d_v] dt  output gate; weight fp32 [d_v]; eps >= 0 (1e-5 in the pages)
+ *   y                 [B, H_v, d_v] dt  output: gated RMSNorm of o = scale * S_new^T q
+ * d_k and d_v in {64, 128}; pointers 16-byte aligned; y must not overlap the inputs. One CTA per
+ * (batch row, key head) runs that key head's value heads in turn, so each conv state has one writer.
+ * Errors: GDN2_ERR_INVALID_ARG (dtype, sizes, H_v % H_k, eps, null required pointer),
+ * GDN2_ERR_UNSUPPORTED (head sizes), GDN2_ERR_MISALIGNED, GDN2_ERR_CUDA. B == 0 is a no-op.
+ * Asynchronous on `stream`.
+ */
+gdn2_status gdn2_mixer_decode_step(const void* xq, const void* xk, const void* xv, const float* conv_q,
+                                   const float* conv_k, const float* conv_v, const void* ag, const void* ab,
+                                   const void* aw, float* state_q, float* state_k, float* state_v, float* state,
+                                   const void* z, const float* weight, float eps, void* y, int B, int Hk, int Hv,
+                                   int dk, int dv, int neg_eigval, float scale, gdn2_dtype dt, void* stream);
+
+/*
  * gdn2_backward -- gradients of the core (dq, dk, dv, dg, db, dw and the initial state) for the
  * recurrence of the burn-gdn2 0.1.5 docs ("Architecture"), given the upstream gradient d_o of o
  * and optionally d_final_state of S_T: the gradients of sum(o * d_o) + sum(S_T * d_final_state).

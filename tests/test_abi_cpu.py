@@ -233,3 +233,22 @@ def test_backward_workspace_sizes(g):
     r = g.lib.gdn2_backward_recurrent_workspace_size(2, 100, 1, 2, 128, 128, 1)
     # one fp32 state per 32-token stretch for each (batch, value head)
     assert r >= units * 128 * 128 * 4
+
+
+def test_mixer_decode_step_argument_errors(g):
+    P = ctypes.c_void_p(0x10000)
+
+    def f(B=1, Hk=1, Hv=2, dk=128, dv=128, dt=1, eps=1e-5, p=P, sq=None):
+        return g.lib.gdn2_mixer_decode_step(p, p, p, p, p, p, p, p, p, sq, None, None, p, p, p, eps, p, B, Hk, Hv, dk,
+                                            dv, 0, 1.0, dt, None)
+
+    assert f(dt=5) == g.GDN2_ERR_INVALID_ARG
+    assert f(Hk=2, Hv=3) == g.GDN2_ERR_INVALID_ARG
+    assert f(eps=-1.0) == g.GDN2_ERR_INVALID_ARG
+    assert f(eps=float("nan")) == g.GDN2_ERR_INVALID_ARG
+    assert f(p=None) == g.GDN2_ERR_INVALID_ARG
+    assert f(dk=32) == g.GDN2_ERR_UNSUPPORTED
+    assert f(dv=256) == g.GDN2_ERR_UNSUPPORTED
+    assert f(p=ctypes.c_void_p(0x10008)) == g.GDN2_ERR_MISALIGNED
+    assert f(sq=ctypes.c_void_p(0x10004)) == g.GDN2_ERR_MISALIGNED
+    assert f(B=0) == g.GDN2_OK
