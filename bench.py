@@ -34,9 +34,11 @@ FLUSH_BYTES = 256 << 20  # > 129 MB L2
 
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one gdn2_chunk_fwd on this
-# workload, from a single-pass ncu capture of factors_tc + state_tc. Reported only while the
-# tensor-core kernel source is the one that was measured.
-TRAFFIC_RECORD = {"chunk_tc_sha256_16": "ddb383fe32ca4778", "bytes": 1732167936 + 2190468608 + 3254820096 + 523984384}
+# workload: a single-pass ncu capture of factors_tc + factors_exact + state_tc on the same heads at a
+# quarter of the tokens (B 2, T 8192: 8192 units, inputs and workspace 1.2 GB >> L2), times 4 (the
+# traffic grows with the units; the ~0.1 GB that stays in L2 across a kernel boundary is not
+# counted). Reported only while the tensor-core kernel source is the one that was measured.
+TRAFFIC_RECORD = {"chunk_tc_sha256_16": "034edefe8e543907", "bytes": 4 * (1837628928)}
 
 
 def recorded_traffic():
@@ -651,14 +653,18 @@ def run_reference(args):
 
 def run_profile(spec: str):
     """One operation of one workload, twice (the second call is the one to capture with ncu -s 1).
-    spec: 'chunk:<workload>', 'decode:<workload>' or 'next:<workload>' (prologue, epilogue, FG2 transform,
-    backward on that workload's shapes)."""
+    spec: 'chunk:<workload>[:T]', 'decode:<workload>' or 'next:<workload>' (prologue, epilogue, FG2
+    transform, backward on that workload's shapes); T overrides the workload's token count (a smaller
+    case of the same heads for captures beyond the one-pass launch list)."""
     import torch
 
     import gated_deltanet_mixer_gdn2_gb300 as g
 
-    op, name = spec.split(":")
+    parts = spec.split(":")
+    op, name = parts[0], parts[1]
     wl = synth.WORKLOADS[name]
+    if len(parts) > 2:
+        wl = wl.with_(T=int(parts[2]))
     device = torch.device("cuda", 0)
     if op == "chunk":
         inp = synth.make_inputs(wl, T=wl.T)
