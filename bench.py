@@ -284,16 +284,19 @@ def run_ours(args, rank, world, device):
                    "l2": "flushed between steps (256 MB write); prefill inputs 2.7 GB > L2",
                    "decode_launch": "the 64 single-token launches replayed from one CUDA graph",
                    "parallelism": f"replicas{world}" if world > 1 else "single GPU"},
-        "roofline": {"kernel": "gdn2_chunk_fwd (factors_tc + state_tc)", "bound": "hbm",
+        "roofline": {"kernel": "gdn2_chunk_fwd (factors_tc + factors_exact + state_tc)", "bound": "hbm",
                      "achieved": round(ach_gbs, 1), "peak": hbm, "unit": "GB/s",
                      "frac": round(ach_gbs / hbm, 4), "traffic": recorded_traffic(),
                      "algorithmic_bytes": cb, "ms": round(ch_ms, 4), "peak_kind": f"{peak_kind} hbm_gbs",
                      "tflops": round(ach_tf, 1), "tc_frac": round(ach_tf / tc_burst, 4),
-                     "tc_peak": tc_burst, "flops": flops},
+                     "tc_peak": tc_burst, "flops": flops,
+                     # the tensor-core fraction the call would reach at the HBM roof: these flops over
+                     # the time its algorithmic bytes take at the measured copy bandwidth
+                     "tc_frac_at_hbm_roof": round(flops / (cb / (hbm * 1e9)) / (tc_burst * 1e12), 4)},
         "decode_in_step": {"us_per_step": round(d_ms * 1e3, 2), "bytes_per_step": dstep_b,
                            "GB/s": round(dstep_b / (d_ms * 1e-3) / 1e9, 1),
                            "note": "4.2 MB state, L2-resident across steps"},
-        "gpu_launches": args.steps * (2 + D),
+        "gpu_launches": args.steps * (3 + D),  # factors_tc, factors_exact, state_tc and the decode steps
         "clocks": clocks,
         "status": g.status_string(status),
         "wall_s_timed": round(wall1 - wall0, 3),
