@@ -565,7 +565,9 @@ __global__ void __launch_bounds__(kGT, 1) grad_kernel(const Tin* __restrict__ q,
             }
             const int o = t * kLS + c4;
             sts4(sm + gk::U0 + o, make_float4(xw.x * xv.x, xw.y * xv.y, xw.z * xv.z, xw.w * xv.w));
-            sts4(sm + gk::G + o, xg);
+            // gates floored as in the forward (a full reset keeps every cumulative sum finite)
+            sts4(sm + gk::G + o, make_float4(fmaxf(xg.x, kGateFloor), fmaxf(xg.y, kGateFloor), fmaxf(xg.z, kGateFloor),
+                                             fmaxf(xg.w, kGateFloor)));
             sts4(sm + gk::K + o, xk);
             sts4(sm + gk::BETA + o, make_float4(xb.x * xk.x, xb.y * xk.y, xb.z * xk.z, xb.w * xk.w));
             sts4(sm + gk::Q + o, xq);

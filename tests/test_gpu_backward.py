@@ -82,21 +82,27 @@ def test_backward_chunked_matches_recurrent_on_long_sequences(g, T, Hk, Hv):
         assert e < 1e-3, (name, e)
 
 
-@pytest.mark.parametrize("decay", ["strong", "none"])
+@pytest.mark.parametrize("decay", ["strong", "none", "reset", "bursts"])
 def test_backward_extreme_decays(g, decay):
     """Gates far from the synthetic recipe: log-decays near -3 per token (products of the pair factors
-    underflow inside a 32-token chunk) and no decay at all (every factor is 1)."""
+    underflow inside a 32-token chunk), no decay at all (every factor is 1), full resets (alpha = 0,
+    g = -inf, at random positions and on whole tokens) and runs of g = -20."""
     import torch
 
     T = 70
-    wl = synth.Workload("bwd-decay", B=1, T=T, Hk=1, Hv=2, dk=128, dv=128, dtype="f32", seed=7, s0_std=0.02)
-    inp = synth.make_inputs(wl)
     rng = np.random.default_rng(11)
-    if decay == "strong":
-        gg = -np.log1p(np.exp(rng.normal(3.0, 1.0, inp.g.shape)))
+    if decay in ("reset", "bursts"):
+        wl = synth.Workload("bwd-decay", B=1, T=T, Hk=1, Hv=2, dk=128, dv=128, dtype="f32", seed=7, s0_std=0.02,
+                            decay=decay)
+        inp = synth.make_inputs(wl)
     else:
-        gg = np.zeros(inp.g.shape)
-    inp = dataclasses.replace(inp, g=gg.astype(np.float32).astype(np.float64))
+        wl = synth.Workload("bwd-decay", B=1, T=T, Hk=1, Hv=2, dk=128, dv=128, dtype="f32", seed=7, s0_std=0.02)
+        inp = synth.make_inputs(wl)
+        if decay == "strong":
+            gg = -np.log1p(np.exp(rng.normal(3.0, 1.0, inp.g.shape)))
+        else:
+            gg = np.zeros(inp.g.shape)
+        inp = dataclasses.replace(inp, g=gg.astype(np.float32).astype(np.float64))
     d_o = rng.standard_normal((1, T, 2, 128)).astype(np.float32).astype(np.float64)
     ds_t = (0.1 * rng.standard_normal((1, 2, 128, 128))).astype(np.float32).astype(np.float64)
     dev = lambda a: synth.to_torch(np.ascontiguousarray(a), "f32", "cuda")
