@@ -431,7 +431,7 @@ def next_rows_rooflines(g, device, hbm, wl):
     sms = torch.cuda.get_device_properties(device).multi_processor_count
     peak_tf = sms * 128 * 2 * 2.07e9 / 1e12          # fp32 lanes x FMA x max SM clock
     ach = flops / (ms * 1e-3) / 1e12
-    res["backward"] = {"kernel": "gdn2_backward (factors_simt_kernel + save_chain_kernel + adjoint_kernel + "
+    res["backward"] = {"kernel": "gdn2_backward (factors_simt_kernel + chains_kernel (both chains) + "
                                  "grad_kernel + group_sum2_kernel)", "ms": round(ms, 3),
                        "algorithmic_flops": int(flops), "achieved": round(ach, 2), "peak": round(peak_tf, 1),
                        "unit": "TFLOP/s", "frac": round(ach / peak_tf, 4), "bound": "alu",

@@ -14,14 +14,13 @@
 // and through the elementwise factors to dq, dk, db, dg, dv, dw; every exponential factor of A and M is
 // <= 1, so no factor can overflow whatever the decays.
 //
-// Five launches: the state-independent factors of every chunk (factors_simt_kernel in token-major form,
-// plus T); the chain over chunks forward (save_chain_kernel: keeps S_n and U_n) and in reverse
-// (adjoint_kernel: keeps dS_{n+1} and dU_n), each one CTA per (batch-head, 64 columns of d_v) with its
-// state slice in registers; the per-token gradients of every (chunk, head) in parallel (grad_kernel,
+// Four launches, all on the caller's stream: the state-independent factors of every chunk
+// (factors_simt_kernel in token-major form, plus T); the chain over chunks forward (keeps S_n and U_n)
+// and in reverse (keeps dS_{n+1} and dU_n) side by side in one launch (chains_kernel), each chain one
+// CTA per (batch-head, 64 columns of d_v) with its state slice in registers; the per-token gradients of every (chunk, head) in parallel (grad_kernel,
 // one 512-thread CTA per SM); the sums of dq, dk over each key head's group. Within a chunk the pair
 // factors e^{G_t - G_s} of tokens in different 8-token blocks are split at a block edge into two
 // factors <= 1.
-#include <mutex>
 #include <type_traits>
 
 #include "common.cuh"
@@ -141,7 +140,7 @@ __device__ __forceinline__ void outer8x4(float (&a)[8][4], float4 x0, float4 x1,
     }
 }
 
-namespace fc {  // shared-memory map of save_chain_kernel (floats)
+namespace fc {  // shared-memory map of the forward chain (floats)
 constexpr int S = 0;                          // S_n [128][kLJ]
 constexpr int U = S + kD * kLJ;               // U [32][kLJ]
 constexpr int RED = U + kCb * kLJ;            // [4][32][64] partial rows products of the warp groups
@@ -152,11 +151,11 @@ constexpr int TOTAL = BUF + 2 * BUF_FLOATS;
 
 // Forward chain keeping, for every chunk n, S_n (the state entering it) and U_n = U~_n - W_n S_n:
 //     S_{n+1} = diag(e^{G_last}) S_n + K^_n^T U_n.
-__global__ void __launch_bounds__(kCT, 1) save_chain_kernel(const float* __restrict__ ws, const float* __restrict__ s0,
-                                                           float* __restrict__ s_save, float* __restrict__ u_save,
-                                                           int NC) {
+__device__ __forceinline__ void save_chain(const float* __restrict__ ws, const float* __restrict__ s0,
+                                           float* __restrict__ s_save, float* __restrict__ u_save, int NC, int bh,
+                                           int col0) {
     extern __shared__ __align__(16) float sm[];
-    const int bh = blockIdx.x, col0 = blockIdx.y * kSl, tid = threadIdx.x;
+    const int tid = threadIdx.x;
     const SimtWs L{kD, kD, kCb, true};
     const ChainRoles R(tid);
     const int c_own = 8 * R.w + 4 * R.kh;  // first of the lane's four state rows
@@ -250,7 +249,7 @@ __global__ void __launch_bounds__(kCT, 1) save_chain_kernel(const float* __restr
     }
 }
 
-namespace ac {  // shared-memory map of adjoint_kernel (floats)
+namespace ac {  // shared-memory map of the reverse chain (floats)
 constexpr int R = 0;                          // dS_{n+1} [128][kLJ]
 constexpr int DU = R + kD * kLJ;              // dU [32][kLJ]
 constexpr int RED = DU + kCb * kLJ;           // [4][32][64] partial rows products of the warp groups
@@ -264,12 +263,12 @@ constexpr int TOTAL = BUF + 2 * BUF_FLOATS;
 //     dU_n = M_n^T dO~_n + K^_n dS_{n+1},   dS_n = diag(e^{G_last}) dS_{n+1} + Q_bar_n^T dO~_n - W_n^T dU_n,
 // keeping dS_{n+1} and dU_n of every chunk and writing dS_0.
 template <typename Tin>
-__global__ void __launch_bounds__(kCT, 1) adjoint_kernel(const float* __restrict__ ws, const Tin* __restrict__ dO,
-                                                        const float* __restrict__ dsT, float* __restrict__ ds0,
-                                                        float* __restrict__ ds_save, float* __restrict__ du_save,
-                                                        int T, int Hv, int NC, float scale) {
+__device__ __forceinline__ void adjoint_chain(const float* __restrict__ ws, const Tin* __restrict__ dO,
+                                              const float* __restrict__ dsT, float* __restrict__ ds0,
+                                              float* __restrict__ ds_save, float* __restrict__ du_save, int T, int Hv,
+                                              int NC, float scale, int bh, int col0) {
     extern __shared__ __align__(16) float sm[];
-    const int bh = blockIdx.x, bi = bh / Hv, hv = bh - bi * Hv, col0 = blockIdx.y * kSl, tid = threadIdx.x;
+    const int bi = bh / Hv, hv = bh - bi * Hv, tid = threadIdx.x;
     const SimtWs L{kD, kD, kCb, true};
     const ChainRoles R(tid);
     const int c_own = 8 * R.w + 4 * R.kh;
@@ -422,6 +421,22 @@ constexpr int TOTAL = DBT + 4 * kD;
 //      factor e^{G_t - G_s} of two tokens in different blocks split at a block edge r between them into
 //      e^{G_t - G_r} e^{G_r - G_s}, both <= 1, so the sums over the other block are plain products
 //   5. dq, dk (fp32, per value head), db and dg = reverse cumulative sum of dG plus dG_last.
+// Both chains in one launch: blockIdx.y < kD / kSl runs the backward chain on column slice blockIdx.y,
+// the rest the forward chain (they only read the factors and write disjoint buffers, so they run side
+// by side; the longer backward chain has the lower block indices and starts first).
+template <typename Tin>
+__global__ void __launch_bounds__(kCT, 1) chains_kernel(const float* __restrict__ ws, const float* __restrict__ s0,
+                                                       float* __restrict__ s_save, float* __restrict__ u_save,
+                                                       const Tin* __restrict__ dO, const float* __restrict__ dsT,
+                                                       float* __restrict__ ds0, float* __restrict__ ds_save,
+                                                       float* __restrict__ du_save, int T, int Hv, int NC, float scale) {
+    constexpr int kSlices = kD / kSl;
+    if (blockIdx.y < kSlices)
+        adjoint_chain<Tin>(ws, dO, dsT, ds0, ds_save, du_save, T, Hv, NC, scale, blockIdx.x, blockIdx.y * kSl);
+    else
+        save_chain(ws, s0, s_save, u_save, NC, blockIdx.x, (blockIdx.y - kSlices) * kSl);
+}
+
 template <typename Tin>
 __global__ void __launch_bounds__(kGT, 1) grad_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k,
                                                       const Tin* __restrict__ v, const Tin* __restrict__ g,
@@ -881,27 +896,6 @@ __global__ void __launch_bounds__(256) group_sum2_kernel(const float* __restrict
     }
 }
 
-// A second stream per device for the backward chain, which runs beside the forward chain (both only
-// read the factors and write disjoint buffers), between a fork and a join event on the caller's stream.
-constexpr int kMaxDevices = 64;
-struct SideStream {
-    cudaStream_t stream = nullptr;
-    cudaEvent_t fork = nullptr, join = nullptr;
-};
-std::mutex g_side_mu;
-SideStream g_side[kMaxDevices];
-
-cudaError_t side_stream(int dev, SideStream** out) {
-    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    SideStream& x = g_side[dev];
-    cudaError_t e;
-    if (!x.stream && (e = cudaStreamCreateWithFlags(&x.stream, cudaStreamNonBlocking)) != cudaSuccess) return e;
-    if (!x.fork && (e = cudaEventCreateWithFlags(&x.fork, cudaEventDisableTiming)) != cudaSuccess) return e;
-    if (!x.join && (e = cudaEventCreateWithFlags(&x.join, cudaEventDisableTiming)) != cudaSuccess) return e;
-    *out = &x;
-    return cudaSuccess;
-}
-
 struct ChunkBwdLayout {
     size_t simt, t, s, u, ds, du, dq, dk, total;
 };
@@ -941,31 +935,16 @@ cudaError_t launch_t(const void* q, const void* k, const void* v, const void* g,
                                         simt, t_ws, /*token_major=*/true, s);
     if (e != cudaSuccess) return e;
     const size_t c_smem = sizeof(float) * (size_t)fc::TOTAL, a_smem = sizeof(float) * (size_t)ac::TOTAL;
+    const size_t ch_smem = c_smem > a_smem ? c_smem : a_smem;
     const size_t g_smem = sizeof(float) * (size_t)gk::TOTAL;
-    e = cudaFuncSetAttribute(save_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)c_smem);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(adjoint_kernel<Tin>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)a_smem);
+    e = cudaFuncSetAttribute(chains_kernel<Tin>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ch_smem);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(grad_kernel<Tin>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)g_smem);
     if (e != cudaSuccess) return e;
-    {   // the two chains side by side: the forward one on the caller's stream, the backward one on the side
-        // stream between a fork and a join (the enqueueing is serialised per process so that the events
-        // can be reused)
-        int dev = 0;
-        if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-        std::lock_guard<std::mutex> lock(g_side_mu);
-        SideStream* side = nullptr;
-        if ((e = side_stream(dev, &side)) != cudaSuccess) return e;
-        if ((e = cudaEventRecord(side->fork, s)) != cudaSuccess) return e;
-        if ((e = cudaStreamWaitEvent(side->stream, side->fork, 0)) != cudaSuccess) return e;
-        save_chain_kernel<<<dim3(B * Hv, kD / kSl), kCT, c_smem, s>>>(simt, s0, s_save, u_save, NC);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        adjoint_kernel<Tin><<<dim3(B * Hv, kD / kSl), kCT, a_smem, side->stream>>>(
-            simt, static_cast<const Tin*>(d_o), dsT, ds0, ds_save, du_save, T, Hv, NC, scale);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        if ((e = cudaEventRecord(side->join, side->stream)) != cudaSuccess) return e;
-        if ((e = cudaStreamWaitEvent(s, side->join, 0)) != cudaSuccess) return e;
-    }
+    // the two chains side by side in one launch, on the caller's stream
+    chains_kernel<Tin><<<dim3(B * Hv, 2 * (kD / kSl)), kCT, ch_smem, s>>>(
+        simt, s0, s_save, u_save, static_cast<const Tin*>(d_o), dsT, ds0, ds_save, du_save, T, Hv, NC, scale);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
     grad_kernel<Tin><<<dim3(NC, B * Hv), kGT, g_smem, s>>>(
         static_cast<const Tin*>(q), static_cast<const Tin*>(k), static_cast<const Tin*>(v), static_cast<const Tin*>(g),
         static_cast<const Tin*>(b), static_cast<const Tin*>(w), static_cast<const Tin*>(d_o), t_ws, s_save, u_save,

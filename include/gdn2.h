@@ -299,11 +299,9 @@ gdn2_status gdn2_mixer_decode_step(const void* xq, const void* xk, const void* x
  * (zeros / not written). dq and dk of a key head sum its value heads. d_k = d_v = 128,
  * B * H_v <= 65535 (GDN2_ERR_UNSUPPORTED otherwise).
  * workspace: gdn2_backward_workspace_size(...) bytes of device memory, 16-byte aligned.
- * Errors: as gdn2_chunk_fwd. Asynchronous on `stream`: the backward chain runs on a library-owned
- * stream of the current device between an event recorded on `stream` and one that `stream` then
- * waits for, so the call stays ordered on `stream` and can be captured in a CUDA graph (the first
- * call on a device creates that stream and its events: make it before capturing). Enqueueing from
- * several host threads is serialised inside the library.
+ * Errors: as gdn2_chunk_fwd. Asynchronous on `stream`: every launch goes to `stream` (the forward
+ * and reverse chains over chunks run side by side inside one launch), the library holds no stream,
+ * event or lock of its own, and the call can be captured in a CUDA graph.
  */
 size_t gdn2_backward_workspace_size(int B, int T, int Hk, int Hv, int dk, int dv, gdn2_dtype dt);
 gdn2_status gdn2_backward(const void* q, const void* k, const void* v, const void* g, const void* b, const void* w,

@@ -152,8 +152,8 @@ def test_backward_chunked_matches_recurrent_at_the_bench_shape(g):
 
 
 def test_backward_in_a_cuda_graph(g):
-    """The chunked backward forks its second chain onto a side stream and joins it back: captured in a
-    CUDA graph and replayed, it gives the same gradients as the eager call."""
+    """The chunked backward, captured in a CUDA graph on a side stream of the caller's and replayed,
+    gives the same gradients as the eager call."""
     import torch
 
     T = 100
