@@ -12,7 +12,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libgdn2.so")
-SOURCES = ["api.cu", "decode.cu", "chunk_simt.cu", "chunk_tc.cu", "noalloc.cu", "transforms.cu", "mixer.cu", "mixer_step.cu", "backward.cu", "backward_chunk.cu"]
+SOURCES = ["api.cu", "decode.cu", "chunk_simt.cu", "chunk_tc.cu", "noalloc.cu", "transforms.cu", "mixer.cu", "mixer_step.cu", "backward.cu", "backward_chunk.cu", "backward_tc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", os.path.join(ROOT, "include"),
          "--expt-relaxed-constexpr"]

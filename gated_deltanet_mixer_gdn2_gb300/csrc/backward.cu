@@ -408,7 +408,7 @@ extern "C" {
 
 size_t gdn2_backward_workspace_size(int B, int T, int Hk, int Hv, int dk, int dv, gdn2_dtype dt) {
     if ((dt != GDN2_F32 && dt != GDN2_BF16) || !bwd_shape_ok(B, T, Hk, Hv, dk, dv) || B == 0 || T == 0) return 0;
-    return backward_chunked_workspace_bytes(B, T, Hv);
+    return dt == GDN2_BF16 ? backward_tc_workspace_bytes(B, T, Hv) : backward_chunked_workspace_bytes(B, T, Hv);
 }
 
 gdn2_status gdn2_backward(const void* q, const void* k, const void* v, const void* g, const void* b, const void* w,
@@ -418,11 +418,16 @@ gdn2_status gdn2_backward(const void* q, const void* k, const void* v, const voi
                           void* stream) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     bool done;
-    const size_t need = bwd_shape_ok(B, T, Hk, Hv, d_k, d_v) && B > 0 && T > 0 ? backward_chunked_workspace_bytes(B, T, Hv) : 0;
+    const size_t need = gdn2_backward_workspace_size(B, T, Hk, Hv, d_k, d_v, dt);
     const gdn2_status st = check_and_trivial(q, k, v, g, b, w, initial_state, d_o, d_final_state, dq, dk, dv, dg, db,
                                              dw, d_initial_state, B, T, Hk, Hv, d_k, d_v, dt, workspace, ws_bytes, need,
                                              s, &done);
     if (done) return st;
+    if (dt == GDN2_BF16)  // tensor cores: chunks of 64, bf16 operands, fp32 accumulators and state
+        return launch_backward_tc(q, k, v, g, b, w, initial_state, d_o, d_final_state, dq, dk, dv, dg, db, dw,
+                                  d_initial_state, B, T, Hk, Hv, scale, workspace, s, wait_limit_ns()) == cudaSuccess
+                   ? GDN2_OK
+                   : GDN2_ERR_CUDA;
     return launch_backward_chunked(q, k, v, g, b, w, initial_state, d_o, d_final_state, dq, dk, dv, dg, db, dw,
                                    d_initial_state, B, T, Hk, Hv, scale, dt, workspace, s) == cudaSuccess
                ? GDN2_OK

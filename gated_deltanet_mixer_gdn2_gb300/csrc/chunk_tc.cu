@@ -27,67 +27,19 @@
 
 #include "common.cuh"
 #include "ptx.cuh"
+#include "tc_common.cuh"
 
 namespace gdn2 {
 
 namespace {
 
-__device__ int g_status_tc;
 
-constexpr int kC = 64;
-constexpr int kD = 128;
 
 // Largest per-channel span G_0 - G_last of the (floored) cumulative log-decay within one chunk that
 // the anchored operands take: every factor then lies in [e^-60, e^60], far inside bf16's range
 // (operands down to |x| ~ 1e-12 keep their value after the e^-60 scaling). Wider chunks go to the
 // exact kernel.
 constexpr float kSpanAnchored = 120.f;
-
-// workspace unit (one chunk of one value head), bytes
-constexpr uint32_t kWsW = 0;         // -W = -T (b.k.e^G)    token-major [64][128] bf16
-constexpr uint32_t kWsQb = 16384;    // q.e^G                token-major [64][128] bf16
-constexpr uint32_t kWsKh = 32768;    // k.e^{G_last - G}     token-major [64][128] bf16
-constexpr uint32_t kWsM = 49152;     // M = causal q-k       [64][64] bf16
-constexpr uint32_t kWsT = 57344;     // T = (I + A)^{-1}      [64][64] bf16
-constexpr uint32_t kWsGam = 65536;   // e^{G_last}           [128] fp32
-constexpr uint32_t kWsUnit = 66048;
-
-// ---------------------------------------------------------------------------------------------
-// helpers
-
-__device__ __forceinline__ void record_timeout() { atomicOr(&g_status_tc, kStatusTimeout); }
-
-// CTA-uniform bounded wait: thread 0 polls with the caller's budget; on failure it records the
-// timeout and drains the barrier with the default budget (copies / MMAs in flight must land before
-// the CTA releases its shared memory and TMEM). Everyone returns the same verdict.
-__device__ __forceinline__ bool cta_wait(uint64_t* bar, uint32_t parity, long long limit_ns, int* flag) {
-    if (threadIdx.x == 0) {
-        bool ok = mbar_wait(bar, parity, limit_ns);
-        if (!ok) {
-            record_timeout();
-            mbar_wait(bar, parity, kDefaultWaitNs);
-        }
-        *flag = ok ? 1 : 0;
-    }
-    __syncthreads();
-    const bool ok = *flag != 0;
-    if (ok) mbar_wait(bar, parity, kDefaultWaitNs);  // completes at once; orders the async writes
-    return ok;
-}
-
-
-
-// 64 fp32 columns of this warp's TMEM lanes starting at column `col`.
-__device__ __forceinline__ void tmem_ld64(uint32_t tmem_base, int warp, int col, float (&x)[64]) {
-    uint32_t r[16];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        tmem_ld16(tmem_base + (static_cast<uint32_t>(32 * warp) << 16) + col + 16 * q, r);
-        tmem_ld_wait();
-#pragma unroll
-        for (int i = 0; i < 16; ++i) x[16 * q + i] = __uint_as_float(r[i]);
-    }
-}
 
 
 // ---------------------------------------------------------------------------------------------
@@ -119,43 +71,6 @@ constexpr uint32_t TB = 40960;
 constexpr uint32_t WSTG = 0;
 constexpr int kThreads = 256;
 }  // namespace fs
-
-__device__ __forceinline__ void unpack8(const uint4& u, float (&x)[8]) {
-    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const float2 f = __bfloat1622float2(h[i]);
-        x[2 * i] = f.x;
-        x[2 * i + 1] = f.y;
-    }
-}
-__device__ __forceinline__ uint4 pack8(const float (&x)[8]) {
-    return make_uint4(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]), pack_bf16x2(x[4], x[5]),
-                      pack_bf16x2(x[6], x[7]));
-}
-
-// Issue n16 x 16-column TMEM loads of this warp's lanes, then one wait.
-template <int N16>
-__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float (&x)[16 * N16]) {
-    uint32_t r[N16][16];
-#pragma unroll
-    for (int q = 0; q < N16; ++q) tmem_ld16(taddr + 16 * q, r[q]);
-    tmem_ld_wait();
-#pragma unroll
-    for (int q = 0; q < N16; ++q)
-#pragma unroll
-        for (int i = 0; i < 16; ++i) x[16 * q + i] = __uint_as_float(r[q][i]);
-}
-
-__device__ __forceinline__ void tma_store_3d(const void* map, const void* src, int c0, int c1, int c2) {
-    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
-                     reinterpret_cast<uint64_t>(map)),
-                 "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2)
-                 : "memory");
-}
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // acc[i][c] += sum_{k = 4 g0}^{4 g1 - 1} L[i][k] R[k][c] for a 2 x 4 register tile (fp32 smem, 16-byte
 // aligned rows ldl / ldr floats apart); k runs upwards, one FMA per term.
@@ -752,61 +667,6 @@ constexpr int kThreads = 10 * 32;
 constexpr uint32_t kDuo = 0, kDs = 128, kCols = 256;
 }  // namespace ss
 
-__device__ __forceinline__ void mbar_arrive1(uint64_t* bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
-// Bounded wait that also gives up as soon as another role has recorded a failure in *err.
-__device__ __forceinline__ bool mbar_wait_or_abort(uint64_t* bar, uint32_t parity, long long limit_ns,
-                                                   volatile int* err) {
-    if (limit_ns <= 0) return false;
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
-    for (;;) {
-        if (mbar_try_wait_sleep(bar, parity, kWaitHintNs)) return true;
-        if (*err) return false;
-        if ((long long)(globaltimer_ns() - t0) > limit_ns) return false;
-    }
-}
-
-__device__ __forceinline__ void note_failure(volatile int* err) {
-    if (!*err) {
-        record_timeout();
-        *err = 1;
-    }
-}
-
-// Warp-uniform wait: lane 0 polls (and records a timeout), the verdict is broadcast, and every lane
-// then observes the completed phase itself.
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, long long limit_ns, volatile int* err) {
-    int ok = 0;
-    if ((threadIdx.x & 31) == 0) {
-        ok = mbar_wait_or_abort(bar, parity, limit_ns, err) ? 1 : 0;
-        if (!ok) note_failure(err);
-    }
-    ok = __shfl_sync(0xffffffffu, ok, 0);
-    if (ok) mbar_wait(bar, parity, kDefaultWaitNs);
-    return ok != 0;
-}
-
-// 32 fp32 values -> bf16 into four 16-byte chunks (c0..c0+3) of a 128-byte-swizzled row
-__device__ __forceinline__ void st_row_bf16x32(uint8_t* tile, int row, int c0, const float* x) {
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-        float y[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) y[e] = x[8 * c + e];
-        *reinterpret_cast<uint4*>(tile + row * 128 + (((c0 + c) ^ (row & 7)) << 4)) = pack8(y);
-    }
-}
-
-__device__ __forceinline__ void tma_store_4d(const void* map, const void* src, int c0, int c1, int c2, int c3) {
-    asm volatile("cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(
-                     reinterpret_cast<uint64_t>(map)),
-                 "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
-                 : "memory");
-}
-
 // The chunk recurrence for 64 of the d_v columns, d_v / 64 CTAs per (batch, value head): the columns of S
 // evolve independently, so each CTA keeps its d_k x 64 slice of the state. Per chunk n, with the
 // factors of the workspace,
@@ -824,7 +684,8 @@ __device__ __forceinline__ void tma_store_4d(const void* map, const void* src, i
 __global__ void __launch_bounds__(ss::kThreads, 1)
     state_tc_kernel(const __grid_constant__ StateMaps maps, const uint8_t* __restrict__ ws,
                     const float* __restrict__ s0, float* __restrict__ sT_out, int Hv, int dk, int dv, int NC,
-                    float scale, long long wait_ns) {
+                    float scale, __nv_bfloat16* __restrict__ s_save, __nv_bfloat16* __restrict__ u_save,
+                    int write_o, long long wait_ns) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(sm);
@@ -1049,7 +910,7 @@ __global__ void __launch_bounds__(ss::kThreads, 1)
                 for (int h = 0; h < 2; ++h) st_row_bf16x32(stg, lane, 4 * h, x + 32 * h);
                 fence_proxy_async_smem();
                 __syncwarp();
-                if (lane == 0) {
+                if (lane == 0 && write_o) {
                     // rows past T are clipped by the tensor map
                     tma_store_4d(&maps.o_st, stg, 64 * hc, hv, m * kC + 32 * (q4 - 2), bi);
                     bulk_commit();
@@ -1101,6 +962,7 @@ __global__ void __launch_bounds__(ss::kThreads, 1)
             st_row_bf16x32(sbt, r, 4, sx + 32);
             fence_proxy_async_smem();
             arrive(s_ready);
+            if (s_save && real_row) st_global_bf16x64(s_save + (static_cast<size_t>(bh) * NC * dk + r) * dv + 64 * hc, sx);
             ok = decay(0, sx);
         }
         for (int n = 0; ok && n < NC; ++n) {
@@ -1115,6 +977,7 @@ __global__ void __launch_bounds__(ss::kThreads, 1)
                 fence_proxy_async_smem();
                 tc_fence_before();
                 arrive(u_ready);
+                if (u_save) st_global_bf16x64(u_save + ((static_cast<size_t>(bh) * NC + n) * kC + r) * dv + 64 * hc, x);
             }
             if (!(ok = warp_wait(s_done, n & 1, wait_ns, err))) break;
             tc_fence_after();
@@ -1129,6 +992,8 @@ __global__ void __launch_bounds__(ss::kThreads, 1)
             fence_proxy_async_smem();
             tc_fence_before();
             arrive(s_ready);
+            if (s_save && real_row && n + 1 < NC)
+                st_global_bf16x64(s_save + ((static_cast<size_t>(bh) * NC + n + 1) * dk + r) * dv + 64 * hc, sx);
             if (n + 1 < NC) {
                 if (!(ok = decay(n + 1, sx))) break;
             } else if (sT_out && real_row) {
@@ -1271,67 +1136,6 @@ __global__ void __launch_bounds__(128, 1)
     if (warp == 0) tmem_dealloc(tmem, 256);
 }
 
-// ---------------------------------------------------------------------------------------------
-// host: tensor maps
-
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = []() -> EncodeTiledFn {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult qr;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &qr) !=
-                cudaSuccess ||
-            qr != cudaDriverEntryPointSuccess)
-            return nullptr;
-        return reinterpret_cast<EncodeTiledFn>(p);
-    }();
-    return fn;
-}
-
-bool make_map(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base, const uint64_t* dims,
-              const uint64_t* strides_bytes, const uint32_t* box, CUtensorMapSwizzle sw) {
-    EncodeTiledFn f = encode_fn();
-    if (!f) return false;
-    cuuint64_t gd[5], gs[4];
-    cuuint32_t bx[5], es[5];
-    for (int i = 0; i < rank; ++i) {
-        gd[i] = dims[i];
-        bx[i] = box[i];
-        es[i] = 1;
-    }
-    for (int i = 0; i < rank - 1; ++i) gs[i] = strides_bytes[i];
-    return f(m, dt, rank, const_cast<void*>(base), gd, gs, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-// token tensor [B, T, H, d] bf16 (d = 128 unless given) viewed as (d, H, T, B); box (64, 1, 64, 1)
-bool token_map(CUtensorMap* m, const void* p, int B, int T, int H, int d = kD) {
-    const uint64_t dims[4] = {(uint64_t)d, (uint64_t)H, (uint64_t)T, (uint64_t)B};
-    const uint64_t st[3] = {(uint64_t)d * 2, (uint64_t)H * d * 2, (uint64_t)T * H * d * 2};
-    const uint32_t box[4] = {64, 1, kC, 1};
-    return make_map(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, p, dims, st, box, CU_TENSOR_MAP_SWIZZLE_128B);
-}
-
-// output [B, T, H, d_v] bf16 viewed as (d_v, H, T, B); box (64, 1, 32, 1), 128-byte swizzle
-bool out_map(CUtensorMap* m, const void* p, int B, int T, int H, int dv) {
-    const uint64_t dims[4] = {(uint64_t)dv, (uint64_t)H, (uint64_t)T, (uint64_t)B};
-    const uint64_t st[3] = {(uint64_t)dv * 2, (uint64_t)H * dv * 2, (uint64_t)T * H * dv * 2};
-    const uint32_t box[4] = {64, 1, 32, 1};
-    return make_map(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, p, dims, st, box, CU_TENSOR_MAP_SWIZZLE_128B);
-}
-
-// workspace section viewed as (cols, rows, units); box (box_cols, box_rows, 1)
-bool ws_map(CUtensorMap* m, const void* p, CUtensorMapDataType dt, int esize, int cols, int rows, int units,
-            int box_cols, int box_rows, CUtensorMapSwizzle sw) {
-    const uint64_t dims[3] = {(uint64_t)cols, (uint64_t)rows, (uint64_t)units};
-    const uint64_t st[2] = {(uint64_t)cols * esize, kWsUnit};
-    const uint32_t box[3] = {(uint32_t)box_cols, (uint32_t)box_rows, 1};
-    return make_map(m, dt, 3, p, dims, st, box, sw);
-}
-
 }  // namespace
 
 // Workspace: the 66 048-byte units, (batch . value head, chunk) order, then the list of units that
@@ -1343,7 +1147,7 @@ size_t chunk_tc_workspace_bytes(const ChunkShape& sh) {
 
 cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const void* g, const void* b,
                             const void* w, const float* s0, float* sT, void* o, const ChunkShape& sh, float scale,
-                            void* ws, cudaStream_t s, long long wait_ns) {
+                            void* ws, cudaStream_t s, long long wait_ns, void* s_save, void* u_save) {
     const int NC = sh.nchunks();
     const int units = NC * sh.B * sh.Hv;
     uint8_t* wsb = static_cast<uint8_t*>(ws);
@@ -1364,7 +1168,7 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const v
         !ws_map(&sm_.m, wsb + kWsM, BF, 2, 64, 64, units, 64, 64, SW) ||
         !ws_map(&sm_.t, wsb + kWsT, BF, 2, 64, 64, units, 64, 64, SW) ||
         !token_map(&sm_.v, v, sh.B, sh.T, sh.Hv, sh.dv) || !token_map(&sm_.wg, w, sh.B, sh.T, sh.Hv, sh.dv) ||
-        !out_map(&sm_.o_st, o, sh.B, sh.T, sh.Hv, sh.dv))
+        !out_map(&sm_.o_st, o ? o : ws, sh.B, sh.T, sh.Hv, sh.dv))  // no output: a map that is never used
         return cudaErrorInvalidValue;
 
     // The state kernel runs one CTA per SM, so it takes the whole 227 KB: operand descriptors can
@@ -1394,7 +1198,8 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const v
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     state_tc_kernel<<<dim3((sh.dv / 64) * sh.B * sh.Hv), ss::kThreads, s_smem, s>>>(sm_, wsb, s0, sT, sh.Hv, sh.dk,
-                                                                                  sh.dv, NC, scale, wait_ns);
+                                                                                  sh.dv, NC, scale, static_cast<__nv_bfloat16*>(s_save), static_cast<__nv_bfloat16*>(u_save), o != nullptr,
+        wait_ns);
     return cudaGetLastError();
 }
 

@@ -151,6 +151,14 @@ cudaError_t launch_chunk_simt(const void* q, const void* k, const void* v, const
 size_t chunk_tc_workspace_bytes(const ChunkShape& sh);
 cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const void* g, const void* b,
                             const void* w, const float* s0, float* sT, void* o, const ChunkShape& sh, float scale,
-                            void* ws, cudaStream_t s, long long wait_ns);
+                            void* ws, cudaStream_t s, long long wait_ns, void* s_save = nullptr,
+                            void* u_save = nullptr);
+// Tensor-core chunked backward (bf16, d_k = d_v = 128, chunks of 64).
+size_t backward_tc_workspace_bytes(int B, int T, int Hv);
+cudaError_t launch_backward_tc(const void* q, const void* k, const void* v, const void* g, const void* b,
+                               const void* w, const float* s0, const void* d_o, const float* dsT, void* dq, void* dk,
+                               void* dv, void* dg, void* db, void* dw, float* ds0, int B, int T, int Hk, int Hv,
+                               float scale, void* ws, cudaStream_t s, long long wait_ns);
+int backward_tc_read_clear_status(cudaStream_t s);
 
 }  // namespace gdn2

@@ -226,10 +226,15 @@ def test_backward_argument_errors(g, entry):
 
 
 def test_backward_workspace_sizes(g):
-    n = g.lib.gdn2_backward_workspace_size(2, 100, 1, 2, 128, 128, 1)
+    n = g.lib.gdn2_backward_workspace_size(2, 100, 1, 2, 128, 128, g.GDN2_F32)
     units = 2 * 2 * ((100 + 31) // 32)   # (batch, value head, 32-token chunk)
-    # per unit: S entering and dS leaving the chunk, U and dU, T; then fp32 dq and dk per value head
+    # fp32 path, per unit: S entering and dS leaving the chunk, U and dU, T; then fp32 dq and dk per value head
     assert n >= units * (2 * 128 * 128 + 2 * 32 * 128 + 32 * 32) * 4 + 2 * 2 * 100 * 2 * 128 * 4
+    nb = g.lib.gdn2_backward_workspace_size(2, 100, 1, 2, 128, 128, g.GDN2_BF16)
+    units64 = 2 * 2 * ((100 + 63) // 64)  # (batch, value head, 64-token chunk)
+    # tensor-core path, per unit: the forward factors (66 048 bytes), bf16 S, dS', U, dU; then fp32 dq and dk
+    # per value head
+    assert nb >= units64 * (66048 + (2 * 128 * 128 + 2 * 64 * 128) * 2) + 2 * 2 * 100 * 2 * 128 * 4
     r = g.lib.gdn2_backward_recurrent_workspace_size(2, 100, 1, 2, 128, 128, 1)
     # one fp32 state per 32-token stretch for each (batch, value head)
     assert r >= units * 128 * 128 * 4
