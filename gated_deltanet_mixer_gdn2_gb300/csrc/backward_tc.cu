@@ -482,9 +482,9 @@ __global__ void __launch_bounds__(gs::kThreads, 1)
         if (tid >= 128) {  // dgamma_c = sum over d_v of dS'[c][v] S[c][v] (both tiles carry the same swizzle)
             const int c = tid - 128;
             float acc = 0.f;
-#pragma unroll
+#pragma unroll 1
             for (int j = 0; j < 2; ++j)
-#pragma unroll
+#pragma unroll 2
                 for (int p = 0; p < 8; ++p) {
                     float x[8], y[8];
                     const int o = c * 128 + ((p ^ (c & 7)) << 4);  // 8 lanes, 8 different 16-byte pieces
@@ -515,20 +515,30 @@ __global__ void __launch_bounds__(gs::kThreads, 1)
             uint8_t* tile = sm + (h ? gs::DW1 : gs::DW0);
             st_row_bf16x32(tile, t, 0, x);
             st_row_bf16x32(tile, t, 4, x + 32);
-        } else {  // G (floored gates, inclusive sum over the chunk) and K_bar = b.k.e^G: thread = channel c
+        } else {  // G (floored gates, inclusive sum over the chunk): thread = channel c
             const int c = 64 * h + 32 * q4 + lane;
             const uint32_t cb = (c >> 6) * 8192;
             float run = 0.f;
 #pragma unroll 8
             for (int t = 0; t < kC; ++t) {
-                const uint32_t o = cb + sw128_off(t, c & 63);
-                run += fmaxf(__bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(sm + gs::GT + o)), kGateFloor);
+                run += fmaxf(__bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(sm + gs::GT + cb + sw128_off(t, c & 63))),
+                             kGateFloor);
                 *reinterpret_cast<float*>(sm + gs::GF + fidx(t, c)) = run;
-                const float bk = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(sm + gs::BT + o)) *
-                                 __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(sm + gs::KT + o));
-                *reinterpret_cast<__nv_bfloat16*>(sm + gs::KB + o) = __float2bfloat16_rn(bk * __expf(run));
             }
             GLs[c] = run;
+        }
+        __syncthreads();
+        {   // K_bar = b.k.e^G: thread = channel c, half of the tokens
+            const int c = tid & (kD - 1), t0 = 32 * (tid >> 7);
+            const uint32_t cb = (c >> 6) * 8192;
+#pragma unroll 4
+            for (int t = t0; t < t0 + 32; ++t) {
+                const uint32_t o = cb + sw128_off(t, c & 63);
+                const float bk = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(sm + gs::BT + o)) *
+                                 __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(sm + gs::KT + o));
+                const float Gt = *reinterpret_cast<const float*>(sm + gs::GF + fidx(t, c));
+                *reinterpret_cast<__nv_bfloat16*>(sm + gs::KB + o) = __float2bfloat16_rn(bk * __expf(Gt));
+            }
         }
         fence_proxy_async_smem();
         tc_fence_before();
@@ -554,23 +564,27 @@ __global__ void __launch_bounds__(gs::kThreads, 1)
         tc_fence_after();
         if (q4 < 2) {  // dU0 -> dv = w.dU0, dw = v.dU0: token row t, d_v half h
             const int t = 32 * q4 + lane;
-            float x[64];
-            tmem_ld_cols<4>(tl + 384 + 64 * h, x);
-            if (t < nvalid) {
-                const size_t o = vrow(t) + 64 * h;
+            const size_t o = vrow(t < nvalid ? t : 0) + 64 * h;
+#pragma unroll 1
+            for (int q = 0; q < 4; ++q) {
+                float x[16];
+                tmem_ld_cols<1>(tl + 384 + 64 * h + 16 * q, x);
+                if (t < nvalid) {
 #pragma unroll
-                for (int cc = 0; cc < 8; ++cc) {
-                    const uint32_t so = h * 8192 + t * 128 + ((cc ^ (t & 7)) << 4);
-                    float wv[8], vv[8], ov[8], ow[8];
-                    unpack8(*reinterpret_cast<const uint4*>(sm + gs::WV + so), wv);
-                    unpack8(*reinterpret_cast<const uint4*>(sm + gs::VR + so), vv);
+                    for (int c2 = 0; c2 < 2; ++c2) {
+                        const int cc = 2 * q + c2;
+                        const uint32_t so = h * 8192 + t * 128 + ((cc ^ (t & 7)) << 4);
+                        float wv[8], vv[8], ov[8], ow[8];
+                        unpack8(*reinterpret_cast<const uint4*>(sm + gs::WV + so), wv);
+                        unpack8(*reinterpret_cast<const uint4*>(sm + gs::VR + so), vv);
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        ov[e] = wv[e] * x[8 * cc + e];
-                        ow[e] = vv[e] * x[8 * cc + e];
+                        for (int e = 0; e < 8; ++e) {
+                            ov[e] = wv[e] * x[8 * c2 + e];
+                            ow[e] = vv[e] * x[8 * c2 + e];
+                        }
+                        reinterpret_cast<uint4*>(dv + o)[cc] = pack8(ov);
+                        reinterpret_cast<uint4*>(dw + o)[cc] = pack8(ow);
                     }
-                    reinterpret_cast<uint4*>(dv + o)[cc] = pack8(ov);
-                    reinterpret_cast<uint4*>(dw + o)[cc] = pack8(ow);
                 }
             }
         } else if (h == 0) {  // dT: token row t -> bf16 [t][s] (MN-major B)
@@ -616,7 +630,10 @@ __global__ void __launch_bounds__(gs::kThreads, 1)
         fence_proxy_async_smem();
         tc_fence_before();
         __syncthreads();
-        // ---- P6b: P T^T (K = 64)
+        // ---- P6b: P T^T (K = 64); while it runs, the per-channel anchors a = (G_0 + G_last) / 2, the span
+        //      check and, for pair terms on the tensor cores, their operands K_til = k.e^{a-G},
+        //      B_a = b.k.e^{G-a}, Q_a = q.e^{G-a} (X = E.([dA] K_til), Y = E.([dM] K_til),
+        //      Z + V = (dA^T B_a + dM^T Q_a) / E with E = e^{G-a})
         if (tid == 0) {
             tc_fence_after();
             constexpr uint32_t id6 = idesc_bf16(128, 64, false, false);
@@ -625,19 +642,6 @@ __global__ void __launch_bounds__(gs::kThreads, 1)
                 mma_bf16(tmem + 448, desc(gs::PM + s * 32, 16), desc(gs::TT + s * 32, 16), id6, s > 0);
             mma_commit(bar + 6);
         }
-        ok = cta_wait(bar + 6, 0, wait_ns, flag);
-    }
-    if (ok) {
-        tc_fence_after();
-        if (q4 < 2) {  // dA = -strict_tril(T^T dT T^T) -> bf16 row
-            const int t = 32 * q4 + lane;
-            float x[32];
-            tmem_ld_cols<2>(tl + 448 + 32 * h, x);
-#pragma unroll
-            for (int j = 0; j < 32; ++j) x[j] = 32 * h + j < t ? -x[j] : 0.f;
-            st_row_bf16x32(sm + gs::DAB, t, 4 * h, x);
-        }
-        // per-channel anchor a = (G_0 + G_last) / 2 and the span check
         float span = 0.f;
         if (tid < kD) {
             const float g0 = *reinterpret_cast<const float*>(sm + gs::GF + fidx(0, tid));
@@ -645,11 +649,7 @@ __global__ void __launch_bounds__(gs::kThreads, 1)
             span = g0 - GLs[tid];
         }
         exact = __syncthreads_or(span > kSpanPair) != 0;
-    }
-    if (ok && !exact) {
-        // ---- pair terms on the tensor cores: X = E.([dA] K_til), Y = E.([dM] K_til), Z + V = (dA^T B_a +
-        //      dM^T Q_a) / E with E = e^{G-a}, K_til = k.e^{a-G}, B_a = b.k.e^{G-a}, Q_a = q.e^{G-a}
-        {
+        if (!exact) {
             const int c = tid & (kD - 1), t0 = 32 * (tid >> 7);
             const float a = ANs[c];
             const uint32_t cb = (c >> 6) * 8192, cl = c & 63;
@@ -666,9 +666,23 @@ __global__ void __launch_bounds__(gs::kThreads, 1)
                 *reinterpret_cast<__nv_bfloat16*>(sm + gs::QA + o) = __float2bfloat16_rn(qq * e);
             }
         }
+        ok = cta_wait(bar + 6, 0, wait_ns, flag);
+    }
+    if (ok) {
+        tc_fence_after();
+        if (q4 < 2) {  // dA = -strict_tril(T^T dT T^T) -> bf16 row
+            const int t = 32 * q4 + lane;
+            float x[32];
+            tmem_ld_cols<2>(tl + 448 + 32 * h, x);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) x[j] = 32 * h + j < t ? -x[j] : 0.f;
+            st_row_bf16x32(sm + gs::DAB, t, 4 * h, x);
+        }
         fence_proxy_async_smem();
         tc_fence_before();
         __syncthreads();
+    }
+    if (ok && !exact) {
         if (tid == 0) {  // [dA ; dM] K_til: M = 128 (both halves used), K = tokens, N = d_k
             tc_fence_after();
             constexpr uint32_t id7 = idesc_bf16(128, 128, false, true);
@@ -682,11 +696,14 @@ __global__ void __launch_bounds__(gs::kThreads, 1)
             tc_fence_after();
             {   // lanes 0-63: X / e^{G-a}, lanes 64-127: Y / e^{G-a}; token row t, channels of half h
                 const int t = 32 * (q4 & 1) + lane;
-                float x[64];
-                tmem_ld_cols<4>(tl + 384 + 64 * h, x);
                 const uint32_t dst = q4 < 2 ? gs::XF : gs::YF;
+#pragma unroll 1
+                for (int q = 0; q < 4; ++q) {
+                    float x[16];
+                    tmem_ld_cols<1>(tl + 384 + 64 * h + 16 * q, x);
 #pragma unroll
-                for (int j = 0; j < 64; ++j) *reinterpret_cast<float*>(sm + dst + fidx(t, 64 * h + j)) = x[j];
+                    for (int j = 0; j < 16; ++j) *reinterpret_cast<float*>(sm + dst + fidx(t, 64 * h + 16 * q + j)) = x[j];
+                }
             }
             tc_fence_before();
             __syncthreads();
@@ -707,10 +724,13 @@ __global__ void __launch_bounds__(gs::kThreads, 1)
             tc_fence_after();
             if (q4 < 2) {  // (Z + V) e^{G-a}
                 const int t = 32 * q4 + lane;
-                float x[64];
-                tmem_ld_cols<4>(tl + 384 + 64 * h, x);
+#pragma unroll 1
+                for (int q = 0; q < 4; ++q) {
+                    float x[16];
+                    tmem_ld_cols<1>(tl + 384 + 64 * h + 16 * q, x);
 #pragma unroll
-                for (int j = 0; j < 64; ++j) *reinterpret_cast<float*>(sm + gs::ZF + fidx(t, 64 * h + j)) = x[j];
+                    for (int j = 0; j < 16; ++j) *reinterpret_cast<float*>(sm + gs::ZF + fidx(t, 64 * h + 16 * q + j)) = x[j];
+                }
             }
             __syncthreads();
         }
@@ -837,19 +857,51 @@ __global__ void __launch_bounds__(gs::kThreads, 1)
         //      db = d(b.k) k; dG_t = dQ_bar q e^G + dK_bar K_bar - dK^ K^ + (b.k) X + q Y - k (Z+V) (into X's
         //      place) and E_t = dK^ K^ (the G_last part, into G's place). From the tensor cores X, Y and
         //      Z + V arrive without their anchor factors e^{+-(G-a)}, which are applied here.
+        // The lanes 0-63 warps take channels 32h .. 32h+31 from tensor memory and copy those of channels
+        // 64+32h .. for the lanes 64-127 warps, which cannot read those lanes, into rooms free by now.
+        const uint32_t QS = gs::TT, KS = gs::WV, HS = gs::GT;  // fp32 [64 t][64], columns swizzled by t
+        auto sidx = [](int t, int cc) { return static_cast<uint32_t>((t * 64 + (cc ^ (t & 31))) * 4); };
         if (q4 < 2) {
             const int t = 32 * q4 + lane;
+#pragma unroll
+            for (int g2 = 0; g2 < 2; ++g2) {
+                const int cc0 = 32 * h + 16 * g2;  // channel 64 + cc0 ..
+                uint32_t rq[16], rk[16], rh[16];
+                tmem_ld16(tl + 64 + cc0, rq);
+                tmem_ld16(tl + 128 + 64 + cc0, rk);
+                tmem_ld16(tl + 256 + 64 + cc0, rh);
+                tmem_ld_wait();
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    *reinterpret_cast<uint32_t*>(sm + QS + sidx(t, cc0 + e)) = rq[e];
+                    *reinterpret_cast<uint32_t*>(sm + KS + sidx(t, cc0 + e)) = rk[e];
+                    *reinterpret_cast<uint32_t*>(sm + HS + sidx(t, cc0 + e)) = rh[e];
+                }
+            }
+        }
+        __syncthreads();
+        {
+            const bool low = q4 < 2;
+            const int t = 32 * (q4 & 1) + lane;
             const bool valid = t < nvalid;
             const size_t vo = valid ? vrow(t) : 0;
-            const uint32_t lb = static_cast<uint32_t>(32 * q4) << 16;
 #pragma unroll 1
-            for (int jj = 0; jj < 4; ++jj) {
-                const int c0 = 64 * h + 16 * jj;
+            for (int g2 = 0; g2 < 2; ++g2) {
+                const int c0 = (low ? 0 : 64) + 32 * h + 16 * g2;
                 uint32_t rq[16], rk[16], rh[16];
-                tmem_ld16(tmem + lb + c0, rq);
-                tmem_ld16(tmem + lb + 128 + c0, rk);
-                tmem_ld16(tmem + lb + 256 + c0, rh);
-                tmem_ld_wait();
+                if (low) {
+                    tmem_ld16(tl + c0, rq);
+                    tmem_ld16(tl + 128 + c0, rk);
+                    tmem_ld16(tl + 256 + c0, rh);
+                    tmem_ld_wait();
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        rq[e] = *reinterpret_cast<const uint32_t*>(sm + QS + sidx(t, c0 - 64 + e));
+                        rk[e] = *reinterpret_cast<const uint32_t*>(sm + KS + sidx(t, c0 - 64 + e));
+                        rh[e] = *reinterpret_cast<const uint32_t*>(sm + HS + sidx(t, c0 - 64 + e));
+                    }
+                }
                 float oq[16], ok_[16], ob[16], qv[16], kv[16], bv[16];
                 {   // the 16 channels of q, k, b in token row t: two 16-byte pieces of each tile
                     const uint32_t cb = (c0 >> 6) * 8192 + t * 128;
