@@ -37,16 +37,24 @@ FLUSH_BYTES = 256 << 20  # > 129 MB L2
 # workload: a single-pass ncu capture of factors_tc + factors_exact + state_tc on the same heads at a
 # quarter of the tokens (B 2, T 8192: 8192 units, inputs and workspace 1.2 GB >> L2), times 4 (the
 # traffic grows with the units; the ~0.1 GB that stays in L2 across a kernel boundary is not
-# counted). Reported only while the tensor-core kernel source is the one that was measured.
-TRAFFIC_RECORD = {"chunk_tc_sha256_16": "034edefe8e543907", "bytes": 4 * (1837628928)}
+# counted). Reported only while the tensor-core forward's source is the one that was measured.
+TRAFFIC_RECORD = {"chunk_tc_sha256_16": "25dc3c41f3eac661", "bytes": 4 * (1837148928)}
+
+
+def chunk_tc_source_sha() -> str:
+    """First 16 hex digits of the sha256 of the tensor-core forward's sources (kernels and shared helpers)."""
+    import hashlib
+
+    h = hashlib.sha256()
+    for name in ("chunk_tc.cu", "tc_common.cuh"):
+        with open(os.path.join(ROOT, "gated_deltanet_mixer_gdn2_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def recorded_traffic():
-    import hashlib
-
-    path = os.path.join(ROOT, "gated_deltanet_mixer_gdn2_gb300", "csrc", "chunk_tc.cu")
     try:
-        sha = hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
+        sha = chunk_tc_source_sha()
     except OSError:
         return None
     return TRAFFIC_RECORD["bytes"] if sha == TRAFFIC_RECORD["chunk_tc_sha256_16"] else None
@@ -406,7 +414,7 @@ def next_rows_rooflines(g, device, hbm, wl):
         res[name] = {"kernel": kernel, "ms": round(ms, 4), "algorithmic_bytes": int(nbytes),
                      "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s", "frac": round(gbs / hbm, 4),
                      "bound": "hbm"}
-    # backward (chunked WY form in fp32 on CUDA cores, 32-token chunks): bound by fp32 arithmetic
+    # backward (bf16: chunked WY form on the tensor cores, 64-token chunks)
     tk = [rnd(B, T, Hk, d), rnd(B, T, Hk, d)]
     tk[0] = (tk[0].float() / tk[0].float().norm(dim=-1, keepdim=True)).to(bf)
     tk[1] = (tk[1].float() / tk[1].float().norm(dim=-1, keepdim=True)).to(bf)
@@ -428,15 +436,17 @@ def next_rows_rooflines(g, device, hbm, wl):
     torch.cuda.synchronize(device)
     ms = e0.elapsed_time(e1) / 2
     flops = backward_flops(tok, Hv, d)
-    sms = torch.cuda.get_device_properties(device).multi_processor_count
-    peak_tf = sms * 128 * 2 * 2.07e9 / 1e12          # fp32 lanes x FMA x max SM clock
+    _, tc_peak, _, pk_kind = peaks()
     ach = flops / (ms * 1e-3) / 1e12
-    res["backward"] = {"kernel": "gdn2_backward (factors_simt_kernel + chains_kernel (both chains) + "
-                                 "grad_kernel + group_sum2_kernel)", "ms": round(ms, 3),
-                       "algorithmic_flops": int(flops), "achieved": round(ach, 2), "peak": round(peak_tf, 1),
-                       "unit": "TFLOP/s", "frac": round(ach / peak_tf, 4), "bound": "alu",
-                       "note": (f"factors and per-chunk gradients: one CTA per (chunk, head); the two chains over "
-                                f"chunks: two CTAs per (batch, value head), {min(2 * B * Hv, sms)} of {sms} SMs")}
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    res["backward"] = {"kernel": "gdn2_backward (factors_tc_kernel + state_tc_kernel keeping S_n and U_n + "
+                                 "rchain_tc_kernel + grad_tc_kernel + group_sum_tc_kernel)", "ms": round(ms, 3),
+                       "algorithmic_flops": int(flops), "achieved": round(ach, 2), "peak": round(tc_peak, 1),
+                       "peak_kind": pk_kind, "unit": "TFLOP/s", "frac": round(ach / tc_peak, 4), "bound": "latency",
+                       "note": (f"flops counted at the recurrent form's 26 d^2 per (token, head); every product runs "
+                                f"on tcgen05, but the per-chunk gradient kernel (one CTA per (chunk, head), all of "
+                                f"shared memory and tensor memory) is a chain of dependent products and read-outs, "
+                                f"and the two chains over chunks use {min(2 * B * Hv, sms)} of {sms} SMs")}
     res["shape"] = f"B={B} T={T} H_k={Hk} H_v={Hv} d={d} bf16 (the bench workload's token tensors)"
     return res
 

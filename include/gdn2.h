@@ -287,13 +287,19 @@ gdn2_status gdn2_mixer_decode_step(const void* xq, const void* xk, const void* x
  * recurrence of the burn-gdn2 0.1.5 docs ("Architecture"), given the upstream gradient d_o of o
  * and optionally d_final_state of S_T: the gradients of sum(o * d_o) + sum(S_T * d_final_state).
  * Reverse mode of the chunked WY form of the same recurrence (burn-gdn2 0.1.5 docs, "chunked WY
- * decomposition (training)"), in fp32 with chunks of 32 tokens, in five
- * launches: the state-independent factors of every chunk (with T = (I + A)^-1); a forward chain
- * that keeps each chunk's starting state S_n and its U; a backward chain that keeps dS_(n+1) and dU;
- * one CTA per (chunk, batch, value head) that forms every per-token gradient of its chunk from those;
- * and a pass that adds the value heads of each key head for dq and dk in a fixed order. The forward
- * outputs are not needed. Gates enter only as ratios exp(G_t - G_s) with t >= s, so no
- * intermediate overflows for any g <= 0.
+ * decomposition (training)"): the state-independent factors of every chunk (with T = (I + A)^-1);
+ * a forward chain that keeps each chunk's starting state S_n and its U; a reverse chain that keeps
+ * dS_(n+1) and dU; one CTA per (chunk, batch, value head) that forms every per-token gradient of
+ * its chunk from those; and a pass that adds the value heads of each key head for dq and dk in a
+ * fixed order. The forward outputs are not needed.
+ *   dt = GDN2_BF16: chunks of 64 tokens on the tensor cores (bf16 operands, fp32 accumulators and
+ *   state): the factors and the forward chain are the chunked forward's, and the pair terms through
+ *   A and M take one anchor per key channel, or CUDA cores with factors exp(G_t - G_s) <= 1 in chunks
+ *   whose log-decay spans more than the anchors take.
+ *   dt = GDN2_F32: chunks of 32 tokens in fp32 on CUDA cores; gates enter only as ratios
+ *   exp(G_t - G_s) with t >= s.
+ * Either way the whole decay domain g <= 0 (g = -inf included: gates are floored at -100) gives
+ * finite gradients.
  * q, k, dq, dk: [B, T, H_k, d_k]; v, w, d_o, dv, dw: [B, T, H_v, d_v]; g, b, dg, db: [B, T, H_v, d_k]
  * (all dtype dt); initial_state, d_final_state, d_initial_state: fp32 [B, H_v, d_k, d_v] or NULL
  * (zeros / not written). dq and dk of a key head sum its value heads. d_k = d_v = 128,
