@@ -8,6 +8,7 @@
 
 #include "common.cuh"
 #include "ptx.cuh"
+#include "tma_map.cuh"
 
 namespace gdn2 {
 namespace {
@@ -173,39 +174,6 @@ __device__ __forceinline__ void tma_store_4d(const void* map, const void* src, i
 
 // ---------------------------------------------------------------------------------------------
 // host: tensor maps
-
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = []() -> EncodeTiledFn {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult qr;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &qr) !=
-                cudaSuccess ||
-            qr != cudaDriverEntryPointSuccess)
-            return nullptr;
-        return reinterpret_cast<EncodeTiledFn>(p);
-    }();
-    return fn;
-}
-
-bool make_map(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base, const uint64_t* dims,
-              const uint64_t* strides_bytes, const uint32_t* box, CUtensorMapSwizzle sw) {
-    EncodeTiledFn f = encode_fn();
-    if (!f) return false;
-    cuuint64_t gd[5], gs[4];
-    cuuint32_t bx[5], es[5];
-    for (int i = 0; i < rank; ++i) {
-        gd[i] = dims[i];
-        bx[i] = box[i];
-        es[i] = 1;
-    }
-    for (int i = 0; i < rank - 1; ++i) gs[i] = strides_bytes[i];
-    return f(m, dt, rank, const_cast<void*>(base), gd, gs, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
 
 // token tensor [B, T, H, d] bf16 (d = 128 unless given) viewed as (d, H, T, B); box (64, 1, 64, 1)
 bool token_map(CUtensorMap* m, const void* p, int B, int T, int H, int d = kD) {
