@@ -277,6 +277,7 @@ def run_ours(args, rank, world, device):
 
     decode_line = decode_roofline(g, device, hbm) if rank == 0 and not args.no_decode_workload else None
     next_rows = next_rows_rooflines(g, device, hbm, wl) if rank == 0 and not args.no_decode_workload else None
+    head_shapes = head_shape_rooflines(g, device, hbm) if rank == 0 and not args.no_decode_workload else None
 
     # end to end through the public API with host buffers (inputs H2D, results D2H every step)
     e2e = None
@@ -313,6 +314,8 @@ def run_ours(args, rank, world, device):
         line["decode"] = decode_line
     if next_rows:
         line["next_rows"] = next_rows
+    if head_shapes:
+        line["head_shapes"] = head_shapes
     if e2e:
         line["e2e"] = e2e
     return line
@@ -362,6 +365,50 @@ def decode_roofline(g, device, hbm):
             "us_per_step": round(us, 2), "bytes_per_step": b, "achieved": round(gbs, 1), "peak": hbm,
             "unit": "GB/s", "frac": round(gbs / hbm, 4), "bound": "hbm",
             "l2": "state 201 MB > L2; 256 back-to-back steps"}
+
+
+def head_shape_rooflines(g, device, hbm):
+    """The chunked forward on the pages' other head shapes (head_dim 64; expand_v = 2 at head_dim 128),
+    bf16, 2 x 16384 tokens, 16 key / 32 value heads, each against the HBM roof of its algorithmic bytes
+    (chunk_bytes); inputs > L2, CUDA events over back-to-back calls."""
+    import torch
+
+    B, T, Hk, Hv = 2, 16384, 16, 32
+    bf = torch.bfloat16
+    gen = torch.Generator(device=device)
+    gen.manual_seed(77)
+    rnd = lambda *s: torch.randn(s, generator=gen, device=device)
+    stream = torch.cuda.current_stream(device)
+    res = []
+    for dk, dv in ((64, 64), (64, 128), (128, 256)):
+        q = torch.nn.functional.normalize(rnd(B, T, Hk, dk), dim=-1).to(bf)
+        k = torch.nn.functional.normalize(rnd(B, T, Hk, dk), dim=-1).to(bf)
+        v, w = rnd(B, T, Hv, dv).to(bf), torch.sigmoid(rnd(B, T, Hv, dv)).to(bf)
+        gg = (-torch.nn.functional.softplus(rnd(B, T, Hv, dk))).to(bf)
+        bb = torch.sigmoid(rnd(B, T, Hv, dk)).to(bf)
+        o = torch.empty_like(v)
+        sT = torch.empty((B, Hv, dk, dv), dtype=torch.float32, device=device)
+        ws = torch.empty(g.gdn2_chunk_fwd_workspace_size(B, T, Hk, Hv, dk, dv, 64), dtype=torch.uint8, device=device)
+        fn = lambda: g.gdn2_chunk_fwd(q, k, v, gg, bb, w, o, None, sT, C=64, workspace=ws)
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize(device)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = 5
+        e0.record(stream)
+        for _ in range(reps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize(device)
+        ms = e0.elapsed_time(e1) / reps
+        nbytes = chunk_bytes(synth.Workload("head-shape", B=B, T=T, Hk=Hk, Hv=Hv, dk=dk, dv=dv, dtype="bf16",
+                                            seed=0, s0_std=0.0))
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        res.append({"shape": f"d_k {dk}, d_v {dv}", "path": "tcgen05", "ms": round(ms, 4),
+                    "algorithmic_bytes": int(nbytes), "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
+                    "frac": round(gbs / hbm, 4)})
+        del q, k, v, w, gg, bb, o, sT, ws
+    return {"workload": f"B={B} T={T} H_k={Hk} H_v={Hv} bf16, chunk 64, from S0 = 0", "shapes": res}
 
 
 def next_rows_rooflines(g, device, hbm, wl):

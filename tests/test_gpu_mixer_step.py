@@ -39,8 +39,11 @@ def _f32dev(a):
     return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).cuda()
 
 
+# groups of 1 to 8 value heads per key head run as thread-block clusters (one CTA per value head);
+# larger groups (12) as one CTA per key head
 @pytest.mark.parametrize("dtype,dk,dv,Hk,Hv,neg", [("bf16", 128, 128, 2, 4, False), ("bf16", 64, 64, 1, 3, True),
-                                                   ("f32", 128, 64, 2, 2, False), ("f32", 64, 128, 1, 2, True)])
+                                                   ("f32", 128, 64, 2, 2, False), ("f32", 64, 128, 1, 2, True),
+                                                   ("f32", 64, 64, 1, 8, False), ("bf16", 64, 128, 1, 12, False)])
 def test_decode_step_against_chained_oracles(g, dtype, dk, dv, Hk, Hv, neg):
     import torch
 
