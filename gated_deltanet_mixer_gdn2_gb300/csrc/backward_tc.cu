@@ -358,7 +358,7 @@ constexpr uint32_t QA = B1 + 49152;          //   which is written once the prod
 constexpr uint32_t GL = BAR + 512;           // G_last fp32 [128]
 constexpr uint32_t AN = BAR + 1024;          // per-channel anchor a fp32 [128]
 constexpr uint32_t DGM = BAR + 1536;         // dgamma = rowsum(dS' . S) fp32 [128]
-constexpr int kThreads = 256;
+constexpr int kThreads = 512;  // 16 warps: four per tensor-memory lane quarter
 // TMEM columns (lane = row of the product):
 //   [0,128)   dO S^T (lanes 0-63: dQ_bar / scale) | dU S^T (lanes 64-127: -dW)
 //   [128,192) dO U^T (lanes 0-63: dM / scale)     then dK_bar = T^T dW over [128,256) (lanes 0-63)
@@ -381,7 +381,7 @@ __device__ __forceinline__ uint32_t fidx(int t, int c) {
 // pair terms on CUDA cores with factors e^{G_t - G_s} <= 1.
 constexpr float kSpanPair = 120.f;
 
-// One CTA per (chunk, batch . value head); 256 threads, one CTA per SM (the inputs fill shared memory).
+// One CTA per (chunk, batch . value head); 512 threads, one CTA per SM (the inputs fill shared memory).
 __global__ void __launch_bounds__(gs::kThreads, 1)
     grad_tc_kernel(const __grid_constant__ GradMaps maps, float* __restrict__ dq_ws,
                    float* __restrict__ dk_ws, __nv_bfloat16* __restrict__ dv, __nv_bfloat16* __restrict__ dg,
@@ -400,7 +400,7 @@ __global__ void __launch_bounds__(gs::kThreads, 1)
     const int bi = bh / Hv, hv = bh - bi * Hv, hk = hv / (Hv / Hk);
     const int u = bh * NC + n;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int q4 = warp & 3, h = warp >> 2;  // TMEM lane quarter, column half
+    const int q4 = warp & 3, h = warp >> 2;  // TMEM lane quarter, column quarter
     const int nvalid = min(kC, T - n * kC);
     auto vrow = [&](int t) { return ((static_cast<size_t>(bi) * T + n * kC + t) * Hv + hv) * kD; };
 
@@ -450,7 +450,7 @@ __global__ void __launch_bounds__(gs::kThreads, 1)
     // ---- U0 = w.v in place of v (both tiles carry the same swizzle)
     if (ok) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
+        for (int i = 0; i < 1024 / gs::kThreads; ++i) {
             const int p = tid + gs::kThreads * i, j = p >> 9, o = (p & 511) * 16;
             uint4* vv = reinterpret_cast<uint4*>(sm + gs::B1 + j * 32768 + 24576 + o);
             float a[8], bw[8];
@@ -479,8 +479,8 @@ __global__ void __launch_bounds__(gs::kThreads, 1)
             }
             mma_commit(bar + 3);
         }
-        if (tid >= 128) {  // dgamma_c = sum over d_v of dS'[c][v] S[c][v] (both tiles carry the same swizzle)
-            const int c = tid - 128;
+        if (tid >= gs::kThreads - kD) {  // dgamma_c = sum over d_v of dS'[c][v] S[c][v] (same swizzle in both)
+            const int c = tid - (gs::kThreads - kD);
             float acc = 0.f;
 #pragma unroll 1
             for (int j = 0; j < 2; ++j)
@@ -506,16 +506,14 @@ __global__ void __launch_bounds__(gs::kThreads, 1)
             for (int j = 0; j < 2; ++j)
                 tma_load_4d(sm + gs::VR + j * 8192, &maps.v, 64 * j, hv, n * kC, bi, bar + 2);
         }
-        if (q4 >= 2) {  // dW = -(dU S^T): token row t, d_k half h -> bf16 operand rows
+        if (q4 >= 2) {  // dW = -(dU S^T): token row t, d_k columns 32h .. -> bf16 operand rows
             const int t = 32 * (q4 - 2) + lane;
-            float x[64];
-            tmem_ld_cols<4>(tl + 64 * h, x);
+            float x[32];
+            tmem_ld_cols<2>(tl + 32 * h, x);
 #pragma unroll
-            for (int j = 0; j < 64; ++j) x[j] = -x[j];
-            uint8_t* tile = sm + (h ? gs::DW1 : gs::DW0);
-            st_row_bf16x32(tile, t, 0, x);
-            st_row_bf16x32(tile, t, 4, x + 32);
-        } else {  // G (floored gates, inclusive sum over the chunk): thread = channel c
+            for (int j = 0; j < 32; ++j) x[j] = -x[j];
+            st_row_bf16x32(sm + ((h >> 1) ? gs::DW1 : gs::DW0), t, 4 * (h & 1), x);
+        } else if (h < 2) {  // G (floored gates, inclusive sum over the chunk): thread = channel c
             const int c = 64 * h + 32 * q4 + lane;
             const uint32_t cb = (c >> 6) * 8192;
             float run = 0.f;
@@ -528,11 +526,11 @@ __global__ void __launch_bounds__(gs::kThreads, 1)
             GLs[c] = run;
         }
         __syncthreads();
-        {   // K_bar = b.k.e^G: thread = channel c, half of the tokens
-            const int c = tid & (kD - 1), t0 = 32 * (tid >> 7);
+        {   // K_bar = b.k.e^G: thread = channel c, a quarter of the tokens
+            const int c = tid & (kD - 1), t0 = 16 * (tid >> 7);
             const uint32_t cb = (c >> 6) * 8192;
 #pragma unroll 4
-            for (int t = t0; t < t0 + 32; ++t) {
+            for (int t = t0; t < t0 + 16; ++t) {
                 const uint32_t o = cb + sw128_off(t, c & 63);
                 const float bk = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(sm + gs::BT + o)) *
                                  __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(sm + gs::KT + o));
@@ -562,18 +560,18 @@ __global__ void __launch_bounds__(gs::kThreads, 1)
     }
     if (ok) {
         tc_fence_after();
-        if (q4 < 2) {  // dU0 -> dv = w.dU0, dw = v.dU0: token row t, d_v half h
+        if (q4 < 2) {  // dU0 -> dv = w.dU0, dw = v.dU0: token row t, d_v columns 32h ..
             const int t = 32 * q4 + lane;
-            const size_t o = vrow(t < nvalid ? t : 0) + 64 * h;
+            const size_t o = vrow(t < nvalid ? t : 0);
 #pragma unroll 1
-            for (int q = 0; q < 4; ++q) {
+            for (int q = 0; q < 2; ++q) {
                 float x[16];
-                tmem_ld_cols<1>(tl + 384 + 64 * h + 16 * q, x);
+                tmem_ld_cols<1>(tl + 384 + 32 * h + 16 * q, x);
                 if (t < nvalid) {
 #pragma unroll
                     for (int c2 = 0; c2 < 2; ++c2) {
-                        const int cc = 2 * q + c2;
-                        const uint32_t so = h * 8192 + t * 128 + ((cc ^ (t & 7)) << 4);
+                        const int cc = 4 * h + 2 * q + c2;  // 16-byte piece of the row: 8 columns
+                        const uint32_t so = (cc >> 3) * 8192 + t * 128 + (((cc & 7) ^ (t & 7)) << 4);
                         float wv[8], vv[8], ov[8], ow[8];
                         unpack8(*reinterpret_cast<const uint4*>(sm + gs::WV + so), wv);
                         unpack8(*reinterpret_cast<const uint4*>(sm + gs::VR + so), vv);
@@ -587,15 +585,14 @@ __global__ void __launch_bounds__(gs::kThreads, 1)
                     }
                 }
             }
-        } else if (h == 0) {  // dT: token row t -> bf16 [t][s] (MN-major B)
+        } else if (h < 2) {  // dT: token row t, columns 32h .. -> bf16 [t][s] (MN-major B)
             const int t = 32 * (q4 - 2) + lane;
-            float x[64];
-            tmem_ld_cols<4>(tl + 192, x);
-            st_row_bf16x32(sm + gs::DT, t, 0, x);
-            st_row_bf16x32(sm + gs::DT, t, 4, x + 32);
+            float x[32];
+            tmem_ld_cols<2>(tl + 192 + 32 * h, x);
+            st_row_bf16x32(sm + gs::DT, t, 4 * h, x);
         }
         __syncthreads();  // w is read: its room takes dA and dM
-        if (q4 < 2) {  // dM = scale tril(dO U^T): token row t, columns 32h .. -> bf16 row
+        if (q4 < 2 && h < 2) {  // dM = scale tril(dO U^T): token row t, columns 32h .. -> bf16 row
             const int t = 32 * q4 + lane;
             float x[32];
             tmem_ld_cols<2>(tl + 128 + 32 * h, x);
@@ -621,7 +618,7 @@ __global__ void __launch_bounds__(gs::kThreads, 1)
     }
     if (ok) {
         tc_fence_after();
-        if (q4 < 2) {  // P -> bf16 K-major rows
+        if (q4 < 2 && h < 2) {  // P -> bf16 K-major rows
             const int t = 32 * q4 + lane;
             float x[32];
             tmem_ld_cols<2>(tl + 384 + 32 * h, x);
@@ -650,11 +647,11 @@ __global__ void __launch_bounds__(gs::kThreads, 1)
         }
         exact = __syncthreads_or(span > kSpanPair) != 0;
         if (!exact) {
-            const int c = tid & (kD - 1), t0 = 32 * (tid >> 7);
+            const int c = tid & (kD - 1), t0 = 16 * (tid >> 7);
             const float a = ANs[c];
             const uint32_t cb = (c >> 6) * 8192, cl = c & 63;
 #pragma unroll 4
-            for (int t = t0; t < t0 + 32; ++t) {
+            for (int t = t0; t < t0 + 16; ++t) {
                 const uint32_t o = cb + sw128_off(t, cl);
                 const float Gt = *reinterpret_cast<const float*>(sm + gs::GF + fidx(t, c));
                 const float e = __expf(Gt - a), ei = __expf(a - Gt);
@@ -670,7 +667,7 @@ __global__ void __launch_bounds__(gs::kThreads, 1)
     }
     if (ok) {
         tc_fence_after();
-        if (q4 < 2) {  // dA = -strict_tril(T^T dT T^T) -> bf16 row
+        if (q4 < 2 && h < 2) {  // dA = -strict_tril(T^T dT T^T) -> bf16 row
             const int t = 32 * q4 + lane;
             float x[32];
             tmem_ld_cols<2>(tl + 448 + 32 * h, x);
@@ -694,15 +691,15 @@ __global__ void __launch_bounds__(gs::kThreads, 1)
         ok = cta_wait(bar + 7, 0, wait_ns, flag);
         if (ok) {
             tc_fence_after();
-            {   // lanes 0-63: X / e^{G-a}, lanes 64-127: Y / e^{G-a}; token row t, channels of half h
+            {   // lanes 0-63: X / e^{G-a}, lanes 64-127: Y / e^{G-a}; token row t, channels 32h ..
                 const int t = 32 * (q4 & 1) + lane;
                 const uint32_t dst = q4 < 2 ? gs::XF : gs::YF;
 #pragma unroll 1
-                for (int q = 0; q < 4; ++q) {
+                for (int q = 0; q < 2; ++q) {
                     float x[16];
-                    tmem_ld_cols<1>(tl + 384 + 64 * h + 16 * q, x);
+                    tmem_ld_cols<1>(tl + 384 + 32 * h + 16 * q, x);
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) *reinterpret_cast<float*>(sm + dst + fidx(t, 64 * h + 16 * q + j)) = x[j];
+                    for (int j = 0; j < 16; ++j) *reinterpret_cast<float*>(sm + dst + fidx(t, 32 * h + 16 * q + j)) = x[j];
                 }
             }
             tc_fence_before();
@@ -725,11 +722,11 @@ __global__ void __launch_bounds__(gs::kThreads, 1)
             if (q4 < 2) {  // (Z + V) e^{G-a}
                 const int t = 32 * q4 + lane;
 #pragma unroll 1
-                for (int q = 0; q < 4; ++q) {
+                for (int q = 0; q < 2; ++q) {
                     float x[16];
-                    tmem_ld_cols<1>(tl + 384 + 64 * h + 16 * q, x);
+                    tmem_ld_cols<1>(tl + 384 + 32 * h + 16 * q, x);
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) *reinterpret_cast<float*>(sm + gs::ZF + fidx(t, 64 * h + 16 * q + j)) = x[j];
+                    for (int j = 0; j < 16; ++j) *reinterpret_cast<float*>(sm + gs::ZF + fidx(t, 32 * h + 16 * q + j)) = x[j];
                 }
             }
             __syncthreads();
@@ -740,7 +737,7 @@ __global__ void __launch_bounds__(gs::kThreads, 1)
         //      Y_t = sum_{s<=t} dM_ts k_s e^{G_t-G_s}; side 1: (Z+V)_s = sum_{u>s} dA_us (b.k)_u e^{G_u-G_s}
         //      + sum_{u>=s} dM_us q_u e^{G_u-G_s}. Tokens in blocks of 8; a pair in different blocks
         //      takes its factor as e^{G_t - G_r} e^{G_r - G_s} with r at the block edge.
-        {
+        if (tid < 2 * kD) {
             const int c = tid & (kD - 1), side = tid >> 7;
             auto DA = [&](int t, int s2) {
                 return __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(sm + gs::DAB + sw128_off(t, s2)));
@@ -857,15 +854,14 @@ __global__ void __launch_bounds__(gs::kThreads, 1)
         //      db = d(b.k) k; dG_t = dQ_bar q e^G + dK_bar K_bar - dK^ K^ + (b.k) X + q Y - k (Z+V) (into X's
         //      place) and E_t = dK^ K^ (the G_last part, into G's place). From the tensor cores X, Y and
         //      Z + V arrive without their anchor factors e^{+-(G-a)}, which are applied here.
-        // The lanes 0-63 warps take channels 32h .. 32h+31 from tensor memory and copy those of channels
-        // 64+32h .. for the lanes 64-127 warps, which cannot read those lanes, into rooms free by now.
+        // The lanes 0-63 warps take channels 16h .. 16h+15 from tensor memory and copy those of channels
+        // 64+16h .. for the lanes 64-127 warps, which cannot read those lanes, into rooms free by now.
         const uint32_t QS = gs::TT, KS = gs::WV, HS = gs::GT;  // fp32 [64 t][64], columns swizzled by t
         auto sidx = [](int t, int cc) { return static_cast<uint32_t>((t * 64 + (cc ^ (t & 31))) * 4); };
         if (q4 < 2) {
             const int t = 32 * q4 + lane;
-#pragma unroll
-            for (int g2 = 0; g2 < 2; ++g2) {
-                const int cc0 = 32 * h + 16 * g2;  // channel 64 + cc0 ..
+            {
+                const int cc0 = 16 * h;  // channel 64 + cc0 ..
                 uint32_t rq[16], rk[16], rh[16];
                 tmem_ld16(tl + 64 + cc0, rq);
                 tmem_ld16(tl + 128 + 64 + cc0, rk);
@@ -885,9 +881,8 @@ __global__ void __launch_bounds__(gs::kThreads, 1)
             const int t = 32 * (q4 & 1) + lane;
             const bool valid = t < nvalid;
             const size_t vo = valid ? vrow(t) : 0;
-#pragma unroll 1
-            for (int g2 = 0; g2 < 2; ++g2) {
-                const int c0 = (low ? 0 : 64) + 32 * h + 16 * g2;
+            {
+                const int c0 = (low ? 0 : 64) + 16 * h;
                 uint32_t rq[16], rk[16], rh[16];
                 if (low) {
                     tmem_ld16(tl + c0, rq);
@@ -963,13 +958,13 @@ __global__ void __launch_bounds__(gs::kThreads, 1)
         }
         __syncthreads();
         // ---- dg_t = sum_{s >= t} dG_s + sum_s E_s + dgamma gamma (the gradient of G_last): thread = channel c
-        //      and half of the tokens; the halves exchange their sums through the room g has left
+        //      and a quarter of the tokens; the quarters exchange their sums through the room g has left
         {
-            const int c = tid & (kD - 1), hf = tid >> 7, t0 = 32 * hf;
-            float* xs = reinterpret_cast<float*>(sm + gs::GT);  // [2 halves][2 sums][128]
+            const int c = tid & (kD - 1), hf = tid >> 7, t0 = 16 * hf;
+            float* xs = reinterpret_cast<float*>(sm + gs::GT);  // [4 quarters][2 sums][128]
             float et = 0.f, sd = 0.f;
 #pragma unroll 8
-            for (int t = t0; t < t0 + 32; ++t) {
+            for (int t = t0; t < t0 + 16; ++t) {
                 et += *reinterpret_cast<const float*>(sm + gs::GF + fidx(t, c));
                 sd += *reinterpret_cast<const float*>(sm + gs::XF + fidx(t, c));
             }
@@ -977,10 +972,12 @@ __global__ void __launch_bounds__(gs::kThreads, 1)
             xs[(2 * hf + 1) * kD + c] = sd;
             __syncthreads();
             const float dgm = reinterpret_cast<const float*>(sm + gs::DGM)[c];
-            const float off = fmaf(dgm, __expf(GLs[c]), xs[c] + xs[2 * kD + c]);
-            float run = hf ? 0.f : xs[3 * kD + c];  // the lower half starts from the upper half's total
+            const float off =
+                fmaf(dgm, __expf(GLs[c]), (xs[c] + xs[2 * kD + c]) + (xs[4 * kD + c] + xs[6 * kD + c]));
+            float run = 0.f;  // a quarter starts from the totals of the later ones
+            for (int q = 3; q > hf; --q) run += xs[(2 * q + 1) * kD + c];
 #pragma unroll 8
-            for (int t = t0 + 31; t >= t0; --t) {
+            for (int t = t0 + 15; t >= t0; --t) {
                 run += *reinterpret_cast<const float*>(sm + gs::XF + fidx(t, c));
                 if (t < nvalid) dg[vrow(t) + c] = __float2bfloat16_rn(run + off);
             }
