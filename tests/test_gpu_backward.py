@@ -147,6 +147,31 @@ def test_backward_bf16_decay_domain(g, decay, T, Hk, Hv):
         assert e < TOL["bf16"], (name, e)
 
 
+@pytest.mark.parametrize("T,Hk,Hv", [(1, 1, 1), (64, 2, 2), (65, 1, 3), (200, 3, 3)])
+def test_backward_bf16_edge_lengths(g, T, Hk, Hv):
+    """The bf16 path at a single token, exactly one chunk, one chunk and one token, and ungrouped heads
+    (H_k = H_v, the key-head sum over one value head), against the oracle."""
+    import torch
+
+    wl = synth.Workload("bwd-edge", B=2, T=T, Hk=Hk, Hv=Hv, dk=128, dv=128, dtype="bf16", seed=60 + T + Hv,
+                        s0_std=0.02)
+    inp = synth.make_inputs(wl)
+    rng = np.random.default_rng(T)
+    d_o = synth.round_to(rng.standard_normal((2, T, Hv, 128)), "bf16").astype(np.float64)
+    ds_t = (0.1 * rng.standard_normal((2, Hv, 128, 128))).astype(np.float32).astype(np.float64)
+    dev = lambda a: synth.to_torch(np.ascontiguousarray(a), "bf16", "cuda")
+    ts = [dev(getattr(inp, n)) for n in ("q", "k", "v", "g", "b", "w")]
+    outs = g.backward(*ts, dev(d_o), H.state_to_device(inp.s0), H.state_to_device(ds_t), scale=0.5)
+    torch.cuda.synchronize()
+    assert g.gdn2_last_device_status() == g.GDN2_OK
+    ref = oback.gradients(inp.q, inp.k, inp.v, inp.g, inp.b, inp.w, inp.s0, d_o, ds_t, scale=0.5)
+    for name, got in zip(("dq", "dk", "dv", "dg", "db", "dw", "ds0"), outs):
+        x = H.to_np(got)
+        assert np.isfinite(x).all(), name
+        e = max_rel_err(x, ref[name])
+        assert e < TOL["bf16"], (name, e)
+
+
 def test_backward_chunked_matches_recurrent_at_the_bench_shape(g):
     """The bench workload's shapes (B 2, T 32768, H_k 16, H_v 32, bf16 tensors): the chunked path against
     the per-token recurrent path, two fp32 computations that share no arithmetic; errors are normwise
