@@ -358,6 +358,11 @@ bool bwd_shape_ok(int B, int T, int Hk, int Hv, int dk, int dv) {
     return B >= 0 && T >= 0 && Hk > 0 && Hv > 0 && Hv % Hk == 0 && dk == kD && dv == kD &&
            static_cast<long long>(B) * T * Hv < (1LL << 31) / kD && static_cast<long long>(B) * Hv <= 65535;
 }
+// The chunked form's shapes: bf16 (tensor cores) takes d_k and d_v of 64 or 128, fp32 128 only.
+bool chunked_shape_ok(int B, int T, int Hk, int Hv, int dk, int dv, gdn2_dtype dt) {
+    if (dt != GDN2_BF16) return bwd_shape_ok(B, T, Hk, Hv, dk, dv);
+    return bwd_shape_ok(B, T, Hk, Hv, kD, kD) && (dk == 64 || dk == kD) && (dv == 64 || dv == kD);
+}
 
 }  // namespace
 }  // namespace gdn2
@@ -372,11 +377,12 @@ gdn2_status check_and_trivial(const void* q, const void* k, const void* v, const
                               const float* initial_state, const void* d_o, const float* d_final_state, void* dq,
                               void* dk, void* dv, void* dg, void* db, void* dw, float* d_initial_state, int B, int T,
                               int Hk, int Hv, int d_k, int d_v, gdn2_dtype dt, void* workspace, size_t ws_bytes,
-                              size_t need, cudaStream_t s, bool* done) {
+                              size_t need, cudaStream_t s, bool* done, bool chunked) {
     *done = true;
     if (dt != GDN2_F32 && dt != GDN2_BF16) return GDN2_ERR_INVALID_ARG;
     if (B < 0 || T < 0 || Hk <= 0 || Hv <= 0 || d_k <= 0 || d_v <= 0 || Hv % Hk) return GDN2_ERR_INVALID_ARG;
-    if (!bwd_shape_ok(B, T, Hk, Hv, d_k, d_v)) return GDN2_ERR_UNSUPPORTED;
+    if (!(chunked ? chunked_shape_ok(B, T, Hk, Hv, d_k, d_v, dt) : bwd_shape_ok(B, T, Hk, Hv, d_k, d_v)))
+        return GDN2_ERR_UNSUPPORTED;
     const size_t state_bytes = sizeof(float) * static_cast<size_t>(B) * Hv * d_k * d_v;
     if (B == 0 || T == 0) {  // no tokens: dS0 = dS_T
         if (d_initial_state && state_bytes) {
@@ -407,8 +413,9 @@ gdn2_status check_and_trivial(const void* q, const void* k, const void* v, const
 extern "C" {
 
 size_t gdn2_backward_workspace_size(int B, int T, int Hk, int Hv, int dk, int dv, gdn2_dtype dt) {
-    if ((dt != GDN2_F32 && dt != GDN2_BF16) || !bwd_shape_ok(B, T, Hk, Hv, dk, dv) || B == 0 || T == 0) return 0;
-    return dt == GDN2_BF16 ? backward_tc_workspace_bytes(B, T, Hv) : backward_chunked_workspace_bytes(B, T, Hv);
+    if ((dt != GDN2_F32 && dt != GDN2_BF16) || !chunked_shape_ok(B, T, Hk, Hv, dk, dv, dt) || B == 0 || T == 0)
+        return 0;
+    return dt == GDN2_BF16 ? backward_tc_workspace_bytes(B, T, Hv, dk, dv) : backward_chunked_workspace_bytes(B, T, Hv);
 }
 
 gdn2_status gdn2_backward(const void* q, const void* k, const void* v, const void* g, const void* b, const void* w,
@@ -421,11 +428,12 @@ gdn2_status gdn2_backward(const void* q, const void* k, const void* v, const voi
     const size_t need = gdn2_backward_workspace_size(B, T, Hk, Hv, d_k, d_v, dt);
     const gdn2_status st = check_and_trivial(q, k, v, g, b, w, initial_state, d_o, d_final_state, dq, dk, dv, dg, db,
                                              dw, d_initial_state, B, T, Hk, Hv, d_k, d_v, dt, workspace, ws_bytes, need,
-                                             s, &done);
+                                             s, &done, true);
     if (done) return st;
     if (dt == GDN2_BF16)  // tensor cores: chunks of 64, bf16 operands, fp32 accumulators and state
         return launch_backward_tc(q, k, v, g, b, w, initial_state, d_o, d_final_state, dq, dk, dv, dg, db, dw,
-                                  d_initial_state, B, T, Hk, Hv, scale, workspace, s, wait_limit_ns()) == cudaSuccess
+                                  d_initial_state, B, T, Hk, Hv, d_k, d_v, scale, workspace, s,
+                                  wait_limit_ns()) == cudaSuccess
                    ? GDN2_OK
                    : GDN2_ERR_CUDA;
     return launch_backward_chunked(q, k, v, g, b, w, initial_state, d_o, d_final_state, dq, dk, dv, dg, db, dw,
@@ -449,7 +457,7 @@ gdn2_status gdn2_backward_recurrent(const void* q, const void* k, const void* v,
     const size_t need = bwd_shape_ok(B, T, Hk, Hv, d_k, d_v) && B > 0 && T > 0 ? bwd_layout(B, T, Hv).total : 0;
     const gdn2_status st = check_and_trivial(q, k, v, g, b, w, initial_state, d_o, d_final_state, dq, dk, dv, dg, db,
                                              dw, d_initial_state, B, T, Hk, Hv, d_k, d_v, dt, workspace, ws_bytes, need,
-                                             s, &done);
+                                             s, &done, false);
     if (done) return st;
     const BwdLayout L = bwd_layout(B, T, Hv);
     uint8_t* ws = static_cast<uint8_t*>(workspace);

@@ -1,5 +1,5 @@
 // backward_tc.cu -- gradients of the GDN-2 core in chunked form on the 5th-generation tensor cores
-// (tcgen05 + TMA + TMEM): bf16 inputs, d_k = d_v = 128, chunks of C = 64 (the recurrence of the
+// (tcgen05 + TMA + TMEM): bf16 inputs, d_k and d_v 64 or 128, chunks of C = 64 (the recurrence of the
 // burn-gdn2 0.1.5 docs, "Architecture", in the chunked WY form of its "chunked WY decomposition
 // (training)" section).
 //
@@ -21,7 +21,9 @@
 // chain in reverse on the tensor cores (fp32 dS in registers), keeping bf16 dS_{n+1} and dU_n;
 // grad_tc_kernel, one CTA per (chunk, head): every product on the tensor cores (the pair terms with
 // one anchor per channel, or on CUDA cores in chunks whose log-decay spans too much for it) and the
-// chain rule on CUDA cores; the sums of dq and dk over the value heads of each key head.
+// chain rule on CUDA cores; the sums of dq and dk over the value heads of each key head. A head size of
+// 64 runs as 128 whose upper 64 channels (or columns) are zeros: the tensor maps declare the true size,
+// so the upper boxes read as zeros, and only the true channels are written.
 #include "common.cuh"
 #include "ptx.cuh"
 #include "tc_common.cuh"
@@ -73,7 +75,8 @@ constexpr uint32_t kDu = 0, kDs = 128, kCols = 256;
 __global__ void __launch_bounds__(rs::kThreads, 1)
     rchain_tc_kernel(const __grid_constant__ RevMaps maps, const uint8_t* __restrict__ ws,
                      const float* __restrict__ dsT, float* __restrict__ ds0, __nv_bfloat16* __restrict__ ds_save,
-                     __nv_bfloat16* __restrict__ du_save, int Hv, int NC, float scale, long long wait_ns) {
+                     __nv_bfloat16* __restrict__ du_save, int Hv, int NC, int dk, int dv, float scale,
+                     long long wait_ns) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(sm);
@@ -92,7 +95,8 @@ __global__ void __launch_bounds__(rs::kThreads, 1)
     volatile int* err = reinterpret_cast<volatile int*>(sm + rs::BAR + 164);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int bh = blockIdx.x >> 1, hc = blockIdx.x & 1;
+    const int nslice = dv >> 6;  // 64-column slices of d_v
+    const int bh = blockIdx.x / nslice, hc = blockIdx.x - bh * nslice;
     const int bi = bh / Hv, hv = bh - bi * Hv;
 
     if (tid == 0) {
@@ -260,11 +264,15 @@ __global__ void __launch_bounds__(rs::kThreads, 1)
         };
         uint8_t* dsb = sm + rs::DSB;
         uint8_t* dub = sm + rs::DUB;
-        const size_t srow = (static_cast<size_t>(bh) * kD + r) * kD + 64 * hc;
+        // with d_k = 64 the rows 64..127 are zero padding: they start at 0 and stay there (their keys are
+        // zero and their decay is 1), and are neither read from dS_T nor written to dS_0
+        const bool real_row = r < dk;
+        const size_t srow = (static_cast<size_t>(bh) * dk + (real_row ? r : 0)) * dv + 64 * hc;
         float sx[64];  // dS' = dS_{n+1}
 #pragma unroll
         for (int j4 = 0; j4 < 16; ++j4) {
-            const float4 f = dsT ? reinterpret_cast<const float4*>(dsT + srow)[j4] : make_float4(0.f, 0.f, 0.f, 0.f);
+            const float4 f = (dsT && real_row) ? reinterpret_cast<const float4*>(dsT + srow)[j4]
+                                               : make_float4(0.f, 0.f, 0.f, 0.f);
             sx[4 * j4] = f.x;
             sx[4 * j4 + 1] = f.y;
             sx[4 * j4 + 2] = f.z;
@@ -278,7 +286,7 @@ __global__ void __launch_bounds__(rs::kThreads, 1)
             st_row_bf16x32(dsb, r, 4, sx + 32);
             fence_proxy_async_smem();
             arrive(ds_ready);
-            st_global_bf16x64(ds_save + (u * kD + r) * kD + 64 * hc, sx);
+            st_global_bf16x64(ds_save + (u * kD + r) * dv + 64 * hc, sx);
             if (!(ok = warp_wait(gam_full + (m & 3), (m >> 2) & 1, wait_ns, err))) break;
             {
                 const float gg = reinterpret_cast<const float*>(sm + rs::GAMC)[(m & 3) * 128 + r];
@@ -295,7 +303,7 @@ __global__ void __launch_bounds__(rs::kThreads, 1)
                 fence_proxy_async_smem();
                 tc_fence_before();
                 arrive(du_ready);
-                st_global_bf16x64(du_save + (u * kC + r) * kD + 64 * hc, x);
+                st_global_bf16x64(du_save + (u * kC + r) * dv + 64 * hc, x);
             }
             if (!(ok = warp_wait(ds_done, m & 1, wait_ns, err))) break;
             tc_fence_after();
@@ -307,7 +315,7 @@ __global__ void __launch_bounds__(rs::kThreads, 1)
             }
             tc_fence_before();
         }
-        if (ok && ds0) {
+        if (ok && ds0 && real_row) {
             float4* dst = reinterpret_cast<float4*>(ds0 + srow);
 #pragma unroll
             for (int j4 = 0; j4 < 16; ++j4)
@@ -386,7 +394,7 @@ __global__ void __launch_bounds__(gs::kThreads, 1)
     grad_tc_kernel(const __grid_constant__ GradMaps maps, float* __restrict__ dq_ws,
                    float* __restrict__ dk_ws, __nv_bfloat16* __restrict__ dv, __nv_bfloat16* __restrict__ dg,
                    __nv_bfloat16* __restrict__ db, __nv_bfloat16* __restrict__ dw, int T, int Hk, int Hv,
-                   float scale, long long wait_ns) {
+                   int d_k, int d_v, float scale, long long wait_ns) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(sm);
@@ -402,7 +410,9 @@ __global__ void __launch_bounds__(gs::kThreads, 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int q4 = warp & 3, h = warp >> 2;  // TMEM lane quarter, column quarter
     const int nvalid = min(kC, T - n * kC);
-    auto vrow = [&](int t) { return ((static_cast<size_t>(bi) * T + n * kC + t) * Hv + hv) * kD; };
+    // token rows of the d_k-indexed outputs (dq, dk per value head, dg, db) and of the d_v-indexed ones
+    auto krow = [&](int t) { return ((static_cast<size_t>(bi) * T + n * kC + t) * Hv + hv) * d_k; };
+    auto vrow = [&](int t) { return ((static_cast<size_t>(bi) * T + n * kC + t) * Hv + hv) * d_v; };
 
     if (tid == 0) {
         for (int i = 0; i < 9; ++i) mbar_init(bar + i, 1);
@@ -567,7 +577,7 @@ __global__ void __launch_bounds__(gs::kThreads, 1)
             for (int q = 0; q < 2; ++q) {
                 float x[16];
                 tmem_ld_cols<1>(tl + 384 + 32 * h + 16 * q, x);
-                if (t < nvalid) {
+                if (t < nvalid && 32 * h < d_v) {
 #pragma unroll
                     for (int c2 = 0; c2 < 2; ++c2) {
                         const int cc = 4 * h + 2 * q + c2;  // 16-byte piece of the row: 8 columns
@@ -879,8 +889,8 @@ __global__ void __launch_bounds__(gs::kThreads, 1)
         {
             const bool low = q4 < 2;
             const int t = 32 * (q4 & 1) + lane;
-            const bool valid = t < nvalid;
-            const size_t vo = valid ? vrow(t) : 0;
+            const bool valid = t < nvalid && (low ? 0 : 64) + 16 * h < d_k;  // a true token and true channels
+            const size_t vo = valid ? krow(t) : 0;
             {
                 const int c0 = (low ? 0 : 64) + 16 * h;
                 uint32_t rq[16], rk[16], rh[16];
@@ -979,7 +989,7 @@ __global__ void __launch_bounds__(gs::kThreads, 1)
 #pragma unroll 8
             for (int t = t0 + 15; t >= t0; --t) {
                 run += *reinterpret_cast<const float*>(sm + gs::XF + fidx(t, c));
-                if (t < nvalid) dg[vrow(t) + c] = __float2bfloat16_rn(run + off);
+                if (t < nvalid && c < d_k) dg[krow(t) + c] = __float2bfloat16_rn(run + off);
             }
         }
     }
@@ -997,18 +1007,18 @@ __global__ void __launch_bounds__(gs::kThreads, 1)
 __global__ void __launch_bounds__(256) group_sum_tc_kernel(const float* __restrict__ dq_ws,
                                                            const float* __restrict__ dk_ws,
                                                            __nv_bfloat16* __restrict__ dq, __nv_bfloat16* __restrict__ dk,
-                                                           long long rows, int Hk, int Hv) {
+                                                           long long rows, int Hk, int Hv, int d) {
     const int group = Hv / Hk;
-    const long long n4 = rows * Hk * (kD / 4);
+    const long long n4 = rows * Hk * (d / 4);
     for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n4;
          i += static_cast<long long>(gridDim.x) * blockDim.x) {
-        const int c4 = static_cast<int>(i % (kD / 4));
-        const long long rh = i / (kD / 4);
+        const int c4 = static_cast<int>(i % (d / 4));
+        const long long rh = i / (d / 4);
         const int hk = static_cast<int>(rh % Hk);
         const long long r = rh / Hk;
         float4 sq = make_float4(0.f, 0.f, 0.f, 0.f), sk = sq;
         for (int m = 0; m < group; ++m) {
-            const size_t src = ((static_cast<size_t>(r) * Hv) + hk * group + m) * kD + 4 * c4;
+            const size_t src = ((static_cast<size_t>(r) * Hv) + hk * group + m) * d + 4 * c4;
             const float4 a = *reinterpret_cast<const float4*>(dq_ws + src), b = *reinterpret_cast<const float4*>(dk_ws + src);
             sq.x += a.x; sq.y += a.y; sq.z += a.z; sq.w += a.w;
             sk.x += b.x; sk.y += b.y; sk.z += b.z; sk.w += b.w;
@@ -1022,41 +1032,44 @@ __global__ void __launch_bounds__(256) group_sum_tc_kernel(const float* __restri
 struct TcBwdLayout {
     size_t fw, s, u, ds, du, dq, dk, total;
 };
-TcBwdLayout tc_bwd_layout(int B, int T, int Hv) {
-    const ChunkShape sh{B, T, 1, Hv, kD, kD, kC};
-    const size_t units = static_cast<size_t>(sh.nchunks()) * B * Hv, tok = static_cast<size_t>(B) * T * Hv * kD * 4;
+// Saves per (chunk, value head): S_n [d_k][d_v], U_n [64][d_v], dS_(n+1) [128][d_v] (rows past d_k are
+// zeros), dU_n [64][d_v], bf16; then fp32 dq and dk per value head.
+TcBwdLayout tc_bwd_layout(int B, int T, int Hv, int dk, int dv) {
+    const ChunkShape sh{B, T, 1, Hv, dk, dv, kC};
+    const size_t units = static_cast<size_t>(sh.nchunks()) * B * Hv, tok = static_cast<size_t>(B) * T * Hv * dk * 4;
     TcBwdLayout L;
     L.fw = 0;
     L.s = align_up(chunk_tc_workspace_bytes(sh), 1024);
-    L.u = align_up(L.s + units * kD * kD * 2, 1024);
-    L.ds = align_up(L.u + units * kC * kD * 2, 1024);
-    L.du = align_up(L.ds + units * kD * kD * 2, 1024);
-    L.dq = align_up(L.du + units * kC * kD * 2, 1024);
+    L.u = align_up(L.s + units * dk * dv * 2, 1024);
+    L.ds = align_up(L.u + units * kC * dv * 2, 1024);
+    L.du = align_up(L.ds + units * kD * dv * 2, 1024);
+    L.dq = align_up(L.du + units * kC * dv * 2, 1024);
     L.dk = align_up(L.dq + tok, 1024);
     L.total = align_up(L.dk + tok, 1024);
     return L;
 }
 
-// bf16 saves [units][rows][128] viewed as (128, rows, units); box (64, rows, 1)
-bool save_map(CUtensorMap* m, const void* p, int rows, size_t units) {
-    const uint64_t dims[3] = {static_cast<uint64_t>(kD), static_cast<uint64_t>(rows), static_cast<uint64_t>(units)};
-    const uint64_t st[2] = {static_cast<uint64_t>(kD) * 2, static_cast<uint64_t>(rows) * kD * 2};
-    const uint32_t box[3] = {64, static_cast<uint32_t>(rows), 1};
+// bf16 saves [units][rows][cols] viewed as (cols, rows, units); box (64, box_rows, 1) (rows and columns
+// past the saved ones read as zeros)
+bool save_map(CUtensorMap* m, const void* p, int cols, int rows, int box_rows, size_t units) {
+    const uint64_t dims[3] = {static_cast<uint64_t>(cols), static_cast<uint64_t>(rows), static_cast<uint64_t>(units)};
+    const uint64_t st[2] = {static_cast<uint64_t>(cols) * 2, static_cast<uint64_t>(rows) * cols * 2};
+    const uint32_t box[3] = {64, static_cast<uint32_t>(box_rows), 1};
     return make_map(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, p, dims, st, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 }  // namespace
 
-size_t backward_tc_workspace_bytes(int B, int T, int Hv) { return tc_bwd_layout(B, T, Hv).total; }
+size_t backward_tc_workspace_bytes(int B, int T, int Hv, int dk, int dv) { return tc_bwd_layout(B, T, Hv, dk, dv).total; }
 
 cudaError_t launch_backward_tc(const void* q, const void* k, const void* v, const void* g, const void* b,
                                const void* w, const float* s0, const void* d_o, const float* dsT, void* dq, void* dk,
                                void* dv, void* dg, void* db, void* dw, float* ds0, int B, int T, int Hk, int Hv,
-                               float scale, void* ws, cudaStream_t s, long long wait_ns) {
-    const ChunkShape sh{B, T, Hk, Hv, kD, kD, kC};
+                               int d_k, int d_v, float scale, void* ws, cudaStream_t s, long long wait_ns) {
+    const ChunkShape sh{B, T, Hk, Hv, d_k, d_v, kC};
     const int NC = sh.nchunks();
     const size_t units = static_cast<size_t>(NC) * B * Hv;
-    const TcBwdLayout L = tc_bwd_layout(B, T, Hv);
+    const TcBwdLayout L = tc_bwd_layout(B, T, Hv, d_k, d_v);
     uint8_t* wsb = static_cast<uint8_t*>(ws);
     __nv_bfloat16* s_save = reinterpret_cast<__nv_bfloat16*>(wsb + L.s);
     __nv_bfloat16* u_save = reinterpret_cast<__nv_bfloat16*>(wsb + L.u);
@@ -1077,14 +1090,15 @@ cudaError_t launch_backward_tc(const void* q, const void* k, const void* v, cons
         !ws_map(&rm.qb, wsb + kWsQb, BF, 2, 128, 64, static_cast<int>(units), 64, 64, SW) ||
         !ws_map(&rm.kh, wsb + kWsKh, BF, 2, 128, 64, static_cast<int>(units), 64, 64, SW) ||
         !ws_map(&rm.m, wsb + kWsM, BF, 2, 64, 64, static_cast<int>(units), 64, 64, SW) ||
-        !token_map(&rm.dout, d_o, B, T, Hv))
+        !token_map(&rm.dout, d_o, B, T, Hv, d_v))
         return cudaErrorInvalidValue;
     GradMaps gm;
-    if (!token_map(&gm.dout, d_o, B, T, Hv) || !token_map(&gm.v, v, B, T, Hv) || !token_map(&gm.w, w, B, T, Hv) ||
-        !token_map(&gm.q, q, B, T, Hk) || !token_map(&gm.k, k, B, T, Hk) || !token_map(&gm.g, g, B, T, Hv) ||
-        !token_map(&gm.b, b, B, T, Hv) || !save_map(&gm.du, du_save, kC, units) ||
-        !save_map(&gm.u, u_save, kC, units) || !save_map(&gm.s, s_save, kD, units) ||
-        !save_map(&gm.ds, ds_save, kD, units) ||
+    if (!token_map(&gm.dout, d_o, B, T, Hv, d_v) || !token_map(&gm.v, v, B, T, Hv, d_v) ||
+        !token_map(&gm.w, w, B, T, Hv, d_v) || !token_map(&gm.q, q, B, T, Hk, d_k) ||
+        !token_map(&gm.k, k, B, T, Hk, d_k) || !token_map(&gm.g, g, B, T, Hv, d_k) ||
+        !token_map(&gm.b, b, B, T, Hv, d_k) || !save_map(&gm.du, du_save, d_v, kC, kC, units) ||
+        !save_map(&gm.u, u_save, d_v, kC, kC, units) || !save_map(&gm.s, s_save, d_v, d_k, kD, units) ||
+        !save_map(&gm.ds, ds_save, d_v, kD, kD, units) ||
         !ws_map(&gm.t, wsb + kWsT, BF, 2, 64, 64, static_cast<int>(units), 64, 64, SW))
         return cudaErrorInvalidValue;
 
@@ -1099,17 +1113,17 @@ cudaError_t launch_backward_tc(const void* q, const void* k, const void* v, cons
     if ((e = cudaFuncSetAttribute(grad_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem)) !=
         cudaSuccess)
         return e;
-    rchain_tc_kernel<<<2 * B * Hv, rs::kThreads, kSmem, s>>>(rm, wsb + L.fw, dsT, ds0, ds_save, du_save, Hv, NC,
-                                                             scale, wait_ns);
+    rchain_tc_kernel<<<(d_v / 64) * B * Hv, rs::kThreads, kSmem, s>>>(rm, wsb + L.fw, dsT, ds0, ds_save, du_save, Hv,
+                                                                       NC, d_k, d_v, scale, wait_ns);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     grad_tc_kernel<<<dim3(NC, B * Hv), gs::kThreads, kSmem, s>>>(
         gm, dq_ws, dk_ws, static_cast<__nv_bfloat16*>(dv), static_cast<__nv_bfloat16*>(dg),
-        static_cast<__nv_bfloat16*>(db), static_cast<__nv_bfloat16*>(dw), T, Hk, Hv, scale, wait_ns);
+        static_cast<__nv_bfloat16*>(db), static_cast<__nv_bfloat16*>(dw), T, Hk, Hv, d_k, d_v, scale, wait_ns);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    const long long rows = static_cast<long long>(B) * T, n4 = rows * Hk * (kD / 4);
+    const long long rows = static_cast<long long>(B) * T, n4 = rows * Hk * (d_k / 4);
     const int gsz = static_cast<int>(n4 / 256 + 1 < 4096 ? n4 / 256 + 1 : 4096);
     group_sum_tc_kernel<<<gsz, 256, 0, s>>>(dq_ws, dk_ws, static_cast<__nv_bfloat16*>(dq),
-                                            static_cast<__nv_bfloat16*>(dk), rows, Hk, Hv);
+                                            static_cast<__nv_bfloat16*>(dk), rows, Hk, Hv, d_k);
     return cudaGetLastError();
 }
 

@@ -153,12 +153,12 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const v
                             const void* w, const float* s0, float* sT, void* o, const ChunkShape& sh, float scale,
                             void* ws, cudaStream_t s, long long wait_ns, void* s_save = nullptr,
                             void* u_save = nullptr);
-// Tensor-core chunked backward (bf16, d_k = d_v = 128, chunks of 64).
-size_t backward_tc_workspace_bytes(int B, int T, int Hv);
+// Tensor-core chunked backward (bf16, d_k and d_v 64 or 128, chunks of 64).
+size_t backward_tc_workspace_bytes(int B, int T, int Hv, int dk, int dv);
 cudaError_t launch_backward_tc(const void* q, const void* k, const void* v, const void* g, const void* b,
                                const void* w, const float* s0, const void* d_o, const float* dsT, void* dq, void* dk,
                                void* dv, void* dg, void* db, void* dw, float* ds0, int B, int T, int Hk, int Hv,
-                               float scale, void* ws, cudaStream_t s, long long wait_ns);
+                               int d_k, int d_v, float scale, void* ws, cudaStream_t s, long long wait_ns);
 int backward_tc_read_clear_status(cudaStream_t s);
 
 }  // namespace gdn2

@@ -302,8 +302,9 @@ gdn2_status gdn2_mixer_decode_step(const void* xq, const void* xk, const void* x
  * finite gradients.
  * q, k, dq, dk: [B, T, H_k, d_k]; v, w, d_o, dv, dw: [B, T, H_v, d_v]; g, b, dg, db: [B, T, H_v, d_k]
  * (all dtype dt); initial_state, d_final_state, d_initial_state: fp32 [B, H_v, d_k, d_v] or NULL
- * (zeros / not written). dq and dk of a key head sum its value heads. d_k = d_v = 128,
- * B * H_v <= 65535 (GDN2_ERR_UNSUPPORTED otherwise).
+ * (zeros / not written). dq and dk of a key head sum its value heads. bf16: d_k and d_v each 64 or
+ * 128 (64 as zero-padded 128); fp32: d_k = d_v = 128; B * H_v <= 65535 (GDN2_ERR_UNSUPPORTED
+ * otherwise). gdn2_backward_recurrent takes d_k = d_v = 128 only.
  * workspace: gdn2_backward_workspace_size(...) bytes of device memory, 16-byte aligned.
  * Errors: as gdn2_chunk_fwd. Asynchronous on `stream`: every launch goes to `stream` (the forward
  * and reverse chains over chunks run side by side inside one launch), the library holds no stream,

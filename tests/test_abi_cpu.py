@@ -214,15 +214,21 @@ def test_backward_argument_errors(g, entry):
     assert f(ptr=0) == g.GDN2_ERR_INVALID_ARG
     assert f(Hk=3, Hv=4) == g.GDN2_ERR_INVALID_ARG
     assert f(dt=4) == g.GDN2_ERR_INVALID_ARG
-    assert f(dk=64, dv=64) == g.GDN2_ERR_UNSUPPORTED
+    assert f(dk=64, dv=64, dt=0) == g.GDN2_ERR_UNSUPPORTED  # fp32: head size 128 only
+    assert f(dk=32, dv=128) == g.GDN2_ERR_UNSUPPORTED
+    assert f(dk=128, dv=192) == g.GDN2_ERR_UNSUPPORTED
     assert f(ptr=0x10004) == g.GDN2_ERR_MISALIGNED
     assert f(ws=0) == g.GDN2_ERR_WORKSPACE
     assert f(wsb=16) == g.GDN2_ERR_WORKSPACE
     assert f(B=32768, T=1, Hv=4) == g.GDN2_ERR_UNSUPPORTED  # (batch, value head) beyond the grid's y range
     size = getattr(g.lib, entry + "_workspace_size")
-    assert size(2, 100, 1, 2, 64, 64, 1) == 0
+    assert size(2, 100, 1, 2, 64, 64, 0) == 0
+    assert size(2, 100, 1, 2, 32, 32, 1) == 0
     assert size(32768, 1, 1, 4, 128, 128, 1) == 0
     assert size(2, 0, 1, 2, 128, 128, 1) == 0
+    # bf16: the chunked form also takes head size 64 (the per-token form does not)
+    assert (size(2, 100, 1, 2, 64, 64, 1) > 0) == (entry == "gdn2_backward")
+    assert (f(dk=64, dv=64, wsb=16) == g.GDN2_ERR_WORKSPACE) == (entry == "gdn2_backward")
 
 
 def test_backward_workspace_sizes(g):

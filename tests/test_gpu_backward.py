@@ -172,6 +172,34 @@ def test_backward_bf16_edge_lengths(g, T, Hk, Hv):
         assert e < TOL["bf16"], (name, e)
 
 
+@pytest.mark.parametrize("dk,dv,decay", [(64, 64, "standard"), (64, 128, "standard"), (128, 64, "standard"),
+                                         (64, 64, "strong")])
+def test_backward_bf16_head_dim_64(g, dk, dv, decay):
+    """head_dim 64 (the pages' quick-start size) on the tensor-core backward: the 64-wide channels or
+    columns read as zero-padded 128; grouped heads, a ragged last chunk, an initial state and dS_T."""
+    import torch
+
+    T, Hk, Hv = 100, 1, 2
+    wl = synth.Workload("bwd-hd64", B=2, T=T, Hk=Hk, Hv=Hv, dk=dk, dv=dv, dtype="bf16", seed=70 + dk + dv,
+                        s0_std=0.02, decay=decay)
+    inp = synth.make_inputs(wl)
+    rng = np.random.default_rng(dk * dv)
+    d_o = synth.round_to(rng.standard_normal((2, T, Hv, dv)), "bf16").astype(np.float64)
+    ds_t = (0.1 * rng.standard_normal((2, Hv, dk, dv))).astype(np.float32).astype(np.float64)
+    dev = lambda a: synth.to_torch(np.ascontiguousarray(a), "bf16", "cuda")
+    ts = [dev(getattr(inp, n)) for n in ("q", "k", "v", "g", "b", "w")]
+    outs = g.backward(*ts, dev(d_o), H.state_to_device(inp.s0), H.state_to_device(ds_t))
+    torch.cuda.synchronize()
+    assert g.gdn2_last_device_status() == g.GDN2_OK
+    ref = oback.gradients(inp.q, inp.k, inp.v, inp.g, inp.b, inp.w, inp.s0, d_o, ds_t)
+    for name, got in zip(("dq", "dk", "dv", "dg", "db", "dw", "ds0"), outs):
+        x = H.to_np(got)
+        assert x.shape == ref[name].shape, name
+        assert np.isfinite(x).all(), name
+        e = max_rel_err(x, ref[name])
+        assert e < TOL["bf16"], (name, e)
+
+
 def test_backward_chunked_matches_recurrent_at_the_bench_shape(g):
     """The bench workload's shapes (B 2, T 32768, H_k 16, H_v 32, bf16 tensors): the chunked path against
     the per-token recurrent path, two fp32 computations that share no arithmetic; errors are normwise
