@@ -168,13 +168,15 @@ constexpr uint32_t kStreamSmemSM = 233472;     // shared memory of one SM (each 
 template <typename Tin, typename TS, int NT, int CPS>
 struct StreamRing {
     static constexpr uint32_t smem = CPS == 1 ? kStreamSmemBlock : (kStreamSmemSM / CPS - 1024) / 128 * 128;
-    static constexpr int parities = NT > 1 ? 2 : 1;            // reduction buffers (alternate per token)
-    static constexpr uint32_t red_bytes = parities * (8 * 2 * 128 + 8) * 4;  // [8 warps][r_b | r_q][128] + [8] k.q
+    // one token: the cross-warp reduction buffer [8 warps][r_b | r_q][128] + [8] k.q
+    static constexpr uint32_t red_bytes = NT > 1 ? 0 : (8 * 2 * 128 + 8) * 4;
     static constexpr uint32_t slab = 128 * 128 * sizeof(TS);
     static constexpr uint32_t tok = NT * 6 * 128 * sizeof(Tin);
     static constexpr uint32_t slot = (slab + tok + 127) / 128 * 128;
-    // per token and d_k row: (alpha, alpha, b.k, b.k, q, q, k, k) fp32, plus the token's 8 partial k.q
-    static constexpr uint32_t rows_bytes = NT > 1 ? NT * (128 * 32 + 32) : 0;
+    // several tokens, per token: [64 d_k row pairs] (alpha, alpha', b.k, b.k') and (q, q', k, k') fp32,
+    // then two partial sums of k.q (float4 units)
+    static constexpr uint32_t tab_f4 = 2 * 64 + 1;
+    static constexpr uint32_t rows_bytes = NT > 1 ? NT * tab_f4 * 16 : 0;
     static constexpr uint32_t avail = smem - red_bytes - rows_bytes - 256;
     static constexpr int depth = avail / slot > 8 ? 8 : (int)(avail / slot);
     static constexpr uint32_t red_off = depth * slot;
@@ -227,10 +229,11 @@ __device__ __forceinline__ void stream_issue(uint8_t* smem_s, uint64_t* bar, int
 
 // Persistent grid over the heads, one CTA per SM, 8 warps: a ring of state slabs (with the tokens of
 // the call) keeps the next depth-1 heads loading and the previous head's store in flight while one
-// head is updated. Per head, thread (warp, lane) holds rows 16 warp .. 16 warp + 15 x columns
-// 4 lane .. 4 lane + 3 of the state in registers across the N tokens; per token the reductions over
-// d_k go in-thread, then across warps through a shared buffer of the token's parity (one block
-// barrier per token).
+// head is updated. One token: thread (warp, lane) holds rows 16 warp .. 16 warp + 15 x columns
+// 4 lane .. 4 lane + 3, and the reductions over d_k go in-thread, then across warps through a shared
+// buffer (one block barrier). Several tokens: a warp holds 16 columns over all d_k rows, so the
+// reductions stay inside the warp and the tokens run without block barriers; the per-row scalars of
+// every token are tabulated once per head.
 template <typename Tin, typename TS, int NT, int CPS>
 __global__ void __launch_bounds__(256, CPS)
     recurrent_stream_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* __restrict__ v,
@@ -349,107 +352,119 @@ __global__ void __launch_bounds__(256, CPS)
             fence_proxy_async_smem();
         }
         if (NT > 1 && row >= 0) {
-            // Several tokens. Per token, this warp's 16 d_k rows' scalars (alpha, b.k, q, k), each duplicated into an
-            // fp32 pair for the packed arithmetic below, and their part of k.q; a warp only reads its
-            // own rows, so no block barrier (the k.q parts are read after the token's barrier).
+            // Several tokens. Thread (warp, lane) holds columns 16 warp + 4 cq .. + 3 (cq = lane mod 4) of
+            // the d_k row pairs (2p, 2p + 1), p = 8 j + rg (rg = lane / 4, j = 0..7): each fp32 pair of the
+            // packed arithmetic is one column over two adjacent rows, so the per-row scalars come as
+            // pairs from the table and the reductions over d_k are in-thread, then over the 8 row
+            // groups of the warp by shuffles: no block barrier between tokens.
             const uint8_t* tkb = smem_s + bsel * R::slot + R::slab;
-            float* rows = reinterpret_cast<float*>(smem_s + R::rows_off);
-            // (lane l takes entry p0 + l: token (p0 + l) / 16, row 16 warp + l mod 16). Every lane runs
-            // every trip, since the shuffles need the whole warp; lanes past the last entry add 0.
-            for (int p0 = 0; p0 < 16 * N; p0 += 32) {
-                const int p = p0 + lane, t = p >> 4, rr = 16 * warp + (p & 15);
-                const bool on = p < 16 * N;
-                float kq = 0.f;
-                if (on) {
-                    const Tin* tk = reinterpret_cast<const Tin*>(tkb) + t * 6 * 128;
-                    const float qq = to_f32(tk[rr]), kk = to_f32(tk[128 + rr]);
-                    const float a = expf(to_f32(tk[256 + rr])), bk = to_f32(tk[384 + rr]) * kk;
-                    float4* dst = reinterpret_cast<float4*>(rows + t * (128 * 8 + 8) + rr * 8);
-                    dst[0] = make_float4(a, a, bk, bk);
-                    dst[1] = make_float4(qq, qq, kk, kk);
-                    kq = kk * qq;
+            float4* tab = reinterpret_cast<float4*>(smem_s + R::rows_off);
+            // the table, per token: [64 row pairs] (alpha, alpha', b.k, b.k'), [64] (q, q', k, k'), and
+            // two partial sums of k.q (one per 32 pairs); thread tid fills pair tid mod 64 of token tid / 64
+            {
+                const int t = tid >> 6, pr = tid & 63;
+                if (t < N) {  // warp-uniform: a token spans two whole warps
+                    const Tin* tk = reinterpret_cast<const Tin*>(tkb) + t * 6 * 128 + 2 * pr;
+                    const float q0 = to_f32(tk[0]), q1 = to_f32(tk[1]), k0 = to_f32(tk[128]), k1 = to_f32(tk[129]);
+                    const float a0 = expf(to_f32(tk[256])), a1 = expf(to_f32(tk[257]));
+                    const float b0 = to_f32(tk[384]) * k0, b1 = to_f32(tk[385]) * k1;
+                    float4* tt = tab + t * R::tab_f4;
+                    tt[pr] = make_float4(a0, a1, b0, b1);
+                    tt[64 + pr] = make_float4(q0, q1, k0, k1);
+                    float kq = fmaf(k1, q1, k0 * q0);
+#pragma unroll
+                    for (int off = 16; off > 0; off >>= 1) kq += __shfl_xor_sync(0xffffffffu, kq, off);
+                    if (lane == 0) reinterpret_cast<float*>(tt + 128)[pr >> 5] = kq;
                 }
-#pragma unroll
-                for (int off = 8; off > 0; off >>= 1) kq += __shfl_xor_sync(0xffffffffu, kq, off);  // 16-lane halves
-                if (on && (lane & 15) == 0) rows[t * (128 * 8 + 8) + 128 * 8 + warp] = kq;
             }
-            __syncwarp();
-            // thread (warp, lane): rows 16 warp .. 16 warp + 15, columns 4 lane .. 4 lane + 3, as two
-            // fp32 pairs per row
+            __syncthreads();
+            const int rg = lane >> 2, cq = lane & 3, col = 16 * warp + 4 * cq;
             TS* S = reinterpret_cast<TS*>(smem_s + bsel * R::slot);
-            uint64_t s[16][2];
+            uint64_t s[8][4];  // s[j][c]: column col + c, rows (2p, 2p + 1), p = 8 j + rg
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const float4 x = load4(S + (16 * warp + i) * 128 + 4 * lane);
-                s[i][0] = f32x2(x.x, x.y);
-                s[i][1] = f32x2(x.z, x.w);
+            for (int j = 0; j < 8; ++j) {
+                const int r0 = 2 * (8 * j + rg);
+                const float4 x = load4(S + r0 * 128 + col), y = load4(S + (r0 + 1) * 128 + col);
+                s[j][0] = f32x2(x.x, y.x);
+                s[j][1] = f32x2(x.y, y.y);
+                s[j][2] = f32x2(x.z, y.z);
+                s[j][3] = f32x2(x.w, y.w);
             }
             for (int t = 0; t < N; ++t) {
-                const Tin* tk = reinterpret_cast<const Tin*>(tkb) + t * 6 * 128;
-                const float* rt_rows = rows + t * (128 * 8 + 8);
-                uint64_t wv[2];
-                {
-                    float v4[4], w4[4];
+                const float4* tt = tab + t * R::tab_f4;
+                uint64_t rb[4] = {0, 0, 0, 0}, rq[4] = {0, 0, 0, 0};  // +0.0f pairs (even-row, odd-row parts)
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const float4 ab = tt[8 * j + rg], qk = tt[64 + 8 * j + rg];
+                    const uint64_t al = f32x2(ab.x, ab.y), bk = f32x2(ab.z, ab.w), qq = f32x2(qk.x, qk.y);
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
-                        v4[c] = to_f32(tk[512 + 4 * lane + c]);
-                        w4[c] = to_f32(tk[640 + 4 * lane + c]);
-                    }
-                    wv[0] = mul_f32x2(f32x2(w4[0], w4[1]), f32x2(v4[0], v4[1]));
-                    wv[1] = mul_f32x2(f32x2(w4[2], w4[3]), f32x2(v4[2], v4[3]));
-                }
-                uint64_t rb[2] = {0, 0}, rq[2] = {0, 0};  // +0.0f pairs
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const ulonglong2 ab = *reinterpret_cast<const ulonglong2*>(rt_rows + (16 * warp + i) * 8);
-                    const uint64_t qp = *reinterpret_cast<const uint64_t*>(rt_rows + (16 * warp + i) * 8 + 4);
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        s[i][h] = mul_f32x2(s[i][h], ab.x);          // alpha
-                        rb[h] = fma_f32x2(s[i][h], ab.y, rb[h]);     // b.k
-                        rq[h] = fma_f32x2(s[i][h], qp, rq[h]);       // q
+                        s[j][c] = mul_f32x2(s[j][c], al);      // alpha
+                        rb[c] = fma_f32x2(s[j][c], bk, rb[c]);  // b.k
+                        rq[c] = fma_f32x2(s[j][c], qq, rq[c]);  // q
                     }
                 }
-                float* rt = red + (t % R::parities) * (8 * 2 * 128 + 8);
-                reinterpret_cast<ulonglong2*>(rt + (warp * 2 + 0) * 128)[lane] = make_ulonglong2(rb[0], rb[1]);
-                reinterpret_cast<ulonglong2*>(rt + (warp * 2 + 1) * 128)[lane] = make_ulonglong2(rq[0], rq[1]);
-                __syncthreads();
-                rb[0] = rb[1] = rq[0] = rq[1] = 0;
+                // v[0..3] = r_b, v[4..7] = r_q of columns col + 0..3, this row group's part; then a
+                // reduce-scatter over the row groups (lane bits 4, 3, 2): row group rg ends with the
+                // whole sum of value rg
+                float v[8];
 #pragma unroll
-                for (int w8 = 0; w8 < 8; ++w8) {
-                    const ulonglong2 x = reinterpret_cast<const ulonglong2*>(rt + (w8 * 2 + 0) * 128)[lane];
-                    const ulonglong2 y = reinterpret_cast<const ulonglong2*>(rt + (w8 * 2 + 1) * 128)[lane];
-                    rb[0] = add_f32x2(rb[0], x.x);
-                    rb[1] = add_f32x2(rb[1], x.y);
-                    rq[0] = add_f32x2(rq[0], y.x);
-                    rq[1] = add_f32x2(rq[1], y.y);
+                for (int c = 0; c < 4; ++c) {
+                    float lo, hi;
+                    f32x2_split(rb[c], lo, hi);
+                    v[c] = lo + hi;
+                    f32x2_split(rq[c], lo, hi);
+                    v[4 + c] = lo + hi;
                 }
-                const float4 kqa = *reinterpret_cast<const float4*>(rt_rows + 128 * 8);
-                const float4 kqb = *reinterpret_cast<const float4*>(rt_rows + 128 * 8 + 4);
-                const float kq = ((kqa.x + kqa.y) + (kqa.z + kqa.w)) + ((kqb.x + kqb.y) + (kqb.z + kqb.w));
-                const uint64_t d[2] = {sub_f32x2(wv[0], rb[0]), sub_f32x2(wv[1], rb[1])};
-                if (warp == 0) {
-                    const uint64_t kq2 = f32x2(kq, kq), sc2 = f32x2(scale, scale);
-                    float ov[4];
-                    f32x2_split(mul_f32x2(sc2, fma_f32x2(kq2, d[0], rq[0])), ov[0], ov[1]);
-                    f32x2_split(mul_f32x2(sc2, fma_f32x2(kq2, d[1], rq[1])), ov[2], ov[3]);
-                    Tin* oh = o + ((static_cast<size_t>(bi) * N + t) * Hv + hv) * 128 + 4 * lane;
+                const bool up4 = (rg & 4) != 0, up2 = (rg & 2) != 0, up1 = (rg & 1) != 0;
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) oh[c] = from_f32<Tin>(ov[c]);
+                for (int i = 0; i < 4; ++i) {
+                    const float keep = up4 ? v[4 + i] : v[i], give = up4 ? v[i] : v[4 + i];
+                    v[i] = keep + __shfl_xor_sync(0xffffffffu, give, 16);
                 }
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const uint64_t kp = *reinterpret_cast<const uint64_t*>(rt_rows + (16 * warp + i) * 8 + 6);
-                    s[i][0] = fma_f32x2(kp, d[0], s[i][0]);
-                    s[i][1] = fma_f32x2(kp, d[1], s[i][1]);
+                for (int i = 0; i < 2; ++i) {
+                    const float keep = up2 ? v[2 + i] : v[i], give = up2 ? v[i] : v[2 + i];
+                    v[i] = keep + __shfl_xor_sync(0xffffffffu, give, 8);
+                }
+                {
+                    const float keep = up1 ? v[1] : v[0], give = up1 ? v[0] : v[1];
+                    v[0] = keep + __shfl_xor_sync(0xffffffffu, give, 4);
+                }
+                // row groups 0..3: d of column col + rg; row groups 4..7 take it and write the output
+                // of column col + rg - 4
+                const Tin* tk = reinterpret_cast<const Tin*>(tkb) + t * 6 * 128;
+                float dd = 0.f;
+                if (rg < 4) dd = to_f32(tk[640 + col + rg]) * to_f32(tk[512 + col + rg]) - v[0];
+                const float dx = __shfl_xor_sync(0xffffffffu, dd, 16);
+                if (rg >= 4) {
+                    const float2 kqp = *reinterpret_cast<const float2*>(tt + 128);
+                    const float kq = kqp.x + kqp.y;
+                    o[((static_cast<size_t>(bi) * N + t) * Hv + hv) * 128 + col + rg - 4] =
+                        from_f32<Tin>(scale * fmaf(kq, dx, v[0]));
+                }
+                uint64_t d2[4];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const float dc = __shfl_sync(0xffffffffu, dd, 4 * c + cq);
+                    d2[c] = f32x2(dc, dc);
+                }
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const float4 qk = tt[64 + 8 * j + rg];
+                    const uint64_t kp = f32x2(qk.z, qk.w);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) s[j][c] = fma_f32x2(kp, d2[c], s[j][c]);
                 }
             }
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                float x0, x1, x2, x3;
-                f32x2_split(s[i][0], x0, x1);
-                f32x2_split(s[i][1], x2, x3);
-                store4(S + (16 * warp + i) * 128 + 4 * lane, make_float4(x0, x1, x2, x3));
+            for (int j = 0; j < 8; ++j) {
+                const int r0 = 2 * (8 * j + rg);
+                float x[4], y[4];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) f32x2_split(s[j][c], x[c], y[c]);
+                store4(S + r0 * 128 + col, make_float4(x[0], x[1], x[2], x[3]));
+                store4(S + (r0 + 1) * 128 + col, make_float4(y[0], y[1], y[2], y[3]));
             }
             fence_proxy_async_smem();
         }
