@@ -528,6 +528,7 @@ def run_variants(device):
         ("fp32 state, 1 token per call", 1, torch.float32, False),
         ("fp32 state, 4 tokens per call", 4, torch.float32, False),
         ("bf16 state, 1 token per call", 1, torch.bfloat16, False),
+        ("bf16 state, 4 tokens per call", 4, torch.bfloat16, False),
         ("fp32 state pool, permuted slot map, 1 token per call", 1, torch.float32, True),
     ]
     stream = torch.cuda.current_stream(device)

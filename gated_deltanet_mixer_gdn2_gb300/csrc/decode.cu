@@ -174,8 +174,8 @@ struct StreamRing {
     static constexpr uint32_t tok = NT * 6 * 128 * sizeof(Tin);
     static constexpr uint32_t slot = (slab + tok + 127) / 128 * 128;
     // several tokens, per token: [64 d_k row pairs] (alpha, alpha', b.k, b.k') and (q, q', k, k') fp32,
-    // then two partial sums of k.q (float4 units)
-    static constexpr uint32_t tab_f4 = 2 * 64 + 1;
+    // two partial sums of k.q, then w.v of the 128 columns (float4 units)
+    static constexpr uint32_t tab_f4 = 2 * 64 + 1 + 32;
     static constexpr uint32_t rows_bytes = NT > 1 ? NT * tab_f4 * 16 : 0;
     static constexpr uint32_t avail = smem - red_bytes - rows_bytes - 256;
     static constexpr int depth = avail / slot > 8 ? 8 : (int)(avail / slot);
@@ -243,9 +243,12 @@ __global__ void __launch_bounds__(256, CPS)
     using R = StreamRing<Tin, TS, NT, CPS>;
     static_assert(R::depth >= 1, "stream ring needs a slot");
     static_assert(R::bar_off + 8 * 8 + 16 <= R::smem, "stream kernel shared memory");
-    // ring slots; heads loading ahead (with a single slot, the next head loads once the previous
-    // store has read the slot, and the other CTA of the SM covers that gap)
-    constexpr int D = R::depth, P = D > 1 ? D - 1 : 1;
+    // ring slots; heads loading ahead. One token: the updated state goes back through its slot, so a
+    // slot is refilled once the store of its head has read it (with a single slot the other CTA of the
+    // SM covers that gap). Several tokens: a slot is refilled as soon as its head's state and tokens
+    // are in registers and the table (the updated state goes from registers to global memory), so
+    // every slot loads ahead.
+    constexpr int D = R::depth, P = NT > 1 ? D : (D > 1 ? D - 1 : 1);
     extern __shared__ __align__(128) uint8_t smem_s[];
     float* red = reinterpret_cast<float*>(smem_s + R::red_off);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem_s + R::bar_off);
@@ -359,27 +362,8 @@ __global__ void __launch_bounds__(256, CPS)
             // groups of the warp by shuffles: no block barrier between tokens.
             const uint8_t* tkb = smem_s + bsel * R::slot + R::slab;
             float4* tab = reinterpret_cast<float4*>(smem_s + R::rows_off);
-            // the table, per token: [64 row pairs] (alpha, alpha', b.k, b.k'), [64] (q, q', k, k'), and
-            // two partial sums of k.q (one per 32 pairs); thread tid fills pair tid mod 64 of token tid / 64
-            {
-                const int t = tid >> 6, pr = tid & 63;
-                if (t < N) {  // warp-uniform: a token spans two whole warps
-                    const Tin* tk = reinterpret_cast<const Tin*>(tkb) + t * 6 * 128 + 2 * pr;
-                    const float q0 = to_f32(tk[0]), q1 = to_f32(tk[1]), k0 = to_f32(tk[128]), k1 = to_f32(tk[129]);
-                    const float a0 = expf(to_f32(tk[256])), a1 = expf(to_f32(tk[257]));
-                    const float b0 = to_f32(tk[384]) * k0, b1 = to_f32(tk[385]) * k1;
-                    float4* tt = tab + t * R::tab_f4;
-                    tt[pr] = make_float4(a0, a1, b0, b1);
-                    tt[64 + pr] = make_float4(q0, q1, k0, k1);
-                    float kq = fmaf(k1, q1, k0 * q0);
-#pragma unroll
-                    for (int off = 16; off > 0; off >>= 1) kq += __shfl_xor_sync(0xffffffffu, kq, off);
-                    if (lane == 0) reinterpret_cast<float*>(tt + 128)[pr >> 5] = kq;
-                }
-            }
-            __syncthreads();
             const int rg = lane >> 2, cq = lane & 3, col = 16 * warp + 4 * cq;
-            TS* S = reinterpret_cast<TS*>(smem_s + bsel * R::slot);
+            const TS* S = reinterpret_cast<const TS*>(smem_s + bsel * R::slot);
             uint64_t s[8][4];  // s[j][c]: column col + c, rows (2p, 2p + 1), p = 8 j + rg
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
@@ -390,6 +374,32 @@ __global__ void __launch_bounds__(256, CPS)
                 s[j][2] = f32x2(x.z, y.z);
                 s[j][3] = f32x2(x.w, y.w);
             }
+            // the table, per token: [64 row pairs] (alpha, alpha', b.k, b.k'), [64] (q, q', k, k'), two
+            // partial sums of k.q (one per 32 pairs) and w.v per column; thread tid fills pair and
+            // column pair tid mod 64 of token tid / 64
+            {
+                const int t = tid >> 6, pr = tid & 63;
+                if (t < N) {  // warp-uniform: a token spans two whole warps
+                    const Tin* tk = reinterpret_cast<const Tin*>(tkb) + t * 6 * 128 + 2 * pr;
+                    const float q0 = to_f32(tk[0]), q1 = to_f32(tk[1]), k0 = to_f32(tk[128]), k1 = to_f32(tk[129]);
+                    const float a0 = expf(to_f32(tk[256])), a1 = expf(to_f32(tk[257]));
+                    const float b0 = to_f32(tk[384]) * k0, b1 = to_f32(tk[385]) * k1;
+                    float4* tt = tab + t * R::tab_f4;
+                    tt[pr] = make_float4(a0, a1, b0, b1);
+                    tt[64 + pr] = make_float4(q0, q1, k0, k1);
+                    reinterpret_cast<float2*>(tt + 129)[pr] =
+                        make_float2(to_f32(tk[640]) * to_f32(tk[512]), to_f32(tk[641]) * to_f32(tk[513]));
+                    float kq = fmaf(k1, q1, k0 * q0);
+#pragma unroll
+                    for (int off = 16; off > 0; off >>= 1) kq += __shfl_xor_sync(0xffffffffu, kq, off);
+                    if (lane == 0) reinterpret_cast<float*>(tt + 128)[pr >> 5] = kq;
+                }
+            }
+            fence_proxy_async_smem();  // the reads of the slot above come before the copy that refills it
+            __syncthreads();
+            if (tid == 0 && kk + D < count)
+                stream_issue<Tin, TS, NT, CPS>(smem_s, full + bsel, bsel, first + (kk + D) * G, N, state, slots,
+                                               n_slots, q, k, v, g, b, w, Hk, Hv);
             for (int t = 0; t < N; ++t) {
                 const float4* tt = tab + t * R::tab_f4;
                 uint64_t rb[4] = {0, 0, 0, 0}, rq[4] = {0, 0, 0, 0};  // +0.0f pairs (even-row, odd-row parts)
@@ -433,9 +443,8 @@ __global__ void __launch_bounds__(256, CPS)
                 }
                 // row groups 0..3: d of column col + rg; row groups 4..7 take it and write the output
                 // of column col + rg - 4
-                const Tin* tk = reinterpret_cast<const Tin*>(tkb) + t * 6 * 128;
                 float dd = 0.f;
-                if (rg < 4) dd = to_f32(tk[640 + col + rg]) * to_f32(tk[512 + col + rg]) - v[0];
+                if (rg < 4) dd = reinterpret_cast<const float*>(tt + 129)[col + rg] - v[0];
                 const float dx = __shfl_xor_sync(0xffffffffu, dd, 16);
                 if (rg >= 4) {
                     const float2 kqp = *reinterpret_cast<const float2*>(tt + 128);
@@ -457,16 +466,26 @@ __global__ void __launch_bounds__(256, CPS)
                     for (int c = 0; c < 4; ++c) s[j][c] = fma_f32x2(kp, d2[c], s[j][c]);
                 }
             }
+            TS* Sg = state + (static_cast<size_t>(row) * Hv + hv) * 16384;
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 const int r0 = 2 * (8 * j + rg);
                 float x[4], y[4];
 #pragma unroll
                 for (int c = 0; c < 4; ++c) f32x2_split(s[j][c], x[c], y[c]);
-                store4(S + r0 * 128 + col, make_float4(x[0], x[1], x[2], x[3]));
-                store4(S + (r0 + 1) * 128 + col, make_float4(y[0], y[1], y[2], y[3]));
+                store4(Sg + r0 * 128 + col, make_float4(x[0], x[1], x[2], x[3]));
+                store4(Sg + (r0 + 1) * 128 + col, make_float4(y[0], y[1], y[2], y[3]));
             }
-            fence_proxy_async_smem();
+        }
+        if (NT > 1) {
+            if (row < 0) {  // an inactive head: nothing to read, the slot is free at once
+                __syncthreads();  // every thread has passed its wait on the slot's barrier
+                if (tid == 0 && kk + D < count)
+                    stream_issue<Tin, TS, NT, CPS>(smem_s, full + bsel, bsel, first + (kk + D) * G, N, state,
+                                                   slots, n_slots, q, k, v, g, b, w, Hk, Hv);
+            }
+            __syncthreads();  // the table is rewritten by the next head
+            continue;
         }
         __syncthreads();
         if (tid == 0) {
