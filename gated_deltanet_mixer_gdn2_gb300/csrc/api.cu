@@ -183,8 +183,9 @@ gdn2_status gdn2_last_device_status(void* stream) {
     const int b = chunk_simt_read_clear_status(s);
     const int c = decode_read_clear_status(s);
     const int d = backward_tc_read_clear_status(s);
-    if (a < 0 || b < 0 || c < 0 || d < 0) return GDN2_ERR_CUDA;
-    return (a | b | c | d) ? GDN2_ERR_TIMEOUT : GDN2_OK;
+    const int e = step_read_clear_status(s);
+    if (a < 0 || b < 0 || c < 0 || d < 0 || e < 0) return GDN2_ERR_CUDA;
+    return (a | b | c | d | e) ? GDN2_ERR_TIMEOUT : GDN2_OK;
 }
 
 void gdn2_set_wait_limit(long long ns) { g_wait_ns.store(ns < 0 ? kDefaultWaitNs : ns, std::memory_order_relaxed); }

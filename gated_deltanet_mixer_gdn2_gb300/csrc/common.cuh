@@ -98,6 +98,7 @@ struct ChunkShape {
 
 // Per-translation-unit status readers (defined next to the kernels).
 int decode_read_clear_status(cudaStream_t s);
+int step_read_clear_status(cudaStream_t s);
 int chunk_simt_read_clear_status(cudaStream_t s);
 int chunk_tc_read_clear_status(cudaStream_t s);
 

@@ -184,18 +184,6 @@ struct StreamRing {
     static constexpr uint32_t bar_off = (rows_off + rows_bytes + 7) / 8 * 8;
 };
 
-__device__ __forceinline__ void bulk_store(void* gdst, const void* ssrc, uint32_t bytes) {
-    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(reinterpret_cast<uint64_t>(gdst)),
-                 "r"(smem_u32(ssrc)), "r"(bytes)
-                 : "memory");
-}
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory"); }
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
 
 // Queue the loads of head h into ring slot `slot`: its state slab and the N tokens' six vectors. An
 // inactive head (slot map gives no row) completes the slot's barrier phase without loading.
@@ -207,7 +195,7 @@ __device__ __forceinline__ void stream_issue(uint8_t* smem_s, uint64_t* bar, int
     const int bi = h / Hv, hv = h - bi * Hv, hk = hv / (Hv / Hk);
     const int row = state_row(slots, n_slots, bi);
     if (row < 0) {
-        mbar_arrive(bar);
+        mbar_arrive1(bar);
         return;
     }
     constexpr uint32_t vb = 128 * sizeof(Tin);

@@ -24,9 +24,16 @@
 //   the cluster writes the new q and k conv states, so every conv state has one writer.
 //   Larger groups: one CTA per (batch row, key head) computes q and k once, updates their conv states,
 //   and runs the value heads of the group one after the other.
+//   Many heads (d_k = d_v = 128, at least four value heads per SM): a persistent grid, each CTA a
+//   contiguous run of (batch row, key head) units, so the value heads of a key head are processed by
+//   one CTA one after another; a ring of shared-memory slots holds each head's state slab, token
+//   vectors and carried conv states by bulk copy, loaded ahead of the head being computed, and the
+//   updated state goes back through its slot by bulk copy. The last value head of a key head writes
+//   the new q and k conv states: its siblings' copies of the old ones have all landed by then.
 #include <cooperative_groups.h>
 
 #include "common.cuh"
+#include "ptx.cuh"
 
 namespace gdn2 {
 namespace {
@@ -34,6 +41,9 @@ namespace {
 constexpr int kStepTaps = 4;
 constexpr float kStepL2Eps = 1e-6f;
 constexpr int kMaxClusterGroup = 8;  // portable cluster size
+
+__device__ int g_status_step;
+int g_step_sms = 0;
 
 __device__ __forceinline__ float sigmoid_acc(float a) { return 1.f / (1.f + expf(-a)); }
 
@@ -317,12 +327,326 @@ __global__ void __launch_bounds__(256, 2)
     if (tid < dv) y[head * dv + tid] = from_f32<T>(o_c * rsqrtf(mean_sq + eps) * wt_c * z_c * sigmoid_acc(z_c));
 }
 
+// ---- persistent form ---------------------------------------------------------------------------
+
+constexpr uint32_t kStepSmem = 232448;  // largest dynamic shared memory of one CTA
+
+// Ring geometry: a slot is the fp32 state slab [128][128], then the head's token vectors (xq, xk, a_g,
+// a_b, xv, a_w; 128 each) and the carried conv rows (q, k, v: 3 x 128 fp32 each).
+template <typename T>
+struct StepRing {
+    static constexpr uint32_t vb = 128 * sizeof(T);
+    static constexpr uint32_t slab = 128 * 128 * 4;
+    static constexpr uint32_t conv_off = slab + 6 * vb;
+    static constexpr uint32_t slot = (conv_off + 9 * 512 + 127) / 128 * 128;
+    static constexpr uint32_t part_bytes = 8 * 2 * 128 * 4;  // [8 warps][r_b | r_q][128] fp32
+    // per-head vectors q, k, alpha, b.k, w.v, o (fp32 [6][128]), reduction partials [16], the update's
+    // cross-warp partials, mbarriers
+    static constexpr uint32_t vecs_bytes = 6 * 512 + 16 * 4 + part_bytes;
+    static constexpr int depth = (kStepSmem - vecs_bytes - 128) / slot > 4 ? 4 : (kStepSmem - vecs_bytes - 128) / slot;
+    static constexpr uint32_t vecs_off = depth * slot;
+    static constexpr uint32_t bar_off = vecs_off + vecs_bytes;
+    static constexpr uint32_t total = bar_off + 8 * 4 + 16;
+};
+
+// Queue the copies of value head h = (batch row) * H_v + (value head) into a slot. Missing conv states
+// (null) are not copied and read as zeros.
+template <typename T>
+__device__ __forceinline__ void step_issue(uint8_t* sl, uint64_t* bar, long long h, const float* state,
+                                           const T* xq, const T* xk, const T* ag, const T* ab, const T* xv,
+                                           const T* aw, const float* sq, const float* sk, const float* sv, int Hk,
+                                           int Hv) {
+    using R = StepRing<T>;
+    const long long bi = h / Hv;
+    const int hv = static_cast<int>(h - bi * Hv), hk = hv / (Hv / Hk);
+    const int nconv = (sq ? 3 : 0) + (sk ? 3 : 0) + (sv ? 3 : 0);
+    mbar_arrive_expect_tx(bar, R::slab + 6 * R::vb + 512 * nconv);
+    bulk_load(sl, state + h * 16384, R::slab, bar);
+    const size_t kq = (static_cast<size_t>(bi) * Hk + hk) * 128, vh = static_cast<size_t>(h) * 128;
+    bulk_load(sl + R::slab + 0 * R::vb, xq + kq, R::vb, bar);
+    bulk_load(sl + R::slab + 1 * R::vb, xk + kq, R::vb, bar);
+    bulk_load(sl + R::slab + 2 * R::vb, ag + vh, R::vb, bar);
+    bulk_load(sl + R::slab + 3 * R::vb, ab + vh, R::vb, bar);
+    bulk_load(sl + R::slab + 4 * R::vb, xv + vh, R::vb, bar);
+    bulk_load(sl + R::slab + 5 * R::vb, aw + vh, R::vb, bar);
+    const size_t Cqk = static_cast<size_t>(Hk) * 128, Cv = static_cast<size_t>(Hv) * 128;
+    uint8_t* cs = sl + R::conv_off;
+    for (int j = 0; j < 3; ++j) {
+        const size_t rq = (static_cast<size_t>(bi) * 3 + j) * Cqk + static_cast<size_t>(hk) * 128;
+        if (sq) bulk_load(cs + (0 + j) * 512, sq + rq, 512, bar);
+        if (sk) bulk_load(cs + (3 + j) * 512, sk + rq, 512, bar);
+        if (sv) bulk_load(cs + (6 + j) * 512, sv + (static_cast<size_t>(bi) * 3 + j) * Cv + static_cast<size_t>(hv) * 128,
+                          512, bar);
+    }
+}
+
+// One CTA per SM, 256 threads: threads 0-127 take the q/k channels and the gates a_g, a_b; threads
+// 128-255 the v channels, a_w, and the gated norm; for the state update warp w holds rows
+// 16 w .. 16 w + 15 (conflict-free rows of the slot) and lane l columns 4 l .. 4 l + 3. The updated
+// state goes back through its slot by bulk copy, and the slot is refilled once that copy has read it.
+template <typename T>
+__global__ void __launch_bounds__(256, 1)
+    mixer_step_stream_kernel(const T* __restrict__ xq, const T* __restrict__ xk, const T* __restrict__ xv,
+                             const float* __restrict__ cq, const float* __restrict__ ck,
+                             const float* __restrict__ cv, const T* __restrict__ ag, const T* __restrict__ ab,
+                             const T* __restrict__ aw, float* __restrict__ sq, float* __restrict__ sk,
+                             float* __restrict__ sv, float* __restrict__ state, const T* __restrict__ z,
+                             const float* __restrict__ weight, float eps, T* __restrict__ y, long long units, int Hk,
+                             int Hv, int neg_eigval, float scale, long long wait_ns) {
+    using R = StepRing<T>;
+    constexpr int D = R::depth, P = D > 1 ? D - 1 : 1;
+    extern __shared__ __align__(128) uint8_t smem_m[];
+    float* s_q = reinterpret_cast<float*>(smem_m + R::vecs_off);
+    float* s_k = s_q + 128;
+    float* s_a = s_q + 256;
+    float* s_bk = s_q + 384;
+    float* s_wv = s_q + 512;
+    float* s_o = s_q + 640;
+    float* s_red = s_q + 768;  // [0..11] q.q, k.k, k.q per q/k warp; [12..15] o.o per v warp
+    float* s_part = s_q + 784;   // the update's cross-warp partials
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem_m + R::bar_off);
+    int* flag = reinterpret_cast<int*>(smem_m + R::bar_off + 8 * 4);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int G = Hv / Hk;
+    const long long u0 = units * blockIdx.x / gridDim.x, u1 = units * (blockIdx.x + 1) / gridDim.x;
+    const long long h0 = u0 * G;
+    const int count = static_cast<int>((u1 - u0) * G);
+    const bool vside = tid >= 128;
+    const int c = tid & 127;  // channel of this thread's side
+    const float wt_c = vside ? weight[c] : 0.f;
+
+    if (tid == 0) {
+        for (int i = 0; i < D; ++i) mbar_init(full + i, 1);
+        fence_mbar_init();
+        for (int kk = 0; kk < P && kk < count; ++kk)
+            step_issue<T>(smem_m + kk * R::slot, full + kk, h0 + kk, state, xq, xk, ag, ab, xv, aw, sq, sk, sv, Hk, Hv);
+    }
+    __syncthreads();
+
+    // conv weights of the head (L2-resident: every batch row shares them), loaded one head ahead
+    auto conv_w = [&](long long h) {
+        const int hv = static_cast<int>(h % Hv);
+        return vside ? *reinterpret_cast<const float4*>(cv + (static_cast<size_t>(hv) * 128 + c) * kStepTaps)
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
+    };
+    auto conv_wq = [&](long long h, const float* wsrc) {
+        const int hk = static_cast<int>(h % Hv) / G;
+        return vside ? make_float4(0.f, 0.f, 0.f, 0.f)
+                     : *reinterpret_cast<const float4*>(wsrc + (static_cast<size_t>(hk) * 128 + c) * kStepTaps);
+    };
+    float4 wv_n = make_float4(0.f, 0.f, 0.f, 0.f), wq_n = wv_n, wk_n = wv_n;
+    float z_n = 0.f;  // the output gate of this thread's channel, one head ahead
+    if (count > 0) {
+        wv_n = conv_w(h0);
+        wq_n = conv_wq(h0, cq);
+        wk_n = conv_wq(h0, ck);
+        if (vside) z_n = to_f32(z[static_cast<size_t>(h0) * 128 + c]);
+    }
+
+    int kk = 0;
+    bool ok = true;
+    for (; kk < count; ++kk) {
+        const long long h = h0 + kk;
+        const int bsel = kk % D;
+        const uint32_t par = (kk / D) & 1;
+        const long long bi = h / Hv;
+        const int hv = static_cast<int>(h - bi * Hv), hk = hv / G, rank = hv - hk * G;
+        const float4 wv4 = wv_n, wq = wq_n, wk = wk_n;
+        const float z_c = z_n;
+        if (kk + 1 < count) {
+            wv_n = conv_w(h + 1);
+            wq_n = conv_wq(h + 1, cq);
+            wk_n = conv_wq(h + 1, ck);
+            if (vside) z_n = to_f32(z[static_cast<size_t>(h + 1) * 128 + c]);
+        }
+        if (tid == 0) {
+            const bool got = mbar_wait(full + bsel, par, wait_ns);
+            if (!got) {
+                atomicOr(&g_status_step, kStatusTimeout);
+                mbar_wait(full + bsel, par, kDefaultWaitNs);
+            }
+            *flag = got ? 1 : 0;
+        }
+        __syncthreads();
+        if (!*flag) {
+            ok = false;
+            break;
+        }
+        mbar_wait(full + bsel, par, kDefaultWaitNs);
+        uint8_t* sl = smem_m + bsel * R::slot;
+        const T* V = reinterpret_cast<const T*>(sl + R::slab);
+        const float* CS = reinterpret_cast<const float*>(sl + R::conv_off);
+
+        // ---- prologue: conv of this side's channel; the partial sums of the two L2 norms and of k.q
+        float xq_c = 0.f, xk_c = 0.f, q3[3] = {0.f, 0.f, 0.f}, k3[3] = {0.f, 0.f, 0.f}, qv = 0.f, kv = 0.f;
+        float xv_c = 0.f, v3[3] = {0.f, 0.f, 0.f};
+        if (!vside) {
+            xq_c = to_f32(V[c]);
+            xk_c = to_f32(V[128 + c]);
+            if (sq) { q3[0] = CS[c]; q3[1] = CS[128 + c]; q3[2] = CS[256 + c]; }
+            if (sk) { k3[0] = CS[384 + c]; k3[1] = CS[512 + c]; k3[2] = CS[640 + c]; }
+            qv = wq.x * q3[0] + wq.y * q3[1] + wq.z * q3[2] + wq.w * xq_c;
+            kv = wk.x * k3[0] + wk.y * k3[1] + wk.z * k3[2] + wk.w * xk_c;
+            float a = qv * qv, b = kv * kv, e = kv * qv;
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) {
+                a += __shfl_xor_sync(0xffffffffu, a, off);
+                b += __shfl_xor_sync(0xffffffffu, b, off);
+                e += __shfl_xor_sync(0xffffffffu, e, off);
+            }
+            if (lane == 0) {
+                s_red[3 * warp] = a;
+                s_red[3 * warp + 1] = b;
+                s_red[3 * warp + 2] = e;
+            }
+            // the raw conv outputs; the L2 norms are applied to the reductions over d_k below
+            s_q[c] = qv;
+            s_k[c] = kv;
+            s_a[c] = sigmoid_acc(-to_f32(V[256 + c]));  // e^{-softplus(a)}
+            s_bk[c] = sigmoid_acc(to_f32(V[384 + c])) * (neg_eigval ? 2.f : 1.f) * kv;
+            if (rank == G - 1) {  // the key head's last value head: every sibling has its copy of the old states
+                const size_t Cqk = static_cast<size_t>(Hk) * 128;
+                const size_t base = static_cast<size_t>(bi) * (kStepTaps - 1) * Cqk + static_cast<size_t>(hk) * 128 + c;
+                if (sq) { sq[base] = q3[1]; sq[base + Cqk] = q3[2]; sq[base + 2 * Cqk] = xq_c; }
+                if (sk) { sk[base] = k3[1]; sk[base + Cqk] = k3[2]; sk[base + 2 * Cqk] = xk_c; }
+            }
+        } else {
+            xv_c = to_f32(V[4 * 128 + c]);
+            if (sv) { v3[0] = CS[768 + c]; v3[1] = CS[896 + c]; v3[2] = CS[1024 + c]; }
+            const float vv = wv4.x * v3[0] + wv4.y * v3[1] + wv4.z * v3[2] + wv4.w * xv_c;
+            s_wv[c] = sigmoid_acc(to_f32(V[5 * 128 + c])) * vv;
+            if (sv) {  // this value head's own conv state: no other head reads it
+                float* sp = sv + static_cast<size_t>(bi) * (kStepTaps - 1) * Hv * 128 + static_cast<size_t>(hv) * 128 + c;
+                const size_t Cv = static_cast<size_t>(Hv) * 128;
+                sp[0] = v3[1]; sp[Cv] = v3[2]; sp[2 * Cv] = xv_c;
+            }
+        }
+        __syncthreads();
+        const float qq = (s_red[0] + s_red[3]) + (s_red[6] + s_red[9]);
+        const float kk2 = (s_red[1] + s_red[4]) + (s_red[7] + s_red[10]);
+        const float kqr = (s_red[2] + s_red[5]) + (s_red[8] + s_red[11]);
+        const float nq = rsqrtf(qq + kStepL2Eps), nk = rsqrtf(kk2 + kStepL2Eps);
+        const float kq = (kqr * nk) * nq;
+
+        // ---- the recurrent update: warp w, rows 16 w .. 16 w + 15; lane l, columns 4 l .. 4 l + 3. The
+        // reductions over d_k go in-thread, then across the warps through a shared buffer.
+        {
+            float* red = s_part;  // [8][r_b | r_q][128]
+            float* S = reinterpret_cast<float*>(sl) + 4 * lane;
+            float4 st[16];
+            float4 rb = make_float4(0.f, 0.f, 0.f, 0.f), rq = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {  // rows 16 w + 4 j .. + 3: their scalars as one broadcast float4 each
+                const int r0 = 16 * warp + 4 * j;
+                const float4 a4 = *reinterpret_cast<const float4*>(s_a + r0);
+                const float4 b4 = *reinterpret_cast<const float4*>(s_bk + r0);
+                const float4 q4 = *reinterpret_cast<const float4*>(s_q + r0);
+                const float av[4] = {a4.x, a4.y, a4.z, a4.w}, bv[4] = {b4.x, b4.y, b4.z, b4.w};
+                const float qv4[4] = {q4.x, q4.y, q4.z, q4.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    float4 t = *reinterpret_cast<const float4*>(S + (r0 + e) * 128);
+                    const float a = av[e], bk = bv[e], qr = qv4[e];
+                    t.x *= a; t.y *= a; t.z *= a; t.w *= a;
+                    rb.x = fmaf(t.x, bk, rb.x); rb.y = fmaf(t.y, bk, rb.y); rb.z = fmaf(t.z, bk, rb.z); rb.w = fmaf(t.w, bk, rb.w);
+                    rq.x = fmaf(t.x, qr, rq.x); rq.y = fmaf(t.y, qr, rq.y); rq.z = fmaf(t.z, qr, rq.z); rq.w = fmaf(t.w, qr, rq.w);
+                    st[4 * j + e] = t;
+                }
+            }
+            reinterpret_cast<float4*>(red + (2 * warp) * 128)[lane] = rb;
+            reinterpret_cast<float4*>(red + (2 * warp + 1) * 128)[lane] = rq;
+            __syncthreads();
+            rb = make_float4(0.f, 0.f, 0.f, 0.f);
+            rq = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int w8 = 0; w8 < 8; ++w8) {
+                const float4 x = reinterpret_cast<const float4*>(red + (2 * w8) * 128)[lane];
+                const float4 y4 = reinterpret_cast<const float4*>(red + (2 * w8 + 1) * 128)[lane];
+                rb.x += x.x; rb.y += x.y; rb.z += x.z; rb.w += x.w;
+                rq.x += y4.x; rq.y += y4.y; rq.z += y4.z; rq.w += y4.w;
+            }
+            // r_b = |k|^-1 S'^T (b . raw k), r_q = |q|^-1 S'^T raw q; the update adds raw k (|k|^-1 d)^T
+            const float4 wv4c = *reinterpret_cast<const float4*>(s_wv + 4 * lane);
+            const float4 d = make_float4(fmaf(-nk, rb.x, wv4c.x), fmaf(-nk, rb.y, wv4c.y), fmaf(-nk, rb.z, wv4c.z),
+                                         fmaf(-nk, rb.w, wv4c.w));
+            if (warp == 0)
+                *reinterpret_cast<float4*>(s_o + 4 * lane) =
+                    make_float4(scale * fmaf(kq, d.x, nq * rq.x), scale * fmaf(kq, d.y, nq * rq.y),
+                                scale * fmaf(kq, d.z, nq * rq.z), scale * fmaf(kq, d.w, nq * rq.w));
+            const float4 dn = make_float4(nk * d.x, nk * d.y, nk * d.z, nk * d.w);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int r0 = 16 * warp + 4 * j;
+                const float4 k4 = *reinterpret_cast<const float4*>(s_k + r0);
+                const float kv4[4] = {k4.x, k4.y, k4.z, k4.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    float4 t = st[4 * j + e];
+                    const float kr = kv4[e];
+                    t.x = fmaf(kr, dn.x, t.x); t.y = fmaf(kr, dn.y, t.y); t.z = fmaf(kr, dn.z, t.z); t.w = fmaf(kr, dn.w, t.w);
+                    *reinterpret_cast<float4*>(S + (r0 + e) * 128) = t;
+                }
+            }
+        }
+        fence_proxy_async_smem();  // the slot's new state is read by the bulk copy below
+        __syncthreads();           // o complete
+        if (tid == 0) {
+            bulk_store(state + h * 16384, sl, R::slab);
+            bulk_commit();
+            if (kk + P < count) {
+                if (D > 1) bulk_wait_read<1>();  // the store of head kk-1 has read the slot it leaves
+                else bulk_wait_read<0>();        // single slot: the store of head kk has read it
+                const int nb = (kk + P) % D;
+                step_issue<T>(smem_m + nb * R::slot, full + nb, h + P, state, xq, xk, ag, ab, xv, aw, sq, sk, sv, Hk,
+                              Hv);
+            }
+        }
+        // ---- gated RMSNorm with the SiLU gate over d_v (the v side's four warps)
+        if (vside) {
+            const float o_c = s_o[c];
+            float e = o_c * o_c;
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) e += __shfl_xor_sync(0xffffffffu, e, off);
+            if (lane == 0) s_red[12 + warp - 4] = e;
+            asm volatile("bar.sync 1, 128;" ::: "memory");
+            const float ms = ((s_red[12] + s_red[13]) + (s_red[14] + s_red[15])) / 128.f;
+            y[static_cast<size_t>(h) * 128 + c] = from_f32<T>(o_c * rsqrtf(ms + eps) * wt_c * z_c * sigmoid_acc(z_c));
+        }
+    }
+    if (tid == 0) {
+        if (!ok)  // drain the copies already issued for heads after kk
+            for (int j = kk + 1; j < kk + P && j < count; ++j) mbar_wait(full + j % D, (j / D) & 1, kDefaultWaitNs);
+        bulk_wait_all();
+    }
+    __syncthreads();
+}
+
 template <int DK, typename T>
 cudaError_t launch_step(const void* xq, const void* xk, const void* xv, const float* cq, const float* ck,
                         const float* cv, const void* ag, const void* ab, const void* aw, float* sq, float* sk,
                         float* sv, float* state, const void* z, const float* weight, float eps, void* y, int B,
                         int Hk, int Hv, int dv, int neg_eigval, float scale, cudaStream_t s) {
     const int G = Hv / Hk;
+    if (g_step_sms == 0) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&g_step_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            g_step_sms = 1;
+    }
+    if (DK == 128 && dv == 128 && static_cast<long long>(B) * Hv >= 4LL * g_step_sms) {
+        using R = StepRing<T>;
+        cudaError_t e = cudaFuncSetAttribute(mixer_step_stream_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)R::total);
+        if (e != cudaSuccess) return e;
+        const long long units = static_cast<long long>(B) * Hk;
+        const int grid = units < g_step_sms ? static_cast<int>(units) : g_step_sms;
+        mixer_step_stream_kernel<T><<<grid, 256, R::total, s>>>(
+            static_cast<const T*>(xq), static_cast<const T*>(xk), static_cast<const T*>(xv), cq, ck, cv,
+            static_cast<const T*>(ag), static_cast<const T*>(ab), static_cast<const T*>(aw), sq, sk, sv, state,
+            static_cast<const T*>(z), weight, eps, static_cast<T*>(y), units, Hk, Hv, neg_eigval, scale,
+            wait_limit_ns());
+        return cudaGetLastError();
+    }
     if (G <= kMaxClusterGroup) {  // one CTA per value head, clusters of the key head's group
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(static_cast<unsigned>(B) * Hv);
@@ -350,6 +674,18 @@ cudaError_t launch_step(const void* xq, const void* xk, const void* xv, const fl
 }
 
 }  // namespace
+
+int step_read_clear_status(cudaStream_t s) {
+    int v = 0;
+    if (cudaMemcpyFromSymbolAsync(&v, g_status_step, sizeof(int), 0, cudaMemcpyDeviceToHost, s) != cudaSuccess) return -1;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return -1;
+    const int zero = 0;
+    if (v && cudaMemcpyToSymbolAsync(g_status_step, &zero, sizeof(int), 0, cudaMemcpyHostToDevice, s) != cudaSuccess)
+        return -1;
+    cudaStreamSynchronize(s);
+    return v;
+}
+
 }  // namespace gdn2
 
 using namespace gdn2;

@@ -39,20 +39,17 @@ def _f32dev(a):
     return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).cuda()
 
 
-# groups of 1 to 8 value heads per key head run as thread-block clusters (one CTA per value head);
-# larger groups (12) as one CTA per key head
-@pytest.mark.parametrize("dtype,dk,dv,Hk,Hv,neg", [("bf16", 128, 128, 2, 4, False), ("bf16", 64, 64, 1, 3, True),
-                                                   ("f32", 128, 64, 2, 2, False), ("f32", 64, 128, 1, 2, True),
-                                                   ("f32", 64, 64, 1, 8, False), ("bf16", 64, 128, 1, 12, False)])
-def test_decode_step_against_chained_oracles(g, dtype, dk, dv, Hk, Hv, neg):
+def _chained(g, dtype, B, N, Hk, Hv, dk, dv, neg, carry, seed):
+    """N fused steps against the fp64 oracles chained token by token; carry = False passes no conv
+    states (every token's conv sees zeros before it)."""
     import torch
 
-    rng = np.random.default_rng(dk + dv + Hv)
-    B, N, scale = 3, 6, 0.7
+    rng = np.random.default_rng(seed)
+    scale = 0.7
     xs, ws, gates, cst, s0, z, wt = _problem(rng, B, N, Hk, Hv, dk, dv, dtype)
     dev = lambda a: synth.to_torch(np.ascontiguousarray(a, dtype=np.float32), dtype, "cuda")
     conv_d = [_f32dev(w) for w in ws]
-    cst_d = [_f32dev(s) for s in cst]
+    cst_d = [_f32dev(s) for s in cst] if carry else [None, None, None]
     st_d = _f32dev(s0)
     w_d = _f32dev(wt)
     ys = []
@@ -60,23 +57,43 @@ def test_decode_step_against_chained_oracles(g, dtype, dk, dv, Hk, Hv, neg):
         tok = lambda a: dev(a[:, t])
         y = torch.empty_like(tok(z))
         g.gdn2_mixer_decode_step(*(tok(x) for x in xs), *conv_d, *(tok(a) for a in gates), st_d, tok(z), w_d, y,
-                                 states=cst_d, neg_eigval=neg, scale=scale)
+                                 states=tuple(cst_d), neg_eigval=neg, scale=scale)
         ys.append(y)
     torch.cuda.synchronize()
     assert g.gdn2_last_device_status() == g.GDN2_OK
     # the oracles, token by token, carrying the conv states and the core state
-    S, cs, y_ref = s0, cst, []
+    S, cs, y_ref = s0, cst if carry else (None, None, None), []
     for t in range(N):
         sl = lambda a: a[:, t:t + 1]
-        q, k, v, gg, b, w, cs = mixer.prologue(*(sl(x) for x in xs), *ws, *(sl(a) for a in gates), states=cs,
+        q, k, v, gg, b, w, ns = mixer.prologue(*(sl(x) for x in xs), *ws, *(sl(a) for a in gates), states=cs,
                                                neg_eigval=neg)
+        if carry:
+            cs = ns
         o, S = oracle.run(q, k, v, gg, b, w, S, scale=scale)
         y_ref.append(mixer.epilogue(o, sl(z), wt)[:, 0])
     tol = H.tol_for(dtype)
     print(H.check("y", H.to_np(torch.stack(ys, dim=1)), np.stack(y_ref, axis=1), tol),
           H.check("core state", st_d.cpu().numpy(), S, tol, head_axis=1))
-    for got, want in zip(cst_d, cs):
-        assert np.array_equal(got.cpu().numpy().astype(np.float64), want)  # conv states hold copies of samples
+    if carry:
+        for got, want in zip(cst_d, cs):
+            assert np.array_equal(got.cpu().numpy().astype(np.float64), want)  # conv states hold copies of samples
+
+
+# groups of 1 to 8 value heads per key head run as thread-block clusters (one CTA per value head);
+# larger groups (12) as one CTA per key head
+@pytest.mark.parametrize("dtype,dk,dv,Hk,Hv,neg", [("bf16", 128, 128, 2, 4, False), ("bf16", 64, 64, 1, 3, True),
+                                                   ("f32", 128, 64, 2, 2, False), ("f32", 64, 128, 1, 2, True),
+                                                   ("f32", 64, 64, 1, 8, False), ("bf16", 64, 128, 1, 12, False)])
+def test_decode_step_against_chained_oracles(g, dtype, dk, dv, Hk, Hv, neg):
+    _chained(g, dtype, 3, 6, Hk, Hv, dk, dv, neg, True, dk + dv + Hv)
+
+
+# the persistent form (d_k = d_v = 128, at least four value heads per SM): groups of 3, 12 and 1 value
+# heads per key head, with and without carried conv states
+@pytest.mark.parametrize("dtype,B,Hk,Hv,neg,carry", [("bf16", 16, 16, 48, False, True), ("f32", 14, 4, 48, True, True),
+                                                     ("bf16", 20, 38, 38, False, False)])
+def test_decode_step_persistent_against_chained_oracles(g, dtype, B, Hk, Hv, neg, carry):
+    _chained(g, dtype, B, 3, Hk, Hv, 128, 128, neg, carry, B + Hk + Hv)
 
 
 def test_decode_step_matches_separate_entry_points(g):
