@@ -46,7 +46,7 @@ def chunk_tc_source_sha() -> str:
     import hashlib
 
     h = hashlib.sha256()
-    for name in ("chunk_tc.cu", "tc_common.cuh"):
+    for name in ("chunk_tc.cu", "tc_common.cuh", "ptx.cuh"):
         with open(os.path.join(ROOT, "gated_deltanet_mixer_gdn2_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
