@@ -38,7 +38,7 @@ FLUSH_BYTES = 256 << 20  # > 129 MB L2
 # quarter of the tokens (B 2, T 8192: 8192 units, inputs and workspace 1.2 GB >> L2), times 4 (the
 # traffic grows with the units; the ~0.1 GB that stays in L2 across a kernel boundary is not
 # counted). Reported only while the tensor-core forward's source is the one that was measured.
-TRAFFIC_RECORD = {"chunk_tc_sha256_16": "6fda7b7f63aa06d2", "bytes": 4 * (1837148928)}
+TRAFFIC_RECORD = {"chunk_tc_sha256_16": "daac68c102f5868b", "bytes": 4 * (1837475072)}
 
 
 def chunk_tc_source_sha() -> str:
@@ -714,9 +714,11 @@ def run_reference(args):
 
 def run_profile(spec: str):
     """One operation of one workload, twice (the second call is the one to capture with ncu -s 1).
-    spec: 'chunk:<workload>[:T]', 'decode:<workload>' or 'next:<workload>' (prologue, epilogue, FG2
-    transform, backward on that workload's shapes); T overrides the workload's token count (a smaller
-    case of the same heads for captures beyond the one-pass launch list)."""
+    spec: 'chunk:<workload>[:T]', 'decode:<workload>', 'update:<workload>:<N>[:bf16]' (gdn2_recurrent_update,
+    N tokens per call, fp32 or bf16 state), 'step:<workload>' (gdn2_mixer_decode_step on that workload's
+    heads, bf16 tokens) or 'next:<workload>' (prologue, epilogue, FG2 transform, backward on that
+    workload's shapes); T overrides the workload's token count (a smaller case of the same heads for
+    captures beyond the one-pass launch list)."""
     import torch
 
     import gated_deltanet_mixer_gdn2_gb300 as g
@@ -741,6 +743,29 @@ def run_profile(spec: str):
         hbm = peaks()[0]
         res = next_rows_rooflines(g, device, hbm, SimpleNamespace(B=wl.B, T=wl.T, Hk=wl.Hk, Hv=wl.Hv, dk=wl.dk))
         print(json.dumps({k: (v["ms"] if isinstance(v, dict) else v) for k, v in res.items()}))
+    elif op == "update":
+        inp = synth.make_inputs(wl, T=wl.T)
+        sdt = torch.bfloat16 if len(parts) > 3 and parts[3] == "bf16" else torch.float32
+        st = torch.from_numpy(inp.s0).to(device).to(sdt)
+        tok = [synth.to_torch(np.ascontiguousarray(getattr(inp, n)), wl.dtype, device)
+               for n in ("q", "k", "v", "g", "b", "w")]
+        o = torch.empty_like(tok[2])
+        for _ in range(2):
+            g.gdn2_recurrent_update(*tok, st, o)
+    elif op == "step":
+        gen = torch.Generator(device=device)
+        gen.manual_seed(11)
+        rn = lambda *s: torch.randn(s, generator=gen, device=device)
+        bf = torch.bfloat16
+        B, Hk, Hv, d = wl.B, wl.Hk, wl.Hv, wl.dk
+        xq, xk, xv = rn(B, Hk, d).to(bf), rn(B, Hk, d).to(bf), rn(B, Hv, d).to(bf)
+        ag, ab, aw, z = (rn(B, Hv, d).to(bf) for _ in range(4))
+        cw = [0.5 * rn(n, 4) for n in (Hk * d, Hk * d, Hv * d)]
+        cs = [rn(B, 3, n) for n in (Hk * d, Hk * d, Hv * d)]
+        st = 0.02 * rn(B, Hv, d, d)
+        y = torch.empty((B, Hv, d), dtype=bf, device=device)
+        for _ in range(2):
+            g.gdn2_mixer_decode_step(xq, xk, xv, *cw, ag, ab, aw, st, z, torch.ones(d, device=device), y, states=cs)
     elif op == "decode":
         inp = synth.make_inputs(wl, T=2)
         st = torch.from_numpy(inp.s0).to(device)
