@@ -57,8 +57,11 @@ __device__ __forceinline__ int state_row(const int* slots, int n_slots, int bi) 
 
 // ---- register kernel ----------------------------------------------------------------------------
 
-template <int DK, typename Tin, typename TS>
-__global__ void __launch_bounds__(256, 2)
+// MINB: blocks per SM the register budget is sized for. Launches of 2-warp CTAs over few heads take 1
+// (their occupancy is set by the grid, and the d_k = 128 kernel then holds its state without
+// spilling); 8-warp CTAs over many heads take 2.
+template <int DK, typename Tin, typename TS, int MINB>
+__global__ void __launch_bounds__(256, MINB)
     recurrent_reg_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* __restrict__ v,
                          const Tin* __restrict__ g, const Tin* __restrict__ b, const Tin* __restrict__ w,
                          TS* __restrict__ state, const int* __restrict__ slots, int n_slots, Tin* __restrict__ o,
@@ -88,6 +91,14 @@ __global__ void __launch_bounds__(256, 2)
         const Tin* kh = k + (tk * Hk + hk) * DK;
         const Tin* gh = g + (tk * Hv + hv) * DK;
         const Tin* bh = b + (tk * Hv + hv) * DK;
+        // w.v is loaded with the row scalars, before the reductions it waits for (at small batch the
+        // token vectors are often not in L2, and a load after the shuffles would add a memory round
+        // trip to the critical path)
+        const Tin* vh = v + (tk * Hv + hv) * dv + col;
+        const Tin* wh = w + (tk * Hv + hv) * dv + col;
+        float wv[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) wv[c] = to_f32(wh[c]) * to_f32(vh[c]);
 
         float4 rb = make_float4(0.f, 0.f, 0.f, 0.f);
         float4 rq = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -127,13 +138,11 @@ __global__ void __launch_bounds__(256, 2)
             kq += __shfl_xor_sync(0xffffffffu, kq, off);
         }
 
-        const Tin* vh = v + (tk * Hv + hv) * dv + col;
-        const Tin* wh = w + (tk * Hv + hv) * dv + col;
         float4 d;
-        d.x = to_f32(wh[0]) * to_f32(vh[0]) - rb.x;
-        d.y = to_f32(wh[1]) * to_f32(vh[1]) - rb.y;
-        d.z = to_f32(wh[2]) * to_f32(vh[2]) - rb.z;
-        d.w = to_f32(wh[3]) * to_f32(vh[3]) - rb.w;
+        d.x = wv[0] - rb.x;
+        d.y = wv[1] - rb.y;
+        d.z = wv[2] - rb.z;
+        d.w = wv[3] - rb.w;
 
         if (rg == 0) {
             Tin* oh = o + (tk * Hv + hv) * dv + col;
@@ -545,10 +554,16 @@ cudaError_t launch_t(const void* q, const void* k, const void* v, const void* g,
     const dim3 block(32 * (dv >= cols ? wpc : dv / 16));
 #define GDN2_DECODE_CASE(DKV)                                                                              \
     case DKV:                                                                                              \
-        recurrent_reg_kernel<DKV, Tin, TS><<<grid, block, 0, s>>>(                                         \
-            static_cast<const Tin*>(q), static_cast<const Tin*>(k), static_cast<const Tin*>(v),            \
-            static_cast<const Tin*>(g), static_cast<const Tin*>(b), static_cast<const Tin*>(w), st, slots, \
-            n_slots, static_cast<Tin*>(o), N, Hk, Hv, dv, scale);                                          \
+        if (wpc == 8)                                                                                      \
+            recurrent_reg_kernel<DKV, Tin, TS, 2><<<grid, block, 0, s>>>(                                  \
+                static_cast<const Tin*>(q), static_cast<const Tin*>(k), static_cast<const Tin*>(v),        \
+                static_cast<const Tin*>(g), static_cast<const Tin*>(b), static_cast<const Tin*>(w), st,    \
+                slots, n_slots, static_cast<Tin*>(o), N, Hk, Hv, dv, scale);                               \
+        else                                                                                               \
+            recurrent_reg_kernel<DKV, Tin, TS, 1><<<grid, block, 0, s>>>(                                  \
+                static_cast<const Tin*>(q), static_cast<const Tin*>(k), static_cast<const Tin*>(v),        \
+                static_cast<const Tin*>(g), static_cast<const Tin*>(b), static_cast<const Tin*>(w), st,    \
+                slots, n_slots, static_cast<Tin*>(o), N, Hk, Hv, dv, scale);                               \
         break;
     switch (dk) {
         GDN2_DECODE_CASE(16)
