@@ -681,6 +681,9 @@ constexpr uint32_t kDuo = 0, kDs = 128, kCols = 256;
 // both rings in flight, an MMA warp issues (one lane), four chain warps read U and the state, four
 // warps form w.v and two of them read the output. They hand over through mbarriers; every wait is
 // bounded.
+// kSave: the backward's form, which also keeps bf16 S_n and U_n of every chunk (s_save, u_save); the
+// forward's form carries no save code in its chain.
+template <bool kSave>
 __global__ void __launch_bounds__(ss::kThreads, 1)
     state_tc_kernel(const __grid_constant__ StateMaps maps, const uint8_t* __restrict__ ws,
                     const float* __restrict__ s0, float* __restrict__ sT_out, int Hv, int dk, int dv, int NC,
@@ -962,7 +965,8 @@ __global__ void __launch_bounds__(ss::kThreads, 1)
             st_row_bf16x32(sbt, r, 4, sx + 32);
             fence_proxy_async_smem();
             arrive(s_ready);
-            if (s_save && real_row) st_global_bf16x64(s_save + (static_cast<size_t>(bh) * NC * dk + r) * dv + 64 * hc, sx);
+            if (kSave && s_save && real_row)
+                st_global_bf16x64(s_save + (static_cast<size_t>(bh) * NC * dk + r) * dv + 64 * hc, sx);
             ok = decay(0, sx);
         }
         for (int n = 0; ok && n < NC; ++n) {
@@ -977,7 +981,7 @@ __global__ void __launch_bounds__(ss::kThreads, 1)
                 fence_proxy_async_smem();
                 tc_fence_before();
                 arrive(u_ready);
-                if (u_save) st_global_bf16x64(u_save + ((static_cast<size_t>(bh) * NC + n) * kC + r) * dv + 64 * hc, x);
+                if (kSave && u_save) st_global_bf16x64(u_save + ((static_cast<size_t>(bh) * NC + n) * kC + r) * dv + 64 * hc, x);
             }
             if (!(ok = warp_wait(s_done, n & 1, wait_ns, err))) break;
             tc_fence_after();
@@ -992,7 +996,7 @@ __global__ void __launch_bounds__(ss::kThreads, 1)
             fence_proxy_async_smem();
             tc_fence_before();
             arrive(s_ready);
-            if (s_save && real_row && n + 1 < NC)
+            if (kSave && s_save && real_row && n + 1 < NC)
                 st_global_bf16x64(s_save + ((static_cast<size_t>(bh) * NC + n + 1) * dk + r) * dv + 64 * hc, sx);
             if (n + 1 < NC) {
                 if (!(ok = decay(n + 1, sx))) break;
@@ -1180,7 +1184,9 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const v
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(factors_exact_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)x_smem);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(state_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s_smem);
+    const bool save = s_save || u_save;
+    e = cudaFuncSetAttribute(save ? state_tc_kernel<true> : state_tc_kernel<false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s_smem);
     if (e != cudaSuccess) return e;
     int dev = 0, nsm = 0;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
@@ -1197,9 +1203,10 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const v
         sh.Hv, NC, sh.dk);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    state_tc_kernel<<<dim3((sh.dv / 64) * sh.B * sh.Hv), ss::kThreads, s_smem, s>>>(sm_, wsb, s0, sT, sh.Hv, sh.dk,
-                                                                                  sh.dv, NC, scale, static_cast<__nv_bfloat16*>(s_save), static_cast<__nv_bfloat16*>(u_save), o != nullptr,
-        wait_ns);
+    auto* state_kernel = save ? state_tc_kernel<true> : state_tc_kernel<false>;
+    state_kernel<<<dim3((sh.dv / 64) * sh.B * sh.Hv), ss::kThreads, s_smem, s>>>(
+        sm_, wsb, s0, sT, sh.Hv, sh.dk, sh.dv, NC, scale, static_cast<__nv_bfloat16*>(s_save),
+        static_cast<__nv_bfloat16*>(u_save), o != nullptr, wait_ns);
     return cudaGetLastError();
 }
 
