@@ -122,17 +122,12 @@ __device__ __forceinline__ void note_failure(volatile int* err) {
     }
 }
 
-// Warp-uniform wait: lane 0 polls (and records a timeout), the verdict is broadcast, and every lane
-// then observes the completed phase itself.
+// Warp-uniform wait: every lane observes the phase itself (bounded), and one vote makes the verdict
+// the warp's; a lane that gave up records the timeout.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, long long limit_ns, volatile int* err) {
-    int ok = 0;
-    if ((threadIdx.x & 31) == 0) {
-        ok = mbar_wait_or_abort(bar, parity, limit_ns, err) ? 1 : 0;
-        if (!ok) note_failure(err);
-    }
-    ok = __shfl_sync(0xffffffffu, ok, 0);
-    if (ok) mbar_wait(bar, parity, kDefaultWaitNs);
-    return ok != 0;
+    const bool ok = mbar_wait_or_abort(bar, parity, limit_ns, err);
+    if (!ok) note_failure(err);
+    return __all_sync(0xffffffffu, ok) != 0;
 }
 
 // 32 fp32 values -> bf16 into four 16-byte chunks (c0..c0+3) of a 128-byte-swizzled row
