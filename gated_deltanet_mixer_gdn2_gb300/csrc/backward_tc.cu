@@ -345,7 +345,7 @@ constexpr uint32_t DS = 98304;    // dS': K-major B (N = 128), block j at DS + 1
 constexpr uint32_t WV = 131072;   // w, block j at WV + 8192 j
 constexpr uint32_t TT = 147456;   // T [64][64] (8 KB) then 8 KB of zeros: the MN-major A operand [T^T ; 0]
 constexpr uint32_t QT = 163840, KT = 180224, GT = 196608, BT = 212992;  // q, k, g, b, block j at +8192 j
-constexpr uint32_t BAR = 229376;  // mbarriers, TMEM base, flag; then G_last, anchors, dgamma
+constexpr uint32_t BAR = 229376;  // mbarriers, TMEM base; then G_last, anchors, dgamma
 constexpr uint32_t TOTAL = BAR + 2048;
 // Rooms reused once their first contents are consumed:
 constexpr uint32_t GF = DS;                  // G fp32, two 16 KB halves of d_k
@@ -400,7 +400,6 @@ __global__ void __launch_bounds__(gs::kThreads, 1)
     const uint32_t sbase = smem_u32(sm);
     uint64_t* bar = reinterpret_cast<uint64_t*>(sm + gs::BAR);  // copies a, b, v; products 1 .. 6, X|Y, Z+V
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + gs::BAR + 96);
-    int* flag = reinterpret_cast<int*>(sm + gs::BAR + 100);
     float* GLs = reinterpret_cast<float*>(sm + gs::GL);
     float* ANs = reinterpret_cast<float*>(sm + gs::AN);
 
@@ -455,7 +454,7 @@ __global__ void __launch_bounds__(gs::kThreads, 1)
     auto desc = [&](uint32_t off, uint32_t lbo) { return smem_desc(sbase + off, lbo, 1024, kSwizzle128B); };
     const uint32_t tl = tmem + (static_cast<uint32_t>(32 * q4) << 16);  // this warp's TMEM lanes
     bool v_issued = false, exact = false;
-    bool ok = cta_wait(bar + 0, 0, wait_ns, flag);
+    bool ok = cta_wait(bar + 0, 0, wait_ns);
 
     // ---- U0 = w.v in place of v (both tiles carry the same swizzle)
     if (ok) {
@@ -505,7 +504,7 @@ __global__ void __launch_bounds__(gs::kThreads, 1)
                 }
             reinterpret_cast<float*>(sm + gs::DGM)[c] = acc;
         }
-        ok = cta_wait(bar + 3, 0, wait_ns, flag) && cta_wait(bar + 1, 0, wait_ns, flag);
+        ok = cta_wait(bar + 3, 0, wait_ns) && cta_wait(bar + 1, 0, wait_ns);
     }
     if (ok) {
         tc_fence_after();
@@ -566,7 +565,7 @@ __global__ void __launch_bounds__(gs::kThreads, 1)
                 mma_bf16(tmem + 384, at + (s * 2048 >> 4), bu + (s * 2048 >> 4), id5, s > 0);
             mma_commit(bar + 4);
         }
-        ok = cta_wait(bar + 4, 0, wait_ns, flag) && cta_wait(bar + 2, 0, wait_ns, flag);
+        ok = cta_wait(bar + 4, 0, wait_ns) && cta_wait(bar + 2, 0, wait_ns);
     }
     if (ok) {
         tc_fence_after();
@@ -624,7 +623,7 @@ __global__ void __launch_bounds__(gs::kThreads, 1)
             for (int s = 0; s < 4; ++s) mma_bf16(tmem + 384, at + (s * 2048 >> 4), bt + (s * 2048 >> 4), id6, s > 0);
             mma_commit(bar + 5);
         }
-        ok = cta_wait(bar + 5, 0, wait_ns, flag);
+        ok = cta_wait(bar + 5, 0, wait_ns);
     }
     if (ok) {
         tc_fence_after();
@@ -673,7 +672,7 @@ __global__ void __launch_bounds__(gs::kThreads, 1)
                 *reinterpret_cast<__nv_bfloat16*>(sm + gs::QA + o) = __float2bfloat16_rn(qq * e);
             }
         }
-        ok = cta_wait(bar + 6, 0, wait_ns, flag);
+        ok = cta_wait(bar + 6, 0, wait_ns);
     }
     if (ok) {
         tc_fence_after();
@@ -698,7 +697,7 @@ __global__ void __launch_bounds__(gs::kThreads, 1)
             for (int s = 0; s < 4; ++s) mma_bf16(tmem + 384, desc(gs::DAB + s * 32, 16), bk + (s * 2048 >> 4), id7, s > 0);
             mma_commit(bar + 7);
         }
-        ok = cta_wait(bar + 7, 0, wait_ns, flag);
+        ok = cta_wait(bar + 7, 0, wait_ns);
         if (ok) {
             tc_fence_after();
             {   // lanes 0-63: X / e^{G-a}, lanes 64-127: Y / e^{G-a}; token row t, channels 32h ..
@@ -725,7 +724,7 @@ __global__ void __launch_bounds__(gs::kThreads, 1)
                 for (int s = 0; s < 4; ++s) mma_bf16(tmem + 384, am + (s * 2048 >> 4), bq + (s * 2048 >> 4), id8, 1);
                 mma_commit(bar + 8);
             }
-            ok = cta_wait(bar + 8, 0, wait_ns, flag);
+            ok = cta_wait(bar + 8, 0, wait_ns);
         }
         if (ok) {
             tc_fence_after();

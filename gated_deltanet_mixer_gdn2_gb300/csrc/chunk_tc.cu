@@ -55,7 +55,7 @@ constexpr uint32_t A1 = 0;        // [b.k.e^{G-a} ; q.e^{G-a}] 128 x 128, K-majo
 constexpr uint32_t K = 32768;     // k -> k.e^{a-G} (64 x 128, K-major, two K blocks)
 constexpr uint32_t G = 49152;     // g -> b.k.e^{G} (64 tokens x 128: MN-major B operand, N = d_k)
 constexpr uint32_t SGS = 65536;   // token-group sums fp32 [16][128]; later M staging [64][64] bf16
-constexpr uint32_t BAR = 73728;   // 2 mbarriers, TMEM base, flag
+constexpr uint32_t BAR = 73728;   // 2 mbarriers, TMEM base
 constexpr uint32_t CST = BAR + 64;  // per-channel anchor a, e^{a}, e^{G_last - a} (fp32 [3][128])
 constexpr uint32_t TOTAL = CST + 3 * 512;
 // solve scratch (A1/K are dead once A|M has been read): fp32, 16-byte aligned rows of 68
@@ -166,7 +166,6 @@ __global__ void __launch_bounds__(fs::kThreads, 3)
     uint64_t* bar_tma = reinterpret_cast<uint64_t*>(sm + fs::BAR);
     uint64_t* bar_mma = bar_tma + 1;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + fs::BAR + 16);
-    int* flag = reinterpret_cast<int*>(sm + fs::BAR + 20);
     float* s_anc = reinterpret_cast<float*>(sm + fs::CST);
     float* s_ea = s_anc + 128;
     float* s_ela = s_anc + 256;
@@ -203,7 +202,7 @@ __global__ void __launch_bounds__(fs::kThreads, 3)
             tma_load_4d(sm + fs::G + kb * 8192, &maps.g, 64 * kb, hv, t0, bi, bar_tma);
         }
     }
-    bool ok = cta_wait(bar_tma, 0, wait_ns, flag);
+    bool ok = cta_wait(bar_tma, 0, wait_ns);
     if (ok) {
         // ---- elementwise pass. Thread = (channel chunk j: 8 channels, token group tg: 4 tokens);
         //      every shared-memory access is one 16-byte chunk of a 128-byte swizzled row.
@@ -351,7 +350,7 @@ __global__ void __launch_bounds__(fs::kThreads, 3)
             }
             mma_commit(bar_mma);
         }
-        ok = cta_wait(bar_mma, 0, wait_ns, flag);
+        ok = cta_wait(bar_mma, 0, wait_ns);
         }
     }
     if (ok) {
@@ -423,7 +422,7 @@ __global__ void __launch_bounds__(fs::kThreads, 3)
             }
             mma_commit(bar_mma);
         }
-        ok = cta_wait(bar_mma, 1, wait_ns, flag);
+        ok = cta_wait(bar_mma, 1, wait_ns);
         if (ok) {
             tc_fence_after();
             const int q4 = warp & 3, half = warp >> 2;
@@ -1049,7 +1048,6 @@ __global__ void __launch_bounds__(128, 1)
     uint8_t* sB = sm + 32768;
     uint64_t* bar = reinterpret_cast<uint64_t*>(sm + 65536);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + 65536 + 16);
-    int* flag = reinterpret_cast<int*>(sm + 65536 + 20);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     constexpr uint32_t kAcol = 128;  // TMEM column of an A operand held in tensor memory
 
@@ -1102,7 +1100,7 @@ __global__ void __launch_bounds__(128, 1)
                 for (int j = 0; j < sh.a_cols / 64; ++j) tma_load_3d(sA + j * sh.a_rows * 128, &maps.a, 64 * j, 0, 0, bar);
             for (int j = 0; j < sh.b_cols / 64; ++j) tma_load_3d(sB + j * sh.b_rows * 128, &maps.b, 64 * j, 0, 0, bar);
         }
-        ok = cta_wait(bar, 0, wait_ns, flag);
+        ok = cta_wait(bar, 0, wait_ns);
     }
     if (ok) {
         if (tid == 0) {
@@ -1125,7 +1123,7 @@ __global__ void __launch_bounds__(128, 1)
             }
             mma_commit(bar + 1);
         }
-        ok = cta_wait(bar + 1, 0, wait_ns, flag);
+        ok = cta_wait(bar + 1, 0, wait_ns);
     }
     if (ok) {
         tc_fence_after();

@@ -32,22 +32,17 @@ constexpr uint32_t kWsUnit = 66048;
 
 __device__ __forceinline__ void record_timeout() { atomicOr(&g_status_tc, kStatusTimeout); }
 
-// CTA-uniform bounded wait: thread 0 polls with the caller's budget; on failure it records the
-// timeout and drains the barrier with the default budget (copies / MMAs in flight must land before
-// the CTA releases its shared memory and TMEM). Everyone returns the same verdict.
-__device__ __forceinline__ bool cta_wait(uint64_t* bar, uint32_t parity, long long limit_ns, int* flag) {
-    if (threadIdx.x == 0) {
-        bool ok = mbar_wait(bar, parity, limit_ns);
-        if (!ok) {
-            record_timeout();
-            mbar_wait(bar, parity, kDefaultWaitNs);
-        }
-        *flag = ok ? 1 : 0;
+// CTA-uniform bounded wait: every thread polls with the caller's budget; a thread that gives up
+// records the timeout and drains the barrier with the default budget (copies / MMAs in flight must
+// land before the CTA releases its shared memory and TMEM). One block vote gives everyone the same
+// verdict.
+__device__ __forceinline__ bool cta_wait(uint64_t* bar, uint32_t parity, long long limit_ns) {
+    bool ok = mbar_wait(bar, parity, limit_ns);  // every thread observes the phase itself
+    if (!ok) {
+        record_timeout();
+        mbar_wait(bar, parity, kDefaultWaitNs);
     }
-    __syncthreads();
-    const bool ok = *flag != 0;
-    if (ok) mbar_wait(bar, parity, kDefaultWaitNs);  // completes at once; orders the async writes
-    return ok;
+    return __syncthreads_and(ok) != 0;
 }
 
 
