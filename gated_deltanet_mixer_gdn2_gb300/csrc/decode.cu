@@ -249,7 +249,6 @@ __global__ void __launch_bounds__(256, CPS)
     extern __shared__ __align__(128) uint8_t smem_s[];
     float* red = reinterpret_cast<float*>(smem_s + R::red_off);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem_s + R::bar_off);
-    int* flag = reinterpret_cast<int*>(smem_s + R::bar_off + 8 * 8);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int G = gridDim.x, first = blockIdx.x;
     const int count = first < nheads ? (nheads - first + G - 1) / G : 0;
@@ -272,20 +271,17 @@ __global__ void __launch_bounds__(256, CPS)
         const int bi = h / Hv, hv = h - bi * Hv;
         const int row = state_row(slots, n_slots, bi);
 
-        if (tid == 0) {
+        {  // every thread observes the slot's phase itself; one block vote decides
             const bool got = mbar_wait(full + bsel, par, wait_ns);
             if (!got) {
                 atomicOr(&g_status_decode, kStatusTimeout);
                 mbar_wait(full + bsel, par, kDefaultWaitNs);
             }
-            *flag = got ? 1 : 0;
+            if (!__syncthreads_and(got)) {
+                ok = false;
+                break;
+            }
         }
-        __syncthreads();
-        if (!*flag) {
-            ok = false;
-            break;
-        }
-        mbar_wait(full + bsel, par, kDefaultWaitNs);
 
         if (NT == 1 && row >= 0) {
             // one token: lanes 0..15 take row 16 warp + lane's q, k, alpha, b.k and pass them round

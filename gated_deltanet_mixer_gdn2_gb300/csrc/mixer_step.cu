@@ -405,7 +405,6 @@ __global__ void __launch_bounds__(256, 1)
     float* s_red = s_q + 768;  // [0..11] q.q, k.k, k.q per q/k warp; [12..15] o.o per v warp
     float* s_part = s_q + 784;   // the update's cross-warp partials
     uint64_t* full = reinterpret_cast<uint64_t*>(smem_m + R::bar_off);
-    int* flag = reinterpret_cast<int*>(smem_m + R::bar_off + 8 * 4);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int G = Hv / Hk;
     const long long u0 = units * blockIdx.x / gridDim.x, u1 = units * (blockIdx.x + 1) / gridDim.x;
@@ -459,20 +458,17 @@ __global__ void __launch_bounds__(256, 1)
             wk_n = conv_wq(h + 1, ck);
             if (vside) z_n = to_f32(z[static_cast<size_t>(h + 1) * 128 + c]);
         }
-        if (tid == 0) {
+        {  // every thread observes the slot's phase itself; one block vote decides
             const bool got = mbar_wait(full + bsel, par, wait_ns);
             if (!got) {
                 atomicOr(&g_status_step, kStatusTimeout);
                 mbar_wait(full + bsel, par, kDefaultWaitNs);
             }
-            *flag = got ? 1 : 0;
+            if (!__syncthreads_and(got)) {
+                ok = false;
+                break;
+            }
         }
-        __syncthreads();
-        if (!*flag) {
-            ok = false;
-            break;
-        }
-        mbar_wait(full + bsel, par, kDefaultWaitNs);
         uint8_t* sl = smem_m + bsel * R::slot;
         const T* V = reinterpret_cast<const T*>(sl + R::slab);
         const float* CS = reinterpret_cast<const float*>(sl + R::conv_off);
