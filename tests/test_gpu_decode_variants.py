@@ -59,12 +59,15 @@ def test_multi_token_equals_repeated_steps(g):
     assert _err(s1.cpu().numpy(), s2.cpu().numpy()) < 1e-5
 
 
-@pytest.mark.parametrize("B,Hv,state_dt", [(4, 2, "f32"), (16, 48, "f32"), (16, 48, "bf16"), (4, 2, "bf16")])
-def test_slot_map_and_inactive_rows(g, B, Hv, state_dt):
-    """B * H_v = 768 heads takes the streaming kernel; 8 heads the register kernel."""
+@pytest.mark.parametrize("B,Hv,state_dt,N", [(4, 2, "f32", 1), (16, 48, "f32", 1), (16, 48, "bf16", 1), (4, 2, "bf16", 1),
+                                              (16, 48, "f32", 3), (16, 48, "bf16", 4)])
+def test_slot_map_and_inactive_rows(g, B, Hv, state_dt, N):
+    """B * H_v = 768 heads takes the streaming kernel (one token, or several with the slot of an
+    inactive head refilled at once); 8 heads the register kernel."""
     import torch
 
-    wl = synth.Workload("t", B=B, T=1, Hk=Hv // 2 if Hv > 1 else 1, Hv=Hv, dk=128, dv=128, seed=50 + B, s0_std=0.02)
+    wl = synth.Workload("t", B=B, T=N, Hk=Hv // 2 if Hv > 1 else 1, Hv=Hv, dk=128, dv=128, seed=50 + B + N,
+                        s0_std=0.02)
     inp = synth.make_inputs(wl)
     n_slots = B + 3
     rng = np.random.default_rng(B)
