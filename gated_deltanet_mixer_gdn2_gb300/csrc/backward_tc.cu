@@ -335,6 +335,8 @@ struct GradMaps {
     CUtensorMap du, u;                   // bf16 [units][64 tokens][128] saves (box 64 x 64)
     CUtensorMap s, ds;                   // bf16 [units][128 d_k][128 d_v] saves (box 64 x 128)
     CUtensorMap t;                       // T of the forward factors
+    CUtensorMap dq_st, dk_st;            // fp32 [B][T][H_v][d_k] sums' inputs (store box 32 channels x 64 tokens)
+    CUtensorMap db_st;                   // bf16 db [B][T][H_v][d_k] (store box 64 channels x 64 tokens)
 };
 
 namespace gs {
@@ -888,8 +890,6 @@ __global__ void __launch_bounds__(gs::kThreads, 1)
         {
             const bool low = q4 < 2;
             const int t = 32 * (q4 & 1) + lane;
-            const bool valid = t < nvalid && (low ? 0 : 64) + 16 * h < d_k;  // a true token and true channels
-            const size_t vo = valid ? krow(t) : 0;
             {
                 const int c0 = (low ? 0 : 64) + 16 * h;
                 uint32_t rq[16], rk[16], rh[16];
@@ -946,26 +946,42 @@ __global__ void __launch_bounds__(gs::kThreads, 1)
                     ok_[e] = fmaf(dkh, eH, zv) + dbeta * bb;
                     ob[e] = dbeta * kk;
                 }
-                if (valid) {
+                // dq, dk, db leave through shared memory and bulk tensor stores (tokens past T and
+                // channels past d_k are clipped by the tensor maps): the rooms of Y, Z + V and the copied
+                // q / k / h columns are free once every thread has passed the barrier below
+                __syncthreads();
+                const int jq = c0 >> 5, cq = (c0 & 31) >> 2;  // fp32 box (32 channels) and its 16-byte chunk
 #pragma unroll
-                    for (int f = 0; f < 4; ++f) {
-                        reinterpret_cast<float4*>(dq_ws + vo + c0)[f] =
-                            make_float4(oq[4 * f], oq[4 * f + 1], oq[4 * f + 2], oq[4 * f + 3]);
-                        reinterpret_cast<float4*>(dk_ws + vo + c0)[f] =
-                            make_float4(ok_[4 * f], ok_[4 * f + 1], ok_[4 * f + 2], ok_[4 * f + 3]);
-                    }
-                    float y0[8], y1[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        y0[e] = ob[e];
-                        y1[e] = ob[8 + e];
-                    }
-                    reinterpret_cast<uint4*>(db + vo + c0)[0] = pack8(y0);
-                    reinterpret_cast<uint4*>(db + vo + c0)[1] = pack8(y1);
+                for (int f = 0; f < 4; ++f) {
+                    const uint32_t o = jq * 8192 + t * 128 + (((cq + f) ^ (t & 7)) << 4);
+                    *reinterpret_cast<float4*>(sm + gs::YF + o) =
+                        make_float4(oq[4 * f], oq[4 * f + 1], oq[4 * f + 2], oq[4 * f + 3]);
+                    *reinterpret_cast<float4*>(sm + gs::ZF + o) =
+                        make_float4(ok_[4 * f], ok_[4 * f + 1], ok_[4 * f + 2], ok_[4 * f + 3]);
                 }
+                const int jb = c0 >> 6, cb8 = (c0 & 63) >> 3;  // bf16 box (64 channels) and its chunk
+                float y0[8], y1[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    y0[e] = ob[e];
+                    y1[e] = ob[8 + e];
+                }
+                *reinterpret_cast<uint4*>(sm + gs::TT + jb * 8192 + t * 128 + ((cb8 ^ (t & 7)) << 4)) = pack8(y0);
+                *reinterpret_cast<uint4*>(sm + gs::TT + jb * 8192 + t * 128 + (((cb8 + 1) ^ (t & 7)) << 4)) = pack8(y1);
             }
         }
+        fence_proxy_async_smem();
         __syncthreads();
+        if (tid == 0) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                tma_store_4d(&maps.dq_st, sm + gs::YF + j * 8192, 32 * j, hv, n * kC, bi);
+                tma_store_4d(&maps.dk_st, sm + gs::ZF + j * 8192, 32 * j, hv, n * kC, bi);
+            }
+            tma_store_4d(&maps.db_st, sm + gs::TT, 0, hv, n * kC, bi);
+            tma_store_4d(&maps.db_st, sm + gs::TT + 8192, 64, hv, n * kC, bi);
+            bulk_commit();
+        }
         // ---- dg_t = sum_{s >= t} dG_s + sum_s E_s + dgamma gamma (the gradient of G_last): thread = channel c
         //      and a quarter of the tokens; the quarters exchange their sums through the room g has left
         {
@@ -992,10 +1008,12 @@ __global__ void __launch_bounds__(gs::kThreads, 1)
             }
         }
     }
-    if (tid == 0) {  // every copy issued has landed before the block releases its shared memory
+    if (tid == 0) {  // every copy issued has landed, and the stores have read their sources, before the
+                     // block releases its shared memory
         mbar_wait(bar + 0, 0, kDefaultWaitNs);
         mbar_wait(bar + 1, 0, kDefaultWaitNs);
         if (v_issued) mbar_wait(bar + 2, 0, kDefaultWaitNs);
+        bulk_wait_all();
     }
     tc_fence_before();
     __syncthreads();
@@ -1061,6 +1079,16 @@ bool save_map(CUtensorMap* m, const void* p, int cols, int rows, int box_rows, s
 
 size_t backward_tc_workspace_bytes(int B, int T, int Hv, int dk, int dv) { return tc_bwd_layout(B, T, Hv, dk, dv).total; }
 
+// [B][T][H][d] token rows (element size esize) as the target of bulk tensor stores: box of box_c
+// channels (128 bytes, 128-byte swizzle) x 64 tokens of one head
+static bool tok_store_map(CUtensorMap* m, const void* p, CUtensorMapDataType dt, int esize, int B, int T, int H,
+                          int d, int box_c) {
+    const uint64_t dims[4] = {(uint64_t)d, (uint64_t)H, (uint64_t)T, (uint64_t)B};
+    const uint64_t st[3] = {(uint64_t)d * esize, (uint64_t)H * d * esize, (uint64_t)T * H * d * esize};
+    const uint32_t box[4] = {(uint32_t)box_c, 1, (uint32_t)kC, 1};
+    return make_map(m, dt, 4, p, dims, st, box, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
 cudaError_t launch_backward_tc(const void* q, const void* k, const void* v, const void* g, const void* b,
                                const void* w, const float* s0, const void* d_o, const float* dsT, void* dq, void* dk,
                                void* dv, void* dg, void* db, void* dw, float* ds0, int B, int T, int Hk, int Hv,
@@ -1098,7 +1126,10 @@ cudaError_t launch_backward_tc(const void* q, const void* k, const void* v, cons
         !token_map(&gm.b, b, B, T, Hv, d_k) || !save_map(&gm.du, du_save, d_v, kC, kC, units) ||
         !save_map(&gm.u, u_save, d_v, kC, kC, units) || !save_map(&gm.s, s_save, d_v, d_k, kD, units) ||
         !save_map(&gm.ds, ds_save, d_v, kD, kD, units) ||
-        !ws_map(&gm.t, wsb + kWsT, BF, 2, 64, 64, static_cast<int>(units), 64, 64, SW))
+        !ws_map(&gm.t, wsb + kWsT, BF, 2, 64, 64, static_cast<int>(units), 64, 64, SW) ||
+        !tok_store_map(&gm.dq_st, dq_ws, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, B, T, Hv, d_k, 32) ||
+        !tok_store_map(&gm.dk_st, dk_ws, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, B, T, Hv, d_k, 32) ||
+        !tok_store_map(&gm.db_st, db, BF, 2, B, T, Hv, d_k, 64))
         return cudaErrorInvalidValue;
 
     // Both kernels run one CTA per SM and take the whole 227 KB: operand descriptors can then never
