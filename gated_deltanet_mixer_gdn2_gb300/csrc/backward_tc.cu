@@ -336,7 +336,7 @@ struct GradMaps {
     CUtensorMap s, ds;                   // bf16 [units][128 d_k][128 d_v] saves (box 64 x 128)
     CUtensorMap t;                       // T of the forward factors
     CUtensorMap dq_st, dk_st;            // fp32 [B][T][H_v][d_k] sums' inputs (store box 32 channels x 64 tokens)
-    CUtensorMap db_st;                   // bf16 db [B][T][H_v][d_k] (store box 64 channels x 64 tokens)
+    CUtensorMap db_st, dg_st;            // bf16 db, dg [B][T][H_v][d_k] (store box 64 channels x 64 tokens)
 };
 
 namespace gs {
@@ -412,7 +412,6 @@ __global__ void __launch_bounds__(gs::kThreads, 1)
     const int q4 = warp & 3, h = warp >> 2;  // TMEM lane quarter, column quarter
     const int nvalid = min(kC, T - n * kC);
     // token rows of the d_k-indexed outputs (dq, dk per value head, dg, db) and of the d_v-indexed ones
-    auto krow = [&](int t) { return ((static_cast<size_t>(bi) * T + n * kC + t) * Hv + hv) * d_k; };
     auto vrow = [&](int t) { return ((static_cast<size_t>(bi) * T + n * kC + t) * Hv + hv) * d_v; };
 
     if (tid == 0) {
@@ -1001,11 +1000,22 @@ __global__ void __launch_bounds__(gs::kThreads, 1)
                 fmaf(dgm, __expf(GLs[c]), (xs[c] + xs[2 * kD + c]) + (xs[4 * kD + c] + xs[6 * kD + c]));
             float run = 0.f;  // a quarter starts from the totals of the later ones
             for (int q = 3; q > hf; --q) run += xs[(2 * q + 1) * kD + c];
+            // dg leaves through the room b has left (128-byte swizzled [64 t][64 c] blocks) and two bulk
+            // tensor stores (tokens past T and channels past d_k clipped by the tensor map)
+            uint8_t* dgs = sm + gs::BT + (c >> 6) * 8192 + 2 * (c & 7);
 #pragma unroll 8
             for (int t = t0 + 15; t >= t0; --t) {
                 run += *reinterpret_cast<const float*>(sm + gs::XF + fidx(t, c));
-                if (t < nvalid && c < d_k) dg[krow(t) + c] = __float2bfloat16_rn(run + off);
+                *reinterpret_cast<__nv_bfloat16*>(dgs + t * 128 + ((((c & 63) >> 3) ^ (t & 7)) << 4)) =
+                    __float2bfloat16_rn(run + off);
             }
+        }
+        fence_proxy_async_smem();
+        __syncthreads();
+        if (tid == 0) {
+            tma_store_4d(&maps.dg_st, sm + gs::BT, 0, hv, n * kC, bi);
+            tma_store_4d(&maps.dg_st, sm + gs::BT + 8192, 64, hv, n * kC, bi);
+            bulk_commit();
         }
     }
     if (tid == 0) {  // every copy issued has landed, and the stores have read their sources, before the
@@ -1129,7 +1139,8 @@ cudaError_t launch_backward_tc(const void* q, const void* k, const void* v, cons
         !ws_map(&gm.t, wsb + kWsT, BF, 2, 64, 64, static_cast<int>(units), 64, 64, SW) ||
         !tok_store_map(&gm.dq_st, dq_ws, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, B, T, Hv, d_k, 32) ||
         !tok_store_map(&gm.dk_st, dk_ws, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, B, T, Hv, d_k, 32) ||
-        !tok_store_map(&gm.db_st, db, BF, 2, B, T, Hv, d_k, 64))
+        !tok_store_map(&gm.db_st, db, BF, 2, B, T, Hv, d_k, 64) ||
+        !tok_store_map(&gm.dg_st, dg, BF, 2, B, T, Hv, d_k, 64))
         return cudaErrorInvalidValue;
 
     // Both kernels run one CTA per SM and take the whole 227 KB: operand descriptors can then never
