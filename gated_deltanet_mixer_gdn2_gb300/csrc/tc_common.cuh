@@ -35,7 +35,7 @@ __device__ __forceinline__ void record_timeout() { atomicOr(&g_status_tc, kStatu
 // CTA-uniform bounded wait: every thread polls with the caller's budget; a thread that gives up
 // records the timeout and drains the barrier with the default budget (copies / MMAs in flight must
 // land before the CTA releases its shared memory and TMEM). One block vote gives everyone the same
-// verdict.
+// outcome.
 __device__ __forceinline__ bool cta_wait(uint64_t* bar, uint32_t parity, long long limit_ns) {
     bool ok = mbar_wait(bar, parity, limit_ns);  // every thread observes the phase itself
     if (!ok) {
@@ -117,7 +117,7 @@ __device__ __forceinline__ void note_failure(volatile int* err) {
     }
 }
 
-// Warp-uniform wait: every lane observes the phase itself (bounded), and one vote makes the verdict
+// Warp-uniform wait: every lane observes the phase itself (bounded), and one vote makes the outcome
 // the warp's; a lane that gave up records the timeout.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, long long limit_ns, volatile int* err) {
     const bool ok = mbar_wait_or_abort(bar, parity, limit_ns, err);
