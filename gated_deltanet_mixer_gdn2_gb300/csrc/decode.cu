@@ -17,10 +17,11 @@
 //   warp shuffles across the 8 row groups. No shared memory, no block barrier.
 //   Streaming kernel (d_k = d_v = 128, up to 4 tokens per call, many heads): a persistent grid walks
 //   the heads; each state slab is bulk-copied into a shared-memory ring with the call's token
-//   vectors, carried through the tokens in registers and bulk-copied back, so that the loads of the
-//   next heads and the store of the previous one are in flight while a head is computed. The ring
-//   takes as many slots as fit: 3 with fp32 state, 5-6 with bf16 state (a bf16 slab is half the
-//   bytes, so twice as many heads keep the HBM busy).
+//   vectors, so that the loads of the next heads are in flight while a head is computed. One token:
+//   the updated slab goes back through its slot by bulk copy (one CTA per SM with 3 fp32 slots, or
+//   two CTAs per SM with 3 bf16 slots each: a bf16 slab is half the bytes). Several tokens: two CTAs
+//   per SM, the state carried through the tokens in registers, the slot refilled as soon as the
+//   state and the tokens' table are in registers, and the updated state stored from registers.
 #include "common.cuh"
 #include "ptx.cuh"
 
