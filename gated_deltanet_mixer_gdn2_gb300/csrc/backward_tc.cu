@@ -393,10 +393,9 @@ constexpr float kSpanPair = 120.f;
 
 // One CTA per (chunk, batch . value head); 512 threads, one CTA per SM (the inputs fill shared memory).
 __global__ void __launch_bounds__(gs::kThreads, 1)
-    grad_tc_kernel(const __grid_constant__ GradMaps maps, float* __restrict__ dq_ws,
-                   float* __restrict__ dk_ws, __nv_bfloat16* __restrict__ dv, __nv_bfloat16* __restrict__ dg,
-                   __nv_bfloat16* __restrict__ db, __nv_bfloat16* __restrict__ dw, int T, int Hk, int Hv,
-                   int d_k, int d_v, float scale, long long wait_ns) {
+    grad_tc_kernel(const __grid_constant__ GradMaps maps, __nv_bfloat16* __restrict__ dv,
+                   __nv_bfloat16* __restrict__ dw, int T, int Hk, int Hv, int d_k, int d_v, float scale,
+                   long long wait_ns) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(sm);
@@ -411,7 +410,7 @@ __global__ void __launch_bounds__(gs::kThreads, 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int q4 = warp & 3, h = warp >> 2;  // TMEM lane quarter, column quarter
     const int nvalid = min(kC, T - n * kC);
-    // token rows of the d_k-indexed outputs (dq, dk per value head, dg, db) and of the d_v-indexed ones
+    // token rows of the d_v-indexed outputs dv, dw (dq, dk, db and dg leave through tensor maps)
     auto vrow = [&](int t) { return ((static_cast<size_t>(bi) * T + n * kC + t) * Hv + hv) * d_v; };
 
     if (tid == 0) {
@@ -1158,8 +1157,7 @@ cudaError_t launch_backward_tc(const void* q, const void* k, const void* v, cons
                                                                        NC, d_k, d_v, scale, wait_ns);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     grad_tc_kernel<<<dim3(NC, B * Hv), gs::kThreads, kSmem, s>>>(
-        gm, dq_ws, dk_ws, static_cast<__nv_bfloat16*>(dv), static_cast<__nv_bfloat16*>(dg),
-        static_cast<__nv_bfloat16*>(db), static_cast<__nv_bfloat16*>(dw), T, Hk, Hv, d_k, d_v, scale, wait_ns);
+        gm, static_cast<__nv_bfloat16*>(dv), static_cast<__nv_bfloat16*>(dw), T, Hk, Hv, d_k, d_v, scale, wait_ns);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     const long long rows = static_cast<long long>(B) * T, n4 = rows * Hk * (d_k / 4);
     const int gsz = static_cast<int>(n4 / 256 + 1 < 4096 ? n4 / 256 + 1 : 4096);
