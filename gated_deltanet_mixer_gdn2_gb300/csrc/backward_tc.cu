@@ -337,6 +337,7 @@ struct GradMaps {
     CUtensorMap t;                       // T of the forward factors
     CUtensorMap dq_st, dk_st;            // fp32 [B][T][H_v][d_k] sums' inputs (store box 32 channels x 64 tokens)
     CUtensorMap db_st, dg_st;            // bf16 db, dg [B][T][H_v][d_k] (store box 64 channels x 64 tokens)
+    CUtensorMap dv_st, dw_st;            // bf16 dv, dw [B][T][H_v][d_v] (store box 64 columns x 64 tokens)
 };
 
 namespace gs {
@@ -393,8 +394,7 @@ constexpr float kSpanPair = 120.f;
 
 // One CTA per (chunk, batch . value head); 512 threads, one CTA per SM (the inputs fill shared memory).
 __global__ void __launch_bounds__(gs::kThreads, 1)
-    grad_tc_kernel(const __grid_constant__ GradMaps maps, __nv_bfloat16* __restrict__ dv,
-                   __nv_bfloat16* __restrict__ dw, int T, int Hk, int Hv, int d_k, int d_v, float scale,
+    grad_tc_kernel(const __grid_constant__ GradMaps maps, int T, int Hk, int Hv, int d_k, int d_v, float scale,
                    long long wait_ns) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -410,8 +410,6 @@ __global__ void __launch_bounds__(gs::kThreads, 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int q4 = warp & 3, h = warp >> 2;  // TMEM lane quarter, column quarter
     const int nvalid = min(kC, T - n * kC);
-    // token rows of the d_v-indexed outputs dv, dw (dq, dk, db and dg leave through tensor maps)
-    auto vrow = [&](int t) { return ((static_cast<size_t>(bi) * T + n * kC + t) * Hv + hv) * d_v; };
 
     if (tid == 0) {
         for (int i = 0; i < 9; ++i) mbar_init(bar + i, 1);
@@ -569,29 +567,27 @@ __global__ void __launch_bounds__(gs::kThreads, 1)
     }
     if (ok) {
         tc_fence_after();
-        if (q4 < 2) {  // dU0 -> dv = w.dU0, dw = v.dU0: token row t, d_v columns 32h ..
+        if (q4 < 2) {  // dU0 -> dv = w.dU0, dw = v.dU0: token row t, d_v columns 32h .., written in place
+                       // of w and v (their last reader) for the bulk tensor stores below
             const int t = 32 * q4 + lane;
-            const size_t o = vrow(t < nvalid ? t : 0);
 #pragma unroll 1
             for (int q = 0; q < 2; ++q) {
                 float x[16];
                 tmem_ld_cols<1>(tl + 384 + 32 * h + 16 * q, x);
-                if (t < nvalid && 32 * h < d_v) {
 #pragma unroll
-                    for (int c2 = 0; c2 < 2; ++c2) {
-                        const int cc = 4 * h + 2 * q + c2;  // 16-byte piece of the row: 8 columns
-                        const uint32_t so = (cc >> 3) * 8192 + t * 128 + (((cc & 7) ^ (t & 7)) << 4);
-                        float wv[8], vv[8], ov[8], ow[8];
-                        unpack8(*reinterpret_cast<const uint4*>(sm + gs::WV + so), wv);
-                        unpack8(*reinterpret_cast<const uint4*>(sm + gs::VR + so), vv);
+                for (int c2 = 0; c2 < 2; ++c2) {
+                    const int cc = 4 * h + 2 * q + c2;  // 16-byte piece of the row: 8 columns
+                    const uint32_t so = (cc >> 3) * 8192 + t * 128 + (((cc & 7) ^ (t & 7)) << 4);
+                    float wv[8], vv[8], ov[8], ow[8];
+                    unpack8(*reinterpret_cast<const uint4*>(sm + gs::WV + so), wv);
+                    unpack8(*reinterpret_cast<const uint4*>(sm + gs::VR + so), vv);
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            ov[e] = wv[e] * x[8 * c2 + e];
-                            ow[e] = vv[e] * x[8 * c2 + e];
-                        }
-                        reinterpret_cast<uint4*>(dv + o)[cc] = pack8(ov);
-                        reinterpret_cast<uint4*>(dw + o)[cc] = pack8(ow);
+                    for (int e = 0; e < 8; ++e) {
+                        ov[e] = wv[e] * x[8 * c2 + e];
+                        ow[e] = vv[e] * x[8 * c2 + e];
                     }
+                    *reinterpret_cast<uint4*>(sm + gs::WV + so) = pack8(ov);
+                    *reinterpret_cast<uint4*>(sm + gs::VR + so) = pack8(ow);
                 }
             }
         } else if (h < 2) {  // dT: token row t, columns 32h .. -> bf16 [t][s] (MN-major B)
@@ -600,7 +596,20 @@ __global__ void __launch_bounds__(gs::kThreads, 1)
             tmem_ld_cols<2>(tl + 192 + 32 * h, x);
             st_row_bf16x32(sm + gs::DT, t, 4 * h, x);
         }
-        __syncthreads();  // w is read: its room takes dA and dM
+        // dv and dw leave by bulk tensor stores (tokens past T and columns past d_v clipped by the maps);
+        // their rooms are taken next, so the stores must have read them first
+        fence_proxy_async_smem();
+        __syncthreads();
+        if (tid == 0) {
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                tma_store_4d(&maps.dv_st, sm + gs::WV + j * 8192, 64 * j, hv, n * kC, bi);
+                tma_store_4d(&maps.dw_st, sm + gs::VR + j * 8192, 64 * j, hv, n * kC, bi);
+            }
+            bulk_commit();
+            bulk_wait_read_all();
+        }
+        __syncthreads();  // w (now dv) is read: its room takes dA and dM
         if (q4 < 2 && h < 2) {  // dM = scale tril(dO U^T): token row t, columns 32h .. -> bf16 row
             const int t = 32 * q4 + lane;
             float x[32];
@@ -1139,7 +1148,8 @@ cudaError_t launch_backward_tc(const void* q, const void* k, const void* v, cons
         !tok_store_map(&gm.dq_st, dq_ws, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, B, T, Hv, d_k, 32) ||
         !tok_store_map(&gm.dk_st, dk_ws, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, B, T, Hv, d_k, 32) ||
         !tok_store_map(&gm.db_st, db, BF, 2, B, T, Hv, d_k, 64) ||
-        !tok_store_map(&gm.dg_st, dg, BF, 2, B, T, Hv, d_k, 64))
+        !tok_store_map(&gm.dg_st, dg, BF, 2, B, T, Hv, d_k, 64) ||
+        !tok_store_map(&gm.dv_st, dv, BF, 2, B, T, Hv, d_v, 64) || !tok_store_map(&gm.dw_st, dw, BF, 2, B, T, Hv, d_v, 64))
         return cudaErrorInvalidValue;
 
     // Both kernels run one CTA per SM and take the whole 227 KB: operand descriptors can then never
@@ -1157,7 +1167,7 @@ cudaError_t launch_backward_tc(const void* q, const void* k, const void* v, cons
                                                                        NC, d_k, d_v, scale, wait_ns);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     grad_tc_kernel<<<dim3(NC, B * Hv), gs::kThreads, kSmem, s>>>(
-        gm, static_cast<__nv_bfloat16*>(dv), static_cast<__nv_bfloat16*>(dw), T, Hk, Hv, d_k, d_v, scale, wait_ns);
+        gm, T, Hk, Hv, d_k, d_v, scale, wait_ns);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     const long long rows = static_cast<long long>(B) * T, n4 = rows * Hk * (d_k / 4);
     const int gsz = static_cast<int>(n4 / 256 + 1 < 4096 ? n4 / 256 + 1 : 4096);
