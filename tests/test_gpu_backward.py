@@ -267,3 +267,43 @@ def test_backward_in_a_cuda_graph(g):
     assert g.gdn2_last_device_status() == g.GDN2_OK
     for name, x, y in zip(("dq", "dk", "dv", "dg", "db", "dw", "ds0"), (*outs, ds0), eager):
         assert torch.equal(x, y), name
+
+
+_CANARY = 4096  # elements of sentinel after each gradient output
+
+
+@pytest.mark.parametrize("T,dk,dv", [(77, 128, 128), (130, 64, 128), (64, 128, 64)])
+def test_backward_writes_stay_in_bounds(g, T, dk, dv):
+    """The tensor-core backward writes dq, dk, db, dg, dv and dw through tensor maps clipped at T and at
+    d_k / d_v: canary elements after every gradient and after dS0 stay untouched (ragged last chunk,
+    64-wide channels or columns), and the gradients match the oracle."""
+    import torch
+
+    wl = synth.Workload("bwd", B=2, T=T, Hk=1, Hv=2, dk=dk, dv=dv, dtype="bf16", seed=90 + T, s0_std=0.02)
+    inp = synth.make_inputs(wl)
+    rng = np.random.default_rng(T)
+    d_o = synth.round_to(rng.standard_normal((2, T, 2, dv)), "bf16").astype(np.float64)
+    dev = lambda a: synth.to_torch(np.ascontiguousarray(a), "bf16", "cuda")
+    ts = [dev(getattr(inp, n)) for n in ("q", "k", "v", "g", "b", "w")]
+
+    def canary(shape, dtype):
+        n = int(np.prod(shape))
+        buf = torch.full((n + _CANARY,), -7.0, dtype=dtype, device="cuda")
+        return buf, buf[:n].view(shape)
+
+    bf = torch.bfloat16
+    shapes = {"dq": (2, T, 1, dk), "dk": (2, T, 1, dk), "dv": (2, T, 2, dv), "dg": (2, T, 2, dk),
+              "db": (2, T, 2, dk), "dw": (2, T, 2, dv)}
+    bufs = {name: canary(shp, bf) for name, shp in shapes.items()}
+    ds0_buf, ds0 = canary((2, 2, dk, dv), torch.float32)
+    g.gdn2_backward(*ts, dev(d_o), *(bufs[n][1] for n in ("dq", "dk", "dv", "dg", "db", "dw")),
+                    H.state_to_device(inp.s0), None, ds0)
+    torch.cuda.synchronize()
+    assert g.gdn2_last_device_status() == g.GDN2_OK
+    for name, (buf, t) in list(bufs.items()) + [("ds0", (ds0_buf, ds0))]:
+        assert bool((buf[t.numel():] == -7.0).all()), f"{name} canary overwritten"
+    ref = oback.gradients(inp.q, inp.k, inp.v, inp.g, inp.b, inp.w, inp.s0, d_o, None)
+    for name in ("dq", "dk", "dv", "dg", "db", "dw"):
+        e = max_rel_err(H.to_np(bufs[name][1]), ref[name])
+        assert e < TOL["bf16"], (name, e)
+    assert max_rel_err(ds0.cpu().numpy(), ref["ds0"]) < TOL["bf16"]
