@@ -22,8 +22,11 @@
 //   two CTAs per SM with 3 bf16 slots each: a bf16 slab is half the bytes). Several tokens: two CTAs
 //   per SM, the state carried through the tokens in registers, the slot refilled as soon as the
 //   state and the tokens' table are in registers, and the updated state stored from registers.
+#include <cuda.h>
+
 #include "common.cuh"
 #include "ptx.cuh"
+#include "tma_map.cuh"
 
 namespace gdn2 {
 
@@ -47,6 +50,17 @@ __device__ __forceinline__ void store4(__nv_bfloat16* p, float4 x) {
     u.x = *reinterpret_cast<const uint32_t*>(&a);
     u.y = *reinterpret_cast<const uint32_t*>(&c);
     *reinterpret_cast<uint2*>(p) = u;
+}
+
+// Columns c .. c + 3 of row r of a 128 x 128 slab stored as 128-byte-wide column boxes of 128 rows
+// (16 KB each) with the 128-byte swizzle: within each 1024-byte group of 8 rows, the 16-byte chunk
+// index of row r is XORed with r mod 8. c is a multiple of 4, so the 4 elements stay in one chunk.
+template <typename TS>
+__device__ __forceinline__ float4 load4_swizzled(const uint8_t* slab, int r, int c) {
+    const int byte = c * static_cast<int>(sizeof(TS));
+    const int bo = byte & 127;
+    return load4(reinterpret_cast<const TS*>(slab + (byte >> 7) * 16384 + r * 128 +
+                                             ((((bo >> 4) ^ (r & 7)) << 4) | (bo & 15))));
 }
 
 // state row of batch element bi: the slot map (when given) or bi itself; -1 = inactive
@@ -187,7 +201,10 @@ struct StreamRing {
     // two partial sums of k.q, then w.v of the 128 columns (float4 units)
     static constexpr uint32_t tab_f4 = 2 * 64 + 1 + 32;
     static constexpr uint32_t rows_bytes = NT > 1 ? NT * tab_f4 * 16 : 0;
-    static constexpr uint32_t avail = smem - red_bytes - rows_bytes - 256;
+    // several tokens: the slab comes by tensor copies with the 128-byte swizzle, whose shared-memory
+    // tiles start on 1024-byte boundaries: the ring is placed on one (at most 1008 bytes of padding)
+    static constexpr uint32_t align_pad = NT > 1 ? 1024 : 0;
+    static constexpr uint32_t avail = smem - red_bytes - rows_bytes - 256 - align_pad;
     static constexpr int depth = avail / slot > 8 ? 8 : (int)(avail / slot);
     static constexpr uint32_t red_off = depth * slot;
     static constexpr uint32_t rows_off = red_off + red_bytes;
@@ -196,11 +213,15 @@ struct StreamRing {
 
 
 // Queue the loads of head h into ring slot `slot`: its state slab and the N tokens' six vectors. An
-// inactive head (slot map gives no row) completes the slot's barrier phase without loading.
+// inactive head (slot map gives no row) completes the slot's barrier phase without loading. One token:
+// the slab by one bulk copy (row-major). Several tokens: by tensor copies of 128-byte-wide column
+// boxes over all 128 rows with the 128-byte swizzle (smap: [rows x H_v][128][128] of the state), so
+// that the warps, each reading 16 columns over 8 rows at a time, read it without bank conflicts.
 template <typename Tin, typename TS, int NT, int CPS>
 __device__ __forceinline__ void stream_issue(uint8_t* smem_s, uint64_t* bar, int slot, int h, int N, const TS* state,
                                              const int* slots, int n_slots, const Tin* q, const Tin* k,
-                                             const Tin* v, const Tin* g, const Tin* b, const Tin* w, int Hk, int Hv) {
+                                             const Tin* v, const Tin* g, const Tin* b, const Tin* w, int Hk, int Hv,
+                                             const CUtensorMap* smap) {
     using R = StreamRing<Tin, TS, NT, CPS>;
     const int bi = h / Hv, hv = h - bi * Hv, hk = hv / (Hv / Hk);
     const int row = state_row(slots, n_slots, bi);
@@ -211,7 +232,13 @@ __device__ __forceinline__ void stream_issue(uint8_t* smem_s, uint64_t* bar, int
     constexpr uint32_t vb = 128 * sizeof(Tin);
     mbar_arrive_expect_tx(bar, R::slab + 6 * vb * N);
     uint8_t* sl = smem_s + slot * R::slot;
-    bulk_load(sl, state + (static_cast<size_t>(row) * Hv + hv) * 16384, R::slab, bar);
+    if (NT > 1) {
+        constexpr int bc = 128 / sizeof(TS);  // columns per 128-byte box row
+#pragma unroll
+        for (int x = 0; x < 128 / bc; ++x) tma_load_3d(sl + x * 16384, smap, x * bc, 0, row * Hv + hv, bar);
+    } else {
+        bulk_load(sl, state + (static_cast<size_t>(row) * Hv + hv) * 16384, R::slab, bar);
+    }
     for (int t = 0; t < N; ++t) {
         uint8_t* tk = sl + R::slab + t * 6 * vb;
         const size_t tt = static_cast<size_t>(bi) * N + t;
@@ -237,17 +264,20 @@ __global__ void __launch_bounds__(256, CPS)
     recurrent_stream_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* __restrict__ v,
                             const Tin* __restrict__ g, const Tin* __restrict__ b, const Tin* __restrict__ w,
                             TS* __restrict__ state, const int* __restrict__ slots, int n_slots,
-                            Tin* __restrict__ o, int nheads, int N, int Hk, int Hv, float scale, long long wait_ns) {
+                            Tin* __restrict__ o, int nheads, int N, int Hk, int Hv, float scale, long long wait_ns,
+                            const __grid_constant__ CUtensorMap smap) {
     using R = StreamRing<Tin, TS, NT, CPS>;
     static_assert(R::depth >= 1, "stream ring needs a slot");
-    static_assert(R::bar_off + 8 * 8 + 16 <= R::smem, "stream kernel shared memory");
+    static_assert(R::align_pad + R::bar_off + 8 * 8 + 16 <= R::smem, "stream kernel shared memory");
+    static_assert(NT == 1 || R::slot % 1024 == 0, "swizzled slabs start on 1024-byte boundaries");
     // ring slots; heads loading ahead. One token: the updated state goes back through its slot, so a
     // slot is refilled once the store of its head has read it (with a single slot the other CTA of the
     // SM covers that gap). Several tokens: a slot is refilled as soon as its head's state and tokens
     // are in registers and the table (the updated state goes from registers to global memory), so
     // every slot loads ahead.
     constexpr int D = R::depth, P = NT > 1 ? D : (D > 1 ? D - 1 : 1);
-    extern __shared__ __align__(128) uint8_t smem_s[];
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    uint8_t* smem_s = smem_raw + (R::align_pad ? (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u : 0u);
     float* red = reinterpret_cast<float*>(smem_s + R::red_off);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem_s + R::bar_off);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -259,7 +289,7 @@ __global__ void __launch_bounds__(256, CPS)
         fence_mbar_init();
         for (int kk = 0; kk < P && kk < count; ++kk)
             stream_issue<Tin, TS, NT, CPS>(smem_s, full + kk, kk, first + kk * G, N, state, slots, n_slots, q, k,
-                                           v, g, b, w, Hk, Hv);
+                                           v, g, b, w, Hk, Hv, &smap);
     }
     __syncthreads();
 
@@ -357,12 +387,12 @@ __global__ void __launch_bounds__(256, CPS)
             const uint8_t* tkb = smem_s + bsel * R::slot + R::slab;
             float4* tab = reinterpret_cast<float4*>(smem_s + R::rows_off);
             const int rg = lane >> 2, cq = lane & 3, col = 16 * warp + 4 * cq;
-            const TS* S = reinterpret_cast<const TS*>(smem_s + bsel * R::slot);
+            const uint8_t* S = smem_s + bsel * R::slot;
             uint64_t s[8][4];  // s[j][c]: column col + c, rows (2p, 2p + 1), p = 8 j + rg
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 const int r0 = 2 * (8 * j + rg);
-                const float4 x = load4(S + r0 * 128 + col), y = load4(S + (r0 + 1) * 128 + col);
+                const float4 x = load4_swizzled<TS>(S, r0, col), y = load4_swizzled<TS>(S, r0 + 1, col);
                 s[j][0] = f32x2(x.x, y.x);
                 s[j][1] = f32x2(x.y, y.y);
                 s[j][2] = f32x2(x.z, y.z);
@@ -393,7 +423,7 @@ __global__ void __launch_bounds__(256, CPS)
             __syncthreads();
             if (tid == 0 && kk + D < count)
                 stream_issue<Tin, TS, NT, CPS>(smem_s, full + bsel, bsel, first + (kk + D) * G, N, state, slots,
-                                               n_slots, q, k, v, g, b, w, Hk, Hv);
+                                               n_slots, q, k, v, g, b, w, Hk, Hv, &smap);
             for (int t = 0; t < N; ++t) {
                 const float4* tt = tab + t * R::tab_f4;
                 uint64_t rb[4] = {0, 0, 0, 0}, rq[4] = {0, 0, 0, 0};  // +0.0f pairs (even-row, odd-row parts)
@@ -476,7 +506,7 @@ __global__ void __launch_bounds__(256, CPS)
                 __syncthreads();  // every thread has passed its wait on the slot's barrier
                 if (tid == 0 && kk + D < count)
                     stream_issue<Tin, TS, NT, CPS>(smem_s, full + bsel, bsel, first + (kk + D) * G, N, state,
-                                                   slots, n_slots, q, k, v, g, b, w, Hk, Hv);
+                                                   slots, n_slots, q, k, v, g, b, w, Hk, Hv, &smap);
             }
             __syncthreads();  // the table is rewritten by the next head
             continue;
@@ -491,7 +521,7 @@ __global__ void __launch_bounds__(256, CPS)
                 else bulk_wait_read<0>();        // single slot: the store of head kk has read it
                 const int nb = (kk + P) % D;
                 stream_issue<Tin, TS, NT, CPS>(smem_s, full + nb, nb, first + (kk + P) * G, N, state, slots, n_slots,
-                                               q, k, v, g, b, w, Hk, Hv);
+                                               q, k, v, g, b, w, Hk, Hv, &smap);
             }
         }
     }
@@ -515,10 +545,22 @@ cudaError_t launch_stream(const void* q, const void* k, const void* v, const voi
     cudaError_t e = cudaFuncSetAttribute(recurrent_stream_kernel<Tin, TS, NT, CPS>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)R::smem);
     if (e != cudaSuccess) return e;
+    // several tokens: the state pool as [rows x H_v][128 rows][128 columns], 128-byte-wide boxes of 128
+    // rows, 128-byte swizzle (unused with one token)
+    CUtensorMap smap = {};
+    if (NT > 1) {
+        const long long rows = slots ? n_slots : heads / Hv;
+        const uint64_t dims[3] = {128, 128, static_cast<uint64_t>(rows) * Hv};
+        const uint64_t strides[2] = {128 * sizeof(TS), 128 * 128 * sizeof(TS)};
+        const uint32_t box[3] = {static_cast<uint32_t>(128 / sizeof(TS)), 128, 1};
+        if (!make_map(&smap, sizeof(TS) == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                      st, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+            return cudaErrorInvalidValue;
+    }
     recurrent_stream_kernel<Tin, TS, NT, CPS><<<CPS * nsm, 256, R::smem, s>>>(
         static_cast<const Tin*>(q), static_cast<const Tin*>(k), static_cast<const Tin*>(v),
         static_cast<const Tin*>(g), static_cast<const Tin*>(b), static_cast<const Tin*>(w), st, slots, n_slots,
-        static_cast<Tin*>(o), static_cast<int>(heads), N, Hk, Hv, scale, wait_limit_ns());
+        static_cast<Tin*>(o), static_cast<int>(heads), N, Hk, Hv, scale, wait_limit_ns(), smap);
     return cudaGetLastError();
 }
 
