@@ -20,8 +20,10 @@
 //   vectors, so that the loads of the next heads are in flight while a head is computed. One token:
 //   the updated slab goes back through its slot by bulk copy (one CTA per SM with 3 fp32 slots, or
 //   two CTAs per SM with 3 bf16 slots each: a bf16 slab is half the bytes). Several tokens: two CTAs
-//   per SM, the state carried through the tokens in registers, the slot refilled as soon as the
-//   state and the tokens' table are in registers, and the updated state stored from registers.
+//   per SM, the slab brought by tensor copies with the 128-byte swizzle (a warp then reads its 16
+//   columns over 8 rows without bank conflicts), the state carried through the tokens in registers,
+//   the slot refilled as soon as the state and the tokens' table are in registers, and the updated
+//   state stored from registers.
 #include <cuda.h>
 
 #include "common.cuh"
