@@ -551,8 +551,8 @@ cudaError_t launch_stream(const void* q, const void* k, const void* v, const voi
     // rows, 128-byte swizzle (unused with one token)
     CUtensorMap smap = {};
     if (NT > 1) {
-        const long long rows = slots ? n_slots : heads / Hv;
-        const uint64_t dims[3] = {128, 128, static_cast<uint64_t>(rows) * Hv};
+        const long long rows = slots ? n_slots : heads / Hv;  // an empty pool: no active head, map unused
+        const uint64_t dims[3] = {128, 128, static_cast<uint64_t>(rows > 0 ? rows : 1) * Hv};
         const uint64_t strides[2] = {128 * sizeof(TS), 128 * 128 * sizeof(TS)};
         const uint32_t box[3] = {static_cast<uint32_t>(128 / sizeof(TS)), 128, 1};
         if (!make_map(&smap, sizeof(TS) == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
